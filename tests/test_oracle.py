@@ -1,0 +1,388 @@
+"""Pins for the CPU oracle: closed forms, invariants, hand-worked fixtures, brute force.
+
+Nothing here touches the CUDA library. Each test fixes a property that the pages or plain
+mathematics determine, so that a plausible slip in the oracle (a dropped term, a reversed
+order, a transposed block, a wrong rounding) fails at least one of them.
+"""
+
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import arith, brute, collectives, naming
+import synth
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+GOLDEN = os.path.join(HERE, "golden")
+
+
+# ---------------------------------------------------------------- element arithmetic
+
+def test_bf16_widening_is_exact_for_every_pattern():
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    f = arith.bf16_to_f32(bits)
+    for b in range(0, 1 << 16, 97):
+        e = (b >> 7) & 0xFF
+        if e == 0xFF:
+            continue
+        v = brute.decode_bf16(b)
+        got = Fraction(float(f[b]))
+        assert got == v.q, hex(b)
+        if v.q == 0:
+            assert (struct.pack("<f", float(f[b]))[3] >> 7) == v.neg
+
+
+def test_bf16_rounding_matches_exact_rule_including_ties():
+    rng = synth.seeded_rng(11)
+    hi = rng.integers(0, 0x7F7F, size=4000, dtype=np.uint32)
+    lo = rng.integers(0, 1 << 16, size=4000, dtype=np.uint32)
+    lo[:1000] = 0x8000  # exact ties
+    lo[1000:1500] = 0x7FFF
+    lo[1500:2000] = 0x8001
+    sign = rng.integers(0, 2, size=4000, dtype=np.uint32) << np.uint32(31)
+    u = sign | (hi << np.uint32(16)) | lo
+    x = u.view(np.float32)
+    got = arith.f32_to_bf16_rne(x)
+    for i in range(0, 4000, 3):
+        want = brute.round_bf16(brute.decode_f32(int(u[i])))
+        gotv = brute.decode_bf16(int(got[i]))
+        assert gotv.key() == want.key(), (hex(int(u[i])), hex(int(got[i])))
+
+
+def test_bf16_rounding_nan_stays_nan():
+    x = np.array([np.nan, -np.nan], dtype=np.float32)
+    r = arith.f32_to_bf16_rne(x)
+    assert np.all(np.isnan(arith.bf16_to_f32(r)))
+
+
+def test_two_term_f32_sum_equals_host_fpu():
+    # fl32(a+b) through binary64 is exact (53 >= 2*24+2: double rounding is innocuous)
+    rng = synth.seeded_rng(12)
+    a = synth.uniform_f32(rng, 3000)
+    b = synth.uniform_f32(rng, 3000) * np.float32(1e-3)
+    got = arith.ordered_sum([a, b], "f32")
+    for i in range(3000):
+        want = struct.unpack("<f", struct.pack("<f", float(a[i]) + float(b[i])))[0]
+        assert struct.pack("<f", want) == struct.pack("<f", float(got[i]))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("R", [2, 3, 5, 8])
+def test_ordered_sum_matches_exact_sequential_rounding(dtype, R):
+    rng = synth.seeded_rng(100 + R)
+    n = 300
+    if dtype == "bf16":
+        xs = [synth.normal_bf16(rng, n) for _ in range(R)]
+        dec = brute.decode_bf16
+        raw = lambda x, i: int(x[i])
+    else:
+        # magnitudes spread over many binades so that the order of additions matters
+        xs = [synth.uniform_f32(rng, n) * np.float32(2.0) ** rng.integers(-12, 12, n).astype(np.float32)
+              for _ in range(R)]
+        dec = brute.decode_f32
+        raw = lambda x, i: int(x.view(np.uint32)[i])
+    got = arith.ordered_sum(xs, dtype)
+    gdec = (lambda i: brute.decode_bf16(int(got[i]))) if dtype == "bf16" else \
+        (lambda i: brute.decode_f32(int(got.view(np.uint32)[i])))
+    for i in range(n):
+        want = brute.element_sum([dec(raw(x, i)) for x in xs], dtype)
+        assert gdec(i).key() == want.key(), i
+
+
+def test_fixed_order_is_observable():
+    # a reversed chain must give a different answer on this data (pins the order)
+    rng = synth.seeded_rng(7)
+    xs = [synth.uniform_f32(rng, 2000) * np.float32(2.0) ** np.float32(k * 6) for k in range(4)]
+    fwd = arith.ordered_sum(xs, "f32")
+    rev = arith.ordered_sum(xs[::-1], "f32")
+    assert not np.array_equal(fwd.view(np.uint32), rev.view(np.uint32))
+
+
+def _read_sum_fixtures():
+    rows = []
+    with open(os.path.join(GOLDEN, "sum_rounding.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            dtype, ins, out, why = [p.strip() for p in line.split(";", 3)]
+            rows.append((dtype, [int(h, 16) for h in ins.split()], int(out, 16), why))
+    return rows
+
+
+@pytest.mark.parametrize("row", _read_sum_fixtures(), ids=lambda r: r[3][:40])
+def test_golden_sum_rounding(row):
+    dtype, ins, out, why = row
+    R = len(ins)
+    npt = np.uint16 if dtype == "bf16" else np.uint32
+    xs = [np.array([v], dtype=npt) for v in ins]
+    if dtype == "f32":
+        xs = [x.view(np.float32) for x in xs]
+    outs = [np.zeros(1, dtype=xs[0].dtype) for _ in range(R)]
+    code = naming.run_naming(R, "sum", dtype, [1] * R, [(r, 0, 1, 0) for r in range(R)],
+                             [1] * R, [(r, 0, 1, 0) for r in range(R)], xs, outs)
+    assert code == 0
+    for r in range(R):
+        got = int(outs[r].view(npt)[0])
+        assert got == out, (why, hex(got))
+    dec = brute.decode_bf16 if dtype == "bf16" else brute.decode_f32
+    want = brute.element_sum([dec(v) for v in ins], dtype)
+    assert dec(out).key() == want.key(), why
+
+
+# ---------------------------------------------------------------- naming semantics
+
+def _naming_case(seed, op, dtype, R):
+    rng = synth.seeded_rng(seed)
+    in_len, in_segs, out_len, out_segs = synth.random_naming(rng, R, 12, 4, 3, op)
+    if dtype == "bf16":
+        ins = [synth.normal_bf16(rng, n) for n in in_len]
+        outs = [synth.normal_bf16(rng, n) for n in out_len]
+    elif dtype == "f32":
+        ins = [synth.uniform_f32(rng, n) * np.float32(2.0) ** rng.integers(-8, 8, n).astype(np.float32)
+               for n in in_len]
+        outs = [synth.uniform_f32(rng, n) for n in out_len]
+    else:
+        ins = [synth.random_bytes(rng, n) for n in in_len]
+        outs = [synth.random_bytes(rng, n) for n in out_len]
+    return in_len, in_segs, out_len, out_segs, ins, outs
+
+
+def _raw(a, i):
+    if a.dtype == np.float32:
+        return int(a.view(np.uint32)[i])
+    return int(a[i])
+
+
+@pytest.mark.parametrize("seed", range(40))
+@pytest.mark.parametrize("op,dtype", [("copy", "bf16"), ("copy", "bytes"), ("copy", "f32"),
+                                      ("sum", "bf16"), ("sum", "f32")])
+def test_naming_matches_brute_force(seed, op, dtype):
+    R = 1 + seed % 3
+    in_len, in_segs, out_len, out_segs, ins, outs = _naming_case(1000 + seed, op, dtype, R)
+    before = [o.copy() for o in outs]
+    code = naming.run_naming(R, op, dtype, in_len, in_segs, out_len, out_segs, ins, outs)
+    assert code == 0
+    raw_in = [[_raw(x, i) for i in range(len(x))] for x in ins]
+    want = brute.evaluate(op, dtype, in_segs, out_segs, raw_in, out_len)
+    dec = brute.decode_bf16 if dtype == "bf16" else brute.decode_f32
+    for d in range(R):
+        for i in range(out_len[d]):
+            if i in want[d]:
+                w = want[d][i]
+                if op == "copy":
+                    assert _raw(outs[d], i) == w
+                else:
+                    assert dec(_raw(outs[d], i)).key() == w.key()
+            else:
+                assert _raw(outs[d], i) == _raw(before[d], i), "unnamed element touched"
+
+
+def test_validation_codes():
+    E = naming.ERR
+    ok_in = [(0, 0, 4, 7), (1, 0, 4, 7)]
+    ok_out = [(0, 0, 4, 7), (1, 0, 4, 7)]
+    v = lambda R=2, op="sum", dt="bf16", il=(4, 4), i=ok_in, ol=(4, 4), o=ok_out: \
+        naming.validate(R, op, dt, list(il), i, list(ol), o)
+    assert v() == E["OK"]
+    assert v(R=0, il=(), ol=(), i=[], o=[]) == E["EINVAL"]
+    assert v(R=65, il=[4] * 65, ol=[4] * 65) == E["EINVAL"]
+    assert v(op="max") == E["EINVAL"]
+    assert v(dt="bytes") == E["EINVAL"]
+    assert v(i=[(2, 0, 4, 7)]) == E["EINVAL"]
+    assert v(i=[(0, 0, 0, 7)], o=[]) == E["EINVAL"]
+    assert v(i=[(0, 1, 4, 7), (1, 0, 4, 7)]) == E["EBOUNDS"]
+    assert v(o=[(1, 2, 4, 7)]) == E["EBOUNDS"]
+    assert v(i=[(0, 0, 4, 7), (1, 0, 3, 7)]) == E["ELEN"]
+    assert v(o=[(0, 0, 4, 8)]) == E["ENAME"]
+    assert v(op="copy") == E["ENAME"]
+    assert v(op="copy", i=[(0, 0, 4, 7)]) == E["OK"]
+    assert v(ol=(8, 4), o=[(0, 0, 4, 7), (0, 3, 4, 7)]) == E["EOVERLAP"]
+    assert v(ol=(8, 4), o=[(0, 0, 4, 7), (0, 4, 4, 7)]) == E["OK"]
+    # an input name nobody consumes is allowed
+    assert v(i=ok_in + [(0, 0, 2, 9)]) == E["OK"]
+    # empty naming is valid and writes nothing
+    assert v(i=[], o=[]) == E["OK"]
+
+
+# ---------------------------------------------------------------- collectives
+
+def _ar_naming(R, n):
+    return [(r, 0, n, 0) for r in range(R)], [(r, 0, n, 0) for r in range(R)]
+
+
+def _run(R, op, dtype, in_len, in_segs, out_len, out_segs, ins):
+    npt = arith.NPTYPE[dtype]
+    outs = [np.zeros(n, dtype=npt) for n in out_len]
+    assert naming.run_naming(R, op, dtype, in_len, in_segs, out_len, out_segs, ins, outs) == 0
+    return outs
+
+
+def _eq(a, b):
+    return np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_allreduce_direct_equals_naming_and_rs_then_ag(dtype):
+    R, n = 8, 64
+    rng = synth.seeded_rng(21)
+    xs = [synth.normal_bf16(rng, n) if dtype == "bf16" else synth.normal_f32(rng, n) for _ in range(R)]
+    direct = collectives.allreduce(xs, dtype)
+    i, o = _ar_naming(R, n)
+    named = _run(R, "sum", dtype, [n] * R, i, [n] * R, o, xs)
+    rs = collectives.reduce_scatter(xs, dtype)
+    ag = collectives.allgather(rs)
+    for r in range(R):
+        assert _eq(direct[r], named[r])
+        assert _eq(direct[r], ag[r])
+
+
+def test_reduce_scatter_alltoall_allgather_broadcast_by_naming():
+    R, n = 4, 16
+    b = n // R
+    rng = synth.seeded_rng(22)
+    xs = [synth.normal_bf16(rng, n) for _ in range(R)]
+    # reduce-scatter: input block j on every rank is name j; rank r's output is name r
+    rs = _run(R, "sum", "bf16", [n] * R, [(r, j * b, b, j) for r in range(R) for j in range(R)],
+              [b] * R, [(r, 0, b, r) for r in range(R)], xs)
+    for r, (x, y) in enumerate(zip(rs, collectives.reduce_scatter(xs, "bf16"))):
+        assert _eq(x, y)
+    # all-gather: input r is name r; output block j is name j
+    ag = _run(R, "copy", "bf16", [n] * R, [(r, 0, n, r) for r in range(R)],
+              [R * n] * R, [(d, j * n, n, j) for d in range(R) for j in range(R)], xs)
+    for x, y in zip(ag, collectives.allgather(xs)):
+        assert _eq(x, y)
+    # broadcast from root 2
+    bc = _run(R, "copy", "bf16", [n] * R, [(2, 0, n, 0)], [n] * R, [(d, 0, n, 0) for d in range(R)], xs)
+    for x, y in zip(bc, collectives.broadcast(xs, 2)):
+        assert _eq(x, y)
+    # all-to-all: (source s, block d) is name s*R+d; it lands at (rank d, block s)
+    a2a = _run(R, "copy", "bf16", [n] * R, [(s, d * b, b, s * R + d) for s in range(R) for d in range(R)],
+               [n] * R, [(d, s * b, b, s * R + d) for s in range(R) for d in range(R)], xs)
+    for x, y in zip(a2a, collectives.alltoall(xs)):
+        assert _eq(x, y)
+
+
+def test_alltoall_twice_is_identity_and_conserves_bytes():
+    R, n = 8, 64
+    rng = synth.seeded_rng(23)
+    xs = [synth.random_bytes(rng, n) for _ in range(R)]
+    once = collectives.alltoall(xs)
+    twice = collectives.alltoall(once)
+    for x, y in zip(xs, twice):
+        assert _eq(x, y)
+    assert sorted(np.concatenate(xs).tolist()) == sorted(np.concatenate(once).tolist())
+    # a2a is a transpose of the (source, block) grid: the block grid must move
+    assert not all(_eq(x, y) for x, y in zip(xs, once))
+
+
+def test_broadcast_single_rank_is_memcpy_and_allgather_conserves():
+    rng = synth.seeded_rng(24)
+    x = synth.random_bytes(rng, 33)
+    assert _eq(collectives.broadcast([x])[0], x)
+    xs = [synth.random_bytes(rng, 5) for _ in range(3)]
+    ag = collectives.allgather(xs)
+    for out in ag:
+        for r in range(3):
+            assert _eq(out[r * 5:(r + 1) * 5], xs[r])
+
+
+def test_single_producer_sum_is_copy():
+    rng = synth.seeded_rng(25)
+    x = synth.normal_bf16(rng, 50)
+    assert _eq(collectives.allreduce([x], "bf16")[0], x)
+    y = synth.normal_f32(rng, 50)
+    assert _eq(collectives.allreduce([y], "f32")[0], y)
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 5, 8])
+def test_identical_inputs_closed_form(k):
+    # k copies of a bf16 value x: the binary32 chain is exact (8+3 significand bits), so the
+    # result is k*x rounded once to bf16 -- computed here with exact rationals
+    rng = synth.seeded_rng(26)
+    x = synth.normal_bf16(rng, 200)
+    out = collectives.allreduce([x] * k, "bf16")[0]
+    for i in range(200):
+        v = brute.decode_bf16(int(x[i]))
+        want = brute.round_bf16(brute.Val(v.q * k, neg=v.neg))
+        assert brute.decode_bf16(int(out[i])).key() == want.key()
+
+
+def test_small_integer_sums_are_exact():
+    R, n = 8, 500
+    rng = synth.seeded_rng(27)
+    xs = [synth.small_int_bf16(rng, n) for _ in range(R)]
+    out = collectives.allreduce(xs, "bf16")[0]
+    ints = sum(arith.bf16_to_f32(x).astype(np.int64) for x in xs)
+    assert np.array_equal(arith.bf16_to_f32(out).astype(np.int64), ints)
+    # sums within +-128 are exact in bf16 too, and independent of order
+    rev = collectives.allreduce(xs[::-1], "bf16")[0]
+    assert _eq(out, rev)
+
+
+def test_moe_dispatch_golden_fixture():
+    routing = np.zeros((2, 2, 2), dtype=np.int32)
+    expect = {}
+    with open(os.path.join(GOLDEN, "moe_dispatch_tiny.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line.startswith("routing"):
+                lhs, rhs = line.split(":")
+                s = int(lhs.split("s=")[1].split()[0])
+                t = int(lhs.split("t=")[1].split()[0])
+                routing[s, t] = [int(v) for v in rhs.split()]
+            elif line.startswith("expect"):
+                lhs, rhs = line.split(":")
+                expect[int(lhs.split("d=")[1])] = [int(v) for v in rhs.split()]
+    xs = [np.array([[100 * s + t] for t in range(2)], dtype=np.int64) for s in range(2)]
+    outs, counts = collectives.moe_dispatch(xs, routing, 2)
+    for d in range(2):
+        assert outs[d][:, 0].tolist() == expect[d]
+        assert counts[d] == len(expect[d])
+
+
+def test_moe_dispatch_counts_and_rows():
+    R, T, H, E, k = 4, 64, 8, 32, 4
+    routing = synth.zipf_topk_routing(5, R, T, E, k, 1.1)
+    assert routing.shape == (R, T, k)
+    for s in range(R):
+        for t in range(T):
+            assert len(set(routing[s, t].tolist())) == k
+    rng = synth.seeded_rng(5)
+    xs = [synth.random_bytes(rng, (T, H)) for _ in range(R)]
+    outs, counts = collectives.moe_dispatch(xs, routing, E // R)
+    dests = collectives.moe_dest_ranks(routing, E // R)
+    assert sum(counts) == int(dests.sum())
+    for d in range(R):
+        want = [xs[s][t] for s in range(R) for t in range(T) if set(routing[s, t] // (E // R)) & {d}]
+        assert len(want) == counts[d]
+        for a, b in zip(outs[d], want):
+            assert _eq(a, b)
+
+
+def test_moe_combine_inverts_dispatch_for_single_destination_tokens():
+    R, T, H, E, k = 2, 8, 4, 4, 1
+    routing = synth.zipf_topk_routing(9, R, T, E, k, 1.1)
+    rng = synth.seeded_rng(9)
+    xs = [synth.normal_bf16(rng, (T, H)) for _ in range(R)]
+    ys, _ = collectives.moe_dispatch(xs, routing, E // R)
+    back = collectives.moe_combine_sum(ys, routing, E // R, "bf16")
+    for s in range(R):
+        assert _eq(back[s], xs[s])
+
+
+def test_epoch_semantics_cycle_through_pool():
+    R, n = 2, 8
+    rng = synth.seeded_rng(31)
+    pool = [[synth.normal_bf16(rng, n) for _ in range(R)] for _ in range(3)]
+    i, o = _ar_naming(R, n)
+    res = naming.run_epochs(R, "sum", "bf16", [n] * R, i, [n] * R, o, pool, 7,
+                            [np.zeros(n, np.uint16)] * R)
+    for e in range(7):
+        want = collectives.allreduce(pool[e % 3], "bf16")
+        for r in range(R):
+            assert _eq(res[e][r], want[r])
