@@ -1,0 +1,387 @@
+"""Benchmark of the collective datapath on one GB300 (emulated ranks).
+
+Default workload (one "step"): the tensor-parallel decode all-reduce — R=8 emulated ranks,
+4096 bf16 (8 KiB) per rank, N(0,1) values from seed 2, a pool of 7 input sets, 10,000
+back-to-back epochs in one persistent launch with the speculative protocol (dual
+buffers, content-tagged reduced-flag validation). Metric: microseconds per epoch.
+
+Also measured in the same run and reported as extra keys: the barrier and dual-buffer
+protocols, a staggered-start stress run of the speculative protocol, and the
+prefill-sized all-reduce (8 x 64 MiB, one-shot vs two-shot) as achieved HBM GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|prefill|sweep|moe]
+
+Under torchrun each rank runs an independent replica on its own GPU (the emulated
+collective needs no inter-GPU exchange); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+R_DECODE, N_DECODE, POOL, EPOCHS = 8, 4096, 7, 10000
+FLUSH_BYTES = 256 << 20  # > 129 MB L2
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid):
+        self.rows = []
+        self.proc = None
+        self.uuid = device_uuid
+
+    def __enter__(self):
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.25)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            for nm, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def _decode_inputs(torch, dev):
+    rng = synth.seeded_rng(2)
+    pool_np = [[synth.normal_bf16(rng, N_DECODE) for _ in range(R_DECODE)] for _ in range(POOL)]
+    host = [np.ascontiguousarray(np.stack([pool_np[p][r] for p in range(POOL)])).view(np.int16)
+            for r in range(R_DECODE)]
+    ins = [torch.from_numpy(h).to(dev) for h in host]
+    return pool_np, host, ins
+
+
+def _time_steps(torch, fn, steps, warmup, flush, stream):
+    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before every step."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    return times
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+    import collective_datapath_copy_gb300 as cdc
+    from collective_datapath_copy_gb300.build import build
+
+    build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.fill_(1)
+    peak, peak_kind = peaks()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+
+    nm = cdc.allreduce(R_DECODE, N_DECODE, "bf16")
+    pool_np, host_in, ins = _decode_inputs(torch, dev)
+    outs = [torch.empty(EPOCHS, N_DECODE, dtype=torch.int16, device=dev) for _ in range(R_DECODE)]
+    kw = dict(n_epochs=EPOCHS, in_epoch_stride=2 * N_DECODE, in_pool=POOL,
+              out_epoch_stride=2 * N_DECODE)
+    plans = {name: cdc.Plan(nm, **cfg) for name, cfg in [
+        ("spec", dict(protocol="spec")),
+        ("dual", dict(protocol="dual")),
+        ("barrier", dict(protocol="barrier")),
+        ("spec_stagger", dict(protocol="spec", inject="stagger", inject_seed=2,
+                              inject_prob_ppm=100000, inject_max_ns=20000, inject_start_ns=5000)),
+    ]}
+
+    def step(name):
+        return lambda: plans[name].run(ins, outs, **kw)
+
+    # headline: speculative protocol, timed K steps, clocks sampled during the region
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(uuid) as clk:
+        t_wall0 = time.perf_counter()
+        times = _time_steps(torch, step("spec"), args.steps, args.warmup, flush, stream)
+        t_wall = time.perf_counter() - t_wall0
+    torch.cuda.synchronize()
+    st = plans["spec"].status()
+    if st["code"] != 0:
+        raise RuntimeError(f"spec run failed: {st}")
+    ms = sum(times) / len(times)
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    us_epoch = ms * 1000.0 / EPOCHS
+
+    # other protocols (same K/W)
+    proto = {}
+    for name in ("dual", "barrier", "spec_stagger"):
+        tt = _time_steps(torch, step(name), max(3, args.steps // 2), 1, flush, stream)
+        s2 = plans[name].status()
+        if s2["code"] != 0:
+            raise RuntimeError(f"{name} failed: {s2}")
+        proto[name] = {"us_per_epoch": round(sum(tt) / len(tt) * 1000 / EPOCHS, 4)}
+        if name == "spec_stagger":
+            proto[name]["retries_per_check"] = (s2["spec_retries"] / s2["spec_checks"]
+                                                if s2["spec_checks"] else 0.0)
+    proto["spec"] = {"us_per_epoch": round(us_epoch, 4),
+                     "retries_per_check": (st["spec_retries"] / st["spec_checks"]
+                                           if st["spec_checks"] else 0.0)}
+
+    # per-epoch latency percentiles from %globaltimer stamps (spec)
+    sp = cdc.Plan(nm, protocol="spec", record_stamps=1, stamp_capacity=EPOCHS)
+    sp.run(ins, outs, **kw)
+    sp.run(ins, outs, **kw)
+    stamps = sp.stamps(EPOCHS).astype(np.int64)
+    d = np.diff(stamps) / 1000.0
+    lat = {"p50_us": round(float(np.percentile(d, 50)), 3),
+           "p99_us": round(float(np.percentile(d, 99)), 3)} if d.size else {}
+    sp.free()
+
+    # end to end through the C ABI with host buffers: H2D of the step's inputs (pinned),
+    # the run, D2H of every epoch's outputs
+    host_pinned_in = [torch.from_numpy(h).pin_memory() for h in host_in]
+    host_pinned_out = [torch.empty(EPOCHS, N_DECODE, dtype=torch.int16).pin_memory()
+                       for _ in range(R_DECODE)]
+    h2d = sum(h.numel() * 2 for h in host_pinned_in)
+    d2h = sum(h.numel() * 2 for h in host_pinned_out)
+
+    def e2e_step():
+        for r in range(R_DECODE):
+            ins[r].copy_(host_pinned_in[r], non_blocking=True)
+        plans["spec"].run(ins, outs, **kw)
+        for r in range(R_DECODE):
+            host_pinned_out[r].copy_(outs[r], non_blocking=True)
+
+    te = _time_steps(torch, e2e_step, max(3, args.steps // 2), 2, flush, stream)
+    e2e_us = sum(te) / len(te) * 1000 / EPOCHS
+
+    # prefill-sized all-reduce: 8 x 64 MiB bf16, one-shot vs two-shot (zero-copy)
+    prefill = {}
+    if not args.skip_prefill:
+        n = 8192 * 4096
+        rng = synth.seeded_rng(4)
+        g = torch.Generator(device=dev)
+        g.manual_seed(4)
+        pins = [torch.randn(n, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
+                for _ in range(R_DECODE)]
+        pouts = [torch.empty(n, dtype=torch.int16, device=dev) for _ in range(R_DECODE)]
+        nmp = cdc.allreduce(R_DECODE, n, "bf16")
+        for dp in ("twoshot", "oneshot"):
+            pl = cdc.Plan(nmp, zero_copy=1, datapath=dp)
+            tt = _time_steps(torch, lambda: pl.run(pins, pouts), 10, 3, flush, stream)
+            assert pl.status()["code"] == 0
+            b = pl.info.min_bytes
+            gbs = b / (sum(tt) / len(tt) / 1000) / 1e9
+            prefill[dp] = {"ms": round(sum(tt) / len(tt), 4), "gbs": round(gbs, 1),
+                           "frac": round(gbs / peak, 4), "min_bytes": b}
+            pl.free()
+        del pins, pouts
+
+    algo_bytes = 2 * R_DECODE * N_DECODE * 2 * EPOCHS
+    achieved = algo_bytes / (ms / 1000) / 1e9
+    for p in plans.values():
+        p.free()
+    clocks = clk.summary()
+    res = {
+        "metric": "us per small All-Reduce epoch (TP decode, 8 emulated ranks x 8 KiB bf16)",
+        "value": round(us_epoch, 4),
+        "unit": "us/epoch",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, pool of 7 input sets)",
+        "config": {"workload": "TP decode all-reduce: R=8 emulated ranks x 4096 bf16 per rank, "
+                               "10000 epochs per step in one persistent launch, speculative "
+                               "protocol (dual buffers, tagged validation), oneshot",
+                   "ranks": R_DECODE, "elems_per_rank": N_DECODE, "epochs_per_step": EPOCHS,
+                   "input_pool": POOL, "protocol": "spec", "l2": "flushed before every timed "
+                   "step (256 MiB write)", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 5),
+                     "traffic": None, "peak_kind": f"of {peak_kind}",
+                     "note": "latency-bound: 128 KiB of algorithmic bytes per epoch"},
+        "latency": lat,
+        "protocols": proto,
+        "prefill_allreduce_64MiB": prefill,
+        "e2e": {"value": round(e2e_us, 4), "unit": "us/epoch", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(pool_np, seconds=args.cpu_seconds)
+    return res
+
+
+# ------------------------------------------------------------------ oracle timing
+
+def cpu_baseline(pool_np, seconds=10.0):
+    """The oracle, as it stands, on the host: fixed-order all-reduce epochs of the decode
+    workload until about `seconds` have passed (a bounded sample of the 10,000 epochs)."""
+    from oracle import collectives
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        for r_out in collectives.allreduce(pool_np[n % POOL], "bf16"):
+            pass
+        n += 1
+        if n % 50 == 0 and time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(dt / n * 1e6, 3), "unit": "us/epoch", "cores": 1, "kind": "oracle",
+            "sample": f"{n} epochs of the 8 x 4096 bf16 all-reduce (numpy, one thread)"}
+
+
+def run_reference(args):
+    rng = synth.seeded_rng(2)
+    pool_np = [[synth.normal_bf16(rng, N_DECODE) for _ in range(R_DECODE)] for _ in range(POOL)]
+    from oracle import collectives
+    per_step = max(20, int(args.ref_epochs))
+    for _ in range(args.warmup):
+        for e in range(per_step):
+            collectives.allreduce(pool_np[e % POOL], "bf16")
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        for e in range(per_step):
+            collectives.allreduce(pool_np[e % POOL], "bf16")
+        times.append(time.perf_counter() - t0)
+    us = sum(times) / len(times) / per_step * 1e6
+    cb = {"value": round(us, 3), "unit": "us/epoch", "cores": 1, "kind": "oracle",
+          "sample": f"{per_step} epochs per step of the 8 x 4096 bf16 all-reduce"}
+    return {
+        "impl": "reference",
+        "metric": "us per small All-Reduce epoch (TP decode, 8 emulated ranks x 8 KiB bf16)",
+        "value": round(us, 3), "unit": "us/epoch", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(sum(times) / len(times) * 1000, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, pool of 7 input sets)",
+        "config": {"workload": "TP decode all-reduce: R=8 emulated ranks x 4096 bf16 per rank "
+                               "(CPU oracle, bounded sample of the 10000 epochs)",
+                   "ranks": R_DECODE, "elems_per_rank": N_DECODE, "input_pool": POOL},
+        "cpu_baseline": cb,
+        "e2e": {"value": round(us, 3), "unit": "us/epoch", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-epochs", type=int, default=2000)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-prefill", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    res = run_ours(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

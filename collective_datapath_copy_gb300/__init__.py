@@ -1,0 +1,13 @@
+"""Collective datapath (copy / reduce) on one GB300, emulating R ranks on one GPU.
+
+A collective is a naming of per-rank input and output segments plus copy or sum
+(``namings``); ``Plan`` compiles it through the C ABI of libcoll.so (include/coll.h) and
+runs it with the staged Stage/Notify/Consume engine (barrier, dual-buffer or speculative
+protocol) or the zero-copy datapath. The library is required: there is no fallback.
+"""
+
+from . import namings  # noqa: F401
+from ._lib import CollError, lib  # noqa: F401
+from .namings import (Naming, allgather, allreduce, alltoall, broadcast,  # noqa: F401
+                      moe_dispatch, reduce_scatter, segs)
+from .plan import Plan, validate, validate_code  # noqa: F401

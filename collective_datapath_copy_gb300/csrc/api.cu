@@ -1,0 +1,344 @@
+// C ABI: plan lifecycle and runs (see include/coll.h for the contract of each call).
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "coll_internal.h"
+#include "engine.cuh"
+
+struct coll_plan_s {
+  coll_compiled c;
+  int device = 0;
+  int num_sms = 0;
+  char *d_tables = nullptr;  // one allocation for every read-only table
+  coll_ref_t *d_refs = nullptr;
+  coll_job_t *d_jobs = nullptr;
+  coll_tile_t *d_tiles = nullptr;
+  coll_unit_t *d_units = nullptr;
+  coll_item_t *d_sitems = nullptr, *d_citems = nullptr;
+  coll_warp_t *d_warps = nullptr;
+  char *d_xbuf = nullptr;
+  unsigned long long *d_pflag = nullptr;
+  uint32_t *d_cflag = nullptr;
+  coll_dev_status_t *d_status = nullptr;
+  uint64_t *d_stamps = nullptr;
+  uint32_t *d_dbg = nullptr;
+  uint32_t stamp_cap = 0;
+  uint64_t epochs_issued = 0;
+  cudaEvent_t done = nullptr;
+  bool ran = false;
+  int last_epochs = 0;
+};
+
+namespace {
+
+template <typename T>
+size_t table_bytes(const std::vector<T> &v) {
+  return (v.size() * sizeof(T) + 255) & ~(size_t)255;
+}
+
+template <typename T>
+T *carve(char *base, size_t &off, const std::vector<T> &v) {
+  T *p = reinterpret_cast<T *>(base + off);
+  off += table_bytes(v);
+  return v.empty() ? nullptr : p;
+}
+
+void release(coll_plan_s *p) {
+  if (!p) return;
+  if (p->done) {
+    cudaEventSynchronize(p->done);
+    cudaEventDestroy(p->done);
+  }
+  cudaFree(p->d_tables);
+  cudaFree(p->d_xbuf);
+  cudaFree(p->d_pflag);
+  cudaFree(p->d_cflag);
+  cudaFree(p->d_status);
+  cudaFree(p->d_stamps);
+  cudaFree(p->d_dbg);
+  delete p;
+}
+
+int zero_state(coll_plan_s *p) {
+  const coll_compiled &c = p->c;
+  if (p->d_pflag && cudaMemset(p->d_pflag, 0, (size_t)c.n_pflag * 2 * 8) != cudaSuccess)
+    return COLL_ECUDA;
+  if (p->d_cflag && cudaMemset(p->d_cflag, 0, (size_t)c.n_cflag * 4) != cudaSuccess)
+    return COLL_ECUDA;
+  if (p->d_dbg && cudaMemset(p->d_dbg, 0, (size_t)c.units.size() * 4) != cudaSuccess)
+    return COLL_ECUDA;
+  if (cudaMemset(p->d_status, 0, sizeof(coll_dev_status_t)) != cudaSuccess) return COLL_ECUDA;
+  p->epochs_issued = 0;
+  return COLL_OK;
+}
+
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
+  return a0 < b1 && b0 < a1;
+}
+
+}  // namespace
+
+extern "C" int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_seg_t *in_segs,
+                         size_t n_in, const uint64_t *in_len, const coll_seg_t *out_segs,
+                         size_t n_out, const uint64_t *out_len, const coll_config_t *cfg) {
+  if (!out) return COLL_EINVAL;
+  *out = nullptr;
+  coll_plan_s *p = new (std::nothrow) coll_plan_s();
+  if (!p) return COLL_ENOMEM;
+  int e = coll_compile(R, op, dtype, in_segs, n_in, in_len, out_segs, n_out, out_len, cfg, 0, &p->c);
+  if (e) {
+    delete p;
+    return e;
+  }
+  coll_compiled &c = p->c;
+  if (cudaGetDevice(&p->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
+    delete p;
+    return COLL_ECUDA;
+  }
+  if (!c.cfg.zero_copy) {
+    int max_ctas = 0;
+    if (coll::engine_max_coresident(c.op, c.dtype, &max_ctas) != cudaSuccess) {
+      delete p;
+      return COLL_ECUDA;
+    }
+    if (c.warps.size() > (size_t)max_ctas) {  // every engine warp must be co-resident
+      delete p;
+      return COLL_EINVAL;
+    }
+  }
+  const size_t tb = table_bytes(c.refs) + table_bytes(c.jobs) + table_bytes(c.tiles) +
+                    table_bytes(c.units) + table_bytes(c.sitems) + table_bytes(c.citems) +
+                    table_bytes(c.warps);
+  std::vector<char> host(tb ? tb : 256, 0);
+  size_t off = 0;
+  auto put = [&](const auto &v) {
+    if (!v.empty()) memcpy(host.data() + off, v.data(), v.size() * sizeof(v[0]));
+    off += table_bytes(v);
+  };
+  put(c.refs); put(c.jobs); put(c.tiles); put(c.units); put(c.sitems); put(c.citems); put(c.warps);
+  bool ok = cudaMalloc(&p->d_tables, host.size()) == cudaSuccess &&
+            cudaMemcpy(p->d_tables, host.data(), host.size(), cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMalloc(&p->d_status, sizeof(coll_dev_status_t)) == cudaSuccess &&
+            cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming) == cudaSuccess;
+  if (ok) {
+    off = 0;
+    p->d_refs = carve(p->d_tables, off, c.refs);
+    p->d_jobs = carve(p->d_tables, off, c.jobs);
+    p->d_tiles = carve(p->d_tables, off, c.tiles);
+    p->d_units = carve(p->d_tables, off, c.units);
+    p->d_sitems = carve(p->d_tables, off, c.sitems);
+    p->d_citems = carve(p->d_tables, off, c.citems);
+    p->d_warps = carve(p->d_tables, off, c.warps);
+  }
+  if (ok && !c.cfg.zero_copy) {
+    const bool dual = c.cfg.protocol != COLL_PROTO_BARRIER;
+    const size_t xb = (size_t)c.xpar_bytes * (dual ? 2 : 1);
+    ok = (xb == 0 || cudaMalloc(&p->d_xbuf, xb) == cudaSuccess) &&
+         (c.n_pflag == 0 || cudaMalloc(&p->d_pflag, (size_t)c.n_pflag * 2 * 8) == cudaSuccess) &&
+         (c.n_cflag == 0 || cudaMalloc(&p->d_cflag, (size_t)c.n_cflag * 4) == cudaSuccess);
+    if (ok && xb) ok = cudaMemset(p->d_xbuf, 0, xb) == cudaSuccess;
+    if (ok && (c.cfg.inject_flags & COLL_INJECT_SPEC_PAUSE) && !c.units.empty())
+      ok = cudaMalloc(&p->d_dbg, c.units.size() * 4) == cudaSuccess;
+    if (ok && c.cfg.record_stamps && c.cfg.stamp_capacity) {
+      p->stamp_cap = c.cfg.stamp_capacity;
+      ok = cudaMalloc(&p->d_stamps, ((size_t)p->stamp_cap + 1) * 8) == cudaSuccess;
+    }
+  }
+  if (ok) ok = zero_state(p) == COLL_OK;
+  if (!ok) {
+    cudaGetLastError();
+    release(p);
+    return COLL_ECUDA;
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    release(p);
+    return COLL_ECUDA;
+  }
+  *out = p;
+  return COLL_OK;
+}
+
+extern "C" int coll_plan_info(coll_plan_t p, coll_plan_info_t *info) {
+  if (!p || !info) return COLL_EINVAL;
+  coll_fill_info(p->c, info);
+  return COLL_OK;
+}
+
+extern "C" int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_epochs,
+                        int64_t in_epoch_stride, int in_pool, int64_t out_epoch_stride,
+                        void *stream) {
+  if (!p || !in || !out || n_epochs < 1 || in_pool < 1) return COLL_EINVAL;
+  const coll_compiled &c = p->c;
+  const int R = c.R;
+  coll::RankPtrs ptr;
+  memset(&ptr, 0, sizeof(ptr));
+  // spans touched over all epochs, for the aliasing check
+  std::vector<uintptr_t> i0(R, 0), i1(R, 0), o0(R, 0), o1(R, 0);
+  const bool staged = !c.cfg.zero_copy;
+  for (int r = 0; r < R; ++r) {
+    if (c.in_used[r]) {
+      if (!in[r]) return COLL_EINVAL;
+      if (staged && ((uintptr_t)in[r] & 15u)) return COLL_EALIGN;
+      const int64_t lo = std::min<int64_t>(0, in_epoch_stride * (in_pool - 1));
+      const int64_t hi = std::max<int64_t>(0, in_epoch_stride * (in_pool - 1));
+      i0[r] = (uintptr_t)in[r] + lo;
+      i1[r] = (uintptr_t)in[r] + hi + c.in_bytes[r];
+    }
+    if (c.out_used[r]) {
+      if (!out[r]) return COLL_EINVAL;
+      if (staged && ((uintptr_t)out[r] & 15u)) return COLL_EALIGN;
+      const int64_t lo = std::min<int64_t>(0, out_epoch_stride * (n_epochs - 1));
+      const int64_t hi = std::max<int64_t>(0, out_epoch_stride * (n_epochs - 1));
+      o0[r] = (uintptr_t)out[r] + lo;
+      o1[r] = (uintptr_t)out[r] + hi + c.out_bytes[r];
+    }
+    ptr.in[r] = (const char *)in[r];
+    ptr.out[r] = (char *)out[r];
+  }
+  if (staged && (((uint64_t)(in_epoch_stride < 0 ? -in_epoch_stride : in_epoch_stride) & 15u) ||
+                 ((uint64_t)(out_epoch_stride < 0 ? -out_epoch_stride : out_epoch_stride) & 15u)))
+    return COLL_EALIGN;
+  for (int r = 0; r < R; ++r) {
+    if (!c.out_used[r]) continue;
+    for (int q = 0; q < R; ++q) {
+      if (c.in_used[q] && overlaps(o0[r], o1[r], i0[q], i1[q])) return COLL_EOVERLAP;
+      if (q != r && c.out_used[q] && overlaps(o0[r], o1[r], o0[q], o1[q])) return COLL_EOVERLAP;
+    }
+    // an output buffer reused across epochs must not overlap itself between epochs
+    if (out_epoch_stride != 0 && n_epochs > 1 &&
+        (uint64_t)(out_epoch_stride < 0 ? -out_epoch_stride : out_epoch_stride) < c.out_bytes[r])
+      return COLL_EOVERLAP;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t err;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != p->device) return COLL_EINVAL;
+  if (c.cfg.zero_copy) {
+    coll::ZcArgs a;
+    memset(&a, 0, sizeof(a));
+    a.ptr = ptr;
+    a.jobs = p->d_jobs;
+    a.refs = p->d_refs;
+    a.tiles = p->d_tiles;
+    a.ntiles = (uint32_t)c.tiles.size();
+    a.n_epochs = (uint32_t)n_epochs;
+    a.in_pool = in_pool;
+    a.in_stride = in_epoch_stride;
+    a.out_stride = out_epoch_stride;
+    const int ctas = c.cfg.ctas ? c.cfg.ctas : 2 * p->num_sms;
+    const int keep = (c.op == COLL_OP_SUM && c.cfg.datapath == COLL_DP_ONESHOT) ? 1 : 0;
+    err = coll::launch_zero_copy(c.op, c.dtype, keep, a, ctas, s);
+  } else {
+    if (p->epochs_issued + (uint64_t)n_epochs >= 0xFFFFFFF0ull) return COLL_EINVAL;  // reset first
+    coll::EngArgs a;
+    memset(&a, 0, sizeof(a));
+    a.ptr = ptr;
+    a.units = p->d_units;
+    a.sitems = p->d_sitems;
+    a.citems = p->d_citems;
+    a.warps = p->d_warps;
+    a.refs = p->d_refs;
+    a.xbuf = p->d_xbuf;
+    a.xpar = c.xpar_bytes;
+    a.pflag = p->d_pflag;
+    a.cflag = p->d_cflag;
+    a.st = p->d_status;
+    a.stamps = p->d_stamps;
+    a.dbg = p->d_dbg;
+    a.stamp_cap = p->stamp_cap;
+    a.n_pflag = c.n_pflag;
+    a.nwarps = (uint32_t)c.warps.size();
+    a.n_epochs = n_epochs;
+    a.in_pool = in_pool;
+    a.epoch_base = (uint32_t)p->epochs_issued;
+    a.in_stride = in_epoch_stride;
+    a.out_stride = out_epoch_stride;
+    a.protocol = c.cfg.protocol;
+    a.spec_check = c.cfg.spec_check;
+    a.spin_ns = c.cfg.spin_limit_ns ? c.cfg.spin_limit_ns : 2000000000ull;
+    a.inject_flags = c.cfg.inject_flags;
+    a.inject_seed = c.cfg.inject_seed;
+    a.inject_rank = c.cfg.inject_rank;
+    a.inject_prob_ppm = c.cfg.inject_prob_ppm;
+    a.inject_max_ns = c.cfg.inject_max_ns;
+    a.inject_start_ns = c.cfg.inject_start_ns;
+    a.inject_pause_ns = c.cfg.inject_pause_ns;
+    a.R = R;
+    err = coll::launch_engine(c.op, c.dtype, a, s);
+    if (err == cudaSuccess) p->epochs_issued += (uint64_t)n_epochs;
+  }
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return COLL_ECUDA;
+  }
+  if (cudaEventRecord(p->done, s) != cudaSuccess) return COLL_ECUDA;
+  p->ran = true;
+  p->last_epochs = n_epochs;
+  return COLL_OK;
+}
+
+extern "C" int coll_status(coll_plan_t p, coll_stats_t *st) {
+  if (!p) return COLL_EINVAL;
+  if (p->ran && cudaEventSynchronize(p->done) != cudaSuccess) return COLL_ECUDA;
+  coll_dev_status_t d;
+  if (cudaMemcpy(&d, p->d_status, sizeof(d), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return COLL_ECUDA;
+  if (st) {
+    memset(st, 0, sizeof(*st));
+    st->status = d.status;
+    st->fail_rank = d.status ? d.fail_rank : -1;
+    st->fail_unit = d.status ? d.fail_unit : -1;
+    st->fail_where = d.fail_where;
+    st->fail_epoch = d.fail_epoch;
+    st->epochs = d.status ? 0 : p->epochs_issued;
+    st->spec_checks = d.spec_checks;
+    st->spec_retries = d.spec_retries;
+  }
+  return d.status;
+}
+
+extern "C" int64_t coll_stamps(coll_plan_t p, uint64_t *host, int64_t n) {
+  if (!p || !host || n < 0) return COLL_EINVAL;
+  if (!p->d_stamps) return 0;
+  if (p->ran && cudaEventSynchronize(p->done) != cudaSuccess) return COLL_ECUDA;
+  int64_t m = std::min<int64_t>(n, (int64_t)std::min<uint32_t>(p->stamp_cap, (uint32_t)p->last_epochs) + 1);
+  if (cudaMemcpy(host, p->d_stamps, (size_t)m * 8, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return COLL_ECUDA;
+  return m;
+}
+
+extern "C" int coll_reset(coll_plan_t p) {
+  if (!p) return COLL_EINVAL;
+  if (p->ran && cudaEventSynchronize(p->done) != cudaSuccess) return COLL_ECUDA;
+  int e = zero_state(p);
+  if (e) return e;
+  return cudaDeviceSynchronize() == cudaSuccess ? COLL_OK : COLL_ECUDA;
+}
+
+extern "C" int coll_free(coll_plan_t p) {
+  if (!p) return COLL_OK;
+  release(p);
+  return COLL_OK;
+}
+
+extern "C" const char *coll_strerror(int code) {
+  switch (code) {
+    case COLL_OK: return "success";
+    case COLL_EINVAL: return "invalid argument";
+    case COLL_ENAME: return "a consumed name has no producer (or several, for copy)";
+    case COLL_ELEN: return "segments with one name have different lengths";
+    case COLL_EBOUNDS: return "segment out of its buffer's bounds";
+    case COLL_EOVERLAP: return "overlapping output segments or buffers";
+    case COLL_EALIGN: return "staged plans need 16-byte-aligned segments, buffers and strides";
+    case COLL_ECUDA: return "CUDA runtime error";
+    case COLL_ETIMEDOUT: return "a bounded device wait expired";
+    case COLL_EDEVICE: return "inconsistent device state";
+    case COLL_ENOMEM: return "out of memory";
+    default: return "unknown error";
+  }
+}

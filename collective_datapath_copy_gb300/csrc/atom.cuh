@@ -1,0 +1,190 @@
+// Atom: the two datapath primitives of a collective, copy and reduce, for sm_103a.
+//
+// Source: Purlin article, figure "Purlin separates the collective stack" and section
+// "The Purlin PDF describes a three-layer design": under the shared orchestration sits a
+// hardware-specific datapath that implements exactly two data movement primitives, copy
+// and reduce. Here both move 16-byte vectors; reduce widens bf16 to binary32, adds in the
+// order it is given (round to nearest even, no FMA: there is nothing to fuse), and rounds
+// once back to bf16 with cvt.rn.
+#pragma once
+
+#include <stdint.h>
+
+namespace coll {
+
+// ------------------------------------------------------------------ memory ops (PTX)
+
+// Read-only input data: non-coherent path, may be cached in L1.
+__device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Streaming read (evict-first): data read exactly once.
+__device__ __forceinline__ uint4 ld_cs_v4(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Peer data written by another warp during this kernel: GPU-scope relaxed load, never
+// served from a stale L1 line.
+__device__ __forceinline__ uint4 ld_relaxed_v4(const void *p) {
+  uint4 r;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p)
+               : "memory");
+  return r;
+}
+
+__device__ __forceinline__ void st_v4(void *p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Streaming store (evict-first): output written once.
+__device__ __forceinline__ void st_cs_v4(void *p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_u32(uint32_t *p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------------ reduce arithmetic
+
+// bf16x8 in a 16-byte vector -> 8 binary32 values (exact widening).
+__device__ __forceinline__ void bf16x8_init(float a[8], uint4 v) {
+  a[0] = __uint_as_float(v.x << 16);
+  a[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  a[2] = __uint_as_float(v.y << 16);
+  a[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  a[4] = __uint_as_float(v.z << 16);
+  a[5] = __uint_as_float(v.z & 0xFFFF0000u);
+  a[6] = __uint_as_float(v.w << 16);
+  a[7] = __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ void bf16x8_add(float a[8], uint4 v) {
+  a[0] = __fadd_rn(a[0], __uint_as_float(v.x << 16));
+  a[1] = __fadd_rn(a[1], __uint_as_float(v.x & 0xFFFF0000u));
+  a[2] = __fadd_rn(a[2], __uint_as_float(v.y << 16));
+  a[3] = __fadd_rn(a[3], __uint_as_float(v.y & 0xFFFF0000u));
+  a[4] = __fadd_rn(a[4], __uint_as_float(v.z << 16));
+  a[5] = __fadd_rn(a[5], __uint_as_float(v.z & 0xFFFF0000u));
+  a[6] = __fadd_rn(a[6], __uint_as_float(v.w << 16));
+  a[7] = __fadd_rn(a[7], __uint_as_float(v.w & 0xFFFF0000u));
+}
+
+// Two binary32 -> packed bf16x2, round to nearest even (lo element in the low half).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint4 bf16x8_pack(const float a[8]) {
+  return make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                    pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+}
+
+__device__ __forceinline__ void f32x4_init(float a[4], uint4 v) {
+  a[0] = __uint_as_float(v.x);
+  a[1] = __uint_as_float(v.y);
+  a[2] = __uint_as_float(v.z);
+  a[3] = __uint_as_float(v.w);
+}
+
+__device__ __forceinline__ void f32x4_add(float a[4], uint4 v) {
+  a[0] = __fadd_rn(a[0], __uint_as_float(v.x));
+  a[1] = __fadd_rn(a[1], __uint_as_float(v.y));
+  a[2] = __fadd_rn(a[2], __uint_as_float(v.z));
+  a[3] = __fadd_rn(a[3], __uint_as_float(v.w));
+}
+
+__device__ __forceinline__ uint4 f32x4_pack(const float a[4]) {
+  return make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                    __float_as_uint(a[3]));
+}
+
+// Accumulator over one 16-byte vector for element type DT (0 = bf16, 1 = f32).
+template <int DT>
+struct Vec16Acc {
+  float a[DT == 0 ? 8 : 4];
+  __device__ __forceinline__ void init(uint4 v) {
+    if constexpr (DT == 0) bf16x8_init(a, v); else f32x4_init(a, v);
+  }
+  __device__ __forceinline__ void add(uint4 v) {
+    if constexpr (DT == 0) bf16x8_add(a, v); else f32x4_add(a, v);
+  }
+  __device__ __forceinline__ uint4 pack() const {
+    if constexpr (DT == 0) return bf16x8_pack(a); else return f32x4_pack(a);
+  }
+};
+
+// ------------------------------------------------------------------ content tag
+
+// Integer mixer (multiply / xor-shift rounds) for the per-piece content tag.
+__device__ __forceinline__ uint32_t mix32(uint32_t x) {
+  x *= 0x9E3779B1u;
+  x ^= x >> 15;
+  x *= 0x2C1B3C6Du;
+  x ^= x >> 12;
+  x *= 0x297A2D39u;
+  x ^= x >> 15;
+  return x;
+}
+
+// Order-independent contribution of vector `vi` (index inside its piece).
+__device__ __forceinline__ uint32_t tag_part(uint4 v, uint32_t vi) {
+  uint32_t s = vi * 0x01000193u;
+  return mix32(v.x ^ s) + mix32(v.y ^ (s + 0x68E31DA4u)) + mix32(v.z ^ (s + 0xB5297A4Du)) +
+         mix32(v.w ^ (s + 0x1B56C4E9u));
+}
+
+__device__ __forceinline__ uint32_t tag_fold(uint32_t h, uint32_t epoch) {
+  return mix32(h + epoch * 0x85EBCA6Bu);
+}
+
+}  // namespace coll

@@ -1,0 +1,476 @@
+// Kernels of the collective datapath for sm_103a.
+//
+// zc_kernel     — zero-copy datapath: every consumer reads the producers' input buffers
+//                 directly; the kernel launch itself orders producers before consumers.
+// engine_kernel — the staged Stage / Notify / Consume engine: a persistent cooperative
+//                 launch in which one warp per CTA plays part of one emulated rank and
+//                 loops over epochs, synchronising with the other ranks' warps only
+//                 through epoch flags in global memory.
+//
+// Sources: Purlin article, "The Purlin PDF describes a three-layer design" (naming,
+// SNAC = Stage / Notify / And Consume, Atom copy/reduce); SiFAR review, "What carries the
+// argument", abstract and Figs. 5, 6, 14 (oneshot and twoshot, top and bottom barriers,
+// dual buffering, speculative reduction validated by a reduced flag with retry).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "atom.cuh"
+#include "engine.cuh"
+
+namespace coll {
+
+namespace {
+
+constexpr unsigned FULL = 0xFFFFFFFFu;
+
+// ============================================================== zero-copy datapath
+
+// KIND: 0 copy (bytes), 1 sum of bf16, 2 sum of f32.
+// KEEP: inputs are read again by other tiles (oneshot) -> keep them cacheable; otherwise
+//       every input byte is read once and streamed.
+template <int KIND, bool KEEP>
+__device__ __forceinline__ uint4 zc_load(const char *p) {
+  if constexpr (KEEP) return ld_nc_v4(p); else return ld_cs_v4(p);
+}
+
+template <int KIND, bool KEEP>
+__global__ void __launch_bounds__(512) zc_kernel(const ZcArgs a) {
+  __shared__ const char *s_src[COLL_MAX_FANIN];
+  __shared__ char *s_dst[COLL_MAX_FANOUT];
+  const uint32_t tid = threadIdx.x, bd = blockDim.x;
+  const uint64_t total = (uint64_t)a.ntiles * a.n_epochs;
+  for (uint64_t t = blockIdx.x; t < total; t += gridDim.x) {
+    const uint32_t e = (uint32_t)(t / a.ntiles);
+    const uint32_t ti = (uint32_t)(t - (uint64_t)e * a.ntiles);
+    const coll_tile_t tile = a.tiles[ti];
+    const coll_job_t job = a.jobs[tile.job];
+    const int64_t ioff = (int64_t)(e % (uint32_t)a.in_pool) * a.in_stride + (int64_t)tile.start;
+    const int64_t ooff = (int64_t)e * a.out_stride + (int64_t)tile.start;
+    __syncthreads();  // the previous tile is done with the pointer tables
+    uint32_t mis = tile.nbytes & 15u;
+    for (uint32_t i = tid; i < job.nsrc; i += bd) {
+      const coll_ref_t r = a.refs[job.src0 + i];
+      const char *p = a.ptr.in[r.rank] + r.off + ioff;
+      s_src[i] = p;
+      mis |= (uint32_t)((uintptr_t)p & 15u);
+    }
+    for (uint32_t i = tid; i < job.ndst; i += bd) {
+      const coll_ref_t r = a.refs[job.dst0 + i];
+      char *p = a.ptr.out[r.rank] + r.off + ooff;
+      s_dst[i] = p;
+      mis |= (uint32_t)((uintptr_t)p & 15u);
+    }
+    const int misaligned = __syncthreads_or(mis != 0);
+    const uint32_t nsrc = job.nsrc, ndst = job.ndst;
+    if (!misaligned) {
+      const uint32_t nvec = tile.nbytes >> 4;
+      if constexpr (KIND == 0) {
+        for (uint32_t base = tid; base < nvec; base += 4 * bd) {
+          uint4 x[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t idx = base + u * bd;
+            if (idx < nvec) x[u] = zc_load<KIND, KEEP>(s_src[0] + (size_t)idx * 16);
+          }
+          for (uint32_t d = 0; d < ndst; ++d) {
+            char *q = s_dst[d];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t idx = base + u * bd;
+              if (idx < nvec) st_cs_v4(q + (size_t)idx * 16, x[u]);
+            }
+          }
+        }
+      } else {
+        for (uint32_t idx = tid; idx < nvec; idx += bd) {
+          Vec16Acc<KIND - 1> acc;
+          for (uint32_t k0 = 0; k0 < nsrc; k0 += 8) {
+            uint4 x[8];
+            const uint32_t kn = nsrc - k0 < 8 ? nsrc - k0 : 8;
+#pragma unroll
+            for (uint32_t k = 0; k < 8; ++k)
+              if (k < kn) x[k] = zc_load<KIND, KEEP>(s_src[k0 + k] + (size_t)idx * 16);
+#pragma unroll
+            for (uint32_t k = 0; k < 8; ++k) {
+              if (k < kn) {
+                if (k0 + k == 0) acc.init(x[k]); else acc.add(x[k]);
+              }
+            }
+          }
+          const uint4 r = acc.pack();
+          for (uint32_t d = 0; d < ndst; ++d) st_cs_v4(s_dst[d] + (size_t)idx * 16, r);
+        }
+      }
+    } else {
+      // Unaligned tile: element-wise path (same arithmetic, same order).
+      if constexpr (KIND == 0) {
+        for (uint32_t i = tid; i < tile.nbytes; i += bd) {
+          const char v = s_src[0][i];
+          for (uint32_t d = 0; d < ndst; ++d) s_dst[d][i] = v;
+        }
+      } else if constexpr (KIND == 1) {
+        for (uint32_t i = tid; i < tile.nbytes / 2; i += bd) {
+          float acc = __uint_as_float((uint32_t)((const uint16_t *)s_src[0])[i] << 16);
+          for (uint32_t k = 1; k < nsrc; ++k)
+            acc = __fadd_rn(acc, __uint_as_float((uint32_t)((const uint16_t *)s_src[k])[i] << 16));
+          const uint16_t r = (uint16_t)(pack_bf16x2(acc, 0.0f) & 0xFFFFu);
+          for (uint32_t d = 0; d < ndst; ++d) ((uint16_t *)s_dst[d])[i] = r;
+        }
+      } else {
+        for (uint32_t i = tid; i < tile.nbytes / 4; i += bd) {
+          float acc = ((const float *)s_src[0])[i];
+          for (uint32_t k = 1; k < nsrc; ++k) acc = __fadd_rn(acc, ((const float *)s_src[k])[i]);
+          for (uint32_t d = 0; d < ndst; ++d) ((float *)s_dst[d])[i] = acc;
+        }
+      }
+    }
+  }
+}
+
+// ============================================================== staged engine
+
+struct CopyAcc {
+  uint4 v;
+  __device__ __forceinline__ void init(uint4 x) { v = x; }
+  __device__ __forceinline__ void add(uint4) {}
+  __device__ __forceinline__ uint4 pack() const { return v; }
+};
+
+template <int KIND>
+struct EngAcc {
+  using type = Vec16Acc<KIND - 1>;
+};
+template <>
+struct EngAcc<0> {
+  using type = CopyAcc;
+};
+
+__device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
+  x += 0x9E3779B97F4A7C15ull;
+  x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+  x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+  return x ^ (x >> 31);
+}
+
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+  if (ns == 0) return;
+  const uint64_t t0 = globaltimer();
+  while (globaltimer() - t0 < ns) {
+  }
+}
+
+// Poll until `ok(value)`; bounded by the spin limit and by the plan's abort word.
+// Returns false on timeout or abort. One lane, one flag.
+template <typename Pred>
+__device__ __forceinline__ bool spin_u64(const unsigned long long *f, Pred ok,
+                                         const coll_dev_status_t *st, uint64_t limit) {
+  uint64_t t0 = 0;
+  for (uint32_t k = 0;; ++k) {
+    const unsigned long long v = ld_acquire_u64(f);
+    if (ok(v)) return true;
+    if ((k & 31u) == 31u) {
+      const uint64_t now = globaltimer();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > limit) return false;
+      if (ld_relaxed_u32(&st->abort)) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool spin_done(const uint32_t *f, uint32_t target,
+                                          const coll_dev_status_t *st, uint64_t limit) {
+  uint64_t t0 = 0;
+  for (uint32_t k = 0;; ++k) {
+    const uint32_t v = ld_acquire_u32(f);
+    if ((int32_t)(v - target) >= 0) return true;
+    if ((k & 31u) == 31u) {
+      const uint64_t now = globaltimer();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > limit) return false;
+      if (ld_relaxed_u32(&st->abort)) return false;
+    }
+  }
+}
+
+__device__ void record_timeout(coll_dev_status_t *st, int rank, int unit, int where,
+                               uint32_t epoch) {
+  if (atomicCAS(&st->status, 0, COLL_ETIMEDOUT) == 0) {
+    st->fail_rank = rank;
+    st->fail_unit = unit;
+    st->fail_where = where;
+    st->fail_epoch = epoch;
+  }
+  st_relaxed_u32(&st->abort, 1u);
+}
+
+// Wait (all lanes cooperating) until every producer flag of a unit carries epoch E.
+__device__ __forceinline__ bool wait_producers(const unsigned long long *pf, uint32_t n,
+                                               uint32_t E, const coll_dev_status_t *st,
+                                               uint64_t limit) {
+  const uint32_t lane = threadIdx.x & 31u;
+  bool ok = true;
+  for (uint32_t j = lane; j < n; j += 32)
+    ok = ok && spin_u64(pf + j, [E](unsigned long long v) { return (uint32_t)(v >> 32) == E; },
+                        st, limit);
+  return __all_sync(FULL, ok);
+}
+
+__device__ __forceinline__ bool wait_consumers_done(const uint32_t *cf, uint32_t n,
+                                                    uint32_t target,
+                                                    const coll_dev_status_t *st,
+                                                    uint64_t limit) {
+  const uint32_t lane = threadIdx.x & 31u;
+  bool ok = true;
+  for (uint32_t j = lane; j < n; j += 32) ok = ok && spin_done(cf + j, target, st, limit);
+  return __all_sync(FULL, ok);
+}
+
+// Reduce (or copy) the n pieces of a unit in slot order, loads in batches of 8 so that
+// every batch's loads are in flight together.
+template <int KIND>
+__device__ __forceinline__ uint4 gather_pieces(const char *xb, uint32_t nbytes, uint32_t n,
+                                               uint32_t lane, bool active) {
+  typename EngAcc<KIND>::type acc;
+  for (uint32_t k0 = 0; k0 < n; k0 += 8) {
+    uint4 x[8];
+    const uint32_t kn = n - k0 < 8 ? n - k0 : 8;
+#pragma unroll
+    for (uint32_t k = 0; k < 8; ++k)
+      if (k < kn && active) x[k] = ld_relaxed_v4(xb + (size_t)(k0 + k) * nbytes + lane * 16);
+    if (active) {
+#pragma unroll
+      for (uint32_t k = 0; k < 8; ++k)
+        if (k < kn) {
+          if (k0 + k == 0) acc.init(x[k]); else acc.add(x[k]);
+        }
+    }
+  }
+  return active ? acc.pack() : make_uint4(0, 0, 0, 0);
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
+  const uint32_t gw = blockIdx.x;
+  if (gw >= a.nwarps) return;
+  const uint32_t lane = threadIdx.x;
+  const coll_warp_t W = a.warps[gw];
+  coll_dev_status_t *st = a.st;
+  const bool spec_proto = a.protocol == COLL_PROTO_SPEC;
+  const bool tagged = spec_proto && a.spec_check == COLL_SPEC_TAGGED;
+  const bool skip_notify =
+      (a.inject_flags & COLL_INJECT_SKIP_NOTIFY) && (int)W.rank == a.inject_rank;
+  const bool pause_consumer =
+      (a.inject_flags & COLL_INJECT_SPEC_PAUSE) && (int)W.rank == a.inject_rank;
+  const bool delay_producer = (a.inject_flags & COLL_INJECT_SPEC_PAUSE) &&
+                              (int)W.rank == (a.inject_rank + 1) % a.R;
+  uint32_t n_checks = 0, n_retries = 0;
+  bool failed = false;
+
+  if ((a.inject_flags & COLL_INJECT_STAGGER) && a.inject_start_ns)
+    spin_ns((uint64_t)W.rank * a.inject_start_ns);
+  if (gw == 0 && lane == 0 && a.stamps) a.stamps[0] = globaltimer();
+
+  for (int i = 0; i < a.n_epochs && !failed; ++i) {
+    const uint32_t E = a.epoch_base + (uint32_t)i + 1u;
+    const uint32_t b = (a.protocol == COLL_PROTO_BARRIER) ? 0u : (E & 1u);
+    const int64_t in_off = (int64_t)(i % a.in_pool) * a.in_stride;
+    const int64_t out_off = (int64_t)i * a.out_stride;
+
+    if ((a.inject_flags & COLL_INJECT_STAGGER) && a.inject_prob_ppm) {
+      const uint64_t h = splitmix64(a.inject_seed ^ ((uint64_t)E * 0xD1B54A32D192ED03ull));
+      if ((h % 1000000ull) < a.inject_prob_ppm && W.rank == (uint32_t)((h >> 40) % (uint64_t)a.R))
+        spin_ns(splitmix64(h) % (a.inject_max_ns + 1));
+    }
+
+    // ---------------- Stage + Notify
+    for (uint32_t s = W.s0; s < W.s1; ++s) {
+      const coll_item_t it = a.sitems[s];
+      const coll_unit_t u = a.units[it.unit];
+      if (a.protocol == COLL_PROTO_BARRIER || (u.flags & COLL_UNIT_REUSE_WAIT)) {
+        // bottom barrier (single buffer) / explicit reuse wait (dual buffers)
+        const uint32_t target = E - (a.protocol == COLL_PROTO_BARRIER ? 1u : 2u);
+        if (!wait_consumers_done(a.cflag + u.cflag0, u.ncflag, target, st, a.spin_ns)) {
+          if (lane == 0) record_timeout(st, (int)W.rank, (int)it.unit, 1, E);
+          failed = true;
+          break;
+        }
+      }
+      if (delay_producer && a.dbg) {
+        // adversarial interleaving: stage only after the paused consumer has loaded
+        if (lane == 0) {
+          const uint64_t t0 = globaltimer();
+          while ((int32_t)(ld_acquire_u32(a.dbg + it.unit) - E) < 0 &&
+                 globaltimer() - t0 < a.inject_max_ns) {
+          }
+        }
+        __syncwarp();
+      }
+      const coll_ref_t r = a.refs[u.src0 + it.slot];
+      const char *src = a.ptr.in[r.rank] + r.off + in_off + u.start;
+      char *dst = a.xbuf + (size_t)b * a.xpar + u.xoff + (size_t)it.slot * u.nbytes;
+      const uint32_t nvec = u.nbytes >> 4;
+      uint32_t h = 0;
+      if (lane < nvec) {
+        const uint4 x = ld_nc_v4(src + lane * 16);
+        st_v4(dst + lane * 16, x);
+        if (tagged) h = tag_part(x, lane);
+      }
+      uint32_t tag = 0;
+      if (tagged) tag = tag_fold(__reduce_add_sync(FULL, h), E);
+      __syncwarp();
+      if (lane == 0 && !skip_notify)
+        st_release_u64(a.pflag + (size_t)b * a.n_pflag + u.pflag0 + it.slot,
+                       ((unsigned long long)E << 32) | tag);
+    }
+    if (failed) break;
+
+    // ---------------- Consume
+    for (uint32_t c = W.c0; c < W.c1; ++c) {
+      const coll_item_t it = a.citems[c];
+      const coll_unit_t u = a.units[it.unit];
+      const uint32_t n = u.nsrc;
+      const uint32_t nvec = u.nbytes >> 4;
+      const bool active = lane < nvec;
+      const char *xb = a.xbuf + (size_t)b * a.xpar + u.xoff;
+      const unsigned long long *pf = a.pflag + (size_t)b * a.n_pflag + u.pflag0;
+      uint4 res = make_uint4(0, 0, 0, 0);
+      bool have = false;
+      bool retried = false;
+      if (spec_proto && n <= 32) {
+        // Speculative consume: load and reduce without waiting, then validate.
+        typename EngAcc<KIND>::type acc;
+        uint32_t myh = 0;
+        unsigned long long f = 0;
+        for (uint32_t k0 = 0; k0 < n; k0 += 8) {
+          uint4 x[8];
+          const uint32_t kn = n - k0 < 8 ? n - k0 : 8;
+#pragma unroll
+          for (uint32_t k = 0; k < 8; ++k)
+            if (k < kn && active) x[k] = ld_relaxed_v4(xb + (size_t)(k0 + k) * u.nbytes + lane * 16);
+          if (k0 == 0 && !pause_consumer && lane < n) f = ld_acquire_u64(pf + lane);
+#pragma unroll
+          for (uint32_t k = 0; k < 8; ++k) {
+            if (k < kn) {
+              if (active) {
+                if (k0 + k == 0) acc.init(x[k]); else acc.add(x[k]);
+              }
+              if (tagged) {
+                const uint32_t hs = __reduce_add_sync(FULL, active ? tag_part(x[k], lane) : 0u);
+                if (lane == k0 + k) myh = hs;
+              }
+            }
+          }
+        }
+        if (pause_consumer) {
+          __syncwarp();
+          if (lane == 0 && a.dbg) st_release_u32(a.dbg + it.unit, E);
+          spin_ns(a.inject_pause_ns);
+          if (lane < n) f = ld_acquire_u64(pf + lane);
+        }
+        const uint32_t fe = (uint32_t)(f >> 32);
+        bool ok;
+        if (tagged) {
+          const bool lane_ok = lane >= n || (fe == E && (uint32_t)f == tag_fold(myh, E));
+          ok = __all_sync(FULL, lane_ok);
+        } else {
+          const uint32_t sum = __reduce_add_sync(FULL, lane < n ? fe : 0u);
+          ok = sum == n * E;
+        }
+        ++n_checks;
+        if (ok) {
+          res = acc.pack();
+          have = true;
+        } else {
+          ++n_retries;
+          retried = true;
+        }
+      }
+      if (!have) {
+        // Top barrier: wait until every producer of the unit has notified epoch E,
+        // then (re)load with L1-bypassing loads.
+        if (!wait_producers(pf, n, E, st, a.spin_ns)) {
+          if (lane == 0) record_timeout(st, (int)W.rank, (int)it.unit, retried ? 3 : 2, E);
+          failed = true;
+          break;
+        }
+        res = gather_pieces<KIND>(xb, u.nbytes, n, lane, active);
+      }
+      if (active) {
+        if (it.slot == COLL_SLOT_ALL) {
+          for (uint32_t d = 0; d < u.ndst; ++d) {
+            const coll_ref_t r = a.refs[u.dst0 + d];
+            st_v4(a.ptr.out[r.rank] + r.off + out_off + u.start + lane * 16, res);
+          }
+        } else {
+          const coll_ref_t r = a.refs[u.dst0 + it.slot];
+          st_v4(a.ptr.out[r.rank] + r.off + out_off + u.start + lane * 16, res);
+        }
+      }
+      if (a.protocol == COLL_PROTO_BARRIER || (u.flags & COLL_UNIT_DONE_FLAGS)) {
+        __syncwarp();
+        if (lane == 0)
+          st_release_u32(a.cflag + u.cflag0 + (it.slot == COLL_SLOT_ALL ? 0u : it.slot), E);
+      }
+    }
+    if (gw == 0 && lane == 0 && a.stamps && (uint32_t)i < a.stamp_cap)
+      a.stamps[i + 1] = globaltimer();
+  }
+  if (lane == 0) {
+    if (n_checks) atomicAdd(&st->spec_checks, (unsigned long long)n_checks);
+    if (n_retries) atomicAdd(&st->spec_retries, (unsigned long long)n_retries);
+  }
+}
+
+int kind_of(int op, int dtype) {
+  if (op == COLL_OP_COPY) return 0;
+  return dtype == COLL_BF16 ? 1 : 2;
+}
+
+}  // namespace
+
+cudaError_t launch_zero_copy(int op, int dtype, int keep, const ZcArgs &a, int ctas,
+                             cudaStream_t s) {
+  const int kind = kind_of(op, dtype);
+  const uint64_t total = (uint64_t)a.ntiles * a.n_epochs;
+  if (total == 0) return cudaSuccess;
+  const int grid = (int)((uint64_t)ctas < total ? (uint64_t)ctas : total);
+  const dim3 block(512);
+  switch (kind * 2 + (keep ? 1 : 0)) {
+    case 0: zc_kernel<0, false><<<grid, block, 0, s>>>(a); break;
+    case 1: zc_kernel<0, true><<<grid, block, 0, s>>>(a); break;
+    case 2: zc_kernel<1, false><<<grid, block, 0, s>>>(a); break;
+    case 3: zc_kernel<1, true><<<grid, block, 0, s>>>(a); break;
+    case 4: zc_kernel<2, false><<<grid, block, 0, s>>>(a); break;
+    default: zc_kernel<2, true><<<grid, block, 0, s>>>(a); break;
+  }
+  return cudaGetLastError();
+}
+
+static const void *engine_fn(int kind) {
+  switch (kind) {
+    case 0: return (const void *)engine_kernel<0>;
+    case 1: return (const void *)engine_kernel<1>;
+    default: return (const void *)engine_kernel<2>;
+  }
+}
+
+cudaError_t engine_max_coresident(int op, int dtype, int *max_ctas) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, engine_fn(kind_of(op, dtype)), 32, 0);
+  if (e != cudaSuccess) return e;
+  *max_ctas = per_sm * sms;
+  return cudaSuccess;
+}
+
+cudaError_t launch_engine(int op, int dtype, const EngArgs &a, cudaStream_t s) {
+  if (a.nwarps == 0 || a.n_epochs == 0) return cudaSuccess;
+  void *args[] = {(void *)&a};
+  return cudaLaunchCooperativeKernel(engine_fn(kind_of(op, dtype)), dim3(a.nwarps), dim3(32),
+                                     args, 0, s);
+}
+
+}  // namespace coll

@@ -1,0 +1,72 @@
+// Launch interface between the host API (api.cu) and the kernels (engine.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "coll_internal.h"
+
+namespace coll {
+
+struct RankPtrs {
+  const char *in[COLL_MAX_RANKS];
+  char *out[COLL_MAX_RANKS];
+};
+
+struct ZcArgs {
+  RankPtrs ptr;
+  const coll_job_t *jobs;
+  const coll_ref_t *refs;
+  const coll_tile_t *tiles;
+  uint32_t ntiles;
+  uint32_t n_epochs;
+  int32_t in_pool;
+  int32_t pad;
+  int64_t in_stride, out_stride;
+};
+
+struct EngArgs {
+  RankPtrs ptr;
+  const coll_unit_t *units;
+  const coll_item_t *sitems;
+  const coll_item_t *citems;
+  const coll_warp_t *warps;
+  const coll_ref_t *refs;
+  char *xbuf;
+  uint64_t xpar;
+  unsigned long long *pflag;  // [2][n_pflag]
+  uint32_t *cflag;            // [n_cflag]
+  coll_dev_status_t *st;
+  uint64_t *stamps;           // [stamp_cap + 1] or null
+  uint32_t *dbg;              // [n_units] handshake words of the SPEC_PAUSE injection
+  uint32_t stamp_cap;
+  uint32_t n_pflag;
+  uint32_t nwarps;
+  int32_t n_epochs;
+  int32_t in_pool;
+  uint32_t epoch_base;  // epochs already run by this plan; epoch i of this run is base+i+1
+  int64_t in_stride, out_stride;
+  int32_t protocol;
+  int32_t spec_check;
+  uint64_t spin_ns;
+  uint64_t inject_flags;
+  uint64_t inject_seed;
+  int32_t inject_rank;
+  uint32_t inject_prob_ppm;
+  uint64_t inject_max_ns;
+  uint64_t inject_start_ns;
+  uint64_t inject_pause_ns;
+  int32_t R;
+};
+
+// Zero-copy: one ordinary launch over all tiles of all epochs.
+cudaError_t launch_zero_copy(int op, int dtype, int oneshot_reuse, const ZcArgs &a, int ctas,
+                             cudaStream_t s);
+
+// Staged Stage/Notify/Consume engine: one cooperative launch of nwarps one-warp CTAs.
+cudaError_t launch_engine(int op, int dtype, const EngArgs &a, cudaStream_t s);
+
+// How many one-warp engine CTAs can be co-resident on the current device.
+cudaError_t engine_max_coresident(int op, int dtype, int *max_ctas);
+
+}  // namespace coll

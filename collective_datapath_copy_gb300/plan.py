@@ -1,0 +1,133 @@
+"""Python face of the C ABI: compile a naming into a plan and run it on torch buffers.
+
+PyTorch provides device memory and streams only; every step of a run (staging, flags,
+copy, reduce) happens inside libcoll.so's kernels.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+
+from . import _lib
+from ._lib import check, lib
+from .namings import Naming
+
+
+def _u64(vals) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(vals, dtype=np.uint64))
+
+
+def _ptr(a: np.ndarray):
+    return C.c_void_p(a.ctypes.data) if a.size else None
+
+
+def validate(naming: Naming, **cfg) -> _lib.PlanInfo:
+    """Host-side compile (no GPU needed). Raises CollError with the library's code."""
+    info = _lib.PlanInfo()
+    c = _lib.make_config(**cfg)
+    il, ol = _u64(naming.in_len), _u64(naming.out_len)
+    ins = np.ascontiguousarray(naming.in_segs)
+    outs = np.ascontiguousarray(naming.out_segs)
+    code = lib().coll_validate(naming.R, _lib.OP[naming.op], _lib.DTYPE[naming.dtype], _ptr(ins),
+                               len(ins), _ptr(il), _ptr(outs), len(outs), _ptr(ol), C.byref(c),
+                               C.byref(info))
+    check(code, "coll_validate")
+    return info
+
+
+def validate_code(R, op, dtype, in_len, in_segs, out_len, out_segs, **cfg) -> int:
+    """Return the library's validation code for raw arguments (for tests)."""
+    c = _lib.make_config(**cfg)
+    il, ol = _u64(in_len), _u64(out_len)
+    ins = np.ascontiguousarray(in_segs)
+    outs = np.ascontiguousarray(out_segs)
+    return lib().coll_validate(R, op, dtype, _ptr(ins), len(ins), _ptr(il) if len(il) else None,
+                               _ptr(outs), len(outs), _ptr(ol) if len(ol) else None,
+                               C.byref(c), None)
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(int(stream.cuda_stream))
+
+
+def _dev_ptrs(tensors, R):
+    arr = (C.c_void_p * R)()
+    for r in range(R):
+        t = tensors[r] if tensors is not None and r < len(tensors) else None
+        arr[r] = None if t is None else t.data_ptr()
+    return arr
+
+
+class Plan:
+    """A compiled collective. Config keywords mirror coll_config_t (protocol='spec'|'dual'|
+    'barrier', datapath='oneshot'|'twoshot', zero_copy, spec_check='tagged'|'literal', ...)."""
+
+    def __init__(self, naming: Naming, **cfg):
+        self.naming = naming
+        self.cfg = dict(cfg)
+        c = _lib.make_config(**cfg)
+        il, ol = _u64(naming.in_len), _u64(naming.out_len)
+        ins = np.ascontiguousarray(naming.in_segs)
+        outs = np.ascontiguousarray(naming.out_segs)
+        h = C.c_void_p()
+        code = lib().coll_plan(C.byref(h), naming.R, _lib.OP[naming.op], _lib.DTYPE[naming.dtype],
+                               _ptr(ins), len(ins), _ptr(il), _ptr(outs), len(outs), _ptr(ol),
+                               C.byref(c))
+        check(code, "coll_plan")
+        self._h = h
+        self.info = _lib.PlanInfo()
+        check(lib().coll_plan_info(self._h, C.byref(self.info)), "coll_plan_info")
+
+    def run(self, ins, outs, n_epochs=1, in_epoch_stride=0, in_pool=1, out_epoch_stride=0,
+            stream=None):
+        """Enqueue n_epochs epochs. ins/outs: per-rank torch CUDA tensors (or None for a
+        rank without segments). Strides are in bytes."""
+        R = self.naming.R
+        code = lib().coll_run(self._h, C.cast(_dev_ptrs(ins, R), C.c_void_p),
+                              C.cast(_dev_ptrs(outs, R), C.c_void_p), int(n_epochs),
+                              int(in_epoch_stride), int(in_pool), int(out_epoch_stride),
+                              _stream_handle(stream))
+        check(code, "coll_run")
+
+    def run_ptrs(self, in_ptrs, out_ptrs, n_epochs=1, in_epoch_stride=0, in_pool=1,
+                 out_epoch_stride=0, stream=None):
+        """Same as run() with raw device addresses (ints)."""
+        R = self.naming.R
+        ia = (C.c_void_p * R)(*[p or None for p in in_ptrs])
+        oa = (C.c_void_p * R)(*[p or None for p in out_ptrs])
+        return lib().coll_run(self._h, C.cast(ia, C.c_void_p), C.cast(oa, C.c_void_p),
+                              int(n_epochs), int(in_epoch_stride), int(in_pool),
+                              int(out_epoch_stride), _stream_handle(stream))
+
+    def status(self) -> dict:
+        st = _lib.Stats()
+        code = lib().coll_status(self._h, C.byref(st))
+        d = {f: getattr(st, f) for f, _ in _lib.Stats._fields_}
+        d["code"] = code
+        return d
+
+    def stamps(self, n: int) -> np.ndarray:
+        buf = np.zeros(n + 1, dtype=np.uint64)
+        m = lib().coll_stamps(self._h, C.c_void_p(buf.ctypes.data), n + 1)
+        if m < 0:
+            check(int(m), "coll_stamps")
+        return buf[:m]
+
+    def reset(self):
+        check(lib().coll_reset(self._h), "coll_reset")
+
+    def free(self):
+        if getattr(self, "_h", None):
+            lib().coll_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass

@@ -1,0 +1,207 @@
+/*
+ * coll.h — C ABI of the collective datapath (libcoll.so), GB300 / sm_103a.
+ *
+ * A collective is stated as a NAMING: each rank's input buffer and output buffer are cut
+ * into segments, every segment carries a name, and an operation (copy or sum) says what an
+ * output segment receives from the input segments that carry its name.
+ *   Source: Purlin article, "The Purlin PDF describes a three-layer design" (collectives
+ *   as a naming of an input and an output layout plus copy or reduction; a shared
+ *   Stage / Notify / And Consume orchestration; an Atom datapath with copy and reduce).
+ * The R ranks are emulated on one GPU: rank r is the buffer pair (in[r], out[r]) plus the
+ * group of warps that produces rank r's data and consumes rank r's outputs.
+ *
+ * Semantics of one epoch (independent of protocol, timing and retries):
+ *   copy: an output segment receives the bytes of the single input segment with its name.
+ *   sum : an output segment receives, per element, the binary32 chain
+ *         acc = x_0; acc = acc + x_k (k = 1..n-1, round to nearest even, no FMA), over the
+ *         input segments with its name ordered by (rank, offset) ascending; bf16 outputs
+ *         are rounded once from acc, to nearest even. Results are bit-exact.
+ *   Output elements that no segment names are not written.
+ *
+ * Threading: the library is thread-safe across plans; a plan allows one run in flight
+ * (a second coll_run on another stream before the first finished is undefined).
+ * All pointers passed to coll_run are device pointers of the current device.
+ */
+#ifndef COLL_H
+#define COLL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ codes */
+#define COLL_OK 0
+#define COLL_EINVAL (-1)    /* bad R (1..64), op, dtype, rank, count 0, config value   */
+#define COLL_ENAME (-2)     /* a consumed name has no producer, or copy with >1        */
+#define COLL_ELEN (-3)      /* segments with one name have different counts            */
+#define COLL_EBOUNDS (-4)   /* offset+count beyond the rank's buffer length            */
+#define COLL_EOVERLAP (-5)  /* output segments of one rank overlap; or (coll_run)
+                               output memory overlaps input or another output         */
+#define COLL_EALIGN (-6)    /* staged (non zero-copy) plans need 16-byte-aligned segment
+                               byte offsets/sizes; coll_run needs 16-byte-aligned bases */
+#define COLL_ECUDA (-7)     /* a CUDA runtime call failed (launch, memory)              */
+#define COLL_ETIMEDOUT (-8) /* async: a bounded device wait expired; kernel returned    */
+#define COLL_EDEVICE (-9)   /* async: the device reported an inconsistent state         */
+#define COLL_ENOMEM (-10)   /* host or device allocation failed                         */
+
+/* ------------------------------------------------------------------ enums */
+#define COLL_OP_COPY 0
+#define COLL_OP_SUM 1
+
+#define COLL_BF16 0  /* 2-byte elements; sum accumulates in binary32          */
+#define COLL_F32 1   /* 4-byte elements                                       */
+#define COLL_BYTES 2 /* 1-byte elements; copy only                            */
+
+/* Stage/Notify/Consume protocols for staged plans (zero_copy == 0).
+ * Source: SiFAR review, "What carries the argument" and abstract: oneshot with a top and a
+ * bottom barrier; dual buffering (epoch parity) removes the bottom barrier; speculative
+ * reduction starts the transfer before the top barrier and validates with a reduced flag,
+ * retrying on mismatch. */
+#define COLL_PROTO_BARRIER 0
+#define COLL_PROTO_DUAL 1
+#define COLL_PROTO_SPEC 2
+
+/* Datapaths for sum. Source: SiFAR review, Fig. 5 (oneshot: every consumer reduces the
+ * whole payload from every producer) and Fig. 6 (twoshot: each part is reduced once, by an
+ * owner, and then delivered to every consumer — here the owner writes it to all of them). */
+#define COLL_DP_ONESHOT 0
+#define COLL_DP_TWOSHOT 1
+
+/* Speculative validation rules (COLL_PROTO_SPEC). */
+#define COLL_SPEC_TAGGED 0  /* flag epochs AND a content tag per piece must match (sound) */
+#define COLL_SPEC_LITERAL 1 /* only sum of flag epochs == n * epoch (the pages' rule);
+                               unsound under reordering, kept as an ablation            */
+
+/* Host-driven fault / timing injection (never a GPU fault; every wait stays bounded). */
+#define COLL_INJECT_SKIP_NOTIFY (1ull << 0) /* rank inject_rank never notifies          */
+#define COLL_INJECT_STAGGER (1ull << 1)     /* random per-epoch rank delays + start skew */
+#define COLL_INJECT_SPEC_PAUSE (1ull << 2)  /* adversarial interleaving: consumers of
+                                               inject_rank load speculatively, signal,
+                                               pause inject_pause_ns, then read the flags;
+                                               rank inject_rank+1 stages each piece only
+                                               after that signal (waiting at most
+                                               inject_max_ns): payload read, then peer
+                                               write + flag, then flag read              */
+
+typedef struct coll_plan_s *coll_plan_t;
+
+/* One segment: elements [offset, offset+count) of rank `rank`'s buffer carry `name`. */
+typedef struct {
+  int32_t rank;
+  int32_t reserved; /* must be 0 */
+  uint64_t offset;  /* elements */
+  uint64_t count;   /* elements, > 0 */
+  uint64_t name;
+} coll_seg_t;
+
+typedef struct {
+  int32_t protocol;       /* COLL_PROTO_*; staged plans only                          */
+  int32_t datapath;       /* COLL_DP_*; sum only                                      */
+  int32_t zero_copy;      /* 1: consumers read the inputs directly, one kernel per
+                             coll_run, no exchange buffers or flags (the kernel launch
+                             is the barrier). 0: staged Stage/Notify/Consume engine.   */
+  int32_t spec_check;     /* COLL_SPEC_*                                              */
+  int32_t unit_bytes;     /* staged: bytes per synchronisation unit: 0 or 512         */
+  int32_t warps_per_rank; /* staged: warps per emulated rank; 0 = one per unit        */
+  int32_t ctas;           /* zero-copy: CTAs in the grid; 0 = 2 x SM count             */
+  int32_t tile_bytes;     /* zero-copy: bytes per tile per destination; 0 = 32768     */
+  uint64_t tma_min_bytes; /* zero-copy copy tiles with at least this many bytes use
+                             the TMA bulk path; 0 = never                               */
+  uint64_t spin_limit_ns; /* bound on every device wait; 0 = 2e9 (2 s)                  */
+  uint32_t record_stamps; /* staged: record a %globaltimer stamp per epoch (capacity
+                             stamp_capacity epochs; later epochs are not stamped)      */
+  uint32_t stamp_capacity;
+  uint64_t inject_flags;  /* COLL_INJECT_*                                            */
+  uint64_t inject_seed;
+  int32_t inject_rank;
+  uint32_t inject_prob_ppm; /* STAGGER: probability per epoch, parts per million      */
+  uint64_t inject_max_ns;   /* STAGGER: max delay; SPEC_PAUSE: producer's bounded wait */
+  uint64_t inject_start_ns; /* STAGGER: rank r starts r * inject_start_ns late          */
+  uint64_t inject_pause_ns; /* SPEC_PAUSE: consumer pause                              */
+} coll_config_t;
+
+typedef struct {
+  uint64_t n_names;      /* consumed names                                           */
+  uint64_t n_jobs;       /* zero-copy jobs (a job = sources -> destinations)          */
+  uint64_t n_tiles;      /* zero-copy tiles                                           */
+  uint64_t n_units;      /* staged synchronisation units                              */
+  uint64_t n_warps;      /* staged engine warps (= CTAs of 32 threads)                */
+  uint64_t min_bytes;    /* algorithmic bytes per epoch: every input byte a named output
+                            depends on read once + every named output byte written once */
+  uint64_t xbuf_bytes;   /* staged exchange buffers (both parities)                   */
+  uint64_t flag_bytes;   /* staged flag words                                         */
+} coll_plan_info_t;
+
+typedef struct {
+  int32_t status;        /* COLL_OK, COLL_ETIMEDOUT or COLL_EDEVICE of the last run    */
+  int32_t fail_rank;     /* timeout: rank of the warp that gave up (-1 if none)        */
+  int32_t fail_unit;     /* timeout: unit it waited on                                 */
+  int32_t fail_where;    /* 1 stage reuse wait, 2 consume wait, 3 retry wait, 4 output
+                            completion wait                                           */
+  uint64_t fail_epoch;   /* timeout: epoch number it waited for                        */
+  uint64_t epochs;       /* epochs completed by this plan, all runs                    */
+  uint64_t spec_checks;  /* speculative validations (units x epochs)                   */
+  uint64_t spec_retries; /* validations that failed and were redone after a wait       */
+} coll_stats_t;
+
+/* Fill *cfg with defaults (spec protocol, oneshot, staged, tagged validation). */
+int coll_config_default(coll_config_t *cfg);
+
+/* Validate a naming and compile it into a plan: host work tables, device tables,
+ * exchange buffers (x2 parities) and zeroed flags for staged plans.
+ * in_len/out_len: R buffer lengths in elements. cfg may be NULL (defaults).
+ * Ownership: the plan owns everything it allocates; coll_free releases it. The segment
+ * arrays are copied and may be freed after the call.
+ * Errors (synchronous, nothing allocated): COLL_EINVAL, COLL_EBOUNDS, COLL_ELEN,
+ * COLL_ENAME, COLL_EOVERLAP (in that order of precedence), COLL_EALIGN, COLL_ENOMEM,
+ * COLL_ECUDA. */
+int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_seg_t *in_segs,
+              size_t n_in, const uint64_t *in_len, const coll_seg_t *out_segs, size_t n_out,
+              const uint64_t *out_len, const coll_config_t *cfg);
+
+/* The host half of coll_plan only: same checks and codes, no device call (usable on a
+ * machine without a GPU). info may be NULL. */
+int coll_validate(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_in,
+                  const uint64_t *in_len, const coll_seg_t *out_segs, size_t n_out,
+                  const uint64_t *out_len, const coll_config_t *cfg,
+                  coll_plan_info_t *info);
+
+int coll_plan_info(coll_plan_t p, coll_plan_info_t *info);
+
+/* Run n_epochs epochs of the plan on `stream` (a cudaStream_t; NULL = legacy default).
+ * in/out: host arrays of R device pointers. Epoch i (0-based) reads
+ * in[r] + (i % in_pool) * in_epoch_stride bytes and writes out[r] + i * out_epoch_stride
+ * bytes (stride 0 overwrites). A rank with no segments may pass NULL.
+ * Staged plans run one cooperative persistent launch for all epochs; zero-copy plans run
+ * one ordinary launch. Returns after enqueueing; device-side failures are reported by
+ * coll_status. Synchronous errors: COLL_EINVAL (n_epochs < 1, in_pool < 1, NULL pointer
+ * for a rank that has segments), COLL_EALIGN, COLL_EOVERLAP, COLL_ECUDA. Buffers must stay
+ * live and unmodified until the stream has passed the run. */
+int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_epochs,
+             int64_t in_epoch_stride, int in_pool, int64_t out_epoch_stride, void *stream);
+
+/* Wait for the plan's last run and report its status and counters. Returns the run's
+ * status (COLL_OK, COLL_ETIMEDOUT, COLL_EDEVICE) or COLL_ECUDA. st may be NULL. */
+int coll_status(coll_plan_t p, coll_stats_t *st);
+
+/* Copy up to n per-epoch %globaltimer stamps (ns) of the last run into host memory;
+ * returns the number copied (synchronises on the last run). */
+int64_t coll_stamps(coll_plan_t p, uint64_t *host, int64_t n);
+
+/* Wait for the last run, then re-zero flags, counters and the epoch counter. */
+int coll_reset(coll_plan_t p);
+
+/* Wait for the last run and release everything the plan owns. NULL is a no-op. */
+int coll_free(coll_plan_t p);
+
+/* Static string for a code. */
+const char *coll_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* COLL_H */

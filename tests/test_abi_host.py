@@ -1,0 +1,181 @@
+"""CPU tests of the C ABI's host half: symbols, validation codes, plan shapes, namings.
+
+No compute call is made (no GPU here); coll_validate runs the whole host compiler.
+"""
+
+import re
+
+import numpy as np
+import pytest
+
+import collective_datapath_copy_gb300 as cdc
+from collective_datapath_copy_gb300 import _lib, namings
+from collective_datapath_copy_gb300.build import build
+import oracle
+from oracle import collectives, naming as onaming
+from oracle.arith import NPTYPE
+import synth
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build()
+
+
+def test_library_exports_every_declared_symbol():
+    with open(_lib.HEADER) as f:
+        text = f.read()
+    declared = set(re.findall(r"^\s*(?:int|int64_t|const char \*)\s*(coll_\w+)\s*\(", text, re.M))
+    assert {"coll_plan", "coll_run", "coll_free", "coll_status", "coll_strerror",
+            "coll_validate", "coll_reset", "coll_stamps", "coll_plan_info",
+            "coll_config_default"} <= declared
+    h = _lib.lib()
+    for name in declared:
+        assert hasattr(h, name), name
+
+
+def test_strerror_covers_codes():
+    for name, code in _lib.D.items():
+        if name.startswith("COLL_E"):
+            assert _lib.lib().coll_strerror(code).decode() != "unknown error"
+
+
+def _code(R, op, dtype, il, i, ol, o, **cfg):
+    return cdc.validate_code(R, _lib.OP.get(op, 7), _lib.DTYPE.get(dtype, 9), il, namings.segs(i),
+                             ol, namings.segs(o), **cfg)
+
+
+MALFORMED = [
+    # (R, op, dtype, in_len, in_segs, out_len, out_segs)
+    (2, "sum", "bf16", (4, 4), [(0, 0, 4, 7), (1, 0, 4, 7)], (4, 4), [(0, 0, 4, 7), (1, 0, 4, 7)]),
+    (2, "max", "bf16", (4, 4), [(0, 0, 4, 7)], (4, 4), [(0, 0, 4, 7)]),
+    (2, "sum", "bytes", (4, 4), [(0, 0, 4, 7)], (4, 4), [(0, 0, 4, 7)]),
+    (2, "sum", "bf16", (4, 4), [(2, 0, 4, 7)], (4, 4), [(0, 0, 4, 7)]),
+    (2, "sum", "bf16", (4, 4), [(0, 0, 0, 7)], (4, 4), []),
+    (2, "sum", "bf16", (4, 4), [(0, 1, 4, 7)], (4, 4), [(0, 0, 4, 7)]),
+    (2, "sum", "bf16", (4, 4), [(0, 0, 4, 7)], (4, 4), [(1, 2, 4, 7)]),
+    (2, "sum", "bf16", (4, 4), [(0, 0, 4, 7), (1, 0, 3, 7)], (4, 4), [(0, 0, 4, 7)]),
+    (2, "sum", "bf16", (4, 4), [(0, 0, 4, 7)], (4, 4), [(0, 0, 4, 8)]),
+    (2, "copy", "bf16", (4, 4), [(0, 0, 4, 7), (1, 0, 4, 7)], (4, 4), [(0, 0, 4, 7)]),
+    (2, "copy", "bf16", (4, 4), [(0, 0, 4, 7)], (8, 4), [(0, 0, 4, 7), (0, 3, 4, 7)]),
+    (2, "copy", "bf16", (4, 4), [(0, 0, 4, 7)], (8, 4), [(0, 0, 4, 7), (0, 4, 4, 7)]),
+    (2, "sum", "bf16", (4, 4), [(0, 0, 4, 7), (1, 0, 4, 7), (0, 0, 2, 9)], (4, 4), [(1, 0, 4, 7)]),
+    (2, "sum", "f32", (4, 4), [], (4, 4), []),
+    (1, "copy", "bytes", (5,), [(0, 0, 5, 1)], (5,), [(0, 0, 5, 1)]),
+]
+
+
+@pytest.mark.parametrize("case", MALFORMED)
+def test_validation_codes_match_oracle(case):
+    R, op, dt, il, i, ol, o = case
+    want = onaming.validate(R, op, dt, list(il), i, list(ol), o)
+    assert _code(R, op, dt, list(il), i, list(ol), o, zero_copy=1) == want
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_naming_codes_match_oracle(seed):
+    rng = synth.seeded_rng(500 + seed)
+    op = "copy" if seed % 2 else "sum"
+    il, i, ol, o = synth.random_naming(rng, 1 + seed % 4, 10, 4, 3, op)
+    # perturb: a random defect in about half the cases
+    i, o = list(i), list(o)
+    kind = seed % 6
+    if kind == 1 and o:
+        r, off, c, n = o[0]
+        o[0] = (r, off + 100, c, n)
+    elif kind == 2 and i:
+        r, off, c, n = i[0]
+        i[0] = (r, off, c + 1, n)
+    elif kind == 3 and o:
+        o.append((o[0][0], o[0][1], o[0][2], o[0][3]))
+    elif kind == 4 and o:
+        o.append((0, 0, 1, 999))
+    R = 1 + seed % 4
+    want = onaming.validate(R, op, "bf16", il, i, ol, o)
+    assert _code(R, op, "bf16", il, i, ol, o, zero_copy=1) == want
+
+
+def test_staged_plans_need_16_byte_alignment():
+    E = _lib.D
+    ok = _code(2, "sum", "bf16", [16, 16], [(0, 0, 8, 0), (1, 0, 8, 0)], [16, 16],
+               [(0, 8, 8, 0), (1, 0, 8, 0)])
+    assert ok == 0
+    bad = _code(2, "sum", "bf16", [16, 16], [(0, 1, 8, 0), (1, 0, 8, 0)], [16, 16],
+                [(0, 8, 8, 0), (1, 0, 8, 0)])
+    assert bad == E["COLL_EALIGN"]
+    # zero-copy plans accept any alignment
+    assert _code(2, "sum", "bf16", [16, 16], [(0, 1, 8, 0), (1, 0, 8, 0)], [16, 16],
+                 [(0, 8, 8, 0), (1, 0, 8, 0)], zero_copy=1) == 0
+
+
+def test_bad_config_rejected():
+    n = namings.allreduce(2, 256)
+    with pytest.raises(cdc.CollError):
+        cdc.validate(n, protocol=7)
+    with pytest.raises(cdc.CollError):
+        cdc.validate(n, unit_bytes=100)
+
+
+M = 1 << 20
+
+
+@pytest.mark.parametrize("kind,min_bytes", [
+    ("allreduce", lambda R, M: 2 * R * M),
+    ("reduce_scatter", lambda R, M: (R + 1) * M),
+    ("allgather", lambda R, M: (R + R * R) * M),
+    ("broadcast", lambda R, M: (1 + R) * M),
+    ("alltoall", lambda R, M: 2 * R * M),
+])
+def test_min_bytes_match_the_closed_forms(kind, min_bytes):
+    R = 8
+    n = M // 2
+    nm = getattr(namings, kind)(R, n, "bf16")
+    info = cdc.validate(nm, zero_copy=1)
+    assert info.min_bytes == min_bytes(R, M)
+
+
+def test_staged_allreduce_shape_for_decode_payload():
+    # 8 ranks x 4096 bf16: 16 units of 512 B, one warp per (rank, unit); dual buffers
+    nm = namings.allreduce(8, 4096, "bf16")
+    info = cdc.validate(nm, protocol="spec")
+    assert info.n_units == 16 and info.n_warps == 128
+    assert info.xbuf_bytes == 2 * 8 * 8192
+    info_b = cdc.validate(nm, protocol="barrier")
+    assert info_b.xbuf_bytes == 8 * 8192
+
+
+def _oracle_on(nm: namings.Naming, ins):
+    outs = [np.zeros(n, dtype=NPTYPE[nm.dtype]) for n in nm.out_len]
+    code = onaming.run_naming(nm.R, nm.op, nm.dtype, nm.in_len, nm.rows("in"), nm.out_len,
+                              nm.rows("out"), ins, outs)
+    assert code == 0
+    return outs
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 8])
+def test_naming_builders_agree_with_direct_definitions(R):
+    n = 4 * R * 3
+    rng = synth.seeded_rng(40 + R)
+    xs = [synth.normal_bf16(rng, n) for _ in range(R)]
+    eq = lambda a, b: all(np.array_equal(x, y) for x, y in zip(a, b))
+    assert eq(_oracle_on(namings.allreduce(R, n), xs), collectives.allreduce(xs, "bf16"))
+    assert eq(_oracle_on(namings.reduce_scatter(R, n), xs), collectives.reduce_scatter(xs, "bf16"))
+    assert eq(_oracle_on(namings.allgather(R, n), xs), collectives.allgather(xs))
+    assert eq(_oracle_on(namings.broadcast(R, n, root=R - 1), xs), collectives.broadcast(xs, R - 1))
+    assert eq(_oracle_on(namings.alltoall(R, n), xs), collectives.alltoall(xs))
+
+
+def test_moe_naming_agrees_with_direct_dispatch():
+    R, T, H, E, k = 4, 32, 8, 64, 8
+    routing = synth.zipf_topk_routing(3, R, T, E, k, 1.1)
+    rng = synth.seeded_rng(3)
+    xs2 = [synth.normal_bf16(rng, (T, H)) for _ in range(R)]
+    nm = namings.moe_dispatch(routing, E // R, H)
+    outs = _oracle_on(nm, [x.ravel() for x in xs2])
+    want, counts = collectives.moe_dispatch(xs2, routing, E // R)
+    assert nm.meta["counts"] == counts
+    for d in range(R):
+        assert np.array_equal(outs[d][:counts[d] * H], want[d].ravel())
+    info = cdc.validate(nm, zero_copy=1)
+    assert info.min_bytes == sum(2 * H * (1 + int(c)) for c in
+                                 collectives.moe_dest_ranks(routing, E // R).sum(-1).ravel())

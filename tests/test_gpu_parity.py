@@ -1,0 +1,423 @@
+"""GPU parity: every datapath and protocol of libcoll.so against the CPU oracle.
+
+Copies and fixed-order sums must be bit-exact. Inputs are the seeded synthetic workloads
+(uniform[-1,1] / N(0,1) bf16 or fp32 values, Zipf routing tables) at sizes the oracle
+finishes in seconds, plus full-size cases checked in full or on samples.
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+import collective_datapath_copy_gb300 as cdc  # noqa: E402
+from collective_datapath_copy_gb300 import namings  # noqa: E402
+from collective_datapath_copy_gb300.build import build  # noqa: E402
+from oracle import collectives, naming as onaming  # noqa: E402
+from oracle.arith import NPTYPE  # noqa: E402
+import synth  # noqa: E402
+
+from gpu_util import bits_equal, empty_dev, from_dev, to_dev  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build()
+    torch.cuda.init()
+    yield
+    torch.cuda.synchronize()
+
+
+def gen(dist, rng, n, dtype):
+    if dtype == "bytes":
+        return synth.random_bytes(rng, n)
+    if dtype == "f32":
+        return synth.uniform_f32(rng, n) if dist == "uniform" else synth.normal_f32(rng, n)
+    return synth.uniform_bf16(rng, n) if dist == "uniform" else synth.normal_bf16(rng, n)
+
+
+def oracle_outputs(nm, ins, init=None):
+    outs = [np.zeros(n, dtype=NPTYPE[nm.dtype]) if init is None else init[r].copy()
+            for r, n in enumerate(nm.out_len)]
+    assert onaming.run_naming(nm.R, nm.op, nm.dtype, nm.in_len, nm.rows("in"), nm.out_len,
+                              nm.rows("out"), ins, outs) == 0
+    return outs
+
+
+def run_once(nm, ins_np, **cfg):
+    """One epoch through the C ABI; returns (per-rank outputs, canary-initialised copy)."""
+    plan = cdc.Plan(nm, **cfg)
+    ins = [to_dev(x, nm.dtype) for x in ins_np]
+    outs = [empty_dev(n, nm.dtype) for n in nm.out_len]
+    init = [from_dev(o, nm.dtype).copy() for o in outs]
+    plan.run(ins, outs)
+    st = plan.status()
+    assert st["code"] == 0, st
+    res = [from_dev(o, nm.dtype) for o in outs]
+    plan.free()
+    return res, init
+
+
+DATAPATHS = [
+    dict(zero_copy=1, datapath="oneshot"),
+    dict(zero_copy=1, datapath="twoshot"),
+    dict(protocol="barrier"),
+    dict(protocol="dual"),
+    dict(protocol="spec"),
+    dict(protocol="spec", datapath="twoshot"),
+    dict(protocol="barrier", datapath="twoshot"),
+]
+
+
+# ------------------------------------------------------------ small all-reduce (R=2, f32)
+
+@pytest.mark.parametrize("cfg", DATAPATHS, ids=lambda c: "-".join(f"{k}={v}" for k, v in c.items()))
+def test_allreduce_r2_f32_1024(cfg):
+    rng = synth.seeded_rng(1)
+    xs = [synth.uniform_f32(rng, 1024) for _ in range(2)]
+    nm = namings.allreduce(2, 1024, "f32")
+    got, _ = run_once(nm, xs, **cfg)
+    want = collectives.allreduce(xs, "f32")
+    for g, w in zip(got, want):
+        assert bits_equal(g, w)
+
+
+# ------------------------------------------------------------ collectives, several sizes
+
+SIZES_B = [1024, 4096, 65536, 1 << 20]
+
+
+@pytest.mark.parametrize("msg_bytes", SIZES_B)
+@pytest.mark.parametrize("kind", ["allreduce", "reduce_scatter", "allgather", "broadcast", "alltoall"])
+@pytest.mark.parametrize("mode", ["zc-oneshot", "zc-twoshot", "staged-spec"])
+def test_collective_sweep_r8_bf16(kind, msg_bytes, mode):
+    R = 8
+    n = msg_bytes // 2
+    rng = synth.seeded_rng(3)
+    xs = [synth.uniform_bf16(rng, n) for _ in range(R)]
+    nm = getattr(namings, kind)(R, n, "bf16")
+    cfg = {"zc-oneshot": dict(zero_copy=1, datapath="oneshot"),
+           "zc-twoshot": dict(zero_copy=1, datapath="twoshot"),
+           "staged-spec": dict(protocol="spec")}[mode]
+    got, _ = run_once(nm, xs, **cfg)
+    if kind == "allreduce":
+        want = collectives.allreduce(xs, "bf16")
+    elif kind == "reduce_scatter":
+        want = collectives.reduce_scatter(xs, "bf16")
+    elif kind == "allgather":
+        want = collectives.allgather(xs)
+    elif kind == "broadcast":
+        want = collectives.broadcast(xs, 0)
+    else:
+        want = collectives.alltoall(xs)
+    for g, w in zip(got, want):
+        assert bits_equal(g, w)
+
+
+# ------------------------------------------------------------ random namings, edge cases
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_namings_zero_copy(seed):
+    op = "copy" if seed % 3 == 0 else "sum"
+    dtype = ["bf16", "f32", "bytes"][seed % 3] if op == "copy" else ["bf16", "f32"][seed % 2]
+    R = 1 + seed % 5
+    rng = synth.seeded_rng(900 + seed)
+    il, i, ol, o = synth.random_naming(rng, R, 3000, 5, 4, op)
+    nm = namings.Naming(R, op, dtype, il, namings.segs(i), ol, namings.segs(o))
+    xs = [gen("normal", rng, n, dtype) for n in il]
+    got, init = run_once(nm, xs, zero_copy=1, datapath="twoshot" if seed % 2 else "oneshot")
+    want = oracle_outputs(nm, xs, init)  # unnamed elements keep the canary
+    for g, w in zip(got, want):
+        assert bits_equal(g, w)
+
+
+@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("protocol", ["barrier", "dual", "spec"])
+def test_random_namings_staged(seed, protocol):
+    # staged plans need 16-byte-aligned segments: scale a random naming by 8 elements
+    op = "copy" if seed % 3 == 0 else "sum"
+    dtype = "bf16"
+    R = 1 + seed % 6
+    rng = synth.seeded_rng(1200 + seed)
+    il, i, ol, o = synth.random_naming(rng, R, 200, 4, 4, op)
+    k = 8
+    il = [x * k for x in il]
+    ol = [x * k for x in ol]
+    i = [(r, off * k, c * k, nmv) for (r, off, c, nmv) in i]
+    o = [(r, off * k, c * k, nmv) for (r, off, c, nmv) in o]
+    nm = namings.Naming(R, op, dtype, il, namings.segs(i), ol, namings.segs(o))
+    xs = [gen("normal", rng, n, dtype) for n in il]
+    got, init = run_once(nm, xs, protocol=protocol, datapath="twoshot" if seed % 2 else "oneshot")
+    want = oracle_outputs(nm, xs, init)
+    for g, w in zip(got, want):
+        assert bits_equal(g, w)
+
+
+def test_many_producers_and_ragged_tail():
+    # 17 producers (more than one batch of 8 loads), n not a multiple of any tile
+    R, n = 17, 12345
+    rng = synth.seeded_rng(77)
+    xs = [synth.normal_f32(rng, n) * np.float32(2.0) ** rng.integers(-10, 10, n).astype(np.float32)
+          for _ in range(R)]
+    nm = namings.allreduce(R, n, "f32")
+    for cfg in (dict(zero_copy=1), dict(zero_copy=1, datapath="twoshot", tile_bytes=4096)):
+        got, _ = run_once(nm, xs, **cfg)
+        want = collectives.allreduce(xs, "f32")
+        for g, w in zip(got, want):
+            assert bits_equal(g, w)
+
+
+def test_misaligned_zero_copy_segments_use_the_elementwise_path():
+    R, n = 3, 1001
+    rng = synth.seeded_rng(78)
+    xs = [synth.normal_bf16(rng, n) for _ in range(R)]
+    i = [(r, 1 + r, 997, 5) for r in range(R)]
+    o = [(r, 3, 997, 5) for r in range(R)]
+    nm = namings.Naming(R, "sum", "bf16", [n] * R, namings.segs(i), [n] * R, namings.segs(o))
+    got, init = run_once(nm, xs, zero_copy=1)
+    want = oracle_outputs(nm, xs, init)
+    for g, w in zip(got, want):
+        assert bits_equal(g, w)
+
+
+def test_empty_naming_and_single_rank():
+    nm = namings.Naming(2, "sum", "bf16", [16, 16], namings.segs([]), [16, 16], namings.segs([]))
+    for cfg in (dict(zero_copy=1), dict(protocol="spec")):
+        got, init = run_once(nm, [np.zeros(16, np.uint16)] * 2, **cfg)
+        for g, w in zip(got, init):
+            assert bits_equal(g, w)
+    rng = synth.seeded_rng(79)
+    x = synth.random_bytes(rng, 4096)
+    got, _ = run_once(namings.broadcast(1, 4096, "bytes"), [x], zero_copy=1)
+    assert bits_equal(got[0], x)
+
+
+def test_special_values_sum():
+    # signed zeros, subnormals, overflow to inf; NaN compared as a class (payloads of NaN
+    # are not fixed by IEEE 754 and differ between host and device adders)
+    vals = np.array([0x8000, 0x8000, 0x0001, 0x7F7F, 0x3F80, 0xBF80, 0x0000, 0x7FC0], np.uint16)
+    R = 2
+    a = np.tile(vals, 64)
+    b = np.tile(np.array([0x8000, 0x0000, 0x0001, 0x7F7F, 0xBF80, 0x3F80, 0x8000, 0x3F80],
+                         np.uint16), 64)
+    nm = namings.allreduce(R, a.size, "bf16")
+    for cfg in (dict(zero_copy=1), dict(protocol="spec")):
+        got, _ = run_once(nm, [a, b], **cfg)
+        want = collectives.allreduce([a, b], "bf16")
+        g = got[0]
+        w = want[0]
+        nan_g = (g & 0x7FFF) > 0x7F80
+        nan_w = (w & 0x7FFF) > 0x7F80
+        assert np.array_equal(nan_g, nan_w)
+        assert np.array_equal(g[~nan_g], w[~nan_w])
+
+
+# ------------------------------------------------------------ decode all-reduce epochs
+
+def _decode_case(R=8, n=4096, pool=7, seed=2):
+    rng = synth.seeded_rng(seed)
+    pool_np = [[synth.normal_bf16(rng, n) for _ in range(R)] for _ in range(pool)]
+    ins = [torch.stack([to_dev(pool_np[p][r], "bf16") for p in range(pool)]).contiguous()
+           for r in range(R)]
+    expect = [collectives.allreduce(pool_np[p], "bf16")[0] for p in range(pool)]
+    expect_dev = torch.stack([to_dev(e, "bf16") for e in expect])  # [pool, n]
+    return ins, expect_dev
+
+
+def _check_epochs(outs, expect_dev, n_epochs, pool):
+    """outs[r]: [n_epochs, n] device tensors; epoch i must equal expect[i % pool]."""
+    idx = torch.arange(n_epochs, device="cuda") % pool
+    want = expect_dev[idx]
+    bad = 0
+    for o in outs:
+        bad += int((o != want).any(dim=1).sum())
+    return bad
+
+
+@pytest.mark.parametrize("protocol", ["barrier", "dual", "spec"])
+@pytest.mark.parametrize("datapath", ["oneshot", "twoshot"])
+def test_decode_allreduce_epochs_bit_exact(protocol, datapath):
+    R, n, pool, E = 8, 4096, 7, 2000
+    ins, expect = _decode_case(R, n, pool)
+    nm = namings.allreduce(R, n, "bf16")
+    plan = cdc.Plan(nm, protocol=protocol, datapath=datapath)
+    outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    plan.run(ins, outs, n_epochs=E, in_epoch_stride=n * 2, in_pool=pool, out_epoch_stride=n * 2)
+    st = plan.status()
+    assert st["code"] == 0, st
+    assert _check_epochs(outs, expect, E, pool) == 0
+    # a second run continues the epoch count and stays exact
+    plan.run(ins, outs, n_epochs=E, in_epoch_stride=n * 2, in_pool=pool, out_epoch_stride=n * 2)
+    assert plan.status()["code"] == 0
+    assert _check_epochs(outs, expect, E, pool) == 0
+    plan.reset()
+    plan.run(ins, outs, n_epochs=E, in_epoch_stride=n * 2, in_pool=pool, out_epoch_stride=n * 2)
+    assert plan.status()["code"] == 0
+    assert _check_epochs(outs, expect, E, pool) == 0
+    plan.free()
+
+
+def test_decode_allreduce_10000_epochs_spec_equals_barrier_under_stagger():
+    R, n, pool, E = 8, 4096, 7, 10000
+    ins, expect = _decode_case(R, n, pool)
+    nm = namings.allreduce(R, n, "bf16")
+    res = {}
+    for name, cfg in [("barrier", dict(protocol="barrier")),
+                      ("dual", dict(protocol="dual")),
+                      ("spec", dict(protocol="spec")),
+                      ("spec-stagger", dict(protocol="spec", inject="stagger", inject_seed=2,
+                                            inject_prob_ppm=100000, inject_max_ns=20000,
+                                            inject_start_ns=5000))]:
+        plan = cdc.Plan(nm, **cfg)
+        outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+        plan.run(ins, outs, n_epochs=E, in_epoch_stride=n * 2, in_pool=pool,
+                 out_epoch_stride=n * 2)
+        st = plan.status()
+        assert st["code"] == 0, (name, st)
+        assert _check_epochs(outs, expect, E, pool) == 0, name
+        res[name] = (outs, st)
+        plan.free()
+    for name in ("dual", "spec", "spec-stagger"):
+        for a, b in zip(res[name][0], res["barrier"][0]):
+            assert torch.equal(a, b)
+    assert res["spec"][1]["spec_checks"] == E * R * 16
+
+
+def test_speculation_with_adversarial_pause_tagged_is_exact_literal_is_not():
+    # consumer rank 2 loads its peers' payloads, signals, then pauses; rank 3 stages each
+    # epoch only after that signal, inside the pause. The pages' literal flag-sum check then accepts the stale
+    # payload (the falsifier of the monotonicity premise); the content tag rejects it and
+    # the retry path reloads.
+    R, n, pool, E = 8, 4096, 7, 300
+    ins, expect = _decode_case(R, n, pool)
+    nm = namings.allreduce(R, n, "bf16")
+    bad = {}
+    for check in ("tagged", "literal"):
+        plan = cdc.Plan(nm, protocol="spec", spec_check=check, inject="spec_pause", inject_rank=2,
+                        inject_max_ns=200000, inject_pause_ns=20000)
+        outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+        plan.run(ins, outs, n_epochs=E, in_epoch_stride=n * 2, in_pool=pool,
+                 out_epoch_stride=n * 2)
+        st = plan.status()
+        assert st["code"] == 0, st
+        bad[check] = (_check_epochs(outs, expect, E, pool), st["spec_retries"])
+        plan.free()
+    assert bad["tagged"][0] == 0
+    assert bad["tagged"][1] > 0
+    assert bad["literal"][0] > 0
+
+
+def test_missing_notify_times_out_and_the_gpu_stays_usable():
+    R, n = 4, 1024
+    rng = synth.seeded_rng(5)
+    xs = [synth.normal_bf16(rng, n) for _ in range(R)]
+    nm = namings.allreduce(R, n, "bf16")
+    plan = cdc.Plan(nm, protocol="dual", inject="skip_notify", inject_rank=1,
+                    spin_limit_ns=20_000_000)
+    ins = [to_dev(x, "bf16") for x in xs]
+    outs = [empty_dev(n, "bf16") for _ in range(R)]
+    plan.run(ins, outs, n_epochs=5)
+    st = plan.status()
+    assert st["code"] == cdc._lib.D["COLL_ETIMEDOUT"], st
+    assert st["fail_epoch"] == 1
+    plan.free()
+    got, _ = run_once(nm, xs, protocol="dual")
+    want = collectives.allreduce(xs, "bf16")
+    assert bits_equal(got[0], want[0])
+
+
+def test_run_rejects_aliasing_and_misalignment():
+    nm = namings.allreduce(2, 1024, "bf16")
+    plan = cdc.Plan(nm, protocol="spec")
+    a = torch.zeros(4096, dtype=torch.int16, device="cuda")
+    code = plan.run_ptrs([a.data_ptr(), a.data_ptr() + 2048], [a.data_ptr() + 2048, a.data_ptr() + 6000])
+    assert code == cdc._lib.D["COLL_EOVERLAP"]
+    code = plan.run_ptrs([a.data_ptr() + 2, a.data_ptr() + 4096], [a.data_ptr() + 8192 - 2048, 0])
+    assert code in (cdc._lib.D["COLL_EALIGN"], cdc._lib.D["COLL_EINVAL"])
+    plan.free()
+
+
+# ------------------------------------------------------------ full-size cases
+
+def test_prefill_allreduce_64mib_oneshot_and_twoshot_full():
+    R, n = 8, 8192 * 4096
+    rng = synth.seeded_rng(4)
+    xs = [synth.normal_bf16(rng, n) for _ in range(R)]
+    want = collectives.allreduce(xs, "bf16")[0]
+    want_dev = to_dev(want, "bf16")
+    ins = [to_dev(x, "bf16") for x in xs]
+    nm = namings.allreduce(R, n, "bf16")
+    for dp in ("oneshot", "twoshot"):
+        plan = cdc.Plan(nm, zero_copy=1, datapath=dp)
+        outs = [torch.empty(n, dtype=torch.int16, device="cuda") for _ in range(R)]
+        plan.run(ins, outs)
+        assert plan.status()["code"] == 0
+        for o in outs:
+            assert torch.equal(o, want_dev), dp
+        plan.free()
+
+
+def test_moe_dispatch_full_size():
+    R, T, H, E, k = 8, 4096, 7168, 256, 8
+    routing = synth.zipf_topk_routing(5, R, T, E, k, 1.1)
+    rng = synth.seeded_rng(5)
+    xs = [synth.normal_bf16(rng, (T, H)) for _ in range(R)]
+    nm = namings.moe_dispatch(routing, E // R, H)
+    want, counts = collectives.moe_dispatch(xs, routing, E // R)
+    assert counts == nm.meta["counts"]
+    plan = cdc.Plan(nm, zero_copy=1)
+    ins = [to_dev(x.ravel(), "bf16") for x in xs]
+    outs = [torch.empty(L, dtype=torch.int16, device="cuda") for L in nm.out_len]
+    plan.run(ins, outs)
+    assert plan.status()["code"] == 0
+    for d in range(R):
+        got = from_dev(outs[d][:counts[d] * H], "bf16")
+        assert bits_equal(got, want[d].ravel())
+    plan.free()
+
+
+@pytest.mark.parametrize("kind", ["allreduce", "reduce_scatter", "allgather", "broadcast", "alltoall"])
+def test_sweep_256mib_sampled(kind):
+    # the largest sweep size: check 4096 sampled output elements per rank against the
+    # oracle's definition evaluated at exactly those elements
+    R, n = 8, (256 << 20) // 2
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    ins = [((torch.rand(n, device="cuda", generator=g) * 2 - 1).to(torch.bfloat16)).view(torch.int16)
+           for _ in range(R)]
+    nm = getattr(namings, kind)(R, n, "bf16")
+    dp = "twoshot" if kind == "allreduce" else "oneshot"
+    plan = cdc.Plan(nm, zero_copy=1, datapath=dp)
+    outs = [torch.empty(L, dtype=torch.int16, device="cuda") for L in nm.out_len]
+    plan.run(ins, outs)
+    assert plan.status()["code"] == 0
+    rng = synth.seeded_rng(33)
+    b = n // R
+    for d in range(R):
+        L = nm.out_len[d]
+        idx = np.sort(rng.integers(0, L, 4096))
+        it = torch.from_numpy(idx).cuda()
+        got = from_dev(outs[d][it], "bf16")
+        if kind in ("allreduce", "reduce_scatter"):
+            src = idx if kind == "allreduce" else idx + d * b
+            st = torch.from_numpy(src).cuda()
+            terms = [from_dev(x[st], "bf16") for x in ins]
+            want = collectives.allreduce(terms, "bf16")[0]
+        elif kind == "allgather":
+            want = np.array([from_dev(ins[i // n][i % n:i % n + 1], "bf16")[0] for i in idx[:256]])
+            got = got[:256]
+        elif kind == "broadcast":
+            want = from_dev(ins[0][it], "bf16")
+        else:
+            s_idx = idx // b
+            want = np.array([from_dev(ins[s][d * b + (i % b):d * b + (i % b) + 1], "bf16")[0]
+                             for s, i in zip(s_idx[:256], idx[:256])])
+            got = got[:256]
+        assert bits_equal(got, want), kind
+    plan.free()
+    del outs, ins
+    torch.cuda.empty_cache()
