@@ -10,7 +10,7 @@ protocols, a staggered-start stress run of the speculative protocol, and the
 prefill-sized all-reduce (8 x 64 MiB, one-shot vs two-shot) as achieved HBM GB/s.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|prefill|sweep|moe]
+                    [--workload decode|sweep|prefill|moe] [--max-bytes B]
 
 Under torchrun each rank runs an independent replica on its own GPU (the emulated
 collective needs no inter-GPU exchange); rank 0 prints one JSON line.
@@ -348,6 +348,89 @@ def run_reference(args):
     }
 
 
+# ------------------------------------------------------------------ other workloads
+
+def _zc_measure(torch, cdc, nm, ins, outs, steps, warmup, flush, stream, **cfg):
+    pl = cdc.Plan(nm, zero_copy=1, **cfg)
+    tt = _time_steps(torch, lambda: pl.run(ins, outs), steps, warmup, flush, stream)
+    st = pl.status()
+    if st["code"] != 0:
+        raise RuntimeError(f"run failed: {st}")
+    b = pl.info.min_bytes
+    pl.free()
+    t = sorted(tt)[len(tt) // 2]
+    return {"us": round(t * 1000, 3), "gbs": round(b / (t / 1000) / 1e9, 1), "min_bytes": b}
+
+
+def run_workload(args):
+    """Non-default workloads: the layout-named sweep, the prefill all-reduce, MoE dispatch.
+    Each prints its own JSON line (median of K steps, L2 flushed before each)."""
+    import torch
+    import collective_datapath_copy_gb300 as cdc
+    from collective_datapath_copy_gb300.build import build
+    build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.fill_(1)
+    peak, peak_kind = peaks()
+    R = 8
+    g = torch.Generator(device=dev)
+    res = {"workload": args.workload, "peak_gbs": peak, "peak_kind": peak_kind}
+    if args.workload == "sweep":
+        sizes = [1 << k for k in range(10, 29, 2)]  # 1 KiB .. 256 MiB per rank
+        if args.max_bytes:
+            sizes = [m for m in sizes if m <= args.max_bytes]
+        rows = []
+        for m in sizes:
+            n = m // 2
+            g.manual_seed(3)
+            ins = [((torch.rand(n, device=dev, generator=g) * 2 - 1).to(torch.bfloat16))
+                   .view(torch.int16) for _ in range(R)]
+            for kind in ("allreduce", "reduce_scatter", "allgather", "broadcast", "alltoall"):
+                nm = getattr(cdc, kind)(R, n, "bf16")
+                outs = [torch.empty(L, dtype=torch.int16, device=dev) for L in nm.out_len]
+                cfgs = {"twoshot": dict(datapath="twoshot")} if kind == "allreduce" else {"": {}}
+                if kind == "allreduce" and m <= (1 << 20):
+                    cfgs["oneshot"] = dict(datapath="oneshot")
+                for tag, cfg in cfgs.items():
+                    r = _zc_measure(torch, cdc, nm, ins, outs, args.steps, args.warmup, flush,
+                                    stream, **cfg)
+                    r.update({"collective": kind + (f"-{tag}" if tag else ""), "bytes_per_rank": m,
+                              "frac": round(r["gbs"] / peak, 4)})
+                    rows.append(r)
+                del outs
+            del ins
+            torch.cuda.empty_cache()
+        res["rows"] = rows
+    elif args.workload == "prefill":
+        n = 8192 * 4096
+        g.manual_seed(4)
+        ins = [torch.randn(n, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
+               for _ in range(R)]
+        outs = [torch.empty(n, dtype=torch.int16, device=dev) for _ in range(R)]
+        nm = cdc.allreduce(R, n, "bf16")
+        for dp in ("twoshot", "oneshot"):
+            r = _zc_measure(torch, cdc, nm, ins, outs, args.steps, args.warmup, flush, stream,
+                            datapath=dp)
+            r["frac"] = round(r["gbs"] / peak, 4)
+            res[dp] = r
+    elif args.workload == "moe":
+        T, H, E, k = 4096, 7168, 256, 8
+        routing = synth.zipf_topk_routing(5, R, T, E, k, 1.1)
+        nm = cdc.moe_dispatch(routing, E // R, H)
+        g.manual_seed(5)
+        ins = [torch.randn(T * H, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
+               for _ in range(R)]
+        outs = [torch.empty(L, dtype=torch.int16, device=dev) for L in nm.out_len]
+        r = _zc_measure(torch, cdc, nm, ins, outs, args.steps, args.warmup, flush, stream)
+        r["frac"] = round(r["gbs"] / peak, 4)
+        r["rows_per_rank"] = nm.meta["counts"]
+        res["dispatch"] = r
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -358,6 +441,8 @@ def main():
     ap.add_argument("--ref-epochs", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--workload", default="decode", choices=["decode", "sweep", "prefill", "moe"])
+    ap.add_argument("--max-bytes", type=int, default=0, help="sweep: largest bytes per rank")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -367,6 +452,10 @@ def main():
         if rank != 0:
             return
         print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.workload != "decode":
+        if rank == 0:
+            print(json.dumps(run_workload(args)), flush=True)
         return
     dist = None
     if world > 1:

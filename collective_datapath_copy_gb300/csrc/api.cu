@@ -89,27 +89,28 @@ extern "C" int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_
   *out = nullptr;
   coll_plan_s *p = new (std::nothrow) coll_plan_s();
   if (!p) return COLL_ENOMEM;
-  int e = coll_compile(R, op, dtype, in_segs, n_in, in_len, out_segs, n_out, out_len, cfg, 0, &p->c);
-  if (e) {
-    delete p;
-    return e;
-  }
-  coll_compiled &c = p->c;
   if (cudaGetDevice(&p->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
     delete p;
     return COLL_ECUDA;
   }
-  if (!c.cfg.zero_copy) {
-    int max_ctas = 0;
-    if (coll::engine_max_coresident(c.op, c.dtype, &max_ctas) != cudaSuccess) {
-      delete p;
-      return COLL_ECUDA;
-    }
-    if (c.warps.size() > (size_t)max_ctas) {  // every engine warp must be co-resident
-      delete p;
-      return COLL_EINVAL;
-    }
+  int max_ctas = coll_default_max_warps();
+  const int eop = (op == COLL_OP_SUM) ? COLL_OP_SUM : COLL_OP_COPY;
+  if (coll::engine_max_coresident(eop, dtype == COLL_F32 ? COLL_F32 : COLL_BF16, &max_ctas) !=
+      cudaSuccess) {
+    delete p;
+    return COLL_ECUDA;
+  }
+  int e = coll_compile(R, op, dtype, in_segs, n_in, in_len, out_segs, n_out, out_len, cfg,
+                       max_ctas, &p->c);
+  if (e) {
+    delete p;
+    return e;
+  }
+  coll_compiled &c = p->c;
+  if (!c.cfg.zero_copy && c.warps.size() > (size_t)max_ctas) {  // must all be co-resident
+    delete p;
+    return COLL_EINVAL;
   }
   const size_t tb = table_bytes(c.refs) + table_bytes(c.jobs) + table_bytes(c.tiles) +
                     table_bytes(c.units) + table_bytes(c.sitems) + table_bytes(c.citems) +

@@ -98,7 +98,9 @@ struct coll_compiled {
 
 int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_in,
                  const uint64_t *in_len, const coll_seg_t *out_segs, size_t n_out,
-                 const uint64_t *out_len, const coll_config_t *cfg, int num_sms,
+                 const uint64_t *out_len, const coll_config_t *cfg, int max_warps,
                  coll_compiled *out);
+// Engine warps that may be co-resident when no device can be asked (host-only compile).
+inline int coll_default_max_warps() { return 1024; }
 void coll_fill_info(const coll_compiled &c, coll_plan_info_t *info);
 #endif

@@ -60,9 +60,8 @@ static int check_config(const coll_config_t &c) {
 
 int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_in,
                  const uint64_t *in_len, const coll_seg_t *out_segs, size_t n_out,
-                 const uint64_t *out_len, const coll_config_t *cfg_in, int num_sms,
+                 const uint64_t *out_len, const coll_config_t *cfg_in, int max_warps,
                  coll_compiled *out) {
-  (void)num_sms;
   coll_compiled c;
   if (cfg_in) c.cfg = *cfg_in; else coll_config_default(&c.cfg);
   const coll_config_t &cfg = c.cfg;
@@ -267,11 +266,14 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
     }
   }
   if (c.units.size() > 0x7FFFFFF0ull || c.n_pflag > 0x7FFFFFF0u) return COLL_EINVAL;
-  // warps: rank r gets W_r warps; item k of its stage (consume) list goes to warp k % W_r
+  // warps: rank r gets W_r warps; item k of its stage (consume) list goes to warp k % W_r.
+  // Every warp must be co-resident (they wait on each other), so the total is capped.
   std::vector<uint32_t> wbase(R + 1, 0);
+  const uint32_t cap_r = std::max<uint32_t>(1u, (uint32_t)(max_warps > 0 ? max_warps : 1024) / (uint32_t)R);
   for (int r = 0; r < R; ++r) {
     uint32_t need = (uint32_t)std::max(S[r].size(), C[r].size());
     uint32_t Wr = cfg.warps_per_rank ? std::min<uint32_t>(need, (uint32_t)cfg.warps_per_rank) : need;
+    Wr = std::min(Wr, cap_r);
     wbase[r + 1] = wbase[r] + Wr;
   }
   const uint32_t nwarps = wbase[R];
@@ -353,7 +355,8 @@ extern "C" int coll_validate(int R, int op, int dtype, const coll_seg_t *in_segs
                              const uint64_t *out_len, const coll_config_t *cfg,
                              coll_plan_info_t *info) {
   coll_compiled c;
-  int e = coll_compile(R, op, dtype, in_segs, n_in, in_len, out_segs, n_out, out_len, cfg, 0, &c);
+  int e = coll_compile(R, op, dtype, in_segs, n_in, in_len, out_segs, n_out, out_len, cfg,
+                       coll_default_max_warps(), &c);
   if (e) return e;
   coll_fill_info(c, info);
   return COLL_OK;
