@@ -165,6 +165,9 @@ def run_ours(args, rank, world, dist):
         ("barrier", dict(protocol="barrier")),
         ("spec_stagger", dict(protocol="spec", inject="stagger", inject_seed=2,
                               inject_prob_ppm=100000, inject_max_ns=20000, inject_start_ns=5000)),
+        ("spec_relaxed", dict(protocol="spec", spec_check="relaxed")),
+        ("spec_literal", dict(protocol="spec", spec_check="literal")),
+        ("spec_twoshot", dict(protocol="spec", datapath="twoshot")),
     ]}
 
     def step(name):
@@ -191,13 +194,14 @@ def run_ours(args, rank, world, dist):
 
     # other protocols (same K/W)
     proto = {}
-    for name in ("dual", "barrier", "spec_stagger"):
+    for name in ("dual", "barrier", "spec_stagger", "spec_relaxed", "spec_literal",
+                 "spec_twoshot"):
         tt = _time_steps(torch, step(name), max(3, args.steps // 2), 1, flush, stream)
         s2 = plans[name].status()
         if s2["code"] != 0:
             raise RuntimeError(f"{name} failed: {s2}")
         proto[name] = {"us_per_epoch": round(sum(tt) / len(tt) * 1000 / EPOCHS, 4)}
-        if name == "spec_stagger":
+        if name.startswith("spec"):
             proto[name]["retries_per_check"] = (s2["spec_retries"] / s2["spec_checks"]
                                                 if s2["spec_checks"] else 0.0)
     proto["spec"] = {"us_per_epoch": round(us_epoch, 4),
@@ -350,16 +354,38 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ other workloads
 
-def _zc_measure(torch, cdc, nm, ins, outs, steps, warmup, flush, stream, **cfg):
+def _zc_measure(torch, cdc, nm, ins, outs, steps, warmup, flush, stream, graph_reps=0, **cfg):
+    """Median single-launch time with L2 flushed before each launch; with graph_reps, also
+    the per-collective time of graph_reps back-to-back launches replayed from a CUDA graph
+    (no host overhead, L2 warm)."""
     pl = cdc.Plan(nm, zero_copy=1, **cfg)
     tt = _time_steps(torch, lambda: pl.run(ins, outs), steps, warmup, flush, stream)
     st = pl.status()
     if st["code"] != 0:
         raise RuntimeError(f"run failed: {st}")
     b = pl.info.min_bytes
-    pl.free()
     t = sorted(tt)[len(tt) // 2]
-    return {"us": round(t * 1000, 3), "gbs": round(b / (t / 1000) / 1e9, 1), "min_bytes": b}
+    r = {"us": round(t * 1000, 3), "gbs": round(b / (t / 1000) / 1e9, 1), "min_bytes": b,
+         "tiles": int(pl.info.n_tiles)}
+    if graph_reps:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            pl.run(ins, outs)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for _ in range(graph_reps):
+                pl.run(ins, outs)
+        g.replay()
+        torch.cuda.synchronize()
+        tg = _time_steps(torch, g.replay, max(3, steps // 2), 1, lambda: None, stream)
+        tgm = sorted(tg)[len(tg) // 2] / graph_reps
+        r["us_graph"] = round(tgm * 1000, 3)
+        del g
+    pl.free()
+    return r
 
 
 def run_workload(args):
@@ -396,7 +422,7 @@ def run_workload(args):
                     cfgs["oneshot"] = dict(datapath="oneshot")
                 for tag, cfg in cfgs.items():
                     r = _zc_measure(torch, cdc, nm, ins, outs, args.steps, args.warmup, flush,
-                                    stream, **cfg)
+                                    stream, graph_reps=50 if m <= (4 << 20) else 0, **cfg)
                     r.update({"collective": kind + (f"-{tag}" if tag else ""), "bytes_per_rank": m,
                               "frac": round(r["gbs"] / peak, 4)})
                     rows.append(r)

@@ -40,7 +40,8 @@ ESIZE = {"bf16": 2, "f32": 4, "bytes": 1}
 PROTOCOL = {"barrier": D["COLL_PROTO_BARRIER"], "dual": D["COLL_PROTO_DUAL"],
             "spec": D["COLL_PROTO_SPEC"]}
 DATAPATH = {"oneshot": D["COLL_DP_ONESHOT"], "twoshot": D["COLL_DP_TWOSHOT"]}
-SPEC_CHECK = {"tagged": D["COLL_SPEC_TAGGED"], "literal": D["COLL_SPEC_LITERAL"]}
+SPEC_CHECK = {"tagged": D["COLL_SPEC_TAGGED"], "literal": D["COLL_SPEC_LITERAL"],
+              "relaxed": D["COLL_SPEC_TAGGED_RELAXED"]}
 INJECT = {"skip_notify": D["COLL_INJECT_SKIP_NOTIFY"], "stagger": D["COLL_INJECT_STAGGER"],
           "spec_pause": D["COLL_INJECT_SPEC_PAUSE"]}
 

@@ -30,6 +30,7 @@ struct coll_plan_s {
   uint64_t epochs_issued = 0;
   cudaEvent_t done = nullptr;
   bool ran = false;
+  bool captured = false;  // a run was captured into a graph: status waits for the device
   int last_epochs = 0;
 };
 
@@ -102,7 +103,7 @@ extern "C" int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_
     return COLL_ECUDA;
   }
   int e = coll_compile(R, op, dtype, in_segs, n_in, in_len, out_segs, n_out, out_len, cfg,
-                       max_ctas, &p->c);
+                       max_ctas, p->num_sms, &p->c);
   if (e) {
     delete p;
     return e;
@@ -231,7 +232,7 @@ extern "C" int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_
     a.in_pool = in_pool;
     a.in_stride = in_epoch_stride;
     a.out_stride = out_epoch_stride;
-    const int ctas = c.cfg.ctas ? c.cfg.ctas : 2 * p->num_sms;
+    const int ctas = c.cfg.ctas ? c.cfg.ctas : 3 * p->num_sms;
     const int keep = (c.op == COLL_OP_SUM && c.cfg.datapath == COLL_DP_ONESHOT) ? 1 : 0;
     err = coll::launch_zero_copy(c.op, c.dtype, keep, a, ctas, s);
   } else {
@@ -277,15 +278,30 @@ extern "C" int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_
     cudaGetLastError();
     return COLL_ECUDA;
   }
-  if (cudaEventRecord(p->done, s) != cudaSuccess) return COLL_ECUDA;
-  p->ran = true;
+  // Inside a stream capture the completion event is not recorded (a captured record
+  // cannot be waited on from outside the graph); coll_status then waits for the device.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return COLL_ECUDA;
+  if (cs == cudaStreamCaptureStatusNone) {
+    if (cudaEventRecord(p->done, s) != cudaSuccess) return COLL_ECUDA;
+    p->ran = true;
+  } else {
+    p->ran = false;
+    p->captured = true;
+  }
   p->last_epochs = n_epochs;
+  return COLL_OK;
+}
+
+static int wait_last(coll_plan_s *p) {
+  if (p->ran && cudaEventSynchronize(p->done) != cudaSuccess) return COLL_ECUDA;
+  if (p->captured && cudaDeviceSynchronize() != cudaSuccess) return COLL_ECUDA;
   return COLL_OK;
 }
 
 extern "C" int coll_status(coll_plan_t p, coll_stats_t *st) {
   if (!p) return COLL_EINVAL;
-  if (p->ran && cudaEventSynchronize(p->done) != cudaSuccess) return COLL_ECUDA;
+  if (wait_last(p)) return COLL_ECUDA;
   coll_dev_status_t d;
   if (cudaMemcpy(&d, p->d_status, sizeof(d), cudaMemcpyDeviceToHost) != cudaSuccess)
     return COLL_ECUDA;
@@ -306,7 +322,7 @@ extern "C" int coll_status(coll_plan_t p, coll_stats_t *st) {
 extern "C" int64_t coll_stamps(coll_plan_t p, uint64_t *host, int64_t n) {
   if (!p || !host || n < 0) return COLL_EINVAL;
   if (!p->d_stamps) return 0;
-  if (p->ran && cudaEventSynchronize(p->done) != cudaSuccess) return COLL_ECUDA;
+  if (wait_last(p)) return COLL_ECUDA;
   int64_t m = std::min<int64_t>(n, (int64_t)std::min<uint32_t>(p->stamp_cap, (uint32_t)p->last_epochs) + 1);
   if (cudaMemcpy(host, p->d_stamps, (size_t)m * 8, cudaMemcpyDeviceToHost) != cudaSuccess)
     return COLL_ECUDA;
@@ -315,7 +331,7 @@ extern "C" int64_t coll_stamps(coll_plan_t p, uint64_t *host, int64_t n) {
 
 extern "C" int coll_reset(coll_plan_t p) {
   if (!p) return COLL_EINVAL;
-  if (p->ran && cudaEventSynchronize(p->done) != cudaSuccess) return COLL_ECUDA;
+  if (wait_last(p)) return COLL_ECUDA;
   int e = zero_state(p);
   if (e) return e;
   return cudaDeviceSynchronize() == cudaSuccess ? COLL_OK : COLL_ECUDA;

@@ -82,6 +82,16 @@ __device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 __device__ __forceinline__ void st_relaxed_u32(uint32_t *p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -176,11 +186,20 @@ __device__ __forceinline__ uint32_t mix32(uint32_t x) {
   return x;
 }
 
-// Order-independent contribution of vector `vi` (index inside its piece).
+// Contribution of vector `vi` (its index inside the piece) to the piece's tag: each 32-bit
+// word is salted by its position, multiplied by an odd constant and xor-shifted; the
+// contributions are summed (so lanes can be reduced in any order).
 __device__ __forceinline__ uint32_t tag_part(uint4 v, uint32_t vi) {
-  uint32_t s = vi * 0x01000193u;
-  return mix32(v.x ^ s) + mix32(v.y ^ (s + 0x68E31DA4u)) + mix32(v.z ^ (s + 0xB5297A4Du)) +
-         mix32(v.w ^ (s + 0x1B56C4E9u));
+  const uint32_t s = vi * 0x9E3779B9u;
+  uint32_t a = (v.x ^ s) * 0x85EBCA77u;
+  uint32_t b = (v.y ^ (s + 0x632BE5ABu)) * 0xC2B2AE3Du;
+  uint32_t c = (v.z ^ (s + 0x165667B1u)) * 0x27D4EB2Fu;
+  uint32_t d = (v.w ^ (s + 0xD3A2646Cu)) * 0x9E3779B1u;
+  a ^= a >> 15;
+  b ^= b >> 13;
+  c ^= c >> 16;
+  d ^= d >> 15;
+  return a + b + c + d;
 }
 
 __device__ __forceinline__ uint32_t tag_fold(uint32_t h, uint32_t epoch) {

@@ -99,8 +99,9 @@ struct coll_compiled {
 int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_in,
                  const uint64_t *in_len, const coll_seg_t *out_segs, size_t n_out,
                  const uint64_t *out_len, const coll_config_t *cfg, int max_warps,
-                 coll_compiled *out);
+                 int num_sms, coll_compiled *out);
 // Engine warps that may be co-resident when no device can be asked (host-only compile).
 inline int coll_default_max_warps() { return 1024; }
+inline int coll_default_num_sms() { return 152; }
 void coll_fill_info(const coll_compiled &c, coll_plan_info_t *info);
 #endif

@@ -33,94 +33,108 @@ __device__ __forceinline__ uint4 zc_load(const char *p) {
   if constexpr (KEEP) return ld_nc_v4(p); else return ld_cs_v4(p);
 }
 
+// One warp per tile. Lane k holds the pointer of producer k and of consumer k for the
+// tile (up to 32 each); the vector loops fetch them with shuffles. Tiles with more than 32
+// producers or consumers, or with an address not 16-byte aligned, take the element-wise
+// path (same arithmetic, same order).
 template <int KIND, bool KEEP>
-__global__ void __launch_bounds__(512) zc_kernel(const ZcArgs a) {
-  __shared__ const char *s_src[COLL_MAX_FANIN];
-  __shared__ char *s_dst[COLL_MAX_FANOUT];
-  const uint32_t tid = threadIdx.x, bd = blockDim.x;
+__global__ void __launch_bounds__(256, 3) zc_kernel(const ZcArgs a) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint64_t gw = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint64_t nw = ((uint64_t)gridDim.x * blockDim.x) >> 5;
   const uint64_t total = (uint64_t)a.ntiles * a.n_epochs;
-  for (uint64_t t = blockIdx.x; t < total; t += gridDim.x) {
+  for (uint64_t t = gw; t < total; t += nw) {
     const uint32_t e = (uint32_t)(t / a.ntiles);
     const uint32_t ti = (uint32_t)(t - (uint64_t)e * a.ntiles);
     const coll_tile_t tile = a.tiles[ti];
     const coll_job_t job = a.jobs[tile.job];
     const int64_t ioff = (int64_t)(e % (uint32_t)a.in_pool) * a.in_stride + (int64_t)tile.start;
     const int64_t ooff = (int64_t)e * a.out_stride + (int64_t)tile.start;
-    __syncthreads();  // the previous tile is done with the pointer tables
-    uint32_t mis = tile.nbytes & 15u;
-    for (uint32_t i = tid; i < job.nsrc; i += bd) {
-      const coll_ref_t r = a.refs[job.src0 + i];
-      const char *p = a.ptr.in[r.rank] + r.off + ioff;
-      s_src[i] = p;
-      mis |= (uint32_t)((uintptr_t)p & 15u);
-    }
-    for (uint32_t i = tid; i < job.ndst; i += bd) {
-      const coll_ref_t r = a.refs[job.dst0 + i];
-      char *p = a.ptr.out[r.rank] + r.off + ooff;
-      s_dst[i] = p;
-      mis |= (uint32_t)((uintptr_t)p & 15u);
-    }
-    const int misaligned = __syncthreads_or(mis != 0);
     const uint32_t nsrc = job.nsrc, ndst = job.ndst;
-    if (!misaligned) {
+    const char *sp = nullptr;
+    char *dp = nullptr;
+    uint32_t mis = tile.nbytes & 15u;
+    if (lane < nsrc) {
+      const coll_ref_t r = a.refs[job.src0 + lane];
+      sp = a.ptr.in[r.rank] + r.off + ioff;
+      mis |= (uint32_t)((uintptr_t)sp & 15u);
+    }
+    if (lane < ndst) {
+      const coll_ref_t r = a.refs[job.dst0 + lane];
+      dp = a.ptr.out[r.rank] + r.off + ooff;
+      mis |= (uint32_t)((uintptr_t)dp & 15u);
+    }
+    const bool slow = __any_sync(FULL, mis != 0) || nsrc > 32 || ndst > 32;
+    if (!slow) {
       const uint32_t nvec = tile.nbytes >> 4;
       if constexpr (KIND == 0) {
-        for (uint32_t base = tid; base < nvec; base += 4 * bd) {
-          uint4 x[4];
+        const char *s0 = (const char *)__shfl_sync(FULL, (uintptr_t)sp, 0);
+        constexpr uint32_t U = 4;
+        for (uint32_t base = lane; base < nvec; base += 32 * U) {
+          uint4 x[U];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t idx = base + u * bd;
-            if (idx < nvec) x[u] = zc_load<KIND, KEEP>(s_src[0] + (size_t)idx * 16);
-          }
+          for (uint32_t u = 0; u < U; ++u)
+            if (base + 32 * u < nvec) x[u] = zc_load<KIND, KEEP>(s0 + (size_t)(base + 32 * u) * 16);
           for (uint32_t d = 0; d < ndst; ++d) {
-            char *q = s_dst[d];
+            char *q = (char *)__shfl_sync(FULL, (uintptr_t)dp, d);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint32_t idx = base + u * bd;
-              if (idx < nvec) st_cs_v4(q + (size_t)idx * 16, x[u]);
-            }
+            for (uint32_t u = 0; u < U; ++u)
+              if (base + 32 * u < nvec) st_cs_v4(q + (size_t)(base + 32 * u) * 16, x[u]);
           }
         }
       } else {
-        for (uint32_t idx = tid; idx < nvec; idx += bd) {
+        for (uint32_t v = lane; v < nvec; v += 32) {
           Vec16Acc<KIND - 1> acc;
           for (uint32_t k0 = 0; k0 < nsrc; k0 += 8) {
             uint4 x[8];
             const uint32_t kn = nsrc - k0 < 8 ? nsrc - k0 : 8;
 #pragma unroll
-            for (uint32_t k = 0; k < 8; ++k)
-              if (k < kn) x[k] = zc_load<KIND, KEEP>(s_src[k0 + k] + (size_t)idx * 16);
-#pragma unroll
             for (uint32_t k = 0; k < 8; ++k) {
+              const char *p = (const char *)__shfl_sync(FULL, (uintptr_t)sp, (k0 + k) & 31u);
+              if (k < kn) x[k] = zc_load<KIND, KEEP>(p + (size_t)v * 16);
+            }
+#pragma unroll
+            for (uint32_t k = 0; k < 8; ++k)
               if (k < kn) {
                 if (k0 + k == 0) acc.init(x[k]); else acc.add(x[k]);
               }
-            }
           }
           const uint4 r = acc.pack();
-          for (uint32_t d = 0; d < ndst; ++d) st_cs_v4(s_dst[d] + (size_t)idx * 16, r);
+          for (uint32_t d = 0; d < ndst; ++d) {
+            char *q = (char *)__shfl_sync(FULL, (uintptr_t)dp, d);
+            st_cs_v4(q + (size_t)v * 16, r);
+          }
         }
       }
     } else {
-      // Unaligned tile: element-wise path (same arithmetic, same order).
+      // Element-wise path: pointers recomputed from the tables.
+      auto src_of = [&](uint32_t k) {
+        const coll_ref_t r = a.refs[job.src0 + k];
+        return a.ptr.in[r.rank] + r.off + ioff;
+      };
+      auto dst_of = [&](uint32_t d) {
+        const coll_ref_t r = a.refs[job.dst0 + d];
+        return a.ptr.out[r.rank] + r.off + ooff;
+      };
       if constexpr (KIND == 0) {
-        for (uint32_t i = tid; i < tile.nbytes; i += bd) {
-          const char v = s_src[0][i];
-          for (uint32_t d = 0; d < ndst; ++d) s_dst[d][i] = v;
+        const char *s0 = src_of(0);
+        for (uint32_t i = lane; i < tile.nbytes; i += 32) {
+          const char v = s0[i];
+          for (uint32_t d = 0; d < ndst; ++d) dst_of(d)[i] = v;
         }
       } else if constexpr (KIND == 1) {
-        for (uint32_t i = tid; i < tile.nbytes / 2; i += bd) {
-          float acc = __uint_as_float((uint32_t)((const uint16_t *)s_src[0])[i] << 16);
+        for (uint32_t i = lane; i < tile.nbytes / 2; i += 32) {
+          float acc = __uint_as_float((uint32_t)((const uint16_t *)src_of(0))[i] << 16);
           for (uint32_t k = 1; k < nsrc; ++k)
-            acc = __fadd_rn(acc, __uint_as_float((uint32_t)((const uint16_t *)s_src[k])[i] << 16));
+            acc = __fadd_rn(acc, __uint_as_float((uint32_t)((const uint16_t *)src_of(k))[i] << 16));
           const uint16_t r = (uint16_t)(pack_bf16x2(acc, 0.0f) & 0xFFFFu);
-          for (uint32_t d = 0; d < ndst; ++d) ((uint16_t *)s_dst[d])[i] = r;
+          for (uint32_t d = 0; d < ndst; ++d) ((uint16_t *)dst_of(d))[i] = r;
         }
       } else {
-        for (uint32_t i = tid; i < tile.nbytes / 4; i += bd) {
-          float acc = ((const float *)s_src[0])[i];
-          for (uint32_t k = 1; k < nsrc; ++k) acc = __fadd_rn(acc, ((const float *)s_src[k])[i]);
-          for (uint32_t d = 0; d < ndst; ++d) ((float *)s_dst[d])[i] = acc;
+        for (uint32_t i = lane; i < tile.nbytes / 4; i += 32) {
+          float acc = ((const float *)src_of(0))[i];
+          for (uint32_t k = 1; k < nsrc; ++k) acc = __fadd_rn(acc, ((const float *)src_of(k))[i]);
+          for (uint32_t d = 0; d < ndst; ++d) ((float *)dst_of(d))[i] = acc;
         }
       }
     }
@@ -248,6 +262,46 @@ __device__ __forceinline__ uint4 gather_pieces(const char *xb, uint32_t nbytes, 
   return active ? acc.pack() : make_uint4(0, 0, 0, 0);
 }
 
+// Speculatively load (and reduce) the n pieces of a unit, issue the flag loads while the
+// payload loads are in flight, and hash what was loaded (per producer, warp-reduced; lane j
+// keeps producer j's hash). Returns the packed result of this attempt.
+// If `side` is set, the warp also hashes `side_v` (the prefetched next input piece, lanes
+// below side_nvec) into side_h while the first batch of loads is in flight.
+template <int KIND>
+__device__ __forceinline__ uint4 spec_attempt(const char *xb, uint32_t nbytes, uint32_t n,
+                                              uint32_t lane, bool active, bool want_hash,
+                                              const unsigned long long *pf, bool acquire_flags,
+                                              bool load_flags, unsigned long long &f,
+                                              uint32_t &myh, bool side, uint4 side_v,
+                                              uint32_t side_nvec, uint32_t &side_h) {
+  typename EngAcc<KIND>::type acc;
+  myh = 0;
+  for (uint32_t k0 = 0; k0 < n; k0 += 8) {
+    uint4 x[8];
+    const uint32_t kn = n - k0 < 8 ? n - k0 : 8;
+#pragma unroll
+    for (uint32_t k = 0; k < 8; ++k)
+      if (k < kn && active) x[k] = ld_relaxed_v4(xb + (size_t)(k0 + k) * nbytes + lane * 16);
+    if (k0 == 0 && load_flags && lane < n)
+      f = acquire_flags ? ld_acquire_u64(pf + lane) : ld_relaxed_u64(pf + lane);
+    if (k0 == 0 && side)
+      side_h = __reduce_add_sync(FULL, lane < side_nvec ? tag_part(side_v, lane) : 0u);
+#pragma unroll
+    for (uint32_t k = 0; k < 8; ++k) {
+      if (k < kn) {
+        if (active) {
+          if (k0 + k == 0) acc.init(x[k]); else acc.add(x[k]);
+        }
+        if (want_hash) {
+          const uint32_t hs = __reduce_add_sync(FULL, active ? tag_part(x[k], lane) : 0u);
+          if (lane == k0 + k) myh = hs;
+        }
+      }
+    }
+  }
+  return active ? acc.pack() : make_uint4(0, 0, 0, 0);
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
   const uint32_t gw = blockIdx.x;
@@ -256,7 +310,10 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
   const coll_warp_t W = a.warps[gw];
   coll_dev_status_t *st = a.st;
   const bool spec_proto = a.protocol == COLL_PROTO_SPEC;
-  const bool tagged = spec_proto && a.spec_check == COLL_SPEC_TAGGED;
+  // content tags: validated by the tagged checks, stored by every spec producer
+  const bool literal = spec_proto && a.spec_check == COLL_SPEC_LITERAL;
+  const bool relaxed = spec_proto && a.spec_check == COLL_SPEC_TAGGED_RELAXED;
+  const bool tagged = spec_proto && !literal;
   const bool skip_notify =
       (a.inject_flags & COLL_INJECT_SKIP_NOTIFY) && (int)W.rank == a.inject_rank;
   const bool pause_consumer =
@@ -265,6 +322,22 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
                               (int)W.rank == (a.inject_rank + 1) % a.R;
   uint32_t n_checks = 0, n_retries = 0;
   bool failed = false;
+
+  // A warp with exactly one stage item prefetches the next epoch's input piece (read-only
+  // during the kernel) and hashes it while its own consume waits on memory, which takes
+  // the input load and the producer-side tag off the critical path.
+  const bool pipelined = (W.s1 - W.s0) == 1u;
+  coll_unit_t su;
+  coll_ref_t sref;
+  uint4 nx = make_uint4(0, 0, 0, 0);
+  uint32_t nh = 0;
+  bool nh_ready = false;
+  if (pipelined) {
+    su = a.units[a.sitems[W.s0].unit];
+    sref = a.refs[su.src0 + a.sitems[W.s0].slot];
+    if (lane < (su.nbytes >> 4) && a.n_epochs > 0)
+      nx = ld_nc_v4(a.ptr.in[sref.rank] + sref.off + su.start + lane * 16);
+  }
 
   if ((a.inject_flags & COLL_INJECT_STAGGER) && a.inject_start_ns)
     spin_ns((uint64_t)W.rank * a.inject_start_ns);
@@ -285,7 +358,7 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
     // ---------------- Stage + Notify
     for (uint32_t s = W.s0; s < W.s1; ++s) {
       const coll_item_t it = a.sitems[s];
-      const coll_unit_t u = a.units[it.unit];
+      const coll_unit_t u = pipelined ? su : a.units[it.unit];
       if (a.protocol == COLL_PROTO_BARRIER || (u.flags & COLL_UNIT_REUSE_WAIT)) {
         // bottom barrier (single buffer) / explicit reuse wait (dual buffers)
         const uint32_t target = E - (a.protocol == COLL_PROTO_BARRIER ? 1u : 2u);
@@ -305,22 +378,33 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
         }
         __syncwarp();
       }
-      const coll_ref_t r = a.refs[u.src0 + it.slot];
-      const char *src = a.ptr.in[r.rank] + r.off + in_off + u.start;
-      char *dst = a.xbuf + (size_t)b * a.xpar + u.xoff + (size_t)it.slot * u.nbytes;
       const uint32_t nvec = u.nbytes >> 4;
+      char *dst = a.xbuf + (size_t)b * a.xpar + u.xoff + (size_t)it.slot * u.nbytes;
+      uint4 x = make_uint4(0, 0, 0, 0);
       uint32_t h = 0;
-      if (lane < nvec) {
-        const uint4 x = ld_nc_v4(src + lane * 16);
-        st_v4(dst + lane * 16, x);
+      if (pipelined) {
+        x = nx;
+        if (tagged && !nh_ready && lane < nvec) h = tag_part(x, lane);
+      } else if (lane < nvec) {
+        const coll_ref_t r = a.refs[u.src0 + it.slot];
+        x = ld_nc_v4(a.ptr.in[r.rank] + r.off + in_off + u.start + lane * 16);
         if (tagged) h = tag_part(x, lane);
       }
+      if (lane < nvec) st_v4(dst + lane * 16, x);
       uint32_t tag = 0;
-      if (tagged) tag = tag_fold(__reduce_add_sync(FULL, h), E);
+      if (tagged) tag = tag_fold(pipelined && nh_ready ? nh : __reduce_add_sync(FULL, h), E);
       __syncwarp();
-      if (lane == 0 && !skip_notify)
-        st_release_u64(a.pflag + (size_t)b * a.n_pflag + u.pflag0 + it.slot,
-                       ((unsigned long long)E << 32) | tag);
+      if (lane == 0 && !skip_notify) {
+        unsigned long long *fp = a.pflag + (size_t)b * a.n_pflag + u.pflag0 + it.slot;
+        const unsigned long long fv = ((unsigned long long)E << 32) | tag;
+        if (relaxed) st_relaxed_u64(fp, fv); else st_release_u64(fp, fv);
+      }
+      if (pipelined) {
+        nh_ready = false;
+        if (i + 1 < a.n_epochs && lane < nvec)
+          nx = ld_nc_v4(a.ptr.in[sref.rank] + sref.off +
+                        (int64_t)((i + 1) % a.in_pool) * a.in_stride + su.start + lane * 16);
+      }
     }
     if (failed) break;
 
@@ -338,56 +422,81 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
       bool retried = false;
       if (spec_proto && n <= 32) {
         // Speculative consume: load and reduce without waiting, then validate.
-        typename EngAcc<KIND>::type acc;
-        uint32_t myh = 0;
         unsigned long long f = 0;
-        for (uint32_t k0 = 0; k0 < n; k0 += 8) {
-          uint4 x[8];
-          const uint32_t kn = n - k0 < 8 ? n - k0 : 8;
-#pragma unroll
-          for (uint32_t k = 0; k < 8; ++k)
-            if (k < kn && active) x[k] = ld_relaxed_v4(xb + (size_t)(k0 + k) * u.nbytes + lane * 16);
-          if (k0 == 0 && !pause_consumer && lane < n) f = ld_acquire_u64(pf + lane);
-#pragma unroll
-          for (uint32_t k = 0; k < 8; ++k) {
-            if (k < kn) {
-              if (active) {
-                if (k0 + k == 0) acc.init(x[k]); else acc.add(x[k]);
-              }
-              if (tagged) {
-                const uint32_t hs = __reduce_add_sync(FULL, active ? tag_part(x[k], lane) : 0u);
-                if (lane == k0 + k) myh = hs;
-              }
-            }
-          }
-        }
+        uint32_t myh = 0;
+        // (the prefetched next input is hashed while this attempt's loads are in flight)
+        const bool side = pipelined && tagged && !nh_ready;
+        res = spec_attempt<KIND>(xb, u.nbytes, n, lane, active, tagged, pf, !relaxed,
+                                 !pause_consumer, f, myh, side, nx,
+                                 pipelined ? (su.nbytes >> 4) : 0u, nh);
+        if (side) nh_ready = true;
         if (pause_consumer) {
           __syncwarp();
           if (lane == 0 && a.dbg) st_release_u32(a.dbg + it.unit, E);
           spin_ns(a.inject_pause_ns);
-          if (lane < n) f = ld_acquire_u64(pf + lane);
+          if (lane < n) f = relaxed ? ld_relaxed_u64(pf + lane) : ld_acquire_u64(pf + lane);
         }
-        const uint32_t fe = (uint32_t)(f >> 32);
+        uint32_t fe = (uint32_t)(f >> 32);
+        bool lane_ok = lane >= n || (fe == E && (!tagged || (uint32_t)f == tag_fold(myh, E)));
         bool ok;
-        if (tagged) {
-          const bool lane_ok = lane >= n || (fe == E && (uint32_t)f == tag_fold(myh, E));
-          ok = __all_sync(FULL, lane_ok);
-        } else {
+        if (literal) {
           const uint32_t sum = __reduce_add_sync(FULL, lane < n ? fe : 0u);
           ok = sum == n * E;
+        } else {
+          ok = __all_sync(FULL, lane_ok);
         }
         ++n_checks;
         if (ok) {
-          res = acc.pack();
           have = true;
         } else {
           ++n_retries;
           retried = true;
+          if (relaxed) {
+            // No ordering to lean on: reload payload and flags until the content tags
+            // match (bounded by the spin limit and the abort word).
+            uint64_t t0 = globaltimer();
+            for (uint32_t k = 0;; ++k) {
+              uint32_t unused = 0;
+              res = spec_attempt<KIND>(xb, u.nbytes, n, lane, active, true, pf, false, true, f,
+                                       myh, false, nx, 0u, unused);
+              fe = (uint32_t)(f >> 32);
+              lane_ok = lane >= n || (fe == E && (uint32_t)f == tag_fold(myh, E));
+              if (__all_sync(FULL, lane_ok)) {
+                have = true;
+                break;
+              }
+              const bool late = (globaltimer() - t0 > a.spin_ns) ||
+                                ((k & 31u) == 31u && ld_relaxed_u32(&st->abort));
+              if (__any_sync(FULL, late)) break;
+            }
+            if (!have) {
+              if (lane == 0) record_timeout(st, (int)W.rank, (int)it.unit, 3, E);
+              failed = true;
+              break;
+            }
+          } else {
+            // Lanes whose acquire already saw epoch E need no further wait; the others spin
+            // until their producer notifies. Then reload everything after the acquires.
+            bool wok = true;
+            for (uint32_t j = lane; j < n; j += 32) {
+              if (j == lane && fe == E) continue;
+              wok = wok && spin_u64(pf + j,
+                                    [E](unsigned long long v) { return (uint32_t)(v >> 32) == E; },
+                                    st, a.spin_ns);
+            }
+            if (!__all_sync(FULL, wok)) {
+              if (lane == 0) record_timeout(st, (int)W.rank, (int)it.unit, 3, E);
+              failed = true;
+              break;
+            }
+            res = gather_pieces<KIND>(xb, u.nbytes, n, lane, active);
+            have = true;
+          }
         }
       }
       if (!have) {
         // Top barrier: wait until every producer of the unit has notified epoch E,
-        // then (re)load with L1-bypassing loads.
+        // then load with L1-bypassing loads.
         if (!wait_producers(pf, n, E, st, a.spin_ns)) {
           if (lane == 0) record_timeout(st, (int)W.rank, (int)it.unit, retried ? 3 : 2, E);
           failed = true;
@@ -412,6 +521,10 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
           st_release_u32(a.cflag + u.cflag0 + (it.slot == COLL_SLOT_ALL ? 0u : it.slot), E);
       }
     }
+    if (pipelined && tagged && !nh_ready && !failed) {
+      nh = __reduce_add_sync(FULL, lane < (su.nbytes >> 4) ? tag_part(nx, lane) : 0u);
+      nh_ready = true;
+    }
     if (gw == 0 && lane == 0 && a.stamps && (uint32_t)i < a.stamp_cap)
       a.stamps[i + 1] = globaltimer();
   }
@@ -433,8 +546,9 @@ cudaError_t launch_zero_copy(int op, int dtype, int keep, const ZcArgs &a, int c
   const int kind = kind_of(op, dtype);
   const uint64_t total = (uint64_t)a.ntiles * a.n_epochs;
   if (total == 0) return cudaSuccess;
-  const int grid = (int)((uint64_t)ctas < total ? (uint64_t)ctas : total);
-  const dim3 block(512);
+  const uint64_t need = (total + 7) / 8;  // 8 warps per CTA
+  const int grid = (int)((uint64_t)ctas < need ? (uint64_t)ctas : need);
+  const dim3 block(256);
   switch (kind * 2 + (keep ? 1 : 0)) {
     case 0: zc_kernel<0, false><<<grid, block, 0, s>>>(a); break;
     case 1: zc_kernel<0, true><<<grid, block, 0, s>>>(a); break;

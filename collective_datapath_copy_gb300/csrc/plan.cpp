@@ -50,7 +50,7 @@ static int check_config(const coll_config_t &c) {
   if (c.protocol < 0 || c.protocol > 2) return COLL_EINVAL;
   if (c.datapath < 0 || c.datapath > 1) return COLL_EINVAL;
   if (c.zero_copy < 0 || c.zero_copy > 1) return COLL_EINVAL;
-  if (c.spec_check < 0 || c.spec_check > 1) return COLL_EINVAL;
+  if (c.spec_check < 0 || c.spec_check > 2) return COLL_EINVAL;
   if (c.unit_bytes != 0 && c.unit_bytes != 512) return COLL_EINVAL;
   if (c.warps_per_rank < 0 || c.ctas < 0) return COLL_EINVAL;
   if (c.tile_bytes < 0 || (c.tile_bytes % 16) != 0) return COLL_EINVAL;
@@ -61,7 +61,7 @@ static int check_config(const coll_config_t &c) {
 int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_in,
                  const uint64_t *in_len, const coll_seg_t *out_segs, size_t n_out,
                  const uint64_t *out_len, const coll_config_t *cfg_in, int max_warps,
-                 coll_compiled *out) {
+                 int num_sms, coll_compiled *out) {
   coll_compiled c;
   if (cfg_in) c.cfg = *cfg_in; else coll_config_default(&c.cfg);
   const coll_config_t &cfg = c.cfg;
@@ -180,7 +180,21 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
 
   if (!staged) {
     // ---------------- zero-copy: jobs and tiles
-    const uint64_t T = cfg.tile_bytes ? (uint64_t)cfg.tile_bytes : 32768u;
+    // One warp per tile. Default tile: the largest power of two (512 B .. 32 KiB) that
+    // still gives about four tiles per resident warp (32 per SM), so small collectives
+    // spread over every SM and large ones keep per-tile overhead low.
+    uint64_t T = cfg.tile_bytes ? (uint64_t)cfg.tile_bytes : 0;
+    if (!T) {
+      uint64_t job_bytes = 0;
+      for (auto &nm : names) {
+        const uint64_t njobs = (!sum || twoshot) ? 1u : nm.cons.size();
+        job_bytes += nm.count * es * njobs;
+      }
+      const uint64_t warps = (uint64_t)(num_sms > 0 ? num_sms : 152) * 32u;
+      const uint64_t want = job_bytes / (4u * warps);
+      T = 512;
+      while (T < 32768u && T * 2 <= want) T *= 2;
+    }
     for (auto &nm : names) {
       const uint64_t bytes = nm.count * es;
       const uint32_t job0 = (uint32_t)c.jobs.size();
@@ -356,7 +370,7 @@ extern "C" int coll_validate(int R, int op, int dtype, const coll_seg_t *in_segs
                              coll_plan_info_t *info) {
   coll_compiled c;
   int e = coll_compile(R, op, dtype, in_segs, n_in, in_len, out_segs, n_out, out_len, cfg,
-                       coll_default_max_warps(), &c);
+                       coll_default_max_warps(), coll_default_num_sms(), &c);
   if (e) return e;
   coll_fill_info(c, info);
   return COLL_OK;

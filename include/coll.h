@@ -74,6 +74,9 @@ extern "C" {
 #define COLL_SPEC_TAGGED 0  /* flag epochs AND a content tag per piece must match (sound) */
 #define COLL_SPEC_LITERAL 1 /* only sum of flag epochs == n * epoch (the pages' rule);
                                unsound under reordering, kept as an ablation            */
+#define COLL_SPEC_TAGGED_RELAXED 2 /* content tags only: notify without a release fence,
+                                      validate by re-hashing and re-load until the tags
+                                      match (bounded); no reliance on memory ordering   */
 
 /* Host-driven fault / timing injection (never a GPU fault; every wait stays bounded). */
 #define COLL_INJECT_SKIP_NOTIFY (1ull << 0) /* rank inject_rank never notifies          */
@@ -106,8 +109,9 @@ typedef struct {
   int32_t spec_check;     /* COLL_SPEC_*                                              */
   int32_t unit_bytes;     /* staged: bytes per synchronisation unit: 0 or 512         */
   int32_t warps_per_rank; /* staged: warps per emulated rank; 0 = one per unit        */
-  int32_t ctas;           /* zero-copy: CTAs in the grid; 0 = 2 x SM count             */
-  int32_t tile_bytes;     /* zero-copy: bytes per tile per destination; 0 = 32768     */
+  int32_t ctas;           /* zero-copy: CTAs (8 warps each) in the grid; 0 = 3 x SMs  */
+  int32_t tile_bytes;     /* zero-copy: bytes per warp tile, multiple of 16; 0 = auto
+                             (512 B .. 32 KiB, about four tiles per resident warp)     */
   uint64_t tma_min_bytes; /* zero-copy copy tiles with at least this many bytes use
                              the TMA bulk path; 0 = never                               */
   uint64_t spin_limit_ns; /* bound on every device wait; 0 = 2e9 (2 s)                  */
@@ -177,7 +181,9 @@ int coll_plan_info(coll_plan_t p, coll_plan_info_t *info);
  * bytes (stride 0 overwrites). A rank with no segments may pass NULL.
  * Staged plans run one cooperative persistent launch for all epochs; zero-copy plans run
  * one ordinary launch. Returns after enqueueing; device-side failures are reported by
- * coll_status. Synchronous errors: COLL_EINVAL (n_epochs < 1, in_pool < 1, NULL pointer
+ * coll_status. Zero-copy runs may be captured into a CUDA graph (the plan's tables are
+ * fixed; the pointers and strides given here are baked into the captured launch).
+ * Synchronous errors: COLL_EINVAL (n_epochs < 1, in_pool < 1, NULL pointer
  * for a rank that has segments), COLL_EALIGN, COLL_EOVERLAP, COLL_ECUDA. Buffers must stay
  * live and unmodified until the stream has passed the run. */
 int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_epochs,

@@ -271,7 +271,15 @@ def test_decode_allreduce_10000_epochs_spec_equals_barrier_under_stagger():
                       ("spec", dict(protocol="spec")),
                       ("spec-stagger", dict(protocol="spec", inject="stagger", inject_seed=2,
                                             inject_prob_ppm=100000, inject_max_ns=20000,
-                                            inject_start_ns=5000))]:
+                                            inject_start_ns=5000)),
+                      ("spec-relaxed", dict(protocol="spec", spec_check="relaxed")),
+                      ("spec-relaxed-stagger", dict(protocol="spec", spec_check="relaxed",
+                                                    inject="stagger", inject_seed=3,
+                                                    inject_prob_ppm=100000, inject_max_ns=20000,
+                                                    inject_start_ns=5000)),
+                      ("spec-twoshot-stagger", dict(protocol="spec", datapath="twoshot",
+                                                    inject="stagger", inject_seed=4,
+                                                    inject_prob_ppm=100000, inject_max_ns=20000))]:
         plan = cdc.Plan(nm, **cfg)
         outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
         plan.run(ins, outs, n_epochs=E, in_epoch_stride=n * 2, in_pool=pool,
@@ -281,7 +289,7 @@ def test_decode_allreduce_10000_epochs_spec_equals_barrier_under_stagger():
         assert _check_epochs(outs, expect, E, pool) == 0, name
         res[name] = (outs, st)
         plan.free()
-    for name in ("dual", "spec", "spec-stagger"):
+    for name in res:
         for a, b in zip(res[name][0], res["barrier"][0]):
             assert torch.equal(a, b)
     assert res["spec"][1]["spec_checks"] == E * R * 16
@@ -296,7 +304,7 @@ def test_speculation_with_adversarial_pause_tagged_is_exact_literal_is_not():
     ins, expect = _decode_case(R, n, pool)
     nm = namings.allreduce(R, n, "bf16")
     bad = {}
-    for check in ("tagged", "literal"):
+    for check in ("tagged", "relaxed", "literal"):
         plan = cdc.Plan(nm, protocol="spec", spec_check=check, inject="spec_pause", inject_rank=2,
                         inject_max_ns=200000, inject_pause_ns=20000)
         outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
@@ -308,6 +316,8 @@ def test_speculation_with_adversarial_pause_tagged_is_exact_literal_is_not():
         plan.free()
     assert bad["tagged"][0] == 0
     assert bad["tagged"][1] > 0
+    assert bad["relaxed"][0] == 0
+    assert bad["relaxed"][1] > 0
     assert bad["literal"][0] > 0
 
 
@@ -421,3 +431,31 @@ def test_sweep_256mib_sampled(kind):
     plan.free()
     del outs, ins
     torch.cuda.empty_cache()
+
+
+def test_zero_copy_plan_replays_inside_a_cuda_graph():
+    R, n = 8, 1 << 16
+    rng = synth.seeded_rng(81)
+    xs = [synth.uniform_bf16(rng, n) for _ in range(R)]
+    nm = namings.allreduce(R, n, "bf16")
+    plan = cdc.Plan(nm, zero_copy=1, datapath="twoshot")
+    ins = [to_dev(x, "bf16") for x in xs]
+    outs = [torch.zeros(n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        plan.run(ins, outs)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for o in outs:
+        o.zero_()
+    with torch.cuda.graph(g):
+        plan.run(ins, outs)
+    g.replay()
+    torch.cuda.synchronize()
+    assert plan.status()["code"] == 0
+    want = collectives.allreduce(xs, "bf16")[0]
+    for o in outs:
+        assert bits_equal(from_dev(o, "bf16"), want)
+    plan.free()
