@@ -232,9 +232,26 @@ extern "C" int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_
     a.in_pool = in_pool;
     a.in_stride = in_epoch_stride;
     a.out_stride = out_epoch_stride;
-    const int ctas = c.cfg.ctas ? c.cfg.ctas : 3 * p->num_sms;
-    const int keep = (c.op == COLL_OP_SUM && c.cfg.datapath == COLL_DP_ONESHOT) ? 1 : 0;
-    err = coll::launch_zero_copy(c.op, c.dtype, keep, a, ctas, s);
+    a.st = p->d_status;
+    a.spin_ns = c.cfg.spin_limit_ns ? c.cfg.spin_limit_ns : 2000000000ull;
+    bool bulk = c.bulk;
+    if (bulk) {  // the bulk copies need 16-byte-aligned bases and strides at run time
+      for (int r = 0; r < R && bulk; ++r) {
+        if (c.in_used[r] && ((uintptr_t)in[r] & 15u)) bulk = false;
+        if (c.out_used[r] && ((uintptr_t)out[r] & 15u)) bulk = false;
+      }
+      if (((uint64_t)in_epoch_stride & 15u) || ((uint64_t)out_epoch_stride & 15u)) bulk = false;
+    }
+    if (bulk) {
+      a.slot_bytes = c.bulk_slot;
+      a.stages = c.bulk_stages;
+      a.maxsrc = c.bulk_maxsrc;
+      err = coll::launch_bulk(c.op, c.dtype, a, c.cfg.ctas ? c.cfg.ctas : p->num_sms, s);
+    } else {
+      const int ctas = c.cfg.ctas ? c.cfg.ctas : 3 * p->num_sms;
+      const int keep = (c.op == COLL_OP_SUM && c.cfg.datapath == COLL_DP_ONESHOT) ? 1 : 0;
+      err = coll::launch_zero_copy(c.op, c.dtype, keep, a, ctas, s);
+    }
   } else {
     if (p->epochs_issued + (uint64_t)n_epochs >= 0xFFFFFFF0ull) return COLL_EINVAL;  // reset first
     coll::EngArgs a;

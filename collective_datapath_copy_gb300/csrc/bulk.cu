@@ -1,0 +1,227 @@
+// Zero-copy datapath, bulk-copy (TMA) variant for large 16-byte-aligned plans, sm_103a.
+//
+// One persistent CTA per SM. Warp 0 is the producer: for each tile it issues one
+// cp.async.bulk (global -> shared, completion on an mbarrier) per producer segment into a
+// ring of shared-memory stages. Warps 1..8 are consumers: they wait for a stage, reduce the
+// staged pieces in the plan's order (binary32, one RNE to bf16) or take the single piece
+// (copy), store the result to every destination with streaming 16-byte stores, and release
+// the stage. The ring keeps up to `stages` tiles of loads in flight per SM independently of
+// register pressure, which is what a streaming copy/reduce needs to reach HBM bandwidth.
+//
+// Every mbarrier wait is bounded by the plan's spin limit; on expiry the CTA records
+// COLL_ETIMEDOUT in the plan status, waits (bounded) for the bulk copies it issued, and
+// returns.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "atom.cuh"
+#include "engine.cuh"
+
+namespace coll {
+
+namespace {
+
+constexpr uint32_t kConsumerWarps = 8;
+constexpr uint32_t kThreads = 32 * (kConsumerWarps + 1);
+
+struct StageHdr {
+  char *dst[COLL_BULK_MAX_DST];
+  uint32_t nbytes, nsrc, ndst, pad;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity; false on timeout or abort.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit,
+                                          const volatile uint32_t *abort_flag) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 15u) {
+      const uint64_t now = globaltimer();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > limit) return false;
+      if (*abort_flag) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t bytes,
+                                          uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint4 lds_v4(const void *p) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(smem_u32(p)));
+  return r;
+}
+
+__device__ void bulk_timeout(coll_dev_status_t *st, uint32_t tile) {
+  if (atomicCAS(&st->status, 0, COLL_ETIMEDOUT) == 0) {
+    st->fail_rank = -1;
+    st->fail_unit = (int)tile;
+    st->fail_where = 5;
+    st->fail_epoch = 0;
+  }
+}
+
+// KIND: 0 copy, 1 sum of bf16, 2 sum of f32.
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ volatile uint32_t s_abort;
+  __shared__ uint32_t s_issued;
+  const uint32_t S = a.stages;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+  uint64_t *empty = full + S;
+  StageHdr *hdr = reinterpret_cast<StageHdr *>(empty + S);
+  const uint32_t head = ((16u * S + (uint32_t)sizeof(StageHdr) * S) + 127u) & ~127u;
+  unsigned char *data = smem + head;
+  const uint32_t stage_bytes = a.maxsrc * a.slot_bytes;
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+  const uint64_t total = (uint64_t)a.ntiles * a.n_epochs;
+
+  if (threadIdx.x == 0) {
+    for (uint32_t s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    s_abort = 0;
+    s_issued = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  uint32_t consumed = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t k = 0;
+      for (uint64_t t = blockIdx.x; t < total; t += gridDim.x, ++k) {
+        const uint32_t s = k % S;
+        if (!mbar_wait(&empty[s], ((k / S) & 1u) ^ 1u, a.spin_ns, &s_abort)) {
+          bulk_timeout(a.st, (uint32_t)t);
+          s_abort = 1;
+          break;
+        }
+        const uint32_t e = (uint32_t)(t / a.ntiles);
+        const coll_tile_t tile = a.tiles[t - (uint64_t)e * a.ntiles];
+        const coll_job_t job = a.jobs[tile.job];
+        const int64_t ioff = (int64_t)(e % (uint32_t)a.in_pool) * a.in_stride + (int64_t)tile.start;
+        const int64_t ooff = (int64_t)e * a.out_stride + (int64_t)tile.start;
+        StageHdr &h = hdr[s];
+        h.nbytes = tile.nbytes;
+        h.nsrc = job.nsrc;
+        h.ndst = job.ndst;
+        for (uint32_t d = 0; d < job.ndst; ++d) {
+          const coll_ref_t r = a.refs[job.dst0 + d];
+          h.dst[d] = a.ptr.out[r.rank] + r.off + ooff;
+        }
+        mbar_expect_tx(&full[s], job.nsrc * tile.nbytes);
+        unsigned char *sd = data + (size_t)s * stage_bytes;
+        for (uint32_t j = 0; j < job.nsrc; ++j) {
+          const coll_ref_t r = a.refs[job.src0 + j];
+          bulk_load(sd + (size_t)j * a.slot_bytes, a.ptr.in[r.rank] + r.off + ioff, tile.nbytes,
+                    &full[s]);
+        }
+        s_issued = k + 1;
+      }
+    }
+  } else {
+    const uint32_t ctid = threadIdx.x - 32;  // consumer thread index
+    uint32_t k = 0;
+    for (uint64_t t = blockIdx.x; t < total; t += gridDim.x, ++k) {
+      const uint32_t s = k % S;
+      if (!mbar_wait(&full[s], (k / S) & 1u, a.spin_ns, &s_abort)) {
+        if (lane == 0) bulk_timeout(a.st, (uint32_t)t);
+        s_abort = 1;
+        break;
+      }
+      const StageHdr &h = hdr[s];
+      const uint32_t nvec = h.nbytes >> 4, nsrc = h.nsrc, ndst = h.ndst;
+      const unsigned char *sd = data + (size_t)s * stage_bytes;
+      for (uint32_t v = ctid; v < nvec; v += 32 * kConsumerWarps) {
+        uint4 r;
+        if constexpr (KIND == 0) {
+          r = lds_v4(sd + (size_t)v * 16);
+        } else {
+          Vec16Acc<KIND - 1> acc;
+          acc.init(lds_v4(sd + (size_t)v * 16));
+          for (uint32_t j = 1; j < nsrc; ++j) acc.add(lds_v4(sd + (size_t)j * a.slot_bytes + (size_t)v * 16));
+          r = acc.pack();
+        }
+        for (uint32_t d = 0; d < ndst; ++d) st_cs_v4(h.dst[d] + (size_t)v * 16, r);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      consumed = k + 1;
+    }
+  }
+  __syncthreads();
+  if (s_abort && threadIdx.x == 32) {
+    // bulk copies issued but not consumed may still be landing in this CTA's shared
+    // memory: wait for them (bounded) before the CTA exits
+    const volatile uint32_t never = 0;
+    for (uint32_t k = consumed; k < s_issued; ++k)
+      mbar_wait(&full[k % S], (k / S) & 1u, 100000000ull, &never);
+  }
+}
+
+}  // namespace
+
+uint32_t bulk_smem_bytes(uint32_t stages, uint32_t maxsrc, uint32_t slot_bytes) {
+  const uint32_t head = ((16u * stages + (uint32_t)sizeof(StageHdr) * stages) + 127u) & ~127u;
+  return head + stages * maxsrc * slot_bytes;
+}
+
+cudaError_t launch_bulk(int op, int dtype, const ZcArgs &a, int ctas, cudaStream_t s) {
+  const uint64_t total = (uint64_t)a.ntiles * a.n_epochs;
+  if (total == 0) return cudaSuccess;
+  const int grid = (int)((uint64_t)ctas < total ? (uint64_t)ctas : total);
+  const uint32_t smem = bulk_smem_bytes(a.stages, a.maxsrc, a.slot_bytes);
+  const void *fn;
+  if (op == COLL_OP_COPY) fn = (const void *)bulk_kernel<0>;
+  else if (dtype == COLL_BF16) fn = (const void *)bulk_kernel<1>;
+  else fn = (const void *)bulk_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  void *args[] = {(void *)&a};
+  return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, smem, s);
+}
+
+}  // namespace coll

@@ -10,6 +10,8 @@
 #define COLL_MAX_FANIN 256   // producers of one name
 #define COLL_MAX_FANOUT 256  // consumers of one name
 #define COLL_WARP_VEC 32     // lanes per warp, one 16-byte vector each per step
+#define COLL_BULK_MAX_SRC 8  // bulk (TMA) zero-copy path: producers per job
+#define COLL_BULK_MAX_DST 8  // bulk (TMA) zero-copy path: consumers per job
 
 // (rank, byte offset) of one segment inside that rank's buffer.
 struct coll_ref_t {
@@ -91,6 +93,10 @@ struct coll_compiled {
   std::vector<coll_unit_t> units;
   std::vector<coll_item_t> sitems, citems;
   std::vector<coll_warp_t> warps;
+  bool bulk = false;          // zero-copy tiles sized for the bulk (TMA) kernel
+  uint32_t bulk_slot = 0;     // bytes of one staged piece (= tile size)
+  uint32_t bulk_maxsrc = 0;   // slots per stage
+  uint32_t bulk_stages = 0;   // stages in the shared-memory ring
   uint64_t xpar_bytes = 0;  // exchange bytes per parity
   uint32_t n_pflag = 0, n_cflag = 0;
   uint64_t n_names = 0, min_bytes = 0;

@@ -23,6 +23,12 @@ struct ZcArgs {
   int32_t in_pool;
   int32_t pad;
   int64_t in_stride, out_stride;
+  coll_dev_status_t *st;  // bulk kernel: timeout reporting
+  uint64_t spin_ns;       // bulk kernel: bound on every mbarrier wait
+  uint32_t slot_bytes;    // bulk kernel: bytes per staged piece
+  uint32_t stages;        // bulk kernel: ring depth
+  uint32_t maxsrc;        // bulk kernel: slots per stage
+  uint32_t pad2;
 };
 
 struct EngArgs {
@@ -62,6 +68,10 @@ struct EngArgs {
 // Zero-copy: one ordinary launch over all tiles of all epochs.
 cudaError_t launch_zero_copy(int op, int dtype, int oneshot_reuse, const ZcArgs &a, int ctas,
                              cudaStream_t s);
+
+// Zero-copy, bulk (TMA) ring: one launch of `ctas` persistent CTAs (one per SM).
+cudaError_t launch_bulk(int op, int dtype, const ZcArgs &a, int ctas, cudaStream_t s);
+uint32_t bulk_smem_bytes(uint32_t stages, uint32_t maxsrc, uint32_t slot_bytes);
 
 // Staged Stage/Notify/Consume engine: one cooperative launch of nwarps one-warp CTAs.
 cudaError_t launch_engine(int op, int dtype, const EngArgs &a, cudaStream_t s);

@@ -183,15 +183,41 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
     // One warp per tile. Default tile: the largest power of two (512 B .. 32 KiB) that
     // still gives about four tiles per resident warp (32 per SM), so small collectives
     // spread over every SM and large ones keep per-tile overhead low.
+    uint64_t job_bytes = 0;
+    uint32_t maxsrc = 0, maxdst = 0;
+    bool aligned = true;
+    for (auto &nm : names) {
+      const uint64_t njobs = (!sum || twoshot) ? 1u : nm.cons.size();
+      job_bytes += nm.count * es * njobs;
+      maxsrc = std::max<uint32_t>(maxsrc, sum ? (uint32_t)nm.prod.size() : 1u);
+      maxdst = std::max<uint32_t>(maxdst, (!sum || twoshot) ? (uint32_t)nm.cons.size() : 1u);
+      if ((nm.count * es) & 15u) aligned = false;
+    }
+    for (size_t i = 0; i < n_in + n_out && aligned; ++i) {
+      const coll_seg_t &sg = i < n_in ? in_segs[i] : out_segs[i - n_in];
+      if ((sg.offset * es) & 15u) aligned = false;
+    }
+    const uint64_t sms = (uint64_t)(num_sms > 0 ? num_sms : 152);
+    // Large aligned plans use the bulk (TMA) ring: one CTA per SM, tiles of
+    // 32 KiB / (producers rounded up to a power of two), at least four tiles per CTA.
+    const uint64_t bulk_min = cfg.tma_min_bytes ? cfg.tma_min_bytes : (4ull << 20);
+    c.bulk = aligned && maxsrc >= 1 && maxsrc <= COLL_BULK_MAX_SRC &&
+             maxdst <= COLL_BULK_MAX_DST && job_bytes >= bulk_min && !cfg.tile_bytes;
     uint64_t T = cfg.tile_bytes ? (uint64_t)cfg.tile_bytes : 0;
-    if (!T) {
-      uint64_t job_bytes = 0;
-      for (auto &nm : names) {
-        const uint64_t njobs = (!sum || twoshot) ? 1u : nm.cons.size();
-        job_bytes += nm.count * es * njobs;
-      }
-      const uint64_t warps = (uint64_t)(num_sms > 0 ? num_sms : 152) * 32u;
-      const uint64_t want = job_bytes / (4u * warps);
+    if (c.bulk) {
+      uint32_t p2 = 1;
+      while (p2 < maxsrc) p2 *= 2;
+      const uint64_t cap = 32768u / p2;
+      const uint64_t want = job_bytes / (4u * sms);
+      T = 1024;
+      while (T < cap && T * 2 <= want) T *= 2;
+      c.bulk_slot = (uint32_t)T;
+      c.bulk_maxsrc = maxsrc;
+      c.bulk_stages = 4;
+    } else if (!T) {
+      // One warp per tile: the largest power of two (512 B .. 32 KiB) that still gives
+      // about four tiles per resident warp (32 per SM).
+      const uint64_t want = job_bytes / (4u * sms * 32u);
       T = 512;
       while (T < 32768u && T * 2 <= want) T *= 2;
     }

@@ -112,8 +112,10 @@ typedef struct {
   int32_t ctas;           /* zero-copy: CTAs (8 warps each) in the grid; 0 = 3 x SMs  */
   int32_t tile_bytes;     /* zero-copy: bytes per warp tile, multiple of 16; 0 = auto
                              (512 B .. 32 KiB, about four tiles per resident warp)     */
-  uint64_t tma_min_bytes; /* zero-copy copy tiles with at least this many bytes use
-                             the TMA bulk path; 0 = never                               */
+  uint64_t tma_min_bytes; /* zero-copy plans whose jobs move at least this many bytes,
+                             with 16-byte-aligned segments and <= 8 producers and
+                             consumers per job, use the bulk-copy (TMA) ring kernel;
+                             0 = 4 MiB; UINT64_MAX = never                             */
   uint64_t spin_limit_ns; /* bound on every device wait; 0 = 2e9 (2 s)                  */
   uint32_t record_stamps; /* staged: record a %globaltimer stamp per epoch (capacity
                              stamp_capacity epochs; later epochs are not stamped)      */

@@ -459,3 +459,65 @@ def test_zero_copy_plan_replays_inside_a_cuda_graph():
     for o in outs:
         assert bits_equal(from_dev(o, "bf16"), want)
     plan.free()
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_bulk_ring_on_small_aligned_namings(seed):
+    # force the bulk-copy (TMA) ring on small random namings (segments scaled to 16 bytes)
+    op = "copy" if seed % 4 == 0 else "sum"
+    dtype = "bf16" if seed % 3 else "f32"
+    k = 8 if dtype == "bf16" else 4
+    R = 1 + seed % 6
+    rng = synth.seeded_rng(1500 + seed)
+    il, i, ol, o = synth.random_naming(rng, R, 300, 4, 4, op)
+    il = [x * k for x in il]
+    ol = [x * k for x in ol]
+    i = [(r, off * k, c * k, nmv) for (r, off, c, nmv) in i]
+    o = [(r, off * k, c * k, nmv) for (r, off, c, nmv) in o]
+    nm = namings.Naming(R, op, dtype, il, namings.segs(i), ol, namings.segs(o))
+    xs = [gen("normal", rng, n, dtype) for n in il]
+    got, init = run_once(nm, xs, zero_copy=1, tma_min_bytes=1,
+                         datapath="twoshot" if seed % 2 else "oneshot")
+    want = oracle_outputs(nm, xs, init)
+    for g, w in zip(got, want):
+        assert bits_equal(g, w)
+
+
+def test_bulk_ring_epochs_over_an_input_pool():
+    R, n, pool, E = 8, 3 * 4096 + 8, 3, 5
+    rng = synth.seeded_rng(82)
+    pool_np = [[synth.normal_bf16(rng, n) for _ in range(R)] for _ in range(pool)]
+    ins = [torch.stack([to_dev(pool_np[p][r], "bf16") for p in range(pool)]).contiguous()
+           for r in range(R)]
+    nm = namings.allreduce(R, n, "bf16")
+    for dp in ("twoshot", "oneshot"):
+        plan = cdc.Plan(nm, zero_copy=1, tma_min_bytes=1, datapath=dp)
+        outs = [torch.zeros(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+        plan.run(ins, outs, n_epochs=E, in_epoch_stride=2 * n, in_pool=pool,
+                 out_epoch_stride=2 * n)
+        assert plan.status()["code"] == 0
+        for e in range(E):
+            want = collectives.allreduce(pool_np[e % pool], "bf16")[0]
+            for r in range(R):
+                assert bits_equal(from_dev(outs[r][e], "bf16"), want), (dp, e, r)
+        plan.free()
+
+
+def test_bulk_plan_with_misaligned_buffers_falls_back_and_stays_exact():
+    R, n = 4, 1 << 20
+    rng = synth.seeded_rng(83)
+    xs = [synth.normal_bf16(rng, n) for _ in range(R)]
+    nm = namings.allreduce(R, n, "bf16")
+    plan = cdc.Plan(nm, zero_copy=1, datapath="twoshot")
+    big_in = [torch.zeros(n + 8, dtype=torch.int16, device="cuda") for _ in range(R)]
+    big_out = [torch.zeros(n + 8, dtype=torch.int16, device="cuda") for _ in range(R)]
+    ins = [b[1:n + 1] for b in big_in]  # 2-byte offset: not 16-byte aligned
+    outs = [b[1:n + 1] for b in big_out]
+    for t, x in zip(ins, xs):
+        t.copy_(to_dev(x, "bf16"))
+    plan.run(ins, outs)
+    assert plan.status()["code"] == 0
+    want = collectives.allreduce(xs, "bf16")[0]
+    for o in outs:
+        assert bits_equal(from_dev(o, "bf16"), want)
+    plan.free()
