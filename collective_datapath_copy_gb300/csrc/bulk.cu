@@ -167,7 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
     uint32_t k = 0;
     for (uint64_t t = blockIdx.x; t < total; t += gridDim.x, ++k) {
       const uint32_t s = k % S;
-      if (!mbar_wait(&full[s], (k / S) & 1u, a.spin_ns, &s_abort)) {
+      const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&full[s], (k / S) & 1u, a.spin_ns, &s_abort));
+      if (!ok) {
         if (lane == 0) bulk_timeout(a.st, (uint32_t)t);
         s_abort = 1;
         break;

@@ -67,23 +67,31 @@ __global__ void __launch_bounds__(256, 3) zc_kernel(const ZcArgs a) {
     const bool slow = __any_sync(FULL, mis != 0) || nsrc > 32 || ndst > 32;
     if (!slow) {
       const uint32_t nvec = tile.nbytes >> 4;
+      // The vector loops are warp-uniform (every lane iterates; loads and stores are
+      // predicated) because they fetch pointers with full-warp shuffles.
       if constexpr (KIND == 0) {
         const char *s0 = (const char *)__shfl_sync(FULL, (uintptr_t)sp, 0);
         constexpr uint32_t U = 4;
-        for (uint32_t base = lane; base < nvec; base += 32 * U) {
+        for (uint32_t base = 0; base < nvec; base += 32 * U) {
           uint4 x[U];
 #pragma unroll
-          for (uint32_t u = 0; u < U; ++u)
-            if (base + 32 * u < nvec) x[u] = zc_load<KIND, KEEP>(s0 + (size_t)(base + 32 * u) * 16);
+          for (uint32_t u = 0; u < U; ++u) {
+            const uint32_t idx = base + 32 * u + lane;
+            if (idx < nvec) x[u] = zc_load<KIND, KEEP>(s0 + (size_t)idx * 16);
+          }
           for (uint32_t d = 0; d < ndst; ++d) {
             char *q = (char *)__shfl_sync(FULL, (uintptr_t)dp, d);
 #pragma unroll
-            for (uint32_t u = 0; u < U; ++u)
-              if (base + 32 * u < nvec) st_cs_v4(q + (size_t)(base + 32 * u) * 16, x[u]);
+            for (uint32_t u = 0; u < U; ++u) {
+              const uint32_t idx = base + 32 * u + lane;
+              if (idx < nvec) st_cs_v4(q + (size_t)idx * 16, x[u]);
+            }
           }
         }
       } else {
-        for (uint32_t v = lane; v < nvec; v += 32) {
+        for (uint32_t base = 0; base < nvec; base += 32) {
+          const uint32_t v = base + lane;
+          const bool act = v < nvec;
           Vec16Acc<KIND - 1> acc;
           for (uint32_t k0 = 0; k0 < nsrc; k0 += 8) {
             uint4 x[8];
@@ -91,18 +99,20 @@ __global__ void __launch_bounds__(256, 3) zc_kernel(const ZcArgs a) {
 #pragma unroll
             for (uint32_t k = 0; k < 8; ++k) {
               const char *p = (const char *)__shfl_sync(FULL, (uintptr_t)sp, (k0 + k) & 31u);
-              if (k < kn) x[k] = zc_load<KIND, KEEP>(p + (size_t)v * 16);
+              if (k < kn && act) x[k] = zc_load<KIND, KEEP>(p + (size_t)v * 16);
             }
+            if (act) {
 #pragma unroll
-            for (uint32_t k = 0; k < 8; ++k)
-              if (k < kn) {
-                if (k0 + k == 0) acc.init(x[k]); else acc.add(x[k]);
-              }
+              for (uint32_t k = 0; k < 8; ++k)
+                if (k < kn) {
+                  if (k0 + k == 0) acc.init(x[k]); else acc.add(x[k]);
+                }
+            }
           }
-          const uint4 r = acc.pack();
+          const uint4 r = act ? acc.pack() : make_uint4(0, 0, 0, 0);
           for (uint32_t d = 0; d < ndst; ++d) {
             char *q = (char *)__shfl_sync(FULL, (uintptr_t)dp, d);
-            st_cs_v4(q + (size_t)v * 16, r);
+            if (act) st_cs_v4(q + (size_t)v * 16, r);
           }
         }
       }
