@@ -22,6 +22,7 @@ namespace coll {
 namespace {
 
 constexpr uint32_t kConsumerWarps = 8;
+constexpr unsigned FULLW = 0xFFFFFFFFu;
 constexpr uint32_t kThreads = 32 * (kConsumerWarps + 1);
 
 struct StageHdr {
@@ -84,14 +85,6 @@ __device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t
       : "memory");
 }
 
-__device__ __forceinline__ uint4 lds_v4(const void *p) {
-  uint4 r;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "r"(smem_u32(p)));
-  return r;
-}
-
 __device__ void bulk_timeout(coll_dev_status_t *st, uint32_t tile) {
   if (atomicCAS(&st->status, 0, COLL_ETIMEDOUT) == 0) {
     st->fail_rank = -1;
@@ -130,44 +123,93 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
 
   uint32_t consumed = 0;
   if (warp == 0) {
-    if (lane == 0) {
-      uint32_t k = 0;
-      for (uint64_t t = blockIdx.x; t < total; t += gridDim.x, ++k) {
-        const uint32_t s = k % S;
-        if (!mbar_wait(&empty[s], ((k / S) & 1u) ^ 1u, a.spin_ns, &s_abort)) {
-          bulk_timeout(a.st, (uint32_t)t);
-          s_abort = 1;
-          break;
-        }
+    // Producer warp. Tiles are resolved 32 at a time, one per lane (tile, job, and the
+    // source/destination pointers, all lanes in parallel), so descriptor fetches cost
+    // three memory round trips per 32 tiles; lane 0 then issues each tile's bulk loads.
+    uint32_t k = 0;
+    bool stop = false;
+    for (uint64_t t0 = blockIdx.x; t0 < total && !stop; t0 += 32ull * gridDim.x) {
+      const uint64_t t = t0 + (uint64_t)lane * gridDim.x;
+      const bool have = t < total;
+      uint32_t nbytes = 0, nsrc = 0, ndst = 0;
+      const char *sp[COLL_BULK_MAX_SRC];
+      char *dp[COLL_BULK_MAX_DST];
+      if (have) {
         const uint32_t e = (uint32_t)(t / a.ntiles);
         const coll_tile_t tile = a.tiles[t - (uint64_t)e * a.ntiles];
         const coll_job_t job = a.jobs[tile.job];
         const int64_t ioff = (int64_t)(e % (uint32_t)a.in_pool) * a.in_stride + (int64_t)tile.start;
         const int64_t ooff = (int64_t)e * a.out_stride + (int64_t)tile.start;
+        nbytes = tile.nbytes;
+        nsrc = job.nsrc;
+        ndst = job.ndst;
+#pragma unroll
+        for (uint32_t j = 0; j < COLL_BULK_MAX_SRC; ++j) {
+          sp[j] = nullptr;
+          if (j < nsrc) {
+            const coll_ref_t r = a.refs[job.src0 + j];
+            sp[j] = a.ptr.in[r.rank] + r.off + ioff;
+          }
+        }
+#pragma unroll
+        for (uint32_t d = 0; d < COLL_BULK_MAX_DST; ++d) {
+          dp[d] = nullptr;
+          if (d < ndst) {
+            const coll_ref_t r = a.refs[job.dst0 + d];
+            dp[d] = a.ptr.out[r.rank] + r.off + ooff;
+          }
+        }
+      } else {
+#pragma unroll
+        for (uint32_t j = 0; j < COLL_BULK_MAX_SRC; ++j) sp[j] = nullptr;
+#pragma unroll
+        for (uint32_t d = 0; d < COLL_BULK_MAX_DST; ++d) dp[d] = nullptr;
+      }
+      const uint32_t batch = __popc(__ballot_sync(FULLW, have));
+      for (uint32_t i = 0; i < batch; ++i, ++k) {
+        const uint32_t s = k % S;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&empty[s], ((k / S) & 1u) ^ 1u, a.spin_ns, &s_abort);
+        ok = __shfl_sync(FULLW, ok, 0);
+        if (!ok) {
+          if (lane == 0) {
+            bulk_timeout(a.st, (uint32_t)(t0 + (uint64_t)i * gridDim.x));
+            s_abort = 1;
+          }
+          stop = true;
+          break;
+        }
+        const uint32_t nb = __shfl_sync(FULLW, nbytes, i);
+        const uint32_t ns = __shfl_sync(FULLW, nsrc, i);
+        const uint32_t nd = __shfl_sync(FULLW, ndst, i);
         StageHdr &h = hdr[s];
-        h.nbytes = tile.nbytes;
-        h.nsrc = job.nsrc;
-        h.ndst = job.ndst;
-        for (uint32_t d = 0; d < job.ndst; ++d) {
-          const coll_ref_t r = a.refs[job.dst0 + d];
-          h.dst[d] = a.ptr.out[r.rank] + r.off + ooff;
+#pragma unroll
+        for (uint32_t d = 0; d < COLL_BULK_MAX_DST; ++d) {
+          char *q = (char *)__shfl_sync(FULLW, (uintptr_t)dp[d], i);
+          if (lane == 0 && d < nd) h.dst[d] = q;
         }
-        mbar_expect_tx(&full[s], job.nsrc * tile.nbytes);
+        if (lane == 0) {
+          h.nbytes = nb;
+          h.nsrc = ns;
+          h.ndst = nd;
+          mbar_expect_tx(&full[s], ns * nb);
+        }
         unsigned char *sd = data + (size_t)s * stage_bytes;
-        for (uint32_t j = 0; j < job.nsrc; ++j) {
-          const coll_ref_t r = a.refs[job.src0 + j];
-          bulk_load(sd + (size_t)j * a.slot_bytes, a.ptr.in[r.rank] + r.off + ioff, tile.nbytes,
-                    &full[s]);
+#pragma unroll
+        for (uint32_t j = 0; j < COLL_BULK_MAX_SRC; ++j) {
+          const char *p = (const char *)__shfl_sync(FULLW, (uintptr_t)sp[j], i);
+          if (lane == 0 && j < ns) bulk_load(sd + (size_t)j * a.slot_bytes, p, nb, &full[s]);
         }
-        s_issued = k + 1;
+        if (lane == 0) s_issued = k + 1;
       }
     }
   } else {
     const uint32_t ctid = threadIdx.x - 32;  // consumer thread index
+    const uint32_t slot_vec = a.slot_bytes >> 4;
     uint32_t k = 0;
     for (uint64_t t = blockIdx.x; t < total; t += gridDim.x, ++k) {
       const uint32_t s = k % S;
-      const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&full[s], (k / S) & 1u, a.spin_ns, &s_abort));
+      const bool ok = __all_sync(FULLW, mbar_wait(&full[s], (k / S) & 1u, a.spin_ns, &s_abort));
       if (!ok) {
         if (lane == 0) bulk_timeout(a.st, (uint32_t)t);
         s_abort = 1;
@@ -175,15 +217,21 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
       }
       const StageHdr &h = hdr[s];
       const uint32_t nvec = h.nbytes >> 4, nsrc = h.nsrc, ndst = h.ndst;
-      const unsigned char *sd = data + (size_t)s * stage_bytes;
+      const uint4 *sd = reinterpret_cast<const uint4 *>(data + (size_t)s * stage_bytes);
       for (uint32_t v = ctid; v < nvec; v += 32 * kConsumerWarps) {
         uint4 r;
         if constexpr (KIND == 0) {
-          r = lds_v4(sd + (size_t)v * 16);
+          r = sd[v];
         } else {
+          uint4 x[COLL_BULK_MAX_SRC];
+#pragma unroll
+          for (uint32_t j = 0; j < COLL_BULK_MAX_SRC; ++j)
+            if (j < nsrc) x[j] = sd[(size_t)j * slot_vec + v];
           Vec16Acc<KIND - 1> acc;
-          acc.init(lds_v4(sd + (size_t)v * 16));
-          for (uint32_t j = 1; j < nsrc; ++j) acc.add(lds_v4(sd + (size_t)j * a.slot_bytes + (size_t)v * 16));
+          acc.init(x[0]);
+#pragma unroll
+          for (uint32_t j = 1; j < COLL_BULK_MAX_SRC; ++j)
+            if (j < nsrc) acc.add(x[j]);
           r = acc.pack();
         }
         for (uint32_t d = 0; d < ndst; ++d) st_cs_v4(h.dst[d] + (size_t)v * 16, r);

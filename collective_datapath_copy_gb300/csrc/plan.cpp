@@ -213,7 +213,9 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
       while (T < cap && T * 2 <= want) T *= 2;
       c.bulk_slot = (uint32_t)T;
       c.bulk_maxsrc = maxsrc;
-      c.bulk_stages = 4;
+      // as many stages as fit in 192 KiB of shared memory (2..8)
+      const uint64_t stage = (uint64_t)maxsrc * T;
+      c.bulk_stages = (uint32_t)std::max<uint64_t>(2, std::min<uint64_t>(8, (192u << 10) / stage));
     } else if (!T) {
       // One warp per tile: the largest power of two (512 B .. 32 KiB) that still gives
       // about four tiles per resident warp (32 per SM).
