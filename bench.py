@@ -117,6 +117,19 @@ def _decode_inputs(torch, dev):
     return pool_np, host, ins
 
 
+def make_flush(torch, dev):
+    """L2 flush between timed steps: write a 256 MiB buffer (> L2), then read another
+    256 MiB buffer so the dirty lines of the write are written back before the timed step
+    starts rather than during it."""
+    wbuf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    rbuf = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def flush():
+        wbuf.fill_(1)
+        rbuf.max()
+    return flush
+
+
 def _time_steps(torch, fn, steps, warmup, flush, stream):
     """Per-step CUDA-event times (ms) on `stream`, L2 flushed before every step."""
     for _ in range(warmup):
@@ -145,8 +158,7 @@ def run_ours(args, rank, world, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
-    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush = lambda: flush_buf.fill_(1)
+    flush = make_flush(torch, dev)
     peak, peak_kind = peaks()
     uuid = None
     try:
@@ -217,6 +229,27 @@ def run_ours(args, rank, world, dist):
     lat = {"p50_us": round(float(np.percentile(d, 50)), 3),
            "p99_us": round(float(np.percentile(d, 99)), 3)} if d.size else {}
     sp.free()
+    # where an epoch's time goes (first warp): stage+notify, wait/validate, store+rest
+    phases = {}
+    for name, cfg in [("spec", dict(protocol="spec")), ("dual", dict(protocol="dual")),
+                      ("spec_relaxed", dict(protocol="spec", spec_check="relaxed"))]:
+        pp = cdc.Plan(nm, record_stamps=2, stamp_capacity=EPOCHS, **cfg)
+        pp.run(ins, outs, **kw)
+        pp.run(ins, outs, **kw)
+        st4 = pp.stamps(EPOCHS).astype(np.int64)[1:].reshape(-1, 4)
+        pp.free()
+        med = lambda x: round(float(np.median(x)) / 1000.0, 3)
+        phases[name] = {"stage_notify_us": med(st4[:, 1] - st4[:, 0]),
+                        "wait_validate_us": med(st4[:, 2] - st4[:, 1]),
+                        "store_rest_us": med(st4[:, 3] - st4[:, 2]),
+                        "epoch_us": med(np.diff(st4[:, 0]))}
+    # the latency floor: one flag round trip between two blocks (near: blocks 0 and 1;
+    # far: block 0 and the last block of an SM-count grid)
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    rtt = {}
+    for tag, peer in (("near", 1), ("far", nsm - 1)):
+        ns, sa, sb = cdc.probe_flag_rtt(peer, 20000)
+        rtt[tag] = {"rtt_ns": round(ns, 1), "sm": [sa, sb]}
 
     # end to end through the C ABI with host buffers: H2D of the step's inputs (pinned),
     # the run, D2H of every epoch's outputs
@@ -287,6 +320,8 @@ def run_ours(args, rank, world, dist):
                      "traffic": None, "peak_kind": f"of {peak_kind}",
                      "note": "latency-bound: 128 KiB of algorithmic bytes per epoch"},
         "latency": lat,
+        "phases": phases,
+        "flag_round_trip": rtt,
         "protocols": proto,
         "prefill_allreduce_64MiB": prefill,
         "e2e": {"value": round(e2e_us, 4), "unit": "us/epoch", "h2d_bytes_per_step": h2d,
@@ -398,8 +433,7 @@ def run_workload(args):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
-    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush = lambda: flush_buf.fill_(1)
+    flush = make_flush(torch, dev)
     peak, peak_kind = peaks()
     R = 8
     g = torch.Generator(device=dev)

@@ -10,4 +10,4 @@ from . import namings  # noqa: F401
 from ._lib import CollError, lib  # noqa: F401
 from .namings import (Naming, allgather, allreduce, alltoall, broadcast,  # noqa: F401
                       moe_dispatch, reduce_scatter, segs)
-from .plan import Plan, validate, validate_code  # noqa: F401
+from .plan import Plan, probe_flag_rtt, validate, validate_code  # noqa: F401

@@ -87,6 +87,8 @@ _SIGS = {
     "coll_reset": (C.c_int, [_P]),
     "coll_free": (C.c_int, [_P]),
     "coll_strerror": (C.c_char_p, [C.c_int]),
+    "coll_probe_flag_rtt": (C.c_int, [C.c_int, C.c_int, C.POINTER(C.c_uint64),
+                                      C.POINTER(C.c_int), C.POINTER(C.c_int)]),
 }
 
 _lib = None
@@ -140,7 +142,7 @@ def make_config(**kw) -> Config:
                 v = sum(INJECT[x] for x in v)
             elif isinstance(v, str):
                 v = INJECT[v]
-        elif k in ("zero_copy", "record_stamps"):
+        elif k == "zero_copy":
             v = int(bool(v))
         if not hasattr(c, k):
             raise TypeError(f"unknown config field {k}")

@@ -148,7 +148,8 @@ extern "C" int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_
       ok = cudaMalloc(&p->d_dbg, c.units.size() * 4) == cudaSuccess;
     if (ok && c.cfg.record_stamps && c.cfg.stamp_capacity) {
       p->stamp_cap = c.cfg.stamp_capacity;
-      ok = cudaMalloc(&p->d_stamps, ((size_t)p->stamp_cap + 1) * 8) == cudaSuccess;
+      const size_t per = c.cfg.record_stamps == 2 ? 4 : 1;
+      ok = cudaMalloc(&p->d_stamps, ((size_t)p->stamp_cap * per + 1) * 8) == cudaSuccess;
     }
   }
   if (ok) ok = zero_state(p) == COLL_OK;
@@ -270,6 +271,7 @@ extern "C" int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_
     a.stamps = p->d_stamps;
     a.dbg = p->d_dbg;
     a.stamp_cap = p->stamp_cap;
+    a.stamp_phases = c.cfg.record_stamps == 2 ? 1u : 0u;
     a.n_pflag = c.n_pflag;
     a.nwarps = (uint32_t)c.warps.size();
     a.n_epochs = n_epochs;
@@ -340,7 +342,9 @@ extern "C" int64_t coll_stamps(coll_plan_t p, uint64_t *host, int64_t n) {
   if (!p || !host || n < 0) return COLL_EINVAL;
   if (!p->d_stamps) return 0;
   if (wait_last(p)) return COLL_ECUDA;
-  int64_t m = std::min<int64_t>(n, (int64_t)std::min<uint32_t>(p->stamp_cap, (uint32_t)p->last_epochs) + 1);
+  const int64_t per = p->c.cfg.record_stamps == 2 ? 4 : 1;
+  int64_t m = std::min<int64_t>(
+      n, (int64_t)std::min<uint32_t>(p->stamp_cap, (uint32_t)p->last_epochs) * per + 1);
   if (cudaMemcpy(host, p->d_stamps, (size_t)m * 8, cudaMemcpyDeviceToHost) != cudaSuccess)
     return COLL_ECUDA;
   return m;
@@ -375,4 +379,28 @@ extern "C" const char *coll_strerror(int code) {
     case COLL_ENOMEM: return "out of memory";
     default: return "unknown error";
   }
+}
+
+extern "C" int coll_probe_flag_rtt(int peer_block, int iters, uint64_t *ns_total, int *sm_a,
+                                   int *sm_b) {
+  if (peer_block < 1 || iters < 1 || !ns_total) return COLL_EINVAL;
+  unsigned long long *d = nullptr;
+  if (cudaMalloc(&d, 1024) != cudaSuccess) return COLL_ECUDA;
+  unsigned long long h[8] = {0};
+  int rc = COLL_OK;
+  if (cudaMemset(d, 0, 1024) != cudaSuccess ||
+      coll::launch_probe_rtt(d, (uint32_t)iters, (uint32_t)peer_block, d + 96, 1000000000ull,
+                             nullptr) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(h, d + 96, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    rc = COLL_ECUDA;
+  }
+  cudaFree(d);
+  if (rc) return rc;
+  if (h[4]) return COLL_ETIMEDOUT;
+  *ns_total = h[0];
+  if (sm_a) *sm_a = (int)h[2];
+  if (sm_b) *sm_b = (int)h[3];
+  return COLL_OK;
 }

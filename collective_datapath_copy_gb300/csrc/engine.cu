@@ -351,7 +351,9 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
 
   if ((a.inject_flags & COLL_INJECT_STAGGER) && a.inject_start_ns)
     spin_ns((uint64_t)W.rank * a.inject_start_ns);
-  if (gw == 0 && lane == 0 && a.stamps) a.stamps[0] = globaltimer();
+  const bool stamp = gw == 0 && lane == 0 && a.stamps;
+  const bool phases = stamp && a.stamp_phases;
+  if (stamp) a.stamps[0] = globaltimer();
 
   for (int i = 0; i < a.n_epochs && !failed; ++i) {
     const uint32_t E = a.epoch_base + (uint32_t)i + 1u;
@@ -364,6 +366,9 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
       if ((h % 1000000ull) < a.inject_prob_ppm && W.rank == (uint32_t)((h >> 40) % (uint64_t)a.R))
         spin_ns(splitmix64(h) % (a.inject_max_ns + 1));
     }
+
+    const bool pst = phases && (uint32_t)i < a.stamp_cap;
+    if (pst) a.stamps[1 + 4 * i] = globaltimer();
 
     // ---------------- Stage + Notify
     for (uint32_t s = W.s0; s < W.s1; ++s) {
@@ -417,6 +422,7 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
       }
     }
     if (failed) break;
+    if (pst) a.stamps[2 + 4 * i] = globaltimer();
 
     // ---------------- Consume
     for (uint32_t c = W.c0; c < W.c1; ++c) {
@@ -514,6 +520,7 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
         }
         res = gather_pieces<KIND>(xb, u.nbytes, n, lane, active);
       }
+      if (pst && c == W.c0) a.stamps[3 + 4 * i] = globaltimer();
       if (active) {
         if (it.slot == COLL_SLOT_ALL) {
           for (uint32_t d = 0; d < u.ndst; ++d) {
@@ -535,12 +542,49 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
       nh = __reduce_add_sync(FULL, lane < (su.nbytes >> 4) ? tag_part(nx, lane) : 0u);
       nh_ready = true;
     }
-    if (gw == 0 && lane == 0 && a.stamps && (uint32_t)i < a.stamp_cap)
-      a.stamps[i + 1] = globaltimer();
+    if (stamp && (uint32_t)i < a.stamp_cap) a.stamps[phases ? 4 + 4 * i : i + 1] = globaltimer();
   }
   if (lane == 0) {
     if (n_checks) atomicAdd(&st->spec_checks, (unsigned long long)n_checks);
     if (n_retries) atomicAdd(&st->spec_retries, (unsigned long long)n_retries);
+  }
+}
+
+// Flag ping-pong between block 0 and block `peer` (one thread each): block 0 stores
+// ping i, block peer answers with pong i. out: [0] ns for all round trips, [1] unused,
+// [2] SM of block 0, [3] SM of block peer, [4] 1 if a wait gave up.
+__global__ void __launch_bounds__(32) probe_rtt_kernel(unsigned long long *flags, uint32_t iters,
+                                                       uint32_t peer, unsigned long long *out,
+                                                       uint64_t limit) {
+  if (threadIdx.x != 0) return;
+  uint32_t smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  if (blockIdx.x == 0) {
+    out[2] = smid;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1; i <= iters; ++i) {
+      st_relaxed_u64(&flags[32], i);
+      for (uint32_t k = 0; ld_acquire_u64(&flags[0]) != i; ++k) {
+        if ((k & 63u) == 63u && globaltimer() - t0 > limit) {
+          out[4] = 1;
+          st_relaxed_u64(&flags[64], 1);
+          return;
+        }
+      }
+    }
+    out[0] = globaltimer() - t0;
+  } else if (blockIdx.x == peer) {
+    out[3] = smid;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1; i <= iters; ++i) {
+      for (uint32_t k = 0; ld_acquire_u64(&flags[32]) != i; ++k) {
+        if ((k & 63u) == 63u && (globaltimer() - t0 > limit || ld_relaxed_u64(&flags[64]))) {
+          out[4] = 1;
+          return;
+        }
+      }
+      st_relaxed_u64(&flags[0], i);
+    }
   }
 }
 
@@ -588,6 +632,13 @@ cudaError_t engine_max_coresident(int op, int dtype, int *max_ctas) {
   if (e != cudaSuccess) return e;
   *max_ctas = per_sm * sms;
   return cudaSuccess;
+}
+
+cudaError_t launch_probe_rtt(unsigned long long *flags, uint32_t iters, uint32_t peer,
+                             unsigned long long *out, uint64_t limit, cudaStream_t s) {
+  void *args[] = {(void *)&flags, (void *)&iters, (void *)&peer, (void *)&out, (void *)&limit};
+  return cudaLaunchCooperativeKernel((const void *)probe_rtt_kernel, dim3(peer + 1), dim3(32),
+                                     args, 0, s);
 }
 
 cudaError_t launch_engine(int op, int dtype, const EngArgs &a, cudaStream_t s) {

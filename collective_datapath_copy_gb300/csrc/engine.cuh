@@ -46,6 +46,7 @@ struct EngArgs {
   uint64_t *stamps;           // [stamp_cap + 1] or null
   uint32_t *dbg;              // [n_units] handshake words of the SPEC_PAUSE injection
   uint32_t stamp_cap;
+  uint32_t stamp_phases;  // 1: four stamps per epoch (start, notified, data ready, end)
   uint32_t n_pflag;
   uint32_t nwarps;
   int32_t n_epochs;
@@ -75,6 +76,10 @@ uint32_t bulk_smem_bytes(uint32_t stages, uint32_t maxsrc, uint32_t slot_bytes);
 
 // Staged Stage/Notify/Consume engine: one cooperative launch of nwarps one-warp CTAs.
 cudaError_t launch_engine(int op, int dtype, const EngArgs &a, cudaStream_t s);
+
+// Flag ping-pong probe between block 0 and block `peer` (cooperative launch).
+cudaError_t launch_probe_rtt(unsigned long long *flags, uint32_t iters, uint32_t peer,
+                             unsigned long long *out, uint64_t limit, cudaStream_t s);
 
 // How many one-warp engine CTAs can be co-resident on the current device.
 cudaError_t engine_max_coresident(int op, int dtype, int *max_ctas);

@@ -112,8 +112,10 @@ class Plan:
         return d
 
     def stamps(self, n: int) -> np.ndarray:
-        buf = np.zeros(n + 1, dtype=np.uint64)
-        m = lib().coll_stamps(self._h, C.c_void_p(buf.ctypes.data), n + 1)
+        """Stamps of the last run: n+1 values (record_stamps=1) or 4n+1 (record_stamps=2)."""
+        per = 4 if int(self.cfg.get("record_stamps", 0)) == 2 else 1
+        buf = np.zeros(per * n + 1, dtype=np.uint64)
+        m = lib().coll_stamps(self._h, C.c_void_p(buf.ctypes.data), per * n + 1)
         if m < 0:
             check(int(m), "coll_stamps")
         return buf[:m]
@@ -131,3 +133,12 @@ class Plan:
             self.free()
         except Exception:
             pass
+
+
+def probe_flag_rtt(peer_block: int = 1, iters: int = 20000):
+    """Round trip (ns) of one flag ping-pong between two blocks, and their SM ids."""
+    ns = C.c_uint64()
+    a, b = C.c_int(), C.c_int()
+    check(lib().coll_probe_flag_rtt(int(peer_block), int(iters), C.byref(ns), C.byref(a),
+                                    C.byref(b)), "coll_probe_flag_rtt")
+    return ns.value / iters, a.value, b.value

@@ -117,8 +117,10 @@ typedef struct {
                              consumers per job, use the bulk-copy (TMA) ring kernel;
                              0 = 4 MiB; UINT64_MAX = never                             */
   uint64_t spin_limit_ns; /* bound on every device wait; 0 = 2e9 (2 s)                  */
-  uint32_t record_stamps; /* staged: record a %globaltimer stamp per epoch (capacity
-                             stamp_capacity epochs; later epochs are not stamped)      */
+  uint32_t record_stamps; /* staged: 1 = one %globaltimer stamp per epoch (capacity
+                             stamp_capacity epochs; later epochs are not stamped);
+                             2 = four per epoch (start, notified, data ready, end) of
+                             the first warp                                            */
   uint32_t stamp_capacity;
   uint64_t inject_flags;  /* COLL_INJECT_*                                            */
   uint64_t inject_seed;
@@ -198,6 +200,13 @@ int coll_status(coll_plan_t p, coll_stats_t *st);
 /* Copy up to n per-epoch %globaltimer stamps (ns) of the last run into host memory;
  * returns the number copied (synchronises on the last run). */
 int64_t coll_stamps(coll_plan_t p, uint64_t *host, int64_t n);
+
+/* Measurement probe (not part of the collective): ping-pong one flag `iters` times
+ * between one thread of block 0 and one thread of block `peer_block` of a cooperative
+ * launch with peer_block+1 one-warp blocks, and report the total ns (%globaltimer) and the
+ * two SM ids. This is the round trip that bounds a flag handshake between two emulated
+ * ranks. Synchronous; allocates and frees 1 KiB. COLL_ETIMEDOUT if a wait exceeded 1 s. */
+int coll_probe_flag_rtt(int peer_block, int iters, uint64_t *ns_total, int *sm_a, int *sm_b);
 
 /* Wait for the last run, then re-zero flags, counters and the epoch counter. */
 int coll_reset(coll_plan_t p);
