@@ -339,12 +339,27 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
   const bool pipelined = (W.s1 - W.s0) == 1u;
   coll_unit_t su;
   coll_ref_t sref;
+  coll_item_t sit;
+  // A warp with a single consume item (the all-reduce case) also keeps that item, its
+  // unit and its output reference in registers: the plan tables are then read once, not
+  // once per epoch (acquire loads may invalidate L1, which would make every table read an
+  // L2 round trip on the critical path).
+  const bool single_c = (W.c1 - W.c0) == 1u;
+  coll_item_t cit;
+  coll_unit_t cu;
+  coll_ref_t cref;
+  if (single_c) {
+    cit = a.citems[W.c0];
+    cu = a.units[cit.unit];
+    cref = a.refs[cu.dst0 + (cit.slot == COLL_SLOT_ALL ? 0u : cit.slot)];
+  }
   uint4 nx = make_uint4(0, 0, 0, 0);
   uint32_t nh = 0;
   bool nh_ready = false;
   if (pipelined) {
-    su = a.units[a.sitems[W.s0].unit];
-    sref = a.refs[su.src0 + a.sitems[W.s0].slot];
+    sit = a.sitems[W.s0];
+    su = a.units[sit.unit];
+    sref = a.refs[su.src0 + sit.slot];
     if (lane < (su.nbytes >> 4) && a.n_epochs > 0)
       nx = ld_nc_v4(a.ptr.in[sref.rank] + sref.off + su.start + lane * 16);
   }
@@ -372,7 +387,7 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
 
     // ---------------- Stage + Notify
     for (uint32_t s = W.s0; s < W.s1; ++s) {
-      const coll_item_t it = a.sitems[s];
+      const coll_item_t it = pipelined ? sit : a.sitems[s];
       const coll_unit_t u = pipelined ? su : a.units[it.unit];
       if (a.protocol == COLL_PROTO_BARRIER || (u.flags & COLL_UNIT_REUSE_WAIT)) {
         // bottom barrier (single buffer) / explicit reuse wait (dual buffers)
@@ -426,8 +441,8 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
 
     // ---------------- Consume
     for (uint32_t c = W.c0; c < W.c1; ++c) {
-      const coll_item_t it = a.citems[c];
-      const coll_unit_t u = a.units[it.unit];
+      const coll_item_t it = single_c ? cit : a.citems[c];
+      const coll_unit_t u = single_c ? cu : a.units[it.unit];
       const uint32_t n = u.nsrc;
       const uint32_t nvec = u.nbytes >> 4;
       const bool active = lane < nvec;
@@ -528,7 +543,7 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
             st_v4(a.ptr.out[r.rank] + r.off + out_off + u.start + lane * 16, res);
           }
         } else {
-          const coll_ref_t r = a.refs[u.dst0 + it.slot];
+          const coll_ref_t r = single_c ? cref : a.refs[u.dst0 + it.slot];
           st_v4(a.ptr.out[r.rank] + r.off + out_off + u.start + lane * 16, res);
         }
       }
