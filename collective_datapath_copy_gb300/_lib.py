@@ -89,6 +89,8 @@ _SIGS = {
     "coll_strerror": (C.c_char_p, [C.c_int]),
     "coll_probe_flag_rtt": (C.c_int, [C.c_int, C.c_int, C.POINTER(C.c_uint64),
                                       C.POINTER(C.c_int), C.POINTER(C.c_int)]),
+    "coll_allreduce_static": (C.c_int, [C.c_int, C.c_int, _P, _P, C.c_uint64, C.c_int,
+                                        C.c_int64, C.c_int, C.c_int64, _P, _P]),
 }
 
 _lib = None

@@ -26,7 +26,7 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompil
               "-ftz=false", "-prec-div=true", "-fmad=false", f"-I{INCLUDE}", f"-I{CSRC}"]
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-ffp-contract=off", f"-I{INCLUDE}", f"-I{CSRC}"]
 
-CU_SOURCES = ["engine.cu", "bulk.cu", "api.cu"]
+CU_SOURCES = ["engine.cu", "bulk.cu", "api.cu", "noalloc.cu"]
 CXX_SOURCES = ["plan.cpp"]
 
 

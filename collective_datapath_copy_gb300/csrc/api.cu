@@ -377,6 +377,7 @@ extern "C" const char *coll_strerror(int code) {
     case COLL_ETIMEDOUT: return "a bounded device wait expired";
     case COLL_EDEVICE: return "inconsistent device state";
     case COLL_ENOMEM: return "out of memory";
+    case COLL_ETOOBIG: return "request exceeds the fixed static scratch array or co-residency";
     default: return "unknown error";
   }
 }

@@ -46,6 +46,8 @@ extern "C" {
 #define COLL_ETIMEDOUT (-8) /* async: a bounded device wait expired; kernel returned    */
 #define COLL_EDEVICE (-9)   /* async: the device reported an inconsistent state         */
 #define COLL_ENOMEM (-10)   /* host or device allocation failed                         */
+#define COLL_ETOOBIG (-11)  /* coll_allreduce_static: the request needs more than its fixed
+                               scratch array or more warps than can be co-resident       */
 
 /* ------------------------------------------------------------------ enums */
 #define COLL_OP_COPY 0
@@ -213,6 +215,29 @@ int coll_reset(coll_plan_t p);
 
 /* Wait for the last run and release everything the plan owns. NULL is a no-op. */
 int coll_free(coll_plan_t p);
+
+/* All-reduce (sum) that allocates nothing. The pages have no counterpart: this exists for
+ * callers that cannot allocate device memory when they need the collective — a serving
+ * process that reserved nearly all HBM up front for weights and KV cache, code inside a
+ * CUDA stream capture, or a latency-critical loop where cudaMalloc/cudaFree would add an
+ * implicit device synchronisation. It calls no allocating routine.
+ * Same result as coll_plan/coll_run for an all-reduce naming (every rank's whole buffer is
+ * one name) with the dual-buffer protocol: out[r] = the rank-order binary32 sum of all R
+ * inputs, rounded once to bf16 for COLL_BF16. in/out: host arrays of R device pointers,
+ * 16-byte aligned, count elements each; epochs, pool and strides as in coll_run; inputs
+ * and outputs must not overlap. status: optional device int32 the kernel sets to
+ * COLL_ETIMEDOUT if a bounded wait expires (cleared by the call; NULL = not reported).
+ * Scratch: a fixed 4 MiB device array held by every GPU that loads the library until the
+ * process exits; it holds 2 x R x ceil(count*size/512) pieces of 512 bytes plus flags, so
+ * R x count x element size up to about 2 MiB fits. Larger requests (or more warps than can
+ * be co-resident) return COLL_ETOOBIG. The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. Every call shares the array and clears its flags on `stream`
+ * first; calls that can overlap on the GPU (other streams, unordered) race on it.
+ * Errors: COLL_EINVAL, COLL_EALIGN, COLL_ETOOBIG, COLL_ECUDA (synchronous). */
+int coll_allreduce_static(int R, int dtype, void *const *in, void *const *out, uint64_t count,
+                          int n_epochs, int64_t in_epoch_stride, int in_pool,
+                          int64_t out_epoch_stride, int32_t *status, void *stream);
 
 /* Static string for a code. */
 const char *coll_strerror(int code);
