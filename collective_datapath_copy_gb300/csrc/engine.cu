@@ -296,17 +296,20 @@ __device__ __forceinline__ uint4 spec_attempt(const char *xb, uint32_t nbytes, u
       f = acquire_flags ? ld_acquire_u64(pf + lane) : ld_relaxed_u64(pf + lane);
     if (k0 == 0 && side)
       side_h = __reduce_add_sync(FULL, lane < side_nvec ? tag_part(side_v, lane) : 0u);
+    if (active) {
 #pragma unroll
-    for (uint32_t k = 0; k < 8; ++k) {
-      if (k < kn) {
-        if (active) {
+      for (uint32_t k = 0; k < 8; ++k)
+        if (k < kn) {
           if (k0 + k == 0) acc.init(x[k]); else acc.add(x[k]);
         }
-        if (want_hash) {
-          const uint32_t hs = __reduce_add_sync(FULL, active ? tag_part(x[k], lane) : 0u);
-          if (lane == k0 + k) myh = hs;
-        }
-      }
+    }
+    if (want_hash) {
+      // per-producer hashes of this batch: lane k0+j receives producer k0+j's sum
+      uint32_t hk[8];
+#pragma unroll
+      for (uint32_t k = 0; k < 8; ++k) hk[k] = (k < kn && active) ? tag_part(x[k], lane) : 0u;
+      const uint32_t hs = reduce_scatter8(hk, lane);
+      if (lane >= k0 && lane < k0 + 8) myh = hs;
     }
   }
   return active ? acc.pack() : make_uint4(0, 0, 0, 0);
