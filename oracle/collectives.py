@@ -12,7 +12,11 @@ and returns the R per-rank output arrays.
 * all-to-all: block d of rank s's input goes to block s of rank d's output;
 * MoE dispatch: each token row goes to every rank that hosts one of its experts
   (feed abstracts on expert-parallel routing), one copy per (token, destination rank),
-  rows at a destination ordered by (source rank, source token).
+  rows at a destination ordered by (source rank, source token); MoE combine is its reverse
+  with a sum over the destinations, in destination-rank order;
+* reduce-to-root, gather and scatter: the rooted forms of all-reduce, all-gather and
+  all-to-all (the Purlin article counts seven collectives without listing them; these are
+  read as the three besides the five named in the workloads).
 
 Sums are the fixed-order binary32 chain of ``oracle.arith.ordered_sum``.
 """
@@ -52,6 +56,28 @@ def alltoall(xs):
     assert n % R == 0
     b = n // R
     return [np.concatenate([xs[s][d * b:(d + 1) * b] for s in range(R)]) for d in range(R)]
+
+
+def reduce_to_root(xs, dtype, root=0):
+    """Only the root receives the full sum (the other ranks' outputs are not written:
+    returned as None)."""
+    s = ordered_sum(list(xs), dtype)
+    return [s.copy() if r == root else None for r in range(len(xs))]
+
+
+def gather(xs, root=0):
+    """The root receives the concatenation of all inputs in rank order."""
+    cat = np.concatenate(list(xs))
+    return [cat.copy() if r == root else None for r in range(len(xs))]
+
+
+def scatter(xs, root=0):
+    """Block d of the root's input goes to rank d."""
+    R = len(xs)
+    n = len(xs[root])
+    assert n % R == 0
+    b = n // R
+    return [xs[root][d * b:(d + 1) * b].copy() for d in range(R)]
 
 
 def moe_dest_ranks(routing, experts_per_rank):

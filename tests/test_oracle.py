@@ -386,3 +386,66 @@ def test_epoch_semantics_cycle_through_pool():
         want = collectives.allreduce(pool[e % 3], "bf16")
         for r in range(R):
             assert _eq(res[e][r], want[r])
+
+
+def test_rooted_collectives_against_their_all_forms():
+    R, n = 4, 32
+    rng = synth.seeded_rng(60)
+    xs = [synth.normal_bf16(rng, n) for _ in range(R)]
+    for root in range(R):
+        red = collectives.reduce_to_root(xs, "bf16", root)
+        assert _eq(red[root], collectives.allreduce(xs, "bf16")[0])
+        assert all(red[r] is None for r in range(R) if r != root)
+        g = collectives.gather(xs, root)
+        assert _eq(g[root], collectives.allgather(xs)[0])
+        sc = collectives.scatter(xs, root)
+        # scatter then gather at the same root is the identity on the root's input
+        assert _eq(collectives.gather(sc, root)[root], xs[root])
+        # scatter is the root's row of an all-to-all
+        a2a = collectives.alltoall(xs)
+        for d in range(R):
+            assert _eq(sc[d], a2a[d][root * (n // R):(root + 1) * (n // R)])
+
+
+def test_rooted_collectives_by_naming():
+    R, n = 3, 12
+    b = n // R
+    rng = synth.seeded_rng(61)
+    xs = [synth.normal_bf16(rng, n) for _ in range(R)]
+    root = 1
+    red = _run(R, "sum", "bf16", [n] * R, [(r, 0, n, 0) for r in range(R)], [n] * R,
+               [(root, 0, n, 0)], xs)
+    assert _eq(red[root], collectives.reduce_to_root(xs, "bf16", root)[root])
+    g = _run(R, "copy", "bf16", [n] * R, [(r, 0, n, r) for r in range(R)], [R * n] * R,
+             [(root, j * n, n, j) for j in range(R)], xs)
+    assert _eq(g[root], collectives.gather(xs, root)[root])
+    sc = _run(R, "copy", "bf16", [n] * R, [(root, d * b, b, d) for d in range(R)], [b] * R,
+              [(d, 0, b, d) for d in range(R)], xs)
+    for d in range(R):
+        assert _eq(sc[d], collectives.scatter(xs, root)[d])
+
+
+def test_moe_combine_is_the_ordered_sum_over_destinations():
+    R, T, H, E, k = 4, 16, 4, 16, 3
+    routing = synth.zipf_topk_routing(12, R, T, E, k, 1.1)
+    rng = synth.seeded_rng(12)
+    # destination buffers hold arbitrary rows (as after an expert computation)
+    dests = collectives.moe_dest_ranks(routing, E // R)
+    counts = [int(dests[:, :, d].sum()) for d in range(R)]
+    ys = [synth.normal_bf16(rng, (c, H)) for c in counts]
+    out = collectives.moe_combine_sum(ys, routing, E // R, "bf16")
+    # brute force: walk the dispatch order and sum by hand in destination order
+    pos = [0] * R
+    rowsof = {}
+    for s_ in range(R):
+        for t in range(T):
+            for d in range(R):
+                if dests[s_, t, d]:
+                    rowsof.setdefault((s_, t), []).append(ys[d][pos[d]])
+                    pos[d] += 1
+    for s_ in range(R):
+        for t in range(T):
+            rows = rowsof[(s_, t)]
+            for h in range(H):
+                want = brute.element_sum([brute.decode_bf16(int(r[h])) for r in rows], "bf16")
+                assert brute.decode_bf16(int(out[s_][t, h])).key() == want.key()
