@@ -10,7 +10,8 @@ protocols, a staggered-start stress run of the speculative protocol, and the
 prefill-sized all-reduce (8 x 64 MiB, one-shot vs two-shot) as achieved HBM GB/s.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|sweep|prefill|moe] [--max-bytes B]
+                    [--workload decode|sweep|prefill|moe|moe_combine|fig15]
+                    [--max-bytes B]
 
 Under torchrun each rank runs an independent replica on its own GPU (the emulated
 collective needs no inter-GPU exchange); rank 0 prints one JSON line.
@@ -448,7 +449,8 @@ def run_workload(args):
             g.manual_seed(3)
             ins = [((torch.rand(n, device=dev, generator=g) * 2 - 1).to(torch.bfloat16))
                    .view(torch.int16) for _ in range(R)]
-            for kind in ("allreduce", "reduce_scatter", "allgather", "broadcast", "alltoall"):
+            for kind in ("allreduce", "reduce_scatter", "allgather", "broadcast", "alltoall",
+                         "reduce_to_root", "gather", "scatter"):
                 nm = getattr(cdc, kind)(R, n, "bf16")
                 outs = [torch.empty(L, dtype=torch.int16, device=dev) for L in nm.out_len]
                 cfgs = {"twoshot": dict(datapath="twoshot")} if kind == "allreduce" else {"": {}}
@@ -476,6 +478,48 @@ def run_workload(args):
                             datapath=dp)
             r["frac"] = round(r["gbs"] / peak, 4)
             res[dp] = r
+    elif args.workload == "fig15":
+        # SiFAR Fig. 15 grid: R = 2/4/8 ranks x 8/16/32 KB payloads, every protocol and
+        # datapath, 2000 epochs per launch; microseconds per epoch (median of K launches)
+        rows = []
+        E = 2000
+        for Rr in (2, 4, 8):
+            for kb in (8, 16, 32):
+                n = kb * 1024 // 2
+                g.manual_seed(15)
+                ins = [torch.randn(7, n, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
+                       for _ in range(Rr)]
+                outs = [torch.empty(E, n, dtype=torch.int16, device=dev) for _ in range(Rr)]
+                nm = cdc.allreduce(Rr, n, "bf16")
+                for proto in ("barrier", "dual", "spec"):
+                    for dp in ("oneshot", "twoshot"):
+                        pl = cdc.Plan(nm, protocol=proto, datapath=dp)
+                        tt = _time_steps(torch, lambda: pl.run(ins, outs, n_epochs=E,
+                                                               in_epoch_stride=2 * n, in_pool=7,
+                                                               out_epoch_stride=2 * n),
+                                         args.steps, args.warmup, flush, stream)
+                        st = pl.status()
+                        if st["code"] != 0:
+                            raise RuntimeError(f"fig15 {Rr} {kb} {proto} {dp}: {st}")
+                        t = sorted(tt)[len(tt) // 2]
+                        rows.append({"R": Rr, "kb": kb, "protocol": proto, "datapath": dp,
+                                     "us_per_epoch": round(t * 1000 / E, 4),
+                                     "retries_per_check": (st["spec_retries"] / st["spec_checks"]
+                                                           if st["spec_checks"] else 0.0)})
+                        pl.free()
+        res["rows"] = rows
+    elif args.workload == "moe_combine":
+        T, H, E, k = 4096, 7168, 256, 8
+        routing = synth.zipf_topk_routing(5, R, T, E, k, 1.1)
+        nm = cdc.moe_combine(routing, E // R, H)
+        g.manual_seed(6)
+        ins = [torch.randn(L, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
+               for L in nm.in_len]
+        outs = [torch.empty(T * H, dtype=torch.int16, device=dev) for _ in range(R)]
+        r = _zc_measure(torch, cdc, nm, ins, outs, args.steps, args.warmup, flush, stream)
+        r["frac"] = round(r["gbs"] / peak, 4)
+        r["rows_per_rank"] = nm.meta["counts"]
+        res["combine"] = r
     elif args.workload == "moe":
         T, H, E, k = 4096, 7168, 256, 8
         routing = synth.zipf_topk_routing(5, R, T, E, k, 1.1)
@@ -501,7 +545,8 @@ def main():
     ap.add_argument("--ref-epochs", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true")
-    ap.add_argument("--workload", default="decode", choices=["decode", "sweep", "prefill", "moe"])
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "sweep", "prefill", "moe", "moe_combine", "fig15"])
     ap.add_argument("--max-bytes", type=int, default=0, help="sweep: largest bytes per rank")
     args = ap.parse_args()
     if args.warmup < 3:

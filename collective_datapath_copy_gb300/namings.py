@@ -119,3 +119,43 @@ def moe_dispatch(routing: np.ndarray, experts_per_rank: int, hidden: int,
     out_len = [max(c, 1) * hidden for c in counts]
     return Naming(R, "copy", dtype, [T * hidden] * R, i, out_len, o,
                   meta={"counts": counts, "dest": dest})
+
+
+def reduce_to_root(R: int, n: int, dtype: str = "bf16", root: int = 0) -> Naming:
+    """Every rank's whole buffer is name 0; only the root's output receives the sum."""
+    i = _segs_cols(np.arange(R), np.zeros(R), np.full(R, n), np.zeros(R))
+    o = _segs_cols([root], [0], [n], [0])
+    return Naming(R, "sum", dtype, [n] * R, i, [n] * R, o)
+
+
+def gather(R: int, n: int, dtype: str = "bf16", root: int = 0) -> Naming:
+    """Input r is name r; block j of the root's output is name j."""
+    i = _segs_cols(np.arange(R), np.zeros(R), np.full(R, n), np.arange(R))
+    o = _segs_cols(np.full(R, root), np.arange(R) * n, np.full(R, n), np.arange(R))
+    return Naming(R, "copy", dtype, [n] * R, i, [R * n] * R, o)
+
+
+def scatter(R: int, n: int, dtype: str = "bf16", root: int = 0) -> Naming:
+    """Block d (of n/R) of the root's input is name d; rank d's output is name d."""
+    assert n % R == 0
+    b = n // R
+    i = _segs_cols(np.full(R, root), np.arange(R) * b, np.full(R, b), np.arange(R))
+    o = _segs_cols(np.arange(R), np.zeros(R), np.full(R, b), np.arange(R))
+    return Naming(R, "copy", dtype, [n] * R, i, [b] * R, o)
+
+
+def moe_combine(routing: np.ndarray, experts_per_rank: int, hidden: int,
+                dtype: str = "bf16") -> Naming:
+    """Reverse of moe_dispatch with a sum: rank d's input holds, in dispatch order, one row
+    per token routed to it; token (s, t) (name s*T+t) receives at rank s the sum of its rows
+    over the destination ranks, which the fixed (rank, offset) order visits ascending.
+    meta["counts"] holds the rows each rank's input has."""
+    R, T, k = routing.shape
+    disp = moe_dispatch(routing, experts_per_rank, hidden, dtype)
+    counts = disp.meta["counts"]
+    o_in = disp.out_segs  # dispatch outputs are the combine inputs
+    names = np.arange(R * T)
+    o = _segs_cols(np.repeat(np.arange(R), T), np.tile(np.arange(T), R) * hidden,
+                   np.full(R * T, hidden), names)
+    return Naming(R, "sum", dtype, list(disp.out_len), o_in.copy(), [T * hidden] * R, o,
+                  meta={"counts": counts, "dest": disp.meta["dest"]})

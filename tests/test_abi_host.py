@@ -179,3 +179,33 @@ def test_moe_naming_agrees_with_direct_dispatch():
     info = cdc.validate(nm, zero_copy=1)
     assert info.min_bytes == sum(2 * H * (1 + int(c)) for c in
                                  collectives.moe_dest_ranks(routing, E // R).sum(-1).ravel())
+
+
+@pytest.mark.parametrize("R", [1, 3, 8])
+def test_rooted_namings_agree_with_direct_definitions(R):
+    n = 4 * R
+    rng = synth.seeded_rng(70 + R)
+    xs = [synth.normal_bf16(rng, n) for _ in range(R)]
+    root = R - 1
+    red = _oracle_on(namings.reduce_to_root(R, n, root=root), xs)
+    assert np.array_equal(red[root], collectives.reduce_to_root(xs, "bf16", root)[root])
+    g = _oracle_on(namings.gather(R, n, root=root), xs)
+    assert np.array_equal(g[root], collectives.gather(xs, root)[root])
+    sc = _oracle_on(namings.scatter(R, n, root=root), xs)
+    for d in range(R):
+        assert np.array_equal(sc[d], collectives.scatter(xs, root)[d])
+
+
+def test_moe_combine_naming_agrees_with_direct_combine():
+    R, T, H, E, k = 4, 24, 8, 32, 4
+    routing = synth.zipf_topk_routing(8, R, T, E, k, 1.1)
+    nm = namings.moe_combine(routing, E // R, H)
+    rng = synth.seeded_rng(8)
+    ys = [synth.normal_bf16(rng, (max(c, 1), H)) for c in nm.meta["counts"]]
+    got = _oracle_on(nm, [y.ravel() for y in ys])
+    want = collectives.moe_combine_sum([y[:c] for y, c in zip(ys, nm.meta["counts"])], routing,
+                                       E // R, "bf16")
+    for s_ in range(R):
+        assert np.array_equal(got[s_], want[s_].ravel())
+    info = cdc.validate(nm, zero_copy=1)
+    assert info.n_names == R * T

@@ -524,3 +524,83 @@ def test_bulk_plan_with_misaligned_buffers_falls_back_and_stays_exact():
     for o in outs:
         assert bits_equal(from_dev(o, "bf16"), want)
     plan.free()
+
+
+# ------------------------------------------------------------ next rows: more collectives
+
+@pytest.mark.parametrize("kind", ["reduce_to_root", "gather", "scatter"])
+@pytest.mark.parametrize("mode", ["zc", "staged-spec", "staged-barrier"])
+def test_rooted_collectives(kind, mode):
+    R, n = 8, 8192
+    rng = synth.seeded_rng(90)
+    xs = [synth.uniform_bf16(rng, n) for _ in range(R)]
+    root = 3
+    nm = getattr(namings, kind)(R, n, "bf16", root=root)
+    cfg = dict(zero_copy=1) if mode == "zc" else dict(protocol=mode.split("-")[1])
+    got, init = run_once(nm, xs, **cfg)
+    want = getattr(collectives, kind)(*( [xs, "bf16", root] if kind == "reduce_to_root" else [xs, root]))
+    for r in range(R):
+        if want[r] is None:
+            assert bits_equal(got[r], init[r])  # not named: untouched
+        else:
+            assert bits_equal(got[r][:len(want[r])], want[r])
+
+
+@pytest.mark.parametrize("T,H,mode", [(256, 512, "zc"), (256, 512, "staged-spec"),
+                                      (4096, 7168, "zc")])
+def test_moe_combine(T, H, mode):
+    R, E, k = 8, 256, 8
+    routing = synth.zipf_topk_routing(6, R, T, E, k, 1.1)
+    nm = namings.moe_combine(routing, E // R, H)
+    rng = synth.seeded_rng(6)
+    ys = [synth.normal_bf16(rng, L) for L in nm.in_len]
+    counts = nm.meta["counts"]
+    cfg = dict(zero_copy=1) if mode == "zc" else dict(protocol="spec")
+    plan = cdc.Plan(nm, **cfg)
+    ins = [to_dev(y, "bf16") for y in ys]
+    outs = [torch.empty(T * H, dtype=torch.int16, device="cuda") for _ in range(R)]
+    plan.run(ins, outs)
+    assert plan.status()["code"] == 0
+    if T * H <= 256 * 512:
+        want = collectives.moe_combine_sum([y.reshape(-1, H)[:c] for y, c in zip(ys, counts)],
+                                           routing, E // R, "bf16")
+        for s in range(R):
+            assert bits_equal(from_dev(outs[s], "bf16"), want[s].ravel())
+    else:
+        # full size: check 64 sampled tokens per rank, each summed by the oracle's definition
+        pos = np.zeros((R,), dtype=np.int64)
+        dest = nm.meta["dest"]
+        rowidx = {}
+        for s in range(R):
+            for t in range(T):
+                for d in range(R):
+                    if dest[s, t, d]:
+                        rowidx[(s, t, d)] = pos[d]
+                        pos[d] += 1
+        srng = synth.seeded_rng(61)
+        for s in range(R):
+            for t in srng.integers(0, T, 64):
+                terms = [ys[d][rowidx[(s, t, d)] * H:(rowidx[(s, t, d)] + 1) * H]
+                         for d in range(R) if dest[s, t, d]]
+                from oracle.arith import ordered_sum
+                want = ordered_sum(terms, "bf16")
+                got = from_dev(outs[s][t * H:(t + 1) * H], "bf16")
+                assert bits_equal(got, want)
+    plan.free()
+
+
+@pytest.mark.parametrize("R", [2, 4, 8])
+@pytest.mark.parametrize("kb", [8, 16, 32])
+@pytest.mark.parametrize("protocol", ["barrier", "dual", "spec"])
+@pytest.mark.parametrize("datapath", ["oneshot", "twoshot"])
+def test_fig15_cells_bit_exact(R, kb, protocol, datapath):
+    # SiFAR's Fig. 15 grid: TP degree 2/4/8 x 8/16/32 KB payloads, every protocol
+    n = kb * 1024 // 2
+    pool, E = 5, 300
+    ins, expect = _decode_case(R, n, pool, seed=15)
+    plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol=protocol, datapath=datapath)
+    outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    plan.run(ins, outs, n_epochs=E, in_epoch_stride=n * 2, in_pool=pool, out_epoch_stride=n * 2)
+    assert plan.status()["code"] == 0
+    assert _check_epochs(outs, expect, E, pool) == 0
+    plan.free()
