@@ -181,6 +181,9 @@ def run_ours(args, rank, world, dist):
         ("spec_relaxed", dict(protocol="spec", spec_check="relaxed")),
         ("spec_literal", dict(protocol="spec", spec_check="literal")),
         ("spec_twoshot", dict(protocol="spec", datapath="twoshot")),
+        ("spec_chain", dict(protocol="spec", chain=1)),
+        ("dual_chain", dict(protocol="dual", chain=1)),
+        ("barrier_chain", dict(protocol="barrier", chain=1)),
     ]}
 
     def step(name):
@@ -208,7 +211,7 @@ def run_ours(args, rank, world, dist):
     # other protocols (same K/W)
     proto = {}
     for name in ("dual", "barrier", "spec_stagger", "spec_relaxed", "spec_literal",
-                 "spec_twoshot"):
+                 "spec_twoshot", "spec_chain", "dual_chain", "barrier_chain"):
         tt = _time_steps(torch, step(name), max(3, args.steps // 2), 1, flush, stream)
         s2 = plans[name].status()
         if s2["code"] != 0:

@@ -58,7 +58,8 @@ class Config(C.Structure):
                 ("inject_flags", C.c_uint64), ("inject_seed", C.c_uint64),
                 ("inject_rank", C.c_int32), ("inject_prob_ppm", C.c_uint32),
                 ("inject_max_ns", C.c_uint64), ("inject_start_ns", C.c_uint64),
-                ("inject_pause_ns", C.c_uint64)]
+                ("inject_pause_ns", C.c_uint64), ("chain", C.c_int32),
+                ("reserved2", C.c_int32)]
 
 
 class PlanInfo(C.Structure):

@@ -26,6 +26,7 @@ struct coll_plan_s {
   coll_dev_status_t *d_status = nullptr;
   uint64_t *d_stamps = nullptr;
   uint32_t *d_dbg = nullptr;
+  uint32_t *d_rank_done = nullptr;
   uint32_t stamp_cap = 0;
   uint64_t epochs_issued = 0;
   cudaEvent_t done = nullptr;
@@ -61,6 +62,7 @@ void release(coll_plan_s *p) {
   cudaFree(p->d_status);
   cudaFree(p->d_stamps);
   cudaFree(p->d_dbg);
+  cudaFree(p->d_rank_done);
   delete p;
 }
 
@@ -71,6 +73,8 @@ int zero_state(coll_plan_s *p) {
   if (p->d_cflag && cudaMemset(p->d_cflag, 0, (size_t)c.n_cflag * 4) != cudaSuccess)
     return COLL_ECUDA;
   if (p->d_dbg && cudaMemset(p->d_dbg, 0, (size_t)c.units.size() * 4) != cudaSuccess)
+    return COLL_ECUDA;
+  if (p->d_rank_done && cudaMemset(p->d_rank_done, 0, (size_t)c.R * 4) != cudaSuccess)
     return COLL_ECUDA;
   if (cudaMemset(p->d_status, 0, sizeof(coll_dev_status_t)) != cudaSuccess) return COLL_ECUDA;
   p->epochs_issued = 0;
@@ -144,6 +148,7 @@ extern "C" int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_
          (c.n_pflag == 0 || cudaMalloc(&p->d_pflag, (size_t)c.n_pflag * 2 * 8) == cudaSuccess) &&
          (c.n_cflag == 0 || cudaMalloc(&p->d_cflag, (size_t)c.n_cflag * 4) == cudaSuccess);
     if (ok && xb) ok = cudaMemset(p->d_xbuf, 0, xb) == cudaSuccess;
+    if (ok && c.cfg.chain) ok = cudaMalloc(&p->d_rank_done, (size_t)c.R * 4) == cudaSuccess;
     if (ok && (c.cfg.inject_flags & COLL_INJECT_SPEC_PAUSE) && !c.units.empty())
       ok = cudaMalloc(&p->d_dbg, c.units.size() * 4) == cudaSuccess;
     if (ok && c.cfg.record_stamps && c.cfg.stamp_capacity) {
@@ -270,6 +275,8 @@ extern "C" int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_
     a.st = p->d_status;
     a.stamps = p->d_stamps;
     a.dbg = p->d_dbg;
+    a.rank_done = p->d_rank_done;
+    a.chain = c.cfg.chain;
     a.stamp_cap = p->stamp_cap;
     a.stamp_phases = c.cfg.record_stamps == 2 ? 1u : 0u;
     a.n_pflag = c.n_pflag;

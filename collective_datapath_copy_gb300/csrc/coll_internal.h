@@ -63,7 +63,8 @@ struct coll_warp_t {
   uint32_t rank;
   uint32_t s0, s1;  // stage items
   uint32_t c0, c1;  // consume items
-  uint32_t pad[3];
+  uint32_t rank_warps;  // warps of this rank (chained epochs count them)
+  uint32_t pad[2];
 };
 
 // Device status block of a plan (zeroed at plan time and by coll_reset).

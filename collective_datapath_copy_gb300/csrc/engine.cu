@@ -386,6 +386,29 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
     }
 
     const bool pst = phases && (uint32_t)i < a.stamp_cap;
+    if (a.chain && a.rank_done) {
+      // dependent chain: wait until every warp of this rank finished epoch E-1's consume
+      bool ok = true;
+      if (lane == 0) {
+        const uint32_t target = W.rank_warps * (E - 1u);
+        uint64_t t0 = 0;
+        for (uint32_t k = 0; (int32_t)(ld_acquire_u32(a.rank_done + W.rank) - target) < 0; ++k) {
+          if ((k & 31u) == 31u) {
+            const uint64_t now = globaltimer();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > a.spin_ns || ld_relaxed_u32(&st->abort)) {
+              ok = false;
+              break;
+            }
+          }
+        }
+      }
+      if (!__all_sync(FULL, __shfl_sync(FULL, ok, 0))) {
+        if (lane == 0) record_timeout(st, (int)W.rank, -1, 4, E);
+        failed = true;
+        break;
+      }
+    }
     if (pst) a.stamps[1 + 4 * i] = globaltimer();
 
     // ---------------- Stage + Notify
@@ -555,6 +578,10 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
         if (lane == 0)
           st_release_u32(a.cflag + u.cflag0 + (it.slot == COLL_SLOT_ALL ? 0u : it.slot), E);
       }
+    }
+    if (a.chain && a.rank_done && !failed) {
+      __syncwarp();
+      if (lane == 0) red_release_add_u32(a.rank_done + W.rank, 1u);
     }
     if (pipelined && tagged && !nh_ready && !failed) {
       nh = __reduce_add_sync(FULL, lane < (su.nbytes >> 4) ? tag_part(nx, lane) : 0u);

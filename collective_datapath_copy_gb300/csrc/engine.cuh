@@ -45,6 +45,8 @@ struct EngArgs {
   coll_dev_status_t *st;
   uint64_t *stamps;           // [stamp_cap + 1] or null
   uint32_t *dbg;              // [n_units] handshake words of the SPEC_PAUSE injection
+  uint32_t *rank_done;        // [R] chained epochs: consume completions per rank
+  int32_t chain;
   uint32_t stamp_cap;
   uint32_t stamp_phases;  // 1: four stamps per epoch (start, notified, data ready, end)
   uint32_t n_pflag;

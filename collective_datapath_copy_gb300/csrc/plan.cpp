@@ -55,6 +55,7 @@ static int check_config(const coll_config_t &c) {
   if (c.warps_per_rank < 0 || c.ctas < 0) return COLL_EINVAL;
   if (c.tile_bytes < 0 || (c.tile_bytes % 16) != 0) return COLL_EINVAL;
   if (c.inject_prob_ppm > 1000000u) return COLL_EINVAL;
+  if (c.chain < 0 || c.chain > 1 || c.reserved2 != 0) return COLL_EINVAL;
   return COLL_OK;
 }
 
@@ -334,6 +335,7 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
       coll_warp_t &W = c.warps[w];
       memset(&W, 0, sizeof(W));
       W.rank = (uint32_t)r;
+      W.rank_warps = Wr;
       W.s0 = (uint32_t)c.sitems.size();
       for (uint32_t k : stage_of_warp[w]) {
         c.sitems.push_back(S[r][k]);
@@ -347,7 +349,6 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
       }
       W.c1 = (uint32_t)c.citems.size();
     }
-    (void)Wr;
   }
   // Dual buffers: restaging unit u (parity of epoch e) overwrites what u's consumers read
   // at epoch e-2. That is already ordered if every consumer warp of u notified epoch e-1

@@ -131,6 +131,11 @@ typedef struct {
   uint64_t inject_max_ns;   /* STAGGER: max delay; SPEC_PAUSE: producer's bounded wait */
   uint64_t inject_start_ns; /* STAGGER: rank r starts r * inject_start_ns late          */
   uint64_t inject_pause_ns; /* SPEC_PAUSE: consumer pause                              */
+  int32_t chain;            /* staged: 1 = rank r stages epoch e+1 only after every one of
+                               its consume items of epoch e is done (a dependent chain, as
+                               when the next layer needs the whole all-reduce output);
+                               0 = back-to-back independent epochs                       */
+  int32_t reserved2;        /* must be 0                                                */
 } coll_config_t;
 
 typedef struct {

@@ -240,11 +240,12 @@ def _check_epochs(outs, expect_dev, n_epochs, pool):
 
 @pytest.mark.parametrize("protocol", ["barrier", "dual", "spec"])
 @pytest.mark.parametrize("datapath", ["oneshot", "twoshot"])
-def test_decode_allreduce_epochs_bit_exact(protocol, datapath):
+@pytest.mark.parametrize("chain", [0, 1])
+def test_decode_allreduce_epochs_bit_exact(protocol, datapath, chain):
     R, n, pool, E = 8, 4096, 7, 2000
     ins, expect = _decode_case(R, n, pool)
     nm = namings.allreduce(R, n, "bf16")
-    plan = cdc.Plan(nm, protocol=protocol, datapath=datapath)
+    plan = cdc.Plan(nm, protocol=protocol, datapath=datapath, chain=chain)
     outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
     plan.run(ins, outs, n_epochs=E, in_epoch_stride=n * 2, in_pool=pool, out_epoch_stride=n * 2)
     st = plan.status()
