@@ -523,6 +523,10 @@ def run_workload(args):
         r["frac"] = round(r["gbs"] / peak, 4)
         r["rows_per_rank"] = nm.meta["counts"]
         res["combine"] = r
+        r2 = _zc_measure(torch, cdc, nm, ins, outs, args.steps, args.warmup, flush, stream,
+                         tma_min_bytes=(1 << 63))
+        r2["frac"] = round(r2["gbs"] / peak, 4)
+        res["combine_warp_kernel"] = r2
     elif args.workload == "moe":
         T, H, E, k = 4096, 7168, 256, 8
         routing = synth.zipf_topk_routing(5, R, T, E, k, 1.1)

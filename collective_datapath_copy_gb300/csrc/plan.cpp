@@ -184,12 +184,13 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
     // One warp per tile. Default tile: the largest power of two (512 B .. 32 KiB) that
     // still gives about four tiles per resident warp (32 per SM), so small collectives
     // spread over every SM and large ones keep per-tile overhead low.
-    uint64_t job_bytes = 0;
+    uint64_t job_bytes = 0, src_bytes = 0;
     uint32_t maxsrc = 0, maxdst = 0;
     bool aligned = true;
     for (auto &nm : names) {
       const uint64_t njobs = (!sum || twoshot) ? 1u : nm.cons.size();
       job_bytes += nm.count * es * njobs;
+      src_bytes += nm.count * es * njobs * (sum ? nm.prod.size() : 1u);
       maxsrc = std::max<uint32_t>(maxsrc, sum ? (uint32_t)nm.prod.size() : 1u);
       maxdst = std::max<uint32_t>(maxdst, (!sum || twoshot) ? (uint32_t)nm.cons.size() : 1u);
       if ((nm.count * es) & 15u) aligned = false;
@@ -201,9 +202,15 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
     const uint64_t sms = (uint64_t)(num_sms > 0 ? num_sms : 152);
     // Large aligned plans use the bulk (TMA) ring: one CTA per SM, tiles of
     // 32 KiB / (producers rounded up to a power of two), at least four tiles per CTA.
+    // The ring's stages are sized for the largest producer count; jobs with fewer
+    // producers leave stage space idle, so the ring is used only when jobs fill at least
+    // three quarters of it on average (uniform collectives); uneven ones (MoE combine)
+    // stay on the warp kernel.
     const uint64_t bulk_min = cfg.tma_min_bytes ? cfg.tma_min_bytes : (4ull << 20);
+    const bool filled = maxsrc > 0 && src_bytes * 4 >= job_bytes * maxsrc * 3;
     c.bulk = aligned && maxsrc >= 1 && maxsrc <= COLL_BULK_MAX_SRC &&
-             maxdst <= COLL_BULK_MAX_DST && job_bytes >= bulk_min && !cfg.tile_bytes;
+             maxdst <= COLL_BULK_MAX_DST && job_bytes >= bulk_min && !cfg.tile_bytes &&
+             (filled || cfg.tma_min_bytes != 0);
     uint64_t T = cfg.tile_bytes ? (uint64_t)cfg.tile_bytes : 0;
     if (c.bulk) {
       uint32_t p2 = 1;
