@@ -40,6 +40,32 @@ R_DECODE, N_DECODE, POOL, EPOCHS = 8, 4096, 7, 10000
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
 
 
+ENGINE_SOURCES = ["engine.cu", "atom.cuh", "engine.cuh", "coll_internal.h"]
+
+
+def sources_sha256(names):
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "collective_datapath_copy_gb300", "csrc")
+    for n in names:
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(kernel, names):
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json), only if
+    it was taken on the current sources of that kernel; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel)
+    if not d or d.get("sources_sha256") != sources_sha256(names):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -321,7 +347,8 @@ def run_ours(args, rank, world, dist):
                    "step (256 MiB write)", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 5),
-                     "traffic": None, "peak_kind": f"of {peak_kind}",
+                     "traffic": recorded_traffic("engine_kernel", ENGINE_SOURCES),
+                     "peak_kind": f"of {peak_kind}",
                      "note": "latency-bound: 128 KiB of algorithmic bytes per epoch"},
         "latency": lat,
         "phases": phases,
@@ -555,7 +582,12 @@ def main():
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "sweep", "prefill", "moe", "moe_combine", "fig15"])
     ap.add_argument("--max-bytes", type=int, default=0, help="sweep: largest bytes per rank")
+    ap.add_argument("--print-sources-sha", action="store_true",
+                    help="print the sha256 of the engine kernel's sources and exit")
     args = ap.parse_args()
+    if args.print_sources_sha:
+        print(sources_sha256(ENGINE_SOURCES))
+        return
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
