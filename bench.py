@@ -144,6 +144,16 @@ def _decode_inputs(torch, dev):
     return pool_np, host, ins
 
 
+def max_over_ranks(value, dist, device):
+    """The slowest replica's time (every rank must call this; dist None = one process)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def make_flush(torch, dev):
     """L2 flush between timed steps: write a 256 MiB buffer (> L2), then read another
     256 MiB buffer so the dirty lines of the write are written back before the timed step
@@ -227,11 +237,7 @@ def run_ours(args, rank, world, dist):
     st = plans["spec"].status()
     if st["code"] != 0:
         raise RuntimeError(f"spec run failed: {st}")
-    ms = sum(times) / len(times)
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(times) / len(times), dist, dev)
     us_epoch = ms * 1000.0 / EPOCHS
 
     # other protocols (same K/W)

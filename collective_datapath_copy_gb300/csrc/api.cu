@@ -255,7 +255,7 @@ extern "C" int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_
       err = coll::launch_bulk(c.op, c.dtype, a, c.cfg.ctas ? c.cfg.ctas : p->num_sms, s);
     } else {
       const int ctas = c.cfg.ctas ? c.cfg.ctas : 3 * p->num_sms;
-      const int keep = (c.op == COLL_OP_SUM && c.cfg.datapath == COLL_DP_ONESHOT) ? 1 : 0;
+      const int keep = c.zc_keep ? 1 : 0;
       err = coll::launch_zero_copy(c.op, c.dtype, keep, a, ctas, s);
     }
   } else {

@@ -94,6 +94,8 @@ struct coll_compiled {
   std::vector<coll_unit_t> units;
   std::vector<coll_item_t> sitems, citems;
   std::vector<coll_warp_t> warps;
+  bool zc_keep = false;       // zero-copy: inputs are re-read (one-shot sums with several
+                              // consumers per name): keep them cacheable
   bool bulk = false;          // zero-copy tiles sized for the bulk (TMA) kernel
   uint32_t bulk_slot = 0;     // bytes of one staged piece (= tile size)
   uint32_t bulk_maxsrc = 0;   // slots per stage

@@ -189,6 +189,7 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
     bool aligned = true;
     for (auto &nm : names) {
       const uint64_t njobs = (!sum || twoshot) ? 1u : nm.cons.size();
+      if (njobs > 1) c.zc_keep = true;
       job_bytes += nm.count * es * njobs;
       src_bytes += nm.count * es * njobs * (sum ? nm.prod.size() : 1u);
       maxsrc = std::max<uint32_t>(maxsrc, sum ? (uint32_t)nm.prod.size() : 1u);
