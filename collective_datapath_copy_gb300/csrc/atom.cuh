@@ -179,10 +179,7 @@ struct Vec16Acc {
 
 // ------------------------------------------------------------------ content tag
 
-// Contribution of vector `vi` (its index inside the piece) to the piece's tag: every 32-bit
-// word is salted by its position and passed through a full-avalanche mixer (two
-// multiply/xor-shift rounds), and the results are summed, so lanes can be reduced in any
-// order and any change of any bit changes the sum except with probability about 2^-32.
+// Full-avalanche 32-bit mixer (two multiply / xor-shift rounds).
 __device__ __forceinline__ uint32_t fmix(uint32_t x) {
   x ^= x >> 16;
   x *= 0x7FEB352Du;
@@ -192,38 +189,25 @@ __device__ __forceinline__ uint32_t fmix(uint32_t x) {
   return x;
 }
 
+// Contribution of vector `vi` (its index inside the piece) to the piece's tag: each word is
+// salted by its position and multiplied by an odd constant (a bijection), the four products
+// are rotated apart and combined, and one full-avalanche round per vector follows, so that
+// the sum over vectors (lanes may be reduced in any order) changes with any change of the
+// bytes except with probability about 2^-32.
 __device__ __forceinline__ uint32_t tag_part(uint4 v, uint32_t vi) {
   const uint32_t s = vi * 0x9E3779B9u;
-  return fmix(v.x ^ s) + fmix(v.y ^ (s + 0x632BE5ABu)) + fmix(v.z ^ (s + 0x165667B1u)) +
-         fmix(v.w ^ (s + 0xD3A2646Cu));
+  const uint32_t a = (v.x ^ s) * 0x85EBCA77u;
+  const uint32_t b = (v.y ^ (s + 0x632BE5ABu)) * 0xC2B2AE3Du;
+  const uint32_t c = (v.z ^ (s + 0x165667B1u)) * 0x27D4EB2Fu;
+  const uint32_t d = (v.w ^ (s + 0xD3A2646Cu)) * 0x9E3779B1u;
+  return fmix(a ^ __funnelshift_l(b, b, 8) ^ __funnelshift_l(c, c, 16) ^
+              __funnelshift_l(d, d, 24));
 }
 
-// Warp reduce-scatter of eight per-lane values: lane L returns the sum over all 32 lanes of
-// h[L & 7] (three halving exchange rounds on lane bits 2, 1, 0, then two full rounds).
-__device__ __forceinline__ uint32_t reduce_scatter8(const uint32_t h[8], uint32_t lane) {
-  const bool b2 = lane & 4u, b1 = lane & 2u, b0 = lane & 1u;
-  uint32_t w[4], u[2];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t send = b2 ? h[i] : h[4 + i];
-    const uint32_t keep = b2 ? h[4 + i] : h[i];
-    w[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint32_t send = b1 ? w[i] : w[2 + i];
-    const uint32_t keep = b1 ? w[2 + i] : w[i];
-    u[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 2);
-  }
-  const uint32_t send = b0 ? u[0] : u[1];
-  uint32_t z = (b0 ? u[1] : u[0]) + __shfl_xor_sync(0xFFFFFFFFu, send, 1);
-  z += __shfl_xor_sync(0xFFFFFFFFu, z, 8);
-  z += __shfl_xor_sync(0xFFFFFFFFu, z, 16);
-  return z;
-}
-
+// A piece's tag: its hash plus the epoch times an odd constant (linear, so that tags of
+// several producers can be checked as one sum).
 __device__ __forceinline__ uint32_t tag_fold(uint32_t h, uint32_t epoch) {
-  return fmix(h + epoch * 0x85EBCA6Bu);
+  return h + epoch * 0x85EBCA6Bu;
 }
 
 }  // namespace coll

@@ -275,6 +275,18 @@ __device__ __forceinline__ uint4 gather_pieces(const char *xb, uint32_t nbytes, 
 // Speculatively load (and reduce) the n pieces of a unit, issue the flag loads while the
 // payload loads are in flight, and hash what was loaded (per producer, warp-reduced; lane j
 // keeps producer j's hash). Returns the packed result of this attempt.
+// Validation of a speculative load: lane j < n holds producer j's flag word {epoch, tag}
+// and every lane holds its share of the hash of what it loaded. Passes iff every producer
+// notified epoch E and the producers' tags (hash + E*K each) add up to the loaded hash plus
+// n*E*K, i.e. the loaded bytes are the notified bytes (up to a 2^-32 collision).
+__device__ __forceinline__ bool tags_match(unsigned long long f, uint32_t myh, uint32_t n,
+                                           uint32_t E, uint32_t lane) {
+  const uint32_t ftag = __reduce_add_sync(FULL, lane < n ? (uint32_t)f : 0u);
+  const uint32_t htot = __reduce_add_sync(FULL, myh);
+  const bool epochs = __all_sync(FULL, lane >= n || (uint32_t)(f >> 32) == E);
+  return epochs && ftag == htot + n * tag_fold(0u, E);
+}
+
 // If `side` is set, the warp also hashes `side_v` (the prefetched next input piece, lanes
 // below side_nvec) into side_h while the first batch of loads is in flight.
 template <int KIND>
@@ -304,12 +316,10 @@ __device__ __forceinline__ uint4 spec_attempt(const char *xb, uint32_t nbytes, u
         }
     }
     if (want_hash) {
-      // per-producer hashes of this batch: lane k0+j receives producer k0+j's sum
-      uint32_t hk[8];
+      // this lane's share of every producer's hash, summed: the check compares totals
 #pragma unroll
-      for (uint32_t k = 0; k < 8; ++k) hk[k] = (k < kn && active) ? tag_part(x[k], lane) : 0u;
-      const uint32_t hs = reduce_scatter8(hk, lane);
-      if (lane >= k0 && lane < k0 + 8) myh = hs;
+      for (uint32_t k = 0; k < 8; ++k)
+        if (k < kn && active) myh += tag_part(x[k], lane);
     }
   }
   return active ? acc.pack() : make_uint4(0, 0, 0, 0);
@@ -359,10 +369,14 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
   uint4 nx = make_uint4(0, 0, 0, 0);
   uint32_t nh = 0;
   bool nh_ready = false;
+  const char *sin_base = nullptr;  // single stage item: its input piece at pool entry 0
+  char *cout_base = nullptr;        // single consume item: its output piece at epoch 0
+  if (single_c) cout_base = a.ptr.out[cref.rank] + cref.off + cu.start;
   if (pipelined) {
     sit = a.sitems[W.s0];
     su = a.units[sit.unit];
     sref = a.refs[su.src0 + sit.slot];
+    sin_base = a.ptr.in[sref.rank] + sref.off + su.start;
     if (lane < (su.nbytes >> 4) && a.n_epochs > 0)
       nx = ld_nc_v4(a.ptr.in[sref.rank] + sref.off + su.start + lane * 16);
   }
@@ -373,10 +387,18 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
   const bool phases = stamp && a.stamp_phases;
   if (stamp) a.stamps[0] = globaltimer();
 
+  // input-pool offset of epoch i and of epoch i+1, advanced without division (a runtime
+  // modulo costs a long dependent chain on this single-warp critical path)
+  int64_t in_off = 0, in_off_next = a.in_pool > 1 ? a.in_stride : 0;
+  int32_t pool_next = a.in_pool > 1 ? 1 : 0;
   for (int i = 0; i < a.n_epochs && !failed; ++i) {
     const uint32_t E = a.epoch_base + (uint32_t)i + 1u;
     const uint32_t b = (a.protocol == COLL_PROTO_BARRIER) ? 0u : (E & 1u);
-    const int64_t in_off = (int64_t)(i % a.in_pool) * a.in_stride;
+    if (i > 0) {
+      in_off = in_off_next;
+      pool_next = pool_next + 1 == a.in_pool ? 0 : pool_next + 1;
+      in_off_next = (int64_t)pool_next * a.in_stride;
+    }
     const int64_t out_off = (int64_t)i * a.out_stride;
 
     if ((a.inject_flags & COLL_INJECT_STAGGER) && a.inject_prob_ppm) {
@@ -457,9 +479,7 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
       }
       if (pipelined) {
         nh_ready = false;
-        if (i + 1 < a.n_epochs && lane < nvec)
-          nx = ld_nc_v4(a.ptr.in[sref.rank] + sref.off +
-                        (int64_t)((i + 1) % a.in_pool) * a.in_stride + su.start + lane * 16);
+        if (i + 1 < a.n_epochs && lane < nvec) nx = ld_nc_v4(sin_base + in_off_next + lane * 16);
       }
     }
     if (failed) break;
@@ -494,13 +514,12 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
           if (lane < n) f = relaxed ? ld_relaxed_u64(pf + lane) : ld_acquire_u64(pf + lane);
         }
         uint32_t fe = (uint32_t)(f >> 32);
-        bool lane_ok = lane >= n || (fe == E && (!tagged || (uint32_t)f == tag_fold(myh, E)));
         bool ok;
         if (literal) {
           const uint32_t sum = __reduce_add_sync(FULL, lane < n ? fe : 0u);
           ok = sum == n * E;
         } else {
-          ok = __all_sync(FULL, lane_ok);
+          ok = tags_match(f, myh, n, E, lane);
         }
         ++n_checks;
         if (ok) {
@@ -517,8 +536,7 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
               res = spec_attempt<KIND>(xb, u.nbytes, n, lane, active, true, pf, false, true, f,
                                        myh, false, nx, 0u, unused);
               fe = (uint32_t)(f >> 32);
-              lane_ok = lane >= n || (fe == E && (uint32_t)f == tag_fold(myh, E));
-              if (__all_sync(FULL, lane_ok)) {
+              if (tags_match(f, myh, n, E, lane)) {
                 have = true;
                 break;
               }
@@ -568,8 +586,10 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
             const coll_ref_t r = a.refs[u.dst0 + d];
             st_v4(a.ptr.out[r.rank] + r.off + out_off + u.start + lane * 16, res);
           }
+        } else if (single_c) {
+          st_v4(cout_base + out_off + lane * 16, res);
         } else {
-          const coll_ref_t r = single_c ? cref : a.refs[u.dst0 + it.slot];
+          const coll_ref_t r = a.refs[u.dst0 + it.slot];
           st_v4(a.ptr.out[r.rank] + r.off + out_off + u.start + lane * 16, res);
         }
       }
