@@ -1,0 +1,142 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check the pins catch each one.
+
+Each mutant replaces one piece of the oracle's arithmetic or layout logic with a subtly
+wrong version; at least one pin (hand-worked fixtures, exact-rational brute force, direct
+definitions, closed forms) must then fail. This shows the pins constrain the oracle rather
+than merely agreeing with it.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import arith, brute, collectives, naming
+import synth
+
+import test_oracle as pins
+
+
+def _golden_ok():
+    try:
+        for row in pins._read_sum_fixtures():
+            pins.test_golden_sum_rounding(row)
+    except AssertionError:
+        return False
+    return True
+
+
+def _brute_ok():
+    try:
+        for seed in range(12):
+            for op, dt in (("sum", "bf16"), ("sum", "f32"), ("copy", "bf16")):
+                pins.test_naming_matches_brute_force(seed, op, dt)
+        for dt in ("bf16", "f32"):
+            for R in (3, 8):
+                pins.test_ordered_sum_matches_exact_sequential_rounding(dt, R)
+    except AssertionError:
+        return False
+    return True
+
+
+def _collectives_ok():
+    try:
+        pins.test_allreduce_direct_equals_naming_and_rs_then_ag("bf16")
+        pins.test_reduce_scatter_alltoall_allgather_broadcast_by_naming()
+        pins.test_alltoall_twice_is_identity_and_conserves_bytes()
+        for k in (3, 8):
+            pins.test_identical_inputs_closed_form(k)
+        pins.test_small_integer_sums_are_exact()
+        pins.test_moe_dispatch_golden_fixture()
+    except AssertionError:
+        return False
+    return True
+
+
+def _all_pins_pass():
+    return _golden_ok() and _brute_ok() and _collectives_ok()
+
+
+def test_unmutated_oracle_passes_every_pin():
+    assert _all_pins_pass()
+
+
+def _reversed_sum(terms, dtype):
+    return ORIG_SUM(list(terms)[::-1], dtype)
+
+
+def _dropped_last(terms, dtype):
+    t = list(terms)
+    return ORIG_SUM(t[:-1] if len(t) > 1 else t, dtype)
+
+
+def _bf16_each_step(terms, dtype):
+    if dtype != "bf16":
+        return ORIG_SUM(terms, dtype)
+    acc = arith.bf16_to_f32(terms[0]).copy()
+    for t in terms[1:]:
+        acc = arith.bf16_to_f32(arith.f32_to_bf16_rne(acc + arith.bf16_to_f32(t)))
+    return arith.f32_to_bf16_rne(acc)
+
+
+def _start_from_plus_zero(terms, dtype):
+    acc = np.zeros(len(terms[0]), dtype=np.float32)
+    for t in terms:
+        acc = acc + arith.to_f32(t, dtype)
+    return arith.f32_to_bf16_rne(acc) if dtype == "bf16" else acc
+
+
+def _truncate_bf16(x):
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    return (u >> np.uint32(16)).astype(np.uint16)
+
+
+def _round_half_up_bf16(x):
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    with np.errstate(over="ignore"):
+        return ((u + np.uint32(0x8000)) >> np.uint32(16)).astype(np.uint16)
+
+
+ORIG_SUM = arith.ordered_sum
+ORIG_RNE = arith.f32_to_bf16_rne
+
+SUM_MUTANTS = {"reversed order": _reversed_sum, "dropped term": _dropped_last,
+               "bf16 rounding after every add": _bf16_each_step,
+               "accumulator starts at +0.0": _start_from_plus_zero}
+RNE_MUTANTS = {"truncation": _truncate_bf16, "round half up": _round_half_up_bf16}
+
+
+@pytest.mark.parametrize("name", sorted(SUM_MUTANTS))
+def test_pins_catch_summation_mutants(name, monkeypatch):
+    fn = SUM_MUTANTS[name]
+    monkeypatch.setattr(arith, "ordered_sum", fn)
+    monkeypatch.setattr(naming, "ordered_sum", fn)
+    monkeypatch.setattr(collectives, "ordered_sum", fn)
+    assert not _all_pins_pass(), name
+
+
+@pytest.mark.parametrize("name", sorted(RNE_MUTANTS))
+def test_pins_catch_rounding_mutants(name, monkeypatch):
+    monkeypatch.setattr(arith, "f32_to_bf16_rne", RNE_MUTANTS[name])
+    assert not _all_pins_pass(), name
+
+
+def test_pins_catch_a_transposed_alltoall(monkeypatch):
+    def wrong(xs):
+        R = len(xs)
+        b = len(xs[0]) // R
+        # block s of source d instead of block d of source s
+        return [np.concatenate([xs[d][s * b:(s + 1) * b] for s in range(R)]) for d in range(R)]
+    monkeypatch.setattr(collectives, "alltoall", wrong)
+    assert not _collectives_ok()
+
+
+def test_pins_catch_copy_from_the_wrong_producer(monkeypatch):
+    orig = naming.run_naming
+
+    def wrong(R, op, dtype, in_len, in_segs, out_len, out_segs, inputs, outputs):
+        if op == "copy" and in_segs:
+            # shift every producer's offset by one element where that stays in bounds
+            in_segs = [(r, off + 1 if off + c < in_len[r] else off, c, nm)
+                       for (r, off, c, nm) in in_segs]
+        return orig(R, op, dtype, in_len, in_segs, out_len, out_segs, inputs, outputs)
+    monkeypatch.setattr(naming, "run_naming", wrong)
+    assert not _all_pins_pass()
