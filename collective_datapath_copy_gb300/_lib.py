@@ -42,6 +42,7 @@ PROTOCOL = {"barrier": D["COLL_PROTO_BARRIER"], "dual": D["COLL_PROTO_DUAL"],
 DATAPATH = {"oneshot": D["COLL_DP_ONESHOT"], "twoshot": D["COLL_DP_TWOSHOT"]}
 SPEC_CHECK = {"tagged": D["COLL_SPEC_TAGGED"], "literal": D["COLL_SPEC_LITERAL"],
               "relaxed": D["COLL_SPEC_TAGGED_RELAXED"]}
+ORDER = {"rank": D["COLL_ORDER_RANK"], "tree": D["COLL_ORDER_TREE"]}
 INJECT = {"skip_notify": D["COLL_INJECT_SKIP_NOTIFY"], "stagger": D["COLL_INJECT_STAGGER"],
           "spec_pause": D["COLL_INJECT_SPEC_PAUSE"]}
 
@@ -59,7 +60,8 @@ class Config(C.Structure):
                 ("inject_rank", C.c_int32), ("inject_prob_ppm", C.c_uint32),
                 ("inject_max_ns", C.c_uint64), ("inject_start_ns", C.c_uint64),
                 ("inject_pause_ns", C.c_uint64), ("chain", C.c_int32),
-                ("reserved2", C.c_int32)]
+                ("reserved2", C.c_int32), ("reduce_order", C.c_int32),
+                ("reserved3", C.c_int32)]
 
 
 class PlanInfo(C.Structure):
@@ -137,6 +139,8 @@ def make_config(**kw) -> Config:
             v = PROTOCOL[v] if isinstance(v, str) else v
         elif k == "datapath":
             v = DATAPATH[v] if isinstance(v, str) else v
+        elif k == "reduce_order":
+            v = ORDER[v] if isinstance(v, str) else v
         elif k == "spec_check":
             v = SPEC_CHECK[v] if isinstance(v, str) else v
         elif k == "inject":

@@ -240,6 +240,7 @@ extern "C" int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_
     a.out_stride = out_epoch_stride;
     a.st = p->d_status;
     a.spin_ns = c.cfg.spin_limit_ns ? c.cfg.spin_limit_ns : 2000000000ull;
+    a.tree = c.cfg.reduce_order == COLL_ORDER_TREE ? 1u : 0u;
     bool bulk = c.bulk;
     if (bulk) {  // the bulk copies need 16-byte-aligned bases and strides at run time
       for (int r = 0; r < R && bulk; ++r) {

@@ -175,7 +175,32 @@ struct Vec16Acc {
   __device__ __forceinline__ uint4 pack() const {
     if constexpr (DT == 0) return bf16x8_pack(a); else return f32x4_pack(a);
   }
+  __device__ __forceinline__ void addf(const Vec16Acc &o) {
+#pragma unroll
+    for (int i = 0; i < (DT == 0 ? 8 : 4); ++i) a[i] = __fadd_rn(a[i], o.a[i]);
+  }
 };
+
+// Pairwise (tree) sum of the first kn (<= 8) vectors: ((x0+x1)+(x2+x3))+((x4+x5)+(x6+x7)),
+// an unpaired element carried up a level. Accumulated into acc (which starts from this
+// group's sum when `first`).
+template <int DT>
+__device__ __forceinline__ void tree8(Vec16Acc<DT> &acc, bool first, const uint4 x[8],
+                                      uint32_t kn) {
+  Vec16Acc<DT> p[4];
+  const uint32_t np = (kn + 1) / 2;
+#pragma unroll
+  for (uint32_t i = 0; i < 4; ++i) {
+    if (i < np) {
+      p[i].init(x[2 * i]);
+      if (2 * i + 1 < kn) p[i].add(x[2 * i + 1]);
+    }
+  }
+  if (1 < np) p[0].addf(p[1]);
+  if (3 < np) p[2].addf(p[3]);
+  if (2 < np) p[0].addf(p[2]);
+  if (first) acc = p[0]; else acc.addf(p[0]);
+}
 
 // ------------------------------------------------------------------ content tag
 

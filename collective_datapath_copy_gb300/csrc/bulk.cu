@@ -95,7 +95,7 @@ __device__ void bulk_timeout(coll_dev_status_t *st, uint32_t tile) {
 }
 
 // KIND: 0 copy, 1 sum of bf16, 2 sum of f32.
-template <int KIND>
+template <int KIND, bool TREE>
 __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ volatile uint32_t s_abort;
@@ -228,10 +228,14 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
           for (uint32_t j = 0; j < COLL_BULK_MAX_SRC; ++j)
             if (j < nsrc) x[j] = sd[(size_t)j * slot_vec + v];
           Vec16Acc<KIND - 1> acc;
-          acc.init(x[0]);
+          if constexpr (TREE) {
+            tree8<KIND - 1>(acc, true, x, nsrc);
+          } else {
+            acc.init(x[0]);
 #pragma unroll
-          for (uint32_t j = 1; j < COLL_BULK_MAX_SRC; ++j)
-            if (j < nsrc) acc.add(x[j]);
+            for (uint32_t j = 1; j < COLL_BULK_MAX_SRC; ++j)
+              if (j < nsrc) acc.add(x[j]);
+          }
           r = acc.pack();
         }
         for (uint32_t d = 0; d < ndst; ++d) st_cs_v4(h.dst[d] + (size_t)v * 16, r);
@@ -264,9 +268,9 @@ cudaError_t launch_bulk(int op, int dtype, const ZcArgs &a, int ctas, cudaStream
   const int grid = (int)((uint64_t)ctas < total ? (uint64_t)ctas : total);
   const uint32_t smem = bulk_smem_bytes(a.stages, a.maxsrc, a.slot_bytes);
   const void *fn;
-  if (op == COLL_OP_COPY) fn = (const void *)bulk_kernel<0>;
-  else if (dtype == COLL_BF16) fn = (const void *)bulk_kernel<1>;
-  else fn = (const void *)bulk_kernel<2>;
+  if (op == COLL_OP_COPY) fn = (const void *)bulk_kernel<0, false>;
+  else if (dtype == COLL_BF16) fn = a.tree ? (const void *)bulk_kernel<1, true> : (const void *)bulk_kernel<1, false>;
+  else fn = a.tree ? (const void *)bulk_kernel<2, true> : (const void *)bulk_kernel<2, false>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   void *args[] = {(void *)&a};

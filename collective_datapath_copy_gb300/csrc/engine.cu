@@ -37,8 +37,8 @@ __device__ __forceinline__ uint4 zc_load(const char *p) {
 // tile (up to 32 each); the vector loops fetch them with shuffles. Tiles with more than 32
 // producers or consumers, or with an address not 16-byte aligned, take the element-wise
 // path (same arithmetic, same order).
-template <int KIND, bool KEEP>
-__global__ void __launch_bounds__(256, 3) zc_kernel(const ZcArgs a) {
+template <int KIND, bool KEEP, bool TREE>
+__global__ void __launch_bounds__(256, TREE ? 2 : 3) zc_kernel(const ZcArgs a) {
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t gw = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint64_t nw = ((uint64_t)gridDim.x * blockDim.x) >> 5;
@@ -102,11 +102,15 @@ __global__ void __launch_bounds__(256, 3) zc_kernel(const ZcArgs a) {
               if (k < kn && act) x[k] = zc_load<KIND, KEEP>(p + (size_t)v * 16);
             }
             if (act) {
+              if constexpr (TREE) {
+                tree8<KIND - 1>(acc, k0 == 0, x, kn);
+              } else {
 #pragma unroll
-              for (uint32_t k = 0; k < 8; ++k)
-                if (k < kn) {
-                  if (k0 + k == 0) acc.init(x[k]); else acc.add(x[k]);
-                }
+                for (uint32_t k = 0; k < 8; ++k)
+                  if (k < kn) {
+                    if (k0 + k == 0) acc.init(x[k]); else acc.add(x[k]);
+                  }
+              }
             }
           }
           const uint4 r = act ? acc.pack() : make_uint4(0, 0, 0, 0);
@@ -668,13 +672,22 @@ cudaError_t launch_zero_copy(int op, int dtype, int keep, const ZcArgs &a, int c
   const uint64_t need = (total + 7) / 8;  // 8 warps per CTA
   const int grid = (int)((uint64_t)ctas < need ? (uint64_t)ctas : need);
   const dim3 block(256);
+  if (a.tree && kind != 0) {
+    switch (kind * 2 + (keep ? 1 : 0)) {
+      case 2: zc_kernel<1, false, true><<<grid, block, 0, s>>>(a); break;
+      case 3: zc_kernel<1, true, true><<<grid, block, 0, s>>>(a); break;
+      case 4: zc_kernel<2, false, true><<<grid, block, 0, s>>>(a); break;
+      default: zc_kernel<2, true, true><<<grid, block, 0, s>>>(a); break;
+    }
+    return cudaGetLastError();
+  }
   switch (kind * 2 + (keep ? 1 : 0)) {
-    case 0: zc_kernel<0, false><<<grid, block, 0, s>>>(a); break;
-    case 1: zc_kernel<0, true><<<grid, block, 0, s>>>(a); break;
-    case 2: zc_kernel<1, false><<<grid, block, 0, s>>>(a); break;
-    case 3: zc_kernel<1, true><<<grid, block, 0, s>>>(a); break;
-    case 4: zc_kernel<2, false><<<grid, block, 0, s>>>(a); break;
-    default: zc_kernel<2, true><<<grid, block, 0, s>>>(a); break;
+    case 0: zc_kernel<0, false, false><<<grid, block, 0, s>>>(a); break;
+    case 1: zc_kernel<0, true, false><<<grid, block, 0, s>>>(a); break;
+    case 2: zc_kernel<1, false, false><<<grid, block, 0, s>>>(a); break;
+    case 3: zc_kernel<1, true, false><<<grid, block, 0, s>>>(a); break;
+    case 4: zc_kernel<2, false, false><<<grid, block, 0, s>>>(a); break;
+    default: zc_kernel<2, true, false><<<grid, block, 0, s>>>(a); break;
   }
   return cudaGetLastError();
 }

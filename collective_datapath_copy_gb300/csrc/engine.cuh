@@ -28,7 +28,7 @@ struct ZcArgs {
   uint32_t slot_bytes;    // bulk kernel: bytes per staged piece
   uint32_t stages;        // bulk kernel: ring depth
   uint32_t maxsrc;        // bulk kernel: slots per stage
-  uint32_t pad2;
+  uint32_t tree;          // 1: pairwise (tree) summation order within groups of 8
 };
 
 struct EngArgs {

@@ -55,7 +55,10 @@ static int check_config(const coll_config_t &c) {
   if (c.warps_per_rank < 0 || c.ctas < 0) return COLL_EINVAL;
   if (c.tile_bytes < 0 || (c.tile_bytes % 16) != 0) return COLL_EINVAL;
   if (c.inject_prob_ppm > 1000000u) return COLL_EINVAL;
-  if (c.chain < 0 || c.chain > 1 || c.reserved2 != 0) return COLL_EINVAL;
+  if (c.chain < 0 || c.chain > 1 || c.reserved2 != 0 || c.reserved3 != 0) return COLL_EINVAL;
+  if (c.reduce_order < 0 || c.reduce_order > 1) return COLL_EINVAL;
+  // the staged engine always sums in rank order
+  if (c.reduce_order != COLL_ORDER_RANK && !c.zero_copy) return COLL_EINVAL;
   return COLL_OK;
 }
 

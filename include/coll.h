@@ -72,6 +72,13 @@ extern "C" {
 #define COLL_DP_ONESHOT 0
 #define COLL_DP_TWOSHOT 1
 
+/* Summation order of sums (zero-copy plans). RANK is the fixed rank order and is
+ * bit-exact; TREE adds each group of up to 8 producers pairwise ((x0+x1)+(x2+x3))+...,
+ * groups in order: a different rounding order, accurate to the first-order bound of any
+ * summation order, (n-1) * 2^-24 * sum|x|, plus the output rounding. */
+#define COLL_ORDER_RANK 0
+#define COLL_ORDER_TREE 1
+
 /* Speculative validation rules (COLL_PROTO_SPEC). */
 #define COLL_SPEC_TAGGED 0  /* flag epochs AND a content tag per piece must match (sound) */
 #define COLL_SPEC_LITERAL 1 /* only sum of flag epochs == n * epoch (the pages' rule);
@@ -136,6 +143,8 @@ typedef struct {
                                when the next layer needs the whole all-reduce output);
                                0 = back-to-back independent epochs                       */
   int32_t reserved2;        /* must be 0                                                */
+  int32_t reduce_order;     /* COLL_ORDER_*; zero-copy plans only                      */
+  int32_t reserved3;        /* must be 0                                                */
 } coll_config_t;
 
 typedef struct {

@@ -605,3 +605,29 @@ def test_fig15_cells_bit_exact(R, kb, protocol, datapath):
     assert plan.status()["code"] == 0
     assert _check_epochs(outs, expect, E, pool) == 0
     plan.free()
+
+
+# ------------------------------------------------------------ tolerance mode (tree order)
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("n_bytes,kind", [(1 << 16, "allreduce"), (1 << 23, "allreduce"),
+                                          (1 << 16, "reduce_scatter"), (1 << 23, "reduce_scatter")])
+def test_tree_order_sums_within_tolerance(dtype, n_bytes, kind):
+    from oracle import tolerance
+    R = 8
+    es = 2 if dtype == "bf16" else 4
+    n = n_bytes // es
+    rng = synth.seeded_rng(95)
+    xs = [gen("normal", rng, n, dtype) for _ in range(R)]
+    nm = getattr(namings, kind)(R, n, dtype)
+    for dp in ("oneshot", "twoshot"):
+        got, _ = run_once(nm, xs, zero_copy=1, reduce_order="tree", datapath=dp)
+        for r in range(R):
+            terms = xs if kind == "allreduce" else [x[r * (n // R):(r + 1) * (n // R)] for x in xs]
+            ok = tolerance.within_tolerance(got[r], terms, dtype)
+            assert ok.all(), (dp, r, int((~ok).sum()))
+
+
+def test_staged_plans_reject_the_tree_order():
+    with pytest.raises(cdc.CollError):
+        cdc.Plan(namings.allreduce(2, 1024, "bf16"), reduce_order="tree")

@@ -449,3 +449,56 @@ def test_moe_combine_is_the_ordered_sum_over_destinations():
             for h in range(H):
                 want = brute.element_sum([brute.decode_bf16(int(r[h])) for r in rows], "bf16")
                 assert brute.decode_bf16(int(out[s_][t, h])).key() == want.key()
+
+
+# ---------------------------------------------------------------- tolerance (other orders)
+
+def _other_order_sum(terms, dtype, order):
+    """A fp32 sum in another order, written out here to exercise the tolerance."""
+    vals = [arith.to_f32(t, dtype) for t in terms]
+    if order == "reversed":
+        vals = vals[::-1]
+    if order == "tree":
+        while len(vals) > 1:
+            vals = [vals[i] + vals[i + 1] if i + 1 < len(vals) else vals[i]
+                    for i in range(0, len(vals), 2)]
+        acc = vals[0]
+    else:
+        acc = vals[0].copy()
+        for v in vals[1:]:
+            acc = acc + v
+    return arith.f32_to_bf16_rne(acc) if dtype == "bf16" else acc
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("order", ["rank", "reversed", "tree"])
+def test_any_summation_order_is_within_tolerance(dtype, order):
+    from oracle import tolerance
+    rng = synth.seeded_rng(300)
+    for R in (2, 3, 8, 17):
+        xs = [synth.normal_bf16(rng, 4000) if dtype == "bf16" else
+              synth.normal_f32(rng, 4000) * np.float32(2.0) ** rng.integers(-20, 20, 4000).astype(np.float32)
+              for _ in range(R)]
+        got = _other_order_sum(xs, dtype, order) if order != "rank" else arith.ordered_sum(xs, dtype)
+        assert tolerance.within_tolerance(got, xs, dtype).all(), (R, order)
+
+
+def test_tolerance_rejects_real_errors():
+    from oracle import tolerance
+    rng = synth.seeded_rng(301)
+    xs = [synth.normal_bf16(rng, 4000) for _ in range(8)]
+    good = arith.ordered_sum(xs, "bf16")
+    # two bf16 ulps off: rejected wherever the exact sum is not tiny against sum |x|
+    bad = (good.astype(np.int32) + 2).astype(np.uint16)
+    ok = tolerance.within_tolerance(bad, xs, "bf16")
+    s = np.abs(tolerance.exact_sum(xs, "bf16"))
+    S = np.sum([np.abs(arith.bf16_to_f32(x)) for x in xs], axis=0)
+    assert not ok[s > S / 8].any()
+    # a dropped term is rejected almost everywhere
+    dropped = arith.ordered_sum(xs[:-1], "bf16")
+    assert tolerance.within_tolerance(dropped, xs, "bf16").mean() < 0.1
+    # fp32: one part in 1e5 is far outside
+    ys = [synth.normal_f32(rng, 4000) for _ in range(8)]
+    g32 = arith.ordered_sum(ys, "f32")
+    assert not tolerance.within_tolerance(g32 * np.float32(1 + 1e-5), ys, "f32")[
+        np.abs(g32) > 1.0].any()
