@@ -80,6 +80,25 @@ def scatter(xs, root=0):
     return [xs[root][d * b:(d + 1) * b].copy() for d in range(R)]
 
 
+def gemv_payloads(wts, xs):
+    """Row-parallel linear layer shards, the payloads of a fused producer: rank r's payload
+    is y_r[j] = bf16_rne(sum over i = 0..k-1, in order, of w_r[i, j] * x_r[i]) with w_r given
+    transposed as [k, n] bf16 and x_r as [k] bf16; the products of two bf16 are exact in
+    binary32 and each add rounds to nearest even; the chain starts from the i = 0 product.
+    (SiFAR review: the collectives run inside megakernels after a layer's computation.)"""
+    from .arith import bf16_to_f32, f32_to_bf16_rne
+    out = []
+    for wt, x in zip(wts, xs):
+        w = bf16_to_f32(wt)
+        xv = bf16_to_f32(x)
+        acc = w[0] * xv[0]
+        with np.errstate(over="ignore", invalid="ignore"):
+            for i in range(1, w.shape[0]):
+                acc = acc + w[i] * xv[i]
+        out.append(f32_to_bf16_rne(acc))
+    return out
+
+
 def moe_dest_ranks(routing, experts_per_rank):
     """routing [R, T, k] expert ids -> boolean [R, T, R]: token (s,t) goes to rank d."""
     R = routing.shape[0]

@@ -502,3 +502,43 @@ def test_tolerance_rejects_real_errors():
     g32 = arith.ordered_sum(ys, "f32")
     assert not tolerance.within_tolerance(g32 * np.float32(1 + 1e-5), ys, "f32")[
         np.abs(g32) > 1.0].any()
+
+
+# ---------------------------------------------------------------- fused producer (GEMV)
+
+def test_gemv_payload_matches_exact_rational_evaluation():
+    rng = synth.seeded_rng(400)
+    for k, n in ((1, 8), (5, 16), (16, 8)):
+        wt = synth.normal_bf16(rng, (k, n))
+        x = synth.normal_bf16(rng, k)
+        y = collectives.gemv_payloads([wt], [x])[0]
+        for j in range(n):
+            prods = [brute.Val(brute.decode_bf16(int(wt[i, j])).q * brute.decode_bf16(int(x[i])).q)
+                     for i in range(k)]
+            acc = prods[0]
+            for p in prods[1:]:
+                acc = brute.add(acc, p, brute.round_f32)
+            want = brute.round_bf16(acc)
+            assert brute.decode_bf16(int(y[j])).key() == want.key() or (acc.q == 0), (k, n, j)
+
+
+def test_gemv_payload_closed_forms():
+    rng = synth.seeded_rng(401)
+    k = n = 32
+    x = synth.normal_bf16(rng, k)
+    perm = rng.permutation(n)
+    one = np.uint16(0x3F80)
+    wt = np.zeros((k, n), dtype=np.uint16)
+    wt[np.arange(k), perm] = one           # column perm[i] picks x[i]
+    y = collectives.gemv_payloads([wt], [x])[0]
+    want = np.zeros(n, dtype=np.uint16)
+    want[perm] = x
+    # zero products add exactly; a product's sign of zero can differ only for zero inputs
+    nz = (x & 0x7FFF) != 0
+    assert np.array_equal(y[perm][nz], x[nz])
+    # scaling every weight by 2 doubles every output exactly (no overflow at these sizes)
+    wt2 = synth.small_int_bf16(rng, (k, n), lim=3)
+    y1 = collectives.gemv_payloads([wt2], [x])[0]
+    wt3 = arith.f32_to_bf16_rne(arith.bf16_to_f32(wt2) * np.float32(2))
+    y2 = collectives.gemv_payloads([wt3], [x])[0]
+    assert np.array_equal(arith.bf16_to_f32(y2), arith.bf16_to_f32(y1) * np.float32(2))
