@@ -10,7 +10,7 @@ protocols, a staggered-start stress run of the speculative protocol, and the
 prefill-sized all-reduce (8 x 64 MiB, one-shot vs two-shot) as achieved HBM GB/s.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|sweep|prefill|moe|moe_combine|fig15]
+                    [--workload decode|sweep|prefill|moe|moe_combine|fig15|fused]
                     [--max-bytes B]
 
 Under torchrun each rank runs an independent replica on its own GPU (the emulated
@@ -544,6 +544,40 @@ def run_workload(args):
                                                            if st["spec_checks"] else 0.0)})
                         pl.free()
         res["rows"] = rows
+    elif args.workload == "fused":
+        # producer fusion: each rank's payload is a row-parallel GEMV shard y_r = W_r x_r
+        # (8 ranks, 4096 outputs, k = 512 per rank) computed in the stage step, then
+        # all-reduced; compared with the all-reduce alone on the same payload size
+        Rr, n, k, E, pool = 8, 4096, 512, 2000, 7
+        g.manual_seed(9)
+        wts = [torch.randn(k, n, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
+               for _ in range(Rr)]
+        xs = [torch.randn(pool, k, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
+              for _ in range(Rr)]
+        ys = [torch.randn(pool, n, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
+              for _ in range(Rr)]
+        outs = [torch.empty(E, n, dtype=torch.int16, device=dev) for _ in range(Rr)]
+        nm = cdc.allreduce(Rr, n, "bf16")
+        rows = []
+        for proto in ("barrier", "dual", "spec"):
+            for chain in (0, 1):
+                pl = cdc.Plan(nm, protocol=proto, chain=chain)
+                tf = _time_steps(torch, lambda: pl.run_gemv(wts, xs, k, outs, n_epochs=E,
+                                                            x_epoch_stride=2 * k, x_pool=pool,
+                                                            out_epoch_stride=2 * n),
+                                 args.steps, args.warmup, flush, stream)
+                ta = _time_steps(torch, lambda: pl.run(ys, outs, n_epochs=E, in_epoch_stride=2 * n,
+                                                       in_pool=pool, out_epoch_stride=2 * n),
+                                 args.steps, args.warmup, flush, stream)
+                if pl.status()["code"] != 0:
+                    raise RuntimeError(f"fused {proto}: {pl.status()}")
+                med = lambda t: round(sorted(t)[len(t) // 2] * 1000 / E, 4)
+                rows.append({"protocol": proto, "chain": chain, "fused_us_per_epoch": med(tf),
+                             "allreduce_only_us_per_epoch": med(ta)})
+                pl.free()
+        res["rows"] = rows
+        res["gemv"] = {"ranks": Rr, "outputs": n, "k_per_rank": k,
+                       "weight_bytes_per_epoch": Rr * n * k * 2}
     elif args.workload == "moe_combine":
         T, H, E, k = 4096, 7168, 256, 8
         routing = synth.zipf_topk_routing(5, R, T, E, k, 1.1)
@@ -586,7 +620,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "sweep", "prefill", "moe", "moe_combine", "fig15"])
+                    choices=["decode", "sweep", "prefill", "moe", "moe_combine", "fig15",
+                             "fused"])
     ap.add_argument("--max-bytes", type=int, default=0, help="sweep: largest bytes per rank")
     ap.add_argument("--print-sources-sha", action="store_true",
                     help="print the sha256 of the engine kernel's sources and exit")

@@ -85,6 +85,8 @@ _SIGS = {
                                 _P, C.POINTER(Config), C.POINTER(PlanInfo)]),
     "coll_plan_info": (C.c_int, [_P, C.POINTER(PlanInfo)]),
     "coll_run": (C.c_int, [_P, _P, _P, C.c_int, C.c_int64, C.c_int, C.c_int64, _P]),
+    "coll_run_gemv": (C.c_int, [_P, _P, _P, C.c_int, _P, C.c_int, C.c_int64, C.c_int,
+                                C.c_int64, _P]),
     "coll_status": (C.c_int, [_P, C.POINTER(Stats)]),
     "coll_stamps": (C.c_int64, [_P, _P, C.c_int64]),
     "coll_reset": (C.c_int, [_P]),

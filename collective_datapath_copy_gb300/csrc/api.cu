@@ -177,12 +177,24 @@ extern "C" int coll_plan_info(coll_plan_t p, coll_plan_info_t *info) {
   return COLL_OK;
 }
 
-extern "C" int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_epochs,
-                        int64_t in_epoch_stride, int in_pool, int64_t out_epoch_stride,
-                        void *stream) {
+// One run. With wt != null (fused producer) `in` holds the GEMV vectors x_r of k elements
+// and the stage computes each payload piece as W_r x_r instead of loading it.
+static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epochs,
+                    int64_t in_epoch_stride, int in_pool, int64_t out_epoch_stride,
+                    void *stream, const void *const *wt, uint32_t k) {
   if (!p || !in || !out || n_epochs < 1 || in_pool < 1) return COLL_EINVAL;
   const coll_compiled &c = p->c;
   const int R = c.R;
+  if (wt) {
+    if (c.cfg.zero_copy || c.dtype != COLL_BF16 || k < 8 || (k & 7u)) return COLL_EINVAL;
+    for (int r = 0; r < R; ++r) {
+      if (!c.in_used[r]) continue;
+      if (!wt[r]) return COLL_EINVAL;
+      if (((uintptr_t)wt[r] & 15u) || (c.in_bytes[r] & 15u)) return COLL_EALIGN;
+    }
+  }
+  // bytes of one rank's per-epoch input as the kernel reads it
+  auto in_span = [&](int r) -> uint64_t { return wt ? (uint64_t)k * 2 : c.in_bytes[r]; };
   coll::RankPtrs ptr;
   memset(&ptr, 0, sizeof(ptr));
   // spans touched over all epochs, for the aliasing check
@@ -195,7 +207,7 @@ extern "C" int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_
       const int64_t lo = std::min<int64_t>(0, in_epoch_stride * (in_pool - 1));
       const int64_t hi = std::max<int64_t>(0, in_epoch_stride * (in_pool - 1));
       i0[r] = (uintptr_t)in[r] + lo;
-      i1[r] = (uintptr_t)in[r] + hi + c.in_bytes[r];
+      i1[r] = (uintptr_t)in[r] + hi + in_span(r);
     }
     if (c.out_used[r]) {
       if (!out[r]) return COLL_EINVAL;
@@ -215,6 +227,9 @@ extern "C" int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_
     if (!c.out_used[r]) continue;
     for (int q = 0; q < R; ++q) {
       if (c.in_used[q] && overlaps(o0[r], o1[r], i0[q], i1[q])) return COLL_EOVERLAP;
+      if (wt && c.in_used[q] &&
+          overlaps(o0[r], o1[r], (uintptr_t)wt[q], (uintptr_t)wt[q] + (uint64_t)k * c.in_bytes[q]))
+        return COLL_EOVERLAP;
       if (q != r && c.out_used[q] && overlaps(o0[r], o1[r], o0[q], o1[q])) return COLL_EOVERLAP;
     }
     // an output buffer reused across epochs must not overlap itself between epochs
@@ -298,6 +313,13 @@ extern "C" int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_
     a.inject_start_ns = c.cfg.inject_start_ns;
     a.inject_pause_ns = c.cfg.inject_pause_ns;
     a.R = R;
+    if (wt) {
+      for (int r = 0; r < R; ++r) {
+        a.wt[r] = static_cast<const char *>(wt[r]);
+        a.wt_stride[r] = (int64_t)c.in_bytes[r];
+      }
+      a.gemv_k = k;
+    }
     err = coll::launch_engine(c.op, c.dtype, a, s);
     if (err == cudaSuccess) p->epochs_issued += (uint64_t)n_epochs;
   }
@@ -318,6 +340,21 @@ extern "C" int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_
   }
   p->last_epochs = n_epochs;
   return COLL_OK;
+}
+
+extern "C" int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_epochs,
+                        int64_t in_epoch_stride, int in_pool, int64_t out_epoch_stride,
+                        void *stream) {
+  return run_impl(p, in, out, n_epochs, in_epoch_stride, in_pool, out_epoch_stride, stream,
+                  nullptr, 0);
+}
+
+extern "C" int coll_run_gemv(coll_plan_t p, const void *const *wt, void *const *x, int k,
+                             void *const *out, int n_epochs, int64_t x_epoch_stride, int x_pool,
+                             int64_t out_epoch_stride, void *stream) {
+  if (!wt || k < 1) return COLL_EINVAL;
+  return run_impl(p, x, out, n_epochs, x_epoch_stride, x_pool, out_epoch_stride, stream, wt,
+                  (uint32_t)k);
 }
 
 static int wait_last(coll_plan_s *p) {

@@ -276,6 +276,36 @@ __device__ __forceinline__ uint4 gather_pieces(const char *xb, uint32_t nbytes, 
   return active ? acc.pack() : make_uint4(0, 0, 0, 0);
 }
 
+// Fused producer: this lane's 8 consecutive payload elements of y = W x, i.e. for each
+// output column j: products w[i][j] * x[i] rounded to binary32, added in order i = 0..k-1
+// (round to nearest even), then rounded once to bf16. wcol points at row 0 of the lane's
+// 8 columns; ws is the row stride in bytes; k is a multiple of 8.
+__device__ __forceinline__ uint4 gemv_piece(const char *wcol, int64_t ws, const char *xp,
+                                            uint32_t k) {
+  float acc[8];
+  for (uint32_t i0 = 0; i0 < k; i0 += 8) {
+    const uint4 xv = ld_nc_v4(xp + (size_t)i0 * 2);
+    uint4 w[8];
+#pragma unroll
+    for (uint32_t t = 0; t < 8; ++t) w[t] = ld_nc_v4(wcol + (int64_t)(i0 + t) * ws);
+    float xf[8];
+    bf16x8_init(xf, xv);
+#pragma unroll
+    for (uint32_t t = 0; t < 8; ++t) {
+      float wf[8];
+      bf16x8_init(wf, w[t]);
+      if (i0 + t == 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = __fmul_rn(wf[e], xf[t]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], __fmul_rn(wf[e], xf[t]));
+      }
+    }
+  }
+  return bf16x8_pack(acc);
+}
+
 // Speculatively load (and reduce) the n pieces of a unit, issue the flag loads while the
 // payload loads are in flight, and hash what was loaded (per producer, warp-reduced; lane j
 // keeps producer j's hash). Returns the packed result of this attempt.
@@ -329,7 +359,7 @@ __device__ __forceinline__ uint4 spec_attempt(const char *xb, uint32_t nbytes, u
   return active ? acc.pack() : make_uint4(0, 0, 0, 0);
 }
 
-template <int KIND>
+template <int KIND, bool GEMV>
 __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
   const uint32_t gw = blockIdx.x;
   if (gw >= a.nwarps) return;
@@ -353,7 +383,8 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
   // A warp with exactly one stage item prefetches the next epoch's input piece (read-only
   // during the kernel) and hashes it while its own consume waits on memory, which takes
   // the input load and the producer-side tag off the critical path.
-  const bool pipelined = (W.s1 - W.s0) == 1u;
+  constexpr bool gemv = GEMV;
+  const bool pipelined = (W.s1 - W.s0) == 1u && !gemv;
   coll_unit_t su;
   coll_ref_t sref;
   coll_item_t sit;
@@ -467,6 +498,14 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
       if (pipelined) {
         x = nx;
         if (tagged && !nh_ready && lane < nvec) h = tag_part(x, lane);
+      } else if constexpr (GEMV) {
+        // fused producer: compute this piece of the payload in place of loading it
+        if (lane < nvec) {
+          const coll_ref_t r = a.refs[u.src0 + it.slot];
+          x = gemv_piece(a.wt[r.rank] + r.off + u.start + lane * 16, a.wt_stride[r.rank],
+                         a.ptr.in[r.rank] + in_off, a.gemv_k);
+          if (tagged) h = tag_part(x, lane);
+        }
       } else if (lane < nvec) {
         const coll_ref_t r = a.refs[u.src0 + it.slot];
         x = ld_nc_v4(a.ptr.in[r.rank] + r.off + in_off + u.start + lane * 16);
@@ -692,11 +731,12 @@ cudaError_t launch_zero_copy(int op, int dtype, int keep, const ZcArgs &a, int c
   return cudaGetLastError();
 }
 
-static const void *engine_fn(int kind) {
+static const void *engine_fn(int kind, bool gemv) {
+  if (gemv) return (const void *)engine_kernel<1, true>;
   switch (kind) {
-    case 0: return (const void *)engine_kernel<0>;
-    case 1: return (const void *)engine_kernel<1>;
-    default: return (const void *)engine_kernel<2>;
+    case 0: return (const void *)engine_kernel<0, false>;
+    case 1: return (const void *)engine_kernel<1, false>;
+    default: return (const void *)engine_kernel<2, false>;
   }
 }
 
@@ -706,7 +746,11 @@ cudaError_t engine_max_coresident(int op, int dtype, int *max_ctas) {
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, engine_fn(kind_of(op, dtype)), 32, 0);
+  int per_sm_g = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, engine_fn(kind_of(op, dtype), false), 32, 0);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_g, engine_fn(1, true), 32, 0);
+  if (per_sm_g < per_sm) per_sm = per_sm_g;
   if (e != cudaSuccess) return e;
   *max_ctas = per_sm * sms;
   return cudaSuccess;
@@ -722,8 +766,8 @@ cudaError_t launch_probe_rtt(unsigned long long *flags, uint32_t iters, uint32_t
 cudaError_t launch_engine(int op, int dtype, const EngArgs &a, cudaStream_t s) {
   if (a.nwarps == 0 || a.n_epochs == 0) return cudaSuccess;
   void *args[] = {(void *)&a};
-  return cudaLaunchCooperativeKernel(engine_fn(kind_of(op, dtype)), dim3(a.nwarps), dim3(32),
-                                     args, 0, s);
+  return cudaLaunchCooperativeKernel(engine_fn(kind_of(op, dtype), a.gemv_k != 0),
+                                     dim3(a.nwarps), dim3(32), args, 0, s);
 }
 
 }  // namespace coll

@@ -32,7 +32,10 @@ struct ZcArgs {
 };
 
 struct EngArgs {
-  RankPtrs ptr;
+  RankPtrs ptr;                        // fused producer: ptr.in[r] is the GEMV vector x_r
+  const char *wt[COLL_MAX_RANKS];      // fused producer: W_r transposed, [k][in_len[r]] bf16
+  int64_t wt_stride[COLL_MAX_RANKS];   // bytes per row of wt[r]
+  uint32_t gemv_k;                     // 0: stage loads its payload; k: stage computes W_r x_r
   const coll_unit_t *units;
   const coll_item_t *sitems;
   const coll_item_t *citems;

@@ -94,6 +94,18 @@ class Plan:
                               _stream_handle(stream))
         check(code, "coll_run")
 
+    def run_gemv(self, wts, xs, k, outs, n_epochs=1, x_epoch_stride=0, x_pool=1,
+                 out_epoch_stride=0, stream=None):
+        """Fused producer: each rank's payload is W_r x_r computed inside the engine.
+        wts[r]: [k, in_len[r]] bf16 (W_r transposed); xs[r]: x vectors (k bf16 per epoch)."""
+        R = self.naming.R
+        code = lib().coll_run_gemv(self._h, C.cast(_dev_ptrs(wts, R), C.c_void_p),
+                                   C.cast(_dev_ptrs(xs, R), C.c_void_p), int(k),
+                                   C.cast(_dev_ptrs(outs, R), C.c_void_p), int(n_epochs),
+                                   int(x_epoch_stride), int(x_pool), int(out_epoch_stride),
+                                   _stream_handle(stream))
+        check(code, "coll_run_gemv")
+
     def run_ptrs(self, in_ptrs, out_ptrs, n_epochs=1, in_epoch_stride=0, in_pool=1,
                  out_epoch_stride=0, stream=None):
         """Same as run() with raw device addresses (ints)."""

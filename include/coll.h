@@ -209,6 +209,21 @@ int coll_plan_info(coll_plan_t p, coll_plan_info_t *info);
 int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_epochs,
              int64_t in_epoch_stride, int in_pool, int64_t out_epoch_stride, void *stream);
 
+/* Fused producer (staged bf16 plans): like coll_run, but each rank's payload is computed
+ * inside the engine's stage step instead of read from memory — the layer that precedes the
+ * collective fused into its persistent loop (SiFAR review: the All-Reduces run inside
+ * megakernels, after each layer's computation). At epoch i rank r's input buffer (in_len[r]
+ * bf16 elements, the buffer the naming refers to) is y_r = W_r x_r(i): wt[r] is W_r given
+ * transposed, k rows of in_len[r] bf16 (row stride in_len[r] elements), and x_r(i) =
+ * x[r] + (i % x_pool) * x_epoch_stride bytes holds k bf16. Element j of y_r: products
+ * wt[r][i][j] * x_r(i)[i] rounded to binary32, added in order i = 0..k-1 (round to nearest
+ * even), then rounded once to bf16. k must be a multiple of 8; in_len[r], wt[r], x[r] and
+ * the strides must give 16-byte alignment. Errors as coll_run, plus COLL_EINVAL for a
+ * zero-copy or non-bf16 plan. */
+int coll_run_gemv(coll_plan_t p, const void *const *wt, void *const *x, int k, void *const *out,
+                  int n_epochs, int64_t x_epoch_stride, int x_pool, int64_t out_epoch_stride,
+                  void *stream);
+
 /* Wait for the plan's last run and report its status and counters. Returns the run's
  * status (COLL_OK, COLL_ETIMEDOUT, COLL_EDEVICE) or COLL_ECUDA. st may be NULL. */
 int coll_status(coll_plan_t p, coll_stats_t *st);

@@ -83,8 +83,9 @@ def scatter(xs, root=0):
 def gemv_payloads(wts, xs):
     """Row-parallel linear layer shards, the payloads of a fused producer: rank r's payload
     is y_r[j] = bf16_rne(sum over i = 0..k-1, in order, of w_r[i, j] * x_r[i]) with w_r given
-    transposed as [k, n] bf16 and x_r as [k] bf16; the products of two bf16 are exact in
-    binary32 and each add rounds to nearest even; the chain starts from the i = 0 product.
+    transposed as [k, n] bf16 and x_r as [k] bf16; each product is rounded to binary32 (it is
+    exact unless it leaves binary32's normal range) and each add rounds to nearest even; the
+    chain starts from the i = 0 product.
     (SiFAR review: the collectives run inside megakernels after a layer's computation.)"""
     from .arith import bf16_to_f32, f32_to_bf16_rne
     out = []

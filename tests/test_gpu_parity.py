@@ -631,3 +631,56 @@ def test_tree_order_sums_within_tolerance(dtype, n_bytes, kind):
 def test_staged_plans_reject_the_tree_order():
     with pytest.raises(cdc.CollError):
         cdc.Plan(namings.allreduce(2, 1024, "bf16"), reduce_order="tree")
+
+
+# ------------------------------------------------------------ fused producer (GEMV + AR)
+
+def _gemv_case(R, n, k, pool, seed):
+    rng = synth.seeded_rng(seed)
+    wts = [synth.normal_bf16(rng, (k, n)) for _ in range(R)]
+    xs = [[synth.normal_bf16(rng, k) for _ in range(pool)] for _ in range(R)]
+    return wts, xs
+
+
+@pytest.mark.parametrize("protocol,datapath,chain", [("barrier", "oneshot", 0), ("dual", "oneshot", 0),
+                                                     ("spec", "oneshot", 0), ("spec", "twoshot", 0),
+                                                     ("spec", "oneshot", 1)])
+def test_fused_gemv_allreduce_bit_exact(protocol, datapath, chain):
+    R, n, k, pool, E = 8, 4096, 256, 3, 24
+    wts, xs = _gemv_case(R, n, k, pool, 97)
+    want = [collectives.allreduce(collectives.gemv_payloads(wts, [xs[r][e % pool] for r in range(R)]),
+                                  "bf16")[0] for e in range(pool)]
+    plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol=protocol, datapath=datapath,
+                    chain=chain)
+    dw = [to_dev(w.ravel(), "bf16") for w in wts]
+    dx = [torch.stack([to_dev(x, "bf16") for x in xs[r]]).contiguous() for r in range(R)]
+    outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    plan.run_gemv(dw, dx, k, outs, n_epochs=E, x_epoch_stride=2 * k, x_pool=pool,
+                  out_epoch_stride=2 * n)
+    assert plan.status()["code"] == 0
+    for e in range(E):
+        for r in range(R):
+            assert bits_equal(from_dev(outs[r][e], "bf16"), want[e % pool]), (e, r)
+    plan.free()
+
+
+def test_fused_gemv_with_a_reduce_scatter_naming_and_bad_arguments():
+    R, n, k = 4, 2048, 64
+    wts, xs = _gemv_case(R, n, k, 1, 98)
+    ys = collectives.gemv_payloads(wts, [x[0] for x in xs])
+    want = collectives.reduce_scatter(ys, "bf16")
+    plan = cdc.Plan(namings.reduce_scatter(R, n, "bf16"), protocol="dual")
+    dw = [to_dev(w.ravel(), "bf16") for w in wts]
+    dx = [to_dev(x[0], "bf16") for x in xs]
+    outs = [torch.empty(n // R, dtype=torch.int16, device="cuda") for _ in range(R)]
+    plan.run_gemv(dw, dx, k, outs)
+    assert plan.status()["code"] == 0
+    for r in range(R):
+        assert bits_equal(from_dev(outs[r], "bf16"), want[r])
+    with pytest.raises(cdc.CollError):
+        plan.run_gemv(dw, dx, 12, outs)  # k not a multiple of 8
+    zc = cdc.Plan(namings.allreduce(R, n, "bf16"), zero_copy=1)
+    with pytest.raises(cdc.CollError):
+        zc.run_gemv(dw, dx, k, [torch.empty(n, dtype=torch.int16, device="cuda") for _ in range(R)])
+    plan.free()
+    zc.free()
