@@ -217,6 +217,8 @@ def run_ours(args, rank, world, dist):
         ("spec_relaxed", dict(protocol="spec", spec_check="relaxed")),
         ("spec_literal", dict(protocol="spec", spec_check="literal")),
         ("spec_twoshot", dict(protocol="spec", datapath="twoshot")),
+        ("ll", dict(protocol="ll")),
+        ("ll_chain", dict(protocol="ll", chain=1)),
         ("spec_chain", dict(protocol="spec", chain=1)),
         ("dual_chain", dict(protocol="dual", chain=1)),
         ("barrier_chain", dict(protocol="barrier", chain=1)),
@@ -243,7 +245,7 @@ def run_ours(args, rank, world, dist):
     # other protocols (same K/W)
     proto = {}
     for name in ("dual", "barrier", "spec_stagger", "spec_relaxed", "spec_literal",
-                 "spec_twoshot", "spec_chain", "dual_chain", "barrier_chain"):
+                 "spec_twoshot", "ll", "ll_chain", "spec_chain", "dual_chain", "barrier_chain"):
         tt = _time_steps(torch, step(name), max(3, args.steps // 2), 1, flush, stream)
         s2 = plans[name].status()
         if s2["code"] != 0:
@@ -268,7 +270,8 @@ def run_ours(args, rank, world, dist):
     # where an epoch's time goes (first warp): stage+notify, wait/validate, store+rest
     phases = {}
     for name, cfg in [("spec", dict(protocol="spec")), ("dual", dict(protocol="dual")),
-                      ("spec_relaxed", dict(protocol="spec", spec_check="relaxed"))]:
+                      ("spec_relaxed", dict(protocol="spec", spec_check="relaxed")),
+                      ("ll", dict(protocol="ll"))]:
         pp = cdc.Plan(nm, record_stamps=2, stamp_capacity=EPOCHS, **cfg)
         pp.run(ins, outs, **kw)
         pp.run(ins, outs, **kw)
@@ -527,7 +530,7 @@ def run_workload(args):
                        for _ in range(Rr)]
                 outs = [torch.empty(E, n, dtype=torch.int16, device=dev) for _ in range(Rr)]
                 nm = cdc.allreduce(Rr, n, "bf16")
-                for proto in ("barrier", "dual", "spec"):
+                for proto in ("barrier", "dual", "spec", "ll"):
                     for dp in ("oneshot", "twoshot"):
                         pl = cdc.Plan(nm, protocol=proto, datapath=dp)
                         tt = _time_steps(torch, lambda: pl.run(ins, outs, n_epochs=E,

@@ -75,7 +75,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
             sys.stdout.write(o)
     objs = [os.path.join(BUILD, s + ".o") for s in CU_SOURCES + CXX_SOURCES]
     tmp = LIB + ".tmp"
-    _run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs])
+    _run([nvcc, *ARCH, "-shared", "-cudart", "static", "-Xlinker", "--no-undefined", "-o", tmp,
+          *objs])
     os.replace(tmp, LIB)
     if verbose:
         sys.stdout.write("built " + LIB + "\n")

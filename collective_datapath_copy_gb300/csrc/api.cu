@@ -101,7 +101,9 @@ extern "C" int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_
   }
   int max_ctas = coll_default_max_warps();
   const int eop = (op == COLL_OP_SUM) ? COLL_OP_SUM : COLL_OP_COPY;
-  if (coll::engine_max_coresident(eop, dtype == COLL_F32 ? COLL_F32 : COLL_BF16, &max_ctas) !=
+  const int eproto = cfg ? cfg->protocol : COLL_PROTO_SPEC;
+  if (coll::engine_max_coresident(eop, dtype == COLL_F32 ? COLL_F32 : COLL_BF16, eproto,
+                                  &max_ctas) !=
       cudaSuccess) {
     delete p;
     return COLL_ECUDA;
@@ -313,6 +315,7 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
     a.inject_start_ns = c.cfg.inject_start_ns;
     a.inject_pause_ns = c.cfg.inject_pause_ns;
     a.R = R;
+    if (wt && c.cfg.protocol == COLL_PROTO_LL) return COLL_EINVAL;  // not combined
     if (wt) {
       for (int r = 0; r < R; ++r) {
         a.wt[r] = static_cast<const char *>(wt[r]);

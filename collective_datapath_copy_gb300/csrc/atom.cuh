@@ -92,6 +92,19 @@ __device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned l
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// Two 8-byte words, each single-copy atomic (tagged-data exchange).
+__device__ __forceinline__ void st_relaxed_v2u64(void *p, unsigned long long a,
+                                                 unsigned long long b) {
+  asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1,%2};" ::"l"(p), "l"(a), "l"(b)
+               : "memory");
+}
+
+__device__ __forceinline__ void ld_relaxed_v2u64(const void *p, unsigned long long &a,
+                                                 unsigned long long &b) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p)
+               : "memory");
+}
+
 __device__ __forceinline__ void st_relaxed_u32(uint32_t *p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

@@ -359,7 +359,7 @@ __device__ __forceinline__ uint4 spec_attempt(const char *xb, uint32_t nbytes, u
   return active ? acc.pack() : make_uint4(0, 0, 0, 0);
 }
 
-template <int KIND, bool GEMV>
+template <int KIND, bool GEMV, bool LL>
 __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
   const uint32_t gw = blockIdx.x;
   if (gw >= a.nwarps) return;
@@ -367,6 +367,8 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
   const coll_warp_t W = a.warps[gw];
   coll_dev_status_t *st = a.st;
   const bool spec_proto = a.protocol == COLL_PROTO_SPEC;
+  constexpr bool ll = LL;
+  const uint32_t slot_mult = ll ? 2u : 1u;  // tagged-data slots are twice the payload
   // content tags: validated by the tagged checks, stored by every spec producer
   const bool literal = spec_proto && a.spec_check == COLL_SPEC_LITERAL;
   const bool relaxed = spec_proto && a.spec_check == COLL_SPEC_TAGGED_RELAXED;
@@ -492,7 +494,7 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
         __syncwarp();
       }
       const uint32_t nvec = u.nbytes >> 4;
-      char *dst = a.xbuf + (size_t)b * a.xpar + u.xoff + (size_t)it.slot * u.nbytes;
+      char *dst = a.xbuf + (size_t)b * a.xpar + u.xoff + (size_t)it.slot * u.nbytes * slot_mult;
       uint4 x = make_uint4(0, 0, 0, 0);
       uint32_t h = 0;
       if (pipelined) {
@@ -511,11 +513,20 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
         x = ld_nc_v4(a.ptr.in[r.rank] + r.off + in_off + u.start + lane * 16);
         if (tagged) h = tag_part(x, lane);
       }
-      if (lane < nvec) st_v4(dst + lane * 16, x);
+      if constexpr (LL) {
+        // tagged data: every 4 payload bytes travel with the epoch in one 8-byte word
+        if (lane < nvec && !skip_notify) {
+          const unsigned long long ep = (unsigned long long)E << 32;
+          st_relaxed_v2u64(dst + lane * 32, ep | x.x, ep | x.y);
+          st_relaxed_v2u64(dst + lane * 32 + 16, ep | x.z, ep | x.w);
+        }
+      } else if (lane < nvec) {
+        st_v4(dst + lane * 16, x);
+      }
       uint32_t tag = 0;
       if (tagged) tag = tag_fold(pipelined && nh_ready ? nh : __reduce_add_sync(FULL, h), E);
       __syncwarp();
-      if (lane == 0 && !skip_notify) {
+      if (lane == 0 && !skip_notify && !ll) {
         unsigned long long *fp = a.pflag + (size_t)b * a.n_pflag + u.pflag0 + it.slot;
         const unsigned long long fv = ((unsigned long long)E << 32) | tag;
         if (relaxed) st_relaxed_u64(fp, fv); else st_release_u64(fp, fv);
@@ -540,7 +551,64 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
       uint4 res = make_uint4(0, 0, 0, 0);
       bool have = false;
       bool retried = false;
-      if (spec_proto && n <= 32) {
+      if constexpr (LL) {
+        // Poll the tagged words of every producer until each carries epoch E (bounded),
+        // then reduce in producer order; batches of 8 producers.
+        typename EngAcc<KIND>::type acc;
+        const size_t pstride = (size_t)u.nbytes * 2;
+        bool ok = true;
+        uint32_t rounds = 0;
+        for (uint32_t k0 = 0; k0 < n && ok; k0 += 8) {
+          const uint32_t kn = n - k0 < 8 ? n - k0 : 8;
+          uint4 d[8];
+          uint32_t pending = active ? ((1u << kn) - 1u) : 0u;
+          uint64_t t0 = 0;
+          for (uint32_t r = 0;; ++r) {
+#pragma unroll
+            for (uint32_t k = 0; k < 8; ++k) {
+              if (pending & (1u << k)) {
+                unsigned long long w0, w1, w2, w3;
+                const char *src = xb + (size_t)(k0 + k) * pstride + lane * 32;
+                ld_relaxed_v2u64(src, w0, w1);
+                ld_relaxed_v2u64(src + 16, w2, w3);
+                if ((uint32_t)(w0 >> 32) == E && (uint32_t)(w1 >> 32) == E &&
+                    (uint32_t)(w2 >> 32) == E && (uint32_t)(w3 >> 32) == E) {
+                  d[k] = make_uint4((uint32_t)w0, (uint32_t)w1, (uint32_t)w2, (uint32_t)w3);
+                  pending &= ~(1u << k);
+                }
+              }
+            }
+            if (__all_sync(FULL, pending == 0)) break;
+            ++rounds;
+            if ((r & 31u) == 31u) {
+              const uint64_t now = globaltimer();
+              if (t0 == 0) t0 = now;
+              const bool late = (t0 != now && now - t0 > a.spin_ns) || ld_relaxed_u32(&st->abort);
+              if (__any_sync(FULL, late)) {
+                ok = false;
+                break;
+              }
+            }
+          }
+          if (ok && active) {
+#pragma unroll
+            for (uint32_t k = 0; k < 8; ++k)
+              if (k < kn) {
+                if (k0 + k == 0) acc.init(d[k]); else acc.add(d[k]);
+              }
+          }
+        }
+        if (!ok) {
+          if (lane == 0) record_timeout(st, (int)W.rank, (int)it.unit, 2, E);
+          failed = true;
+          break;
+        }
+        ++n_checks;
+        if (rounds) ++n_retries;
+        res = active ? acc.pack() : make_uint4(0, 0, 0, 0);
+        have = true;
+      }
+      if (!LL && spec_proto && n <= 32) {
         // Speculative consume: load and reduce without waiting, then validate.
         unsigned long long f = 0;
         uint32_t myh = 0;
@@ -731,27 +799,37 @@ cudaError_t launch_zero_copy(int op, int dtype, int keep, const ZcArgs &a, int c
   return cudaGetLastError();
 }
 
-static const void *engine_fn(int kind, bool gemv) {
-  if (gemv) return (const void *)engine_kernel<1, true>;
+static const void *engine_fn(int kind, bool gemv, bool ll) {
+  if (gemv) return (const void *)engine_kernel<1, true, false>;
+  if (ll) {
+    switch (kind) {
+      case 0: return (const void *)engine_kernel<0, false, true>;
+      case 1: return (const void *)engine_kernel<1, false, true>;
+      default: return (const void *)engine_kernel<2, false, true>;
+    }
+  }
   switch (kind) {
-    case 0: return (const void *)engine_kernel<0, false>;
-    case 1: return (const void *)engine_kernel<1, false>;
-    default: return (const void *)engine_kernel<2, false>;
+    case 0: return (const void *)engine_kernel<0, false, false>;
+    case 1: return (const void *)engine_kernel<1, false, false>;
+    default: return (const void *)engine_kernel<2, false, false>;
   }
 }
 
-cudaError_t engine_max_coresident(int op, int dtype, int *max_ctas) {
-  int dev = 0, sms = 0, per_sm = 0;
+cudaError_t engine_max_coresident(int op, int dtype, int protocol, int *max_ctas) {
+  int dev = 0, sms = 0, per_sm = 0, per_sm_g = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  int per_sm_g = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, engine_fn(kind_of(op, dtype), false), 32, 0);
+  const bool ll = protocol == COLL_PROTO_LL;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, engine_fn(kind_of(op, dtype), false, ll),
+                                                    32, 0);
   if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_g, engine_fn(1, true), 32, 0);
-  if (per_sm_g < per_sm) per_sm = per_sm_g;
-  if (e != cudaSuccess) return e;
+  if (!ll) {  // a plan of this protocol may also run the fused-producer variant
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_g, engine_fn(1, true, false), 32, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm_g < per_sm) per_sm = per_sm_g;
+  }
   *max_ctas = per_sm * sms;
   return cudaSuccess;
 }
@@ -766,8 +844,9 @@ cudaError_t launch_probe_rtt(unsigned long long *flags, uint32_t iters, uint32_t
 cudaError_t launch_engine(int op, int dtype, const EngArgs &a, cudaStream_t s) {
   if (a.nwarps == 0 || a.n_epochs == 0) return cudaSuccess;
   void *args[] = {(void *)&a};
-  return cudaLaunchCooperativeKernel(engine_fn(kind_of(op, dtype), a.gemv_k != 0),
-                                     dim3(a.nwarps), dim3(32), args, 0, s);
+  return cudaLaunchCooperativeKernel(
+      engine_fn(kind_of(op, dtype), a.gemv_k != 0, a.protocol == COLL_PROTO_LL),
+      dim3(a.nwarps), dim3(32), args, 0, s);
 }
 
 }  // namespace coll

@@ -87,6 +87,6 @@ cudaError_t launch_probe_rtt(unsigned long long *flags, uint32_t iters, uint32_t
                              unsigned long long *out, uint64_t limit, cudaStream_t s);
 
 // How many one-warp engine CTAs can be co-resident on the current device.
-cudaError_t engine_max_coresident(int op, int dtype, int *max_ctas);
+cudaError_t engine_max_coresident(int op, int dtype, int protocol, int *max_ctas);
 
 }  // namespace coll

@@ -47,7 +47,7 @@ extern "C" int coll_config_default(coll_config_t *cfg) {
 }
 
 static int check_config(const coll_config_t &c) {
-  if (c.protocol < 0 || c.protocol > 2) return COLL_EINVAL;
+  if (c.protocol < 0 || c.protocol > 3) return COLL_EINVAL;
   if (c.datapath < 0 || c.datapath > 1) return COLL_EINVAL;
   if (c.zero_copy < 0 || c.zero_copy > 1) return COLL_EINVAL;
   if (c.spec_check < 0 || c.spec_check > 2) return COLL_EINVAL;
@@ -300,7 +300,8 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
       u.dst0 = dst0;
       u.ndst = (uint32_t)nm.cons.size();
       u.xoff = c.xpar_bytes;
-      c.xpar_bytes += (uint64_t)u.nbytes * u.nsrc;
+      // tagged-data slots hold an epoch word beside every 4 payload bytes
+      c.xpar_bytes += (uint64_t)u.nbytes * u.nsrc * (cfg.protocol == COLL_PROTO_LL ? 2u : 1u);
       u.pflag0 = c.n_pflag;
       c.n_pflag += u.nsrc;
       u.ncflag = twoshot ? 1u : u.ndst;

@@ -65,6 +65,11 @@ extern "C" {
 #define COLL_PROTO_BARRIER 0
 #define COLL_PROTO_DUAL 1
 #define COLL_PROTO_SPEC 2
+/* Lamport-style tagged data (the pages' push-based baseline, SiFAR review, Fig. 20): dual
+ * buffers whose 8-byte words each carry 4 payload bytes and the epoch; a consumer polls the
+ * words themselves until every tag shows its epoch. 8-byte single-copy atomicity validates
+ * every word: no flags, no fence, no hash; twice the exchange bytes. */
+#define COLL_PROTO_LL 3
 
 /* Datapaths for sum. Source: SiFAR review, Fig. 5 (oneshot: every consumer reduces the
  * whole payload from every producer) and Fig. 6 (twoshot: each part is reduced once, by an

@@ -136,7 +136,7 @@ def test_random_namings_zero_copy(seed):
 
 
 @pytest.mark.parametrize("seed", range(12))
-@pytest.mark.parametrize("protocol", ["barrier", "dual", "spec"])
+@pytest.mark.parametrize("protocol", ["barrier", "dual", "spec", "ll"])
 def test_random_namings_staged(seed, protocol):
     # staged plans need 16-byte-aligned segments: scale a random naming by 8 elements
     op = "copy" if seed % 3 == 0 else "sum"
@@ -238,7 +238,7 @@ def _check_epochs(outs, expect_dev, n_epochs, pool):
     return bad
 
 
-@pytest.mark.parametrize("protocol", ["barrier", "dual", "spec"])
+@pytest.mark.parametrize("protocol", ["barrier", "dual", "spec", "ll"])
 @pytest.mark.parametrize("datapath", ["oneshot", "twoshot"])
 @pytest.mark.parametrize("chain", [0, 1])
 def test_decode_allreduce_epochs_bit_exact(protocol, datapath, chain):
@@ -278,6 +278,10 @@ def test_decode_allreduce_10000_epochs_spec_equals_barrier_under_stagger():
                                                     inject="stagger", inject_seed=3,
                                                     inject_prob_ppm=100000, inject_max_ns=20000,
                                                     inject_start_ns=5000)),
+                      ("ll", dict(protocol="ll")),
+                      ("ll-stagger", dict(protocol="ll", inject="stagger", inject_seed=5,
+                                          inject_prob_ppm=100000, inject_max_ns=20000,
+                                          inject_start_ns=5000)),
                       ("spec-twoshot-stagger", dict(protocol="spec", datapath="twoshot",
                                                     inject="stagger", inject_seed=4,
                                                     inject_prob_ppm=100000, inject_max_ns=20000))]:
@@ -325,12 +329,13 @@ def test_speculation_with_adversarial_pause_tagged_is_exact_literal_is_not():
     assert bad["literal"][0] > 0
 
 
-def test_missing_notify_times_out_and_the_gpu_stays_usable():
+@pytest.mark.parametrize("protocol", ["dual", "ll"])
+def test_missing_notify_times_out_and_the_gpu_stays_usable(protocol):
     R, n = 4, 1024
     rng = synth.seeded_rng(5)
     xs = [synth.normal_bf16(rng, n) for _ in range(R)]
     nm = namings.allreduce(R, n, "bf16")
-    plan = cdc.Plan(nm, protocol="dual", inject="skip_notify", inject_rank=1,
+    plan = cdc.Plan(nm, protocol=protocol, inject="skip_notify", inject_rank=1,
                     spin_limit_ns=20_000_000)
     ins = [to_dev(x, "bf16") for x in xs]
     outs = [empty_dev(n, "bf16") for _ in range(R)]
@@ -592,7 +597,7 @@ def test_moe_combine(T, H, mode):
 
 @pytest.mark.parametrize("R", [2, 4, 8])
 @pytest.mark.parametrize("kb", [8, 16, 32])
-@pytest.mark.parametrize("protocol", ["barrier", "dual", "spec"])
+@pytest.mark.parametrize("protocol", ["barrier", "dual", "spec", "ll"])
 @pytest.mark.parametrize("datapath", ["oneshot", "twoshot"])
 def test_fig15_cells_bit_exact(R, kb, protocol, datapath):
     # SiFAR's Fig. 15 grid: TP degree 2/4/8 x 8/16/32 KB payloads, every protocol
@@ -684,3 +689,18 @@ def test_fused_gemv_with_a_reduce_scatter_naming_and_bad_arguments():
         zc.run_gemv(dw, dx, k, [torch.empty(n, dtype=torch.int16, device="cuda") for _ in range(R)])
     plan.free()
     zc.free()
+
+
+
+@pytest.mark.parametrize("cfg", [dict(zero_copy=1), dict(zero_copy=1, datapath="twoshot"),
+                                 dict(protocol="spec"), dict(protocol="ll"), dict(protocol="dual")],
+                         ids=lambda c: "-".join(f"{k}={v}" for k, v in c.items()))
+@pytest.mark.parametrize("R", [40, 64])
+def test_more_than_32_ranks(R, cfg):
+    n = 1024
+    rng = synth.seeded_rng(99)
+    xs = [synth.normal_bf16(rng, n) for _ in range(R)]
+    got, _ = run_once(namings.allreduce(R, n, "bf16"), xs, **cfg)
+    want = collectives.allreduce(xs, "bf16")[0]
+    for g in got:
+        assert bits_equal(g, want)
