@@ -244,7 +244,9 @@ int64_t coll_stamps(coll_plan_t p, uint64_t *host, int64_t n);
  * ranks. Synchronous; allocates and frees 1 KiB. COLL_ETIMEDOUT if a wait exceeded 1 s. */
 int coll_probe_flag_rtt(int peer_block, int iters, uint64_t *ns_total, int *sm_a, int *sm_b);
 
-/* Wait for the last run, then re-zero flags, counters and the epoch counter. */
+/* Wait for the last run, then re-zero flags, counters and the epoch counter. After a run
+ * that reported COLL_ETIMEDOUT the plan's flags are inconsistent: call this before the next
+ * coll_run on the plan. */
 int coll_reset(coll_plan_t p);
 
 /* Wait for the last run and release everything the plan owns. NULL is a no-op. */
