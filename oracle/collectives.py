@@ -80,23 +80,35 @@ def scatter(xs, root=0):
     return [xs[root][d * b:(d + 1) * b].copy() for d in range(R)]
 
 
-def gemv_payloads(wts, xs):
+GEMV_KBLOCKS = 8
+
+
+def gemv_payloads(wts, xs, kblocks=GEMV_KBLOCKS):
     """Row-parallel linear layer shards, the payloads of a fused producer: rank r's payload
-    is y_r[j] = bf16_rne(sum over i = 0..k-1, in order, of w_r[i, j] * x_r[i]) with w_r given
-    transposed as [k, n] bf16 and x_r as [k] bf16; each product is rounded to binary32 (it is
-    exact unless it leaves binary32's normal range) and each add rounds to nearest even; the
-    chain starts from the i = 0 product.
-    (SiFAR review: the collectives run inside megakernels after a layer's computation.)"""
+    is y_r = W_r x_r with w_r given transposed as [k, n] bf16 and x_r as [k] bf16.
+
+    Reading (the pages leave the layer's arithmetic open; SiFAR review: the collectives run
+    inside megakernels after a layer's computation): the k terms of each output are split
+    into `kblocks` consecutive blocks of k/kblocks; a block's sum is the binary32 chain over
+    its terms in order, starting from its first product; the block sums are then added in
+    block order; one round to bf16 at the end. Each product w*x is rounded to binary32 (it is
+    exact unless it leaves binary32's normal range) and each add rounds to nearest even."""
     from .arith import bf16_to_f32, f32_to_bf16_rne
     out = []
     for wt, x in zip(wts, xs):
         w = bf16_to_f32(wt)
         xv = bf16_to_f32(x)
-        acc = w[0] * xv[0]
+        k = w.shape[0]
+        assert k % kblocks == 0
+        kb = k // kblocks
+        total = None
         with np.errstate(over="ignore", invalid="ignore"):
-            for i in range(1, w.shape[0]):
-                acc = acc + w[i] * xv[i]
-        out.append(f32_to_bf16_rne(acc))
+            for b in range(kblocks):
+                acc = w[b * kb] * xv[b * kb]
+                for i in range(b * kb + 1, (b + 1) * kb):
+                    acc = acc + w[i] * xv[i]
+                total = acc if total is None else total + acc
+        out.append(f32_to_bf16_rne(total))
     return out
 
 

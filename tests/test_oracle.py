@@ -508,18 +508,34 @@ def test_tolerance_rejects_real_errors():
 
 def test_gemv_payload_matches_exact_rational_evaluation():
     rng = synth.seeded_rng(400)
-    for k, n in ((1, 8), (5, 16), (16, 8)):
+    for k, n, nb in ((8, 8, 8), (16, 16, 8), (24, 8, 8), (5, 8, 1)):
         wt = synth.normal_bf16(rng, (k, n))
         x = synth.normal_bf16(rng, k)
-        y = collectives.gemv_payloads([wt], [x])[0]
+        y = collectives.gemv_payloads([wt], [x], kblocks=nb)[0]
+        kb = k // nb
         for j in range(n):
             prods = [brute.Val(brute.decode_bf16(int(wt[i, j])).q * brute.decode_bf16(int(x[i])).q)
                      for i in range(k)]
-            acc = prods[0]
-            for p in prods[1:]:
-                acc = brute.add(acc, p, brute.round_f32)
-            want = brute.round_bf16(acc)
-            assert brute.decode_bf16(int(y[j])).key() == want.key() or (acc.q == 0), (k, n, j)
+            tot = None
+            for b in range(nb):
+                acc = prods[b * kb]
+                for p in prods[b * kb + 1:(b + 1) * kb]:
+                    acc = brute.add(acc, p, brute.round_f32)
+                tot = acc if tot is None else brute.add(tot, acc, brute.round_f32)
+            want = brute.round_bf16(tot)
+            assert brute.decode_bf16(int(y[j])).key() == want.key() or (tot.q == 0), (k, n, j)
+
+
+def test_gemv_block_order_is_observable():
+    # the blocked order differs from one chain over all k on this data (pins the blocking)
+    rng = synth.seeded_rng(402)
+    k, n = 64, 512
+    wt = synth.normal_bf16(rng, (k, n))
+    x = synth.normal_bf16(rng, k)
+    xs = x.copy()
+    a = collectives.gemv_payloads([wt], [x], kblocks=8)[0]
+    b = collectives.gemv_payloads([wt], [xs], kblocks=1)[0]
+    assert not np.array_equal(a, b)
 
 
 def test_gemv_payload_closed_forms():
