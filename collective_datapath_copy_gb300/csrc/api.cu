@@ -188,7 +188,8 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
   const coll_compiled &c = p->c;
   const int R = c.R;
   if (wt) {
-    if (c.cfg.zero_copy || c.dtype != COLL_BF16 || k < 8 || (k & 7u)) return COLL_EINVAL;
+    // eight warps each take k/8 rows, eight at a time: k must be a multiple of 64
+    if (c.cfg.zero_copy || c.dtype != COLL_BF16 || k < 64 || (k & 63u)) return COLL_EINVAL;
     for (int r = 0; r < R; ++r) {
       if (!c.in_used[r]) continue;
       if (!wt[r]) return COLL_EINVAL;

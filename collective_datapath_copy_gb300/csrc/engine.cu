@@ -276,39 +276,125 @@ __device__ __forceinline__ uint4 gather_pieces(const char *xb, uint32_t nbytes, 
   return active ? acc.pack() : make_uint4(0, 0, 0, 0);
 }
 
-// Fused producer: this lane's 8 consecutive payload elements of y = W x, i.e. for each
-// output column j: products w[i][j] * x[i] rounded to binary32, added in order i = 0..k-1
-// (round to nearest even), then rounded once to bf16. wcol points at row 0 of the lane's
-// 8 columns; ws is the row stride in bytes; k is a multiple of 8.
-__device__ __forceinline__ uint4 gemv_piece(const char *wcol, int64_t ws, const char *xp,
-                                            uint32_t k) {
-  float acc[8];
-  for (uint32_t i0 = 0; i0 < k; i0 += 8) {
-    const uint4 xv = ld_nc_v4(xp + (size_t)i0 * 2);
-    uint4 w[8];
+// ------------------------------------------------------------------ fused producer
+// The fused-producer variant runs eight warps per CTA: warp 0 plays the engine warp, and at
+// each stage all eight warps compute one k-block each of the piece's dot products (lane l:
+// outputs 8l..8l+7). Block b covers rows [b*k/8, (b+1)*k/8): products rounded to binary32,
+// added in row order from the block's first product; warp 0 then adds the eight block sums
+// in block order and rounds once to bf16.
+constexpr uint32_t kGemvWarps = 8;
+
+struct GemvShared {
+  const char *wcol;  // row 0 of the piece's columns (lane offset not included)
+  const char *xp;    // x vector of this epoch
+  int64_t ws;        // row stride in bytes
+  uint32_t k;
+  uint32_t active;   // lanes below this hold outputs
+  uint32_t exit;
+  float part[kGemvWarps][32][8];
+};
+
+__device__ __forceinline__ GemvShared &gemv_smem() {
+  __shared__ GemvShared g;
+  return g;
+}
+
+__device__ __forceinline__ void gemv_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__device__ __forceinline__ void gemv_rows8(float acc[8], const uint4 w[8], uint4 xv, bool first) {
+  float xf[8];
+  bf16x8_init(xf, xv);
 #pragma unroll
-    for (uint32_t t = 0; t < 8; ++t) w[t] = ld_nc_v4(wcol + (int64_t)(i0 + t) * ws);
-    float xf[8];
-    bf16x8_init(xf, xv);
+  for (uint32_t t = 0; t < 8; ++t) {
+    float wf[8];
+    bf16x8_init(wf, w[t]);
+    if (first && t == 0) {
 #pragma unroll
-    for (uint32_t t = 0; t < 8; ++t) {
-      float wf[8];
-      bf16x8_init(wf, w[t]);
-      if (i0 + t == 0) {
+      for (int e = 0; e < 8; ++e) acc[e] = __fmul_rn(wf[e], xf[t]);
+    } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = __fmul_rn(wf[e], xf[t]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], __fmul_rn(wf[e], xf[t]));
-      }
+      for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], __fmul_rn(wf[e], xf[t]));
     }
   }
+}
+
+// This warp's k-block into g.part[wid][lane]; weight rows double-buffered in registers.
+__device__ __forceinline__ void gemv_block(GemvShared &g, uint32_t wid, uint32_t lane) {
+  const uint32_t kb = g.k / kGemvWarps;
+  const uint32_t r0 = wid * kb;
+  const bool act = lane < g.active;
+  const char *wp = g.wcol + (int64_t)r0 * g.ws + lane * 16;
+  const char *xp = g.xp + (size_t)r0 * 2;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  uint4 wa[8], wb[8], xa = make_uint4(0, 0, 0, 0), xb = make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (uint32_t t = 0; t < 8; ++t) wa[t] = act ? ld_nc_v4(wp + (int64_t)t * g.ws) : make_uint4(0, 0, 0, 0);
+  xa = ld_nc_v4(xp);
+  for (uint32_t i0 = 0; i0 < kb; i0 += 16) {
+    if (i0 + 8 < kb) {
+#pragma unroll
+      for (uint32_t t = 0; t < 8; ++t)
+        wb[t] = act ? ld_nc_v4(wp + (int64_t)(i0 + 8 + t) * g.ws) : make_uint4(0, 0, 0, 0);
+      xb = ld_nc_v4(xp + (size_t)(i0 + 8) * 2);
+    }
+    gemv_rows8(acc, wa, xa, i0 == 0);
+    if (i0 + 8 >= kb) break;
+    if (i0 + 16 < kb) {
+#pragma unroll
+      for (uint32_t t = 0; t < 8; ++t)
+        wa[t] = act ? ld_nc_v4(wp + (int64_t)(i0 + 16 + t) * g.ws) : make_uint4(0, 0, 0, 0);
+      xa = ld_nc_v4(xp + (size_t)(i0 + 16) * 2);
+    }
+    gemv_rows8(acc, wb, xb, false);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) g.part[wid][lane][e] = acc[e];
+}
+
+// Helper warps (1..7): compute a block whenever warp 0 opens a stage, until told to exit.
+__device__ void gemv_helper_loop(uint32_t wid, uint32_t lane) {
+  GemvShared &g = gemv_smem();
+  for (;;) {
+    gemv_bar();
+    if (g.exit) return;
+    gemv_block(g, wid, lane);
+    gemv_bar();
+  }
+}
+
+// Warp 0 (all 32 lanes): one piece of y = W x for the lanes below `active`.
+__device__ __forceinline__ uint4 gemv_piece_mw(const char *wcol, int64_t ws, const char *xp,
+                                               uint32_t k, uint32_t active, uint32_t lane) {
+  GemvShared &g = gemv_smem();
+  if (lane == 0) {
+    g.wcol = wcol;
+    g.xp = xp;
+    g.ws = ws;
+    g.k = k;
+    g.active = active;
+    g.exit = 0;
+  }
+  __syncwarp();
+  gemv_bar();  // open: helpers start their blocks
+  gemv_block(g, 0, lane);
+  gemv_bar();  // every block sum is in shared memory
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = g.part[0][lane][e];
+#pragma unroll
+  for (uint32_t b = 1; b < kGemvWarps; ++b)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], g.part[b][lane][e]);
   return bf16x8_pack(acc);
 }
 
-// Speculatively load (and reduce) the n pieces of a unit, issue the flag loads while the
-// payload loads are in flight, and hash what was loaded (per producer, warp-reduced; lane j
-// keeps producer j's hash). Returns the packed result of this attempt.
+__device__ __forceinline__ void gemv_release_helpers(uint32_t lane) {
+  GemvShared &g = gemv_smem();
+  if (lane == 0) g.exit = 1;
+  __syncwarp();
+  gemv_bar();
+}
+
 // Validation of a speculative load: lane j < n holds producer j's flag word {epoch, tag}
 // and every lane holds its share of the hash of what it loaded. Passes iff every producer
 // notified epoch E and the producers' tags (hash + E*K each) add up to the loaded hash plus
@@ -360,10 +446,22 @@ __device__ __forceinline__ uint4 spec_attempt(const char *xb, uint32_t nbytes, u
 }
 
 template <int KIND, bool GEMV, bool LL>
-__global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
+__global__ void __launch_bounds__(GEMV ? 32 * kGemvWarps : 32, 1) engine_kernel(const EngArgs a) {
   const uint32_t gw = blockIdx.x;
-  if (gw >= a.nwarps) return;
-  const uint32_t lane = threadIdx.x;
+  const uint32_t lane = threadIdx.x & 31u;
+  if constexpr (GEMV) {
+    const uint32_t wid = threadIdx.x >> 5;
+    if (wid != 0) {
+      gemv_helper_loop(wid, lane);
+      return;
+    }
+    if (gw >= a.nwarps) {
+      gemv_release_helpers(lane);
+      return;
+    }
+  } else {
+    if (gw >= a.nwarps) return;
+  }
   const coll_warp_t W = a.warps[gw];
   coll_dev_status_t *st = a.st;
   const bool spec_proto = a.protocol == COLL_PROTO_SPEC;
@@ -501,13 +599,11 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
         x = nx;
         if (tagged && !nh_ready && lane < nvec) h = tag_part(x, lane);
       } else if constexpr (GEMV) {
-        // fused producer: compute this piece of the payload in place of loading it
-        if (lane < nvec) {
-          const coll_ref_t r = a.refs[u.src0 + it.slot];
-          x = gemv_piece(a.wt[r.rank] + r.off + u.start + lane * 16, a.wt_stride[r.rank],
-                         a.ptr.in[r.rank] + in_off, a.gemv_k);
-          if (tagged) h = tag_part(x, lane);
-        }
+        // fused producer: the CTA's eight warps compute this piece of the payload
+        const coll_ref_t r = a.refs[u.src0 + it.slot];
+        x = gemv_piece_mw(a.wt[r.rank] + r.off + u.start, a.wt_stride[r.rank],
+                          a.ptr.in[r.rank] + in_off, a.gemv_k, nvec, lane);
+        if (tagged && lane < nvec) h = tag_part(x, lane);
       } else if (lane < nvec) {
         const coll_ref_t r = a.refs[u.src0 + it.slot];
         x = ld_nc_v4(a.ptr.in[r.rank] + r.off + in_off + u.start + lane * 16);
@@ -720,6 +816,7 @@ __global__ void __launch_bounds__(32) engine_kernel(const EngArgs a) {
     }
     if (stamp && (uint32_t)i < a.stamp_cap) a.stamps[phases ? 4 + 4 * i : i + 1] = globaltimer();
   }
+  if constexpr (GEMV) gemv_release_helpers(lane);
   if (lane == 0) {
     if (n_checks) atomicAdd(&st->spec_checks, (unsigned long long)n_checks);
     if (n_retries) atomicAdd(&st->spec_retries, (unsigned long long)n_retries);
@@ -826,7 +923,8 @@ cudaError_t engine_max_coresident(int op, int dtype, int protocol, int *max_ctas
                                                     32, 0);
   if (e != cudaSuccess) return e;
   if (!ll) {  // a plan of this protocol may also run the fused-producer variant
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_g, engine_fn(1, true, false), 32, 0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_g, engine_fn(1, true, false),
+                                                      32 * kGemvWarps, 0);
     if (e != cudaSuccess) return e;
     if (per_sm_g < per_sm) per_sm = per_sm_g;
   }
@@ -844,9 +942,10 @@ cudaError_t launch_probe_rtt(unsigned long long *flags, uint32_t iters, uint32_t
 cudaError_t launch_engine(int op, int dtype, const EngArgs &a, cudaStream_t s) {
   if (a.nwarps == 0 || a.n_epochs == 0) return cudaSuccess;
   void *args[] = {(void *)&a};
+  const bool gemv = a.gemv_k != 0;
   return cudaLaunchCooperativeKernel(
-      engine_fn(kind_of(op, dtype), a.gemv_k != 0, a.protocol == COLL_PROTO_LL),
-      dim3(a.nwarps), dim3(32), args, 0, s);
+      engine_fn(kind_of(op, dtype), gemv, a.protocol == COLL_PROTO_LL), dim3(a.nwarps),
+      dim3(gemv ? 32 * kGemvWarps : 32), args, 0, s);
 }
 
 }  // namespace coll

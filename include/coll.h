@@ -220,11 +220,13 @@ int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_epochs,
  * megakernels, after each layer's computation). At epoch i rank r's input buffer (in_len[r]
  * bf16 elements, the buffer the naming refers to) is y_r = W_r x_r(i): wt[r] is W_r given
  * transposed, k rows of in_len[r] bf16 (row stride in_len[r] elements), and x_r(i) =
- * x[r] + (i % x_pool) * x_epoch_stride bytes holds k bf16. Element j of y_r: products
- * wt[r][i][j] * x_r(i)[i] rounded to binary32, added in order i = 0..k-1 (round to nearest
- * even), then rounded once to bf16. k must be a multiple of 8; in_len[r], wt[r], x[r] and
- * the strides must give 16-byte alignment. Errors as coll_run, plus COLL_EINVAL for a
- * zero-copy or non-bf16 plan. */
+ * x[r] + (i % x_pool) * x_epoch_stride bytes holds k bf16. Element j of y_r: the k terms are
+ * taken in 8 consecutive blocks of k/8; within a block, products wt[r][i][j] * x_r(i)[i]
+ * rounded to binary32 are added in row order from the block's first product (round to
+ * nearest even); the 8 block sums are added in block order; one rounding to bf16. Each
+ * engine CTA runs 8 warps in this mode (every plan warp must still be co-resident). k must
+ * be a multiple of 64; in_len[r], wt[r], x[r] and the strides must give 16-byte alignment.
+ * Errors as coll_run, plus COLL_EINVAL for a zero-copy, tagged-data or non-bf16 plan. */
 int coll_run_gemv(coll_plan_t p, const void *const *wt, void *const *x, int k, void *const *out,
                   int n_epochs, int64_t x_epoch_stride, int x_pool, int64_t out_epoch_stride,
                   void *stream);
