@@ -478,6 +478,12 @@ def run_workload(args):
     R = 8
     g = torch.Generator(device=dev)
     res = {"workload": args.workload, "peak_gbs": peak, "peak_kind": peak_kind}
+    # the floor of this timing method: a one-element kernel timed the same way (flush, then
+    # CUDA events around one launch); single-launch times below include it
+    one = torch.zeros(1, device=dev)
+    tfl = _time_steps(torch, lambda: one.add_(1), max(5, args.steps), args.warmup, flush, stream)
+    floor_us = sorted(tfl)[len(tfl) // 2] * 1000
+    res["launch_floor_us"] = round(floor_us, 3)
     if args.workload == "sweep":
         sizes = [1 << k for k in range(10, 29, 2)]  # 1 KiB .. 256 MiB per rank
         if args.max_bytes:
@@ -498,8 +504,11 @@ def run_workload(args):
                 for tag, cfg in cfgs.items():
                     r = _zc_measure(torch, cdc, nm, ins, outs, args.steps, args.warmup, flush,
                                     stream, graph_reps=50 if m <= (4 << 20) else 0, **cfg)
+                    net = max(r["us"] - floor_us, 1e-3)
                     r.update({"collective": kind + (f"-{tag}" if tag else ""), "bytes_per_rank": m,
-                              "frac": round(r["gbs"] / peak, 4)})
+                              "frac": round(r["gbs"] / peak, 4),
+                              "frac_excl_launch_floor": round(r["min_bytes"] / (net * 1e-6) / 1e9
+                                                              / peak, 4)})
                     rows.append(r)
                 del outs
             del ins
