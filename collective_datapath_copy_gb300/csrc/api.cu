@@ -33,6 +33,7 @@ struct coll_plan_s {
   bool ran = false;
   bool captured = false;  // a run was captured into a graph: status waits for the device
   int last_epochs = 0;
+  int gemv_cap = -1;  // co-resident fused-producer CTAs; queried on the first fused run
 };
 
 namespace {
@@ -195,6 +196,13 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
       if (!wt[r]) return COLL_EINVAL;
       if (((uintptr_t)wt[r] & 15u) || (c.in_bytes[r] & 15u)) return COLL_EALIGN;
     }
+    // the fused CTAs are larger (nine warps and a shared-memory ring): all must still fit
+    if (p->gemv_cap < 0 && coll::engine_gemv_max_coresident(&p->gemv_cap) != cudaSuccess) {
+      cudaGetLastError();
+      p->gemv_cap = -1;
+      return COLL_ECUDA;
+    }
+    if (c.warps.size() > (size_t)p->gemv_cap) return COLL_EINVAL;
   }
   // bytes of one rank's per-epoch input as the kernel reads it
   auto in_span = [&](int r) -> uint64_t { return wt ? (uint64_t)k * 2 : c.in_bytes[r]; };

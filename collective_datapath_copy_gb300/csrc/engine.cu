@@ -16,6 +16,7 @@
 
 #include "atom.cuh"
 #include "engine.cuh"
+#include "tma.cuh"
 
 namespace coll {
 
@@ -277,20 +278,53 @@ __device__ __forceinline__ uint4 gather_pieces(const char *xb, uint32_t nbytes, 
 }
 
 // ------------------------------------------------------------------ fused producer
-// The fused-producer variant runs eight warps per CTA: warp 0 plays the engine warp, and at
-// each stage all eight warps compute one k-block each of the piece's dot products (lane l:
-// outputs 8l..8l+7). Block b covers rows [b*k/8, (b+1)*k/8): products rounded to binary32,
-// added in row order from the block's first product; warp 0 then adds the eight block sums
-// in block order and rounds once to bf16.
-constexpr uint32_t kGemvWarps = 8;
+// The fused-producer variant runs twelve warps per CTA in three warpgroups. Warp 0 plays the
+// engine warp; warps 4..11 are compute warps: at each stage compute warp b computes k-block b
+// of the piece's dot products (lane l: outputs 8l..8l+7). Block b covers rows
+// [b*k/8, (b+1)*k/8): products rounded to binary32, added in row order from the block's
+// first product; warp 0 then adds the eight block sums in block order and rounds once to
+// bf16. Warps 1..3 only complete the first warpgroup. The register file is split by
+// warpgroup (setmaxnreg): the engine's warpgroup takes 248 registers a thread, the compute
+// warpgroups 120, so neither the engine state nor the compute loop spills.
+//
+// The weight rows reach the compute warps through shared-memory slots of 8 rows filled by
+// asynchronous copies; each compute warp owns 6 slots (a private ring) and streams its own
+// k-block through them. Fill q of warp b (its q-th slot of rows over the run: piece
+// q / (k/64), slot q % (k/64) of block b, pieces in epoch-major stage-item order) lands in
+// the warp's slot q % 6; having read fill q, the warp issues fill q + 6 into the same slot.
+// So each warp always has its next 6 slots of rows in flight: while the engine warp runs the
+// exchange of one epoch, the next piece's rows are already arriving (the weights do not
+// depend on the epoch's data), and within a long block a refill has 5 slots of compute to
+// land.
+constexpr uint32_t kGemvWarps = 8;                                   // compute warps
+constexpr uint32_t kGemvFirst = 4;                                   // warp of compute warp 0
+constexpr uint32_t kGemvThreads = 32 * (kGemvFirst + kGemvWarps);   // 384
+constexpr uint32_t kGemvBarThreads = 32 * (1 + kGemvWarps);          // engine + compute warps
+constexpr uint32_t kGemvLaunchRegs = 168;  // per thread at launch: 65536 / 384, rounded to 8
+constexpr uint32_t kGemvEngineRegs = 248;  // engine warpgroup after the split
+constexpr uint32_t kGemvComputeRegs = 120; // compute warpgroups after the split
+static_assert(128 * kGemvEngineRegs + 256 * kGemvComputeRegs <= kGemvThreads * kGemvLaunchRegs,
+              "the split must fit in the registers the CTA was launched with");
+constexpr uint32_t kGemvRows = 8;                        // weight rows per ring slot
+constexpr uint32_t kGemvPitch = 512;                     // bytes per staged row (a piece is <= 512 B)
+constexpr uint32_t kGemvSlotBytes = kGemvRows * kGemvPitch;
+constexpr uint32_t kGemvSlotsPerWarp = 6;
+constexpr uint32_t kGemvSlots = kGemvSlotsPerWarp * kGemvWarps;  // 192 KiB of rows in flight
+constexpr uint32_t kGemvSmemBytes = kGemvSlots * kGemvSlotBytes + kGemvSlots * 8;
+constexpr uint32_t kGemvMaxItems = 16;                   // stage items whose rows are cached
 
 struct GemvShared {
-  const char *wcol;  // row 0 of the piece's columns (lane offset not included)
   const char *xp;    // x vector of this epoch
-  int64_t ws;        // row stride in bytes
-  uint32_t k;
   uint32_t active;   // lanes below this hold outputs
-  uint32_t exit;
+  uint32_t exit;     // set by warp 0: the other warps return
+  uint32_t fail;     // a compute warp's ring wait gave up
+  uint32_t nitems;   // stage items of this warp, in order
+  uint32_t S;        // slots per piece
+  uint64_t total;    // fills of the whole run, per compute warp
+  const char *wbase[kGemvMaxItems];  // row 0 of each item's columns
+  int64_t wstride[kGemvMaxItems];
+  uint32_t wbytes[kGemvMaxItems];
+  uint32_t fills[kGemvSlots];        // fills issued per slot
   float part[kGemvWarps][32][8];
 };
 
@@ -299,84 +333,277 @@ __device__ __forceinline__ GemvShared &gemv_smem() {
   return g;
 }
 
-__device__ __forceinline__ void gemv_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+struct GemvRing {
+  unsigned char *rows;  // [kGemvSlots][kGemvRows][kGemvPitch]
+  uint64_t *full;       // [kGemvSlots] completes when a fill's rows have landed
+};
 
-__device__ __forceinline__ void gemv_rows8(float acc[8], const uint4 w[8], uint4 xv, bool first) {
-  float xf[8];
-  bf16x8_init(xf, xv);
+__device__ __forceinline__ GemvRing gemv_ring() {
+  extern __shared__ __align__(128) unsigned char gemv_dyn[];
+  GemvRing r;
+  r.rows = gemv_dyn;
+  r.full = reinterpret_cast<uint64_t *>(gemv_dyn + kGemvSlots * kGemvSlotBytes);
+  return r;
+}
+
+__device__ __forceinline__ void gemv_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kGemvBarThreads) : "memory");
+}
+
+// Where the rows of one fill come from.
+struct GemvSrc {
+  const char *base;
+  int64_t stride;
+  uint32_t nbytes;
+};
+
+// Rows of item `idx` of this CTA's warp: cached in shared memory for the first items, read
+// from the plan tables beyond that.
+__device__ __forceinline__ GemvSrc gemv_item(const EngArgs &a, const GemvShared &g,
+                                             const coll_warp_t &W, uint32_t idx) {
+  if (idx < kGemvMaxItems) return GemvSrc{g.wbase[idx], g.wstride[idx], g.wbytes[idx]};
+  const coll_item_t it = a.sitems[W.s0 + idx];
+  const coll_unit_t u = a.units[it.unit];
+  const coll_ref_t r = a.refs[u.src0 + it.slot];
+  return GemvSrc{a.wt[r.rank] + r.off + u.start, a.wt_stride[r.rank], u.nbytes};
+}
+
+// Issue one fill into `slot` (all lanes call): rows 8*rj..8*rj+7 of `src`, each lane copying
+// its 16 bytes of every row with cp.async (the load/store unit's asynchronous copy: small
+// strided rows are cheap this way, where one bulk copy per 512-byte row would queue on the
+// bulk-copy unit). Each lane then arrives on the slot's barrier once its copies have landed
+// (32 arrivals complete the fill). Lane 0 counts the fill. The slot must be free: the
+// calling warp has issued its reads of the previous fill (each lane's copies land only in
+// the column that lane read, hundreds of cycles after the shared-memory reads it issued
+// before them).
+__device__ __forceinline__ void gemv_fill(GemvShared &g, const GemvRing &ring, uint32_t slot,
+                                          const GemvSrc &src, uint32_t rj, uint32_t lane) {
+  if (lane == 0)
+    *reinterpret_cast<volatile uint32_t *>(&g.fills[slot]) = g.fills[slot] + 1u;
+  if (lane * 16u < src.nbytes) {
+    const uint32_t d = smem_u32(ring.rows + slot * kGemvSlotBytes + lane * 16);
+    const char *p = src.base + (int64_t)rj * kGemvRows * src.stride + lane * 16;
+#pragma unroll
+    for (uint32_t t = 0; t < kGemvRows; ++t)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + t * kGemvPitch),
+                   "l"(p + (int64_t)t * src.stride)
+                   : "memory");
+  }
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&ring.full[slot]))
+               : "memory");
+}
+
+// Packed pairs of binary32 (sm_100 family): two IEEE operations, round to nearest even.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// bf16 elements 2j, 2j+1 of a word -> {binary32, binary32}
+__device__ __forceinline__ uint64_t bf16x2_widen(uint32_t w) {
+  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// Eight rows of this lane's eight outputs: acc[p] holds outputs (2p, 2p+1).
+template <bool FIRST>
+__device__ __forceinline__ void gemv_rows8(uint64_t acc[4], const uint4 w[8], uint4 xv) {
+  const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
   for (uint32_t t = 0; t < 8; ++t) {
-    float wf[8];
-    bf16x8_init(wf, w[t]);
-    if (first && t == 0) {
+    const float xf = __uint_as_float((t & 1u) ? (xw[t >> 1] & 0xFFFF0000u) : (xw[t >> 1] << 16));
+    const uint64_t xx = f2_pack(xf, xf);
+    const uint32_t ww[4] = {w[t].x, w[t].y, w[t].z, w[t].w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = __fmul_rn(wf[e], xf[t]);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], __fmul_rn(wf[e], xf[t]));
+    for (uint32_t p = 0; p < 4; ++p) {
+      const uint64_t prod = f2_mul(bf16x2_widen(ww[p]), xx);
+      acc[p] = (FIRST && t == 0) ? prod : f2_add(acc[p], prod);
     }
   }
 }
 
-// This warp's k-block into g.part[wid][lane]; weight rows double-buffered in registers.
-__device__ __forceinline__ void gemv_block(GemvShared &g, uint32_t wid, uint32_t lane) {
-  const uint32_t kb = g.k / kGemvWarps;
-  const uint32_t r0 = wid * kb;
+// Position of a compute warp's reads in its private ring, and of the refills it issues.
+struct GemvCursor {
+  uint64_t q, lap;  // fill read next: number q, lap q / 6 of the warp's slot q % 6
+  uint32_t slot;    // ring slot (warp base + q % 6)
+  uint32_t rp_j;    // refill q + 6: slot rp_j of the block ...
+  uint32_t ri;      // ... of stage item ri
+  GemvSrc src;      // rows of item ri
+};
+
+// Fill number `q` of compute warp `wid` into its slot (all lanes call).
+__device__ __forceinline__ void gemv_fill_block(GemvShared &g, const GemvRing &ring, uint32_t slot,
+                                                const GemvSrc &src, uint32_t wid, uint32_t bs,
+                                                uint32_t j, uint32_t lane) {
+  gemv_fill(g, ring, slot, src, wid * bs + j, lane);
+}
+
+// Compute warp `wid`, before its first block: issue its first 6 fills.
+__device__ void gemv_warp_prologue(const EngArgs &a, GemvShared &g, const GemvRing &ring,
+                                   const coll_warp_t &W, uint32_t wid, uint32_t lane) {
+  const uint32_t bs = g.S / kGemvWarps;
+  uint32_t j = 0, ri = 0;
+  GemvSrc src = gemv_item(a, g, W, 0);
+  for (uint32_t q = 0; q < kGemvSlotsPerWarp && q < g.total; ++q) {
+    gemv_fill_block(g, ring, wid * kGemvSlotsPerWarp + q, src, wid, bs, j, lane);
+    if (++j == bs) {
+      j = 0;
+      if (++ri == g.nitems) ri = 0;
+      src = gemv_item(a, g, W, ri);
+    }
+  }
+}
+
+// This warp's k-block of piece `piece` into g.part[wid][lane], streaming the block's rows
+// through the warp's private ring (see above). The readiness of up to 32 slots is tested at
+// once, so slots that landed during the exchange cost no wait each.
+__device__ __forceinline__ void gemv_block(const EngArgs &a, GemvShared &g, const GemvRing &ring,
+                                           const coll_warp_t &W, uint64_t piece, uint32_t wid,
+                                           uint32_t lane) {
+  const uint32_t bs = g.S / kGemvWarps;  // slots per block
+  const uint64_t total = g.total;
+  const uint32_t base = wid * kGemvSlotsPerWarp;
+  GemvCursor c;
+  c.q = piece * bs;
+  c.lap = c.q / kGemvSlotsPerWarp;
+  c.slot = base + (uint32_t)(c.q - c.lap * kGemvSlotsPerWarp);
+  // refill q + 6: piece (q + 6) / bs, slot (q + 6) % bs of this warp's block
+  const uint64_t rq = c.q + kGemvSlotsPerWarp;
+  const uint64_t rpiece = rq / bs;  // one division per block
+  c.rp_j = (uint32_t)(rq - rpiece * bs);
+  c.ri = (uint32_t)(rpiece % g.nitems);
+  c.src = gemv_item(a, g, W, c.ri);
   const bool act = lane < g.active;
-  const char *wp = g.wcol + (int64_t)r0 * g.ws + lane * 16;
-  const char *xp = g.xp + (size_t)r0 * 2;
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  uint4 wa[8], wb[8], xa = make_uint4(0, 0, 0, 0), xb = make_uint4(0, 0, 0, 0);
-#pragma unroll
-  for (uint32_t t = 0; t < 8; ++t) wa[t] = act ? ld_nc_v4(wp + (int64_t)t * g.ws) : make_uint4(0, 0, 0, 0);
-  xa = ld_nc_v4(xp);
-  for (uint32_t i0 = 0; i0 < kb; i0 += 16) {
-    if (i0 + 8 < kb) {
-#pragma unroll
-      for (uint32_t t = 0; t < 8; ++t)
-        wb[t] = act ? ld_nc_v4(wp + (int64_t)(i0 + 8 + t) * g.ws) : make_uint4(0, 0, 0, 0);
-      xb = ld_nc_v4(xp + (size_t)(i0 + 8) * 2);
+  // x of this block: lane t holds the 8 values of slot 32c+t of chunk c, loaded together
+  // (one memory round trip per 32 slots), and each slot's values are broadcast by shuffle
+  const char *xp = g.xp + (size_t)wid * bs * (kGemvRows * 2);
+  uint64_t acc[4] = {0, 0, 0, 0};
+  uint4 xl = make_uint4(0, 0, 0, 0);
+  uint32_t ready = 0;  // bit t: the fill of slot 32c+t of this chunk has already landed
+  for (uint32_t j = 0; j < bs; ++j) {
+    if ((j & 31u) == 0u) {
+      // per chunk of 32 slots: one x load and one readiness test per lane, in parallel
+      // (only the fills already issued, at most 6 ahead, can have landed)
+      bool r = false;
+      if (j + lane < bs) xl = ld_nc_v4(xp + (size_t)(j + lane) * 16);
+      if (j + lane < bs && lane < kGemvSlotsPerWarp) {
+        const uint64_t ql = c.q + lane;
+        const uint64_t lp = ql / kGemvSlotsPerWarp;
+        const uint32_t sl = base + (uint32_t)(ql - lp * kGemvSlotsPerWarp);
+        r = mbar_test_wait(&ring.full[sl], (uint32_t)(lp & 1u));
+      }
+      ready = __ballot_sync(FULL, r);
+      __syncwarp();  // orders each lane's acquiring test before every lane's reads
     }
-    gemv_rows8(acc, wa, xa, i0 == 0);
-    if (i0 + 8 >= kb) break;
-    if (i0 + 16 < kb) {
-#pragma unroll
-      for (uint32_t t = 0; t < 8; ++t)
-        wa[t] = act ? ld_nc_v4(wp + (int64_t)(i0 + 16 + t) * g.ws) : make_uint4(0, 0, 0, 0);
-      xa = ld_nc_v4(xp + (size_t)(i0 + 16) * 2);
+    uint4 xv;
+    xv.x = __shfl_sync(FULL, xl.x, j & 31u);
+    xv.y = __shfl_sync(FULL, xl.y, j & 31u);
+    xv.z = __shfl_sync(FULL, xl.z, j & 31u);
+    xv.w = __shfl_sync(FULL, xl.w, j & 31u);
+    bool ok = true;
+    if (!((ready >> (j & 31u)) & 1u)) {
+      // (this warp issued the fill itself, so the slot's previous phase has completed and
+      // the parity identifies the fill)
+      if (lane == 0)
+        ok = mbar_wait_until(&ring.full[c.slot], (uint32_t)(c.lap & 1u), a.spin_ns,
+                             [&a]() { return ld_relaxed_u32(&a.st->abort) != 0u; });
+      ok = __shfl_sync(FULL, ok, 0);
+      __syncwarp();  // orders lane 0's acquiring wait before every lane's reads
     }
-    gemv_rows8(acc, wb, xb, false);
+    if (!ok) {
+      if (lane == 0) {
+        record_timeout(a.st, (int)W.rank, -1, 6, 0);
+        g.fail = 1;
+      }
+      break;
+    }
+    const unsigned char *s = ring.rows + c.slot * kGemvSlotBytes + lane * 16;
+    uint4 w[8];
+#pragma unroll
+    for (uint32_t t = 0; t < 8; ++t)
+      w[t] = act ? *reinterpret_cast<const uint4 *>(s + t * kGemvPitch) : make_uint4(0, 0, 0, 0);
+    // Refill the slot now, so that the copies overlap this slot's arithmetic: each lane's
+    // copies overwrite only the 16-byte column it has just read, after its reads in program
+    // order.
+    if (c.q + kGemvSlotsPerWarp < total)
+      gemv_fill_block(g, ring, c.slot, c.src, wid, bs, c.rp_j, lane);
+    if (j == 0) gemv_rows8<true>(acc, w, xv); else gemv_rows8<false>(acc, w, xv);
+    ++c.q;
+    if (++c.slot == base + kGemvSlotsPerWarp) {
+      c.slot = base;
+      ++c.lap;
+    }
+    if (++c.rp_j == bs) {
+      c.rp_j = 0;
+      if (++c.ri == g.nitems) c.ri = 0;
+      c.src = gemv_item(a, g, W, c.ri);
+    }
   }
 #pragma unroll
-  for (int e = 0; e < 8; ++e) g.part[wid][lane][e] = acc[e];
+  for (int p = 0; p < 4; ++p) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(acc[p]));
+    g.part[wid][lane][2 * p] = lo;
+    g.part[wid][lane][2 * p + 1] = hi;
+  }
 }
 
-// Helper warps (1..7): compute a block whenever warp 0 opens a stage, until told to exit.
-__device__ void gemv_helper_loop(uint32_t wid, uint32_t lane) {
+// Warp 0, before the epoch loop: cache the stage items' row sources and the run's sizes.
+__device__ void gemv_prologue(const EngArgs &a, const coll_warp_t &W, uint32_t lane) {
   GemvShared &g = gemv_smem();
-  for (;;) {
+  const uint32_t nitems = W.s1 - W.s0;
+  if (lane == 0) {
+    g.nitems = nitems;
+    g.S = a.gemv_k / kGemvRows;
+    g.total = (uint64_t)a.n_epochs * nitems * (a.gemv_k / (kGemvRows * kGemvWarps));
+  }
+  for (uint32_t idx = lane; idx < nitems && idx < kGemvMaxItems; idx += 32) {
+    const coll_item_t it = a.sitems[W.s0 + idx];
+    const coll_unit_t u = a.units[it.unit];
+    const coll_ref_t r = a.refs[u.src0 + it.slot];
+    g.wbase[idx] = a.wt[r.rank] + r.off + u.start;
+    g.wstride[idx] = a.wt_stride[r.rank];
+    g.wbytes[idx] = u.nbytes;
+  }
+}
+
+// Compute warp `wid` (0..7): compute block wid whenever warp 0 opens a stage, until told to
+// exit.
+__device__ void gemv_helper_loop(const EngArgs &a, const coll_warp_t &W, uint32_t wid,
+                                 uint32_t lane) {
+  GemvShared &g = gemv_smem();
+  const GemvRing ring = gemv_ring();
+  gemv_warp_prologue(a, g, ring, W, wid, lane);
+  for (uint64_t piece = 0;; ++piece) {
     gemv_bar();
     if (g.exit) return;
-    gemv_block(g, wid, lane);
+    gemv_block(a, g, ring, W, piece, wid, lane);
     gemv_bar();
   }
 }
 
-// Warp 0 (all 32 lanes): one piece of y = W x for the lanes below `active`.
-__device__ __forceinline__ uint4 gemv_piece_mw(const char *wcol, int64_t ws, const char *xp,
-                                               uint32_t k, uint32_t active, uint32_t lane) {
+// Warp 0 (all 32 lanes): piece number `piece` of y = W x for the lanes below `active`;
+// false if a ring wait gave up (the status word then holds the timeout).
+__device__ __forceinline__ bool gemv_piece_mw(const EngArgs &a, const coll_warp_t &W,
+                                              const char *xp, uint32_t active, uint64_t piece,
+                                              uint32_t lane, uint4 &res) {
   GemvShared &g = gemv_smem();
+  const GemvRing ring = gemv_ring();
   if (lane == 0) {
-    g.wcol = wcol;
     g.xp = xp;
-    g.ws = ws;
-    g.k = k;
     g.active = active;
-    g.exit = 0;
   }
   __syncwarp();
-  gemv_bar();  // open: helpers start their blocks
-  gemv_block(g, 0, lane);
+  gemv_bar();  // open: the compute warps start their blocks
   gemv_bar();  // every block sum is in shared memory
   float acc[8];
 #pragma unroll
@@ -385,14 +612,25 @@ __device__ __forceinline__ uint4 gemv_piece_mw(const char *wcol, int64_t ws, con
   for (uint32_t b = 1; b < kGemvWarps; ++b)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], g.part[b][lane][e]);
-  return bf16x8_pack(acc);
+  res = bf16x8_pack(acc);
+  return __shfl_sync(FULL, g.fail, 0) == 0u;
 }
 
-__device__ __forceinline__ void gemv_release_helpers(uint32_t lane) {
+// Warp 0 at the end: release the other warps, then wait (bounded) for every fill issued
+// so far, so that no bulk copy lands after the CTA has exited (after a failure some
+// fills are never read).
+__device__ __forceinline__ void gemv_finish(uint32_t lane) {
   GemvShared &g = gemv_smem();
-  if (lane == 0) g.exit = 1;
+  const GemvRing ring = gemv_ring();
+  if (lane == 0) *reinterpret_cast<volatile uint32_t *>(&g.exit) = 1u;
   __syncwarp();
   gemv_bar();
+  if (lane == 0) {
+    for (uint32_t s = 0; s < kGemvSlots; ++s) {
+      const uint32_t n = g.fills[s];
+      if (n) mbar_wait_until(&ring.full[s], (n - 1u) & 1u, 100000000ull, []() { return false; });
+    }
+  }
 }
 
 // Validation of a speculative load: lane j < n holds producer j's flag word {epoch, tag}
@@ -446,19 +684,36 @@ __device__ __forceinline__ uint4 spec_attempt(const char *xb, uint32_t nbytes, u
 }
 
 template <int KIND, bool GEMV, bool LL>
-__global__ void __launch_bounds__(GEMV ? 32 * kGemvWarps : 32, 1) engine_kernel(const EngArgs a) {
+__global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(const EngArgs a) {
   const uint32_t gw = blockIdx.x;
   const uint32_t lane = threadIdx.x & 31u;
   if constexpr (GEMV) {
     const uint32_t wid = threadIdx.x >> 5;
-    if (wid != 0) {
-      gemv_helper_loop(wid, lane);
+    if (threadIdx.x == 0) {
+      GemvShared &g = gemv_smem();
+      const GemvRing ring = gemv_ring();
+      g.exit = 0;
+      g.fail = 0;
+      for (uint32_t s = 0; s < kGemvSlots; ++s) {
+        g.fills[s] = 0;
+        mbar_init(&ring.full[s], 32);  // one arrival per lane of the filling warp
+      }
+      mbar_init_fence();
+    }
+    __syncthreads();
+    if (gw >= a.nwarps) return;  // (every CTA of a launch is a plan warp)
+    if (wid == 0) gemv_prologue(a, a.warps[gw], lane);
+    __syncthreads();  // the item cache and the run's fill count are set
+    // The register split: the compute warpgroups shrink, the engine's warpgroup grows. Each
+    // role then runs to the end without rejoining the other, so that each is compiled for
+    // its own register budget.
+    if (wid >= kGemvFirst) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGemvComputeRegs));
+      gemv_helper_loop(a, a.warps[gw], wid - kGemvFirst, lane);
       return;
     }
-    if (gw >= a.nwarps) {
-      gemv_release_helpers(lane);
-      return;
-    }
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kGemvEngineRegs));
+    if (wid != 0) return;
   } else {
     if (gw >= a.nwarps) return;
   }
@@ -479,12 +734,14 @@ __global__ void __launch_bounds__(GEMV ? 32 * kGemvWarps : 32, 1) engine_kernel(
                               (int)W.rank == (a.inject_rank + 1) % a.R;
   uint32_t n_checks = 0, n_retries = 0;
   bool failed = false;
+  uint64_t gpiece = 0;  // fused producer: pieces computed so far
 
   // A warp with exactly one stage item prefetches the next epoch's input piece (read-only
   // during the kernel) and hashes it while its own consume waits on memory, which takes
   // the input load and the producer-side tag off the critical path.
   constexpr bool gemv = GEMV;
-  const bool pipelined = (W.s1 - W.s0) == 1u && !gemv;
+  const bool single_s = (W.s1 - W.s0) == 1u;
+  const bool pipelined = single_s && !gemv;
   coll_unit_t su;
   coll_ref_t sref;
   coll_item_t sit;
@@ -507,10 +764,12 @@ __global__ void __launch_bounds__(GEMV ? 32 * kGemvWarps : 32, 1) engine_kernel(
   const char *sin_base = nullptr;  // single stage item: its input piece at pool entry 0
   char *cout_base = nullptr;        // single consume item: its output piece at epoch 0
   if (single_c) cout_base = a.ptr.out[cref.rank] + cref.off + cu.start;
-  if (pipelined) {
+  if (single_s) {
     sit = a.sitems[W.s0];
     su = a.units[sit.unit];
     sref = a.refs[su.src0 + sit.slot];
+  }
+  if (pipelined) {
     sin_base = a.ptr.in[sref.rank] + sref.off + su.start;
     if (lane < (su.nbytes >> 4) && a.n_epochs > 0)
       nx = ld_nc_v4(a.ptr.in[sref.rank] + sref.off + su.start + lane * 16);
@@ -570,8 +829,8 @@ __global__ void __launch_bounds__(GEMV ? 32 * kGemvWarps : 32, 1) engine_kernel(
 
     // ---------------- Stage + Notify
     for (uint32_t s = W.s0; s < W.s1; ++s) {
-      const coll_item_t it = pipelined ? sit : a.sitems[s];
-      const coll_unit_t u = pipelined ? su : a.units[it.unit];
+      const coll_item_t it = single_s ? sit : a.sitems[s];
+      const coll_unit_t u = single_s ? su : a.units[it.unit];
       if (a.protocol == COLL_PROTO_BARRIER || (u.flags & COLL_UNIT_REUSE_WAIT)) {
         // bottom barrier (single buffer) / explicit reuse wait (dual buffers)
         const uint32_t target = E - (a.protocol == COLL_PROTO_BARRIER ? 1u : 2u);
@@ -599,10 +858,13 @@ __global__ void __launch_bounds__(GEMV ? 32 * kGemvWarps : 32, 1) engine_kernel(
         x = nx;
         if (tagged && !nh_ready && lane < nvec) h = tag_part(x, lane);
       } else if constexpr (GEMV) {
-        // fused producer: the CTA's eight warps compute this piece of the payload
-        const coll_ref_t r = a.refs[u.src0 + it.slot];
-        x = gemv_piece_mw(a.wt[r.rank] + r.off + u.start, a.wt_stride[r.rank],
-                          a.ptr.in[r.rank] + in_off, a.gemv_k, nvec, lane);
+        // fused producer: the CTA's eight compute warps make this piece of the payload from
+        // the weight rows the streaming warp has staged
+        const coll_ref_t r = single_s ? sref : a.refs[u.src0 + it.slot];
+        if (!gemv_piece_mw(a, W, a.ptr.in[r.rank] + in_off, nvec, gpiece++, lane, x)) {
+          failed = true;
+          break;
+        }
         if (tagged && lane < nvec) h = tag_part(x, lane);
       } else if (lane < nvec) {
         const coll_ref_t r = a.refs[u.src0 + it.slot];
@@ -816,7 +1078,7 @@ __global__ void __launch_bounds__(GEMV ? 32 * kGemvWarps : 32, 1) engine_kernel(
     }
     if (stamp && (uint32_t)i < a.stamp_cap) a.stamps[phases ? 4 + 4 * i : i + 1] = globaltimer();
   }
-  if constexpr (GEMV) gemv_release_helpers(lane);
+  if constexpr (GEMV) gemv_finish(lane);
   if (lane == 0) {
     if (n_checks) atomicAdd(&st->spec_checks, (unsigned long long)n_checks);
     if (n_retries) atomicAdd(&st->spec_retries, (unsigned long long)n_retries);
@@ -913,21 +1175,34 @@ static const void *engine_fn(int kind, bool gemv, bool ll) {
 }
 
 cudaError_t engine_max_coresident(int op, int dtype, int protocol, int *max_ctas) {
-  int dev = 0, sms = 0, per_sm = 0, per_sm_g = 0;
+  int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const bool ll = protocol == COLL_PROTO_LL;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, engine_fn(kind_of(op, dtype), false, ll),
-                                                    32, 0);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, engine_fn(kind_of(op, dtype), false, protocol == COLL_PROTO_LL), 32, 0);
   if (e != cudaSuccess) return e;
-  if (!ll) {  // a plan of this protocol may also run the fused-producer variant
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_g, engine_fn(1, true, false),
-                                                      32 * kGemvWarps, 0);
-    if (e != cudaSuccess) return e;
-    if (per_sm_g < per_sm) per_sm = per_sm_g;
-  }
+  *max_ctas = per_sm * sms;
+  return cudaSuccess;
+}
+
+cudaError_t engine_gemv_max_coresident(int *max_ctas) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const void *fn = engine_fn(1, true, false);
+  // the in-kernel register split assumes the launch allocation it was written for
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, fn);
+  if (e != cudaSuccess) return e;
+  if ((uint32_t)fa.numRegs != kGemvLaunchRegs) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kGemvThreads, kGemvSmemBytes);
+  if (e != cudaSuccess) return e;
   *max_ctas = per_sm * sms;
   return cudaSuccess;
 }
@@ -943,9 +1218,14 @@ cudaError_t launch_engine(int op, int dtype, const EngArgs &a, cudaStream_t s) {
   if (a.nwarps == 0 || a.n_epochs == 0) return cudaSuccess;
   void *args[] = {(void *)&a};
   const bool gemv = a.gemv_k != 0;
-  return cudaLaunchCooperativeKernel(
-      engine_fn(kind_of(op, dtype), gemv, a.protocol == COLL_PROTO_LL), dim3(a.nwarps),
-      dim3(gemv ? 32 * kGemvWarps : 32), args, 0, s);
+  const void *fn = engine_fn(kind_of(op, dtype), gemv, a.protocol == COLL_PROTO_LL);
+  if (gemv) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmemBytes);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaLaunchCooperativeKernel(fn, dim3(a.nwarps), dim3(gemv ? kGemvThreads : 32), args,
+                                     gemv ? kGemvSmemBytes : 0, s);
 }
 
 }  // namespace coll

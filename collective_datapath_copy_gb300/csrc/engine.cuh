@@ -79,7 +79,8 @@ cudaError_t launch_zero_copy(int op, int dtype, int oneshot_reuse, const ZcArgs 
 cudaError_t launch_bulk(int op, int dtype, const ZcArgs &a, int ctas, cudaStream_t s);
 uint32_t bulk_smem_bytes(uint32_t stages, uint32_t maxsrc, uint32_t slot_bytes);
 
-// Staged Stage/Notify/Consume engine: one cooperative launch of nwarps one-warp CTAs.
+// Staged Stage/Notify/Consume engine: one cooperative launch of nwarps one-warp CTAs (nine
+// warps each for the fused producer).
 cudaError_t launch_engine(int op, int dtype, const EngArgs &a, cudaStream_t s);
 
 // Flag ping-pong probe between block 0 and block `peer` (cooperative launch).
@@ -88,5 +89,8 @@ cudaError_t launch_probe_rtt(unsigned long long *flags, uint32_t iters, uint32_t
 
 // How many one-warp engine CTAs can be co-resident on the current device.
 cudaError_t engine_max_coresident(int op, int dtype, int protocol, int *max_ctas);
+
+// How many fused-producer engine CTAs (nine warps, a 192 KiB weight ring) can be co-resident.
+cudaError_t engine_gemv_max_coresident(int *max_ctas);
 
 }  // namespace coll

@@ -683,13 +683,84 @@ def test_fused_gemv_with_a_reduce_scatter_naming_and_bad_arguments():
     for r in range(R):
         assert bits_equal(from_dev(outs[r], "bf16"), want[r])
     with pytest.raises(cdc.CollError):
-        plan.run_gemv(dw, dx, 12, outs)  # k not a multiple of 8
+        plan.run_gemv(dw, dx, 12, outs)  # k not a multiple of 64
     zc = cdc.Plan(namings.allreduce(R, n, "bf16"), zero_copy=1)
     with pytest.raises(cdc.CollError):
         zc.run_gemv(dw, dx, k, [torch.empty(n, dtype=torch.int16, device="cuda") for _ in range(R)])
     plan.free()
     zc.free()
 
+
+
+@pytest.mark.parametrize("k,n,wpr", [(64, 4096, 0), (1024, 4096, 0), (512, 4096, 2), (128, 1000, 0),
+                                     (8192, 1024, 0)],
+                         ids=["k64-several-pieces-per-ring-lap", "k1024-ring-wraps-inside-a-piece",
+                              "k512-four-pieces-per-warp", "k128-ragged-last-piece",
+                              "k8192-largest-x"])
+def test_fused_gemv_weight_ring_shapes(k, n, wpr):
+    # The streaming warp fills a 48-slot ring (8 weight rows per slot) ahead of the compute
+    # warps; these shapes cover a ring lap holding several pieces, a piece longer than the
+    # ring, warps with several stage items, and a last piece shorter than 512 bytes.
+    R, pool, E = 4, 2, 6
+    wts, xs = _gemv_case(R, n, k, pool, 99 + k)
+    want = [collectives.allreduce(collectives.gemv_payloads(wts, [xs[r][e] for r in range(R)]),
+                                  "bf16")[0] for e in range(pool)]
+    plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="dual", warps_per_rank=wpr)
+    dw = [to_dev(w.ravel(), "bf16") for w in wts]
+    dx = [torch.stack([to_dev(x, "bf16") for x in xs[r]]).contiguous() for r in range(R)]
+    outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    plan.run_gemv(dw, dx, k, outs, n_epochs=E, x_epoch_stride=2 * k, x_pool=pool,
+                  out_epoch_stride=2 * n)
+    assert plan.status()["code"] == 0
+    for e in range(E):
+        for r in range(R):
+            assert bits_equal(from_dev(outs[r][e], "bf16"), want[e % pool]), (e, r)
+    plan.free()
+
+
+def test_fused_gemv_rejects_a_plan_wider_than_the_gpu_and_keeps_the_plain_run():
+    # 8 ranks x 32 KiB: 512 one-warp engine CTAs fit at once, 512 fused CTAs (one per SM) do not
+    R, n, k = 8, 16384, 64
+    nm = namings.allreduce(R, n, "bf16")
+    plan = cdc.Plan(nm, protocol="dual")
+    assert plan.info.n_warps > torch.cuda.get_device_properties(0).multi_processor_count
+    wts, xs = _gemv_case(R, n, k, 1, 90)
+    dw = [to_dev(w.ravel(), "bf16") for w in wts]
+    dx = [to_dev(x[0], "bf16") for x in xs]
+    outs = [torch.empty(n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    with pytest.raises(cdc.CollError):
+        plan.run_gemv(dw, dx, k, outs)
+    ys = collectives.gemv_payloads(wts, [x[0] for x in xs])
+    plan.run([to_dev(y, "bf16") for y in ys], outs)
+    assert plan.status()["code"] == 0
+    want = collectives.allreduce(ys, "bf16")
+    for r in range(R):
+        assert bits_equal(from_dev(outs[r], "bf16"), want[r])
+    plan.free()
+
+
+def test_fused_gemv_missing_notify_times_out_and_the_gpu_stays_usable():
+    # the engine warp gives up, releases the compute warps and stops the streaming warp,
+    # which waits for the weight copies it issued before the CTA exits
+    R, n, k = 4, 4096, 512
+    wts, xs = _gemv_case(R, n, k, 1, 91)
+    plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="dual", inject="skip_notify",
+                    inject_rank=1, spin_limit_ns=20_000_000)
+    dw = [to_dev(w.ravel(), "bf16") for w in wts]
+    dx = [to_dev(x[0], "bf16") for x in xs]
+    outs = [torch.empty(8, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    plan.run_gemv(dw, dx, k, outs, n_epochs=8, out_epoch_stride=2 * n)
+    st = plan.status()
+    assert st["code"] == cdc._lib.D["COLL_ETIMEDOUT"], st
+    assert st["fail_epoch"] == 1
+    plan.free()
+    ok = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="dual")
+    ok.run_gemv(dw, dx, k, outs, n_epochs=8, out_epoch_stride=2 * n)
+    assert ok.status()["code"] == 0
+    want = collectives.allreduce(collectives.gemv_payloads(wts, [x[0] for x in xs]), "bf16")
+    for r in range(R):
+        assert bits_equal(from_dev(outs[r][7], "bf16"), want[r])
+    ok.free()
 
 
 @pytest.mark.parametrize("cfg", [dict(zero_copy=1), dict(zero_copy=1, datapath="twoshot"),
