@@ -40,7 +40,7 @@ R_DECODE, N_DECODE, POOL, EPOCHS = 8, 4096, 7, 10000
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
 
 
-ENGINE_SOURCES = ["engine.cu", "atom.cuh", "engine.cuh", "coll_internal.h"]
+ENGINE_SOURCES = ["engine.cu", "atom.cuh", "engine.cuh", "coll_internal.h", "tma.cuh"]
 
 
 def sources_sha256(names):
