@@ -8,6 +8,7 @@ protocol) or the zero-copy datapath. The library is required: there is no fallba
 
 from . import namings  # noqa: F401
 from ._lib import CollError, lib  # noqa: F401
-from .namings import (Naming, allgather, allreduce, alltoall, broadcast, gather,  # noqa: F401
-                      moe_combine, moe_dispatch, reduce_scatter, reduce_to_root, scatter, segs)
+from .namings import (Naming, allgather, allreduce, alltoall, alltoallv_from_routing,  # noqa: F401
+                      broadcast, gather, moe_combine, moe_dispatch, reduce_scatter,
+                      reduce_to_root, scatter, segs)
 from .plan import Plan, probe_flag_rtt, validate, validate_code  # noqa: F401

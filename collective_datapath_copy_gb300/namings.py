@@ -121,6 +121,13 @@ def moe_dispatch(routing: np.ndarray, experts_per_rank: int, hidden: int,
                   meta={"counts": counts, "dest": dest})
 
 
+def alltoallv_from_routing(routing: np.ndarray, experts_per_rank: int, hidden: int,
+                           dtype: str = "bf16") -> Naming:
+    """All-to-all with uneven splits derived from a routing table: the same naming as
+    moe_dispatch (one copy of each token row per destination rank)."""
+    return moe_dispatch(routing, experts_per_rank, hidden, dtype)
+
+
 def reduce_to_root(R: int, n: int, dtype: str = "bf16", root: int = 0) -> Naming:
     """Every rank's whole buffer is name 0; only the root's output receives the sum."""
     i = _segs_cols(np.arange(R), np.zeros(R), np.full(R, n), np.zeros(R))

@@ -171,6 +171,8 @@ def test_moe_naming_agrees_with_direct_dispatch():
     rng = synth.seeded_rng(3)
     xs2 = [synth.normal_bf16(rng, (T, H)) for _ in range(R)]
     nm = namings.moe_dispatch(routing, E // R, H)
+    alias = namings.alltoallv_from_routing(routing, E // R, H)
+    assert np.array_equal(alias.out_segs, nm.out_segs) and np.array_equal(alias.in_segs, nm.in_segs)
     outs = _oracle_on(nm, [x.ravel() for x in xs2])
     want, counts = collectives.moe_dispatch(xs2, routing, E // R)
     assert nm.meta["counts"] == counts
