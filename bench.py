@@ -217,6 +217,7 @@ def run_ours(args, rank, world, dist):
         ("spec_relaxed", dict(protocol="spec", spec_check="relaxed")),
         ("spec_literal", dict(protocol="spec", spec_check="literal")),
         ("spec_twoshot", dict(protocol="spec", datapath="twoshot")),
+        ("spec_twoshot_pull", dict(protocol="spec", datapath="twoshot_pull")),
         ("ll", dict(protocol="ll")),
         ("ll_chain", dict(protocol="ll", chain=1)),
         ("spec_chain", dict(protocol="spec", chain=1)),
@@ -245,7 +246,8 @@ def run_ours(args, rank, world, dist):
     # other protocols (same K/W)
     proto = {}
     for name in ("dual", "barrier", "spec_stagger", "spec_relaxed", "spec_literal",
-                 "spec_twoshot", "ll", "ll_chain", "spec_chain", "dual_chain", "barrier_chain"):
+                 "spec_twoshot", "spec_twoshot_pull", "ll", "ll_chain", "spec_chain", "dual_chain",
+                 "barrier_chain"):
         tt = _time_steps(torch, step(name), max(3, args.steps // 2), 1, flush, stream)
         s2 = plans[name].status()
         if s2["code"] != 0:
@@ -540,7 +542,9 @@ def run_workload(args):
                 outs = [torch.empty(E, n, dtype=torch.int16, device=dev) for _ in range(Rr)]
                 nm = cdc.allreduce(Rr, n, "bf16")
                 for proto in ("barrier", "dual", "spec", "ll"):
-                    for dp in ("oneshot", "twoshot"):
+                    for dp in ("oneshot", "twoshot", "twoshot_pull"):
+                        if proto == "ll" and dp == "twoshot_pull":
+                            continue  # tagged data has no flags to pull on
                         pl = cdc.Plan(nm, protocol=proto, datapath=dp)
                         tt = _time_steps(torch, lambda: pl.run(ins, outs, n_epochs=E,
                                                                in_epoch_stride=2 * n, in_pool=7,

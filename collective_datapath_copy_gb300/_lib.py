@@ -39,7 +39,8 @@ DTYPE = {"bf16": D["COLL_BF16"], "f32": D["COLL_F32"], "bytes": D["COLL_BYTES"]}
 ESIZE = {"bf16": 2, "f32": 4, "bytes": 1}
 PROTOCOL = {"barrier": D["COLL_PROTO_BARRIER"], "dual": D["COLL_PROTO_DUAL"],
             "spec": D["COLL_PROTO_SPEC"], "ll": D["COLL_PROTO_LL"]}
-DATAPATH = {"oneshot": D["COLL_DP_ONESHOT"], "twoshot": D["COLL_DP_TWOSHOT"]}
+DATAPATH = {"oneshot": D["COLL_DP_ONESHOT"], "twoshot": D["COLL_DP_TWOSHOT"],
+            "twoshot_pull": D["COLL_DP_TWOSHOT_PULL"]}
 SPEC_CHECK = {"tagged": D["COLL_SPEC_TAGGED"], "literal": D["COLL_SPEC_LITERAL"],
               "relaxed": D["COLL_SPEC_TAGGED_RELAXED"]}
 ORDER = {"rank": D["COLL_ORDER_RANK"], "tree": D["COLL_ORDER_TREE"]}

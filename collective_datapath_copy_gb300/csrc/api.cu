@@ -18,11 +18,14 @@ struct coll_plan_s {
   coll_job_t *d_jobs = nullptr;
   coll_tile_t *d_tiles = nullptr;
   coll_unit_t *d_units = nullptr;
-  coll_item_t *d_sitems = nullptr, *d_citems = nullptr;
+  coll_item_t *d_sitems = nullptr, *d_citems = nullptr, *d_pitems = nullptr;
   coll_warp_t *d_warps = nullptr;
   char *d_xbuf = nullptr;
   unsigned long long *d_pflag = nullptr;
   uint32_t *d_cflag = nullptr;
+  char *d_rbuf = nullptr;      // two-shot pull: reduced pieces [parity][unit]
+  uint32_t *d_rflag = nullptr; // two-shot pull: [parity][unit] epoch of the reduced piece
+  uint32_t *d_dflag = nullptr; // two-shot pull: [n_dflag] epoch each consumer has pulled
   coll_dev_status_t *d_status = nullptr;
   uint64_t *d_stamps = nullptr;
   uint32_t *d_dbg = nullptr;
@@ -60,6 +63,9 @@ void release(coll_plan_s *p) {
   cudaFree(p->d_xbuf);
   cudaFree(p->d_pflag);
   cudaFree(p->d_cflag);
+  cudaFree(p->d_rbuf);
+  cudaFree(p->d_rflag);
+  cudaFree(p->d_dflag);
   cudaFree(p->d_status);
   cudaFree(p->d_stamps);
   cudaFree(p->d_dbg);
@@ -74,6 +80,10 @@ int zero_state(coll_plan_s *p) {
   if (p->d_cflag && cudaMemset(p->d_cflag, 0, (size_t)c.n_cflag * 4) != cudaSuccess)
     return COLL_ECUDA;
   if (p->d_dbg && cudaMemset(p->d_dbg, 0, (size_t)c.units.size() * 4) != cudaSuccess)
+    return COLL_ECUDA;
+  if (p->d_rflag && cudaMemset(p->d_rflag, 0, c.units.size() * 2 * 4) != cudaSuccess)
+    return COLL_ECUDA;
+  if (p->d_dflag && cudaMemset(p->d_dflag, 0, (size_t)c.n_dflag * 4) != cudaSuccess)
     return COLL_ECUDA;
   if (p->d_rank_done && cudaMemset(p->d_rank_done, 0, (size_t)c.R * 4) != cudaSuccess)
     return COLL_ECUDA;
@@ -122,14 +132,15 @@ extern "C" int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_
   }
   const size_t tb = table_bytes(c.refs) + table_bytes(c.jobs) + table_bytes(c.tiles) +
                     table_bytes(c.units) + table_bytes(c.sitems) + table_bytes(c.citems) +
-                    table_bytes(c.warps);
+                    table_bytes(c.pitems) + table_bytes(c.warps);
   std::vector<char> host(tb ? tb : 256, 0);
   size_t off = 0;
   auto put = [&](const auto &v) {
     if (!v.empty()) memcpy(host.data() + off, v.data(), v.size() * sizeof(v[0]));
     off += table_bytes(v);
   };
-  put(c.refs); put(c.jobs); put(c.tiles); put(c.units); put(c.sitems); put(c.citems); put(c.warps);
+  put(c.refs); put(c.jobs); put(c.tiles); put(c.units); put(c.sitems); put(c.citems);
+  put(c.pitems); put(c.warps);
   bool ok = cudaMalloc(&p->d_tables, host.size()) == cudaSuccess &&
             cudaMemcpy(p->d_tables, host.data(), host.size(), cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMalloc(&p->d_status, sizeof(coll_dev_status_t)) == cudaSuccess &&
@@ -142,6 +153,7 @@ extern "C" int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_
     p->d_units = carve(p->d_tables, off, c.units);
     p->d_sitems = carve(p->d_tables, off, c.sitems);
     p->d_citems = carve(p->d_tables, off, c.citems);
+    p->d_pitems = carve(p->d_tables, off, c.pitems);
     p->d_warps = carve(p->d_tables, off, c.warps);
   }
   if (ok && !c.cfg.zero_copy) {
@@ -151,6 +163,10 @@ extern "C" int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_
          (c.n_pflag == 0 || cudaMalloc(&p->d_pflag, (size_t)c.n_pflag * 2 * 8) == cudaSuccess) &&
          (c.n_cflag == 0 || cudaMalloc(&p->d_cflag, (size_t)c.n_cflag * 4) == cudaSuccess);
     if (ok && xb) ok = cudaMemset(p->d_xbuf, 0, xb) == cudaSuccess;
+    if (ok && c.rpar_bytes)
+      ok = cudaMalloc(&p->d_rbuf, (size_t)c.rpar_bytes * (dual ? 2 : 1)) == cudaSuccess &&
+           cudaMalloc(&p->d_rflag, c.units.size() * 2 * 4) == cudaSuccess &&
+           cudaMalloc(&p->d_dflag, (size_t)c.n_dflag * 4) == cudaSuccess;
     if (ok && c.cfg.chain) ok = cudaMalloc(&p->d_rank_done, (size_t)c.R * 4) == cudaSuccess;
     if (ok && (c.cfg.inject_flags & COLL_INJECT_SPEC_PAUSE) && !c.units.empty())
       ok = cudaMalloc(&p->d_dbg, c.units.size() * 4) == cudaSuccess;
@@ -299,6 +315,12 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
     a.xpar = c.xpar_bytes;
     a.pflag = p->d_pflag;
     a.cflag = p->d_cflag;
+    a.pitems = p->d_pitems;
+    a.rbuf = p->d_rbuf;
+    a.rpar = c.rpar_bytes;
+    a.rflag = p->d_rflag;
+    a.dflag = p->d_dflag;
+    a.n_units = (uint32_t)c.units.size();
     a.st = p->d_status;
     a.stamps = p->d_stamps;
     a.dbg = p->d_dbg;

@@ -40,6 +40,7 @@ struct coll_tile_t {
 // those flags and reduces or copies the pieces into its output segment(s).
 #define COLL_UNIT_REUSE_WAIT 1u  // stagers must wait for consumers' done flags (dual/spec)
 #define COLL_UNIT_DONE_FLAGS 2u  // consumers write done flags
+#define COLL_UNIT_PULL 4u        // two-shot pull: the owner writes the reduced piece to rbuf
 struct coll_unit_t {
   uint64_t start;   // byte offset inside the name's segments
   uint64_t xoff;    // byte offset of slot 0 inside one parity of the exchange buffer
@@ -50,7 +51,8 @@ struct coll_unit_t {
   uint32_t cflag0;  // consumer done-flag base
   uint32_t ncflag;  // number of done flags (ndst for oneshot/copy, 1 for twoshot)
   uint32_t flags;   // COLL_UNIT_*
-  uint32_t pad[3];
+  uint32_t dflag0;  // two-shot pull: base of the ndst pulled flags (consumer i read rbuf)
+  uint64_t roff;    // two-shot pull: offset of the reduced piece in one parity of rbuf
 };
 
 #define COLL_SLOT_ALL 0xFFFFFFFFu
@@ -64,7 +66,7 @@ struct coll_warp_t {
   uint32_t s0, s1;  // stage items
   uint32_t c0, c1;  // consume items
   uint32_t rank_warps;  // warps of this rank (chained epochs count them)
-  uint32_t pad[2];
+  uint32_t p0, p1;      // pull items (two-shot pull)
 };
 
 // Device status block of a plan (zeroed at plan time and by coll_reset).
@@ -92,7 +94,7 @@ struct coll_compiled {
   std::vector<coll_job_t> jobs;
   std::vector<coll_tile_t> tiles;
   std::vector<coll_unit_t> units;
-  std::vector<coll_item_t> sitems, citems;
+  std::vector<coll_item_t> sitems, citems, pitems;
   std::vector<coll_warp_t> warps;
   bool zc_keep = false;       // zero-copy: inputs are re-read (one-shot sums with several
                               // consumers per name): keep them cacheable
@@ -101,7 +103,8 @@ struct coll_compiled {
   uint32_t bulk_maxsrc = 0;   // slots per stage
   uint32_t bulk_stages = 0;   // stages in the shared-memory ring
   uint64_t xpar_bytes = 0;  // exchange bytes per parity
-  uint32_t n_pflag = 0, n_cflag = 0;
+  uint64_t rpar_bytes = 0;  // two-shot pull: reduced-piece bytes per parity
+  uint32_t n_pflag = 0, n_cflag = 0, n_dflag = 0;
   uint64_t n_names = 0, min_bytes = 0;
 };
 

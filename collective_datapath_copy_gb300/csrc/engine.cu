@@ -1049,7 +1049,19 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(con
         res = gather_pieces<KIND>(xb, u.nbytes, n, lane, active);
       }
       if (pst && c == W.c0) a.stamps[3 + 4 * i] = globaltimer();
-      if (active) {
+      if (u.flags & COLL_UNIT_PULL) {
+        // two-shot pull: publish the reduced piece in this parity's slot of rbuf, once
+        // every consumer has pulled the piece it held before (the two-shot bottom barrier)
+        const uint32_t target = E - (a.protocol == COLL_PROTO_BARRIER ? 1u : 2u);
+        if (!wait_consumers_done(a.dflag + u.dflag0, u.ndst, target, st, a.spin_ns)) {
+          if (lane == 0) record_timeout(st, (int)W.rank, (int)it.unit, 7, E);
+          failed = true;
+          break;
+        }
+        if (active) st_v4(a.rbuf + (size_t)b * a.rpar + u.roff + lane * 16, res);
+        __syncwarp();
+        if (lane == 0) st_release_u32(a.rflag + (size_t)b * a.n_units + it.unit, E);
+      } else if (active) {
         if (it.slot == COLL_SLOT_ALL) {
           for (uint32_t d = 0; d < u.ndst; ++d) {
             const coll_ref_t r = a.refs[u.dst0 + d];
@@ -1068,7 +1080,30 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(con
           st_release_u32(a.cflag + u.cflag0 + (it.slot == COLL_SLOT_ALL ? 0u : it.slot), E);
       }
     }
-    if (a.chain && a.rank_done && !failed) {
+    if (failed) break;
+
+    // ---------------- Pull (two-shot pull): copy each owner's reduced piece of epoch E
+    for (uint32_t q = W.p0; q < W.p1; ++q) {
+      const coll_item_t it = a.pitems[q];
+      const coll_unit_t u = a.units[it.unit];
+      bool ok = true;
+      if (lane == 0) ok = spin_done(a.rflag + (size_t)b * a.n_units + it.unit, E, st, a.spin_ns);
+      if (!__shfl_sync(FULL, ok, 0)) {
+        if (lane == 0) record_timeout(st, (int)W.rank, (int)it.unit, 8, E);
+        failed = true;
+        break;
+      }
+      __syncwarp();  // lane 0's acquire orders every lane's loads below
+      if (lane < (u.nbytes >> 4)) {
+        const uint4 v = ld_relaxed_v4(a.rbuf + (size_t)b * a.rpar + u.roff + lane * 16);
+        const coll_ref_t r = a.refs[u.dst0 + it.slot];
+        st_v4(a.ptr.out[r.rank] + r.off + out_off + u.start + lane * 16, v);
+      }
+      __syncwarp();
+      if (lane == 0) st_release_u32(a.dflag + u.dflag0 + it.slot, E);  // read: may reuse
+    }
+    if (failed) break;
+    if (a.chain && a.rank_done) {
       __syncwarp();
       if (lane == 0) red_release_add_u32(a.rank_done + W.rank, 1u);
     }

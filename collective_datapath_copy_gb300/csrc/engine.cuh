@@ -45,6 +45,12 @@ struct EngArgs {
   uint64_t xpar;
   unsigned long long *pflag;  // [2][n_pflag]
   uint32_t *cflag;            // [n_cflag]
+  const coll_item_t *pitems;  // two-shot pull: pull items (unit, consumer slot)
+  char *rbuf;                 // two-shot pull: reduced pieces, [parity] x rpar bytes
+  uint64_t rpar;
+  uint32_t *rflag;            // two-shot pull: [2][n_units] epoch of each reduced piece
+  uint32_t *dflag;            // two-shot pull: epoch each consumer has pulled
+  uint32_t n_units;
   coll_dev_status_t *st;
   uint64_t *stamps;           // [stamp_cap + 1] or null
   uint32_t *dbg;              // [n_units] handshake words of the SPEC_PAUSE injection

@@ -48,7 +48,10 @@ extern "C" int coll_config_default(coll_config_t *cfg) {
 
 static int check_config(const coll_config_t &c) {
   if (c.protocol < 0 || c.protocol > 3) return COLL_EINVAL;
-  if (c.datapath < 0 || c.datapath > 1) return COLL_EINVAL;
+  if (c.datapath < 0 || c.datapath > 2) return COLL_EINVAL;
+  // the pull needs the staged exchange buffers; tagged data has no flags to pull on
+  if (c.datapath == COLL_DP_TWOSHOT_PULL && (c.zero_copy || c.protocol == COLL_PROTO_LL))
+    return COLL_EINVAL;
   if (c.zero_copy < 0 || c.zero_copy > 1) return COLL_EINVAL;
   if (c.spec_check < 0 || c.spec_check > 2) return COLL_EINVAL;
   if (c.unit_bytes != 0 && c.unit_bytes != 512) return COLL_EINVAL;
@@ -160,7 +163,8 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
     c.out_bytes[r] = out_len[r] * es;
   }
   const bool sum = op == COLL_OP_SUM;
-  const bool twoshot = sum && cfg.datapath == COLL_DP_TWOSHOT;
+  const bool pull = sum && cfg.datapath == COLL_DP_TWOSHOT_PULL;
+  const bool twoshot = sum && (cfg.datapath == COLL_DP_TWOSHOT || pull);
   c.n_names = names.size();
   for (auto &nm : names) {
     // producers in (rank, offset) order: the fixed summation order
@@ -281,7 +285,7 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
 
   // ---------------- staged: units, items, warps
   const uint32_t U = 512;
-  std::vector<std::vector<coll_item_t>> S(R), C(R);  // per-rank stage / consume items
+  std::vector<std::vector<coll_item_t>> S(R), C(R), P(R);  // per-rank stage / consume / pull
   std::vector<uint32_t> unit_owner;
   for (auto &nm : names) {
     const uint64_t bytes = nm.count * es;
@@ -307,6 +311,13 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
       u.ncflag = twoshot ? 1u : u.ndst;
       u.cflag0 = c.n_cflag;
       c.n_cflag += u.ncflag;
+      if (pull) {
+        u.flags |= COLL_UNIT_PULL;
+        u.roff = c.rpar_bytes;
+        c.rpar_bytes += u.nbytes;
+        u.dflag0 = c.n_dflag;
+        c.n_dflag += u.ndst;
+      }
       const uint32_t ui = (uint32_t)c.units.size();
       c.units.push_back(u);
       for (uint32_t j = 0; j < u.nsrc; ++j)
@@ -314,30 +325,36 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
       if (twoshot) {
         const uint32_t owner = (uint32_t)out_segs[nm.cons[piece % nm.cons.size()]].rank;
         C[owner].push_back(coll_item_t{ui, COLL_SLOT_ALL});
+        if (pull)
+          for (uint32_t i = 0; i < u.ndst; ++i)
+            P[out_segs[nm.cons[i]].rank].push_back(coll_item_t{ui, i});
       } else {
         for (uint32_t i = 0; i < u.ndst; ++i)
           C[out_segs[nm.cons[i]].rank].push_back(coll_item_t{ui, i});
       }
     }
   }
-  if (c.units.size() > 0x7FFFFFF0ull || c.n_pflag > 0x7FFFFFF0u) return COLL_EINVAL;
+  if (c.units.size() > 0x7FFFFFF0ull || c.n_pflag > 0x7FFFFFF0u || c.n_dflag > 0x7FFFFFF0u)
+    return COLL_EINVAL;
   // warps: rank r gets W_r warps; item k of its stage (consume) list goes to warp k % W_r.
   // Every warp must be co-resident (they wait on each other), so the total is capped.
   std::vector<uint32_t> wbase(R + 1, 0);
   const uint32_t cap_r = std::max<uint32_t>(1u, (uint32_t)(max_warps > 0 ? max_warps : 1024) / (uint32_t)R);
   for (int r = 0; r < R; ++r) {
-    uint32_t need = (uint32_t)std::max(S[r].size(), C[r].size());
+    uint32_t need = (uint32_t)std::max(std::max(S[r].size(), C[r].size()), P[r].size());
     uint32_t Wr = cfg.warps_per_rank ? std::min<uint32_t>(need, (uint32_t)cfg.warps_per_rank) : need;
     Wr = std::min(Wr, cap_r);
     wbase[r + 1] = wbase[r] + Wr;
   }
   const uint32_t nwarps = wbase[R];
   c.warps.resize(nwarps);
-  std::vector<std::vector<uint32_t>> stage_of_warp(nwarps), cons_of_warp(nwarps);
+  std::vector<std::vector<uint32_t>> stage_of_warp(nwarps), cons_of_warp(nwarps),
+      pull_of_warp(nwarps);
   for (int r = 0; r < R; ++r) {
     const uint32_t Wr = wbase[r + 1] - wbase[r];
     for (size_t k = 0; k < S[r].size(); ++k) stage_of_warp[wbase[r] + k % Wr].push_back((uint32_t)k);
     for (size_t k = 0; k < C[r].size(); ++k) cons_of_warp[wbase[r] + k % Wr].push_back((uint32_t)k);
+    for (size_t k = 0; k < P[r].size(); ++k) pull_of_warp[wbase[r] + k % Wr].push_back((uint32_t)k);
   }
   // which warp stages / consumes each unit slot
   std::vector<std::vector<uint32_t>> stagers(c.units.size()), consumers(c.units.size());
@@ -360,6 +377,9 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
         consumers[C[r][k].unit].push_back(w);
       }
       W.c1 = (uint32_t)c.citems.size();
+      W.p0 = (uint32_t)c.pitems.size();
+      for (uint32_t k : pull_of_warp[w]) c.pitems.push_back(P[r][k]);
+      W.p1 = (uint32_t)c.pitems.size();
     }
   }
   // Dual buffers: restaging unit u (parity of epoch e) overwrites what u's consumers read
@@ -401,8 +421,11 @@ void coll_fill_info(const coll_compiled &c, coll_plan_info_t *info) {
   info->n_warps = c.warps.size();
   info->min_bytes = c.min_bytes;
   const bool dual = c.cfg.protocol != COLL_PROTO_BARRIER;
-  info->xbuf_bytes = c.cfg.zero_copy ? 0 : c.xpar_bytes * (dual ? 2 : 1);
-  info->flag_bytes = c.cfg.zero_copy ? 0 : (uint64_t)c.n_pflag * 2 * 8 + (uint64_t)c.n_cflag * 4;
+  info->xbuf_bytes = c.cfg.zero_copy ? 0 : (c.xpar_bytes + c.rpar_bytes) * (dual ? 2 : 1);
+  info->flag_bytes = c.cfg.zero_copy ? 0
+                                     : (uint64_t)c.n_pflag * 2 * 8 + (uint64_t)c.n_cflag * 4 +
+                                           (uint64_t)c.units.size() * (c.rpar_bytes ? 2 * 4 : 0) +
+                                           (uint64_t)c.n_dflag * 4;
 }
 
 extern "C" int coll_validate(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_in,

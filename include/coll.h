@@ -73,9 +73,15 @@ extern "C" {
 
 /* Datapaths for sum. Source: SiFAR review, Fig. 5 (oneshot: every consumer reduces the
  * whole payload from every producer) and Fig. 6 (twoshot: each part is reduced once, by an
- * owner, and then delivered to every consumer — here the owner writes it to all of them). */
+ * owner, and then delivered to every consumer). TWOSHOT: the owner writes the reduced part
+ * to every consumer (push). TWOSHOT_PULL (staged plans only, not with COLL_PROTO_LL): the
+ * owner writes it to a second exchange buffer and notifies; every consumer waits for that
+ * flag and copies the part into its output (the all-gather pull of the pages), then signals
+ * that it has read it; the owner waits for those signals before it overwrites the buffer
+ * (the two-shot bottom barrier). Same result bits as ONESHOT and TWOSHOT. */
 #define COLL_DP_ONESHOT 0
 #define COLL_DP_TWOSHOT 1
+#define COLL_DP_TWOSHOT_PULL 2
 
 /* Summation order of sums (zero-copy plans). RANK is the fixed rank order and is
  * bit-exact; TREE adds each group of up to 8 producers pairwise ((x0+x1)+(x2+x3))+...,

@@ -114,6 +114,27 @@ def test_bad_config_rejected():
         cdc.validate(n, protocol=7)
     with pytest.raises(cdc.CollError):
         cdc.validate(n, unit_bytes=100)
+    with pytest.raises(cdc.CollError):
+        cdc.validate(n, datapath=3)
+    # the two-shot pull needs the staged exchange and flags
+    with pytest.raises(cdc.CollError):
+        cdc.validate(n, datapath="twoshot_pull", zero_copy=1)
+    with pytest.raises(cdc.CollError):
+        cdc.validate(n, datapath="twoshot_pull", protocol="ll")
+
+
+def test_twoshot_pull_plan_shape():
+    # 8 ranks x 4096 bf16: 16 units; each owner reduces 2 of them into the second exchange
+    # buffer, and every rank pulls all 16: 16 pull items per rank, on 16 warps per rank
+    nm = namings.allreduce(8, 4096, "bf16")
+    push = cdc.validate(nm, protocol="dual", datapath="twoshot")
+    pull = cdc.validate(nm, protocol="dual", datapath="twoshot_pull")
+    assert pull.n_units == push.n_units == 16
+    assert pull.n_warps == 128
+    assert pull.xbuf_bytes == push.xbuf_bytes + 2 * 8192  # + reduced pieces, two parities
+    assert pull.flag_bytes == push.flag_bytes + 16 * 2 * 4 + 16 * 8 * 4
+    barrier = cdc.validate(nm, protocol="barrier", datapath="twoshot_pull")
+    assert barrier.xbuf_bytes == 8 * 8192 + 8192
 
 
 M = 1 << 20

@@ -70,6 +70,8 @@ DATAPATHS = [
     dict(protocol="spec"),
     dict(protocol="spec", datapath="twoshot"),
     dict(protocol="barrier", datapath="twoshot"),
+    dict(protocol="spec", datapath="twoshot_pull"),
+    dict(protocol="barrier", datapath="twoshot_pull"),
 ]
 
 
@@ -151,7 +153,10 @@ def test_random_namings_staged(seed, protocol):
     o = [(r, off * k, c * k, nmv) for (r, off, c, nmv) in o]
     nm = namings.Naming(R, op, dtype, il, namings.segs(i), ol, namings.segs(o))
     xs = [gen("normal", rng, n, dtype) for n in il]
-    got, init = run_once(nm, xs, protocol=protocol, datapath="twoshot" if seed % 2 else "oneshot")
+    dp = ["oneshot", "twoshot", "twoshot_pull"][seed % 3]
+    if protocol == "ll" and dp == "twoshot_pull":
+        dp = "twoshot"
+    got, init = run_once(nm, xs, protocol=protocol, datapath=dp)
     want = oracle_outputs(nm, xs, init)
     for g, w in zip(got, want):
         assert bits_equal(g, w)
@@ -239,12 +244,16 @@ def _check_epochs(outs, expect_dev, n_epochs, pool):
 
 
 @pytest.mark.parametrize("protocol", ["barrier", "dual", "spec", "ll"])
-@pytest.mark.parametrize("datapath", ["oneshot", "twoshot"])
+@pytest.mark.parametrize("datapath", ["oneshot", "twoshot", "twoshot_pull"])
 @pytest.mark.parametrize("chain", [0, 1])
 def test_decode_allreduce_epochs_bit_exact(protocol, datapath, chain):
     R, n, pool, E = 8, 4096, 7, 2000
     ins, expect = _decode_case(R, n, pool)
     nm = namings.allreduce(R, n, "bf16")
+    if protocol == "ll" and datapath == "twoshot_pull":
+        with pytest.raises(cdc.CollError):  # tagged data has no flags to pull on
+            cdc.Plan(nm, protocol=protocol, datapath=datapath, chain=chain)
+        return
     plan = cdc.Plan(nm, protocol=protocol, datapath=datapath, chain=chain)
     outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
     plan.run(ins, outs, n_epochs=E, in_epoch_stride=n * 2, in_pool=pool, out_epoch_stride=n * 2)
@@ -284,7 +293,12 @@ def test_decode_allreduce_10000_epochs_spec_equals_barrier_under_stagger():
                                           inject_start_ns=5000)),
                       ("spec-twoshot-stagger", dict(protocol="spec", datapath="twoshot",
                                                     inject="stagger", inject_seed=4,
-                                                    inject_prob_ppm=100000, inject_max_ns=20000))]:
+                                                    inject_prob_ppm=100000, inject_max_ns=20000)),
+                      ("dual-pull-stagger", dict(protocol="dual", datapath="twoshot_pull",
+                                                 inject="stagger", inject_seed=6,
+                                                 inject_prob_ppm=100000, inject_max_ns=20000,
+                                                 inject_start_ns=5000)),
+                      ("spec-pull", dict(protocol="spec", datapath="twoshot_pull"))]:
         plan = cdc.Plan(nm, **cfg)
         outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
         plan.run(ins, outs, n_epochs=E, in_epoch_stride=n * 2, in_pool=pool,
@@ -329,13 +343,14 @@ def test_speculation_with_adversarial_pause_tagged_is_exact_literal_is_not():
     assert bad["literal"][0] > 0
 
 
-@pytest.mark.parametrize("protocol", ["dual", "ll"])
-def test_missing_notify_times_out_and_the_gpu_stays_usable(protocol):
+@pytest.mark.parametrize("protocol,datapath", [("dual", "oneshot"), ("ll", "oneshot"),
+                                               ("dual", "twoshot_pull")])
+def test_missing_notify_times_out_and_the_gpu_stays_usable(protocol, datapath):
     R, n = 4, 1024
     rng = synth.seeded_rng(5)
     xs = [synth.normal_bf16(rng, n) for _ in range(R)]
     nm = namings.allreduce(R, n, "bf16")
-    plan = cdc.Plan(nm, protocol=protocol, inject="skip_notify", inject_rank=1,
+    plan = cdc.Plan(nm, protocol=protocol, datapath=datapath, inject="skip_notify", inject_rank=1,
                     spin_limit_ns=20_000_000)
     ins = [to_dev(x, "bf16") for x in xs]
     outs = [empty_dev(n, "bf16") for _ in range(R)]
@@ -598,9 +613,11 @@ def test_moe_combine(T, H, mode):
 @pytest.mark.parametrize("R", [2, 4, 8])
 @pytest.mark.parametrize("kb", [8, 16, 32])
 @pytest.mark.parametrize("protocol", ["barrier", "dual", "spec", "ll"])
-@pytest.mark.parametrize("datapath", ["oneshot", "twoshot"])
+@pytest.mark.parametrize("datapath", ["oneshot", "twoshot", "twoshot_pull"])
 def test_fig15_cells_bit_exact(R, kb, protocol, datapath):
     # SiFAR's Fig. 15 grid: TP degree 2/4/8 x 8/16/32 KB payloads, every protocol
+    if protocol == "ll" and datapath == "twoshot_pull":
+        pytest.skip("tagged data has no flags to pull on (rejected at plan time)")
     n = kb * 1024 // 2
     pool, E = 5, 300
     ins, expect = _decode_case(R, n, pool, seed=15)
@@ -649,7 +666,8 @@ def _gemv_case(R, n, k, pool, seed):
 
 @pytest.mark.parametrize("protocol,datapath,chain", [("barrier", "oneshot", 0), ("dual", "oneshot", 0),
                                                      ("spec", "oneshot", 0), ("spec", "twoshot", 0),
-                                                     ("spec", "oneshot", 1)])
+                                                     ("spec", "oneshot", 1),
+                                                     ("dual", "twoshot_pull", 1)])
 def test_fused_gemv_allreduce_bit_exact(protocol, datapath, chain):
     R, n, k, pool, E = 8, 4096, 256, 3, 24
     wts, xs = _gemv_case(R, n, k, pool, 97)
