@@ -113,7 +113,8 @@ extern "C" int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_
   int max_ctas = coll_default_max_warps();
   const int eop = (op == COLL_OP_SUM) ? COLL_OP_SUM : COLL_OP_COPY;
   const int eproto = cfg ? cfg->protocol : COLL_PROTO_SPEC;
-  if (coll::engine_max_coresident(eop, dtype == COLL_F32 ? COLL_F32 : COLL_BF16, eproto,
+  const int edp = cfg ? cfg->datapath : COLL_DP_ONESHOT;
+  if (coll::engine_max_coresident(eop, dtype == COLL_F32 ? COLL_F32 : COLL_BF16, eproto, edp,
                                   &max_ctas) !=
       cudaSuccess) {
     delete p;
@@ -213,7 +214,8 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
       if (((uintptr_t)wt[r] & 15u) || (c.in_bytes[r] & 15u)) return COLL_EALIGN;
     }
     // the fused CTAs are larger (nine warps and a shared-memory ring): all must still fit
-    if (p->gemv_cap < 0 && coll::engine_gemv_max_coresident(&p->gemv_cap) != cudaSuccess) {
+    if (p->gemv_cap < 0 &&
+        coll::engine_gemv_max_coresident(c.rpar_bytes != 0, &p->gemv_cap) != cudaSuccess) {
       cudaGetLastError();
       p->gemv_cap = -1;
       return COLL_ECUDA;

@@ -683,7 +683,9 @@ __device__ __forceinline__ uint4 spec_attempt(const char *xb, uint32_t nbytes, u
   return active ? acc.pack() : make_uint4(0, 0, 0, 0);
 }
 
-template <int KIND, bool GEMV, bool LL>
+// KIND: 0 copy, 1 sum of bf16, 2 sum of f32. GEMV: fused producer. LL: tagged data.
+// PULL: two-shot pull plans (the publish/pull steps are compiled only into this variant).
+template <int KIND, bool GEMV, bool LL, bool PULL>
 __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(const EngArgs a) {
   const uint32_t gw = blockIdx.x;
   const uint32_t lane = threadIdx.x & 31u;
@@ -1049,7 +1051,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(con
         res = gather_pieces<KIND>(xb, u.nbytes, n, lane, active);
       }
       if (pst && c == W.c0) a.stamps[3 + 4 * i] = globaltimer();
-      if (u.flags & COLL_UNIT_PULL) {
+      if (PULL && (u.flags & COLL_UNIT_PULL)) {
         // two-shot pull: publish the reduced piece in this parity's slot of rbuf, once
         // every consumer has pulled the piece it held before (the two-shot bottom barrier)
         const uint32_t target = E - (a.protocol == COLL_PROTO_BARRIER ? 1u : 2u);
@@ -1083,7 +1085,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(con
     if (failed) break;
 
     // ---------------- Pull (two-shot pull): copy each owner's reduced piece of epoch E
-    for (uint32_t q = W.p0; q < W.p1; ++q) {
+    for (uint32_t q = W.p0; PULL && q < W.p1; ++q) {
       const coll_item_t it = a.pitems[q];
       const coll_unit_t u = a.units[it.unit];
       bool ok = true;
@@ -1193,42 +1195,49 @@ cudaError_t launch_zero_copy(int op, int dtype, int keep, const ZcArgs &a, int c
   return cudaGetLastError();
 }
 
-static const void *engine_fn(int kind, bool gemv, bool ll) {
-  if (gemv) return (const void *)engine_kernel<1, true, false>;
+static const void *engine_fn(int kind, bool gemv, bool ll, bool pull) {
+  if (gemv) return pull ? (const void *)engine_kernel<1, true, false, true>
+                        : (const void *)engine_kernel<1, true, false, false>;
   if (ll) {
     switch (kind) {
-      case 0: return (const void *)engine_kernel<0, false, true>;
-      case 1: return (const void *)engine_kernel<1, false, true>;
-      default: return (const void *)engine_kernel<2, false, true>;
+      case 0: return (const void *)engine_kernel<0, false, true, false>;
+      case 1: return (const void *)engine_kernel<1, false, true, false>;
+      default: return (const void *)engine_kernel<2, false, true, false>;
     }
   }
+  if (pull && kind != 0)  // (pull plans are sums)
+    return kind == 1 ? (const void *)engine_kernel<1, false, false, true>
+                     : (const void *)engine_kernel<2, false, false, true>;
   switch (kind) {
-    case 0: return (const void *)engine_kernel<0, false, false>;
-    case 1: return (const void *)engine_kernel<1, false, false>;
-    default: return (const void *)engine_kernel<2, false, false>;
+    case 0: return (const void *)engine_kernel<0, false, false, false>;
+    case 1: return (const void *)engine_kernel<1, false, false, false>;
+    default: return (const void *)engine_kernel<2, false, false, false>;
   }
 }
 
-cudaError_t engine_max_coresident(int op, int dtype, int protocol, int *max_ctas) {
+cudaError_t engine_max_coresident(int op, int dtype, int protocol, int datapath, int *max_ctas) {
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, engine_fn(kind_of(op, dtype), false, protocol == COLL_PROTO_LL), 32, 0);
+      &per_sm,
+      engine_fn(kind_of(op, dtype), false, protocol == COLL_PROTO_LL,
+                datapath == COLL_DP_TWOSHOT_PULL),
+      32, 0);
   if (e != cudaSuccess) return e;
   *max_ctas = per_sm * sms;
   return cudaSuccess;
 }
 
-cudaError_t engine_gemv_max_coresident(int *max_ctas) {
+cudaError_t engine_gemv_max_coresident(bool pull, int *max_ctas) {
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const void *fn = engine_fn(1, true, false);
+  const void *fn = engine_fn(1, true, false, pull);
   // the in-kernel register split assumes the launch allocation it was written for
   cudaFuncAttributes fa;
   e = cudaFuncGetAttributes(&fa, fn);
@@ -1253,7 +1262,7 @@ cudaError_t launch_engine(int op, int dtype, const EngArgs &a, cudaStream_t s) {
   if (a.nwarps == 0 || a.n_epochs == 0) return cudaSuccess;
   void *args[] = {(void *)&a};
   const bool gemv = a.gemv_k != 0;
-  const void *fn = engine_fn(kind_of(op, dtype), gemv, a.protocol == COLL_PROTO_LL);
+  const void *fn = engine_fn(kind_of(op, dtype), gemv, a.protocol == COLL_PROTO_LL, a.rpar != 0);
   if (gemv) {
     const cudaError_t e =
         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmemBytes);

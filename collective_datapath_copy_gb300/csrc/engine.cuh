@@ -94,9 +94,9 @@ cudaError_t launch_probe_rtt(unsigned long long *flags, uint32_t iters, uint32_t
                              unsigned long long *out, uint64_t limit, cudaStream_t s);
 
 // How many one-warp engine CTAs can be co-resident on the current device.
-cudaError_t engine_max_coresident(int op, int dtype, int protocol, int *max_ctas);
+cudaError_t engine_max_coresident(int op, int dtype, int protocol, int datapath, int *max_ctas);
 
 // How many fused-producer engine CTAs (nine warps, a 192 KiB weight ring) can be co-resident.
-cudaError_t engine_gemv_max_coresident(int *max_ctas);
+cudaError_t engine_gemv_max_coresident(bool pull, int *max_ctas);
 
 }  // namespace coll
