@@ -374,6 +374,7 @@ def run_ours(args, rank, world, dist):
     }
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(pool_np, seconds=args.cpu_seconds)
+        res["cpu_baseline_all_cores"] = cpu_baseline_all_cores(seconds=args.cpu_seconds / 2)
     return res
 
 
@@ -394,6 +395,46 @@ def cpu_baseline(pool_np, seconds=10.0):
     dt = time.perf_counter() - t0
     return {"value": round(dt / n * 1e6, 3), "unit": "us/epoch", "cores": 1, "kind": "oracle",
             "sample": f"{n} epochs of the 8 x 4096 bf16 all-reduce (numpy, one thread)"}
+
+
+def _oracle_worker(seconds):
+    """One host process of the all-cores oracle timing: the same oracle loop as above."""
+    from oracle import collectives
+    rng = synth.seeded_rng(2)
+    pool_np = [[synth.normal_bf16(rng, N_DECODE) for _ in range(R_DECODE)] for _ in range(POOL)]
+    collectives.allreduce(pool_np[0], "bf16")  # warm
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        collectives.allreduce(pool_np[n % POOL], "bf16")
+        n += 1
+        if n % 20 == 0 and time.perf_counter() - t0 > seconds:
+            break
+    return n, time.perf_counter() - t0
+
+
+def cpu_baseline_all_cores(seconds=5.0):
+    """The same oracle run as independent epochs in one spawned process per allowed host
+    core (the oracle is single-threaded numpy); aggregate epochs per second of all of them."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    env_keep = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS")}
+    os.environ["OMP_NUM_THREADS"] = os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    try:
+        with mp.get_context("spawn").Pool(cores) as p:
+            res = p.map(_oracle_worker, [seconds] * cores)
+    finally:
+        for k, v in env_keep.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    total = sum(n for n, _ in res)
+    window = max(dt for _, dt in res)
+    return {"value": round(window / total * 1e6, 3), "unit": "us/epoch", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{total} epochs of the 8 x 4096 bf16 all-reduce in {cores} processes "
+                      f"(numpy, one thread each), {window:.1f} s"}
 
 
 def run_reference(args):
