@@ -218,34 +218,112 @@ __device__ __forceinline__ void tree8(Vec16Acc<DT> &acc, bool first, const uint4
 // ------------------------------------------------------------------ content tag
 
 // Full-avalanche 32-bit mixer (two multiply / xor-shift rounds).
+constexpr uint32_t kFmixK1 = 0x7FEB352Du, kFmixK2 = 0x846CA68Bu;
+constexpr uint32_t kTagSalt = 0x9E3779B9u;
+constexpr uint32_t kTagOff1 = 0x632BE5ABu, kTagOff2 = 0x165667B1u, kTagOff3 = 0xD3A2646Cu;
+constexpr uint32_t kTagMulX = 0x85EBCA77u, kTagMulY = 0xC2B2AE3Du, kTagMulZ = 0x27D4EB2Fu,
+                   kTagMulW = 0x9E3779B1u, kTagMulB = 0xA54FF53Bu;
+
 __device__ __forceinline__ uint32_t fmix(uint32_t x) {
   x ^= x >> 16;
-  x *= 0x7FEB352Du;
+  x *= kFmixK1;
   x ^= x >> 15;
-  x *= 0x846CA68Bu;
+  x *= kFmixK2;
   x ^= x >> 16;
   return x;
 }
 
-// Contribution of vector `vi` (its index inside the piece) to the piece's tag: each word is
-// salted by its position and multiplied by an odd constant (a bijection), the four products
-// are rotated apart and combined, and one full-avalanche round per vector follows, so that
-// the sum over vectors (lanes may be reduced in any order) changes with any change of the
-// bytes except with probability about 2^-32.
-__device__ __forceinline__ uint32_t tag_part(uint4 v, uint32_t vi) {
-  const uint32_t s = vi * 0x9E3779B9u;
-  const uint32_t a = (v.x ^ s) * 0x85EBCA77u;
-  const uint32_t b = (v.y ^ (s + 0x632BE5ABu)) * 0xC2B2AE3Du;
-  const uint32_t c = (v.z ^ (s + 0x165667B1u)) * 0x27D4EB2Fu;
-  const uint32_t d = (v.w ^ (s + 0xD3A2646Cu)) * 0x9E3779B1u;
-  return fmix(a ^ __funnelshift_l(b, b, 8) ^ __funnelshift_l(c, c, 16) ^
-              __funnelshift_l(d, d, 24));
+// Contribution of vector `vi` (its index inside the piece) to the piece's two tags. Each
+// word is salted by its position and multiplied by an odd constant (a bijection); tag A
+// combines the four products with rotations and XOR and runs a full-avalanche round, tag B
+// combines them with other rotations and additions and runs its own mixing round. The sums
+// over vectors (lanes may be reduced in any order) then change with any change of the bytes
+// except with probability about 2^-32 for tag A (which also catches structured changes such
+// as two flipped sign bits) and 2^-48 for tag A with the 16 bits of tag B a flag keeps.
+__device__ __forceinline__ uint2 tag_part(uint4 v, uint32_t vi) {
+  const uint32_t s = vi * kTagSalt;
+  const uint32_t a = (v.x ^ s) * kTagMulX;
+  const uint32_t b = (v.y ^ (s + kTagOff1)) * kTagMulY;
+  const uint32_t c = (v.z ^ (s + kTagOff2)) * kTagMulZ;
+  const uint32_t d = (v.w ^ (s + kTagOff3)) * kTagMulW;
+  const uint32_t ta = fmix(a ^ __funnelshift_l(b, b, 8) ^ __funnelshift_l(c, c, 16) ^
+                           __funnelshift_l(d, d, 24));
+  uint32_t tb = a + __funnelshift_l(b, b, 13) + __funnelshift_l(c, c, 7) +
+                __funnelshift_l(d, d, 21);
+  tb ^= tb >> 16;
+  tb *= kTagMulB;
+  tb ^= tb >> 13;
+  return make_uint2(ta, tb);
+}
+
+// The sums of tag_part(v[k], vi) over k < kn, the same values, computed stage by stage: the
+// eight vectors' independent dependency chains then interleave on the one warp that
+// validates a piece (computed one after the other they cost about twice as long).
+__device__ __forceinline__ uint2 tag_parts8(const uint4 v[8], uint32_t kn, uint32_t vi) {
+  const uint32_t s = vi * kTagSalt;
+  uint32_t t[8], u[8];
+#pragma unroll
+  for (uint32_t k = 0; k < 8; ++k) {
+    t[k] = (v[k].x ^ s) * kTagMulX;
+    u[k] = t[k];
+  }
+#pragma unroll
+  for (uint32_t k = 0; k < 8; ++k) {
+    const uint32_t b = (v[k].y ^ (s + kTagOff1)) * kTagMulY;
+    t[k] ^= __funnelshift_l(b, b, 8);
+    u[k] += __funnelshift_l(b, b, 13);
+  }
+#pragma unroll
+  for (uint32_t k = 0; k < 8; ++k) {
+    const uint32_t c = (v[k].z ^ (s + kTagOff2)) * kTagMulZ;
+    t[k] ^= __funnelshift_l(c, c, 16);
+    u[k] += __funnelshift_l(c, c, 7);
+  }
+#pragma unroll
+  for (uint32_t k = 0; k < 8; ++k) {
+    const uint32_t d = (v[k].w ^ (s + kTagOff3)) * kTagMulW;
+    t[k] ^= __funnelshift_l(d, d, 24);
+    u[k] += __funnelshift_l(d, d, 21);
+  }
+#pragma unroll
+  for (uint32_t k = 0; k < 8; ++k) {
+    t[k] ^= t[k] >> 16;
+    u[k] ^= u[k] >> 16;
+  }
+#pragma unroll
+  for (uint32_t k = 0; k < 8; ++k) {
+    t[k] *= kFmixK1;
+    u[k] *= kTagMulB;
+  }
+#pragma unroll
+  for (uint32_t k = 0; k < 8; ++k) {
+    t[k] ^= t[k] >> 15;
+    u[k] ^= u[k] >> 13;
+  }
+#pragma unroll
+  for (uint32_t k = 0; k < 8; ++k) t[k] *= kFmixK2;
+#pragma unroll
+  for (uint32_t k = 0; k < 8; ++k) t[k] ^= t[k] >> 16;
+  uint2 h = make_uint2(0u, 0u);
+#pragma unroll
+  for (uint32_t k = 0; k < 8; ++k)
+    if (k < kn) {
+      h.x += t[k];
+      h.y += u[k];
+    }
+  return h;
 }
 
 // A piece's tag: its hash plus the epoch times an odd constant (linear, so that tags of
 // several producers can be checked as one sum).
 __device__ __forceinline__ uint32_t tag_fold(uint32_t h, uint32_t epoch) {
   return h + epoch * 0x85EBCA6Bu;
+}
+__device__ __forceinline__ uint32_t tag_fold_b(uint32_t h, uint32_t epoch) {
+  return h + epoch * 0xC2B2AE35u;
+}
+__device__ __forceinline__ uint2 reduce_add2(uint2 h) {
+  return make_uint2(__reduce_add_sync(0xFFFFFFFFu, h.x), __reduce_add_sync(0xFFFFFFFFu, h.y));
 }
 
 }  // namespace coll

@@ -232,6 +232,18 @@ __device__ void record_timeout(coll_dev_status_t *st, int rank, int unit, int wh
   st_relaxed_u32(&st->abort, 1u);
 }
 
+// A producer slot's flag word: {epoch mod 2^16 : 16 | tag B mod 2^16 : 16 | tag A : 32},
+// written with one 64-bit store. Flags of one slot only ever hold E or an epoch one or two
+// before it, so 16 bits of epoch tell them apart across any wrap.
+__device__ __forceinline__ unsigned long long flag_word(uint32_t E, uint32_t ta, uint32_t tb) {
+  return ((unsigned long long)(E & 0xFFFFu) << 48) | ((unsigned long long)(tb & 0xFFFFu) << 32) |
+         ta;
+}
+__device__ __forceinline__ uint32_t flag_epoch(unsigned long long f) { return (uint32_t)(f >> 48); }
+__device__ __forceinline__ bool flag_is(unsigned long long f, uint32_t E) {
+  return flag_epoch(f) == (E & 0xFFFFu);
+}
+
 // Wait (all lanes cooperating) until every producer flag of a unit carries epoch E.
 __device__ __forceinline__ bool wait_producers(const unsigned long long *pf, uint32_t n,
                                                uint32_t E, const coll_dev_status_t *st,
@@ -239,7 +251,7 @@ __device__ __forceinline__ bool wait_producers(const unsigned long long *pf, uin
   const uint32_t lane = threadIdx.x & 31u;
   bool ok = true;
   for (uint32_t j = lane; j < n; j += 32)
-    ok = ok && spin_u64(pf + j, [E](unsigned long long v) { return (uint32_t)(v >> 32) == E; },
+    ok = ok && spin_u64(pf + j, [E](unsigned long long v) { return flag_is(v, E); },
                         st, limit);
   return __all_sync(FULL, ok);
 }
@@ -633,16 +645,19 @@ __device__ __forceinline__ void gemv_finish(uint32_t lane) {
   }
 }
 
-// Validation of a speculative load: lane j < n holds producer j's flag word {epoch, tag}
-// and every lane holds its share of the hash of what it loaded. Passes iff every producer
-// notified epoch E and the producers' tags (hash + E*K each) add up to the loaded hash plus
-// n*E*K, i.e. the loaded bytes are the notified bytes (up to a 2^-32 collision).
-__device__ __forceinline__ bool tags_match(unsigned long long f, uint32_t myh, uint32_t n,
+// Validation of a speculative load: lane j < n holds producer j's flag word and every lane
+// holds its share of the two hashes of what it loaded. Passes iff every flag shows epoch E
+// and, for each tag, the producers' tags (hash + E*K each) add up to the loaded hash plus
+// n*E*K (tag A modulo 2^32, tag B modulo 2^16), i.e. the loaded bytes are the notified
+// bytes up to a 48-bit collision.
+__device__ __forceinline__ bool tags_match(unsigned long long f, uint2 myh, uint32_t n,
                                            uint32_t E, uint32_t lane) {
-  const uint32_t ftag = __reduce_add_sync(FULL, lane < n ? (uint32_t)f : 0u);
-  const uint32_t htot = __reduce_add_sync(FULL, myh);
-  const bool epochs = __all_sync(FULL, lane >= n || (uint32_t)(f >> 32) == E);
-  return epochs && ftag == htot + n * tag_fold(0u, E);
+  const uint32_t fta = __reduce_add_sync(FULL, lane < n ? (uint32_t)f : 0u);
+  const uint32_t ftb = __reduce_add_sync(FULL, lane < n ? (uint32_t)(f >> 32) & 0xFFFFu : 0u);
+  const uint2 h = reduce_add2(myh);
+  const bool epochs = __all_sync(FULL, lane >= n || flag_is(f, E));
+  return epochs && fta == h.x + n * tag_fold(0u, E) &&
+         ((ftb - (h.y + n * tag_fold_b(0u, E))) & 0xFFFFu) == 0u;
 }
 
 // If `side` is set, the warp also hashes `side_v` (the prefetched next input piece, lanes
@@ -652,20 +667,21 @@ __device__ __forceinline__ uint4 spec_attempt(const char *xb, uint32_t nbytes, u
                                               uint32_t lane, bool active, bool want_hash,
                                               const unsigned long long *pf, bool acquire_flags,
                                               bool load_flags, unsigned long long &f,
-                                              uint32_t &myh, bool side, uint4 side_v,
-                                              uint32_t side_nvec, uint32_t &side_h) {
+                                              uint2 &myh, bool side, uint4 side_v,
+                                              uint32_t side_nvec, uint2 &side_h) {
   typename EngAcc<KIND>::type acc;
-  myh = 0;
+  myh = make_uint2(0u, 0u);
   for (uint32_t k0 = 0; k0 < n; k0 += 8) {
     uint4 x[8];
     const uint32_t kn = n - k0 < 8 ? n - k0 : 8;
 #pragma unroll
     for (uint32_t k = 0; k < 8; ++k)
-      if (k < kn && active) x[k] = ld_relaxed_v4(xb + (size_t)(k0 + k) * nbytes + lane * 16);
+      x[k] = (k < kn && active) ? ld_relaxed_v4(xb + (size_t)(k0 + k) * nbytes + lane * 16)
+                                : make_uint4(0, 0, 0, 0);
     if (k0 == 0 && load_flags && lane < n)
       f = acquire_flags ? ld_acquire_u64(pf + lane) : ld_relaxed_u64(pf + lane);
     if (k0 == 0 && side)
-      side_h = __reduce_add_sync(FULL, lane < side_nvec ? tag_part(side_v, lane) : 0u);
+      side_h = reduce_add2(lane < side_nvec ? tag_part(side_v, lane) : make_uint2(0u, 0u));
     if (active) {
 #pragma unroll
       for (uint32_t k = 0; k < 8; ++k)
@@ -673,11 +689,11 @@ __device__ __forceinline__ uint4 spec_attempt(const char *xb, uint32_t nbytes, u
           if (k0 + k == 0) acc.init(x[k]); else acc.add(x[k]);
         }
     }
-    if (want_hash) {
-      // this lane's share of every producer's hash, summed: the check compares totals
-#pragma unroll
-      for (uint32_t k = 0; k < 8; ++k)
-        if (k < kn && active) myh += tag_part(x[k], lane);
+    if (want_hash && active) {
+      // this lane's share of every producer's hashes, summed: the check compares totals
+      const uint2 h = tag_parts8(x, kn, lane);
+      myh.x += h.x;
+      myh.y += h.y;
     }
   }
   return active ? acc.pack() : make_uint4(0, 0, 0, 0);
@@ -761,7 +777,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(con
     cref = a.refs[cu.dst0 + (cit.slot == COLL_SLOT_ALL ? 0u : cit.slot)];
   }
   uint4 nx = make_uint4(0, 0, 0, 0);
-  uint32_t nh = 0;
+  uint2 nh = make_uint2(0u, 0u);
   bool nh_ready = false;
   const char *sin_base = nullptr;  // single stage item: its input piece at pool entry 0
   char *cout_base = nullptr;        // single consume item: its output piece at epoch 0
@@ -855,7 +871,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(con
       const uint32_t nvec = u.nbytes >> 4;
       char *dst = a.xbuf + (size_t)b * a.xpar + u.xoff + (size_t)it.slot * u.nbytes * slot_mult;
       uint4 x = make_uint4(0, 0, 0, 0);
-      uint32_t h = 0;
+      uint2 h = make_uint2(0u, 0u);
       if (pipelined) {
         x = nx;
         if (tagged && !nh_ready && lane < nvec) h = tag_part(x, lane);
@@ -883,12 +899,15 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(con
       } else if (lane < nvec) {
         st_v4(dst + lane * 16, x);
       }
-      uint32_t tag = 0;
-      if (tagged) tag = tag_fold(pipelined && nh_ready ? nh : __reduce_add_sync(FULL, h), E);
+      uint2 tag = make_uint2(0u, 0u);
+      if (tagged) {
+        const uint2 hs = pipelined && nh_ready ? nh : reduce_add2(h);
+        tag = make_uint2(tag_fold(hs.x, E), tag_fold_b(hs.y, E));
+      }
       __syncwarp();
       if (lane == 0 && !skip_notify && !ll) {
         unsigned long long *fp = a.pflag + (size_t)b * a.n_pflag + u.pflag0 + it.slot;
-        const unsigned long long fv = ((unsigned long long)E << 32) | tag;
+        const unsigned long long fv = flag_word(E, tag.x, tag.y);
         if (relaxed) st_relaxed_u64(fp, fv); else st_release_u64(fp, fv);
       }
       if (pipelined) {
@@ -971,7 +990,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(con
       if (!LL && spec_proto && n <= 32) {
         // Speculative consume: load and reduce without waiting, then validate.
         unsigned long long f = 0;
-        uint32_t myh = 0;
+        uint2 myh = make_uint2(0u, 0u);
         // (the prefetched next input is hashed while this attempt's loads are in flight)
         const bool side = pipelined && tagged && !nh_ready;
         res = spec_attempt<KIND>(xb, u.nbytes, n, lane, active, tagged, pf, !relaxed,
@@ -984,11 +1003,12 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(con
           spin_ns(a.inject_pause_ns);
           if (lane < n) f = relaxed ? ld_relaxed_u64(pf + lane) : ld_acquire_u64(pf + lane);
         }
-        uint32_t fe = (uint32_t)(f >> 32);
+        uint32_t fe = flag_epoch(f);
         bool ok;
         if (literal) {
+          // the pages' reduced flag: the epochs add up to n * E (16-bit epoch fields)
           const uint32_t sum = __reduce_add_sync(FULL, lane < n ? fe : 0u);
-          ok = sum == n * E;
+          ok = ((sum - n * E) & 0xFFFFu) == 0u;
         } else {
           ok = tags_match(f, myh, n, E, lane);
         }
@@ -1003,10 +1023,10 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(con
             // match (bounded by the spin limit and the abort word).
             uint64_t t0 = globaltimer();
             for (uint32_t k = 0;; ++k) {
-              uint32_t unused = 0;
+              uint2 unused = make_uint2(0u, 0u);
               res = spec_attempt<KIND>(xb, u.nbytes, n, lane, active, true, pf, false, true, f,
                                        myh, false, nx, 0u, unused);
-              fe = (uint32_t)(f >> 32);
+              fe = flag_epoch(f);
               if (tags_match(f, myh, n, E, lane)) {
                 have = true;
                 break;
@@ -1025,9 +1045,9 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(con
             // until their producer notifies. Then reload everything after the acquires.
             bool wok = true;
             for (uint32_t j = lane; j < n; j += 32) {
-              if (j == lane && fe == E) continue;
+              if (j == lane && fe == (E & 0xFFFFu)) continue;
               wok = wok && spin_u64(pf + j,
-                                    [E](unsigned long long v) { return (uint32_t)(v >> 32) == E; },
+                                    [E](unsigned long long v) { return flag_is(v, E); },
                                     st, a.spin_ns);
             }
             if (!__all_sync(FULL, wok)) {
@@ -1110,7 +1130,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(con
       if (lane == 0) red_release_add_u32(a.rank_done + W.rank, 1u);
     }
     if (pipelined && tagged && !nh_ready && !failed) {
-      nh = __reduce_add_sync(FULL, lane < (su.nbytes >> 4) ? tag_part(nx, lane) : 0u);
+      nh = reduce_add2(lane < (su.nbytes >> 4) ? tag_part(nx, lane) : make_uint2(0u, 0u));
       nh_ready = true;
     }
     if (stamp && (uint32_t)i < a.stamp_cap) a.stamps[phases ? 4 + 4 * i : i + 1] = globaltimer();

@@ -43,7 +43,7 @@ struct EngArgs {
   const coll_ref_t *refs;
   char *xbuf;
   uint64_t xpar;
-  unsigned long long *pflag;  // [2][n_pflag]
+  unsigned long long *pflag;  // [2][n_pflag] {epoch:16, tag B:16, tag A:32}
   uint32_t *cflag;            // [n_cflag]
   const coll_item_t *pitems;  // two-shot pull: pull items (unit, consumer slot)
   char *rbuf;                 // two-shot pull: reduced pieces, [parity] x rpar bytes

@@ -90,8 +90,11 @@ extern "C" {
 #define COLL_ORDER_RANK 0
 #define COLL_ORDER_TREE 1
 
-/* Speculative validation rules (COLL_PROTO_SPEC). */
-#define COLL_SPEC_TAGGED 0  /* flag epochs AND a content tag per piece must match (sound) */
+/* Speculative validation rules (COLL_PROTO_SPEC). A producer publishes one 64-bit flag word
+ * per piece, {epoch mod 2^16, tag B mod 2^16, tag A}: two independent content hashes of the
+ * piece (32 and 16 bits kept) with the epoch folded in. A stale or torn read passes the
+ * tagged checks only if both collide (about 2^-48 per stale read). */
+#define COLL_SPEC_TAGGED 0  /* flag epochs AND the content tags must match (sound)      */
 #define COLL_SPEC_LITERAL 1 /* only sum of flag epochs == n * epoch (the pages' rule);
                                unsound under reordering, kept as an ablation            */
 #define COLL_SPEC_TAGGED_RELAXED 2 /* content tags only: notify without a release fence,
