@@ -501,6 +501,8 @@ __device__ __forceinline__ void gemv_block(const EngArgs &a, GemvShared &g, cons
   uint64_t acc[4] = {0, 0, 0, 0};
   uint4 xl = make_uint4(0, 0, 0, 0);
   uint32_t ready = 0;  // bit t: the fill of slot 32c+t of this chunk has already landed
+  const uint64_t qe = (piece + 1) * bs;  // first fill of the next piece
+  bool done = true;
   for (uint32_t j = 0; j < bs; ++j) {
     if ((j & 31u) == 0u) {
       // per chunk of 32 slots: one x load and one readiness test per lane, in parallel
@@ -536,6 +538,7 @@ __device__ __forceinline__ void gemv_block(const EngArgs &a, GemvShared &g, cons
         record_timeout(a.st, (int)W.rank, -1, 6, 0);
         g.fail = 1;
       }
+      done = false;
       break;
     }
     const unsigned char *s = ring.rows + c.slot * kGemvSlotBytes + lane * 16;
@@ -543,10 +546,12 @@ __device__ __forceinline__ void gemv_block(const EngArgs &a, GemvShared &g, cons
 #pragma unroll
     for (uint32_t t = 0; t < 8; ++t)
       w[t] = act ? *reinterpret_cast<const uint4 *>(s + t * kGemvPitch) : make_uint4(0, 0, 0, 0);
-    // Refill the slot now, so that the copies overlap this slot's arithmetic: each lane's
-    // copies overwrite only the 16-byte column it has just read, after its reads in program
-    // order.
-    if (c.q + kGemvSlotsPerWarp < total)
+    // A refill this block still needs is issued now, so that the copies overlap this slot's
+    // arithmetic (each lane's copies overwrite only the 16-byte column it has just read,
+    // after its reads in program order); refills for later pieces wait for the end of the
+    // block, so that their copies stream during the exchange instead of competing with
+    // this block's.
+    if (c.q + kGemvSlotsPerWarp < total && c.q + kGemvSlotsPerWarp < qe)
       gemv_fill_block(g, ring, c.slot, c.src, wid, bs, c.rp_j, lane);
     if (j == 0) gemv_rows8<true>(acc, w, xv); else gemv_rows8<false>(acc, w, xv);
     ++c.q;
@@ -566,6 +571,29 @@ __device__ __forceinline__ void gemv_block(const EngArgs &a, GemvShared &g, cons
     asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(acc[p]));
     g.part[wid][lane][2 * p] = lo;
     g.part[wid][lane][2 * p + 1] = hi;
+  }
+  if (!done && lane == 0) g.fail = 1;
+}
+
+// The refills gemv_block deferred: the last min(6, bs) slots of block `piece`, refilled with
+// fills of later pieces (a division or two each, at most six per block). Issued after the
+// block's results are handed to warp 0, so that their copies stream while it runs the
+// exchange.
+__device__ __forceinline__ void gemv_deferred_refills(const EngArgs &a, GemvShared &g,
+                                                      const GemvRing &ring, const coll_warp_t &W,
+                                                      uint64_t piece, uint32_t wid,
+                                                      uint32_t lane) {
+  const uint32_t bs = g.S / kGemvWarps;
+  const uint64_t qe = (piece + 1) * bs;
+  const uint32_t m = bs < kGemvSlotsPerWarp ? bs : kGemvSlotsPerWarp;
+  for (uint32_t d = 0; d < m; ++d) {
+    const uint64_t q = qe - m + d;             // a slot read in this block
+    const uint64_t t = q + kGemvSlotsPerWarp;  // its refill
+    if (t >= g.total) break;
+    const uint64_t pt = t / bs;
+    const GemvSrc src = gemv_item(a, g, W, (uint32_t)(pt % g.nitems));
+    gemv_fill_block(g, ring, wid * kGemvSlotsPerWarp + (uint32_t)(q % kGemvSlotsPerWarp), src,
+                    wid, bs, (uint32_t)(t - pt * bs), lane);
   }
 }
 
@@ -600,6 +628,7 @@ __device__ void gemv_helper_loop(const EngArgs &a, const coll_warp_t &W, uint32_
     if (g.exit) return;
     gemv_block(a, g, ring, W, piece, wid, lane);
     gemv_bar();
+    if (!g.fail) gemv_deferred_refills(a, g, ring, W, piece, wid, lane);
   }
 }
 
