@@ -271,6 +271,34 @@ def test_decode_allreduce_epochs_bit_exact(protocol, datapath, chain):
     plan.free()
 
 
+@pytest.mark.parametrize("cfg", [dict(protocol="barrier"), dict(protocol="dual"),
+                                 dict(protocol="spec"), dict(protocol="spec", spec_check="relaxed"),
+                                 dict(protocol="spec", spec_check="literal"),
+                                 dict(protocol="dual", datapath="twoshot_pull")],
+                         ids=lambda c: "-".join(str(v) for v in c.values()))
+def test_flag_epochs_cross_the_16_bit_wrap(cfg):
+    # producer flags keep the epoch modulo 2^16: run past epoch 65,536 (one launch, and a
+    # second launch continuing the count) and check the last epochs against the oracle
+    R, n, pool = 8, 1024, 7
+    ins, expect = _decode_case(R, n, pool, seed=21)
+    plan = cdc.Plan(namings.allreduce(R, n, "bf16"), **cfg)
+    tail = 64
+    E1 = 65_530
+    outs = [torch.zeros(tail, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    # epochs 1..E1 overwrite one scratch row each (only the flags' progress matters here)
+    scratch = [torch.empty(n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    plan.run(ins, scratch, n_epochs=E1, in_epoch_stride=n * 2, in_pool=pool, out_epoch_stride=0)
+    assert plan.status()["code"] == 0
+    # the next launch continues at epoch E1 + 1 and crosses 65,536
+    E2 = tail
+    plan.run(ins, outs, n_epochs=E2, in_epoch_stride=n * 2, in_pool=pool, out_epoch_stride=n * 2)
+    st = plan.status()
+    assert st["code"] == 0, st
+    # epoch E1 + 1 + i of the plan reads pool entry i % pool of this launch
+    assert _check_epochs(outs, expect, E2, pool) == 0
+    plan.free()
+
+
 def test_decode_allreduce_10000_epochs_spec_equals_barrier_under_stagger():
     R, n, pool, E = 8, 4096, 7, 10000
     ins, expect = _decode_case(R, n, pool)
