@@ -310,6 +310,26 @@ def run_ours(args, rank, world, dist):
     te = _time_steps(torch, e2e_step, max(3, args.steps // 2), 2, flush, stream)
     e2e_us = sum(te) / len(te) * 1000 / EPOCHS
 
+    # the smallest configuration: all-reduce of 2 x 1024 fp32, barrier protocol, one epoch per
+    # launch; median of 1000 launches, each timed with CUDA events
+    g1 = torch.Generator(device=dev)
+    g1.manual_seed(1)
+    s_in = [(torch.rand(1024, device=dev, generator=g1) * 2 - 1) for _ in range(2)]
+    s_out = [torch.empty(1024, device=dev) for _ in range(2)]
+    s_plan = cdc.Plan(cdc.allreduce(2, 1024, "f32"), protocol="barrier")
+    for _ in range(20):
+        s_plan.run(s_in, s_out)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(1000)]
+    for a_, b_ in ev:
+        a_.record(stream)
+        s_plan.run(s_in, s_out, stream=stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    assert s_plan.status()["code"] == 0
+    small_us = sorted(a_.elapsed_time(b_) for a_, b_ in ev)[500] * 1000
+    s_plan.free()
+
     # prefill-sized all-reduce: 8 x 64 MiB bf16, one-shot vs two-shot (zero-copy)
     prefill = {}
     if not args.skip_prefill:
@@ -366,6 +386,8 @@ def run_ours(args, rank, world, dist):
         "flag_round_trip": rtt,
         "protocols": proto,
         "prefill_allreduce_64MiB": prefill,
+        "small_allreduce_2x1024_f32": {"median_us": round(small_us, 3), "launches": 1000,
+                                       "protocol": "barrier", "epochs_per_launch": 1},
         "e2e": {"value": round(e2e_us, 4), "unit": "us/epoch", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
