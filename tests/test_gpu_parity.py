@@ -739,10 +739,10 @@ def test_fused_gemv_with_a_reduce_scatter_naming_and_bad_arguments():
 
 
 @pytest.mark.parametrize("k,n,wpr", [(64, 4096, 0), (1024, 4096, 0), (512, 4096, 2), (128, 1000, 0),
-                                     (8192, 1024, 0)],
+                                     (8192, 1024, 0), (64, 4352, 1)],
                          ids=["k64-several-pieces-per-ring-lap", "k1024-ring-wraps-inside-a-piece",
                               "k512-four-pieces-per-warp", "k128-ragged-last-piece",
-                              "k8192-largest-x"])
+                              "k8192-largest-x", "k64-seventeen-pieces-per-warp"])
 def test_fused_gemv_weight_ring_shapes(k, n, wpr):
     # The streaming warp fills a 48-slot ring (8 weight rows per slot) ahead of the compute
     # warps; these shapes cover a ring lap holding several pieces, a piece longer than the
