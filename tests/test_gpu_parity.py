@@ -715,6 +715,29 @@ def test_fused_gemv_allreduce_bit_exact(protocol, datapath, chain):
     plan.free()
 
 
+@pytest.mark.parametrize("chain", [0, 1])
+def test_fused_gemv_2000_epochs_under_stagger(chain):
+    # timing perturbation of the fused loop: ranks delayed at random (up to 20 us) and
+    # started apart; every epoch must still equal the oracle
+    R, n, k, pool, E = 8, 4096, 256, 3, 2000
+    wts, xs = _gemv_case(R, n, k, pool, 97)
+    want = [collectives.allreduce(collectives.gemv_payloads(wts, [xs[r][e] for r in range(R)]),
+                                  "bf16")[0] for e in range(pool)]
+    want_dev = torch.stack([to_dev(w, "bf16") for w in want])
+    plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="spec", chain=chain,
+                    inject="stagger", inject_seed=7 + chain, inject_prob_ppm=100000,
+                    inject_max_ns=20000, inject_start_ns=5000)
+    dw = [to_dev(w.ravel(), "bf16") for w in wts]
+    dx = [torch.stack([to_dev(x, "bf16") for x in xs[r]]).contiguous() for r in range(R)]
+    outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    plan.run_gemv(dw, dx, k, outs, n_epochs=E, x_epoch_stride=2 * k, x_pool=pool,
+                  out_epoch_stride=2 * n)
+    st = plan.status()
+    assert st["code"] == 0, st
+    assert _check_epochs(outs, want_dev, E, pool) == 0
+    plan.free()
+
+
 def test_fused_gemv_with_a_reduce_scatter_naming_and_bad_arguments():
     R, n, k = 4, 2048, 64
     wts, xs = _gemv_case(R, n, k, 1, 98)
