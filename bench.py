@@ -375,7 +375,8 @@ def run_ours(args, rank, world, dist):
                                "protocol (dual buffers, tagged validation), oneshot",
                    "ranks": R_DECODE, "elems_per_rank": N_DECODE, "epochs_per_step": EPOCHS,
                    "input_pool": POOL, "protocol": "spec", "l2": "flushed before every timed "
-                   "step (256 MiB write)", "parallelism": f"replicas x{world}"},
+                   "step (256 MiB written, then another 256 MiB read)",
+                   "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 5),
                      "traffic": recorded_traffic("engine_kernel", ENGINE_SOURCES),
