@@ -11,4 +11,4 @@ from ._lib import CollError, lib  # noqa: F401
 from .namings import (Naming, allgather, allreduce, alltoall, alltoallv_from_routing,  # noqa: F401
                       broadcast, gather, moe_combine, moe_dispatch, reduce_scatter,
                       reduce_to_root, scatter, segs)
-from .plan import Plan, probe_flag_rtt, validate, validate_code  # noqa: F401
+from .plan import Plan, allreduce_static, probe_flag_rtt, validate, validate_code  # noqa: F401

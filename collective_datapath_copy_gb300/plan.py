@@ -154,3 +154,20 @@ def probe_flag_rtt(peer_block: int = 1, iters: int = 20000):
     check(lib().coll_probe_flag_rtt(int(peer_block), int(iters), C.byref(ns), C.byref(a),
                                     C.byref(b)), "coll_probe_flag_rtt")
     return ns.value / iters, a.value, b.value
+
+
+def allreduce_static(ins, outs, count, dtype="bf16", n_epochs=1, in_epoch_stride=0, in_pool=1,
+                     out_epoch_stride=0, status=None, stream=None) -> int:
+    """coll_allreduce_static: an all-reduce (fixed rank order, dual buffers) that allocates
+    nothing, its exchange buffers and flags in a fixed device array of the library. ins/outs:
+    per-rank torch CUDA tensors of `count` elements; strides in bytes; `status`: optional
+    int32 CUDA tensor that receives COLL_ETIMEDOUT if a bounded wait expires. Returns the
+    library's code (raises on a synchronous error)."""
+    R = len(ins)
+    code = lib().coll_allreduce_static(
+        R, _lib.DTYPE[dtype], C.cast(_dev_ptrs(ins, R), C.c_void_p),
+        C.cast(_dev_ptrs(outs, R), C.c_void_p), int(count), int(n_epochs), int(in_epoch_stride),
+        int(in_pool), int(out_epoch_stride),
+        C.c_void_p(status.data_ptr()) if status is not None else None, _stream_handle(stream))
+    check(code, "coll_allreduce_static")
+    return code

@@ -84,3 +84,22 @@ def test_static_allreduce_rejects_what_does_not_fit():
     outs = [torch.zeros(n, dtype=torch.int16, device="cuda") for _ in range(R)]
     assert static_allreduce(ins, outs, n, "bf16") == _lib.D["COLL_ETOOBIG"]
     assert static_allreduce(ins, outs, 3, "bf16") == _lib.D["COLL_EALIGN"]
+
+
+def test_python_binding_of_the_static_allreduce():
+    # cdc.allreduce_static marshals the same call; errors surface as CollError
+    R, n = 4, 2048
+    ins = _inputs(41, R, 1, n, "bf16")
+    plan = cdc.Plan(cdc.allreduce(R, n, "bf16"), protocol="dual")
+    ref = [torch.zeros(n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    plan.run(ins, ref)
+    assert plan.status()["code"] == 0
+    got = [torch.zeros(n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    assert cdc.allreduce_static(ins, got, n, "bf16") == 0
+    torch.cuda.synchronize()
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+    big = [torch.zeros(1 << 20, dtype=torch.int16, device="cuda") for _ in range(8)]
+    with pytest.raises(cdc.CollError):
+        cdc.allreduce_static(big, [torch.zeros_like(b) for b in big], 1 << 20, "bf16")
+    plan.free()
