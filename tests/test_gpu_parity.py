@@ -400,6 +400,18 @@ def test_run_rejects_aliasing_and_misalignment():
     assert code == cdc._lib.D["COLL_EOVERLAP"]
     code = plan.run_ptrs([a.data_ptr() + 2, a.data_ptr() + 4096], [a.data_ptr() + 8192 - 2048, 0])
     assert code in (cdc._lib.D["COLL_EALIGN"], cdc._lib.D["COLL_EINVAL"])
+    # degenerate run arguments: no epochs, an empty input pool, a missing rank's buffer,
+    # output epochs that overlap each other
+    b = torch.zeros(4 * 4096, dtype=torch.int16, device="cuda")
+    ins = [b.data_ptr(), b.data_ptr() + 2048]
+    outs = [b.data_ptr() + 8192, b.data_ptr() + 16384]
+    E = cdc._lib.D
+    assert plan.run_ptrs(ins, outs, n_epochs=0) == E["COLL_EINVAL"]
+    assert plan.run_ptrs(ins, outs, in_pool=0) == E["COLL_EINVAL"]
+    assert plan.run_ptrs([ins[0], 0], outs) == E["COLL_EINVAL"]
+    assert plan.run_ptrs(ins, outs, n_epochs=2, out_epoch_stride=1024) == E["COLL_EOVERLAP"]
+    assert plan.run_ptrs(ins, outs) == 0  # and the plan still runs
+    assert plan.status()["code"] == 0
     plan.free()
 
 
