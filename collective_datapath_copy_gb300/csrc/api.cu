@@ -17,6 +17,7 @@ struct coll_plan_s {
   coll_ref_t *d_refs = nullptr;
   coll_job_t *d_jobs = nullptr;
   coll_tile_t *d_tiles = nullptr;
+  coll_btile_t *d_btiles = nullptr;
   coll_unit_t *d_units = nullptr;
   coll_item_t *d_sitems = nullptr, *d_citems = nullptr, *d_pitems = nullptr;
   coll_warp_t *d_warps = nullptr;
@@ -132,6 +133,7 @@ extern "C" int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_
     return COLL_EINVAL;
   }
   const size_t tb = table_bytes(c.refs) + table_bytes(c.jobs) + table_bytes(c.tiles) +
+                    table_bytes(c.btiles) +
                     table_bytes(c.units) + table_bytes(c.sitems) + table_bytes(c.citems) +
                     table_bytes(c.pitems) + table_bytes(c.warps);
   std::vector<char> host(tb ? tb : 256, 0);
@@ -140,7 +142,8 @@ extern "C" int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_
     if (!v.empty()) memcpy(host.data() + off, v.data(), v.size() * sizeof(v[0]));
     off += table_bytes(v);
   };
-  put(c.refs); put(c.jobs); put(c.tiles); put(c.units); put(c.sitems); put(c.citems);
+  put(c.refs); put(c.jobs); put(c.tiles); put(c.btiles); put(c.units); put(c.sitems);
+  put(c.citems);
   put(c.pitems); put(c.warps);
   bool ok = cudaMalloc(&p->d_tables, host.size()) == cudaSuccess &&
             cudaMemcpy(p->d_tables, host.data(), host.size(), cudaMemcpyHostToDevice) == cudaSuccess &&
@@ -151,6 +154,7 @@ extern "C" int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_
     p->d_refs = carve(p->d_tables, off, c.refs);
     p->d_jobs = carve(p->d_tables, off, c.jobs);
     p->d_tiles = carve(p->d_tables, off, c.tiles);
+    p->d_btiles = carve(p->d_tables, off, c.btiles);
     p->d_units = carve(p->d_tables, off, c.units);
     p->d_sitems = carve(p->d_tables, off, c.sitems);
     p->d_citems = carve(p->d_tables, off, c.citems);
@@ -277,6 +281,7 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
     a.jobs = p->d_jobs;
     a.refs = p->d_refs;
     a.tiles = p->d_tiles;
+    a.btiles = p->d_btiles;
     a.ntiles = (uint32_t)c.tiles.size();
     a.n_epochs = (uint32_t)n_epochs;
     a.in_pool = in_pool;

@@ -69,9 +69,9 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
 
   uint32_t consumed = 0;
   if (warp == 0) {
-    // Producer warp. Tiles are resolved 32 at a time, one per lane (tile, job, and the
-    // source/destination pointers, all lanes in parallel), so descriptor fetches cost
-    // three memory round trips per 32 tiles; lane 0 then issues each tile's bulk loads.
+    // Producer warp. Tiles are resolved 32 at a time, one per lane: each tile's record
+    // carries its sources and destinations (rank, offset), so a batch costs one memory
+    // round trip; lane 0 then issues each tile's bulk loads.
     uint32_t k = 0;
     bool stop = false;
     for (uint64_t t0 = blockIdx.x; t0 < total && !stop; t0 += 32ull * gridDim.x) {
@@ -80,36 +80,39 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
       uint32_t nbytes = 0, nsrc = 0, ndst = 0;
       const char *sp[COLL_BULK_MAX_SRC];
       char *dp[COLL_BULK_MAX_DST];
+#pragma unroll
+      for (uint32_t j = 0; j < COLL_BULK_MAX_SRC; ++j) sp[j] = nullptr;
+#pragma unroll
+      for (uint32_t d = 0; d < COLL_BULK_MAX_DST; ++d) dp[d] = nullptr;
       if (have) {
         const uint32_t e = (uint32_t)(t / a.ntiles);
-        const coll_tile_t tile = a.tiles[t - (uint64_t)e * a.ntiles];
-        const coll_job_t job = a.jobs[tile.job];
-        const int64_t ioff = (int64_t)(e % (uint32_t)a.in_pool) * a.in_stride + (int64_t)tile.start;
-        const int64_t ooff = (int64_t)e * a.out_stride + (int64_t)tile.start;
-        nbytes = tile.nbytes;
-        nsrc = job.nsrc;
-        ndst = job.ndst;
+        const uint4 *rec = reinterpret_cast<const uint4 *>(a.btiles + (t - (uint64_t)e * a.ntiles));
+        uint4 w[9];  // the 144-byte record, loaded at once
 #pragma unroll
-        for (uint32_t j = 0; j < COLL_BULK_MAX_SRC; ++j) {
-          sp[j] = nullptr;
-          if (j < nsrc) {
-            const coll_ref_t r = a.refs[job.src0 + j];
-            sp[j] = a.ptr.in[r.rank] + r.off + ioff;
-          }
+        for (uint32_t q = 0; q < 9; ++q) w[q] = ld_nc_v4(rec + q);
+        const uint64_t start = ((uint64_t)w[0].y << 32) | w[0].x;
+        nbytes = w[0].z;
+        nsrc = w[0].w & 0xFFFFu;
+        ndst = w[0].w >> 16;
+        uint64_t ref[COLL_BULK_MAX_SRC + COLL_BULK_MAX_DST];
+#pragma unroll
+        for (uint32_t q = 0; q < 8; ++q) {
+          ref[2 * q] = ((uint64_t)w[q + 1].y << 32) | w[q + 1].x;
+          ref[2 * q + 1] = ((uint64_t)w[q + 1].w << 32) | w[q + 1].z;
         }
+        const int64_t ioff = (int64_t)(e % (uint32_t)a.in_pool) * a.in_stride + (int64_t)start;
+        const int64_t ooff = (int64_t)e * a.out_stride + (int64_t)start;
+        constexpr uint64_t kOffMask = (1ull << 56) - 1u;
 #pragma unroll
-        for (uint32_t d = 0; d < COLL_BULK_MAX_DST; ++d) {
-          dp[d] = nullptr;
+        for (uint32_t j = 0; j < COLL_BULK_MAX_SRC; ++j)
+          if (j < nsrc)
+            sp[j] = a.ptr.in[(uint32_t)(ref[j] >> 56)] + (ref[j] & kOffMask) + ioff;
+#pragma unroll
+        for (uint32_t d = 0; d < COLL_BULK_MAX_DST; ++d)
           if (d < ndst) {
-            const coll_ref_t r = a.refs[job.dst0 + d];
-            dp[d] = a.ptr.out[r.rank] + r.off + ooff;
+            const uint64_t r = ref[COLL_BULK_MAX_SRC + d];
+            dp[d] = a.ptr.out[(uint32_t)(r >> 56)] + (r & kOffMask) + ooff;
           }
-        }
-      } else {
-#pragma unroll
-        for (uint32_t j = 0; j < COLL_BULK_MAX_SRC; ++j) sp[j] = nullptr;
-#pragma unroll
-        for (uint32_t d = 0; d < COLL_BULK_MAX_DST; ++d) dp[d] = nullptr;
       }
       const uint32_t batch = __popc(__ballot_sync(FULLW, have));
       for (uint32_t i = 0; i < batch; ++i, ++k) {

@@ -55,6 +55,16 @@ struct coll_unit_t {
   uint64_t roff;    // two-shot pull: offset of the reduced piece in one parity of rbuf
 };
 
+// Zero-copy bulk ring: one tile with its sources and destinations inlined (rank in the
+// top 8 bits, segment byte offset below), so that resolving a tile is one memory round trip.
+#define COLL_BULK_REF(rank, off) (((uint64_t)(rank) << 56) | (uint64_t)(off))
+struct coll_btile_t {
+  uint64_t start;   // byte offset inside the job's segments
+  uint32_t nbytes;
+  uint16_t nsrc, ndst;
+  uint64_t ref[COLL_BULK_MAX_SRC + COLL_BULK_MAX_DST];  // sources, then destinations
+};
+
 #define COLL_SLOT_ALL 0xFFFFFFFFu
 struct coll_item_t {
   uint32_t unit;
@@ -93,6 +103,7 @@ struct coll_compiled {
   std::vector<coll_ref_t> refs;
   std::vector<coll_job_t> jobs;
   std::vector<coll_tile_t> tiles;
+  std::vector<coll_btile_t> btiles;  // bulk ring plans: tiles with inlined references
   std::vector<coll_unit_t> units;
   std::vector<coll_item_t> sitems, citems, pitems;
   std::vector<coll_warp_t> warps;

@@ -18,6 +18,7 @@ struct ZcArgs {
   const coll_job_t *jobs;
   const coll_ref_t *refs;
   const coll_tile_t *tiles;
+  const coll_btile_t *btiles;  // bulk kernel: the same tiles with their references inlined
   uint32_t ntiles;
   uint32_t n_epochs;
   int32_t in_pool;

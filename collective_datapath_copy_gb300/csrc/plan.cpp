@@ -279,6 +279,24 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
       }
     }
     if (c.tiles.size() > 0xFFFFFFF0ull) return COLL_EINVAL;
+    if (c.bulk) {
+      c.btiles.resize(c.tiles.size());
+      for (size_t i = 0; i < c.tiles.size(); ++i) {
+        const coll_tile_t &t = c.tiles[i];
+        const coll_job_t &j = c.jobs[t.job];
+        coll_btile_t &b = c.btiles[i];
+        memset(&b, 0, sizeof(b));
+        b.start = t.start;
+        b.nbytes = t.nbytes;
+        b.nsrc = (uint16_t)j.nsrc;
+        b.ndst = (uint16_t)j.ndst;
+        for (uint32_t k = 0; k < j.nsrc; ++k)
+          b.ref[k] = COLL_BULK_REF(c.refs[j.src0 + k].rank, c.refs[j.src0 + k].off);
+        for (uint32_t k = 0; k < j.ndst; ++k)
+          b.ref[COLL_BULK_MAX_SRC + k] =
+              COLL_BULK_REF(c.refs[j.dst0 + k].rank, c.refs[j.dst0 + k].off);
+      }
+    }
     *out = std::move(c);
     return COLL_OK;
   }
