@@ -44,30 +44,62 @@ __global__ void __launch_bounds__(256, TREE ? 2 : 3) zc_kernel(const ZcArgs a) {
   const uint64_t gw = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint64_t nw = ((uint64_t)gridDim.x * blockDim.x) >> 5;
   const uint64_t total = (uint64_t)a.ntiles * a.n_epochs;
+  constexpr uint64_t kOffMask = (1ull << 56) - 1u;
   for (uint64_t t = gw; t < total; t += nw) {
     const uint32_t e = (uint32_t)(t / a.ntiles);
     const uint32_t ti = (uint32_t)(t - (uint64_t)e * a.ntiles);
-    const coll_tile_t tile = a.tiles[ti];
-    const coll_job_t job = a.jobs[tile.job];
-    const int64_t ioff = (int64_t)(e % (uint32_t)a.in_pool) * a.in_stride + (int64_t)tile.start;
-    const int64_t ooff = (int64_t)e * a.out_stride + (int64_t)tile.start;
-    const uint32_t nsrc = job.nsrc, ndst = job.ndst;
+    // The tile's segments: from its inline record when the plan has one (one memory round
+    // trip: lanes 0..17 read the record's 8-byte words), else through tile -> job -> refs.
+    const uint64_t *rec = a.btiles ? reinterpret_cast<const uint64_t *>(a.btiles + ti) : nullptr;
+    uint64_t start, word = 0;
+    uint32_t nbytes, nsrc, ndst;
+    coll_job_t job{};
+    if (rec) {
+      if (lane < 2u + COLL_BULK_MAX_SRC + COLL_BULK_MAX_DST) word = __ldg((const unsigned long long *)rec + lane);
+      start = __shfl_sync(FULL, word, 0);
+      const uint64_t hdr = __shfl_sync(FULL, word, 1);
+      nbytes = (uint32_t)hdr;
+      nsrc = (uint32_t)(hdr >> 32) & 0xFFFFu;
+      ndst = (uint32_t)(hdr >> 48);
+    } else {
+      const coll_tile_t tile = a.tiles[ti];
+      job = a.jobs[tile.job];
+      start = tile.start;
+      nbytes = tile.nbytes;
+      nsrc = job.nsrc;
+      ndst = job.ndst;
+    }
+    const int64_t ioff = (int64_t)(e % (uint32_t)a.in_pool) * a.in_stride + (int64_t)start;
+    const int64_t ooff = (int64_t)e * a.out_stride + (int64_t)start;
     const char *sp = nullptr;
     char *dp = nullptr;
-    uint32_t mis = tile.nbytes & 15u;
-    if (lane < nsrc) {
-      const coll_ref_t r = a.refs[job.src0 + lane];
-      sp = a.ptr.in[r.rank] + r.off + ioff;
-      mis |= (uint32_t)((uintptr_t)sp & 15u);
-    }
-    if (lane < ndst) {
-      const coll_ref_t r = a.refs[job.dst0 + lane];
-      dp = a.ptr.out[r.rank] + r.off + ooff;
-      mis |= (uint32_t)((uintptr_t)dp & 15u);
+    uint32_t mis = nbytes & 15u;
+    if (rec) {
+      const uint64_t rs = __shfl_sync(FULL, word, 2u + (lane & 7u));
+      const uint64_t rd = __shfl_sync(FULL, word, 2u + COLL_BULK_MAX_SRC + (lane & 7u));
+      if (lane < nsrc) {
+        sp = a.ptr.in[(uint32_t)(rs >> 56)] + (rs & kOffMask) + ioff;
+        mis |= (uint32_t)((uintptr_t)sp & 15u);
+      }
+      if (lane < ndst) {
+        dp = a.ptr.out[(uint32_t)(rd >> 56)] + (rd & kOffMask) + ooff;
+        mis |= (uint32_t)((uintptr_t)dp & 15u);
+      }
+    } else {
+      if (lane < nsrc) {
+        const coll_ref_t r = a.refs[job.src0 + lane];
+        sp = a.ptr.in[r.rank] + r.off + ioff;
+        mis |= (uint32_t)((uintptr_t)sp & 15u);
+      }
+      if (lane < ndst) {
+        const coll_ref_t r = a.refs[job.dst0 + lane];
+        dp = a.ptr.out[r.rank] + r.off + ooff;
+        mis |= (uint32_t)((uintptr_t)dp & 15u);
+      }
     }
     const bool slow = __any_sync(FULL, mis != 0) || nsrc > 32 || ndst > 32;
     if (!slow) {
-      const uint32_t nvec = tile.nbytes >> 4;
+      const uint32_t nvec = nbytes >> 4;
       // The vector loops are warp-uniform (every lane iterates; loads and stores are
       // predicated) because they fetch pointers with full-warp shuffles.
       if constexpr (KIND == 0) {
@@ -122,23 +154,31 @@ __global__ void __launch_bounds__(256, TREE ? 2 : 3) zc_kernel(const ZcArgs a) {
         }
       }
     } else {
-      // Element-wise path: pointers recomputed from the tables.
+      // Element-wise path: pointers recomputed from the tables (or the inline record).
       auto src_of = [&](uint32_t k) {
+        if (rec) {
+          const uint64_t r = __ldg((const unsigned long long *)rec + 2 + k);
+          return (const char *)(a.ptr.in[(uint32_t)(r >> 56)] + (r & kOffMask) + ioff);
+        }
         const coll_ref_t r = a.refs[job.src0 + k];
-        return a.ptr.in[r.rank] + r.off + ioff;
+        return (const char *)(a.ptr.in[r.rank] + r.off + ioff);
       };
       auto dst_of = [&](uint32_t d) {
+        if (rec) {
+          const uint64_t r = __ldg((const unsigned long long *)rec + 2 + COLL_BULK_MAX_SRC + d);
+          return a.ptr.out[(uint32_t)(r >> 56)] + (r & kOffMask) + ooff;
+        }
         const coll_ref_t r = a.refs[job.dst0 + d];
         return a.ptr.out[r.rank] + r.off + ooff;
       };
       if constexpr (KIND == 0) {
         const char *s0 = src_of(0);
-        for (uint32_t i = lane; i < tile.nbytes; i += 32) {
+        for (uint32_t i = lane; i < nbytes; i += 32) {
           const char v = s0[i];
           for (uint32_t d = 0; d < ndst; ++d) dst_of(d)[i] = v;
         }
       } else if constexpr (KIND == 1) {
-        for (uint32_t i = lane; i < tile.nbytes / 2; i += 32) {
+        for (uint32_t i = lane; i < nbytes / 2; i += 32) {
           float acc = __uint_as_float((uint32_t)((const uint16_t *)src_of(0))[i] << 16);
           for (uint32_t k = 1; k < nsrc; ++k)
             acc = __fadd_rn(acc, __uint_as_float((uint32_t)((const uint16_t *)src_of(k))[i] << 16));
@@ -146,7 +186,7 @@ __global__ void __launch_bounds__(256, TREE ? 2 : 3) zc_kernel(const ZcArgs a) {
           for (uint32_t d = 0; d < ndst; ++d) ((uint16_t *)dst_of(d))[i] = r;
         }
       } else {
-        for (uint32_t i = lane; i < tile.nbytes / 4; i += 32) {
+        for (uint32_t i = lane; i < nbytes / 4; i += 32) {
           float acc = ((const float *)src_of(0))[i];
           for (uint32_t k = 1; k < nsrc; ++k) acc = __fadd_rn(acc, ((const float *)src_of(k))[i]);
           for (uint32_t d = 0; d < ndst; ++d) ((float *)dst_of(d))[i] = acc;

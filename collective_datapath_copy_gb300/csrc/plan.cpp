@@ -279,7 +279,9 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
       }
     }
     if (c.tiles.size() > 0xFFFFFFF0ull) return COLL_EINVAL;
-    if (c.bulk) {
+    // inline tile records whenever every job fits them (the bulk ring needs them; the warp
+    // kernel uses them when present)
+    if (maxsrc <= COLL_BULK_MAX_SRC && maxdst <= COLL_BULK_MAX_DST) {
       c.btiles.resize(c.tiles.size());
       for (size_t i = 0; i < c.tiles.size(); ++i) {
         const coll_tile_t &t = c.tiles[i];
