@@ -80,6 +80,7 @@ class Plan:
                                C.byref(c))
         check(code, "coll_plan")
         self._h = h
+        self._run_fn = lib().coll_run
         self.info = _lib.PlanInfo()
         check(lib().coll_plan_info(self._h, C.byref(self.info)), "coll_plan_info")
 
@@ -88,11 +89,20 @@ class Plan:
         """Enqueue n_epochs epochs. ins/outs: per-rank torch CUDA tensors (or None for a
         rank without segments). Strides are in bytes."""
         R = self.naming.R
-        code = lib().coll_run(self._h, C.cast(_dev_ptrs(ins, R), C.c_void_p),
-                              C.cast(_dev_ptrs(outs, R), C.c_void_p), int(n_epochs),
-                              int(in_epoch_stride), int(in_pool), int(out_epoch_stride),
-                              _stream_handle(stream))
-        check(code, "coll_run")
+        code = self._run_fn(self._h, C.cast(_dev_ptrs(ins, R), C.c_void_p),
+                            C.cast(_dev_ptrs(outs, R), C.c_void_p), int(n_epochs),
+                            int(in_epoch_stride), int(in_pool), int(out_epoch_stride),
+                            _stream_handle(stream))
+        if code:
+            check(code, "coll_run")
+
+    def bind(self, ins, outs, n_epochs=1, in_epoch_stride=0, in_pool=1, out_epoch_stride=0,
+             stream=None):
+        """Marshal a run once (buffers, strides, stream) and return a callable that enqueues
+        it again: the per-call host cost is then the library call itself, which matters when
+        small collectives are issued one by one on the same buffers."""
+        return BoundRun(self, ins, outs, n_epochs, in_epoch_stride, in_pool, out_epoch_stride,
+                        stream)
 
     def run_gemv(self, wts, xs, k, outs, n_epochs=1, x_epoch_stride=0, x_pool=1,
                  out_epoch_stride=0, stream=None):
@@ -154,6 +164,28 @@ def probe_flag_rtt(peer_block: int = 1, iters: int = 20000):
     check(lib().coll_probe_flag_rtt(int(peer_block), int(iters), C.byref(ns), C.byref(a),
                                     C.byref(b)), "coll_probe_flag_rtt")
     return ns.value / iters, a.value, b.value
+
+
+class BoundRun:
+    """A run of a plan with its arguments marshalled once (see Plan.bind). Calling it
+    enqueues the run again and raises CollError on a synchronous error. The buffers must stay
+    alive and the stream valid while the object is used."""
+
+    def __init__(self, plan, ins, outs, n_epochs, in_epoch_stride, in_pool, out_epoch_stride,
+                 stream):
+        R = plan.naming.R
+        self._plan = plan
+        self._keep = (list(ins), list(outs))  # keep the tensors alive
+        self._ia = C.cast(_dev_ptrs(ins, R), C.c_void_p)
+        self._oa = C.cast(_dev_ptrs(outs, R), C.c_void_p)
+        self._args = (int(n_epochs), int(in_epoch_stride), int(in_pool), int(out_epoch_stride),
+                      _stream_handle(stream))
+        self._fn = lib().coll_run
+
+    def __call__(self):
+        code = self._fn(self._plan._h, self._ia, self._oa, *self._args)
+        if code:
+            check(code, "coll_run")
 
 
 def allreduce_static(ins, outs, count, dtype="bf16", n_epochs=1, in_epoch_stride=0, in_pool=1,

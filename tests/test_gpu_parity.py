@@ -392,6 +392,20 @@ def test_missing_notify_times_out_and_the_gpu_stays_usable(protocol, datapath):
     assert bits_equal(got[0], want[0])
 
 
+def test_bound_run_repeats_the_same_call():
+    R, n = 8, 4096
+    ins, expect = _decode_case(R, n, 1, seed=51)
+    plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="spec")
+    outs = [torch.zeros(1, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    run = plan.bind(ins, outs)
+    for _ in range(5):
+        run()
+    assert plan.status()["code"] == 0
+    assert _check_epochs(outs, expect, 1, 1) == 0
+    assert plan.status()["spec_checks"] == 5 * R * 16
+    plan.free()
+
+
 def test_run_rejects_aliasing_and_misalignment():
     nm = namings.allreduce(2, 1024, "bf16")
     plan = cdc.Plan(nm, protocol="spec")
