@@ -272,6 +272,9 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
   }
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t err;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return COLL_ECUDA;
+  const bool capturing = cs != cudaStreamCaptureStatusNone;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != p->device) return COLL_EINVAL;
   if (c.cfg.zero_copy) {
@@ -339,7 +342,24 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
     a.nwarps = (uint32_t)c.warps.size();
     a.n_epochs = n_epochs;
     a.in_pool = in_pool;
-    a.epoch_base = (uint32_t)p->epochs_issued;
+    // A captured run is replayed with the epochs it was captured with. So once a plan has
+    // been captured, every run (the captured one, each of its replays, and later direct
+    // runs) first clears the plan's flags on the stream and counts epochs from 1 again:
+    // flags left by an earlier replay can then never pass for this run's.
+    const bool restart = capturing || p->captured;
+    if (restart) {
+      const size_t nu = c.units.size();
+      if ((p->d_pflag && cudaMemsetAsync(p->d_pflag, 0, (size_t)c.n_pflag * 2 * 8, s)) ||
+          (p->d_cflag && cudaMemsetAsync(p->d_cflag, 0, (size_t)c.n_cflag * 4, s)) ||
+          (p->d_rflag && cudaMemsetAsync(p->d_rflag, 0, nu * 2 * 4, s)) ||
+          (p->d_dflag && cudaMemsetAsync(p->d_dflag, 0, (size_t)c.n_dflag * 4, s)) ||
+          (p->d_dbg && cudaMemsetAsync(p->d_dbg, 0, nu * 4, s)) ||
+          (p->d_rank_done && cudaMemsetAsync(p->d_rank_done, 0, (size_t)c.R * 4, s))) {
+        cudaGetLastError();
+        return COLL_ECUDA;
+      }
+    }
+    a.epoch_base = restart ? 0u : (uint32_t)p->epochs_issued;
     a.in_stride = in_epoch_stride;
     a.out_stride = out_epoch_stride;
     a.protocol = c.cfg.protocol;
@@ -362,7 +382,7 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
       a.gemv_k = k;
     }
     err = coll::launch_engine(c.op, c.dtype, a, s);
-    if (err == cudaSuccess) p->epochs_issued += (uint64_t)n_epochs;
+    if (err == cudaSuccess && !restart) p->epochs_issued += (uint64_t)n_epochs;
   }
   if (err != cudaSuccess) {
     cudaGetLastError();
@@ -370,9 +390,7 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
   }
   // Inside a stream capture the completion event is not recorded (a captured record
   // cannot be waited on from outside the graph); coll_status then waits for the device.
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return COLL_ECUDA;
-  if (cs == cudaStreamCaptureStatusNone) {
+  if (!capturing) {
     if (cudaEventRecord(p->done, s) != cudaSuccess) return COLL_ECUDA;
     p->ran = true;
   } else {

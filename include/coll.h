@@ -215,8 +215,11 @@ int coll_plan_info(coll_plan_t p, coll_plan_info_t *info);
  * bytes (stride 0 overwrites). A rank with no segments may pass NULL.
  * Staged plans run one cooperative persistent launch for all epochs; zero-copy plans run
  * one ordinary launch. Returns after enqueueing; device-side failures are reported by
- * coll_status. Zero-copy runs may be captured into a CUDA graph (the plan's tables are
- * fixed; the pointers and strides given here are baked into the captured launch).
+ * coll_status. Runs may be captured into a CUDA graph (the plan's tables are fixed; the
+ * pointers and strides given here are baked into the captured launch). Once a staged plan
+ * has been captured, each of its runs, the captured one with every replay included, first
+ * clears the plan's flags on the stream and counts its epochs from 1. A plan still runs one
+ * run at a time: replays and direct runs of it must not overlap.
  * Synchronous errors: COLL_EINVAL (n_epochs < 1, in_pool < 1, NULL pointer
  * for a rank that has segments), COLL_EALIGN, COLL_EOVERLAP, COLL_ECUDA. Buffers must stay
  * live and unmodified until the stream has passed the run. */

@@ -539,6 +539,49 @@ def test_zero_copy_plan_replays_inside_a_cuda_graph():
     plan.free()
 
 
+@pytest.mark.parametrize("cfg", [dict(protocol="spec"), dict(protocol="dual"),
+                                 dict(protocol="barrier"), dict(protocol="spec", chain=1),
+                                 dict(protocol="dual", datapath="twoshot_pull")],
+                         ids=lambda c: "-".join(str(v) for v in c.values()))
+def test_staged_plan_replays_inside_a_cuda_graph(cfg):
+    # a captured staged run clears the plan's flags and counts its epochs from 1 on every
+    # replay; new input contents between replays must show up in the outputs
+    R, n, E = 8, 4096, 3
+    nm = namings.allreduce(R, n, "bf16")
+    plan = cdc.Plan(nm, **cfg)
+    ins = [torch.zeros(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    outs = [torch.zeros(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    kw = dict(n_epochs=E, in_epoch_stride=2 * n, in_pool=E, out_epoch_stride=2 * n)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        plan.run(ins, outs, **kw)  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        plan.run(ins, outs, **kw)
+    for rep in range(3):
+        rng = synth.seeded_rng(600 + rep)
+        xs = [[synth.normal_bf16(rng, n) for _ in range(E)] for _ in range(R)]
+        for r in range(R):
+            ins[r].copy_(torch.stack([to_dev(x, "bf16") for x in xs[r]]))
+        g.replay()
+        torch.cuda.synchronize()
+        assert plan.status()["code"] == 0, rep
+        for e in range(E):
+            want = collectives.allreduce([xs[r][e] for r in range(R)], "bf16")[0]
+            for r in range(R):
+                assert bits_equal(from_dev(outs[r][e], "bf16"), want), (rep, e, r)
+    # a direct run after the replays
+    plan.run(ins, outs, **kw)
+    assert plan.status()["code"] == 0
+    for e in range(E):
+        want = collectives.allreduce([xs[r][e] for r in range(R)], "bf16")[0]
+        assert bits_equal(from_dev(outs[0][e], "bf16"), want)
+    plan.free()
+
+
 @pytest.mark.parametrize("seed", range(16))
 def test_bulk_ring_on_small_aligned_namings(seed):
     # force the bulk-copy (TMA) ring on small random namings (segments scaled to 16 bytes)
