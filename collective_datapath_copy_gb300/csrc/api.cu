@@ -354,7 +354,10 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
           (p->d_rflag && cudaMemsetAsync(p->d_rflag, 0, nu * 2 * 4, s)) ||
           (p->d_dflag && cudaMemsetAsync(p->d_dflag, 0, (size_t)c.n_dflag * 4, s)) ||
           (p->d_dbg && cudaMemsetAsync(p->d_dbg, 0, nu * 4, s)) ||
-          (p->d_rank_done && cudaMemsetAsync(p->d_rank_done, 0, (size_t)c.R * 4, s))) {
+          (p->d_rank_done && cudaMemsetAsync(p->d_rank_done, 0, (size_t)c.R * 4, s)) ||
+          // tagged data keeps its epochs in the exchange words themselves
+          (c.cfg.protocol == COLL_PROTO_LL && p->d_xbuf &&
+           cudaMemsetAsync(p->d_xbuf, 0, (size_t)c.xpar_bytes * 2, s))) {
         cudaGetLastError();
         return COLL_ECUDA;
       }

@@ -541,7 +541,8 @@ def test_zero_copy_plan_replays_inside_a_cuda_graph():
 
 @pytest.mark.parametrize("cfg", [dict(protocol="spec"), dict(protocol="dual"),
                                  dict(protocol="barrier"), dict(protocol="spec", chain=1),
-                                 dict(protocol="dual", datapath="twoshot_pull")],
+                                 dict(protocol="dual", datapath="twoshot_pull"),
+                                 dict(protocol="ll"), dict(protocol="spec", spec_check="relaxed")],
                          ids=lambda c: "-".join(str(v) for v in c.values()))
 def test_staged_plan_replays_inside_a_cuda_graph(cfg):
     # a captured staged run clears the plan's flags and counts its epochs from 1 on every
