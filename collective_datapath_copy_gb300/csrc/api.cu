@@ -88,6 +88,10 @@ int zero_state(coll_plan_s *p) {
     return COLL_ECUDA;
   if (p->d_rank_done && cudaMemset(p->d_rank_done, 0, (size_t)c.R * 4) != cudaSuccess)
     return COLL_ECUDA;
+  // tagged data keeps its epochs in the exchange words: epochs restart at 1 after a reset
+  if (c.cfg.protocol == COLL_PROTO_LL && p->d_xbuf &&
+      cudaMemset(p->d_xbuf, 0, (size_t)c.xpar_bytes * 2) != cudaSuccess)
+    return COLL_ECUDA;
   if (cudaMemset(p->d_status, 0, sizeof(coll_dev_status_t)) != cudaSuccess) return COLL_ECUDA;
   p->epochs_issued = 0;
   return COLL_OK;

@@ -299,6 +299,26 @@ def test_flag_epochs_cross_the_16_bit_wrap(cfg):
     plan.free()
 
 
+@pytest.mark.parametrize("protocol", ["ll", "dual", "spec"])
+def test_reset_then_rerun_with_new_inputs(protocol):
+    # after coll_reset epochs count from 1 again: nothing left from the earlier run (flags,
+    # or the epochs inside tagged-data words) may pass for the new run's
+    R, n = 8, 4096
+    nm = namings.allreduce(R, n, "bf16")
+    plan = cdc.Plan(nm, protocol=protocol)
+    outs = [torch.zeros(n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    for rep in range(3):
+        rng = synth.seeded_rng(700 + rep)
+        xs = [synth.normal_bf16(rng, n) for _ in range(R)]
+        plan.run([to_dev(x, "bf16") for x in xs], outs)
+        assert plan.status()["code"] == 0
+        want = collectives.allreduce(xs, "bf16")[0]
+        for o in outs:
+            assert bits_equal(from_dev(o, "bf16"), want), rep
+        plan.reset()
+    plan.free()
+
+
 def test_decode_allreduce_10000_epochs_spec_equals_barrier_under_stagger():
     R, n, pool, E = 8, 4096, 7, 10000
     ins, expect = _decode_case(R, n, pool)
