@@ -216,6 +216,7 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
   if (wt) {
     // eight warps each take k/8 rows, eight at a time: k must be a multiple of 64
     if (c.cfg.zero_copy || c.dtype != COLL_BF16 || k < 64 || (k & 63u)) return COLL_EINVAL;
+    if (c.cfg.protocol == COLL_PROTO_LL) return COLL_EINVAL;  // tagged data is not fused
     for (int r = 0; r < R; ++r) {
       if (!c.in_used[r]) continue;
       if (!wt[r]) return COLL_EINVAL;
@@ -380,7 +381,6 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
     a.inject_start_ns = c.cfg.inject_start_ns;
     a.inject_pause_ns = c.cfg.inject_pause_ns;
     a.R = R;
-    if (wt && c.cfg.protocol == COLL_PROTO_LL) return COLL_EINVAL;  // not combined
     if (wt) {
       for (int r = 0; r < R; ++r) {
         a.wt[r] = static_cast<const char *>(wt[r]);

@@ -7,6 +7,7 @@
 #include "coll.h"
 
 #define COLL_MAX_RANKS 64
+#define COLL_MAX_ELEMS (1ull << 48)  // elements in one rank's buffer
 #define COLL_MAX_FANIN 256   // producers of one name
 #define COLL_MAX_FANOUT 256  // consumers of one name
 #define COLL_WARP_VEC 32     // lanes per warp, one 16-byte vector each per step

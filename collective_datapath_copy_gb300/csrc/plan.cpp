@@ -82,6 +82,9 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
   if (!in_len || !out_len) return COLL_EINVAL;
   if ((n_in && !in_segs) || (n_out && !out_segs)) return COLL_EINVAL;
   if (n_in > 0xFFFFFFF0u || n_out > 0xFFFFFFF0u) return COLL_EINVAL;
+  // byte sizes (elements x element size, times ranks) must stay far from 64-bit overflow
+  for (int r = 0; r < R; ++r)
+    if (in_len[r] > COLL_MAX_ELEMS || out_len[r] > COLL_MAX_ELEMS) return COLL_EBOUNDS;
   // 2. segments: rank, count, reserved
   for (size_t i = 0; i < n_in + n_out; ++i) {
     const coll_seg_t &s = i < n_in ? in_segs[i] : out_segs[i - n_in];

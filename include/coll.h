@@ -190,7 +190,8 @@ int coll_config_default(coll_config_t *cfg);
 
 /* Validate a naming and compile it into a plan: host work tables, device tables,
  * exchange buffers (x2 parities) and zeroed flags for staged plans.
- * in_len/out_len: R buffer lengths in elements. cfg may be NULL (defaults).
+ * R: 1..64 ranks. in_len/out_len: R buffer lengths in elements, each at most 2^48
+ * (COLL_EBOUNDS beyond). cfg may be NULL (defaults).
  * Ownership: the plan owns everything it allocates; coll_free releases it. The segment
  * arrays are copied and may be freed after the call.
  * Errors (synchronous, nothing allocated): COLL_EINVAL, COLL_EBOUNDS, COLL_ELEN,

@@ -123,6 +123,18 @@ def test_bad_config_rejected():
         cdc.validate(n, datapath="twoshot_pull", protocol="ll")
 
 
+def test_buffer_lengths_beyond_the_limit_are_rejected():
+    # byte sizes stay far from 64-bit overflow: at most 2^48 elements per rank's buffer
+    E = _lib.D
+    big = 1 << 48
+    assert _code(2, "copy", "bf16", [big, 16], [(0, 0, 8, 0)], [16, 16], [(1, 0, 8, 0)],
+                 zero_copy=1) == 0
+    assert _code(2, "copy", "bf16", [big + 1, 16], [(0, 0, 8, 0)], [16, 16], [(1, 0, 8, 0)],
+                 zero_copy=1) == E["COLL_EBOUNDS"]
+    assert _code(2, "sum", "f32", [16, 16], [(0, 0, 8, 0)], [16, (1 << 63) + 16],
+                 [(1, 0, 8, 0)], zero_copy=1) == E["COLL_EBOUNDS"]
+
+
 def test_twoshot_pull_plan_shape():
     # 8 ranks x 4096 bf16: 16 units; each owner reduces 2 of them into the second exchange
     # buffer, and every rank pulls all 16: 16 pull items per rank, on 16 warps per rank
