@@ -63,6 +63,31 @@ def _dev_ptrs(tensors, R):
     return arr
 
 
+def _check_buffers(R, tensors, used, nbytes, stride, count, where):
+    """The library sees only addresses. Before a run, check that every buffer it will touch
+    is a CUDA tensor whose storage holds all the bytes the run reads or writes there:
+    nbytes[r] at each of `count` epochs spaced `stride` bytes apart. A tensor that is too
+    small would otherwise be overrun on the device."""
+    for r in range(R):
+        if not used[r]:
+            continue
+        t = tensors[r] if tensors is not None and r < len(tensors) else None
+        if t is None:
+            continue  # the library rejects a missing buffer itself
+        if not t.is_cuda:
+            raise ValueError(f"{where}: buffer of rank {r} is not a CUDA tensor")
+        st = t.untyped_storage()
+        s0, s1 = st.data_ptr(), st.data_ptr() + st.nbytes()
+        reach = int(stride) * (int(count) - 1) if count > 1 else 0
+        lo = t.data_ptr() + min(0, reach)
+        hi = t.data_ptr() + max(0, reach) + int(nbytes[r])
+        if lo < s0 or hi > s1:
+            raise _lib.CollError(_lib.D["COLL_EBOUNDS"],
+                                 f"{where}: buffer of rank {r} holds {s1 - t.data_ptr()} bytes "
+                                 f"from its start, the run touches [{lo - t.data_ptr()}, "
+                                 f"{hi - t.data_ptr()})")
+
+
 class Plan:
     """A compiled collective. Config keywords mirror coll_config_t (protocol='spec'|'dual'|
     'barrier', datapath='oneshot'|'twoshot', zero_copy, spec_check='tagged'|'literal', ...)."""
@@ -81,6 +106,19 @@ class Plan:
         check(code, "coll_plan")
         self._h = h
         self._run_fn = lib().coll_run
+        # what a run touches, per rank: the whole buffer of every rank that holds a segment
+        # of a consumed name (inputs) or any output segment (outputs)
+        es = _lib.ESIZE[naming.dtype]
+        consumed = {int(x) for x in np.asarray(naming.out_segs["name"])}
+        self._in_used = [False] * naming.R
+        for row in naming.in_segs:
+            if int(row["name"]) in consumed:
+                self._in_used[int(row["rank"])] = True
+        self._out_used = [False] * naming.R
+        for row in naming.out_segs:
+            self._out_used[int(row["rank"])] = True
+        self._in_bytes = [int(x) * es for x in naming.in_len]
+        self._out_bytes = [int(x) * es for x in naming.out_len]
         self.info = _lib.PlanInfo()
         check(lib().coll_plan_info(self._h, C.byref(self.info)), "coll_plan_info")
 
@@ -89,12 +127,21 @@ class Plan:
         """Enqueue n_epochs epochs. ins/outs: per-rank torch CUDA tensors (or None for a
         rank without segments). Strides are in bytes."""
         R = self.naming.R
+        self._check(ins, outs, n_epochs, in_epoch_stride, in_pool, out_epoch_stride)
         code = self._run_fn(self._h, C.cast(_dev_ptrs(ins, R), C.c_void_p),
                             C.cast(_dev_ptrs(outs, R), C.c_void_p), int(n_epochs),
                             int(in_epoch_stride), int(in_pool), int(out_epoch_stride),
                             _stream_handle(stream))
         if code:
             check(code, "coll_run")
+
+    def _check(self, ins, outs, n_epochs, in_epoch_stride, in_pool, out_epoch_stride,
+               in_bytes=None):
+        R = self.naming.R
+        _check_buffers(R, ins, self._in_used, in_bytes or self._in_bytes, in_epoch_stride,
+                       in_pool, "coll_run")
+        _check_buffers(R, outs, self._out_used, self._out_bytes, out_epoch_stride, n_epochs,
+                       "coll_run")
 
     def bind(self, ins, outs, n_epochs=1, in_epoch_stride=0, in_pool=1, out_epoch_stride=0,
              stream=None):
@@ -109,6 +156,10 @@ class Plan:
         """Fused producer: each rank's payload is W_r x_r computed inside the engine.
         wts[r]: [k, in_len[r]] bf16 (W_r transposed); xs[r]: x vectors (k bf16 per epoch)."""
         R = self.naming.R
+        self._check(xs, outs, n_epochs, x_epoch_stride, x_pool, out_epoch_stride,
+                    in_bytes=[2 * int(k)] * R)
+        _check_buffers(R, wts, self._in_used, [int(k) * b for b in self._in_bytes],
+                       0, 1, "coll_run_gemv")
         code = lib().coll_run_gemv(self._h, C.cast(_dev_ptrs(wts, R), C.c_void_p),
                                    C.cast(_dev_ptrs(xs, R), C.c_void_p), int(k),
                                    C.cast(_dev_ptrs(outs, R), C.c_void_p), int(n_epochs),
@@ -174,6 +225,7 @@ class BoundRun:
     def __init__(self, plan, ins, outs, n_epochs, in_epoch_stride, in_pool, out_epoch_stride,
                  stream):
         R = plan.naming.R
+        plan._check(ins, outs, n_epochs, in_epoch_stride, in_pool, out_epoch_stride)
         self._plan = plan
         self._keep = (list(ins), list(outs))  # keep the tensors alive
         self._ia = C.cast(_dev_ptrs(ins, R), C.c_void_p)

@@ -449,6 +449,35 @@ def test_run_rejects_aliasing_and_misalignment():
     plan.free()
 
 
+def test_binding_rejects_buffers_too_small_for_the_run():
+    # the library sees addresses only: the binding checks each tensor's storage against the
+    # bytes the run will touch (epoch strides included) before anything is enqueued
+    R, n = 2, 1024
+    nm = namings.allreduce(R, n, "bf16")
+    plan = cdc.Plan(nm, protocol="dual")
+    E = cdc._lib.D
+    ins = [torch.zeros(n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    outs = [torch.zeros(n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    short = [torch.zeros(n - 8, dtype=torch.int16, device="cuda"), outs[1]]
+    with pytest.raises(cdc.CollError) as e:
+        plan.run(ins, short)
+    assert e.value.code == E["COLL_EBOUNDS"]
+    with pytest.raises(cdc.CollError) as e:  # 3 epochs of output need 3 n elements
+        plan.run(ins, outs, n_epochs=3, out_epoch_stride=2 * n)
+    assert e.value.code == E["COLL_EBOUNDS"]
+    with pytest.raises(cdc.CollError) as e:  # an input pool of 2 sets
+        plan.bind(ins, outs, in_pool=2, in_epoch_stride=2 * n)
+    assert e.value.code == E["COLL_EBOUNDS"]
+    with pytest.raises(ValueError):
+        plan.run([x.cpu() for x in ins], outs)
+    # a view into a larger storage may reach beyond the view itself
+    big = torch.zeros(3, n, dtype=torch.int16, device="cuda")
+    plan.run(ins, [big[0], outs[1]], n_epochs=3, out_epoch_stride=0)
+    plan.run(ins, [big[0, :8], big[1, :8]], n_epochs=1)  # storage covers both ranks' outputs
+    assert plan.status()["code"] == 0
+    plan.free()
+
+
 # ------------------------------------------------------------ full-size cases
 
 def test_prefill_allreduce_64mib_oneshot_and_twoshot_full():
@@ -875,6 +904,27 @@ def test_fused_gemv_weight_ring_shapes(k, n, wpr):
         for r in range(R):
             assert bits_equal(from_dev(outs[r][e], "bf16"), want[e % pool]), (e, r)
     plan.free()
+
+
+def test_fused_gemv_signed_zeros():
+    # each block's chain starts from its first product: weights of -0 against x >= +0 give
+    # -0 payloads, and the fixed-order sum of -0 over ranks stays -0; a rank with +0
+    # payloads turns the sum into +0
+    R, n, k = 4, 1024, 128
+    rng = synth.seeded_rng(93)
+    xs = [(synth.normal_bf16(rng, k) & np.uint16(0x7FFF)).astype(np.uint16) for _ in range(R)]
+    for signs in ((1, 1, 1, 1), (1, 0, 1, 1)):
+        wts = [np.full((k, n), 0x8000 if sg else 0x0000, dtype=np.uint16) for sg in signs]
+        want = collectives.allreduce(collectives.gemv_payloads(wts, xs), "bf16")[0]
+        assert np.all(want == (0x8000 if all(signs) else 0x0000))
+        plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="spec")
+        outs = [torch.empty(n, dtype=torch.int16, device="cuda") for _ in range(R)]
+        plan.run_gemv([to_dev(w.ravel(), "bf16") for w in wts], [to_dev(x, "bf16") for x in xs],
+                      k, outs)
+        assert plan.status()["code"] == 0
+        for r in range(R):
+            assert bits_equal(from_dev(outs[r], "bf16"), want), (signs, r)
+        plan.free()
 
 
 def test_fused_gemv_rejects_a_plan_wider_than_the_gpu_and_keeps_the_plain_run():

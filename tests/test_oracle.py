@@ -558,3 +558,8 @@ def test_gemv_payload_closed_forms():
     wt3 = arith.f32_to_bf16_rne(arith.bf16_to_f32(wt2) * np.float32(2))
     y2 = collectives.gemv_payloads([wt3], [x])[0]
     assert np.array_equal(arith.bf16_to_f32(y2), arith.bf16_to_f32(y1) * np.float32(2))
+    # every product -0 (weights -0, x >= +0): each block's chain starts from its first
+    # product, so -0 + -0 + ... stays -0 (a chain from +0.0 would give +0)
+    wz = np.full((k, n), 0x8000, dtype=np.uint16)
+    xp = (x & np.uint16(0x7FFF)).astype(np.uint16)
+    assert np.all(collectives.gemv_payloads([wz], [xp])[0] == 0x8000)

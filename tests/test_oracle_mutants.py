@@ -140,3 +140,109 @@ def test_pins_catch_copy_from_the_wrong_producer(monkeypatch):
         return orig(R, op, dtype, in_len, in_segs, out_len, out_segs, inputs, outputs)
     monkeypatch.setattr(naming, "run_naming", wrong)
     assert not _all_pins_pass()
+
+
+# ---------------------------------------------------------------- fused producer, tolerance
+
+def _gemv_ok():
+    try:
+        pins.test_gemv_payload_matches_exact_rational_evaluation()
+        pins.test_gemv_block_order_is_observable()
+        pins.test_gemv_payload_closed_forms()
+    except AssertionError:
+        return False
+    return True
+
+
+def _gemv_mutant(kind):
+    from oracle.arith import bf16_to_f32, f32_to_bf16_rne
+
+    def gemv(wts, xs, kblocks=collectives.GEMV_KBLOCKS):
+        out = []
+        for wt, x in zip(wts, xs):
+            w, xv = bf16_to_f32(wt), bf16_to_f32(x)
+            k = w.shape[0]
+            kb = k // kblocks
+            sums = []
+            for b in range(kblocks):
+                rows = range(b * kb, (b + 1) * kb)
+                if kind == "accumulator starts at +0.0":
+                    acc = np.zeros(w.shape[1], np.float32)
+                    for i in rows:
+                        acc = acc + w[i] * xv[i]
+                elif kind == "products rounded to bf16":
+                    acc = None
+                    for i in rows:
+                        p = bf16_to_f32(f32_to_bf16_rne(w[i] * xv[i]))
+                        acc = p if acc is None else acc + p
+                else:
+                    acc = w[rows[0]] * xv[rows[0]]
+                    for i in rows[1:]:
+                        acc = acc + w[i] * xv[i]
+                sums.append(acc)
+            if kind == "blocks added in reverse":
+                sums = sums[::-1]
+            if kind == "one chain, no blocks" and kblocks > 1:
+                acc = w[0] * xv[0]
+                for i in range(1, k):
+                    acc = acc + w[i] * xv[i]
+                sums = [acc]
+            if kind == "last row dropped":
+                sums[-1] = sums[-1] - w[k - 1] * xv[k - 1]
+            total = sums[0]
+            for s_ in sums[1:]:
+                total = total + s_
+            out.append(f32_to_bf16_rne(total))
+        return out
+    return gemv
+
+
+GEMV_MUTANTS = ["accumulator starts at +0.0", "products rounded to bf16",
+                "blocks added in reverse", "one chain, no blocks", "last row dropped"]
+
+
+def test_unmutated_gemv_oracle_passes_its_pins():
+    assert _gemv_ok()
+
+
+@pytest.mark.parametrize("kind", GEMV_MUTANTS)
+def test_pins_catch_gemv_mutants(kind, monkeypatch):
+    monkeypatch.setattr(collectives, "gemv_payloads", _gemv_mutant(kind))
+    assert not _gemv_ok(), kind
+
+
+def _tolerance_ok():
+    try:
+        for dt in ("bf16", "f32"):
+            for order in ("rank", "reversed", "tree"):
+                pins.test_any_summation_order_is_within_tolerance(dt, order)
+        pins.test_tolerance_rejects_real_errors()
+    except AssertionError:
+        return False
+    return True
+
+
+@pytest.mark.parametrize("kind", ["ten times looser", "no accumulation term",
+                                  "absolute instead of relative"])
+def test_pins_catch_tolerance_mutants(kind, monkeypatch):
+    from oracle import tolerance
+    orig = tolerance.within_tolerance
+
+    def wrong(got, terms, dtype):
+        n = len(terms)
+        s = tolerance.exact_sum(terms, dtype)
+        S = np.sum([np.abs(arith.to_f32(t, dtype).astype(np.float64)) for t in terms], axis=0)
+        g = (arith.bf16_to_f32(got) if dtype == "bf16"
+             else np.asarray(got, np.float32)).astype(np.float64)
+        rt = tolerance.RTOL[dtype]
+        if kind == "ten times looser":
+            bound = 10 * rt * np.abs(s) + (n - 1) * 2.0 ** -24 * S * (1 + rt)
+        elif kind == "no accumulation term":
+            bound = rt * np.abs(s)
+        else:
+            bound = np.full_like(s, rt)
+        return np.abs(g - s) <= bound
+    assert _tolerance_ok()
+    monkeypatch.setattr(tolerance, "within_tolerance", wrong)
+    assert not _tolerance_ok(), kind
+    monkeypatch.setattr(tolerance, "within_tolerance", orig)
