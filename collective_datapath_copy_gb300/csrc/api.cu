@@ -1,8 +1,11 @@
 // C ABI: plan lifecycle and runs (see include/coll.h for the contract of each call).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
 
+#include <memory>
 #include <new>
 #include <vector>
 
@@ -38,6 +41,10 @@ struct coll_plan_s {
   bool captured = false;  // a run was captured into a graph: status waits for the device
   int last_epochs = 0;
   int gemv_cap = -1;  // co-resident fused-producer CTAs; queried on the first fused run
+  // tensor maps of the last fused run's weight matrices, and what they were encoded for
+  std::unique_ptr<coll::GemvMaps> gmaps;
+  std::vector<const void *> gmaps_wt;
+  uint32_t gmaps_k = 0;
 };
 
 namespace {
@@ -99,6 +106,56 @@ int zero_state(coll_plan_s *p) {
 
 bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
   return a0 < b1 && b0 < a1;
+}
+
+// The driver's tensor-map encoder, looked up once through the runtime (no link to the
+// driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      p = nullptr;
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// Tensor maps of the fused run's weight matrices W_r ([k rows][in_len[r] bf16], rows
+// in_bytes[r] apart), boxes of 256 columns x 16 rows; reused while the run's matrices and
+// k stay the same.
+int gemv_maps(coll_plan_s *p, const void *const *wt, uint32_t k) {
+  const coll_compiled &c = p->c;
+  std::vector<const void *> key(wt, wt + c.R);
+  if (p->gmaps && p->gmaps_k == k && p->gmaps_wt == key) return COLL_OK;
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return COLL_ECUDA;
+  if (!p->gmaps) {
+    p->gmaps.reset(new (std::nothrow) coll::GemvMaps());
+    if (!p->gmaps) return COLL_ENOMEM;
+  }
+  memset(p->gmaps.get(), 0, sizeof(coll::GemvMaps));
+  p->gmaps_wt.clear();
+  for (int r = 0; r < c.R; ++r) {
+    if (!c.in_used[r]) continue;
+    const cuuint64_t dims[2] = {(cuuint64_t)(c.in_bytes[r] / 2), (cuuint64_t)k};
+    const cuuint64_t strides[1] = {(cuuint64_t)c.in_bytes[r]};
+    const cuuint32_t box[2] = {256, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    if (dims[0] > 0xFFFFFFFFull || strides[0] >= (1ull << 40)) return COLL_EINVAL;
+    if (encode(&p->gmaps->m[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(wt[r]),
+               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return COLL_EINVAL;
+  }
+  p->gmaps_wt = key;
+  p->gmaps_k = k;
+  return COLL_OK;
 }
 
 }  // namespace
@@ -214,8 +271,8 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
   const coll_compiled &c = p->c;
   const int R = c.R;
   if (wt) {
-    // eight warps each take k/8 rows, eight at a time: k must be a multiple of 64
-    if (c.cfg.zero_copy || c.dtype != COLL_BF16 || k < 64 || (k & 63u)) return COLL_EINVAL;
+    // eight warps each take k/8 rows, sixteen at a time: k must be a multiple of 128
+    if (c.cfg.zero_copy || c.dtype != COLL_BF16 || k < 128 || (k & 127u)) return COLL_EINVAL;
     if (c.cfg.protocol == COLL_PROTO_LL) return COLL_EINVAL;  // tagged data is not fused
     for (int r = 0; r < R; ++r) {
       if (!c.in_used[r]) continue;
@@ -230,6 +287,7 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
       return COLL_ECUDA;
     }
     if (c.warps.size() > (size_t)p->gemv_cap) return COLL_EINVAL;
+    if (const int e = gemv_maps(p, wt, k)) return e;
   }
   // bytes of one rank's per-epoch input as the kernel reads it
   auto in_span = [&](int r) -> uint64_t { return wt ? (uint64_t)k * 2 : c.in_bytes[r]; };
@@ -388,7 +446,7 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
       }
       a.gemv_k = k;
     }
-    err = coll::launch_engine(c.op, c.dtype, a, s);
+    err = coll::launch_engine(c.op, c.dtype, a, wt ? p->gmaps.get() : nullptr, s);
     if (err == cudaSuccess && !restart) p->epochs_issued += (uint64_t)n_epochs;
   }
   if (err != cudaSuccess) {

@@ -339,15 +339,17 @@ __device__ __forceinline__ uint4 gather_pieces(const char *xb, uint32_t nbytes, 
 // warpgroup (setmaxnreg): the engine's warpgroup takes 248 registers a thread, the compute
 // warpgroups 120, so neither the engine state nor the compute loop spills.
 //
-// The weight rows reach the compute warps through shared-memory slots of 8 rows filled by
-// asynchronous copies; each compute warp owns 6 slots (a private ring) and streams its own
-// k-block through them. Fill q of warp b (its q-th slot of rows over the run: piece
-// q / (k/64), slot q % (k/64) of block b, pieces in epoch-major stage-item order) lands in
-// the warp's slot q % 6; having read fill q, the warp issues fill q + 6 into the same slot.
-// So each warp always has its next 6 slots of rows in flight: while the engine warp runs the
-// exchange of one epoch, the next piece's rows are already arriving (the weights do not
-// depend on the epoch's data), and within a long block a refill has 5 slots of compute to
-// land.
+// The weight rows reach the compute warps through shared-memory slots of 16 rows, each
+// filled by one tensor copy (TMA: a box of 256 columns x 16 rows of W_r, so a ragged last
+// piece reads zeros past the matrix); each compute warp owns 3 slots (a private ring) and
+// streams its own k-block through them. Fill q of warp b (its q-th slot of rows over the run:
+// piece q / (k/128), slot q % (k/128) of block b, pieces in epoch-major stage-item order)
+// lands in the warp's slot q % 3; having read fill q, the warp issues fill q + 3 into the
+// same slot. So each warp always has its next 3 slots (48 rows) in flight: while the engine
+// warp runs the exchange of one epoch, the next piece's rows are already arriving (the
+// weights do not depend on the epoch's data). Few large fills beat many small ones here:
+// streaming rows through shared memory is bound by its bandwidth (every byte is written by
+// the copy and read once), and each fill costs a fixed wait and issue on top.
 constexpr uint32_t kGemvWarps = 8;                                   // compute warps
 constexpr uint32_t kGemvFirst = 4;                                   // warp of compute warp 0
 constexpr uint32_t kGemvThreads = 32 * (kGemvFirst + kGemvWarps);   // 384
@@ -357,12 +359,14 @@ constexpr uint32_t kGemvEngineRegs = 248;  // engine warpgroup after the split
 constexpr uint32_t kGemvComputeRegs = 120; // compute warpgroups after the split
 static_assert(128 * kGemvEngineRegs + 256 * kGemvComputeRegs <= kGemvThreads * kGemvLaunchRegs,
               "the split must fit in the registers the CTA was launched with");
-constexpr uint32_t kGemvRows = 8;                        // weight rows per ring slot
-constexpr uint32_t kGemvPitch = 512;                     // bytes per staged row (a piece is <= 512 B)
+constexpr uint32_t kGemvRows = 16;                       // weight rows per ring slot (one copy)
+constexpr uint32_t kGemvCols = 256;                      // bf16 columns per copied row (a piece)
+constexpr uint32_t kGemvPitch = 2 * kGemvCols;           // bytes per staged row
 constexpr uint32_t kGemvSlotBytes = kGemvRows * kGemvPitch;
-constexpr uint32_t kGemvSlotsPerWarp = 6;
+constexpr uint32_t kGemvSlotsPerWarp = 3;
 constexpr uint32_t kGemvSlots = kGemvSlotsPerWarp * kGemvWarps;  // 192 KiB of rows in flight
-constexpr uint32_t kGemvSmemBytes = kGemvSlots * kGemvSlotBytes + kGemvSlots * 8;
+// (the ring starts 128-byte aligned: the tensor copies land there)
+constexpr uint32_t kGemvSmemBytes = kGemvSlots * kGemvSlotBytes + kGemvSlots * 8 + 128;
 constexpr uint32_t kGemvMaxItems = 16;                   // stage items whose rows are cached
 
 struct GemvShared {
@@ -373,10 +377,10 @@ struct GemvShared {
   uint32_t nitems;   // stage items of this warp, in order
   uint32_t S;        // slots per piece
   uint64_t total;    // fills of the whole run, per compute warp
-  const char *wbase[kGemvMaxItems];  // row 0 of each item's columns
-  int64_t wstride[kGemvMaxItems];
-  uint32_t wbytes[kGemvMaxItems];
-  uint32_t fills[kGemvSlots];        // fills issued per slot
+  const CUtensorMap *maps;                 // W_r of each rank (kernel parameters)
+  const CUtensorMap *wmap[kGemvMaxItems];  // each cached item's matrix ...
+  uint32_t wcol[kGemvMaxItems];            // ... and its first column
+  uint32_t fills[kGemvSlots];              // fills issued per slot
   float part[kGemvWarps][32][8];
 };
 
@@ -393,8 +397,8 @@ struct GemvRing {
 __device__ __forceinline__ GemvRing gemv_ring() {
   extern __shared__ __align__(128) unsigned char gemv_dyn[];
   GemvRing r;
-  r.rows = gemv_dyn;
-  r.full = reinterpret_cast<uint64_t *>(gemv_dyn + kGemvSlots * kGemvSlotBytes);
+  r.rows = gemv_dyn + ((128u - (smem_u32(gemv_dyn) & 127u)) & 127u);
+  r.full = reinterpret_cast<uint64_t *>(r.rows + kGemvSlots * kGemvSlotBytes);
   return r;
 }
 
@@ -402,47 +406,35 @@ __device__ __forceinline__ void gemv_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(kGemvBarThreads) : "memory");
 }
 
-// Where the rows of one fill come from.
+// Where the rows of one fill come from: W_r's tensor map and the piece's first column.
 struct GemvSrc {
-  const char *base;
-  int64_t stride;
-  uint32_t nbytes;
+  const CUtensorMap *map;
+  uint32_t col;
 };
 
 // Rows of item `idx` of this CTA's warp: cached in shared memory for the first items, read
 // from the plan tables beyond that.
 __device__ __forceinline__ GemvSrc gemv_item(const EngArgs &a, const GemvShared &g,
                                              const coll_warp_t &W, uint32_t idx) {
-  if (idx < kGemvMaxItems) return GemvSrc{g.wbase[idx], g.wstride[idx], g.wbytes[idx]};
+  if (idx < kGemvMaxItems) return GemvSrc{g.wmap[idx], g.wcol[idx]};
   const coll_item_t it = a.sitems[W.s0 + idx];
   const coll_unit_t u = a.units[it.unit];
   const coll_ref_t r = a.refs[u.src0 + it.slot];
-  return GemvSrc{a.wt[r.rank] + r.off + u.start, a.wt_stride[r.rank], u.nbytes};
+  return GemvSrc{g.maps + r.rank, (uint32_t)((r.off + u.start) >> 1)};
 }
 
-// Issue one fill into `slot` (all lanes call): rows 8*rj..8*rj+7 of `src`, each lane copying
-// its 16 bytes of every row with cp.async (the load/store unit's asynchronous copy: small
-// strided rows are cheap this way, where one bulk copy per 512-byte row would queue on the
-// bulk-copy unit). Each lane then arrives on the slot's barrier once its copies have landed
-// (32 arrivals complete the fill). Lane 0 counts the fill. The slot must be free: the
-// calling warp has issued its reads of the previous fill (each lane's copies land only in
-// the column that lane read, hundreds of cycles after the shared-memory reads it issued
-// before them).
+// Issue one fill into `slot` (all lanes call; lane 0 issues): rows 16*rj..16*rj+15 of the
+// piece's 256 columns, one tensor copy whose bytes complete the slot's barrier. Lane 0
+// counts the fill. The slot must be free: every lane of the calling warp has finished its
+// reads of the previous fill (their values are in registers and the warp has synchronised).
 __device__ __forceinline__ void gemv_fill(GemvShared &g, const GemvRing &ring, uint32_t slot,
                                           const GemvSrc &src, uint32_t rj, uint32_t lane) {
-  if (lane == 0)
+  if (lane == 0) {
     *reinterpret_cast<volatile uint32_t *>(&g.fills[slot]) = g.fills[slot] + 1u;
-  if (lane * 16u < src.nbytes) {
-    const uint32_t d = smem_u32(ring.rows + slot * kGemvSlotBytes + lane * 16);
-    const char *p = src.base + (int64_t)rj * kGemvRows * src.stride + lane * 16;
-#pragma unroll
-    for (uint32_t t = 0; t < kGemvRows; ++t)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + t * kGemvPitch),
-                   "l"(p + (int64_t)t * src.stride)
-                   : "memory");
+    mbar_expect_tx(&ring.full[slot], kGemvSlotBytes);
+    tensor_load_2d(ring.rows + slot * kGemvSlotBytes, src.map, src.col, rj * kGemvRows,
+                   &ring.full[slot]);
   }
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&ring.full[slot]))
-               : "memory");
 }
 
 // Packed pairs of binary32 (sm_100 family): two IEEE operations, round to nearest even.
@@ -483,86 +475,85 @@ __device__ __forceinline__ void gemv_rows8(uint64_t acc[4], const uint4 w[8], ui
   }
 }
 
-// Position of a compute warp's reads in its private ring, and of the refills it issues.
+// Position of a compute warp's reads in its private ring, and of the refills it issues. It
+// lives across blocks and only ever steps forward (no division on the compute path).
 struct GemvCursor {
-  uint64_t q, lap;  // fill read next: number q, lap q / 6 of the warp's slot q % 6
-  uint32_t slot;    // ring slot (warp base + q % 6)
-  uint32_t rp_j;    // refill q + 6: slot rp_j of the block ...
+  uint64_t q, lap;  // fill read next: number q, lap q / 3 of the warp's slot q % 3
+  uint32_t slot;    // ring slot (warp base + q % 3)
+  uint32_t rp_j;    // refill q + 3: slot rp_j of the block ...
   uint32_t ri;      // ... of stage item ri
   GemvSrc src;      // rows of item ri
 };
 
-// Fill number `q` of compute warp `wid` into its slot (all lanes call).
-__device__ __forceinline__ void gemv_fill_block(GemvShared &g, const GemvRing &ring, uint32_t slot,
-                                                const GemvSrc &src, uint32_t wid, uint32_t bs,
-                                                uint32_t j, uint32_t lane) {
-  gemv_fill(g, ring, slot, src, wid * bs + j, lane);
-}
+// Refills of the next piece's slots, held back until the block's results are handed over:
+// n consecutive fills (consecutive slots of the ring, consecutive refill positions), the
+// first of them into `slot`, slot rj of the block of stage item ri.
+struct GemvPending {
+  uint32_t n, slot, rj, ri;
+  GemvSrc src;
+};
 
-// Compute warp `wid`, before its first block: issue its first 6 fills.
+// Compute warp `wid`, before its first block: issue its first 3 fills and set the cursor
+// (next read: fill 0; next refill: fill 3).
 __device__ void gemv_warp_prologue(const EngArgs &a, GemvShared &g, const GemvRing &ring,
-                                   const coll_warp_t &W, uint32_t wid, uint32_t lane) {
+                                   const coll_warp_t &W, uint32_t wid, uint32_t lane,
+                                   GemvCursor &c) {
   const uint32_t bs = g.S / kGemvWarps;
   uint32_t j = 0, ri = 0;
   GemvSrc src = gemv_item(a, g, W, 0);
-  for (uint32_t q = 0; q < kGemvSlotsPerWarp && q < g.total; ++q) {
-    gemv_fill_block(g, ring, wid * kGemvSlotsPerWarp + q, src, wid, bs, j, lane);
+  for (uint32_t q = 0; q < kGemvSlotsPerWarp; ++q) {
+    if (q < g.total) gemv_fill(g, ring, wid * kGemvSlotsPerWarp + q, src, wid * bs + j, lane);
     if (++j == bs) {
       j = 0;
       if (++ri == g.nitems) ri = 0;
       src = gemv_item(a, g, W, ri);
     }
   }
+  c.q = 0;
+  c.lap = 0;
+  c.slot = wid * kGemvSlotsPerWarp;
+  c.rp_j = j;
+  c.ri = ri;
+  c.src = src;
 }
 
 // This warp's k-block of piece `piece` into g.part[wid][lane], streaming the block's rows
-// through the warp's private ring (see above). The readiness of up to 32 slots is tested at
-// once, so slots that landed during the exchange cost no wait each.
+// through the warp's private ring (see above). The readiness of the slots already issued is
+// tested at once, so slots that landed during the exchange cost no wait each.
 __device__ __forceinline__ void gemv_block(const EngArgs &a, GemvShared &g, const GemvRing &ring,
-                                           const coll_warp_t &W, uint64_t piece, uint32_t wid,
-                                           uint32_t lane) {
+                                           const coll_warp_t &W, uint32_t wid, uint32_t lane,
+                                           GemvCursor &c, GemvPending &pend) {
   const uint32_t bs = g.S / kGemvWarps;  // slots per block
   const uint64_t total = g.total;
   const uint32_t base = wid * kGemvSlotsPerWarp;
-  GemvCursor c;
-  c.q = piece * bs;
-  c.lap = c.q / kGemvSlotsPerWarp;
-  c.slot = base + (uint32_t)(c.q - c.lap * kGemvSlotsPerWarp);
-  // refill q + 6: piece (q + 6) / bs, slot (q + 6) % bs of this warp's block
-  const uint64_t rq = c.q + kGemvSlotsPerWarp;
-  const uint64_t rpiece = rq / bs;  // one division per block
-  c.rp_j = (uint32_t)(rq - rpiece * bs);
-  c.ri = (uint32_t)(rpiece % g.nitems);
-  c.src = gemv_item(a, g, W, c.ri);
   const bool act = lane < g.active;
-  // x of this block: lane t holds the 8 values of slot 32c+t of chunk c, loaded together
+  // x of this block: lane t holds the 16 values of slot 32c+t of chunk c, loaded together
   // (one memory round trip per 32 slots), and each slot's values are broadcast by shuffle
   const char *xp = g.xp + (size_t)wid * bs * (kGemvRows * 2);
   uint64_t acc[4] = {0, 0, 0, 0};
-  uint4 xl = make_uint4(0, 0, 0, 0);
+  uint4 xl[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
   uint32_t ready = 0;  // bit t: the fill of slot 32c+t of this chunk has already landed
-  const uint64_t qe = (piece + 1) * bs;  // first fill of the next piece
+  const uint64_t qe = c.q + bs;  // first fill of the next piece
+  pend.n = 0;
   bool done = true;
   for (uint32_t j = 0; j < bs; ++j) {
     if ((j & 31u) == 0u) {
       // per chunk of 32 slots: one x load and one readiness test per lane, in parallel
-      // (only the fills already issued, at most 6 ahead, can have landed)
+      // (only the fills already issued, at most 3 ahead, can have landed)
       bool r = false;
-      if (j + lane < bs) xl = ld_nc_v4(xp + (size_t)(j + lane) * 16);
+      if (j + lane < bs) {
+        xl[0] = ld_nc_v4(xp + (size_t)(j + lane) * 32);
+        xl[1] = ld_nc_v4(xp + (size_t)(j + lane) * 32 + 16);
+      }
       if (j + lane < bs && lane < kGemvSlotsPerWarp) {
-        const uint64_t ql = c.q + lane;
-        const uint64_t lp = ql / kGemvSlotsPerWarp;
-        const uint32_t sl = base + (uint32_t)(ql - lp * kGemvSlotsPerWarp);
-        r = mbar_test_wait(&ring.full[sl], (uint32_t)(lp & 1u));
+        const uint32_t o = c.slot - base + lane;  // fill c.q + lane: slot o % 3, lap + o / 3
+        const uint32_t wrap = o >= kGemvSlotsPerWarp ? 1u : 0u;
+        r = mbar_test_wait(&ring.full[base + o - wrap * kGemvSlotsPerWarp],
+                           (uint32_t)((c.lap + wrap) & 1u));
       }
       ready = __ballot_sync(FULL, r);
       __syncwarp();  // orders each lane's acquiring test before every lane's reads
     }
-    uint4 xv;
-    xv.x = __shfl_sync(FULL, xl.x, j & 31u);
-    xv.y = __shfl_sync(FULL, xl.y, j & 31u);
-    xv.z = __shfl_sync(FULL, xl.z, j & 31u);
-    xv.w = __shfl_sync(FULL, xl.w, j & 31u);
     bool ok = true;
     if (!((ready >> (j & 31u)) & 1u)) {
       // (this warp issued the fill itself, so the slot's previous phase has completed and
@@ -582,18 +573,38 @@ __device__ __forceinline__ void gemv_block(const EngArgs &a, GemvShared &g, cons
       break;
     }
     const unsigned char *s = ring.rows + c.slot * kGemvSlotBytes + lane * 16;
-    uint4 w[8];
 #pragma unroll
-    for (uint32_t t = 0; t < 8; ++t)
-      w[t] = act ? *reinterpret_cast<const uint4 *>(s + t * kGemvPitch) : make_uint4(0, 0, 0, 0);
-    // A refill this block still needs is issued now, so that the copies overlap this slot's
-    // arithmetic (each lane's copies overwrite only the 16-byte column it has just read,
-    // after its reads in program order); refills for later pieces wait for the end of the
-    // block, so that their copies stream during the exchange instead of competing with
-    // this block's.
-    if (c.q + kGemvSlotsPerWarp < total && c.q + kGemvSlotsPerWarp < qe)
-      gemv_fill_block(g, ring, c.slot, c.src, wid, bs, c.rp_j, lane);
-    if (j == 0) gemv_rows8<true>(acc, w, xv); else gemv_rows8<false>(acc, w, xv);
+    for (uint32_t h = 0; h < 2; ++h) {  // rows 8h..8h+7 of the slot
+      uint4 xv;
+      xv.x = __shfl_sync(FULL, xl[h].x, j & 31u);
+      xv.y = __shfl_sync(FULL, xl[h].y, j & 31u);
+      xv.z = __shfl_sync(FULL, xl[h].z, j & 31u);
+      xv.w = __shfl_sync(FULL, xl[h].w, j & 31u);
+      uint4 w[8];
+#pragma unroll
+      for (uint32_t t = 0; t < 8; ++t)
+        w[t] = act ? *reinterpret_cast<const uint4 *>(s + (8 * h + t) * kGemvPitch)
+                   : make_uint4(0, 0, 0, 0);
+      if (j == 0 && h == 0) gemv_rows8<true>(acc, w, xv); else gemv_rows8<false>(acc, w, xv);
+    }
+    // The slot's rows are in registers and used: once the warp has synchronised, the copy
+    // may overwrite the slot. A refill this block still needs is issued now; refills for
+    // later pieces wait for the end of the block, so that their copies stream during the
+    // exchange instead of competing with this block's.
+    __syncwarp();
+    if (c.q + kGemvSlotsPerWarp < total) {
+      if (c.q + kGemvSlotsPerWarp < qe) {
+        gemv_fill(g, ring, c.slot, c.src, wid * bs + c.rp_j, lane);
+      } else {
+        if (pend.n == 0) {
+          pend.slot = c.slot;
+          pend.rj = c.rp_j;
+          pend.ri = c.ri;
+          pend.src = c.src;
+        }
+        ++pend.n;
+      }
+    }
     ++c.q;
     if (++c.slot == base + kGemvSlotsPerWarp) {
       c.slot = base;
@@ -615,60 +626,53 @@ __device__ __forceinline__ void gemv_block(const EngArgs &a, GemvShared &g, cons
   if (!done && lane == 0) g.fail = 1;
 }
 
-// The refills gemv_block deferred: the last min(6, bs) slots of block `piece`, refilled with
-// fills of later pieces (a division or two each, at most six per block). Issued after the
-// block's results are handed to warp 0, so that their copies stream while it runs the
-// exchange.
-__device__ __forceinline__ void gemv_deferred_refills(const EngArgs &a, GemvShared &g,
-                                                      const GemvRing &ring, const coll_warp_t &W,
-                                                      uint64_t piece, uint32_t wid,
-                                                      uint32_t lane) {
-  const uint32_t bs = g.S / kGemvWarps;
-  const uint64_t qe = (piece + 1) * bs;
-  const uint32_t m = bs < kGemvSlotsPerWarp ? bs : kGemvSlotsPerWarp;
-  for (uint32_t d = 0; d < m; ++d) {
-    const uint64_t q = qe - m + d;             // a slot read in this block
-    const uint64_t t = q + kGemvSlotsPerWarp;  // its refill
-    if (t >= g.total) break;
-    const uint64_t pt = t / bs;
-    const GemvSrc src = gemv_item(a, g, W, (uint32_t)(pt % g.nitems));
-    gemv_fill_block(g, ring, wid * kGemvSlotsPerWarp + (uint32_t)(q % kGemvSlotsPerWarp), src,
-                    wid, bs, (uint32_t)(t - pt * bs), lane);
-  }
-}
-
 // Warp 0, before the epoch loop: cache the stage items' row sources and the run's sizes.
-__device__ void gemv_prologue(const EngArgs &a, const coll_warp_t &W, uint32_t lane) {
+__device__ void gemv_prologue(const EngArgs &a, const CUtensorMap *maps, const coll_warp_t &W,
+                              uint32_t lane) {
   GemvShared &g = gemv_smem();
   const uint32_t nitems = W.s1 - W.s0;
   if (lane == 0) {
     g.nitems = nitems;
     g.S = a.gemv_k / kGemvRows;
     g.total = (uint64_t)a.n_epochs * nitems * (a.gemv_k / (kGemvRows * kGemvWarps));
+    g.maps = maps;
   }
   for (uint32_t idx = lane; idx < nitems && idx < kGemvMaxItems; idx += 32) {
     const coll_item_t it = a.sitems[W.s0 + idx];
     const coll_unit_t u = a.units[it.unit];
     const coll_ref_t r = a.refs[u.src0 + it.slot];
-    g.wbase[idx] = a.wt[r.rank] + r.off + u.start;
-    g.wstride[idx] = a.wt_stride[r.rank];
-    g.wbytes[idx] = u.nbytes;
+    g.wmap[idx] = maps + r.rank;
+    g.wcol[idx] = (uint32_t)((r.off + u.start) >> 1);
   }
 }
 
 // Compute warp `wid` (0..7): compute block wid whenever warp 0 opens a stage, until told to
-// exit.
+// exit. After each block, the refills it held back are issued: their copies stream while
+// warp 0 runs the exchange.
 __device__ void gemv_helper_loop(const EngArgs &a, const coll_warp_t &W, uint32_t wid,
                                  uint32_t lane) {
   GemvShared &g = gemv_smem();
   const GemvRing ring = gemv_ring();
-  gemv_warp_prologue(a, g, ring, W, wid, lane);
-  for (uint64_t piece = 0;; ++piece) {
+  GemvCursor c;
+  GemvPending pend;
+  gemv_warp_prologue(a, g, ring, W, wid, lane, c);
+  for (;;) {
     gemv_bar();
     if (g.exit) return;
-    gemv_block(a, g, ring, W, piece, wid, lane);
+    gemv_block(a, g, ring, W, wid, lane, c, pend);
     gemv_bar();
-    if (!g.fail) gemv_deferred_refills(a, g, ring, W, piece, wid, lane);
+    if (g.fail) continue;
+    const uint32_t bs = g.S / kGemvWarps;
+    const uint32_t base = wid * kGemvSlotsPerWarp;
+    for (uint32_t d = 0; d < pend.n; ++d) {
+      gemv_fill(g, ring, pend.slot, pend.src, wid * bs + pend.rj, lane);
+      if (++pend.slot == base + kGemvSlotsPerWarp) pend.slot = base;
+      if (++pend.rj == bs) {
+        pend.rj = 0;
+        if (++pend.ri == g.nitems) pend.ri = 0;
+        pend.src = gemv_item(a, g, W, pend.ri);
+      }
+    }
   }
 }
 
@@ -770,8 +774,13 @@ __device__ __forceinline__ uint4 spec_attempt(const char *xb, uint32_t nbytes, u
 
 // KIND: 0 copy, 1 sum of bf16, 2 sum of f32. GEMV: fused producer. LL: tagged data.
 // PULL: two-shot pull plans (the publish/pull steps are compiled only into this variant).
+// (the fused producer also takes the tensor maps of the ranks' weight matrices)
+template <bool GEMV> struct MapsArg { using type = NoMaps; };
+template <> struct MapsArg<true> { using type = GemvMaps; };
+
 template <int KIND, bool GEMV, bool LL, bool PULL>
-__global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(const EngArgs a) {
+__global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
+    engine_kernel(const EngArgs a, const __grid_constant__ typename MapsArg<GEMV>::type maps) {
   const uint32_t gw = blockIdx.x;
   const uint32_t lane = threadIdx.x & 31u;
   if constexpr (GEMV) {
@@ -783,13 +792,13 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1) engine_kernel(con
       g.fail = 0;
       for (uint32_t s = 0; s < kGemvSlots; ++s) {
         g.fills[s] = 0;
-        mbar_init(&ring.full[s], 32);  // one arrival per lane of the filling warp
+        mbar_init(&ring.full[s], 1);  // the filling lane's arrival, plus the copy's bytes
       }
       mbar_init_fence();
     }
     __syncthreads();
     if (gw >= a.nwarps) return;  // (every CTA of a launch is a plan warp)
-    if (wid == 0) gemv_prologue(a, a.warps[gw], lane);
+    if (wid == 0) gemv_prologue(a, maps.m, a.warps[gw], lane);
     __syncthreads();  // the item cache and the run's fill count are set
     // The register split: the compute warpgroups shrink, the engine's warpgroup grows. Each
     // role then runs to the end without rejoining the other, so that each is compiled for
@@ -1347,10 +1356,13 @@ cudaError_t launch_probe_rtt(unsigned long long *flags, uint32_t iters, uint32_t
                                      args, 0, s);
 }
 
-cudaError_t launch_engine(int op, int dtype, const EngArgs &a, cudaStream_t s) {
+cudaError_t launch_engine(int op, int dtype, const EngArgs &a, const GemvMaps *maps,
+                          cudaStream_t s) {
   if (a.nwarps == 0 || a.n_epochs == 0) return cudaSuccess;
-  void *args[] = {(void *)&a};
   const bool gemv = a.gemv_k != 0;
+  if (gemv && !maps) return cudaErrorInvalidValue;
+  NoMaps none{0};
+  void *args[] = {(void *)&a, gemv ? (void *)maps : (void *)&none};
   const void *fn = engine_fn(kind_of(op, dtype), gemv, a.protocol == COLL_PROTO_LL, a.rpar != 0);
   if (gemv) {
     const cudaError_t e =

@@ -1,6 +1,7 @@
 // Launch interface between the host API (api.cu) and the kernels (engine.cu).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the type only; maps are encoded through the runtime)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -78,6 +79,15 @@ struct EngArgs {
   int32_t R;
 };
 
+// Fused producer: one 2-D tensor map per rank over W_r ([k rows][in_len[r] bf16 columns],
+// box of 256 columns x 16 rows), passed by value as a kernel parameter.
+struct GemvMaps {
+  CUtensorMap m[COLL_MAX_RANKS];
+};
+struct NoMaps {
+  uint32_t unused;
+};
+
 // Zero-copy: one ordinary launch over all tiles of all epochs.
 cudaError_t launch_zero_copy(int op, int dtype, int oneshot_reuse, const ZcArgs &a, int ctas,
                              cudaStream_t s);
@@ -86,9 +96,10 @@ cudaError_t launch_zero_copy(int op, int dtype, int oneshot_reuse, const ZcArgs 
 cudaError_t launch_bulk(int op, int dtype, const ZcArgs &a, int ctas, cudaStream_t s);
 uint32_t bulk_smem_bytes(uint32_t stages, uint32_t maxsrc, uint32_t slot_bytes);
 
-// Staged Stage/Notify/Consume engine: one cooperative launch of nwarps one-warp CTAs (nine
-// warps each for the fused producer).
-cudaError_t launch_engine(int op, int dtype, const EngArgs &a, cudaStream_t s);
+// Staged Stage/Notify/Consume engine: one cooperative launch of nwarps one-warp CTAs (twelve
+// warps each for the fused producer, which needs `maps`; null otherwise).
+cudaError_t launch_engine(int op, int dtype, const EngArgs &a, const GemvMaps *maps,
+                          cudaStream_t s);
 
 // Flag ping-pong probe between block 0 and block `peer` (cooperative launch).
 cudaError_t launch_probe_rtt(unsigned long long *flags, uint32_t iters, uint32_t peer,
@@ -97,7 +108,7 @@ cudaError_t launch_probe_rtt(unsigned long long *flags, uint32_t iters, uint32_t
 // How many one-warp engine CTAs can be co-resident on the current device.
 cudaError_t engine_max_coresident(int op, int dtype, int protocol, int datapath, int *max_ctas);
 
-// How many fused-producer engine CTAs (nine warps, a 192 KiB weight ring) can be co-resident.
+// How many fused-producer engine CTAs (twelve warps, a 192 KiB weight ring) can be co-resident.
 cudaError_t engine_gemv_max_coresident(bool pull, int *max_ctas);
 
 }  // namespace coll

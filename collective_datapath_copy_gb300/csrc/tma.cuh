@@ -93,4 +93,19 @@ __device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t
       : "memory");
 }
 
+// Tensor copy of one 2-D box (the map's box size) at element coordinates (x, y) from global
+// memory to this CTA's shared memory (128-byte aligned); completion is counted on `bar`'s
+// transaction count. x times the element size must be a multiple of 16 bytes. A slot that
+// threads read before is overwritten only after those reads have completed and the
+// threads have synchronised with the issuing one (as with a consumer's release of a slot
+// to a producer's copy).
+__device__ __forceinline__ void tensor_load_2d(void *sdst, const void *tmap, uint32_t x,
+                                               uint32_t y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(sdst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 }  // namespace coll

@@ -237,11 +237,13 @@ int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_epochs,
  * taken in 8 consecutive blocks of k/8; within a block, products wt[r][i][j] * x_r(i)[i]
  * rounded to binary32 are added in row order from the block's first product (round to
  * nearest even); the 8 block sums are added in block order; one rounding to bf16. Each
- * engine CTA runs eight warps in this mode and stages the weight rows in a 192 KiB
- * shared-memory ring, one CTA per SM. k must be a multiple of 64;
- * in_len[r], wt[r], x[r] and the strides must give 16-byte alignment. Errors as coll_run,
- * plus COLL_EINVAL for a zero-copy, tagged-data or non-bf16 plan, or for a plan with more
- * warps than SMs can hold fused CTAs at once. */
+ * engine CTA runs twelve warps in this mode (eight of them compute) and stages the weight
+ * rows in a 192 KiB shared-memory ring through tensor copies (TMA) of 16 rows, one CTA per
+ * SM. k must be a multiple of 128; in_len[r], wt[r], x[r] and the strides must give
+ * 16-byte alignment, and in_len[r] must be below 2^32. The tensor maps of W_r are encoded
+ * on the host at the first run with these matrices (and again when wt or k change).
+ * Errors as coll_run, plus COLL_EINVAL for a zero-copy, tagged-data or non-bf16 plan, or
+ * for a plan with more warps than SMs can hold fused CTAs at once. */
 int coll_run_gemv(coll_plan_t p, const void *const *wt, void *const *x, int k, void *const *out,
                   int n_epochs, int64_t x_epoch_stride, int x_pool, int64_t out_epoch_stride,
                   void *stream);

@@ -858,7 +858,7 @@ def test_fused_gemv_2000_epochs_under_stagger(chain):
 
 
 def test_fused_gemv_with_a_reduce_scatter_naming_and_bad_arguments():
-    R, n, k = 4, 2048, 64
+    R, n, k = 4, 2048, 128
     wts, xs = _gemv_case(R, n, k, 1, 98)
     ys = collectives.gemv_payloads(wts, [x[0] for x in xs])
     want = collectives.reduce_scatter(ys, "bf16")
@@ -871,7 +871,9 @@ def test_fused_gemv_with_a_reduce_scatter_naming_and_bad_arguments():
     for r in range(R):
         assert bits_equal(from_dev(outs[r], "bf16"), want[r])
     with pytest.raises(cdc.CollError):
-        plan.run_gemv(dw, dx, 12, outs)  # k not a multiple of 64
+        plan.run_gemv(dw, dx, 12, outs)  # k not a multiple of 128
+    with pytest.raises(cdc.CollError):
+        plan.run_gemv(dw, dx, 64, outs)  # nor is 64
     zc = cdc.Plan(namings.allreduce(R, n, "bf16"), zero_copy=1)
     with pytest.raises(cdc.CollError):
         zc.run_gemv(dw, dx, k, [torch.empty(n, dtype=torch.int16, device="cuda") for _ in range(R)])
@@ -880,15 +882,19 @@ def test_fused_gemv_with_a_reduce_scatter_naming_and_bad_arguments():
 
 
 
-@pytest.mark.parametrize("k,n,wpr", [(64, 4096, 0), (1024, 4096, 0), (512, 4096, 2), (128, 1000, 0),
-                                     (8192, 1024, 0), (64, 4352, 1)],
-                         ids=["k64-several-pieces-per-ring-lap", "k1024-ring-wraps-inside-a-piece",
+@pytest.mark.parametrize("k,n,wpr", [(128, 4096, 0), (1024, 4096, 0), (512, 4096, 2),
+                                     (128, 1000, 0), (256, 1000, 0), (8192, 1024, 0),
+                                     (128, 4352, 1), (384, 4096, 0)],
+                         ids=["k128-several-pieces-per-ring-lap", "k1024-ring-wraps-inside-a-piece",
                               "k512-four-pieces-per-warp", "k128-ragged-last-piece",
-                              "k8192-largest-x", "k64-seventeen-pieces-per-warp"])
+                              "k256-ragged-last-piece-two-fills", "k8192-largest-x",
+                              "k128-seventeen-pieces-per-warp", "k384-three-fills-per-block"])
 def test_fused_gemv_weight_ring_shapes(k, n, wpr):
-    # The streaming warp fills a 48-slot ring (8 weight rows per slot) ahead of the compute
-    # warps; these shapes cover a ring lap holding several pieces, a piece longer than the
-    # ring, warps with several stage items, and a last piece shorter than 512 bytes.
+    # Each compute warp streams its rows through a private ring of 3 slots (16 weight rows
+    # per slot, one tensor copy each); these shapes cover a ring lap holding several pieces,
+    # a piece longer than the ring, warps with several stage items (more than the 16 whose
+    # sources are cached), a block as long as the ring, and a last piece shorter than 512
+    # bytes, whose copies read zeros past the matrix.
     R, pool, E = 4, 2, 6
     wts, xs = _gemv_case(R, n, k, pool, 99 + k)
     want = [collectives.allreduce(collectives.gemv_payloads(wts, [xs[r][e] for r in range(R)]),
@@ -929,7 +935,7 @@ def test_fused_gemv_signed_zeros():
 
 def test_fused_gemv_rejects_a_plan_wider_than_the_gpu_and_keeps_the_plain_run():
     # 8 ranks x 32 KiB: 512 one-warp engine CTAs fit at once, 512 fused CTAs (one per SM) do not
-    R, n, k = 8, 16384, 64
+    R, n, k = 8, 16384, 128
     nm = namings.allreduce(R, n, "bf16")
     plan = cdc.Plan(nm, protocol="dual")
     assert plan.info.n_warps > torch.cuda.get_device_properties(0).multi_processor_count
