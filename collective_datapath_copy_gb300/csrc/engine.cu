@@ -1365,9 +1365,20 @@ cudaError_t launch_engine(int op, int dtype, const EngArgs &a, const GemvMaps *m
   void *args[] = {(void *)&a, gemv ? (void *)maps : (void *)&none};
   const void *fn = engine_fn(kind_of(op, dtype), gemv, a.protocol == COLL_PROTO_LL, a.rpar != 0);
   if (gemv) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmemBytes);
-    if (e != cudaSuccess) return e;
+    // (once per variant: the attribute stays set, and a stream capture then records the
+    // launch alone)
+    static bool smem_set[64][2] = {};
+    int dev = 0;
+    const cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return de;
+    bool scratch = false;
+    bool &set = dev >= 0 && dev < 64 ? smem_set[dev][a.rpar != 0 ? 1 : 0] : scratch;
+    if (!set) {
+      const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)kGemvSmemBytes);
+      if (e != cudaSuccess) return e;
+      set = true;
+    }
   }
   return cudaLaunchCooperativeKernel(fn, dim3(a.nwarps), dim3(gemv ? kGemvThreads : 32), args,
                                      gemv ? kGemvSmemBytes : 0, s);

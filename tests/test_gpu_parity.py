@@ -632,6 +632,54 @@ def test_staged_plan_replays_inside_a_cuda_graph(cfg):
     plan.free()
 
 
+def test_fused_run_replays_inside_a_cuda_graph_and_follows_new_weights():
+    # the weight matrices' tensor maps travel as kernel parameters: a captured fused run keeps
+    # the maps it was captured with, and a direct run with other matrices (or another k)
+    # re-encodes them
+    R, n, k, E = 4, 2048, 256, 3
+    nm = namings.allreduce(R, n, "bf16")
+    plan = cdc.Plan(nm, protocol="spec")
+    rng = synth.seeded_rng(610)
+    wts = [synth.normal_bf16(rng, (k, n)) for _ in range(R)]
+    dw = [to_dev(w.ravel(), "bf16") for w in wts]
+    xs_dev = [torch.zeros(E, k, dtype=torch.int16, device="cuda") for _ in range(R)]
+    outs = [torch.zeros(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    kw = dict(n_epochs=E, x_epoch_stride=2 * k, x_pool=E, out_epoch_stride=2 * n)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        plan.run_gemv(dw, xs_dev, k, outs, **kw)  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        plan.run_gemv(dw, xs_dev, k, outs, **kw)
+    for rep in range(2):
+        xs = [[synth.normal_bf16(rng, k) for _ in range(E)] for _ in range(R)]
+        for r in range(R):
+            xs_dev[r].copy_(torch.stack([to_dev(x, "bf16") for x in xs[r]]))
+        g.replay()
+        torch.cuda.synchronize()
+        assert plan.status()["code"] == 0, rep
+        for e in range(E):
+            want = collectives.allreduce(
+                collectives.gemv_payloads(wts, [xs[r][e] for r in range(R)]), "bf16")[0]
+            for r in range(R):
+                assert bits_equal(from_dev(outs[r][e], "bf16"), want), (rep, e, r)
+    # other matrices, then a smaller k over the same matrices' first rows
+    wts2 = [synth.normal_bf16(rng, (k, n)) for _ in range(R)]
+    dw2 = [to_dev(w.ravel(), "bf16") for w in wts2]
+    for wl, dl, kk in ((wts2, dw2, k), (wts2, dw2, 128)):
+        xs = [synth.normal_bf16(rng, kk) for _ in range(R)]
+        plan.run_gemv(dl, [to_dev(x, "bf16") for x in xs], kk, [o[0] for o in outs])
+        assert plan.status()["code"] == 0
+        want = collectives.allreduce(
+            collectives.gemv_payloads([w[:kk] for w in wl], xs), "bf16")[0]
+        for r in range(R):
+            assert bits_equal(from_dev(outs[r][0], "bf16"), want), (kk, r)
+    plan.free()
+
+
 @pytest.mark.parametrize("seed", range(16))
 def test_bulk_ring_on_small_aligned_namings(seed):
     # force the bulk-copy (TMA) ring on small random namings (segments scaled to 16 bytes)
