@@ -154,7 +154,8 @@ class Plan:
     def run_gemv(self, wts, xs, k, outs, n_epochs=1, x_epoch_stride=0, x_pool=1,
                  out_epoch_stride=0, stream=None):
         """Fused producer: each rank's payload is W_r x_r computed inside the engine.
-        wts[r]: [k, in_len[r]] bf16 (W_r transposed); xs[r]: x vectors (k bf16 per epoch)."""
+        wts[r]: [k, in_len[r]] bf16 (W_r transposed); xs[r]: x vectors (k bf16 per epoch);
+        k a multiple of 128 (coll_run_gemv has the full contract)."""
         R = self.naming.R
         self._check(xs, outs, n_epochs, x_epoch_stride, x_pool, out_epoch_stride,
                     in_bytes=[2 * int(k)] * R)
