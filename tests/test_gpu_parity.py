@@ -243,6 +243,35 @@ def _check_epochs(outs, expect_dev, n_epochs, pool):
     return bad
 
 
+@pytest.mark.parametrize("cfg", [
+    dict(protocol="spec"),
+    dict(protocol="spec", inject="stagger", inject_seed=11, inject_prob_ppm=100000,
+         inject_max_ns=20000, inject_start_ns=5000),
+    dict(protocol="spec", spec_check="relaxed", inject="stagger", inject_seed=12,
+         inject_prob_ppm=100000, inject_max_ns=20000, inject_start_ns=5000),
+    dict(protocol="ll", inject="stagger", inject_seed=13, inject_prob_ppm=100000,
+         inject_max_ns=20000, inject_start_ns=5000)],
+    ids=["spec", "spec-stagger", "spec-relaxed-stagger", "ll-stagger"])
+def test_decode_allreduce_300000_epochs_soak(cfg):
+    # 30 runs of 10,000 epochs on one plan (epochs 1..300,000: the 16-bit epoch fields of
+    # the flag words wrap four times), every epoch of every run checked against the oracle
+    R, n, pool, E, runs = 8, 4096, 7, 10000, 30
+    ins, expect = _decode_case(R, n, pool, seed=21)
+    plan = cdc.Plan(namings.allreduce(R, n, "bf16"), **cfg)
+    outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    for run in range(runs):
+        for o in outs:
+            o.fill_(-1)
+        plan.run(ins, outs, n_epochs=E, in_epoch_stride=n * 2, in_pool=pool,
+                 out_epoch_stride=n * 2)
+        st = plan.status()
+        assert st["code"] == 0, (run, st)
+        # (each run counts its inputs from the pool's first set; the flag epochs go on)
+        assert _check_epochs(outs, expect, E, pool) == 0, run
+    assert plan.status()["epochs"] == E * runs
+    plan.free()
+
+
 @pytest.mark.parametrize("protocol", ["barrier", "dual", "spec", "ll"])
 @pytest.mark.parametrize("datapath", ["oneshot", "twoshot", "twoshot_pull"])
 @pytest.mark.parametrize("chain", [0, 1])
