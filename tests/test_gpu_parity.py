@@ -1010,6 +1010,45 @@ def test_fused_gemv_signed_zeros():
         plan.free()
 
 
+@pytest.mark.parametrize("unsafe", ["weights", "x"])
+def test_fused_gemv_product_overflow_keeps_the_separate_rounding(unsafe):
+    # Each product is rounded to binary32 before it is added. Here one output's products are
+    # -(2-2^-7)*2^127 and then 2^128, which overflows when rounded alone: multiply-then-add
+    # gives +inf, where a fused multiply-add would give 2^120. The large magnitudes sit in
+    # the weights, or in one epoch's x.
+    R, n, k, E = 2, 256, 128, 3
+    rng = synth.seeded_rng(94)
+    wts = [synth.normal_bf16(rng, (k, n)) for _ in range(R)]
+    xs = [[synth.normal_bf16(rng, k) for _ in range(E)] for _ in range(R)]
+    for r in range(R):
+        wts[r][:, 0] = 0
+    if unsafe == "weights":
+        wts[0][0, 0], wts[0][1, 0] = 0xE07F, 0x6080    # -(2-2^-7)*2^65, 2^66
+        for r in range(R):
+            for e in range(E):
+                xs[r][e][0] = xs[r][e][1] = 0x5E80     # 2^62
+    else:
+        wts[0][0, 0], wts[0][1, 0] = 0xDEFF, 0x5E80    # -(2-2^-7)*2^62, 2^62
+        xs[0][1][0], xs[0][1][1] = 0x6000, 0x6080      # epoch 1: 2^65, 2^66
+    want = [collectives.allreduce(collectives.gemv_payloads(wts, [xs[r][e] for r in range(R)]),
+                                  "bf16")[0] for e in range(E)]
+    if unsafe == "weights":
+        assert all(w[0] == 0x7F80 for w in want)
+    else:
+        assert want[1][0] == 0x7F80 and want[0][0] != 0x7F80
+    plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="dual")
+    dw = [to_dev(w.ravel(), "bf16") for w in wts]
+    dx = [torch.stack([to_dev(x, "bf16") for x in xs[r]]).contiguous() for r in range(R)]
+    outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    plan.run_gemv(dw, dx, k, outs, n_epochs=E, x_epoch_stride=2 * k, x_pool=E,
+                  out_epoch_stride=2 * n)
+    assert plan.status()["code"] == 0
+    for e in range(E):
+        for r in range(R):
+            assert bits_equal(from_dev(outs[r][e], "bf16"), want[e]), (e, r)
+    plan.free()
+
+
 def test_fused_gemv_rejects_a_plan_wider_than_the_gpu_and_keeps_the_plain_run():
     # 8 ranks x 32 KiB: 512 one-warp engine CTAs fit at once, 512 fused CTAs (one per SM) do not
     R, n, k = 8, 16384, 128
