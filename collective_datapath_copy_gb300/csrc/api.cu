@@ -279,7 +279,7 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
       if (!wt[r]) return COLL_EINVAL;
       if (((uintptr_t)wt[r] & 15u) || (c.in_bytes[r] & 15u)) return COLL_EALIGN;
     }
-    // the fused CTAs are larger (nine warps and a shared-memory ring): all must still fit
+    // the fused CTAs are larger (twelve warps and a shared-memory ring): all must still fit
     if (p->gemv_cap < 0 &&
         coll::engine_gemv_max_coresident(c.rpar_bytes != 0, &p->gemv_cap) != cudaSuccess) {
       cudaGetLastError();
