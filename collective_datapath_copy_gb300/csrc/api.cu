@@ -41,6 +41,7 @@ struct coll_plan_s {
   bool captured = false;  // a run was captured into a graph: status waits for the device
   int last_epochs = 0;
   int gemv_cap = -1;  // co-resident fused-producer CTAs; queried on the first fused run
+  bool single_items = false;  // every warp has one stage and one consume item
   // tensor maps of the last fused run's weight matrices, and what they were encoded for
   std::unique_ptr<coll::GemvMaps> gmaps;
   std::vector<const void *> gmaps_wt;
@@ -243,6 +244,9 @@ extern "C" int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_
     }
   }
   if (ok) ok = zero_state(p) == COLL_OK;
+  p->single_items = !c.warps.empty();
+  for (const coll_warp_t &w : c.warps)
+    if (w.s1 - w.s0 != 1 || w.c1 - w.c0 != 1) p->single_items = false;
   if (!ok) {
     cudaGetLastError();
     release(p);
@@ -439,6 +443,7 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
     a.inject_start_ns = c.cfg.inject_start_ns;
     a.inject_pause_ns = c.cfg.inject_pause_ns;
     a.R = R;
+    a.single_items = p->single_items ? 1u : 0u;
     if (wt) {
       for (int r = 0; r < R; ++r) {
         a.wt[r] = static_cast<const char *>(wt[r]);

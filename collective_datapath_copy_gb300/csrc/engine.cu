@@ -774,13 +774,22 @@ __device__ __forceinline__ uint4 spec_attempt(const char *xb, uint32_t nbytes, u
 
 // KIND: 0 copy, 1 sum of bf16, 2 sum of f32. GEMV: fused producer. LL: tagged data.
 // PULL: two-shot pull plans (the publish/pull steps are compiled only into this variant).
+// FP: 0 for the general engine; otherwise a variant for plans whose every warp has one
+// stage item and one consume item, run without fault injection, stamps or chained epochs,
+// under one speculative protocol known at compile time (1 with content tags, 2 the same
+// fence-free). On the single warp that carries a piece through an epoch, every runtime mode
+// test is a dependent instruction on the critical path; compiled out, the decode epoch
+// drops by about a sixth. (A dual-buffer variant measured slower than the general engine
+// and is not built.)
 // (the fused producer also takes the tensor maps of the ranks' weight matrices)
 template <bool GEMV> struct MapsArg { using type = NoMaps; };
 template <> struct MapsArg<true> { using type = GemvMaps; };
 
-template <int KIND, bool GEMV, bool LL, bool PULL>
+template <int KIND, bool GEMV, bool LL, bool PULL, int FP>
 __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
     engine_kernel(const EngArgs a, const __grid_constant__ typename MapsArg<GEMV>::type maps) {
+  static_assert(FP == 0 || (!GEMV && !LL && !PULL), "the specialised variants are plain");
+  constexpr bool fast = FP != 0;
   const uint32_t gw = blockIdx.x;
   const uint32_t lane = threadIdx.x & 31u;
   if constexpr (GEMV) {
@@ -815,19 +824,22 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
   }
   const coll_warp_t W = a.warps[gw];
   coll_dev_status_t *st = a.st;
-  const bool spec_proto = a.protocol == COLL_PROTO_SPEC;
+  const bool spec_proto = fast || a.protocol == COLL_PROTO_SPEC;
+  const bool barrier_proto = !fast && a.protocol == COLL_PROTO_BARRIER;
   constexpr bool ll = LL;
   const uint32_t slot_mult = ll ? 2u : 1u;  // tagged-data slots are twice the payload
   // content tags: validated by the tagged checks, stored by every spec producer
-  const bool literal = spec_proto && a.spec_check == COLL_SPEC_LITERAL;
-  const bool relaxed = spec_proto && a.spec_check == COLL_SPEC_TAGGED_RELAXED;
+  const bool literal = !fast && spec_proto && a.spec_check == COLL_SPEC_LITERAL;
+  const bool relaxed = fast ? FP == 2 : spec_proto && a.spec_check == COLL_SPEC_TAGGED_RELAXED;
   const bool tagged = spec_proto && !literal;
-  const bool skip_notify =
-      (a.inject_flags & COLL_INJECT_SKIP_NOTIFY) && (int)W.rank == a.inject_rank;
-  const bool pause_consumer =
-      (a.inject_flags & COLL_INJECT_SPEC_PAUSE) && (int)W.rank == a.inject_rank;
-  const bool delay_producer = (a.inject_flags & COLL_INJECT_SPEC_PAUSE) &&
+  const bool skip_notify = !fast && (a.inject_flags & COLL_INJECT_SKIP_NOTIFY) &&
+                           (int)W.rank == a.inject_rank;
+  const bool pause_consumer = !fast && (a.inject_flags & COLL_INJECT_SPEC_PAUSE) &&
+                              (int)W.rank == a.inject_rank;
+  const bool delay_producer = !fast && (a.inject_flags & COLL_INJECT_SPEC_PAUSE) &&
                               (int)W.rank == (a.inject_rank + 1) % a.R;
+  const bool chained = !fast && a.chain && a.rank_done;
+  const bool stagger = !fast && (a.inject_flags & COLL_INJECT_STAGGER);
   uint32_t n_checks = 0, n_retries = 0;
   bool failed = false;
   uint64_t gpiece = 0;  // fused producer: pieces computed so far
@@ -836,7 +848,8 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
   // during the kernel) and hashes it while its own consume waits on memory, which takes
   // the input load and the producer-side tag off the critical path.
   constexpr bool gemv = GEMV;
-  const bool single_s = (W.s1 - W.s0) == 1u;
+  const bool single_s = fast || (W.s1 - W.s0) == 1u;
+  const uint32_t s_end = fast ? W.s0 + 1u : W.s1;
   const bool pipelined = single_s && !gemv;
   coll_unit_t su;
   coll_ref_t sref;
@@ -845,7 +858,8 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
   // unit and its output reference in registers: the plan tables are then read once, not
   // once per epoch (acquire loads may invalidate L1, which would make every table read an
   // L2 round trip on the critical path).
-  const bool single_c = (W.c1 - W.c0) == 1u;
+  const bool single_c = fast || (W.c1 - W.c0) == 1u;
+  const uint32_t c_end = fast ? W.c0 + 1u : W.c1;
   coll_item_t cit;
   coll_unit_t cu;
   coll_ref_t cref;
@@ -871,9 +885,9 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
       nx = ld_nc_v4(a.ptr.in[sref.rank] + sref.off + su.start + lane * 16);
   }
 
-  if ((a.inject_flags & COLL_INJECT_STAGGER) && a.inject_start_ns)
+  if (stagger && a.inject_start_ns)
     spin_ns((uint64_t)W.rank * a.inject_start_ns);
-  const bool stamp = gw == 0 && lane == 0 && a.stamps;
+  const bool stamp = !fast && gw == 0 && lane == 0 && a.stamps;
   const bool phases = stamp && a.stamp_phases;
   if (stamp) a.stamps[0] = globaltimer();
 
@@ -883,7 +897,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
   int32_t pool_next = a.in_pool > 1 ? 1 : 0;
   for (int i = 0; i < a.n_epochs && !failed; ++i) {
     const uint32_t E = a.epoch_base + (uint32_t)i + 1u;
-    const uint32_t b = (a.protocol == COLL_PROTO_BARRIER) ? 0u : (E & 1u);
+    const uint32_t b = barrier_proto ? 0u : (E & 1u);
     if (i > 0) {
       in_off = in_off_next;
       pool_next = pool_next + 1 == a.in_pool ? 0 : pool_next + 1;
@@ -891,14 +905,14 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
     }
     const int64_t out_off = (int64_t)i * a.out_stride;
 
-    if ((a.inject_flags & COLL_INJECT_STAGGER) && a.inject_prob_ppm) {
+    if (stagger && a.inject_prob_ppm) {
       const uint64_t h = splitmix64(a.inject_seed ^ ((uint64_t)E * 0xD1B54A32D192ED03ull));
       if ((h % 1000000ull) < a.inject_prob_ppm && W.rank == (uint32_t)((h >> 40) % (uint64_t)a.R))
         spin_ns(splitmix64(h) % (a.inject_max_ns + 1));
     }
 
     const bool pst = phases && (uint32_t)i < a.stamp_cap;
-    if (a.chain && a.rank_done) {
+    if (chained) {
       // dependent chain: wait until every warp of this rank finished epoch E-1's consume
       bool ok = true;
       if (lane == 0) {
@@ -924,12 +938,12 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
     if (pst) a.stamps[1 + 4 * i] = globaltimer();
 
     // ---------------- Stage + Notify
-    for (uint32_t s = W.s0; s < W.s1; ++s) {
+    for (uint32_t s = W.s0; s < s_end; ++s) {
       const coll_item_t it = single_s ? sit : a.sitems[s];
       const coll_unit_t u = single_s ? su : a.units[it.unit];
-      if (a.protocol == COLL_PROTO_BARRIER || (u.flags & COLL_UNIT_REUSE_WAIT)) {
+      if (barrier_proto || (u.flags & COLL_UNIT_REUSE_WAIT)) {
         // bottom barrier (single buffer) / explicit reuse wait (dual buffers)
-        const uint32_t target = E - (a.protocol == COLL_PROTO_BARRIER ? 1u : 2u);
+        const uint32_t target = E - (barrier_proto ? 1u : 2u);
         if (!wait_consumers_done(a.cflag + u.cflag0, u.ncflag, target, st, a.spin_ns)) {
           if (lane == 0) record_timeout(st, (int)W.rank, (int)it.unit, 1, E);
           failed = true;
@@ -997,7 +1011,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
     if (pst) a.stamps[2 + 4 * i] = globaltimer();
 
     // ---------------- Consume
-    for (uint32_t c = W.c0; c < W.c1; ++c) {
+    for (uint32_t c = W.c0; c < c_end; ++c) {
       const coll_item_t it = single_c ? cit : a.citems[c];
       const coll_unit_t u = single_c ? cu : a.units[it.unit];
       const uint32_t n = u.nsrc;
@@ -1152,7 +1166,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
       if (PULL && (u.flags & COLL_UNIT_PULL)) {
         // two-shot pull: publish the reduced piece in this parity's slot of rbuf, once
         // every consumer has pulled the piece it held before (the two-shot bottom barrier)
-        const uint32_t target = E - (a.protocol == COLL_PROTO_BARRIER ? 1u : 2u);
+        const uint32_t target = E - (barrier_proto ? 1u : 2u);
         if (!wait_consumers_done(a.dflag + u.dflag0, u.ndst, target, st, a.spin_ns)) {
           if (lane == 0) record_timeout(st, (int)W.rank, (int)it.unit, 7, E);
           failed = true;
@@ -1174,7 +1188,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
           st_v4(a.ptr.out[r.rank] + r.off + out_off + u.start + lane * 16, res);
         }
       }
-      if (a.protocol == COLL_PROTO_BARRIER || (u.flags & COLL_UNIT_DONE_FLAGS)) {
+      if (barrier_proto || (u.flags & COLL_UNIT_DONE_FLAGS)) {
         __syncwarp();
         if (lane == 0)
           st_release_u32(a.cflag + u.cflag0 + (it.slot == COLL_SLOT_ALL ? 0u : it.slot), E);
@@ -1203,7 +1217,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
       if (lane == 0) st_release_u32(a.dflag + u.dflag0 + it.slot, E);  // read: may reuse
     }
     if (failed) break;
-    if (a.chain && a.rank_done) {
+    if (chained) {
       __syncwarp();
       if (lane == 0) red_release_add_u32(a.rank_done + W.rank, 1u);
     }
@@ -1293,38 +1307,61 @@ cudaError_t launch_zero_copy(int op, int dtype, int keep, const ZcArgs &a, int c
   return cudaGetLastError();
 }
 
-static const void *engine_fn(int kind, bool gemv, bool ll, bool pull) {
-  if (gemv) return pull ? (const void *)engine_kernel<1, true, false, true>
-                        : (const void *)engine_kernel<1, true, false, false>;
+static const void *engine_fn(int kind, bool gemv, bool ll, bool pull, int fp = 0) {
+  if (gemv) return pull ? (const void *)engine_kernel<1, true, false, true, 0>
+                        : (const void *)engine_kernel<1, true, false, false, 0>;
   if (ll) {
     switch (kind) {
-      case 0: return (const void *)engine_kernel<0, false, true, false>;
-      case 1: return (const void *)engine_kernel<1, false, true, false>;
-      default: return (const void *)engine_kernel<2, false, true, false>;
+      case 0: return (const void *)engine_kernel<0, false, true, false, 0>;
+      case 1: return (const void *)engine_kernel<1, false, true, false, 0>;
+      default: return (const void *)engine_kernel<2, false, true, false, 0>;
     }
   }
   if (pull && kind != 0)  // (pull plans are sums)
-    return kind == 1 ? (const void *)engine_kernel<1, false, false, true>
-                     : (const void *)engine_kernel<2, false, false, true>;
+    return kind == 1 ? (const void *)engine_kernel<1, false, false, true, 0>
+                     : (const void *)engine_kernel<2, false, false, true, 0>;
+  if (fp != 0 && kind != 0) {  // (the specialised variants are sums)
+    switch ((kind - 1) * 2 + fp) {
+      case 1: return (const void *)engine_kernel<1, false, false, false, 1>;
+      case 2: return (const void *)engine_kernel<1, false, false, false, 2>;
+      case 3: return (const void *)engine_kernel<2, false, false, false, 1>;
+      default: return (const void *)engine_kernel<2, false, false, false, 2>;
+    }
+  }
   switch (kind) {
-    case 0: return (const void *)engine_kernel<0, false, false, false>;
-    case 1: return (const void *)engine_kernel<1, false, false, false>;
-    default: return (const void *)engine_kernel<2, false, false, false>;
+    case 0: return (const void *)engine_kernel<0, false, false, false, 0>;
+    case 1: return (const void *)engine_kernel<1, false, false, false, 0>;
+    default: return (const void *)engine_kernel<2, false, false, false, 0>;
   }
 }
 
+// The specialised variant a run of these arguments may use (0: the general engine).
+static int engine_fp(int kind, const EngArgs &a) {
+  if (kind == 0 || a.gemv_k != 0 || a.rpar != 0 || !a.single_items || a.inject_flags != 0 ||
+      a.stamps != nullptr || a.dbg != nullptr || (a.chain && a.rank_done))
+    return 0;
+  if (a.protocol == COLL_PROTO_SPEC && a.spec_check == COLL_SPEC_TAGGED) return 1;
+  if (a.protocol == COLL_PROTO_SPEC && a.spec_check == COLL_SPEC_TAGGED_RELAXED) return 2;
+  return 0;
+}
+
 cudaError_t engine_max_coresident(int op, int dtype, int protocol, int datapath, int *max_ctas) {
-  int dev = 0, sms = 0, per_sm = 0;
+  int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm,
-      engine_fn(kind_of(op, dtype), false, protocol == COLL_PROTO_LL,
-                datapath == COLL_DP_TWOSHOT_PULL),
-      32, 0);
-  if (e != cudaSuccess) return e;
+  const int kind = kind_of(op, dtype);
+  const bool ll = protocol == COLL_PROTO_LL, pull = datapath == COLL_DP_TWOSHOT_PULL;
+  // a run may use a specialised variant: every variant it may use must fit
+  int per_sm = 1 << 30;
+  for (int fp = 0; fp <= ((kind != 0 && !ll && !pull) ? 2 : 0); ++fp) {
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, engine_fn(kind, false, ll, pull, fp),
+                                                      32, 0);
+    if (e != cudaSuccess) return e;
+    per_sm = n < per_sm ? n : per_sm;
+  }
   *max_ctas = per_sm * sms;
   return cudaSuccess;
 }
@@ -1363,7 +1400,9 @@ cudaError_t launch_engine(int op, int dtype, const EngArgs &a, const GemvMaps *m
   if (gemv && !maps) return cudaErrorInvalidValue;
   NoMaps none{0};
   void *args[] = {(void *)&a, gemv ? (void *)maps : (void *)&none};
-  const void *fn = engine_fn(kind_of(op, dtype), gemv, a.protocol == COLL_PROTO_LL, a.rpar != 0);
+  const int kind = kind_of(op, dtype);
+  const void *fn =
+      engine_fn(kind, gemv, a.protocol == COLL_PROTO_LL, a.rpar != 0, engine_fp(kind, a));
   if (gemv) {
     // (once per variant: the attribute stays set, and a stream capture then records the
     // launch alone)

@@ -77,6 +77,7 @@ struct EngArgs {
   uint64_t inject_start_ns;
   uint64_t inject_pause_ns;
   int32_t R;
+  uint32_t single_items;  // 1: every warp has one stage item and one consume item
 };
 
 // Fused producer: one 2-D tensor map per rank over W_r ([k rows][in_len[r] bf16 columns],
