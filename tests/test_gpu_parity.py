@@ -272,6 +272,34 @@ def test_decode_allreduce_300000_epochs_soak(cfg):
     plan.free()
 
 
+@pytest.mark.parametrize("check", ["tagged", "relaxed"])
+def test_specialised_and_stamped_engines_agree(check):
+    # a plain speculative run of the decode plan takes the variant specialised for it; the
+    # same plan with per-epoch stamps runs the general engine: both give the oracle's bits,
+    # and the stamps advance with every epoch
+    R, n, pool, E = 8, 4096, 7, 1000
+    ins, expect = _decode_case(R, n, pool, seed=23)
+    nm = namings.allreduce(R, n, "bf16")
+    got = []
+    for cfg in (dict(), dict(record_stamps=1, stamp_capacity=E),
+                dict(record_stamps=2, stamp_capacity=E)):
+        plan = cdc.Plan(nm, protocol="spec", spec_check=check, **cfg)
+        outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+        plan.run(ins, outs, n_epochs=E, in_epoch_stride=n * 2, in_pool=pool,
+                 out_epoch_stride=n * 2)
+        assert plan.status()["code"] == 0, cfg
+        assert _check_epochs(outs, expect, E, pool) == 0, cfg
+        if cfg:
+            per = 4 if cfg["record_stamps"] == 2 else 1
+            st = plan.stamps(E).astype(np.int64)
+            assert len(st) == per * E + 1
+            assert (np.diff(st[1:].reshape(E, per)[:, 0]) > 0).all()
+        got.append(outs)
+        plan.free()
+    for a, b in zip(got[0], got[1]):
+        assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("protocol", ["barrier", "dual", "spec", "ll"])
 @pytest.mark.parametrize("datapath", ["oneshot", "twoshot", "twoshot_pull"])
 @pytest.mark.parametrize("chain", [0, 1])
