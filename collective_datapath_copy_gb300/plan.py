@@ -68,6 +68,7 @@ def _check_buffers(R, tensors, used, nbytes, stride, count, where):
     is a CUDA tensor whose storage holds all the bytes the run reads or writes there:
     nbytes[r] at each of `count` epochs spaced `stride` bytes apart. A tensor that is too
     small would otherwise be overrun on the device."""
+    reach = int(stride) * (int(count) - 1) if count > 1 else 0
     for r in range(R):
         if not used[r]:
             continue
@@ -76,9 +77,11 @@ def _check_buffers(R, tensors, used, nbytes, stride, count, where):
             continue  # the library rejects a missing buffer itself
         if not t.is_cuda:
             raise ValueError(f"{where}: buffer of rank {r} is not a CUDA tensor")
+        need = reach + int(nbytes[r])
+        if reach >= 0 and need <= t.nbytes and t.is_contiguous():
+            continue  # within the tensor's own bytes (the common case: no storage lookup)
         st = t.untyped_storage()
         s0, s1 = st.data_ptr(), st.data_ptr() + st.nbytes()
-        reach = int(stride) * (int(count) - 1) if count > 1 else 0
         lo = t.data_ptr() + min(0, reach)
         hi = t.data_ptr() + max(0, reach) + int(nbytes[r])
         if lo < s0 or hi > s1:
