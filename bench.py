@@ -466,6 +466,42 @@ def cpu_baseline_all_cores(seconds=5.0):
                       f"throughput, not one epoch's latency"}
 
 
+def cpu_oracle_collectives(m_bytes=4 << 20, seconds=0.5, R=8):
+    """The oracle timed on the host for the sweep's collectives: each collective of M bytes
+    of bf16 per rank (a bounded sample of the sweep's sizes) repeated for about `seconds`,
+    reported in GB/s over the same minimal bytes as the GPU rows (one thread, numpy)."""
+    import collective_datapath_copy_gb300 as cdc
+    from oracle import collectives
+    n = m_bytes // 2
+    rng = synth.seeded_rng(3)
+    xs = [synth.uniform_bf16(rng, n) for _ in range(R)]
+    calls = {"allreduce": lambda: collectives.allreduce(xs, "bf16"),
+             "reduce_scatter": lambda: collectives.reduce_scatter(xs, "bf16"),
+             "allgather": lambda: collectives.allgather(xs),
+             "broadcast": lambda: collectives.broadcast(xs, 0),
+             "alltoall": lambda: collectives.alltoall(xs),
+             "reduce_to_root": lambda: collectives.reduce_to_root(xs, "bf16", 0),
+             "gather": lambda: collectives.gather(xs, 0),
+             "scatter": lambda: collectives.scatter(xs, 0)}
+    rows = []
+    for kind, fn in calls.items():
+        min_bytes = int(cdc.validate(getattr(cdc, kind)(R, n, "bf16"), zero_copy=1).min_bytes)
+        fn()
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            fn()
+            reps += 1
+            if time.perf_counter() - t0 > seconds:
+                break
+        dt = (time.perf_counter() - t0) / reps
+        rows.append({"collective": kind, "bytes_per_rank": m_bytes,
+                     "gbs": round(min_bytes / dt / 1e9, 3), "ms": round(dt * 1e3, 3)})
+    return {"kind": "oracle", "cores": 1, "rows": rows,
+            "sample": f"each collective at {m_bytes >> 20} MiB per rank, repeated for about "
+                      f"{seconds} s (numpy, one thread)"}
+
+
 def run_reference(args):
     rng = synth.seeded_rng(2)
     pool_np = [[synth.normal_bf16(rng, N_DECODE) for _ in range(R_DECODE)] for _ in range(POOL)]
@@ -586,6 +622,8 @@ def run_workload(args):
             del ins
             torch.cuda.empty_cache()
         res["rows"] = rows
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_oracle_collectives()
     elif args.workload == "prefill":
         n = 8192 * 4096
         g.manual_seed(4)
