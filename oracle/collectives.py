@@ -80,35 +80,29 @@ def scatter(xs, root=0):
     return [xs[root][d * b:(d + 1) * b].copy() for d in range(R)]
 
 
-GEMV_KBLOCKS = 8
-
-
-def gemv_payloads(wts, xs, kblocks=GEMV_KBLOCKS):
+def gemv_payloads(wts, xs):
     """Row-parallel linear layer shards, the payloads of a fused producer: rank r's payload
-    is y_r = W_r x_r with w_r given transposed as [k, n] bf16 and x_r as [k] bf16.
+    is y_r = W_r x_r, with W_r given transposed as wt[r] = [k, n] bf16 and x_r as [k] bf16.
 
-    Reading (the pages leave the layer's arithmetic open; SiFAR review: the collectives run
-    inside megakernels after a layer's computation): the k terms of each output are split
-    into `kblocks` consecutive blocks of k/kblocks; a block's sum is the binary32 chain over
-    its terms in order, starting from its first product; the block sums are then added in
-    block order; one round to bf16 at the end. Each product w*x is rounded to binary32 (it is
-    exact unless it leaves binary32's normal range) and each add rounds to nearest even."""
+    The pages say only that the all-reduces run inside megakernels, after each layer's
+    computation (SiFAR review, Summary); they leave the layer's arithmetic open. The plain
+    reading of y = W x is taken: for output j, the k products wt[i, j] * x[i] are each
+    rounded to binary32 (exact unless a product leaves binary32's range), then added as ONE
+    binary32 chain in row order i = 0..k-1, starting from the first product (round to
+    nearest even at every add, no fused multiply-add), and the chain is rounded once to
+    bf16. A datapath that adds the products in another order is held to the tolerance of
+    ``oracle.tolerance.gemv_within_tolerance``."""
     from .arith import bf16_to_f32, f32_to_bf16_rne
     out = []
     for wt, x in zip(wts, xs):
         w = bf16_to_f32(wt)
         xv = bf16_to_f32(x)
         k = w.shape[0]
-        assert k % kblocks == 0
-        kb = k // kblocks
-        total = None
         with np.errstate(over="ignore", invalid="ignore"):
-            for b in range(kblocks):
-                acc = w[b * kb] * xv[b * kb]
-                for i in range(b * kb + 1, (b + 1) * kb):
-                    acc = acc + w[i] * xv[i]
-                total = acc if total is None else total + acc
-        out.append(f32_to_bf16_rne(total))
+            acc = w[0] * xv[0]
+            for i in range(1, k):
+                acc = acc + w[i] * xv[i]
+        out.append(f32_to_bf16_rne(acc))
     return out
 
 

@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 import collective_datapath_copy_gb300 as cdc  # noqa: E402
 from collective_datapath_copy_gb300 import namings  # noqa: E402
 from collective_datapath_copy_gb300.build import build  # noqa: E402
-from oracle import collectives, naming as onaming  # noqa: E402
+from oracle import arith as oracle_arith, collectives, naming as onaming, tolerance  # noqa: E402
 from oracle.arith import NPTYPE  # noqa: E402
 import synth  # noqa: E402
 
@@ -691,6 +691,41 @@ def test_staged_plan_replays_inside_a_cuda_graph(cfg):
     plan.free()
 
 
+# The fused producer's kernel adds each output's k products in eight consecutive k-blocks
+# (one per compute warp) and then adds the block sums in order: another order than the
+# oracle's plain row-order chain. Its outputs are therefore held to the oracle's tolerance
+# for other summation orders (oracle.tolerance.gemv_sum_within_tolerance), computed from
+# the plain definition of y = W x and the rank-order sum over ranks.
+
+def fused_sum_ok(got, wts, xs):
+    """got: bf16 patterns of the rank-order sum over ranks of the payloads W_r x_r."""
+    return bool(tolerance.gemv_sum_within_tolerance(got, wts, xs).all())
+
+
+def fused_epoch_bounds(wts, xs_by_set):
+    """Device tensors (t, bound) [sets, n] of the acceptance intervals of each input set
+    (finite results only: these cases have no infinities or NaNs)."""
+    ts, bs = [], []
+    for xs in xs_by_set:
+        t, b, ref = tolerance.gemv_sum_interval(wts, xs)
+        assert np.isfinite(oracle_arith.bf16_to_f32(ref)).all()
+        ts.append(t)
+        bs.append(b)
+    return (torch.from_numpy(np.stack(ts)).to("cuda"), torch.from_numpy(np.stack(bs)).to("cuda"))
+
+
+def check_fused_epochs(outs, t_dev, b_dev, n_epochs, pool):
+    """outs[r]: [n_epochs, n] bf16 device tensors; epoch i must lie within input set i %
+    pool's interval. Returns the number of (rank, epoch) rows with an element outside."""
+    idx = torch.arange(n_epochs, device="cuda") % pool
+    t, b = t_dev[idx], b_dev[idx]
+    bad = 0
+    for o in outs:
+        g = ((o.to(torch.int32) & 0xFFFF) << 16).view(torch.float32).double()
+        bad += int(((g - t).abs() > b).any(dim=1).sum())
+    return bad
+
+
 def test_fused_run_replays_inside_a_cuda_graph_and_follows_new_weights():
     # the weight matrices' tensor maps travel as kernel parameters: a captured fused run keeps
     # the maps it was captured with, and a direct run with other matrices (or another k)
@@ -721,10 +756,9 @@ def test_fused_run_replays_inside_a_cuda_graph_and_follows_new_weights():
         torch.cuda.synchronize()
         assert plan.status()["code"] == 0, rep
         for e in range(E):
-            want = collectives.allreduce(
-                collectives.gemv_payloads(wts, [xs[r][e] for r in range(R)]), "bf16")[0]
+            xe = [xs[r][e] for r in range(R)]
             for r in range(R):
-                assert bits_equal(from_dev(outs[r][e], "bf16"), want), (rep, e, r)
+                assert fused_sum_ok(from_dev(outs[r][e], "bf16"), wts, xe), (rep, e, r)
     # other matrices, then a smaller k over the same matrices' first rows
     wts2 = [synth.normal_bf16(rng, (k, n)) for _ in range(R)]
     dw2 = [to_dev(w.ravel(), "bf16") for w in wts2]
@@ -732,10 +766,8 @@ def test_fused_run_replays_inside_a_cuda_graph_and_follows_new_weights():
         xs = [synth.normal_bf16(rng, kk) for _ in range(R)]
         plan.run_gemv(dl, [to_dev(x, "bf16") for x in xs], kk, [o[0] for o in outs])
         assert plan.status()["code"] == 0
-        want = collectives.allreduce(
-            collectives.gemv_payloads([w[:kk] for w in wl], xs), "bf16")[0]
         for r in range(R):
-            assert bits_equal(from_dev(outs[r][0], "bf16"), want), (kk, r)
+            assert fused_sum_ok(from_dev(outs[r][0], "bf16"), [w[:kk] for w in wl], xs), (kk, r)
     plan.free()
 
 
@@ -922,11 +954,9 @@ def _gemv_case(R, n, k, pool, seed):
                                                      ("spec", "oneshot", 0), ("spec", "twoshot", 0),
                                                      ("spec", "oneshot", 1),
                                                      ("dual", "twoshot_pull", 1)])
-def test_fused_gemv_allreduce_bit_exact(protocol, datapath, chain):
+def test_fused_gemv_allreduce_matches_the_oracle(protocol, datapath, chain):
     R, n, k, pool, E = 8, 4096, 256, 3, 24
     wts, xs = _gemv_case(R, n, k, pool, 97)
-    want = [collectives.allreduce(collectives.gemv_payloads(wts, [xs[r][e % pool] for r in range(R)]),
-                                  "bf16")[0] for e in range(pool)]
     plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol=protocol, datapath=datapath,
                     chain=chain)
     dw = [to_dev(w.ravel(), "bf16") for w in wts]
@@ -936,8 +966,11 @@ def test_fused_gemv_allreduce_bit_exact(protocol, datapath, chain):
                   out_epoch_stride=2 * n)
     assert plan.status()["code"] == 0
     for e in range(E):
-        for r in range(R):
-            assert bits_equal(from_dev(outs[r][e], "bf16"), want[e % pool]), (e, r)
+        xe = [xs[r][e % pool] for r in range(R)]
+        got = [from_dev(outs[r][e], "bf16") for r in range(R)]
+        assert fused_sum_ok(got[0], wts, xe), e
+        for r in range(1, R):  # every rank holds the same sum (same order, same payloads)
+            assert bits_equal(got[r], got[0]), (e, r)
     plan.free()
 
 
@@ -947,9 +980,7 @@ def test_fused_gemv_2000_epochs_under_stagger(chain):
     # started apart; every epoch must still equal the oracle
     R, n, k, pool, E = 8, 4096, 256, 3, 2000
     wts, xs = _gemv_case(R, n, k, pool, 97)
-    want = [collectives.allreduce(collectives.gemv_payloads(wts, [xs[r][e] for r in range(R)]),
-                                  "bf16")[0] for e in range(pool)]
-    want_dev = torch.stack([to_dev(w, "bf16") for w in want])
+    t_dev, b_dev = fused_epoch_bounds(wts, [[xs[r][e] for r in range(R)] for e in range(pool)])
     plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="spec", chain=chain,
                     inject="stagger", inject_seed=7 + chain, inject_prob_ppm=100000,
                     inject_max_ns=20000, inject_start_ns=5000)
@@ -960,23 +991,29 @@ def test_fused_gemv_2000_epochs_under_stagger(chain):
                   out_epoch_stride=2 * n)
     st = plan.status()
     assert st["code"] == 0, st
-    assert _check_epochs(outs, want_dev, E, pool) == 0
+    assert check_fused_epochs(outs, t_dev, b_dev, E, pool) == 0
+    # timing does not move bits: every epoch equals the first epoch of its input set
+    for o in outs:
+        assert bool((o == o[torch.arange(E, device="cuda") % pool]).all())
     plan.free()
 
 
 def test_fused_gemv_with_a_reduce_scatter_naming_and_bad_arguments():
     R, n, k = 4, 2048, 128
     wts, xs = _gemv_case(R, n, k, 1, 98)
-    ys = collectives.gemv_payloads(wts, [x[0] for x in xs])
-    want = collectives.reduce_scatter(ys, "bf16")
+    x0 = [x[0] for x in xs]
     plan = cdc.Plan(namings.reduce_scatter(R, n, "bf16"), protocol="dual")
     dw = [to_dev(w.ravel(), "bf16") for w in wts]
     dx = [to_dev(x[0], "bf16") for x in xs]
     outs = [torch.empty(n // R, dtype=torch.int16, device="cuda") for _ in range(R)]
     plan.run_gemv(dw, dx, k, outs)
     assert plan.status()["code"] == 0
-    for r in range(R):
-        assert bits_equal(from_dev(outs[r], "bf16"), want[r])
+    b = n // R
+    for r in range(R):  # rank r holds block r of the sum
+        ok = tolerance.gemv_sum_within_tolerance(
+            np.concatenate([np.zeros(r * b, np.uint16), from_dev(outs[r], "bf16"),
+                            np.zeros(n - (r + 1) * b, np.uint16)]), wts, x0)
+        assert ok[r * b:(r + 1) * b].all(), r
     with pytest.raises(cdc.CollError):
         plan.run_gemv(dw, dx, 12, outs)  # k not a multiple of 128
     with pytest.raises(cdc.CollError):
@@ -1004,8 +1041,6 @@ def test_fused_gemv_weight_ring_shapes(k, n, wpr):
     # bytes, whose copies read zeros past the matrix.
     R, pool, E = 4, 2, 6
     wts, xs = _gemv_case(R, n, k, pool, 99 + k)
-    want = [collectives.allreduce(collectives.gemv_payloads(wts, [xs[r][e] for r in range(R)]),
-                                  "bf16")[0] for e in range(pool)]
     plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="dual", warps_per_rank=wpr)
     dw = [to_dev(w.ravel(), "bf16") for w in wts]
     dx = [torch.stack([to_dev(x, "bf16") for x in xs[r]]).contiguous() for r in range(R)]
@@ -1014,15 +1049,16 @@ def test_fused_gemv_weight_ring_shapes(k, n, wpr):
                   out_epoch_stride=2 * n)
     assert plan.status()["code"] == 0
     for e in range(E):
+        xe = [xs[r][e % pool] for r in range(R)]
         for r in range(R):
-            assert bits_equal(from_dev(outs[r][e], "bf16"), want[e % pool]), (e, r)
+            assert fused_sum_ok(from_dev(outs[r][e], "bf16"), wts, xe), (e, r)
     plan.free()
 
 
 def test_fused_gemv_signed_zeros():
-    # each block's chain starts from its first product: weights of -0 against x >= +0 give
-    # -0 payloads, and the fixed-order sum of -0 over ranks stays -0; a rank with +0
-    # payloads turns the sum into +0
+    # a chain starts from its first product: weights of -0 against x >= +0 give -0 payloads
+    # (in any order: -0 + -0 is -0), and the fixed-order sum of -0 over ranks stays -0; a
+    # rank with +0 payloads turns the sum into +0. Exact bits, whatever the adding order.
     R, n, k = 4, 1024, 128
     rng = synth.seeded_rng(93)
     xs = [(synth.normal_bf16(rng, k) & np.uint16(0x7FFF)).astype(np.uint16) for _ in range(R)]
@@ -1062,6 +1098,7 @@ def test_fused_gemv_product_overflow_keeps_the_separate_rounding(unsafe):
         xs[0][1][0], xs[0][1][1] = 0x6000, 0x6080      # epoch 1: 2^65, 2^66
     want = [collectives.allreduce(collectives.gemv_payloads(wts, [xs[r][e] for r in range(R)]),
                                   "bf16")[0] for e in range(E)]
+    # (the infinity is the same in any adding order: +inf absorbs the finite terms)
     if unsafe == "weights":
         assert all(w[0] == 0x7F80 for w in want)
     else:
@@ -1074,8 +1111,12 @@ def test_fused_gemv_product_overflow_keeps_the_separate_rounding(unsafe):
                   out_epoch_stride=2 * n)
     assert plan.status()["code"] == 0
     for e in range(E):
+        xe = [xs[r][e] for r in range(R)]
         for r in range(R):
-            assert bits_equal(from_dev(outs[r][e], "bf16"), want[e]), (e, r)
+            got = from_dev(outs[r][e], "bf16")
+            if want[e][0] == 0x7F80:
+                assert got[0] == 0x7F80, (e, r)
+            assert fused_sum_ok(got, wts, xe), (e, r)
     plan.free()
 
 
@@ -1118,9 +1159,8 @@ def test_fused_gemv_missing_notify_times_out_and_the_gpu_stays_usable():
     ok = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="dual")
     ok.run_gemv(dw, dx, k, outs, n_epochs=8, out_epoch_stride=2 * n)
     assert ok.status()["code"] == 0
-    want = collectives.allreduce(collectives.gemv_payloads(wts, [x[0] for x in xs]), "bf16")
     for r in range(R):
-        assert bits_equal(from_dev(outs[r][7], "bf16"), want[r])
+        assert fused_sum_ok(from_dev(outs[r][7], "bf16"), wts, [x[0] for x in xs])
     ok.free()
 
 

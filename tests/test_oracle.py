@@ -506,36 +506,74 @@ def test_tolerance_rejects_real_errors():
 
 # ---------------------------------------------------------------- fused producer (GEMV)
 
-def test_gemv_payload_matches_exact_rational_evaluation():
+def _brute_gemv_chain(wt, x, j, order):
+    """Output j of y = W x by exact rational arithmetic: products exact, then the binary32
+    chain over the rows in the given order, from the first product; one bf16 rounding."""
+    prods = [brute.Val(brute.decode_bf16(int(wt[i, j])).q * brute.decode_bf16(int(x[i])).q,
+                       neg=brute.decode_bf16(int(wt[i, j])).neg != brute.decode_bf16(int(x[i])).neg)
+             for i in order]
+    acc = prods[0]
+    for p in prods[1:]:
+        acc = brute.add(acc, p, brute.round_f32)
+    return brute.round_bf16(acc)
+
+
+GEMV_PIN_SHAPES = ((8, 8), (16, 16), (24, 8), (5, 8), (64, 24), (32, 32))
+
+
+def _order_sensitive_gemv():
+    """k = 16 rows against x = 1: column j holds 2^24 at row a_j, -2^24 at row b_j and ones
+    elsewhere. In binary32, 2^24 + 1 rounds back to 2^24 (a tie, to even) while -2^24 + 1 is
+    exact, so the result depends on where the large terms fall in the adding order: the
+    plain chain, its reverse and an eight-block order all give different values."""
+    k = 16
+    pos = [(0, 15), (15, 0), (0, 1), (7, 8), (3, 12), (14, 2)]
+    wt = np.full((k, len(pos)), 0x3F80, dtype=np.uint16)        # 1.0
+    for j, (a, b) in enumerate(pos):
+        wt[a, j], wt[b, j] = 0x4B80, 0xCB80                     # 2^24, -2^24
+    return wt, np.full(k, 0x3F80, dtype=np.uint16)
+
+
+def _gemv_pin_cases():
     rng = synth.seeded_rng(400)
-    for k, n, nb in ((8, 8, 8), (16, 16, 8), (24, 8, 8), (5, 8, 1)):
-        wt = synth.normal_bf16(rng, (k, n))
-        x = synth.normal_bf16(rng, k)
-        y = collectives.gemv_payloads([wt], [x], kblocks=nb)[0]
-        kb = k // nb
+    cases = [(synth.normal_bf16(rng, (k, n)), synth.normal_bf16(rng, k)) for k, n in GEMV_PIN_SHAPES]
+    return cases + [_order_sensitive_gemv()]
+
+
+def test_gemv_payload_matches_exact_rational_evaluation():
+    # the plain definition of y = W x, evaluated independently: k products, one chain in row
+    # order; square shapes make a transposed operand visible too
+    for wt, x in _gemv_pin_cases():
+        k, n = wt.shape
+        y = collectives.gemv_payloads([wt], [x])[0]
         for j in range(n):
+            want = _brute_gemv_chain(wt, x, j, range(k))
+            assert brute.decode_bf16(int(y[j])).key() == want.key(), (k, n, j)
+
+
+def test_gemv_row_order_is_observable():
+    # On the pins' data, the row order decides bits: the reversed chain and a chain taken in
+    # eight consecutive blocks (then the block sums in order) each differ from the plain chain
+    # somewhere, so the exact-rational pin above fixes the order, not only the value.
+    diff_rev = diff_blk = False
+    for wt, x in _gemv_pin_cases():
+        k, n = wt.shape
+        if k % 8:
+            continue
+        kb = k // 8
+        for j in range(n):
+            plain = _brute_gemv_chain(wt, x, j, range(k)).key()
+            diff_rev |= _brute_gemv_chain(wt, x, j, range(k - 1, -1, -1)).key() != plain
             prods = [brute.Val(brute.decode_bf16(int(wt[i, j])).q * brute.decode_bf16(int(x[i])).q)
                      for i in range(k)]
             tot = None
-            for b in range(nb):
+            for b in range(8):
                 acc = prods[b * kb]
                 for p in prods[b * kb + 1:(b + 1) * kb]:
                     acc = brute.add(acc, p, brute.round_f32)
                 tot = acc if tot is None else brute.add(tot, acc, brute.round_f32)
-            want = brute.round_bf16(tot)
-            assert brute.decode_bf16(int(y[j])).key() == want.key() or (tot.q == 0), (k, n, j)
-
-
-def test_gemv_block_order_is_observable():
-    # the blocked order differs from one chain over all k on this data (pins the blocking)
-    rng = synth.seeded_rng(402)
-    k, n = 64, 512
-    wt = synth.normal_bf16(rng, (k, n))
-    x = synth.normal_bf16(rng, k)
-    xs = x.copy()
-    a = collectives.gemv_payloads([wt], [x], kblocks=8)[0]
-    b = collectives.gemv_payloads([wt], [xs], kblocks=1)[0]
-    assert not np.array_equal(a, b)
+            diff_blk |= brute.round_bf16(tot).key() != plain
+    assert diff_rev and diff_blk
 
 
 def test_gemv_payload_closed_forms():
@@ -547,8 +585,6 @@ def test_gemv_payload_closed_forms():
     wt = np.zeros((k, n), dtype=np.uint16)
     wt[np.arange(k), perm] = one           # column perm[i] picks x[i]
     y = collectives.gemv_payloads([wt], [x])[0]
-    want = np.zeros(n, dtype=np.uint16)
-    want[perm] = x
     # zero products add exactly; a product's sign of zero can differ only for zero inputs
     nz = (x & 0x7FFF) != 0
     assert np.array_equal(y[perm][nz], x[nz])
@@ -558,8 +594,102 @@ def test_gemv_payload_closed_forms():
     wt3 = arith.f32_to_bf16_rne(arith.bf16_to_f32(wt2) * np.float32(2))
     y2 = collectives.gemv_payloads([wt3], [x])[0]
     assert np.array_equal(arith.bf16_to_f32(y2), arith.bf16_to_f32(y1) * np.float32(2))
-    # every product -0 (weights -0, x >= +0): each block's chain starts from its first
-    # product, so -0 + -0 + ... stays -0 (a chain from +0.0 would give +0)
+    # small integers: every product and partial sum is exact, so y is the integer dot
+    # product (rounded to bf16 once), whatever the order
+    wi = synth.small_int_bf16(rng, (k, n), lim=4)
+    xi = synth.small_int_bf16(rng, k, lim=4)
+    dot = arith.bf16_to_f32(wi).astype(np.int64).T @ arith.bf16_to_f32(xi).astype(np.int64)
+    yi = collectives.gemv_payloads([wi], [xi])[0]
+    assert np.array_equal(yi, arith.f32_to_bf16_rne(dot.astype(np.float32)))
+    # every product -0 (weights -0, x >= +0): the chain starts from its first product, so
+    # -0 + -0 + ... stays -0 (a chain from +0.0 would give +0)
     wz = np.full((k, n), 0x8000, dtype=np.uint16)
     xp = (x & np.uint16(0x7FFF)).astype(np.uint16)
     assert np.all(collectives.gemv_payloads([wz], [xp])[0] == 0x8000)
+
+
+def _blocked_gemv(wt, x, blocks):
+    """y = W x with the k products added in `blocks` consecutive blocks (each a binary32
+    chain from its first product), the block sums then added in block order: an alternative
+    order, written out here to exercise the tolerance."""
+    w, xv = arith.bf16_to_f32(wt), arith.bf16_to_f32(x)
+    kb = w.shape[0] // blocks
+    tot = None
+    for b in range(blocks):
+        acc = w[b * kb] * xv[b * kb]
+        for i in range(b * kb + 1, (b + 1) * kb):
+            acc = acc + w[i] * xv[i]
+        tot = acc if tot is None else tot + acc
+    return arith.f32_to_bf16_rne(tot)
+
+
+@pytest.mark.parametrize("blocks", [1, 8, 64])
+def test_gemv_other_orders_are_within_tolerance(blocks):
+    from oracle import tolerance
+    rng = synth.seeded_rng(403)
+    k, n, R = 512, 700, 4
+    wts = [synth.normal_bf16(rng, (k, n)) for _ in range(R)]
+    xs = [synth.normal_bf16(rng, k) for _ in range(R)]
+    ys = [_blocked_gemv(w, x, blocks) for w, x in zip(wts, xs)]
+    for w, x, y in zip(wts, xs, ys):
+        assert tolerance.gemv_within_tolerance(y, w, x).all()
+    s = arith.ordered_sum(ys, "bf16")
+    assert tolerance.gemv_sum_within_tolerance(s, wts, xs).all()
+    # under heavy cancellation (2^24 - 2^24 plus small terms) the orders give values far
+    # apart in relative terms, all within the accumulation term of the bound
+    w, x = _order_sensitive_gemv()
+    for y in (collectives.gemv_payloads([w], [x])[0], _blocked_gemv(w, x, min(blocks, 16)),
+              collectives.gemv_payloads([w[::-1].copy()], [x[::-1].copy()])[0]):
+        assert tolerance.gemv_within_tolerance(y, w, x).all()
+
+
+def test_gemv_tolerance_rejects_real_errors():
+    from oracle import tolerance
+    rng = synth.seeded_rng(404)
+    k, n, R = 256, 600, 4
+    wts = [synth.normal_bf16(rng, (k, n)) for _ in range(R)]
+    xs = [synth.normal_bf16(rng, k) for _ in range(R)]
+    ys = collectives.gemv_payloads(wts, xs)
+    w, x, y = wts[0], xs[0], ys[0]
+    p = arith.bf16_to_f32(w).astype(np.float64) * arith.bf16_to_f32(x).astype(np.float64)[:, None]
+    big = np.abs(p.sum(axis=0)) > np.abs(p).sum(axis=0) / 8
+    # three bf16 ulps off: rejected wherever the exact value is not tiny against sum |p|
+    bad = (y.astype(np.int32) + 3).astype(np.uint16)
+    assert not tolerance.gemv_within_tolerance(bad, w, x)[big].any()
+    # the last row dropped, the weights transposed (square), a sign flipped: rejected
+    # almost everywhere
+    dropped = collectives.gemv_payloads([w[:-1]], [x[:-1]])[0]
+    assert tolerance.gemv_within_tolerance(dropped, w, x).mean() < 0.2
+    ws = synth.normal_bf16(rng, (k, k))
+    yt = collectives.gemv_payloads([np.ascontiguousarray(ws.T)], [x])[0]
+    assert tolerance.gemv_within_tolerance(yt, ws, x).mean() < 0.05
+    assert tolerance.gemv_within_tolerance(y ^ np.uint16(0x8000), w, x).mean() < 0.05
+    # over ranks: a rank dropped, or the sum three ulps off, is rejected
+    s = arith.ordered_sum(ys, "bf16")
+    assert tolerance.gemv_sum_within_tolerance(s, wts, xs).all()
+    assert tolerance.gemv_sum_within_tolerance(arith.ordered_sum(ys[:-1], "bf16"),
+                                               wts, xs).mean() < 0.2
+    t = np.sum([(arith.bf16_to_f32(a).astype(np.float64) *
+                 arith.bf16_to_f32(b).astype(np.float64)[:, None]).sum(axis=0)
+                for a, b in zip(wts, xs)], axis=0)
+    Sy = np.sum([np.abs(arith.bf16_to_f32(v)) for v in ys], axis=0)
+    # (each payload may sit one rounding away from the plain one, so the sum over four
+    # ranks may move by a few ulps; eight is outside)
+    bad_s = (s.astype(np.int32) + 8).astype(np.uint16)
+    assert not tolerance.gemv_sum_within_tolerance(bad_s, wts, xs)[np.abs(t) > Sy / 2].any()
+
+
+def test_gemv_tolerance_compares_special_values_by_class():
+    # a product that overflows binary32 makes the payload infinite in any order
+    from oracle import tolerance
+    rng = synth.seeded_rng(405)
+    k, n = 16, 8
+    w = synth.normal_bf16(rng, (k, n))
+    x = synth.normal_bf16(rng, k)
+    w[3, 2], x[3] = 0x7F00, 0x7F00            # 2^127 * 2^127 overflows
+    y = collectives.gemv_payloads([w], [x])[0]
+    assert y[2] == 0x7F80
+    ok = tolerance.gemv_within_tolerance(y, w, x)
+    assert ok.all()
+    assert not tolerance.gemv_within_tolerance(np.where(np.arange(n) == 2, 0x7F7F, y)
+                                               .astype(np.uint16), w, x)[2]

@@ -147,7 +147,7 @@ def test_pins_catch_copy_from_the_wrong_producer(monkeypatch):
 def _gemv_ok():
     try:
         pins.test_gemv_payload_matches_exact_rational_evaluation()
-        pins.test_gemv_block_order_is_observable()
+        pins.test_gemv_row_order_is_observable()
         pins.test_gemv_payload_closed_forms()
     except AssertionError:
         return False
@@ -157,48 +157,44 @@ def _gemv_ok():
 def _gemv_mutant(kind):
     from oracle.arith import bf16_to_f32, f32_to_bf16_rne
 
-    def gemv(wts, xs, kblocks=collectives.GEMV_KBLOCKS):
+    def gemv(wts, xs):
         out = []
         for wt, x in zip(wts, xs):
+            if kind == "weights transposed" and wt.shape[0] == wt.shape[1]:
+                wt = np.ascontiguousarray(wt.T)
             w, xv = bf16_to_f32(wt), bf16_to_f32(x)
             k = w.shape[0]
-            kb = k // kblocks
-            sums = []
-            for b in range(kblocks):
-                rows = range(b * kb, (b + 1) * kb)
-                if kind == "accumulator starts at +0.0":
-                    acc = np.zeros(w.shape[1], np.float32)
-                    for i in rows:
-                        acc = acc + w[i] * xv[i]
-                elif kind == "products rounded to bf16":
-                    acc = None
-                    for i in rows:
-                        p = bf16_to_f32(f32_to_bf16_rne(w[i] * xv[i]))
-                        acc = p if acc is None else acc + p
-                else:
-                    acc = w[rows[0]] * xv[rows[0]]
-                    for i in rows[1:]:
-                        acc = acc + w[i] * xv[i]
-                sums.append(acc)
-            if kind == "blocks added in reverse":
-                sums = sums[::-1]
-            if kind == "one chain, no blocks" and kblocks > 1:
-                acc = w[0] * xv[0]
-                for i in range(1, k):
-                    acc = acc + w[i] * xv[i]
-                sums = [acc]
-            if kind == "last row dropped":
-                sums[-1] = sums[-1] - w[k - 1] * xv[k - 1]
-            total = sums[0]
-            for s_ in sums[1:]:
-                total = total + s_
-            out.append(f32_to_bf16_rne(total))
+            rows = list(range(k))
+            if kind == "rows in reverse":
+                rows = rows[::-1]
+            if kind == "last row dropped" and k > 1:
+                rows = rows[:-1]
+            prod = lambda i: w[i] * xv[i]
+            if kind == "products rounded to bf16":
+                prod = lambda i: bf16_to_f32(f32_to_bf16_rne(w[i] * xv[i]))
+            if kind == "eight k-blocks" and k % 8 == 0:
+                kb = k // 8
+                acc = None
+                for b in range(8):
+                    part = prod(b * kb)
+                    for i in range(b * kb + 1, (b + 1) * kb):
+                        part = part + prod(i)
+                    acc = part if acc is None else acc + part
+            elif kind == "accumulator starts at +0.0":
+                acc = np.zeros(w.shape[1], np.float32)
+                for i in rows:
+                    acc = acc + prod(i)
+            else:
+                acc = prod(rows[0])
+                for i in rows[1:]:
+                    acc = acc + prod(i)
+            out.append(f32_to_bf16_rne(acc))
         return out
     return gemv
 
 
-GEMV_MUTANTS = ["accumulator starts at +0.0", "products rounded to bf16",
-                "blocks added in reverse", "one chain, no blocks", "last row dropped"]
+GEMV_MUTANTS = ["accumulator starts at +0.0", "products rounded to bf16", "eight k-blocks",
+                "rows in reverse", "last row dropped", "weights transposed"]
 
 
 def test_unmutated_gemv_oracle_passes_its_pins():
@@ -246,3 +242,33 @@ def test_pins_catch_tolerance_mutants(kind, monkeypatch):
     monkeypatch.setattr(tolerance, "within_tolerance", wrong)
     assert not _tolerance_ok(), kind
     monkeypatch.setattr(tolerance, "within_tolerance", orig)
+
+
+def _gemv_tolerance_ok():
+    try:
+        for blocks in (1, 8, 64):
+            pins.test_gemv_other_orders_are_within_tolerance(blocks)
+        pins.test_gemv_tolerance_rejects_real_errors()
+        pins.test_gemv_tolerance_compares_special_values_by_class()
+    except AssertionError:
+        return False
+    return True
+
+
+@pytest.mark.parametrize("kind", ["ten times looser", "no accumulation term",
+                                  "special values compared as numbers"])
+def test_pins_catch_gemv_tolerance_mutants(kind, monkeypatch):
+    from oracle import tolerance
+    assert _gemv_tolerance_ok()
+    if kind == "special values compared as numbers":
+        monkeypatch.setattr(tolerance, "_same_special", lambda got, ref: np.zeros(got.shape, bool))
+    else:
+        def wrong(p):
+            s = p.sum(axis=0)
+            S = np.abs(p).sum(axis=0)
+            rt = tolerance.RTOL["bf16"]
+            if kind == "ten times looser":
+                return s, 10 * (rt * np.abs(s) + (p.shape[0] - 1) * 2.0 ** -24 * S)
+            return s, rt * np.abs(s)
+        monkeypatch.setattr(tolerance, "_gemv_bound", wrong)
+    assert not _gemv_tolerance_ok(), kind
