@@ -3,19 +3,20 @@
 // in one fixed file-scope device array instead of memory a plan allocates.
 //
 // Some callers cannot allocate device memory at the point where they need the collective:
-// a serving process that reserved nearly all HBM up front for weights and KV cache (a late
-// cudaMalloc fails or fragments that reservation), code between cudaStreamBeginCapture and
-// cudaStreamEndCapture, and latency-critical loops where cudaMalloc/cudaFree would add an
-// implicit device synchronisation. This entry point serves them; everything it needs beyond
-// the caller's inputs and outputs is in g_static_scratch.
+// a serving process that reserved nearly all HBM up front for weights and the KV cache (a
+// late cudaMalloc then fails, or fragments that reservation), and latency-critical loops
+// where a cudaMalloc/cudaFree pair would add an implicit device synchronisation. This entry
+// point serves them; everything it needs beyond the caller's inputs and outputs is in
+// g_static_scratch.
 //
 // g_static_scratch is kStaticScratchBytes on every device that loads the library and stays
 // allocated until the process exits. Host code must not pass its name to a kernel (in host
 // code the symbol is only a host-side stand-in); the device address is looked up once per
-// device with cudaGetSymbolAddress, on the first call made while that device is current.
-// All calls share the array and it keeps the last call's contents: each call clears the
-// flag words it uses before its kernel runs, on the caller's stream. Calls that can overlap
-// on the GPU (different streams, or no ordering between them) race on the array.
+// device with cudaGetSymbolAddress, on the first call made while that device is current
+// (make that first call before any stream capture). All calls share the array and it keeps
+// the last call's contents: each call clears the flag words it uses before its kernel
+// runs, on the caller's stream. Calls that can overlap on the GPU (different streams, or
+// no ordering between them) race on the array.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -96,6 +97,9 @@ __global__ void __launch_bounds__(32) static_allreduce_kernel(const StaticArgs a
       }
       return;
     }
+    // lane j's acquire of rank j's flag must order every lane's loads of rank j's slot: a
+    // vote orders nothing in memory, the warp barrier does
+    __syncwarp();
     Vec16Acc<DT> acc;
     for (uint32_t j0 = 0; j0 < a.R; j0 += 8) {
       uint4 x[8];
@@ -145,6 +149,7 @@ extern "C" int coll_allreduce_static(int R, int dtype, void *const *in, void *co
       count == 0 || n_epochs < 1 || in_pool < 1)
     return COLL_EINVAL;
   const uint64_t es = dtype == COLL_BF16 ? 2 : 4;
+  if (count > kStaticScratchBytes / es) return COLL_ETOOBIG;  // (and count * es cannot wrap)
   const uint64_t bytes = count * es;
   if (bytes & 15u) return COLL_EALIGN;
   if ((uint64_t)(in_epoch_stride < 0 ? -in_epoch_stride : in_epoch_stride) & 15u ||

@@ -247,7 +247,10 @@ class BoundRun:
 def allreduce_static(ins, outs, count, dtype="bf16", n_epochs=1, in_epoch_stride=0, in_pool=1,
                      out_epoch_stride=0, status=None, stream=None) -> int:
     """coll_allreduce_static: an all-reduce (fixed rank order, dual buffers) that allocates
-    nothing, its exchange buffers and flags in a fixed device array of the library. ins/outs:
+    nothing, for callers that cannot allocate device memory at that point (HBM already
+    reserved for weights and the KV cache; loops that must not pay cudaMalloc's implicit
+    synchronisation); its exchange buffers and flags live in a fixed device array of the
+    library, shared by every call, so calls must not overlap on the GPU. ins/outs:
     per-rank torch CUDA tensors of `count` elements; strides in bytes; `status`: optional
     int32 CUDA tensor that receives COLL_ETIMEDOUT if a bounded wait expires. Returns the
     library's code (raises on a synchronous error)."""

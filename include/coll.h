@@ -185,11 +185,17 @@ typedef struct {
   uint64_t spec_retries; /* validations that failed and were redone after a wait       */
 } coll_stats_t;
 
-/* Fill *cfg with defaults (spec protocol, oneshot, staged, tagged validation). */
+/* Fill *cfg with defaults (spec protocol, oneshot, staged, tagged validation).
+ * Source: SiFAR review, "What carries the argument" (speculative reduction over dual
+ * buffers is the protocol the review's All-Reduce is built on). */
 int coll_config_default(coll_config_t *cfg);
 
 /* Validate a naming and compile it into a plan: host work tables, device tables,
  * exchange buffers (x2 parities) and zeroed flags for staged plans.
+ * Source: Purlin article, "The Purlin PDF describes a three-layer design": the top layer
+ * states a collective as a naming of an input and an output layout plus copy or reduction,
+ * and SNAC derives the coordination from that statement; here the plan compiler derives
+ * which warp stages, notifies and consumes each piece, and which flags each consumer reads.
  * R: 1..64 ranks. in_len/out_len: R buffer lengths in elements, each at most 2^48
  * (COLL_EBOUNDS beyond). cfg may be NULL (defaults).
  * Ownership: the plan owns everything it allocates; coll_free releases it. The segment
@@ -202,15 +208,21 @@ int coll_plan(coll_plan_t *out, int R, int op, int dtype, const coll_seg_t *in_s
               const uint64_t *out_len, const coll_config_t *cfg);
 
 /* The host half of coll_plan only: same checks and codes, no device call (usable on a
- * machine without a GPU). info may be NULL. */
+ * machine without a GPU). info may be NULL.
+ * Source: as coll_plan (Purlin article, "three-layer design": the naming layer). */
 int coll_validate(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_in,
                   const uint64_t *in_len, const coll_seg_t *out_segs, size_t n_out,
                   const uint64_t *out_len, const coll_config_t *cfg,
                   coll_plan_info_t *info);
 
+/* Sizes of a compiled plan and its minimal (algorithmic) bytes per epoch. No counterpart
+ * on the pages; the minimal bytes are the denominator of the bandwidth figures. */
 int coll_plan_info(coll_plan_t p, coll_plan_info_t *info);
 
 /* Run n_epochs epochs of the plan on `stream` (a cudaStream_t; NULL = legacy default).
+ * Source: Purlin article, "three-layer design" (Stage, Notify, And Consume orchestrates the
+ * Atom datapath's copy and reduce); SiFAR review, "What carries the argument" and Figs. 5
+ * and 6 (the protocols and the oneshot / twoshot datapaths a staged plan runs).
  * in/out: host arrays of R device pointers. Epoch i (0-based) reads
  * in[r] + (i % in_pool) * in_epoch_stride bytes and writes out[r] + i * out_epoch_stride
  * bytes (stride 0 overwrites). A rank with no segments may pass NULL.
@@ -249,14 +261,21 @@ int coll_run_gemv(coll_plan_t p, const void *const *wt, void *const *x, int k, v
                   void *stream);
 
 /* Wait for the plan's last run and report its status and counters. Returns the run's
- * status (COLL_OK, COLL_ETIMEDOUT, COLL_EDEVICE) or COLL_ECUDA. st may be NULL. */
+ * status (COLL_OK, COLL_ETIMEDOUT, COLL_EDEVICE) or COLL_ECUDA. st may be NULL.
+ * Source: SiFAR review, Referee Report, major comment 1 and Figs. 23-25 (validations that
+ * fail are retried, and the mis-speculation rate is reported: spec_checks, spec_retries);
+ * "What would settle it" (a wait that never ends is the failure to detect: a bounded wait
+ * ends the run with COLL_ETIMEDOUT and fail_* say where). */
 int coll_status(coll_plan_t p, coll_stats_t *st);
 
 /* Copy up to n per-epoch %globaltimer stamps (ns) of the last run into host memory;
- * returns the number copied (synchronises on the last run). */
+ * returns the number copied (synchronises on the last run).
+ * Source: SiFAR review, Fig. 15 and Referee Report minor comment 4 (latency per payload /
+ * TP cell): the stamps give the per-epoch latency distribution of a run. */
 int64_t coll_stamps(coll_plan_t p, uint64_t *host, int64_t n);
 
-/* Measurement probe (not part of the collective): ping-pong one flag `iters` times
+/* Measurement probe (not part of the collective; SiFAR review, "If this is right": once
+ * GPUs are in lockstep, the top barrier costs a flag exchange): ping-pong one flag `iters` times
  * between one thread of block 0 and one thread of block `peer_block` of a cooperative
  * launch with peer_block+1 one-warp blocks, and report the total ns (%globaltimer) and the
  * two SM ids. This is the round trip that bounds a flag handshake between two emulated
@@ -265,17 +284,20 @@ int coll_probe_flag_rtt(int peer_block, int iters, uint64_t *ns_total, int *sm_a
 
 /* Wait for the last run, then re-zero flags, counters and the epoch counter. After a run
  * that reported COLL_ETIMEDOUT the plan's flags are inconsistent: call this before the next
- * coll_run on the plan. */
+ * coll_run on the plan. No counterpart on the pages (the flags of the SNAC layer restart). */
 int coll_reset(coll_plan_t p);
 
-/* Wait for the last run and release everything the plan owns. NULL is a no-op. */
+/* Wait for the last run and release everything the plan owns. NULL is a no-op.
+ * Source: Purlin article, "three-layer design" (the plan holds the SNAC layer's exchange
+ * buffers and flags for one naming; freeing it ends that naming's coordination). */
 int coll_free(coll_plan_t p);
 
 /* All-reduce (sum) that allocates nothing. The pages have no counterpart: this exists for
  * callers that cannot allocate device memory when they need the collective — a serving
- * process that reserved nearly all HBM up front for weights and KV cache, code inside a
- * CUDA stream capture, or a latency-critical loop where cudaMalloc/cudaFree would add an
- * implicit device synchronisation. It calls no allocating routine.
+ * process that reserved nearly all HBM up front for weights and the KV cache (a late
+ * cudaMalloc fails or fragments that reservation), or a latency-critical loop where a
+ * cudaMalloc/cudaFree pair would add an implicit device synchronisation. It calls no
+ * allocating routine.
  * Same result as coll_plan/coll_run for an all-reduce naming (every rank's whole buffer is
  * one name) with the dual-buffer protocol: out[r] = the rank-order binary32 sum of all R
  * inputs, rounded once to bf16 for COLL_BF16. in/out: host arrays of R device pointers,
@@ -285,7 +307,8 @@ int coll_free(coll_plan_t p);
  * Scratch: a fixed 4 MiB device array held by every GPU that loads the library until the
  * process exits; it holds 2 x R x ceil(count*size/512) pieces of 512 bytes plus flags, so
  * R x count x element size up to about 2 MiB fits. Larger requests (or more warps than can
- * be co-resident) return COLL_ETOOBIG. The first call on a device looks up the array's
+ * be co-resident), including any count whose byte size exceeds the array, return
+ * COLL_ETOOBIG. The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture. Every call shares the array and clears its flags on `stream`
  * first; calls that can overlap on the GPU (other streams, unordered) race on it.
@@ -294,7 +317,7 @@ int coll_allreduce_static(int R, int dtype, void *const *in, void *const *out, u
                           int n_epochs, int64_t in_epoch_stride, int in_pool,
                           int64_t out_epoch_stride, int32_t *status, void *stream);
 
-/* Static string for a code. */
+/* Static string for a code. No counterpart on the pages. */
 const char *coll_strerror(int code);
 
 #ifdef __cplusplus
