@@ -41,6 +41,7 @@ FLUSH_BYTES = 256 << 20  # > 129 MB L2
 
 
 ENGINE_SOURCES = ["engine.cu", "atom.cuh", "engine.cuh", "coll_internal.h", "tma.cuh"]
+BULK_SOURCES = ["bulk.cu", "atom.cuh", "engine.cuh", "coll_internal.h", "tma.cuh"]
 
 
 def sources_sha256(names):
@@ -185,6 +186,159 @@ def _time_steps(torch, fn, steps, warmup, flush, stream):
     return times
 
 
+def _stats_us(times_ms, per=1):
+    """median / min / max of per-step times (ms), divided by `per`, in microseconds."""
+    t = sorted(x * 1000.0 / per for x in times_ms)
+    return {"us_median": round(t[len(t) // 2], 3), "us_min": round(t[0], 3),
+            "us_max": round(t[-1], 3), "steps": len(t)}
+
+
+def _time_stream(torch, fns, steps, warmup, flush, stream):
+    """Per-step CUDA-event times (ms) of the launches `fns` issued back to back (L2 flushed
+    before each step, not between the launches of a step)."""
+    def run_all():
+        for f in fns:
+            f()
+    return _time_steps(torch, run_all, steps, warmup, flush, stream)
+
+
+def measure_zero_copy(torch, cdc, nm, in_sets, out_sets, steps, warmup, flush, stream, peak,
+                      **cfg):
+    """One zero-copy plan, timed two ways, each the median (with min and max) of `steps`
+    steps:
+    - single: one launch right after an L2 flush (CUDA events around the launch; the time
+      includes the launch and the event pair, about 5 us that a one-element kernel timed the
+      same way also takes);
+    - stream: 2 x len(in_sets) launches back to back, cycling over input/output sets that
+      together exceed L2, so every launch reads inputs no recent launch touched; per-launch
+      time = the step's time / launches (launch overheads overlap the previous launch).
+    GB/s and the fraction of `peak` are over the plan's minimal bytes (each input byte a
+    named output depends on read once, each named output byte written once)."""
+    pl = cdc.Plan(nm, zero_copy=1, **cfg)
+    runs = [pl.bind(i, o) for i, o in zip(in_sets, out_sets)]
+    b = int(pl.info.min_bytes)
+    one = _time_steps(torch, runs[0], steps, warmup, flush, stream)
+    seq = runs * 2
+    many = _time_stream(torch, seq, steps, 1, flush, stream)
+    st = pl.status()
+    if st["code"] != 0:
+        raise RuntimeError(f"run failed: {st}")
+    kern = "bulk_kernel" if pl.info.bulk_tile_bytes else "zc_kernel"
+    pl.free()
+    res = {"min_bytes": b, "kernel": kern}
+    for key, tt, per in (("single", one, 1), ("stream", many, len(seq))):
+        r = _stats_us(tt, per)
+        r["gbs"] = round(b / (r["us_median"] * 1e-6) / 1e9, 1)
+        r["frac"] = round(r["gbs"] / peak, 4)
+        res[key] = r
+    res["stream"]["launches_per_step"] = len(seq)
+    return res
+
+
+LARGE_KINDS = ("allreduce", "reduce_scatter", "allgather", "broadcast", "alltoall",
+               "reduce_to_root", "gather", "scatter")
+L2_BYTES = 129e6
+
+
+def large_collectives(torch, cdc, dev, flush, stream, peak, steps, warmup,
+                      sizes_mib=(16, 64, 256)):
+    """Every collective at every large size per rank: zero-copy datapath, R=8 emulated ranks,
+    bf16 uniform[-1,1] (synth.device_uniform_bf16), timed by measure_zero_copy."""
+    R = 8
+    rows = []
+    for mib in sizes_mib:
+        n = (mib << 20) // 2
+        for kind in LARGE_KINDS:
+            nm = getattr(cdc, kind)(R, n, "bf16")
+            set_bytes = 2 * (sum(nm.in_len) + sum(nm.out_len))
+            nsets = max(2, min(3, int(3 * L2_BYTES // set_bytes) + 1))
+            in_sets = [[synth.device_uniform_bf16(torch, 3000 + 100 * k + r, n, dev)
+                        for r in range(R)] for k in range(nsets)]
+            out_sets = [[torch.empty(L, dtype=torch.int16, device=dev) for L in nm.out_len]
+                        for _ in range(nsets)]
+            cfg = {"datapath": "twoshot"} if kind == "allreduce" else {}
+            r = measure_zero_copy(torch, cdc, nm, in_sets, out_sets, steps, warmup, flush,
+                                  stream, peak, **cfg)
+            r.update({"collective": kind + ("-twoshot" if kind == "allreduce" else ""),
+                      "mib_per_rank": mib, "sets": nsets})
+            rows.append(r)
+            del in_sets, out_sets
+        torch.cuda.empty_cache()
+    return rows
+
+
+def prefill_allreduce(torch, cdc, dev, flush, stream, peak, steps, warmup):
+    """The prefill all-reduce, 8 x 8192 x 4096 bf16 (64 MiB per rank), N(0,1): two-shot
+    (reduce once, push to every rank) and one-shot (every rank reduces all eight)."""
+    R, n = 8, 8192 * 4096
+    nm = cdc.allreduce(R, n, "bf16")
+    in_sets = [[synth.device_normal_bf16(torch, 4000 + 100 * k + r, n, dev) for r in range(R)]
+               for k in range(2)]
+    out_sets = [[torch.empty(n, dtype=torch.int16, device=dev) for _ in range(R)]
+                for _ in range(2)]
+    res = {dp: measure_zero_copy(torch, cdc, nm, in_sets, out_sets, steps, warmup, flush,
+                                 stream, peak, datapath=dp)
+           for dp in ("twoshot", "oneshot")}
+    del in_sets, out_sets
+    torch.cuda.empty_cache()
+    return res
+
+
+def moe_collectives(torch, cdc, dev, flush, stream, peak, steps, warmup,
+                    which=("dispatch", "combine")):
+    """MoE dispatch (each token row to every rank hosting one of its top-8 of 256 experts,
+    Zipf(1.1) popularity; 8 x 4096 tokens x 7168 bf16) and its reverse, the combine (a sum
+    over the destination ranks)."""
+    R, T, H, E, k = 8, 4096, 7168, 256, 8
+    routing = synth.zipf_topk_routing(5, R, T, E, k, 1.1)
+    res = {}
+    for name in which:
+        nm = (cdc.moe_dispatch if name == "dispatch" else cdc.moe_combine)(routing, E // R, H)
+        in_sets = [[synth.device_normal_bf16(torch, 5000 + 100 * s_ + r, L, dev)
+                    for r, L in enumerate(nm.in_len)] for s_ in range(2)]
+        out_sets = [[torch.empty(L, dtype=torch.int16, device=dev) for L in nm.out_len]
+                    for _ in range(2)]
+        res[name] = measure_zero_copy(torch, cdc, nm, in_sets, out_sets, steps, warmup, flush,
+                                      stream, peak)
+        res[name]["rows_per_rank"] = [int(c) for c in nm.meta["counts"]]
+        del in_sets, out_sets
+        torch.cuda.empty_cache()
+    return res
+
+
+def large_payloads(torch, cdc, dev, flush, stream, peak, steps, warmup):
+    """Every large-payload configuration: the collectives at 16, 64 and 256 MiB per rank,
+    the prefill all-reduce and MoE dispatch / combine."""
+    a = (torch, cdc, dev, flush, stream, peak, steps, warmup)
+    return {"method": "zero-copy datapath, R=8 emulated ranks, bf16; 'single' = one launch "
+                      "right after an L2 flush, 'stream' = launches back to back over input "
+                      "sets that together exceed L2; median (min, max) of the steps; GB/s "
+                      "over the minimal bytes",
+            "collectives": large_collectives(*a), "prefill_allreduce_64MiB": prefill_allreduce(*a),
+            "moe": moe_collectives(*a)}
+
+
+def large_rooflines(large, peak, peak_kind):
+    """Roofline records of the two zero-copy kernels at full size: the bulk (TMA) ring on the
+    prefill two-shot all-reduce and the warp kernel on MoE dispatch. achieved = minimal
+    bytes per launch / the per-launch time of the back-to-back ('stream') measurement;
+    traffic = DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    kernel's current sources."""
+    out = {}
+    for key, r, kern, srcs in (
+            ("bulk_kernel: prefill all-reduce two-shot, 8 x 64 MiB",
+             large["prefill_allreduce_64MiB"]["twoshot"], "bulk_kernel/prefill_twoshot",
+             BULK_SOURCES),
+            ("zc_kernel: MoE dispatch, 8 x 4096 x 7168", large["moe"]["dispatch"],
+             "zc_kernel/moe_dispatch", ENGINE_SOURCES)):
+        st = r["stream"]
+        out[key] = {"bound": "hbm", "achieved": st["gbs"], "peak": peak, "unit": "GB/s",
+                    "frac": round(st["gbs"] / peak, 4), "peak_kind": f"of {peak_kind}",
+                    "traffic": recorded_traffic(kern, srcs), "algorithmic_bytes": r["min_bytes"],
+                    "us_per_launch": st["us_median"]}
+    return out
+
+
 def run_ours(args, rank, world, dist):
     import torch
     import collective_datapath_copy_gb300 as cdc
@@ -252,13 +406,14 @@ def run_ours(args, rank, world, dist):
         s2 = plans[name].status()
         if s2["code"] != 0:
             raise RuntimeError(f"{name} failed: {s2}")
-        proto[name] = {"us_per_epoch": round(sum(tt) / len(tt) * 1000 / EPOCHS, 4)}
+        proto[name] = _stats_us(tt, EPOCHS)
+        proto[name]["us_per_epoch"] = proto[name]["us_median"]
         if name.startswith("spec"):
             proto[name]["retries_per_check"] = (s2["spec_retries"] / s2["spec_checks"]
                                                 if s2["spec_checks"] else 0.0)
-    proto["spec"] = {"us_per_epoch": round(us_epoch, 4),
-                     "retries_per_check": (st["spec_retries"] / st["spec_checks"]
-                                           if st["spec_checks"] else 0.0)}
+    proto["spec"] = dict(_stats_us(times, EPOCHS), us_per_epoch=round(us_epoch, 4),
+                         retries_per_check=(st["spec_retries"] / st["spec_checks"]
+                                            if st["spec_checks"] else 0.0))
 
     # per-epoch latency percentiles from %globaltimer stamps (spec)
     sp = cdc.Plan(nm, protocol="spec", record_stamps=1, stamp_capacity=EPOCHS)
@@ -333,27 +488,17 @@ def run_ours(args, rank, world, dist):
     small_us = sorted(a_.elapsed_time(b_) for a_, b_ in ev)[500] * 1000
     s_plan.free()
 
-    # prefill-sized all-reduce: 8 x 64 MiB bf16, one-shot vs two-shot (zero-copy)
-    prefill = {}
-    if not args.skip_prefill:
-        n = 8192 * 4096
-        rng = synth.seeded_rng(4)
-        g = torch.Generator(device=dev)
-        g.manual_seed(4)
-        pins = [torch.randn(n, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
-                for _ in range(R_DECODE)]
-        pouts = [torch.empty(n, dtype=torch.int16, device=dev) for _ in range(R_DECODE)]
-        nmp = cdc.allreduce(R_DECODE, n, "bf16")
-        for dp in ("twoshot", "oneshot"):
-            pl = cdc.Plan(nmp, zero_copy=1, datapath=dp)
-            tt = _time_steps(torch, lambda: pl.run(pins, pouts), 10, 3, flush, stream)
-            assert pl.status()["code"] == 0
-            b = pl.info.min_bytes
-            gbs = b / (sum(tt) / len(tt) / 1000) / 1e9
-            prefill[dp] = {"ms": round(sum(tt) / len(tt), 4), "gbs": round(gbs, 1),
-                           "frac": round(gbs / peak, 4), "min_bytes": b}
-            pl.free()
-        del pins, pouts
+    # large payloads: every collective at 16 / 64 / 256 MiB per rank, the prefill
+    # all-reduce and MoE dispatch / combine (zero-copy datapath)
+    large = None
+    if not args.skip_large:
+        for p in plans.values():
+            p.free()
+        plans.clear()
+        del outs
+        torch.cuda.empty_cache()
+        large = large_payloads(torch, cdc, dev, flush, stream, peak, max(10, args.steps // 2),
+                               args.warmup)
 
     algo_bytes = 2 * R_DECODE * N_DECODE * 2 * EPOCHS
     achieved = algo_bytes / (ms / 1000) / 1e9
@@ -385,11 +530,14 @@ def run_ours(args, rank, world, dist):
                      "traffic": recorded_traffic("engine_kernel", ENGINE_SOURCES),
                      "peak_kind": f"of {peak_kind}",
                      "note": "latency-bound: 128 KiB of algorithmic bytes per epoch"},
+        "value_stats": dict(_stats_us(times, EPOCHS), note="per-step spread of the timed steps "
+                            "(value = their total / (steps x epochs))"),
         "latency": lat,
         "phases": phases,
         "flag_round_trip": rtt,
         "protocols": proto,
-        "prefill_allreduce_64MiB": prefill,
+        "large_payloads": large,
+        "rooflines_large": large_rooflines(large, peak, peak_kind) if large else None,
         "small_allreduce_2x1024_f32": {"median_us": round(small_us, 3), "launches": 1000,
                                        "protocol": "barrier", "epochs_per_launch": 1},
         "e2e": {"value": round(e2e_us, 4), "unit": "us/epoch", "h2d_bytes_per_step": h2d,
@@ -537,36 +685,34 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ other workloads
 
-def _zc_measure(torch, cdc, nm, ins, outs, steps, warmup, flush, stream, graph_reps=0, **cfg):
-    """Median single-launch time with L2 flushed before each launch; with graph_reps, also
-    the per-collective time of graph_reps back-to-back launches replayed from a CUDA graph
-    (no host overhead, L2 warm)."""
+def _zc_measure(torch, cdc, nm, ins, outs, steps, warmup, flush, stream, graph_reps=50, **cfg):
+    """A small zero-copy collective: the per-collective time of `graph_reps` launches
+    replayed back to back from a CUDA graph (no host work; the inputs stay in L2), median of
+    the steps, in microseconds; and, for context, one launch right after an L2 flush, whose
+    CUDA-event time is mostly the launch and the event pair at these sizes."""
     pl = cdc.Plan(nm, zero_copy=1, **cfg)
     tt = _time_steps(torch, lambda: pl.run(ins, outs), steps, warmup, flush, stream)
     st = pl.status()
     if st["code"] != 0:
         raise RuntimeError(f"run failed: {st}")
-    b = pl.info.min_bytes
-    t = sorted(tt)[len(tt) // 2]
-    r = {"us": round(t * 1000, 3), "gbs": round(b / (t / 1000) / 1e9, 1), "min_bytes": b,
-         "tiles": int(pl.info.n_tiles)}
-    if graph_reps:
-        g = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
+    r = {"min_bytes": int(pl.info.min_bytes), "tiles": int(pl.info.n_tiles),
+         "single_launch": _stats_us(tt)}
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        pl.run(ins, outs)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        for _ in range(graph_reps):
             pl.run(ins, outs)
-        torch.cuda.current_stream().wait_stream(side)
-        torch.cuda.synchronize()
-        with torch.cuda.graph(g):
-            for _ in range(graph_reps):
-                pl.run(ins, outs)
-        g.replay()
-        torch.cuda.synchronize()
-        tg = _time_steps(torch, g.replay, max(3, steps // 2), 1, lambda: None, stream)
-        tgm = sorted(tg)[len(tg) // 2] / graph_reps
-        r["us_graph"] = round(tgm * 1000, 3)
-        del g
+    g.replay()
+    torch.cuda.synchronize()
+    tg = _time_steps(torch, g.replay, max(3, steps // 2), 1, lambda: None, stream)
+    r["graph"] = _stats_us(tg, graph_reps)
+    r["graph"]["launches_per_replay"] = graph_reps
+    del g
     pl.free()
     return r
 
@@ -586,56 +732,45 @@ def run_workload(args):
     R = 8
     g = torch.Generator(device=dev)
     res = {"workload": args.workload, "peak_gbs": peak, "peak_kind": peak_kind}
-    # the floor of this timing method: a one-element kernel timed the same way (flush, then
-    # CUDA events around one launch); single-launch times below include it
+    # context for the single-launch times: a one-element kernel timed the same way (L2
+    # flush, then CUDA events around one launch)
     one = torch.zeros(1, device=dev)
     tfl = _time_steps(torch, lambda: one.add_(1), max(5, args.steps), args.warmup, flush, stream)
-    floor_us = sorted(tfl)[len(tfl) // 2] * 1000
-    res["launch_floor_us"] = round(floor_us, 3)
+    res["one_element_kernel_us"] = _stats_us(tfl)
     if args.workload == "sweep":
-        sizes = [1 << k for k in range(10, 29, 2)]  # 1 KiB .. 256 MiB per rank
+        # small sizes (1 KiB .. 4 MiB per rank): a single launch is dominated by its launch,
+        # so the per-collective time comes from 50 launches replayed from a CUDA graph;
+        # large sizes (16 MiB and up): measure_zero_copy
+        sizes = [1 << k for k in range(10, 29, 2)]
         if args.max_bytes:
             sizes = [m for m in sizes if m <= args.max_bytes]
         rows = []
-        for m in sizes:
+        for m in [m for m in sizes if m <= (4 << 20)]:
             n = m // 2
-            g.manual_seed(3)
-            ins = [((torch.rand(n, device=dev, generator=g) * 2 - 1).to(torch.bfloat16))
-                   .view(torch.int16) for _ in range(R)]
-            for kind in ("allreduce", "reduce_scatter", "allgather", "broadcast", "alltoall",
-                         "reduce_to_root", "gather", "scatter"):
+            ins = [synth.device_uniform_bf16(torch, 3000 + r, n, dev) for r in range(R)]
+            for kind in LARGE_KINDS:
                 nm = getattr(cdc, kind)(R, n, "bf16")
                 outs = [torch.empty(L, dtype=torch.int16, device=dev) for L in nm.out_len]
-                cfgs = {"twoshot": dict(datapath="twoshot")} if kind == "allreduce" else {"": {}}
-                if kind == "allreduce" and m <= (1 << 20):
-                    cfgs["oneshot"] = dict(datapath="oneshot")
+                cfgs = {"twoshot": dict(datapath="twoshot"), "oneshot": dict(datapath="oneshot")} \
+                    if kind == "allreduce" else {"": {}}
                 for tag, cfg in cfgs.items():
                     r = _zc_measure(torch, cdc, nm, ins, outs, args.steps, args.warmup, flush,
-                                    stream, graph_reps=50 if m <= (4 << 20) else 0, **cfg)
-                    net = max(r["us"] - floor_us, 1e-3)
-                    r.update({"collective": kind + (f"-{tag}" if tag else ""), "bytes_per_rank": m,
-                              "frac": round(r["gbs"] / peak, 4),
-                              "frac_excl_launch_floor": round(r["min_bytes"] / (net * 1e-6) / 1e9
-                                                              / peak, 4)})
+                                    stream, graph_reps=50, **cfg)
+                    r.update({"collective": kind + (f"-{tag}" if tag else ""), "bytes_per_rank": m})
                     rows.append(r)
                 del outs
             del ins
             torch.cuda.empty_cache()
-        res["rows"] = rows
+        res["small"] = rows
+        big = [m >> 20 for m in sizes if m >= (16 << 20)]
+        if big:
+            res["large"] = large_collectives(torch, cdc, dev, flush, stream, peak, args.steps,
+                                             args.warmup, sizes_mib=big)
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_oracle_collectives()
     elif args.workload == "prefill":
-        n = 8192 * 4096
-        g.manual_seed(4)
-        ins = [torch.randn(n, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
-               for _ in range(R)]
-        outs = [torch.empty(n, dtype=torch.int16, device=dev) for _ in range(R)]
-        nm = cdc.allreduce(R, n, "bf16")
-        for dp in ("twoshot", "oneshot"):
-            r = _zc_measure(torch, cdc, nm, ins, outs, args.steps, args.warmup, flush, stream,
-                            datapath=dp)
-            r["frac"] = round(r["gbs"] / peak, 4)
-            res[dp] = r
+        res.update(prefill_allreduce(torch, cdc, dev, flush, stream, peak, args.steps,
+                                     args.warmup))
     elif args.workload == "fig15":
         # SiFAR Fig. 15 grid: R = 2/4/8 ranks x 8/16/32 KB payloads, every protocol and
         # datapath, 2000 epochs per launch; microseconds per epoch (median of K launches)
@@ -702,34 +837,10 @@ def run_workload(args):
         res["rows"] = rows
         res["gemv"] = {"ranks": Rr, "outputs": n, "k_per_rank": k,
                        "weight_bytes_per_epoch": Rr * n * k * 2}
-    elif args.workload == "moe_combine":
-        T, H, E, k = 4096, 7168, 256, 8
-        routing = synth.zipf_topk_routing(5, R, T, E, k, 1.1)
-        nm = cdc.moe_combine(routing, E // R, H)
-        g.manual_seed(6)
-        ins = [torch.randn(L, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
-               for L in nm.in_len]
-        outs = [torch.empty(T * H, dtype=torch.int16, device=dev) for _ in range(R)]
-        r = _zc_measure(torch, cdc, nm, ins, outs, args.steps, args.warmup, flush, stream)
-        r["frac"] = round(r["gbs"] / peak, 4)
-        r["rows_per_rank"] = nm.meta["counts"]
-        res["combine"] = r
-        r2 = _zc_measure(torch, cdc, nm, ins, outs, args.steps, args.warmup, flush, stream,
-                         tma_min_bytes=(1 << 63))
-        r2["frac"] = round(r2["gbs"] / peak, 4)
-        res["combine_warp_kernel"] = r2
-    elif args.workload == "moe":
-        T, H, E, k = 4096, 7168, 256, 8
-        routing = synth.zipf_topk_routing(5, R, T, E, k, 1.1)
-        nm = cdc.moe_dispatch(routing, E // R, H)
-        g.manual_seed(5)
-        ins = [torch.randn(T * H, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
-               for _ in range(R)]
-        outs = [torch.empty(L, dtype=torch.int16, device=dev) for L in nm.out_len]
-        r = _zc_measure(torch, cdc, nm, ins, outs, args.steps, args.warmup, flush, stream)
-        r["frac"] = round(r["gbs"] / peak, 4)
-        r["rows_per_rank"] = nm.meta["counts"]
-        res["dispatch"] = r
+    elif args.workload in ("moe", "moe_combine"):
+        which = ("dispatch",) if args.workload == "moe" else ("combine",)
+        res.update(moe_collectives(torch, cdc, dev, flush, stream, peak, args.steps, args.warmup,
+                                   which=which))
     return res
 
 
@@ -742,7 +853,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-epochs", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--skip-large", action="store_true",
+                    help="leave out the large-payload collectives of the default run")
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "sweep", "prefill", "moe", "moe_combine", "fig15",
                              "fused"])

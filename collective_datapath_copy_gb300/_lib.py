@@ -67,7 +67,8 @@ class Config(C.Structure):
 
 class PlanInfo(C.Structure):
     _fields_ = [(n, C.c_uint64) for n in ("n_names", "n_jobs", "n_tiles", "n_units", "n_warps",
-                                          "min_bytes", "xbuf_bytes", "flag_bytes")]
+                                          "min_bytes", "xbuf_bytes", "flag_bytes",
+                                          "bulk_tile_bytes")]
 
 
 class Stats(C.Structure):

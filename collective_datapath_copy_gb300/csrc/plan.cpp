@@ -443,6 +443,7 @@ void coll_fill_info(const coll_compiled &c, coll_plan_info_t *info) {
   info->n_units = c.units.size();
   info->n_warps = c.warps.size();
   info->min_bytes = c.min_bytes;
+  info->bulk_tile_bytes = c.bulk ? c.bulk_slot : 0;
   const bool dual = c.cfg.protocol != COLL_PROTO_BARRIER;
   info->xbuf_bytes = c.cfg.zero_copy ? 0 : (c.xpar_bytes + c.rpar_bytes) * (dual ? 2 : 1);
   info->flag_bytes = c.cfg.zero_copy ? 0

@@ -171,6 +171,8 @@ typedef struct {
                             depends on read once + every named output byte written once */
   uint64_t xbuf_bytes;   /* staged exchange buffers (both parities)                   */
   uint64_t flag_bytes;   /* staged flag words                                         */
+  uint64_t bulk_tile_bytes; /* zero-copy: bytes per tile of the bulk (TMA) ring kernel the
+                               plan was compiled for; 0 = the warp kernel               */
 } coll_plan_info_t;
 
 typedef struct {

@@ -16,4 +16,6 @@ from .inputs import (  # noqa: F401
     zipf_topk_routing,
     random_naming,
     seeded_rng,
+    device_uniform_bf16,
+    device_normal_bf16,
 )

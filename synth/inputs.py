@@ -111,3 +111,28 @@ def random_naming(rng: np.random.Generator, n_ranks: int, max_len: int, max_segs
             out_segs.append((r, pos + gap, c, name))
             pos += gap + c
     return in_len, in_segs, out_len, out_segs
+
+
+def _device_trunc_bf16(torch, x):
+    """float32 device tensor -> bf16 bit patterns (int16), by the same truncation as
+    ``bf16_bits_from_f32_trunc`` (the upper 16 bits of each binary32 pattern)."""
+    return (x.view(torch.int32) >> 16).to(torch.int16)
+
+
+def device_uniform_bf16(torch, seed: int, shape, device, lo=-1.0, hi=1.0):
+    """uniform[lo, hi) bf16 patterns (int16 tensor) drawn on the device by torch's generator
+    seeded with `seed`: the recipe for inputs of hundreds of MiB per rank, which numpy would
+    take minutes to draw. Same distribution and truncation as ``uniform_bf16``; another
+    random stream."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    x = torch.rand(shape, device=device, generator=g, dtype=torch.float32) * (hi - lo) + lo
+    return _device_trunc_bf16(torch, x)
+
+
+def device_normal_bf16(torch, seed: int, shape, device):
+    """N(0,1) bf16 patterns (int16 tensor) drawn on the device (see device_uniform_bf16)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return _device_trunc_bf16(torch, torch.randn(shape, device=device, generator=g,
+                                                 dtype=torch.float32))

@@ -576,15 +576,13 @@ def test_moe_dispatch_full_size():
     plan.free()
 
 
-@pytest.mark.parametrize("kind", ["allreduce", "reduce_scatter", "allgather", "broadcast", "alltoall"])
+@pytest.mark.parametrize("kind", ["allreduce", "reduce_scatter", "allgather", "broadcast", "alltoall",
+                                  "reduce_to_root", "gather", "scatter"])
 def test_sweep_256mib_sampled(kind):
     # the largest sweep size: check 4096 sampled output elements per rank against the
     # oracle's definition evaluated at exactly those elements
     R, n = 8, (256 << 20) // 2
-    g = torch.Generator(device="cuda")
-    g.manual_seed(3)
-    ins = [((torch.rand(n, device="cuda", generator=g) * 2 - 1).to(torch.bfloat16)).view(torch.int16)
-           for _ in range(R)]
+    ins = [synth.device_uniform_bf16(torch, 3000 + r, n, "cuda") for r in range(R)]
     nm = getattr(namings, kind)(R, n, "bf16")
     dp = "twoshot" if kind == "allreduce" else "oneshot"
     plan = cdc.Plan(nm, zero_copy=1, datapath=dp)
@@ -593,27 +591,38 @@ def test_sweep_256mib_sampled(kind):
     assert plan.status()["code"] == 0
     rng = synth.seeded_rng(33)
     b = n // R
+
+    def pick(r, positions):  # input elements of rank r at the given positions
+        return from_dev(ins[r][torch.from_numpy(positions).cuda()], "bf16")
+
     for d in range(R):
+        if kind in ("reduce_to_root", "gather") and d != 0:
+            continue  # only the root's output is named
         L = nm.out_len[d]
         idx = np.sort(rng.integers(0, L, 4096))
-        it = torch.from_numpy(idx).cuda()
-        got = from_dev(outs[d][it], "bf16")
-        if kind in ("allreduce", "reduce_scatter"):
-            src = idx if kind == "allreduce" else idx + d * b
-            st = torch.from_numpy(src).cuda()
-            terms = [from_dev(x[st], "bf16") for x in ins]
-            want = collectives.allreduce(terms, "bf16")[0]
-        elif kind == "allgather":
-            want = np.array([from_dev(ins[i // n][i % n:i % n + 1], "bf16")[0] for i in idx[:256]])
-            got = got[:256]
+        got = from_dev(outs[d][torch.from_numpy(idx).cuda()], "bf16")
+        if kind in ("allreduce", "reduce_scatter", "reduce_to_root"):
+            src = idx + d * b if kind == "reduce_scatter" else idx
+            want = collectives.allreduce([pick(r, src) for r in range(R)], "bf16")[0]
+        elif kind in ("allgather", "gather"):
+            # output element i is element i % n of rank i // n's input
+            want = np.empty(idx.size, np.uint16)
+            for s_ in range(R):
+                m = idx // n == s_
+                if m.any():
+                    want[m] = pick(s_, idx[m] % n)
         elif kind == "broadcast":
-            want = from_dev(ins[0][it], "bf16")
+            want = pick(0, idx)
+        elif kind == "scatter":
+            want = pick(0, idx + d * b)
         else:
-            s_idx = idx // b
-            want = np.array([from_dev(ins[s][d * b + (i % b):d * b + (i % b) + 1], "bf16")[0]
-                             for s, i in zip(s_idx[:256], idx[:256])])
-            got = got[:256]
-        assert bits_equal(got, want), kind
+            # all-to-all: block s of rank d's output is block d of rank s's input
+            want = np.empty(idx.size, np.uint16)
+            for s_ in range(R):
+                m = idx // b == s_
+                if m.any():
+                    want[m] = pick(s_, d * b + idx[m] % b)
+        assert bits_equal(got, want), (kind, d)
     plan.free()
     del outs, ins
     torch.cuda.empty_cache()
