@@ -3,11 +3,13 @@
 Default workload (one "step"): the tensor-parallel decode all-reduce — R=8 emulated ranks,
 4096 bf16 (8 KiB) per rank, N(0,1) values from seed 2, a pool of 7 input sets, 10,000
 back-to-back epochs in one persistent launch with the speculative protocol (dual
-buffers, content-tagged reduced-flag validation). Metric: microseconds per epoch.
+buffers, fence-free content-tagged validation of the reduced flag, 200 ns speculation
+delay). Metric: microseconds per epoch.
 
-Also measured in the same run and reported as extra keys: the barrier and dual-buffer
-protocols, a staggered-start stress run of the speculative protocol, and the
-prefill-sized all-reduce (8 x 64 MiB, one-shot vs two-shot) as achieved HBM GB/s.
+Also measured in the same run and reported as extra keys: the other protocols and checks,
+a staggered-start stress run, per-epoch latency percentiles, and every large-payload
+configuration (eight collectives at 16, 64 and 256 MiB per rank, the prefill all-reduce
+one-shot and two-shot, MoE dispatch and combine) as achieved HBM GB/s.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload decode|sweep|prefill|moe|moe_combine|fig15|fused]
@@ -209,16 +211,17 @@ def measure_zero_copy(torch, cdc, nm, in_sets, out_sets, steps, warmup, flush, s
     - single: one launch right after an L2 flush (CUDA events around the launch; the time
       includes the launch and the event pair, about 5 us that a one-element kernel timed the
       same way also takes);
-    - stream: 2 x len(in_sets) launches back to back, cycling over input/output sets that
-      together exceed L2, so every launch reads inputs no recent launch touched; per-launch
-      time = the step's time / launches (launch overheads overlap the previous launch).
+    - stream: launches back to back (six, or four when the sets are large), cycling over
+      input/output sets that together exceed L2, so every launch reads inputs no recent
+      launch left in L2; per-launch time = the step's time / launches (launch overheads
+      overlap the previous launch).
     GB/s and the fraction of `peak` are over the plan's minimal bytes (each input byte a
     named output depends on read once, each named output byte written once)."""
     pl = cdc.Plan(nm, zero_copy=1, **cfg)
     runs = [pl.bind(i, o) for i, o in zip(in_sets, out_sets)]
     b = int(pl.info.min_bytes)
     one = _time_steps(torch, runs[0], steps, warmup, flush, stream)
-    seq = runs * 2
+    seq = runs * max(2, 6 // len(runs))
     many = _time_stream(torch, seq, steps, 1, flush, stream)
     st = pl.status()
     if st["code"] != 0:
@@ -233,6 +236,13 @@ def measure_zero_copy(torch, cdc, nm, in_sets, out_sets, steps, warmup, flush, s
         res[key] = r
     res["stream"]["launches_per_step"] = len(seq)
     return res
+
+
+def _cold_sets(set_bytes):
+    """Input/output sets to cycle through in the back-to-back measurement so that no launch
+    finds its data in L2: three below L2's size, two up to four times it, one beyond (a
+    launch then evicts everything the previous one touched)."""
+    return 3 if set_bytes < L2_BYTES else (2 if set_bytes < 4 * L2_BYTES else 1)
 
 
 LARGE_KINDS = ("allreduce", "reduce_scatter", "allgather", "broadcast", "alltoall",
@@ -250,8 +260,7 @@ def large_collectives(torch, cdc, dev, flush, stream, peak, steps, warmup,
         n = (mib << 20) // 2
         for kind in LARGE_KINDS:
             nm = getattr(cdc, kind)(R, n, "bf16")
-            set_bytes = 2 * (sum(nm.in_len) + sum(nm.out_len))
-            nsets = max(2, min(3, int(3 * L2_BYTES // set_bytes) + 1))
+            nsets = _cold_sets(2 * (sum(nm.in_len) + sum(nm.out_len)))
             in_sets = [[synth.device_uniform_bf16(torch, 3000 + 100 * k + r, n, dev)
                         for r in range(R)] for k in range(nsets)]
             out_sets = [[torch.empty(L, dtype=torch.int16, device=dev) for L in nm.out_len]
@@ -272,10 +281,11 @@ def prefill_allreduce(torch, cdc, dev, flush, stream, peak, steps, warmup):
     (reduce once, push to every rank) and one-shot (every rank reduces all eight)."""
     R, n = 8, 8192 * 4096
     nm = cdc.allreduce(R, n, "bf16")
+    ns = _cold_sets(2 * 2 * R * n)
     in_sets = [[synth.device_normal_bf16(torch, 4000 + 100 * k + r, n, dev) for r in range(R)]
-               for k in range(2)]
+               for k in range(ns)]
     out_sets = [[torch.empty(n, dtype=torch.int16, device=dev) for _ in range(R)]
-                for _ in range(2)]
+                for _ in range(ns)]
     res = {dp: measure_zero_copy(torch, cdc, nm, in_sets, out_sets, steps, warmup, flush,
                                  stream, peak, datapath=dp)
            for dp in ("twoshot", "oneshot")}
@@ -294,10 +304,11 @@ def moe_collectives(torch, cdc, dev, flush, stream, peak, steps, warmup,
     res = {}
     for name in which:
         nm = (cdc.moe_dispatch if name == "dispatch" else cdc.moe_combine)(routing, E // R, H)
+        ns = _cold_sets(2 * (sum(nm.in_len) + sum(nm.out_len)))
         in_sets = [[synth.device_normal_bf16(torch, 5000 + 100 * s_ + r, L, dev)
-                    for r, L in enumerate(nm.in_len)] for s_ in range(2)]
+                    for r, L in enumerate(nm.in_len)] for s_ in range(ns)]
         out_sets = [[torch.empty(L, dtype=torch.int16, device=dev) for L in nm.out_len]
-                    for _ in range(2)]
+                    for _ in range(ns)]
         res[name] = measure_zero_copy(torch, cdc, nm, in_sets, out_sets, steps, warmup, flush,
                                       stream, peak)
         res[name]["rows_per_rank"] = [int(c) for c in nm.meta["counts"]]
@@ -320,22 +331,22 @@ def large_payloads(torch, cdc, dev, flush, stream, peak, steps, warmup):
 
 def large_rooflines(large, peak, peak_kind):
     """Roofline records of the two zero-copy kernels at full size: the bulk (TMA) ring on the
-    prefill two-shot all-reduce and the warp kernel on MoE dispatch. achieved = minimal
-    bytes per launch / the per-launch time of the back-to-back ('stream') measurement;
-    traffic = DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    kernel's current sources."""
+    prefill two-shot all-reduce and the warp kernel on MoE combine (uneven producer counts).
+    achieved = minimal bytes per launch / the per-launch time of the back-to-back ('stream')
+    measurement; traffic = DRAM bytes per launch from the committed ncu summary, if it was
+    taken on the kernel's current sources."""
     out = {}
-    for key, r, kern, srcs in (
-            ("bulk_kernel: prefill all-reduce two-shot, 8 x 64 MiB",
-             large["prefill_allreduce_64MiB"]["twoshot"], "bulk_kernel/prefill_twoshot",
-             BULK_SOURCES),
-            ("zc_kernel: MoE dispatch, 8 x 4096 x 7168", large["moe"]["dispatch"],
-             "zc_kernel/moe_dispatch", ENGINE_SOURCES)):
+    for what, r in (("prefill all-reduce two-shot, 8 x 64 MiB",
+                     large["prefill_allreduce_64MiB"]["twoshot"]),
+                    ("MoE combine, 8 x 4096 x 7168", large["moe"]["combine"])):
         st = r["stream"]
-        out[key] = {"bound": "hbm", "achieved": st["gbs"], "peak": peak, "unit": "GB/s",
-                    "frac": round(st["gbs"] / peak, 4), "peak_kind": f"of {peak_kind}",
-                    "traffic": recorded_traffic(kern, srcs), "algorithmic_bytes": r["min_bytes"],
-                    "us_per_launch": st["us_median"]}
+        kern = r["kernel"]
+        srcs = BULK_SOURCES if kern == "bulk_kernel" else ENGINE_SOURCES
+        out[f"{kern}: {what}"] = {
+            "bound": "hbm", "achieved": st["gbs"], "peak": peak, "unit": "GB/s",
+            "frac": round(st["gbs"] / peak, 4), "peak_kind": f"of {peak_kind}",
+            "traffic": recorded_traffic(f"{kern}/{what.split(',')[0]}", srcs),
+            "algorithmic_bytes": r["min_bytes"], "us_per_launch": st["us_median"]}
     return out
 
 
@@ -368,7 +379,8 @@ def run_ours(args, rank, world, dist):
         ("barrier", dict(protocol="barrier")),
         ("spec_stagger", dict(protocol="spec", inject="stagger", inject_seed=2,
                               inject_prob_ppm=100000, inject_max_ns=20000, inject_start_ns=5000)),
-        ("spec_relaxed", dict(protocol="spec", spec_check="relaxed")),
+        ("spec_fenced", dict(protocol="spec", spec_check="tagged")),
+        ("spec_no_delay", dict(protocol="spec", spec_delay_ns=0)),
         ("spec_literal", dict(protocol="spec", spec_check="literal")),
         ("spec_twoshot", dict(protocol="spec", datapath="twoshot")),
         ("spec_twoshot_pull", dict(protocol="spec", datapath="twoshot_pull")),
@@ -399,7 +411,7 @@ def run_ours(args, rank, world, dist):
 
     # other protocols (same K/W)
     proto = {}
-    for name in ("dual", "barrier", "spec_stagger", "spec_relaxed", "spec_literal",
+    for name in ("dual", "barrier", "spec_stagger", "spec_fenced", "spec_no_delay", "spec_literal",
                  "spec_twoshot", "spec_twoshot_pull", "ll", "ll_chain", "spec_chain", "dual_chain",
                  "barrier_chain"):
         tt = _time_steps(torch, step(name), max(3, args.steps // 2), 1, flush, stream)
@@ -423,14 +435,15 @@ def run_ours(args, rank, world, dist):
     d = np.diff(stamps) / 1000.0
     lat = {"p50_us": round(float(np.percentile(d, 50)), 3),
            "p99_us": round(float(np.percentile(d, 99)), 3),
-           "engine": "general (stamped): per-epoch stamps run the instrumented engine, the "
-                     "timed value the variant specialised for this plan"} if d.size else {}
+           "p999_us": round(float(np.percentile(d, 99.9)), 3),
+           "engine": "the specialised variant of the timed run, with one %globaltimer stamp "
+                     "per epoch (first warp)"} if d.size else {}
     sp.free()
     # where an epoch's time goes (first warp): stage+notify, wait/validate, store+rest
-    # (measured on the general, stamped engine)
+    # (four stamps per epoch run the general engine)
     phases = {}
     for name, cfg in [("spec", dict(protocol="spec")), ("dual", dict(protocol="dual")),
-                      ("spec_relaxed", dict(protocol="spec", spec_check="relaxed")),
+                      ("spec_fenced", dict(protocol="spec", spec_check="tagged")),
                       ("ll", dict(protocol="ll"))]:
         pp = cdc.Plan(nm, record_stamps=2, stamp_capacity=EPOCHS, **cfg)
         pp.run(ins, outs, **kw)
@@ -520,7 +533,8 @@ def run_ours(args, rank, world, dist):
         "data": "synthetic (seeded N(0,1) bf16, pool of 7 input sets)",
         "config": {"workload": "TP decode all-reduce: R=8 emulated ranks x 4096 bf16 per rank, "
                                "10000 epochs per step in one persistent launch, speculative "
-                               "protocol (dual buffers, tagged validation), oneshot",
+                               "protocol (dual buffers, fence-free content-tagged validation, "
+                               "200 ns speculation delay), oneshot",
                    "ranks": R_DECODE, "elems_per_rank": N_DECODE, "epochs_per_step": EPOCHS,
                    "input_pool": POOL, "protocol": "spec", "l2": "flushed before every timed "
                    "step (256 MiB written, then another 256 MiB read)",

@@ -61,7 +61,7 @@ class Config(C.Structure):
                 ("inject_rank", C.c_int32), ("inject_prob_ppm", C.c_uint32),
                 ("inject_max_ns", C.c_uint64), ("inject_start_ns", C.c_uint64),
                 ("inject_pause_ns", C.c_uint64), ("chain", C.c_int32),
-                ("reserved2", C.c_int32), ("reduce_order", C.c_int32),
+                ("spec_delay_ns", C.c_int32), ("reduce_order", C.c_int32),
                 ("reserved3", C.c_int32)]
 
 

@@ -127,7 +127,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // Tensor maps of the fused run's weight matrices W_r ([k rows][in_len[r] bf16], rows
-// in_bytes[r] apart), boxes of 256 columns x 16 rows; reused while the run's matrices and
+// in_bytes[r] apart), boxes of 256 columns x 64 rows; reused while the run's matrices and
 // k stay the same.
 int gemv_maps(coll_plan_s *p, const void *const *wt, uint32_t k) {
   const coll_compiled &c = p->c;
@@ -145,7 +145,7 @@ int gemv_maps(coll_plan_s *p, const void *const *wt, uint32_t k) {
     if (!c.in_used[r]) continue;
     const cuuint64_t dims[2] = {(cuuint64_t)(c.in_bytes[r] / 2), (cuuint64_t)k};
     const cuuint64_t strides[1] = {(cuuint64_t)c.in_bytes[r]};
-    const cuuint32_t box[2] = {256, 16};
+    const cuuint32_t box[2] = {256, 64};
     const cuuint32_t estr[2] = {1, 1};
     if (dims[0] > 0xFFFFFFFFull || strides[0] >= (1ull << 40)) return COLL_EINVAL;
     if (encode(&p->gmaps->m[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(wt[r]),
@@ -275,15 +275,17 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
   const coll_compiled &c = p->c;
   const int R = c.R;
   if (wt) {
-    // eight warps each take k/8 rows, sixteen at a time: k must be a multiple of 128
-    if (c.cfg.zero_copy || c.dtype != COLL_BF16 || k < 128 || (k & 127u)) return COLL_EINVAL;
+    // the compute takes the rows sixteen at a time and x is staged whole: k is a multiple
+    // of 16, at most 8192
+    if (c.cfg.zero_copy || c.dtype != COLL_BF16 || k < 16 || (k & 15u) || k > 8192)
+      return COLL_EINVAL;
     if (c.cfg.protocol == COLL_PROTO_LL) return COLL_EINVAL;  // tagged data is not fused
     for (int r = 0; r < R; ++r) {
       if (!c.in_used[r]) continue;
       if (!wt[r]) return COLL_EINVAL;
       if (((uintptr_t)wt[r] & 15u) || (c.in_bytes[r] & 15u)) return COLL_EALIGN;
     }
-    // the fused CTAs are larger (twelve warps and a shared-memory ring): all must still fit
+    // the fused CTAs are larger (eight warps and a shared-memory ring): all must still fit
     if (p->gemv_cap < 0 &&
         coll::engine_gemv_max_coresident(c.rpar_bytes != 0, &p->gemv_cap) != cudaSuccess) {
       cudaGetLastError();
@@ -434,6 +436,10 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
     a.out_stride = out_epoch_stride;
     a.protocol = c.cfg.protocol;
     a.spec_check = c.cfg.spec_check;
+    a.spec_delay_ns =
+        c.cfg.protocol != COLL_PROTO_SPEC ? 0u
+        : c.cfg.spec_delay_ns >= 0      ? (uint32_t)c.cfg.spec_delay_ns
+        : c.cfg.spec_check == COLL_SPEC_TAGGED_RELAXED ? 200u : 0u;
     a.spin_ns = c.cfg.spin_limit_ns ? c.cfg.spin_limit_ns : 2000000000ull;
     a.inject_flags = c.cfg.inject_flags;
     a.inject_seed = c.cfg.inject_seed;

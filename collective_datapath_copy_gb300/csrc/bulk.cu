@@ -26,7 +26,11 @@ constexpr uint32_t kConsumerWarps = 8;
 constexpr unsigned FULLW = 0xFFFFFFFFu;
 constexpr uint32_t kThreads = 32 * (kConsumerWarps + 1);
 
-struct StageHdr {
+// A resolved tile: its sources and destinations as pointers, sizes and counts. The
+// producer warp resolves tiles 32 at a time (one per lane) into one half of a two-batch
+// table in shared memory; a stage records which entry it holds.
+struct TileRec {
+  const char *src[COLL_BULK_MAX_SRC];
   char *dst[COLL_BULK_MAX_DST];
   uint32_t nbytes, nsrc, ndst, pad;
 };
@@ -44,13 +48,14 @@ __device__ void bulk_timeout(coll_dev_status_t *st, uint32_t tile) {
 template <int KIND, bool TREE>
 __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ TileRec table[2][32];
   __shared__ volatile uint32_t s_abort;
   __shared__ uint32_t s_issued;
   const uint32_t S = a.stages;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
   uint64_t *empty = full + S;
-  StageHdr *hdr = reinterpret_cast<StageHdr *>(empty + S);
-  const uint32_t head = ((16u * S + (uint32_t)sizeof(StageHdr) * S) + 127u) & ~127u;
+  uint32_t *stile = reinterpret_cast<uint32_t *>(empty + S);  // table entry of each stage
+  const uint32_t head = ((16u * S + 4u * S) + 127u) & ~127u;
   unsigned char *data = smem + head;
   const uint32_t stage_bytes = a.maxsrc * a.slot_bytes;
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
@@ -69,21 +74,17 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
 
   uint32_t consumed = 0;
   if (warp == 0) {
-    // Producer warp. Tiles are resolved 32 at a time, one per lane: each tile's record
-    // carries its sources and destinations (rank, offset), so a batch costs one memory
-    // round trip; lane 0 then issues each tile's bulk loads.
-    uint32_t k = 0;
+    // Producer warp. Each batch: lane i resolves tile t0 + i * grid from its record (one
+    // memory round trip for 32 tiles) into table[batch & 1][i]. Then, tile by tile: lane 0
+    // waits for the stage to be free, records the tile's entry and the bytes to expect, and
+    // lanes j < nsrc each issue source j's bulk copy. The table half of batch m + 1 is
+    // written only after every tile of batch m was issued, by which time the consumers
+    // have released every tile of batch m - 1 (the ring has fewer than 32 stages).
+    uint32_t k = 0, s = 0, lap = 0, half = 0;
     bool stop = false;
-    for (uint64_t t0 = blockIdx.x; t0 < total && !stop; t0 += 32ull * gridDim.x) {
+    for (uint64_t t0 = blockIdx.x; t0 < total && !stop; t0 += 32ull * gridDim.x, half ^= 1u) {
       const uint64_t t = t0 + (uint64_t)lane * gridDim.x;
       const bool have = t < total;
-      uint32_t nbytes = 0, nsrc = 0, ndst = 0;
-      const char *sp[COLL_BULK_MAX_SRC];
-      char *dp[COLL_BULK_MAX_DST];
-#pragma unroll
-      for (uint32_t j = 0; j < COLL_BULK_MAX_SRC; ++j) sp[j] = nullptr;
-#pragma unroll
-      for (uint32_t d = 0; d < COLL_BULK_MAX_DST; ++d) dp[d] = nullptr;
       if (have) {
         const uint32_t e = (uint32_t)(t / a.ntiles);
         const uint4 *rec = reinterpret_cast<const uint4 *>(a.btiles + (t - (uint64_t)e * a.ntiles));
@@ -91,34 +92,39 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
 #pragma unroll
         for (uint32_t q = 0; q < 9; ++q) w[q] = ld_nc_v4(rec + q);
         const uint64_t start = ((uint64_t)w[0].y << 32) | w[0].x;
-        nbytes = w[0].z;
-        nsrc = w[0].w & 0xFFFFu;
-        ndst = w[0].w >> 16;
-        uint64_t ref[COLL_BULK_MAX_SRC + COLL_BULK_MAX_DST];
-#pragma unroll
-        for (uint32_t q = 0; q < 8; ++q) {
-          ref[2 * q] = ((uint64_t)w[q + 1].y << 32) | w[q + 1].x;
-          ref[2 * q + 1] = ((uint64_t)w[q + 1].w << 32) | w[q + 1].z;
-        }
+        TileRec &tr = table[half][lane];
+        tr.nbytes = w[0].z;
+        tr.nsrc = w[0].w & 0xFFFFu;
+        tr.ndst = w[0].w >> 16;
         const int64_t ioff = (int64_t)(e % (uint32_t)a.in_pool) * a.in_stride + (int64_t)start;
         const int64_t ooff = (int64_t)e * a.out_stride + (int64_t)start;
         constexpr uint64_t kOffMask = (1ull << 56) - 1u;
 #pragma unroll
-        for (uint32_t j = 0; j < COLL_BULK_MAX_SRC; ++j)
-          if (j < nsrc)
-            sp[j] = a.ptr.in[(uint32_t)(ref[j] >> 56)] + (ref[j] & kOffMask) + ioff;
-#pragma unroll
-        for (uint32_t d = 0; d < COLL_BULK_MAX_DST; ++d)
-          if (d < ndst) {
-            const uint64_t r = ref[COLL_BULK_MAX_SRC + d];
-            dp[d] = a.ptr.out[(uint32_t)(r >> 56)] + (r & kOffMask) + ooff;
+        for (uint32_t q = 0; q < 8; ++q) {
+          const uint64_t rs = ((uint64_t)w[q + 1].y << 32) | w[q + 1].x;   // ref 2q
+          const uint64_t rd = ((uint64_t)w[q + 1].w << 32) | w[q + 1].z;   // ref 2q + 1
+          // refs 0..7 are sources, 8..15 destinations
+          const uint64_t r0 = rs, r1 = rd;
+          const uint32_t i0 = 2 * q, i1 = 2 * q + 1;
+          if (i0 < COLL_BULK_MAX_SRC) {
+            tr.src[i0] = i0 < tr.nsrc ? a.ptr.in[(uint32_t)(r0 >> 56)] + (r0 & kOffMask) + ioff : nullptr;
+          } else {
+            const uint32_t d = i0 - COLL_BULK_MAX_SRC;
+            tr.dst[d] = d < tr.ndst ? a.ptr.out[(uint32_t)(r0 >> 56)] + (r0 & kOffMask) + ooff : nullptr;
           }
+          if (i1 < COLL_BULK_MAX_SRC) {
+            tr.src[i1] = i1 < tr.nsrc ? a.ptr.in[(uint32_t)(r1 >> 56)] + (r1 & kOffMask) + ioff : nullptr;
+          } else {
+            const uint32_t d = i1 - COLL_BULK_MAX_SRC;
+            tr.dst[d] = d < tr.ndst ? a.ptr.out[(uint32_t)(r1 >> 56)] + (r1 & kOffMask) + ooff : nullptr;
+          }
+        }
       }
       const uint32_t batch = __popc(__ballot_sync(FULLW, have));
+      __syncwarp();  // the table half is written before any lane reads it
       for (uint32_t i = 0; i < batch; ++i, ++k) {
-        const uint32_t s = k % S;
         bool ok = true;
-        if (lane == 0) ok = mbar_wait(&empty[s], ((k / S) & 1u) ^ 1u, a.spin_ns, &s_abort);
+        if (lane == 0) ok = mbar_wait(&empty[s], (lap & 1u) ^ 1u, a.spin_ns, &s_abort);
         ok = __shfl_sync(FULLW, ok, 0);
         if (!ok) {
           if (lane == 0) {
@@ -128,43 +134,36 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
           stop = true;
           break;
         }
-        const uint32_t nb = __shfl_sync(FULLW, nbytes, i);
-        const uint32_t ns = __shfl_sync(FULLW, nsrc, i);
-        const uint32_t nd = __shfl_sync(FULLW, ndst, i);
-        StageHdr &h = hdr[s];
-#pragma unroll
-        for (uint32_t d = 0; d < COLL_BULK_MAX_DST; ++d) {
-          char *q = (char *)__shfl_sync(FULLW, (uintptr_t)dp[d], i);
-          if (lane == 0 && d < nd) h.dst[d] = q;
-        }
+        const TileRec &tr = table[half][i];
+        const uint32_t nb = tr.nbytes, ns = tr.nsrc;
         if (lane == 0) {
-          h.nbytes = nb;
-          h.nsrc = ns;
-          h.ndst = nd;
+          stile[s] = half * 32u + i;
           mbar_expect_tx(&full[s], ns * nb);
+          s_issued = k + 1;
         }
-        unsigned char *sd = data + (size_t)s * stage_bytes;
-#pragma unroll
-        for (uint32_t j = 0; j < COLL_BULK_MAX_SRC; ++j) {
-          const char *p = (const char *)__shfl_sync(FULLW, (uintptr_t)sp[j], i);
-          if (lane == 0 && j < ns) bulk_load(sd + (size_t)j * a.slot_bytes, p, nb, &full[s]);
+        __syncwarp();  // the bytes are expected before any copy can complete them
+        if (lane < ns)
+          bulk_load(data + (size_t)s * stage_bytes + (size_t)lane * a.slot_bytes, tr.src[lane], nb,
+                    &full[s]);
+        if (++s == S) {
+          s = 0;
+          ++lap;
         }
-        if (lane == 0) s_issued = k + 1;
       }
     }
   } else {
     const uint32_t ctid = threadIdx.x - 32;  // consumer thread index
     const uint32_t slot_vec = a.slot_bytes >> 4;
-    uint32_t k = 0;
+    uint32_t k = 0, s = 0, lap = 0;
     for (uint64_t t = blockIdx.x; t < total; t += gridDim.x, ++k) {
-      const uint32_t s = k % S;
-      const bool ok = __all_sync(FULLW, mbar_wait(&full[s], (k / S) & 1u, a.spin_ns, &s_abort));
+      const bool ok = __all_sync(FULLW, mbar_wait(&full[s], lap & 1u, a.spin_ns, &s_abort));
       if (!ok) {
         if (lane == 0) bulk_timeout(a.st, (uint32_t)t);
         s_abort = 1;
         break;
       }
-      const StageHdr &h = hdr[s];
+      const uint32_t ent = stile[s];
+      const TileRec &h = table[ent >> 5][ent & 31u];
       const uint32_t nvec = h.nbytes >> 4, nsrc = h.nsrc, ndst = h.ndst;
       const uint4 *sd = reinterpret_cast<const uint4 *>(data + (size_t)s * stage_bytes);
       for (uint32_t v = ctid; v < nvec; v += 32 * kConsumerWarps) {
@@ -192,6 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       consumed = k + 1;
+      if (++s == S) {
+        s = 0;
+        ++lap;
+      }
     }
   }
   __syncthreads();
@@ -207,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
 }  // namespace
 
 uint32_t bulk_smem_bytes(uint32_t stages, uint32_t maxsrc, uint32_t slot_bytes) {
-  const uint32_t head = ((16u * stages + (uint32_t)sizeof(StageHdr) * stages) + 127u) & ~127u;
+  const uint32_t head = ((16u * stages + 4u * stages) + 127u) & ~127u;
   return head + stages * maxsrc * slot_bytes;
 }
 

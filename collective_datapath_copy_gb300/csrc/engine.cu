@@ -330,58 +330,60 @@ __device__ __forceinline__ uint4 gather_pieces(const char *xb, uint32_t nbytes, 
 }
 
 // ------------------------------------------------------------------ fused producer
-// The fused-producer variant runs twelve warps per CTA in three warpgroups. Warp 0 plays the
-// engine warp; warps 4..11 are compute warps: at each stage compute warp b computes k-block b
-// of the piece's dot products (lane l: outputs 8l..8l+7). Block b covers rows
-// [b*k/8, (b+1)*k/8): products rounded to binary32, added in row order from the block's
-// first product; warp 0 then adds the eight block sums in block order and rounds once to
-// bf16. Warps 1..3 only complete the first warpgroup. The register file is split by
-// warpgroup (setmaxnreg): the engine's warpgroup takes 248 registers a thread, the compute
-// warpgroups 120, so neither the engine state nor the compute loop spills.
-//
-// The weight rows reach the compute warps through shared-memory slots of 16 rows, each
-// filled by one tensor copy (TMA: a box of 256 columns x 16 rows of W_r, so a ragged last
-// piece reads zeros past the matrix); each compute warp owns 3 slots (a private ring) and
-// streams its own k-block through them. Fill q of warp b (its q-th slot of rows over the run:
-// piece q / (k/128), slot q % (k/128) of block b, pieces in epoch-major stage-item order)
-// lands in the warp's slot q % 3; having read fill q, the warp issues fill q + 3 into the
-// same slot. So each warp always has its next 3 slots (48 rows) in flight: while the engine
-// warp runs the exchange of one epoch, the next piece's rows are already arriving (the
-// weights do not depend on the epoch's data). Few large fills beat many small ones here:
-// streaming rows through shared memory is bound by its bandwidth (every byte is written by
-// the copy and read once), and each fill costs a fixed wait and issue on top.
-constexpr uint32_t kGemvWarps = 8;                                   // compute warps
-constexpr uint32_t kGemvFirst = 4;                                   // warp of compute warp 0
-constexpr uint32_t kGemvThreads = 32 * (kGemvFirst + kGemvWarps);   // 384
-constexpr uint32_t kGemvBarThreads = 32 * (1 + kGemvWarps);          // engine + compute warps
-constexpr uint32_t kGemvLaunchRegs = 168;  // per thread at launch: 65536 / 384, rounded to 8
-constexpr uint32_t kGemvEngineRegs = 248;  // engine warpgroup after the split
-constexpr uint32_t kGemvComputeRegs = 120; // compute warpgroups after the split
-static_assert(128 * kGemvEngineRegs + 256 * kGemvComputeRegs <= kGemvThreads * kGemvLaunchRegs,
-              "the split must fit in the registers the CTA was launched with");
-constexpr uint32_t kGemvRows = 16;                       // weight rows per ring slot (one copy)
-constexpr uint32_t kGemvCols = 256;                      // bf16 columns per copied row (a piece)
-constexpr uint32_t kGemvPitch = 2 * kGemvCols;           // bytes per staged row
-constexpr uint32_t kGemvSlotBytes = kGemvRows * kGemvPitch;
-constexpr uint32_t kGemvSlotsPerWarp = 3;
-constexpr uint32_t kGemvSlots = kGemvSlotsPerWarp * kGemvWarps;  // 192 KiB of rows in flight
-// (the ring starts 128-byte aligned: the tensor copies land there)
-constexpr uint32_t kGemvSmemBytes = kGemvSlots * kGemvSlotBytes + kGemvSlots * 8 + 128;
-constexpr uint32_t kGemvMaxItems = 16;                   // stage items whose rows are cached
+// The fused-producer variant computes each rank's payload piece as y = W_r x in the stage
+// step: for every output column, the k products (rounded to binary32) added in row order
+// from the first one, then rounded once to bf16 — the plain definition of the dot product,
+// in the order it is written. A CTA runs eight warps:
+//   warp 0      the engine warp (the staged protocol, unchanged);
+//   warp 1      the weight streamer: lane 0 fills a ring of shared-memory slots, each one
+//               tensor copy (TMA) of 64 rows x 256 columns of W_r, for the pieces of the
+//               whole run in order (the weights do not depend on the epoch's data, so it
+//               runs ahead by as many slots as the ring holds, across exchanges);
+//   warp 2      the x streamer: lane 0 copies piece q's x (k bf16, one bulk copy) into one
+//               of two buffers, once the engine has opened piece q (that also frees the
+//               buffer: piece q is opened only after piece q - 2 was taken, whose x was read
+//               before its results were written);
+//   warp 3      idle;
+//   warps 4..7  compute warps: lane l of compute warp w owns columns 64w + 2l and
+//               64w + 2l + 1 of the piece and carries their two chains over all k rows
+//               (packed binary32 pairs), so no order is split; it writes the rounded
+//               results into one of two result slots.
+// The engine takes piece q's results from its slot and opens piece q + 2 (at most one
+// piece computed ahead; the result slot of piece q + 2 is the one just taken): without chained epochs the next piece is computed while the
+// engine runs the current exchange. With chained epochs an epoch's pieces are opened only
+// after the rank's previous epoch is complete, as the next layer's input would depend on it.
+// Every wait is bounded by the plan's spin limit and stops on the abort word or when the
+// engine ends the run; the streamers then wait (bounded) for the copies they issued.
+constexpr uint32_t kGemvComputeWarps = 4;
+constexpr uint32_t kGemvFirst = 4;                        // warp of compute warp 0
+constexpr uint32_t kGemvThreads = 32 * (kGemvFirst + kGemvComputeWarps);  // 256
+constexpr uint32_t kGemvRows = 64;                        // weight rows per slot (one copy)
+constexpr uint32_t kGemvCols = 256;                       // bf16 columns of a piece
+constexpr uint32_t kGemvPitch = 2 * kGemvCols;            // bytes per staged row
+constexpr uint32_t kGemvSlotBytes = kGemvRows * kGemvPitch;  // 32 KiB
+constexpr uint32_t kGemvSlots = 5;                        // 160 KiB of rows in flight
+constexpr uint32_t kGemvMaxK = 8192;                      // rows of W_r (length of x)
+constexpr uint32_t kGemvXBytes = 2 * kGemvMaxK;
+constexpr uint32_t kGemvMaxItems = 16;                    // stage items whose rows are cached
+// dynamic shared memory: ring, two x buffers, two result slots, barriers (+128 for the
+// alignment of the ring, where the tensor copies land)
+constexpr uint32_t kGemvBars = 2 * kGemvSlots + 4;
+constexpr uint32_t kGemvSmemBytes =
+    kGemvSlots * kGemvSlotBytes + 2 * kGemvXBytes + 2 * kGemvPitch + kGemvBars * 8 + 128;
 
 struct GemvShared {
-  const char *xp;    // x vector of this epoch
-  uint32_t active;   // lanes below this hold outputs
-  uint32_t exit;     // set by warp 0: the other warps return
-  uint32_t fail;     // a compute warp's ring wait gave up
-  uint32_t nitems;   // stage items of this warp, in order
-  uint32_t S;        // slots per piece
-  uint64_t total;    // fills of the whole run, per compute warp
+  uint64_t go;          // pieces the compute may start (written by warp 0, release.cta)
+  uint64_t chain_open;  // with chained epochs: pieces of the epochs already allowed
+  uint64_t total;       // pieces of the run (epochs x items)
+  uint64_t taken;       // pieces whose results warp 0 has taken
+  uint32_t exit;        // set by warp 0 when its loop ends: the other roles stop
+  uint32_t nitems;      // stage items of this warp, in order
+  uint32_t kslots;      // slots per piece (k / 64, rounded up)
+  uint32_t k;
   const CUtensorMap *maps;                 // W_r of each rank (kernel parameters)
   const CUtensorMap *wmap[kGemvMaxItems];  // each cached item's matrix ...
-  uint32_t wcol[kGemvMaxItems];            // ... and its first column
-  uint32_t fills[kGemvSlots];              // fills issued per slot
-  float part[kGemvWarps][32][8];
+  uint32_t wcol[kGemvMaxItems];            // ... its first column ...
+  uint32_t wrank[kGemvMaxItems];           // ... and its rank (the x buffer's owner)
 };
 
 __device__ __forceinline__ GemvShared &gemv_smem() {
@@ -389,52 +391,182 @@ __device__ __forceinline__ GemvShared &gemv_smem() {
   return g;
 }
 
-struct GemvRing {
-  unsigned char *rows;  // [kGemvSlots][kGemvRows][kGemvPitch]
-  uint64_t *full;       // [kGemvSlots] completes when a fill's rows have landed
+struct GemvBufs {
+  unsigned char *ring;  // [kGemvSlots][kGemvRows][kGemvPitch]
+  unsigned char *x;     // [2][kGemvXBytes]
+  unsigned char *res;   // [2][kGemvPitch]
+  uint64_t *full;       // [kGemvSlots] a fill's rows have landed
+  uint64_t *empty;      // [kGemvSlots] every compute warp has read the slot
+  uint64_t *xfull;      // [2] piece's x has landed
+  uint64_t *rfull;      // [2] every compute warp has written its results
 };
 
-__device__ __forceinline__ GemvRing gemv_ring() {
+__device__ __forceinline__ GemvBufs gemv_bufs() {
   extern __shared__ __align__(128) unsigned char gemv_dyn[];
-  GemvRing r;
-  r.rows = gemv_dyn + ((128u - (smem_u32(gemv_dyn) & 127u)) & 127u);
-  r.full = reinterpret_cast<uint64_t *>(r.rows + kGemvSlots * kGemvSlotBytes);
-  return r;
+  GemvBufs b;
+  b.ring = gemv_dyn + ((128u - (smem_u32(gemv_dyn) & 127u)) & 127u);
+  b.x = b.ring + kGemvSlots * kGemvSlotBytes;
+  b.res = b.x + 2 * kGemvXBytes;
+  b.full = reinterpret_cast<uint64_t *>(b.res + 2 * kGemvPitch);
+  b.empty = b.full + kGemvSlots;
+  b.xfull = b.empty + kGemvSlots;
+  b.rfull = b.xfull + 2;
+  return b;
 }
 
-__device__ __forceinline__ void gemv_bar() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kGemvBarThreads) : "memory");
+__device__ __forceinline__ uint64_t ld_acquire_cta_shared(const uint64_t *p) {
+  uint64_t v;
+  asm volatile("ld.acquire.cta.shared.u64 %0, [%1];" : "=l"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_cta_shared(uint64_t *p, uint64_t v) {
+  asm volatile("st.release.cta.shared.u64 [%0], %1;" ::"r"(smem_u32(p)), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_release_cta_shared(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }
 
-// Where the rows of one fill come from: W_r's tensor map and the piece's first column.
+// The bound on the waits of the streamers and the compute warps. They wait on the engine warp
+// of their CTA (directly or through each other), whose own waits are bounded by the spin
+// limit and which ends the run (or records the timeout) when one expires; a longer bound
+// here keeps a slow but live engine from being reported as a timeout of another role.
+__device__ __forceinline__ uint64_t gemv_role_limit(const EngArgs &a) {
+  return a.spin_ns > (~0ull >> 4) ? ~0ull : a.spin_ns << 4;
+}
+
+// Stop polling: the engine ended the run, or some warp of the plan gave up.
+__device__ __forceinline__ bool gemv_stop(const EngArgs &a) {
+  const GemvShared &g = gemv_smem();
+  return *reinterpret_cast<const volatile uint32_t *>(&g.exit) != 0u ||
+         ld_relaxed_u32(&a.st->abort) != 0u;
+}
+
+// Where piece q's rows and x come from (cached for the first items).
 struct GemvSrc {
   const CUtensorMap *map;
   uint32_t col;
+  uint32_t rank;
 };
 
-// Rows of item `idx` of this CTA's warp: cached in shared memory for the first items, read
-// from the plan tables beyond that.
 __device__ __forceinline__ GemvSrc gemv_item(const EngArgs &a, const GemvShared &g,
                                              const coll_warp_t &W, uint32_t idx) {
-  if (idx < kGemvMaxItems) return GemvSrc{g.wmap[idx], g.wcol[idx]};
+  if (idx < kGemvMaxItems) return GemvSrc{g.wmap[idx], g.wcol[idx], g.wrank[idx]};
   const coll_item_t it = a.sitems[W.s0 + idx];
   const coll_unit_t u = a.units[it.unit];
   const coll_ref_t r = a.refs[u.src0 + it.slot];
-  return GemvSrc{g.maps + r.rank, (uint32_t)((r.off + u.start) >> 1)};
+  return GemvSrc{g.maps + r.rank, (uint32_t)((r.off + u.start) >> 1), r.rank};
 }
 
-// Issue one fill into `slot` (all lanes call; lane 0 issues): rows 16*rj..16*rj+15 of the
-// piece's 256 columns, one tensor copy whose bytes complete the slot's barrier. Lane 0
-// counts the fill. The slot must be free: every lane of the calling warp has finished its
-// reads of the previous fill (their values are in registers and the warp has synchronised).
-__device__ __forceinline__ void gemv_fill(GemvShared &g, const GemvRing &ring, uint32_t slot,
-                                          const GemvSrc &src, uint32_t rj, uint32_t lane) {
+// Warp 0, before the role split: cache the stage items' row sources and the run's sizes,
+// and open the first pieces.
+__device__ void gemv_prologue(const EngArgs &a, const CUtensorMap *maps, const coll_warp_t &W,
+                              bool chained, uint32_t lane) {
+  GemvShared &g = gemv_smem();
+  const uint32_t nitems = W.s1 - W.s0;
   if (lane == 0) {
-    *reinterpret_cast<volatile uint32_t *>(&g.fills[slot]) = g.fills[slot] + 1u;
-    mbar_expect_tx(&ring.full[slot], kGemvSlotBytes);
-    tensor_load_2d(ring.rows + slot * kGemvSlotBytes, src.map, src.col, rj * kGemvRows,
-                   &ring.full[slot]);
+    g.nitems = nitems;
+    g.k = a.gemv_k;
+    g.kslots = (a.gemv_k + kGemvRows - 1u) / kGemvRows;
+    g.total = (uint64_t)a.n_epochs * nitems;
+    g.maps = maps;
+    g.exit = 0;
+    g.taken = 0;
+    g.chain_open = chained ? 0u : ~0ull;
+    g.go = chained ? 0u : (g.total < 2u ? g.total : 2u);
   }
+  for (uint32_t idx = lane; idx < nitems && idx < kGemvMaxItems; idx += 32) {
+    const coll_item_t it = a.sitems[W.s0 + idx];
+    const coll_unit_t u = a.units[it.unit];
+    const coll_ref_t r = a.refs[u.src0 + it.slot];
+    g.wmap[idx] = maps + r.rank;
+    g.wcol[idx] = (uint32_t)((r.off + u.start) >> 1);
+    g.wrank[idx] = r.rank;
+  }
+}
+
+// Warp 0: open pieces up to min(taken + 2, chain_open) for the x streamer and the compute.
+__device__ __forceinline__ void gemv_open(GemvShared &g) {
+  const uint64_t lim = g.taken + 2ull < g.chain_open ? g.taken + 2ull : g.chain_open;
+  st_release_cta_shared(&g.go, lim < g.total ? lim : g.total);
+}
+
+// Warp 1, lane 0: every weight fill of the run in order; fill f lands in slot f % S once
+// the compute warps have released that slot's previous fill. A last fill past row k reads
+// zeros (the rows lie outside the tensor map) and is only partly used.
+__device__ void gemv_weight_streamer(const EngArgs &a, const coll_warp_t &W) {
+  GemvShared &g = gemv_smem();
+  const GemvBufs b = gemv_bufs();
+  const uint64_t fills = g.total * g.kslots;
+  uint64_t f = 0;
+  uint32_t s = 0, lap = 0, j = 0, item = 0;
+  GemvSrc src = gemv_item(a, g, W, 0);
+  bool ok = true;
+  for (; f < fills; ++f) {
+    ok = mbar_wait_until(&b.empty[s], (lap & 1u) ^ 1u, gemv_role_limit(a),
+                         [&a]() { return gemv_stop(a); });
+    if (!ok) break;
+    mbar_expect_tx(&b.full[s], kGemvSlotBytes);
+    tensor_load_2d(b.ring + (size_t)s * kGemvSlotBytes, src.map, src.col, j * kGemvRows,
+                   &b.full[s]);
+    if (++s == kGemvSlots) {
+      s = 0;
+      ++lap;
+    }
+    if (++j == g.kslots) {
+      j = 0;
+      if (++item == g.nitems) item = 0;
+      src = gemv_item(a, g, W, item);
+    }
+  }
+  if (!ok && !gemv_stop(a)) record_timeout(a.st, (int)W.rank, -1, 6, 0);
+  // every fill issued has landed before the CTA may exit (bounded): the last fill of each
+  // slot is the latest phase of its barrier
+  const uint64_t issued = f;
+  for (uint32_t t = 0; t < kGemvSlots && (uint64_t)t < issued; ++t) {
+    const uint64_t last = issued - 1u - ((issued - 1u - t) % kGemvSlots);
+    mbar_wait_until(&b.full[t], (uint32_t)((last / kGemvSlots) & 1u), 100000000ull,
+                    []() { return false; });
+  }
+}
+
+// Warp 2, lane 0: piece q's x (k bf16) into buffer q % 2, once the engine has opened piece
+// q (so the buffer's previous piece, q - 2, has been read and its results taken). The
+// acquire here and the release of the copy's arrival order the compute lanes' reads of the
+// result slot after the engine's, through the x barrier they wait on.
+__device__ void gemv_x_streamer(const EngArgs &a, const coll_warp_t &W) {
+  GemvShared &g = gemv_smem();
+  const GemvBufs b = gemv_bufs();
+  const uint32_t xbytes = g.k * 2u;
+  uint64_t q = 0;
+  uint32_t item = 0, pool = 0;
+  bool ok = true;
+  for (; q < g.total; ++q) {
+    // wait until the engine opens piece q
+    uint64_t t0 = 0;
+    for (uint32_t it = 0; ld_acquire_cta_shared(&g.go) <= q; ++it) {
+      __nanosleep(64);  // (polling at full rate would take issue slots from a compute warp)
+      if ((it & 15u) == 15u) {
+        const uint64_t now = globaltimer();
+        if (t0 == 0) t0 = now;
+        else if (now - t0 > gemv_role_limit(a)) ok = false;
+        if (!ok || gemv_stop(a)) break;
+      }
+    }
+    if (!ok || ld_acquire_cta_shared(&g.go) <= q) break;
+    const uint32_t p = (uint32_t)(q & 1u);
+    const GemvSrc src = gemv_item(a, g, W, item);
+    const char *xp = a.ptr.in[src.rank] + (int64_t)pool * a.in_stride;
+    mbar_expect_tx(&b.xfull[p], xbytes);
+    bulk_load(b.x + (size_t)p * kGemvXBytes, xp, xbytes, &b.xfull[p]);
+    if (++item == g.nitems) {
+      item = 0;
+      if (++pool == (uint32_t)a.in_pool) pool = 0;
+    }
+  }
+  if (!ok && !gemv_stop(a)) record_timeout(a.st, (int)W.rank, -1, 6, 0);
+  for (uint64_t t = q > 2 ? q - 2 : 0; t < q; ++t)
+    mbar_wait_until(&b.xfull[t & 1u], (uint32_t)((t >> 1) & 1u), 100000000ull,
+                    []() { return false; });
 }
 
 // Packed pairs of binary32 (sm_100 family): two IEEE operations, round to nearest even.
@@ -453,269 +585,152 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
-// bf16 elements 2j, 2j+1 of a word -> {binary32, binary32}
-__device__ __forceinline__ uint64_t bf16x2_widen(uint32_t w) {
-  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+
+// The products of sixteen rows for this lane's two columns: prod[r] = w[row][c..c+1] * x[row]
+// (each rounded to binary32), independent of the running sums.
+__device__ __forceinline__ void gemv_prods16(uint64_t prod[16], const unsigned char *slot,
+                                             uint32_t colb, const unsigned char *xrow) {
+  const uint4 xa = *reinterpret_cast<const uint4 *>(xrow);
+  const uint4 xb = *reinterpret_cast<const uint4 *>(xrow + 16);
+  const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+  for (uint32_t r = 0; r < 16; ++r) {
+    const uint32_t w = *reinterpret_cast<const uint32_t *>(slot + r * kGemvPitch + colb);
+    const float xf = __uint_as_float((r & 1u) ? (xw[r >> 1] & 0xFFFF0000u) : (xw[r >> 1] << 16));
+    prod[r] = f2_mul(f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)),
+                     f2_pack(xf, xf));
+  }
 }
 
-// Eight rows of this lane's eight outputs: acc[p] holds outputs (2p, 2p+1).
+// The running sums over sixteen products in row order (FIRST: the chain starts from the
+// first of them).
 template <bool FIRST>
-__device__ __forceinline__ void gemv_rows8(uint64_t acc[4], const uint4 w[8], uint4 xv) {
-  const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+__device__ __forceinline__ void gemv_adds16(uint64_t &acc, const uint64_t prod[16]) {
 #pragma unroll
-  for (uint32_t t = 0; t < 8; ++t) {
-    const float xf = __uint_as_float((t & 1u) ? (xw[t >> 1] & 0xFFFF0000u) : (xw[t >> 1] << 16));
-    const uint64_t xx = f2_pack(xf, xf);
-    const uint32_t ww[4] = {w[t].x, w[t].y, w[t].z, w[t].w};
+  for (uint32_t r = 0; r < 16; ++r) acc = (FIRST && r == 0) ? prod[r] : f2_add(acc, prod[r]);
+}
+
+// BLOCKS blocks of sixteen rows of a slot, in order: the products of block c + 1 are formed
+// while block c's sums run (they do not depend on them), so the in-order chain of adds has
+// independent work to overlap; the order of the adds is unchanged.
+template <bool FIRST, uint32_t BLOCKS>
+__device__ __forceinline__ void gemv_slot_rows(uint64_t &acc, const unsigned char *slot,
+                                               uint32_t colb, const unsigned char *xs) {
+  uint64_t prod[2][16];
+  gemv_prods16(prod[0], slot, colb, xs);
 #pragma unroll
-    for (uint32_t p = 0; p < 4; ++p) {
-      const uint64_t prod = f2_mul(bf16x2_widen(ww[p]), xx);
-      acc[p] = (FIRST && t == 0) ? prod : f2_add(acc[p], prod);
-    }
+  for (uint32_t c = 0; c < BLOCKS; ++c) {
+    if (c + 1 < BLOCKS)
+      gemv_prods16(prod[(c + 1) & 1], slot + (c + 1) * 16 * kGemvPitch, colb, xs + (c + 1) * 32);
+    if (FIRST && c == 0) gemv_adds16<true>(acc, prod[c & 1]);
+    else gemv_adds16<false>(acc, prod[c & 1]);
   }
 }
 
-// Position of a compute warp's reads in its private ring, and of the refills it issues. It
-// lives across blocks and only ever steps forward (no division on the compute path).
-struct GemvCursor {
-  uint64_t q, lap;  // fill read next: number q, lap q / 3 of the warp's slot q % 3
-  uint32_t slot;    // ring slot (warp base + q % 3)
-  uint32_t rp_j;    // refill q + 3: slot rp_j of the block ...
-  uint32_t ri;      // ... of stage item ri
-  GemvSrc src;      // rows of item ri
-};
-
-// Refills of the next piece's slots, held back until the block's results are handed over:
-// n consecutive fills (consecutive slots of the ring, consecutive refill positions), the
-// first of them into `slot`, slot rj of the block of stage item ri.
-struct GemvPending {
-  uint32_t n, slot, rj, ri;
-  GemvSrc src;
-};
-
-// Compute warp `wid`, before its first block: issue its first 3 fills and set the cursor
-// (next read: fill 0; next refill: fill 3).
-__device__ void gemv_warp_prologue(const EngArgs &a, GemvShared &g, const GemvRing &ring,
-                                   const coll_warp_t &W, uint32_t wid, uint32_t lane,
-                                   GemvCursor &c) {
-  const uint32_t bs = g.S / kGemvWarps;
-  uint32_t j = 0, ri = 0;
-  GemvSrc src = gemv_item(a, g, W, 0);
-  for (uint32_t q = 0; q < kGemvSlotsPerWarp; ++q) {
-    if (q < g.total) gemv_fill(g, ring, wid * kGemvSlotsPerWarp + q, src, wid * bs + j, lane);
-    if (++j == bs) {
-      j = 0;
-      if (++ri == g.nitems) ri = 0;
-      src = gemv_item(a, g, W, ri);
-    }
+// The rows of one fill: 64, or fewer (a multiple of 16) in a last fill past row k.
+template <bool FIRST>
+__device__ __forceinline__ void gemv_fill_rows(uint64_t &acc, const unsigned char *slot,
+                                               uint32_t colb, const unsigned char *xs,
+                                               uint32_t rows) {
+  switch (rows) {
+    case 16: gemv_slot_rows<FIRST, 1>(acc, slot, colb, xs); break;
+    case 32: gemv_slot_rows<FIRST, 2>(acc, slot, colb, xs); break;
+    case 48: gemv_slot_rows<FIRST, 3>(acc, slot, colb, xs); break;
+    default: gemv_slot_rows<FIRST, 4>(acc, slot, colb, xs); break;
   }
-  c.q = 0;
-  c.lap = 0;
-  c.slot = wid * kGemvSlotsPerWarp;
-  c.rp_j = j;
-  c.ri = ri;
-  c.src = src;
 }
 
-// This warp's k-block of piece `piece` into g.part[wid][lane], streaming the block's rows
-// through the warp's private ring (see above). The readiness of the slots already issued is
-// tested at once, so slots that landed during the exchange cost no wait each.
-__device__ __forceinline__ void gemv_block(const EngArgs &a, GemvShared &g, const GemvRing &ring,
-                                           const coll_warp_t &W, uint32_t wid, uint32_t lane,
-                                           GemvCursor &c, GemvPending &pend) {
-  const uint32_t bs = g.S / kGemvWarps;  // slots per block
-  const uint64_t total = g.total;
-  const uint32_t base = wid * kGemvSlotsPerWarp;
-  const bool act = lane < g.active;
-  // x of this block: lane t holds the 16 values of slot 32c+t of chunk c, loaded together
-  // (one memory round trip per 32 slots), and each slot's values are broadcast by shuffle
-  const char *xp = g.xp + (size_t)wid * bs * (kGemvRows * 2);
-  uint64_t acc[4] = {0, 0, 0, 0};
-  uint4 xl[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-  uint32_t ready = 0;  // bit t: the fill of slot 32c+t of this chunk has already landed
-  const uint64_t qe = c.q + bs;  // first fill of the next piece
-  pend.n = 0;
-  bool done = true;
-  for (uint32_t j = 0; j < bs; ++j) {
-    if ((j & 31u) == 0u) {
-      // per chunk of 32 slots: one x load and one readiness test per lane, in parallel
-      // (only the fills already issued, at most 3 ahead, can have landed)
-      bool r = false;
-      if (j + lane < bs) {
-        xl[0] = ld_nc_v4(xp + (size_t)(j + lane) * 32);
-        xl[1] = ld_nc_v4(xp + (size_t)(j + lane) * 32 + 16);
-      }
-      if (j + lane < bs && lane < kGemvSlotsPerWarp) {
-        const uint32_t o = c.slot - base + lane;  // fill c.q + lane: slot o % 3, lap + o / 3
-        const uint32_t wrap = o >= kGemvSlotsPerWarp ? 1u : 0u;
-        r = mbar_test_wait(&ring.full[base + o - wrap * kGemvSlotsPerWarp],
-                           (uint32_t)((c.lap + wrap) & 1u));
-      }
-      ready = __ballot_sync(FULL, r);
-      __syncwarp();  // orders each lane's acquiring test before every lane's reads
-    }
-    bool ok = true;
-    if (!((ready >> (j & 31u)) & 1u)) {
-      // (this warp issued the fill itself, so the slot's previous phase has completed and
-      // the parity identifies the fill)
-      if (lane == 0)
-        ok = mbar_wait_until(&ring.full[c.slot], (uint32_t)(c.lap & 1u), a.spin_ns,
-                             [&a]() { return ld_relaxed_u32(&a.st->abort) != 0u; });
-      ok = __shfl_sync(FULL, ok, 0);
-      __syncwarp();  // orders lane 0's acquiring wait before every lane's reads
-    }
-    if (!ok) {
-      if (lane == 0) {
-        record_timeout(a.st, (int)W.rank, -1, 6, 0);
-        g.fail = 1;
-      }
-      done = false;
-      break;
-    }
-    const unsigned char *s = ring.rows + c.slot * kGemvSlotBytes + lane * 16;
-#pragma unroll
-    for (uint32_t h = 0; h < 2; ++h) {  // rows 8h..8h+7 of the slot
-      uint4 xv;
-      xv.x = __shfl_sync(FULL, xl[h].x, j & 31u);
-      xv.y = __shfl_sync(FULL, xl[h].y, j & 31u);
-      xv.z = __shfl_sync(FULL, xl[h].z, j & 31u);
-      xv.w = __shfl_sync(FULL, xl[h].w, j & 31u);
-      uint4 w[8];
-#pragma unroll
-      for (uint32_t t = 0; t < 8; ++t)
-        w[t] = act ? *reinterpret_cast<const uint4 *>(s + (8 * h + t) * kGemvPitch)
-                   : make_uint4(0, 0, 0, 0);
-      if (j == 0 && h == 0) gemv_rows8<true>(acc, w, xv); else gemv_rows8<false>(acc, w, xv);
-    }
-    // The slot's rows are in registers and used: once the warp has synchronised, the copy
-    // may overwrite the slot. A refill this block still needs is issued now; refills for
-    // later pieces wait for the end of the block, so that their copies stream during the
-    // exchange instead of competing with this block's.
+// Compute warp `cw` (0..3): every piece of the run in order. Waits are taken by lane 0 and
+// shared; a __syncwarp after each orders lane 0's acquiring wait before every lane's reads,
+// and one before each of lane 0's arrivals orders every lane's reads (of a slot) or writes
+// (of results) before it.
+__device__ void gemv_compute(const EngArgs &a, const coll_warp_t &W, uint32_t cw,
+                             uint32_t lane) {
+  GemvShared &g = gemv_smem();
+  const GemvBufs b = gemv_bufs();
+  const uint32_t colb = (64u * cw + 2u * lane) * 2u;  // byte offset of this lane's columns
+  uint32_t s = 0, lap = 0;
+  bool ok = true;
+  for (uint64_t q = 0; q < g.total && ok; ++q) {
+    const uint32_t p = (uint32_t)(q & 1u);
+    if (lane == 0)
+      ok = mbar_wait_until(&b.xfull[p], (uint32_t)((q >> 1) & 1u), gemv_role_limit(a),
+                           [&a]() { return gemv_stop(a); });
+    ok = __shfl_sync(FULL, ok, 0);
     __syncwarp();
-    if (c.q + kGemvSlotsPerWarp < total) {
-      if (c.q + kGemvSlotsPerWarp < qe) {
-        gemv_fill(g, ring, c.slot, c.src, wid * bs + c.rp_j, lane);
-      } else {
-        if (pend.n == 0) {
-          pend.slot = c.slot;
-          pend.rj = c.rp_j;
-          pend.ri = c.ri;
-          pend.src = c.src;
-        }
-        ++pend.n;
+    if (!ok) break;
+    const unsigned char *xq = b.x + (size_t)p * kGemvXBytes;
+    uint64_t acc = 0;
+    for (uint32_t j = 0; j < g.kslots; ++j) {
+      if (lane == 0)
+        ok = mbar_wait_until(&b.full[s], lap & 1u, gemv_role_limit(a),
+                             [&a]() { return gemv_stop(a); });
+      ok = __shfl_sync(FULL, ok, 0);
+      __syncwarp();
+      if (!ok) break;
+      const unsigned char *slot = b.ring + (size_t)s * kGemvSlotBytes;
+      const unsigned char *xs = xq + (size_t)j * (kGemvRows * 2);
+      // rows of this fill: 64, or fewer (a multiple of 16) in a last fill past row k
+      const uint32_t rows = g.k - j * kGemvRows < kGemvRows ? g.k - j * kGemvRows : kGemvRows;
+      if (j == 0) gemv_fill_rows<true>(acc, slot, colb, xs, rows);
+      else gemv_fill_rows<false>(acc, slot, colb, xs, rows);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&b.empty[s]);  // the warp's reads of the slot are done
+      if (++s == kGemvSlots) {
+        s = 0;
+        ++lap;
       }
     }
-    ++c.q;
-    if (++c.slot == base + kGemvSlotsPerWarp) {
-      c.slot = base;
-      ++c.lap;
-    }
-    if (++c.rp_j == bs) {
-      c.rp_j = 0;
-      if (++c.ri == g.nitems) c.ri = 0;
-      c.src = gemv_item(a, g, W, c.ri);
-    }
-  }
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
+    if (!ok) break;
+    // piece q's x has landed, so the engine has opened piece q: it has taken piece q - 2
+    // from this result slot (its release of the opening, the streamer's acquire and the
+    // x barrier order that before these writes)
     float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(acc[p]));
-    g.part[wid][lane][2 * p] = lo;
-    g.part[wid][lane][2 * p + 1] = hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(acc));
+    *reinterpret_cast<uint32_t *>(b.res + (size_t)p * kGemvPitch + colb) = pack_bf16x2(lo, hi);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&b.rfull[p]);
   }
-  if (!done && lane == 0) g.fail = 1;
+  if (!ok && lane == 0 && !gemv_stop(a)) record_timeout(a.st, (int)W.rank, -1, 6, 0);
 }
 
-// Warp 0, before the epoch loop: cache the stage items' row sources and the run's sizes.
-__device__ void gemv_prologue(const EngArgs &a, const CUtensorMap *maps, const coll_warp_t &W,
-                              uint32_t lane) {
+// Warp 0 (all 32 lanes): take piece q's results (lanes below `active` hold 8 outputs each)
+// and open piece q + 2; false if the wait gave up.
+__device__ __forceinline__ bool gemv_take(const EngArgs &a, uint64_t q, uint32_t active,
+                                          uint32_t lane, uint4 &res) {
   GemvShared &g = gemv_smem();
-  const uint32_t nitems = W.s1 - W.s0;
-  if (lane == 0) {
-    g.nitems = nitems;
-    g.S = a.gemv_k / kGemvRows;
-    g.total = (uint64_t)a.n_epochs * nitems * (a.gemv_k / (kGemvRows * kGemvWarps));
-    g.maps = maps;
-  }
-  for (uint32_t idx = lane; idx < nitems && idx < kGemvMaxItems; idx += 32) {
-    const coll_item_t it = a.sitems[W.s0 + idx];
-    const coll_unit_t u = a.units[it.unit];
-    const coll_ref_t r = a.refs[u.src0 + it.slot];
-    g.wmap[idx] = maps + r.rank;
-    g.wcol[idx] = (uint32_t)((r.off + u.start) >> 1);
-  }
-}
-
-// Compute warp `wid` (0..7): compute block wid whenever warp 0 opens a stage, until told to
-// exit. After each block, the refills it held back are issued: their copies stream while
-// warp 0 runs the exchange.
-__device__ void gemv_helper_loop(const EngArgs &a, const coll_warp_t &W, uint32_t wid,
-                                 uint32_t lane) {
-  GemvShared &g = gemv_smem();
-  const GemvRing ring = gemv_ring();
-  GemvCursor c;
-  GemvPending pend;
-  gemv_warp_prologue(a, g, ring, W, wid, lane, c);
-  for (;;) {
-    gemv_bar();
-    if (g.exit) return;
-    gemv_block(a, g, ring, W, wid, lane, c, pend);
-    gemv_bar();
-    if (g.fail) continue;
-    const uint32_t bs = g.S / kGemvWarps;
-    const uint32_t base = wid * kGemvSlotsPerWarp;
-    for (uint32_t d = 0; d < pend.n; ++d) {
-      gemv_fill(g, ring, pend.slot, pend.src, wid * bs + pend.rj, lane);
-      if (++pend.slot == base + kGemvSlotsPerWarp) pend.slot = base;
-      if (++pend.rj == bs) {
-        pend.rj = 0;
-        if (++pend.ri == g.nitems) pend.ri = 0;
-        pend.src = gemv_item(a, g, W, pend.ri);
-      }
-    }
-  }
-}
-
-// Warp 0 (all 32 lanes): piece number `piece` of y = W x for the lanes below `active`;
-// false if a ring wait gave up (the status word then holds the timeout).
-__device__ __forceinline__ bool gemv_piece_mw(const EngArgs &a, const coll_warp_t &W,
-                                              const char *xp, uint32_t active, uint64_t piece,
-                                              uint32_t lane, uint4 &res) {
-  GemvShared &g = gemv_smem();
-  const GemvRing ring = gemv_ring();
-  if (lane == 0) {
-    g.xp = xp;
-    g.active = active;
-  }
+  const GemvBufs b = gemv_bufs();
+  const uint32_t p = (uint32_t)(q & 1u);
+  bool ok = true;
+  if (lane == 0)
+    ok = mbar_wait_until(&b.rfull[p], (uint32_t)((q >> 1) & 1u), a.spin_ns,
+                         [&a]() { return ld_relaxed_u32(&a.st->abort) != 0u; });
+  ok = __shfl_sync(FULL, ok, 0);
   __syncwarp();
-  gemv_bar();  // open: the compute warps start their blocks
-  gemv_bar();  // every block sum is in shared memory
-  float acc[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] = g.part[0][lane][e];
-#pragma unroll
-  for (uint32_t b = 1; b < kGemvWarps; ++b)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], g.part[b][lane][e]);
-  res = bf16x8_pack(acc);
-  return __shfl_sync(FULL, g.fail, 0) == 0u;
+  if (!ok) return false;
+  res = lane < active ? *reinterpret_cast<const uint4 *>(b.res + (size_t)p * kGemvPitch + lane * 16)
+                      : make_uint4(0, 0, 0, 0);
+  __syncwarp();  // every lane's read of the slot precedes lane 0's release of it
+  if (lane == 0) {
+    g.taken = q + 1u;
+    gemv_open(g);
+  }
+  return true;
 }
 
-// Warp 0 at the end: release the other warps, then wait (bounded) for every fill issued
-// so far, so that no bulk copy lands after the CTA has exited (after a failure some
-// fills are never read).
+// Warp 0, at an epoch whose chained wait has passed: open that epoch's pieces.
+__device__ __forceinline__ void gemv_open_epoch(uint32_t epoch_index, uint32_t lane) {
+  GemvShared &g = gemv_smem();
+  if (lane == 0) {
+    g.chain_open = (uint64_t)(epoch_index + 1u) * g.nitems;
+    gemv_open(g);
+  }
+}
+
+// Warp 0 at the end of its loop: the other roles stop waiting.
 __device__ __forceinline__ void gemv_finish(uint32_t lane) {
   GemvShared &g = gemv_smem();
-  const GemvRing ring = gemv_ring();
-  if (lane == 0) *reinterpret_cast<volatile uint32_t *>(&g.exit) = 1u;
-  __syncwarp();
-  gemv_bar();
-  if (lane == 0) {
-    for (uint32_t s = 0; s < kGemvSlots; ++s) {
-      const uint32_t n = g.fills[s];
-      if (n) mbar_wait_until(&ring.full[s], (n - 1u) & 1u, 100000000ull, []() { return false; });
-    }
-  }
+  if (lane == 0) st_release_cta_shared(&g.exit, 1u);
 }
 
 // Validation of a speculative load: lane j < n holds producer j's flag word and every lane
@@ -775,12 +790,13 @@ __device__ __forceinline__ uint4 spec_attempt(const char *xb, uint32_t nbytes, u
 // KIND: 0 copy, 1 sum of bf16, 2 sum of f32. GEMV: fused producer. LL: tagged data.
 // PULL: two-shot pull plans (the publish/pull steps are compiled only into this variant).
 // FP: 0 for the general engine; otherwise a variant for plans whose every warp has one
-// stage item and one consume item, run without fault injection, stamps or chained epochs,
-// under one speculative protocol known at compile time (1 with content tags, 2 the same
-// fence-free). On the single warp that carries a piece through an epoch, every runtime mode
-// test is a dependent instruction on the critical path; compiled out, the decode epoch
-// drops by about a sixth. (A dual-buffer variant measured slower than the general engine
-// and is not built.)
+// stage item and one consume item, run without fault injection, phase stamps or chained
+// epochs, under one speculative protocol known at compile time (1 with content tags, 2 the
+// same fence-free; 3 and 4 the same two with one %globaltimer stamp per epoch, so that the
+// latency distribution is taken on the specialised code). On the single warp that carries a
+// piece through an epoch, every runtime mode test is a dependent instruction on the critical
+// path; compiled out, the decode epoch drops by about a sixth. (A dual-buffer variant
+// measured slower than the general engine and is not built.)
 // (the fused producer also takes the tensor maps of the ranks' weight matrices)
 template <bool GEMV> struct MapsArg { using type = NoMaps; };
 template <> struct MapsArg<true> { using type = GemvMaps; };
@@ -790,34 +806,40 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
     engine_kernel(const EngArgs a, const __grid_constant__ typename MapsArg<GEMV>::type maps) {
   static_assert(FP == 0 || (!GEMV && !LL && !PULL), "the specialised variants are plain");
   constexpr bool fast = FP != 0;
+  constexpr bool fp_relaxed = FP == 2 || FP == 4;  // the specialised fence-free check
+  constexpr bool fp_stamps = FP >= 3;              // ... with one stamp per epoch
   const uint32_t gw = blockIdx.x;
   const uint32_t lane = threadIdx.x & 31u;
   if constexpr (GEMV) {
     const uint32_t wid = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-      GemvShared &g = gemv_smem();
-      const GemvRing ring = gemv_ring();
-      g.exit = 0;
-      g.fail = 0;
+      const GemvBufs bb = gemv_bufs();
       for (uint32_t s = 0; s < kGemvSlots; ++s) {
-        g.fills[s] = 0;
-        mbar_init(&ring.full[s], 1);  // the filling lane's arrival, plus the copy's bytes
+        mbar_init(&bb.full[s], 1);  // the streamer's arrival, plus the copy's bytes
+        mbar_init(&bb.empty[s], kGemvComputeWarps);
+      }
+      for (uint32_t p = 0; p < 2; ++p) {
+        mbar_init(&bb.xfull[p], 1);
+        mbar_init(&bb.rfull[p], kGemvComputeWarps);
       }
       mbar_init_fence();
     }
     __syncthreads();
     if (gw >= a.nwarps) return;  // (every CTA of a launch is a plan warp)
-    if (wid == 0) gemv_prologue(a, maps.m, a.warps[gw], lane);
-    __syncthreads();  // the item cache and the run's fill count are set
-    // The register split: the compute warpgroups shrink, the engine's warpgroup grows. Each
-    // role then runs to the end without rejoining the other, so that each is compiled for
-    // its own register budget.
-    if (wid >= kGemvFirst) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGemvComputeRegs));
-      gemv_helper_loop(a, a.warps[gw], wid - kGemvFirst, lane);
+    if (wid == 0) gemv_prologue(a, maps.m, a.warps[gw], a.chain && a.rank_done, lane);
+    __syncthreads();  // the item cache, the run's sizes and the first opened pieces are set
+    if (wid == 1) {
+      if (lane == 0) gemv_weight_streamer(a, a.warps[gw]);
       return;
     }
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kGemvEngineRegs));
+    if (wid == 2) {
+      if (lane == 0) gemv_x_streamer(a, a.warps[gw]);
+      return;
+    }
+    if (wid >= kGemvFirst) {
+      gemv_compute(a, a.warps[gw], wid - kGemvFirst, lane);
+      return;
+    }
     if (wid != 0) return;
   } else {
     if (gw >= a.nwarps) return;
@@ -830,7 +852,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
   const uint32_t slot_mult = ll ? 2u : 1u;  // tagged-data slots are twice the payload
   // content tags: validated by the tagged checks, stored by every spec producer
   const bool literal = !fast && spec_proto && a.spec_check == COLL_SPEC_LITERAL;
-  const bool relaxed = fast ? FP == 2 : spec_proto && a.spec_check == COLL_SPEC_TAGGED_RELAXED;
+  const bool relaxed = fast ? fp_relaxed : spec_proto && a.spec_check == COLL_SPEC_TAGGED_RELAXED;
   const bool tagged = spec_proto && !literal;
   const bool skip_notify = !fast && (a.inject_flags & COLL_INJECT_SKIP_NOTIFY) &&
                            (int)W.rank == a.inject_rank;
@@ -887,8 +909,8 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
 
   if (stagger && a.inject_start_ns)
     spin_ns((uint64_t)W.rank * a.inject_start_ns);
-  const bool stamp = !fast && gw == 0 && lane == 0 && a.stamps;
-  const bool phases = stamp && a.stamp_phases;
+  const bool stamp = (!fast || fp_stamps) && gw == 0 && lane == 0 && a.stamps;
+  const bool phases = !fast && stamp && a.stamp_phases;
   if (stamp) a.stamps[0] = globaltimer();
 
   // input-pool offset of epoch i and of epoch i+1, advanced without division (a runtime
@@ -934,6 +956,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
         failed = true;
         break;
       }
+      if constexpr (GEMV) gemv_open_epoch((uint32_t)i, lane);  // this epoch's inputs are ready
     }
     if (pst) a.stamps[1 + 4 * i] = globaltimer();
 
@@ -968,10 +991,10 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
         x = nx;
         if (tagged && !nh_ready && lane < nvec) h = tag_part(x, lane);
       } else if constexpr (GEMV) {
-        // fused producer: the CTA's eight compute warps make this piece of the payload from
-        // the weight rows the streaming warp has staged
-        const coll_ref_t r = single_s ? sref : a.refs[u.src0 + it.slot];
-        if (!gemv_piece_mw(a, W, a.ptr.in[r.rank] + in_off, nvec, gpiece++, lane, x)) {
+        // fused producer: the CTA's compute warps have made this piece of the payload (W_r x,
+        // one ordered chain per output) from the rows and the x the streamers staged
+        if (!gemv_take(a, gpiece++, nvec, lane, x)) {
+          if (lane == 0) record_timeout(st, (int)W.rank, (int)it.unit, 6, E);
           failed = true;
           break;
         }
@@ -1085,6 +1108,10 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
         uint2 myh = make_uint2(0u, 0u);
         // (the prefetched next input is hashed while this attempt's loads are in flight)
         const bool side = pipelined && tagged && !nh_ready;
+        // The speculation window: loads issued right after this warp's own notify mostly
+        // race the peers' stores of the same epoch and fail validation; a short wait first
+        // (the plan's spec_delay_ns) trades a little latency for fewer reloads.
+        if (a.spec_delay_ns) spin_ns(a.spec_delay_ns);
         res = spec_attempt<KIND>(xb, u.nbytes, n, lane, active, tagged, pf, !relaxed,
                                  !pause_consumer, f, myh, side, nx,
                                  pipelined ? (su.nbytes >> 4) : 0u, nh);
@@ -1321,11 +1348,15 @@ static const void *engine_fn(int kind, bool gemv, bool ll, bool pull, int fp = 0
     return kind == 1 ? (const void *)engine_kernel<1, false, false, true, 0>
                      : (const void *)engine_kernel<2, false, false, true, 0>;
   if (fp != 0 && kind != 0) {  // (the specialised variants are sums)
-    switch ((kind - 1) * 2 + fp) {
+    switch ((kind - 1) * 4 + fp) {
       case 1: return (const void *)engine_kernel<1, false, false, false, 1>;
       case 2: return (const void *)engine_kernel<1, false, false, false, 2>;
-      case 3: return (const void *)engine_kernel<2, false, false, false, 1>;
-      default: return (const void *)engine_kernel<2, false, false, false, 2>;
+      case 3: return (const void *)engine_kernel<1, false, false, false, 3>;
+      case 4: return (const void *)engine_kernel<1, false, false, false, 4>;
+      case 5: return (const void *)engine_kernel<2, false, false, false, 1>;
+      case 6: return (const void *)engine_kernel<2, false, false, false, 2>;
+      case 7: return (const void *)engine_kernel<2, false, false, false, 3>;
+      default: return (const void *)engine_kernel<2, false, false, false, 4>;
     }
   }
   switch (kind) {
@@ -1338,10 +1369,11 @@ static const void *engine_fn(int kind, bool gemv, bool ll, bool pull, int fp = 0
 // The specialised variant a run of these arguments may use (0: the general engine).
 static int engine_fp(int kind, const EngArgs &a) {
   if (kind == 0 || a.gemv_k != 0 || a.rpar != 0 || !a.single_items || a.inject_flags != 0 ||
-      a.stamps != nullptr || a.dbg != nullptr || (a.chain && a.rank_done))
+      (a.stamps != nullptr && a.stamp_phases) || a.dbg != nullptr || (a.chain && a.rank_done))
     return 0;
-  if (a.protocol == COLL_PROTO_SPEC && a.spec_check == COLL_SPEC_TAGGED) return 1;
-  if (a.protocol == COLL_PROTO_SPEC && a.spec_check == COLL_SPEC_TAGGED_RELAXED) return 2;
+  const int st = a.stamps != nullptr ? 2 : 0;
+  if (a.protocol == COLL_PROTO_SPEC && a.spec_check == COLL_SPEC_TAGGED) return 1 + st;
+  if (a.protocol == COLL_PROTO_SPEC && a.spec_check == COLL_SPEC_TAGGED_RELAXED) return 2 + st;
   return 0;
 }
 
@@ -1355,7 +1387,7 @@ cudaError_t engine_max_coresident(int op, int dtype, int protocol, int datapath,
   const bool ll = protocol == COLL_PROTO_LL, pull = datapath == COLL_DP_TWOSHOT_PULL;
   // a run may use a specialised variant: every variant it may use must fit
   int per_sm = 1 << 30;
-  for (int fp = 0; fp <= ((kind != 0 && !ll && !pull) ? 2 : 0); ++fp) {
+  for (int fp = 0; fp <= ((kind != 0 && !ll && !pull) ? 4 : 0); ++fp) {
     int n = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, engine_fn(kind, false, ll, pull, fp),
                                                       32, 0);
@@ -1373,11 +1405,6 @@ cudaError_t engine_gemv_max_coresident(bool pull, int *max_ctas) {
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const void *fn = engine_fn(1, true, false, pull);
-  // the in-kernel register split assumes the launch allocation it was written for
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, fn);
-  if (e != cudaSuccess) return e;
-  if ((uint32_t)fa.numRegs != kGemvLaunchRegs) return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmemBytes);
   if (e != cudaSuccess) return e;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kGemvThreads, kGemvSmemBytes);

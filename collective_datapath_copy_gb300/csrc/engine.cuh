@@ -78,10 +78,11 @@ struct EngArgs {
   uint64_t inject_pause_ns;
   int32_t R;
   uint32_t single_items;  // 1: every warp has one stage item and one consume item
+  uint32_t spec_delay_ns; // speculative protocol: wait before the first speculative loads
 };
 
 // Fused producer: one 2-D tensor map per rank over W_r ([k rows][in_len[r] bf16 columns],
-// box of 256 columns x 16 rows), passed by value as a kernel parameter.
+// box of 256 columns x 64 rows), passed by value as a kernel parameter.
 struct GemvMaps {
   CUtensorMap m[COLL_MAX_RANKS];
 };

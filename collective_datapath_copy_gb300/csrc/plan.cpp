@@ -40,7 +40,8 @@ extern "C" int coll_config_default(coll_config_t *cfg) {
   cfg->protocol = COLL_PROTO_SPEC;
   cfg->datapath = COLL_DP_ONESHOT;
   cfg->zero_copy = 0;
-  cfg->spec_check = COLL_SPEC_TAGGED;
+  cfg->spec_check = COLL_SPEC_TAGGED_RELAXED;
+  cfg->spec_delay_ns = -1;
   cfg->unit_bytes = 0;
   cfg->inject_rank = -1;
   return COLL_OK;
@@ -58,7 +59,8 @@ static int check_config(const coll_config_t &c) {
   if (c.warps_per_rank < 0 || c.ctas < 0) return COLL_EINVAL;
   if (c.tile_bytes < 0 || (c.tile_bytes % 16) != 0) return COLL_EINVAL;
   if (c.inject_prob_ppm > 1000000u) return COLL_EINVAL;
-  if (c.chain < 0 || c.chain > 1 || c.reserved2 != 0 || c.reserved3 != 0) return COLL_EINVAL;
+  if (c.chain < 0 || c.chain > 1 || c.reserved3 != 0) return COLL_EINVAL;
+  if (c.spec_delay_ns < -1 || c.spec_delay_ns > 100000) return COLL_EINVAL;
   if (c.reduce_order < 0 || c.reduce_order > 1) return COLL_EINVAL;
   // the staged engine always sums in rank order
   if (c.reduce_order != COLL_ORDER_RANK && !c.zero_copy) return COLL_EINVAL;

@@ -156,7 +156,12 @@ typedef struct {
                                its consume items of epoch e is done (a dependent chain, as
                                when the next layer needs the whole all-reduce output);
                                0 = back-to-back independent epochs                       */
-  int32_t reserved2;        /* must be 0                                                */
+  int32_t spec_delay_ns;    /* COLL_PROTO_SPEC: ns a consumer waits after its own notify
+                               before its first speculative loads (loads issued at once
+                               mostly race the peers' stores of the same epoch and are
+                               retried): -1 = the check's default (200 for
+                               COLL_SPEC_TAGGED_RELAXED, 0 otherwise), 0..100000 = that
+                               many ns                                                   */
   int32_t reduce_order;     /* COLL_ORDER_*; zero-copy plans only                      */
   int32_t reserved3;        /* must be 0                                                */
 } coll_config_t;
@@ -187,7 +192,8 @@ typedef struct {
   uint64_t spec_retries; /* validations that failed and were redone after a wait       */
 } coll_stats_t;
 
-/* Fill *cfg with defaults (spec protocol, oneshot, staged, tagged validation).
+/* Fill *cfg with defaults (spec protocol with the fence-free tagged check and its default
+ * speculation delay, oneshot, staged).
  * Source: SiFAR review, "What carries the argument" (speculative reduction over dual
  * buffers is the protocol the review's All-Reduce is built on). */
 int coll_config_default(coll_config_t *cfg);
@@ -243,21 +249,22 @@ int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_epochs,
 
 /* Fused producer (staged bf16 plans): like coll_run, but each rank's payload is computed
  * inside the engine's stage step instead of read from memory — the layer that precedes the
- * collective fused into its persistent loop (SiFAR review: the All-Reduces run inside
- * megakernels, after each layer's computation). At epoch i rank r's input buffer (in_len[r]
- * bf16 elements, the buffer the naming refers to) is y_r = W_r x_r(i): wt[r] is W_r given
- * transposed, k rows of in_len[r] bf16 (row stride in_len[r] elements), and x_r(i) =
- * x[r] + (i % x_pool) * x_epoch_stride bytes holds k bf16. Element j of y_r: the k terms are
- * taken in 8 consecutive blocks of k/8; within a block, products wt[r][i][j] * x_r(i)[i]
- * rounded to binary32 are added in row order from the block's first product (round to
- * nearest even); the 8 block sums are added in block order; one rounding to bf16. Each
- * engine CTA runs twelve warps in this mode (eight of them compute) and stages the weight
- * rows in a 192 KiB shared-memory ring through tensor copies (TMA) of 16 rows, one CTA per
- * SM. k must be a multiple of 128; in_len[r], wt[r], x[r] and the strides must give
- * 16-byte alignment, and in_len[r] must be below 2^32. The tensor maps of W_r are encoded
- * on the host at the first run with these matrices (and again when wt or k change).
- * Errors as coll_run, plus COLL_EINVAL for a zero-copy, tagged-data or non-bf16 plan, or
- * for a plan with more warps than SMs can hold fused CTAs at once. */
+ * collective fused into its persistent loop (SiFAR review, Summary: the All-Reduces run
+ * inside megakernels, after each layer's computation). At epoch i rank r's input buffer
+ * (in_len[r] bf16 elements, the buffer the naming refers to) is y_r = W_r x_r(i): wt[r] is
+ * W_r given transposed, k rows of in_len[r] bf16 (row stride in_len[r] elements), and
+ * x_r(i) = x[r] + (i % x_pool) * x_epoch_stride bytes holds k bf16. Element j of y_r is the
+ * plain dot product: the k products wt[r][i][j] * x_r(i)[i], each rounded to binary32, added
+ * in row order i = 0..k-1 from the first product (round to nearest even, no fused
+ * multiply-add), then rounded once to bf16. Results are bit-exact. Each engine CTA runs
+ * eight warps in this mode (four compute, two streaming the weight rows and x into shared
+ * memory by tensor and bulk copies), one CTA per SM; without chained epochs the next piece
+ * is computed while the current one is exchanged. k must be a multiple of 16, at most
+ * 8192; in_len[r], wt[r], x[r] and the strides must give 16-byte alignment, and in_len[r]
+ * must be below 2^32. The tensor maps of W_r are encoded on the host at the first run with
+ * these matrices (and again when wt or k change).
+ * Errors as coll_run, plus COLL_EINVAL for a zero-copy, tagged-data or non-bf16 plan, a k
+ * outside those limits, or a plan with more warps than SMs can hold fused CTAs at once. */
 int coll_run_gemv(coll_plan_t p, const void *const *wt, void *const *x, int k, void *const *out,
                   int n_epochs, int64_t x_epoch_stride, int x_pool, int64_t out_epoch_stride,
                   void *stream);

@@ -121,6 +121,19 @@ def test_bad_config_rejected():
         cdc.validate(n, datapath="twoshot_pull", zero_copy=1)
     with pytest.raises(cdc.CollError):
         cdc.validate(n, datapath="twoshot_pull", protocol="ll")
+    # the speculation delay: -1 (the check's default) up to 100 us
+    for ok in (-1, 0, 200, 100000):
+        cdc.validate(n, protocol="spec", spec_delay_ns=ok)
+    for bad in (-2, 100001):
+        with pytest.raises(cdc.CollError):
+            cdc.validate(n, protocol="spec", spec_delay_ns=bad)
+
+
+def test_default_config_is_the_fence_free_speculative_check():
+    c = _lib.make_config()
+    assert c.protocol == _lib.D["COLL_PROTO_SPEC"]
+    assert c.spec_check == _lib.D["COLL_SPEC_TAGGED_RELAXED"]
+    assert c.spec_delay_ns == -1
 
 
 def test_buffer_lengths_beyond_the_limit_are_rejected():

@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 import collective_datapath_copy_gb300 as cdc  # noqa: E402
 from collective_datapath_copy_gb300 import namings  # noqa: E402
 from collective_datapath_copy_gb300.build import build  # noqa: E402
-from oracle import arith as oracle_arith, collectives, naming as onaming, tolerance  # noqa: E402
+from oracle import collectives, naming as onaming  # noqa: E402
 from oracle.arith import NPTYPE  # noqa: E402
 import synth  # noqa: E402
 
@@ -245,13 +245,15 @@ def _check_epochs(outs, expect_dev, n_epochs, pool):
 
 @pytest.mark.parametrize("cfg", [
     dict(protocol="spec"),
-    dict(protocol="spec", inject="stagger", inject_seed=11, inject_prob_ppm=100000,
-         inject_max_ns=20000, inject_start_ns=5000),
+    dict(protocol="spec", spec_check="tagged"),
+    dict(protocol="spec", spec_check="tagged", inject="stagger", inject_seed=11,
+         inject_prob_ppm=100000, inject_max_ns=20000, inject_start_ns=5000),
     dict(protocol="spec", spec_check="relaxed", inject="stagger", inject_seed=12,
          inject_prob_ppm=100000, inject_max_ns=20000, inject_start_ns=5000),
     dict(protocol="ll", inject="stagger", inject_seed=13, inject_prob_ppm=100000,
          inject_max_ns=20000, inject_start_ns=5000)],
-    ids=["spec", "spec-stagger", "spec-relaxed-stagger", "ll-stagger"])
+    ids=["spec-default-fence-free", "spec-tagged", "spec-tagged-stagger", "spec-relaxed-stagger",
+         "ll-stagger"])
 def test_decode_allreduce_300000_epochs_soak(cfg):
     # 30 runs of 10,000 epochs on one plan (epochs 1..300,000: the 16-bit epoch fields of
     # the flag words wrap four times), every epoch of every run checked against the oracle
@@ -274,9 +276,10 @@ def test_decode_allreduce_300000_epochs_soak(cfg):
 
 @pytest.mark.parametrize("check", ["tagged", "relaxed"])
 def test_specialised_and_stamped_engines_agree(check):
-    # a plain speculative run of the decode plan takes the variant specialised for it; the
-    # same plan with per-epoch stamps runs the general engine: both give the oracle's bits,
-    # and the stamps advance with every epoch
+    # a plain speculative run of the decode plan takes the variant specialised for it; with
+    # one stamp per epoch it takes the specialised variant that also stamps, and with four
+    # stamps per epoch the general engine: all give the oracle's bits, and the stamps
+    # advance with every epoch
     R, n, pool, E = 8, 4096, 7, 1000
     ins, expect = _decode_case(R, n, pool, seed=23)
     nm = namings.allreduce(R, n, "bf16")
@@ -298,6 +301,31 @@ def test_specialised_and_stamped_engines_agree(check):
         plan.free()
     for a, b in zip(got[0], got[1]):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("delay", [0, 50, 200, 2000])
+@pytest.mark.parametrize("check", ["tagged", "relaxed", "literal"])
+def test_speculation_delay_keeps_the_bits(check, delay):
+    # the wait before the first speculative loads moves only timing: every epoch stays the
+    # oracle's, on the specialised variants (tagged, relaxed) and the general engine
+    R, n, pool, E = 8, 4096, 7, 2000
+    ins, expect = _decode_case(R, n, pool, seed=24)
+    plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="spec", spec_check=check,
+                    spec_delay_ns=delay)
+    outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    plan.run(ins, outs, n_epochs=E, in_epoch_stride=n * 2, in_pool=pool, out_epoch_stride=n * 2)
+    st = plan.status()
+    assert st["code"] == 0, st
+    assert st["spec_checks"] == E * R * 16
+    assert _check_epochs(outs, expect, E, pool) == 0
+    plan.free()
+
+
+def test_speculation_delay_is_validated():
+    nm = namings.allreduce(2, 1024, "bf16")
+    for bad in (-2, 100001):
+        with pytest.raises(cdc.CollError):
+            cdc.Plan(nm, protocol="spec", spec_delay_ns=bad)
 
 
 @pytest.mark.parametrize("protocol", ["barrier", "dual", "spec", "ll"])
@@ -383,10 +411,10 @@ def test_decode_allreduce_10000_epochs_spec_equals_barrier_under_stagger():
     res = {}
     for name, cfg in [("barrier", dict(protocol="barrier")),
                       ("dual", dict(protocol="dual")),
-                      ("spec", dict(protocol="spec")),
-                      ("spec-stagger", dict(protocol="spec", inject="stagger", inject_seed=2,
-                                            inject_prob_ppm=100000, inject_max_ns=20000,
-                                            inject_start_ns=5000)),
+                      ("spec", dict(protocol="spec", spec_check="tagged")),
+                      ("spec-stagger", dict(protocol="spec", spec_check="tagged", inject="stagger",
+                                            inject_seed=2, inject_prob_ppm=100000,
+                                            inject_max_ns=20000, inject_start_ns=5000)),
                       ("spec-relaxed", dict(protocol="spec", spec_check="relaxed")),
                       ("spec-relaxed-stagger", dict(protocol="spec", spec_check="relaxed",
                                                     inject="stagger", inject_seed=3,
@@ -419,7 +447,7 @@ def test_decode_allreduce_10000_epochs_spec_equals_barrier_under_stagger():
     assert res["spec"][1]["spec_checks"] == E * R * 16
     # the content tags of producer and consumer agree: first attempts do pass (tags computed
     # differently on the two sides would fail every one); how many pass depends on how
-    # closely the warps run in step, 40-55 % retried in the specialised variants
+    # closely the warps run in step and on the speculation delay
     assert res["spec"][1]["spec_retries"] < 0.9 * res["spec"][1]["spec_checks"]
     assert res["spec-relaxed"][1]["spec_retries"] < 0.9 * res["spec-relaxed"][1]["spec_checks"]
 
@@ -700,39 +728,20 @@ def test_staged_plan_replays_inside_a_cuda_graph(cfg):
     plan.free()
 
 
-# The fused producer's kernel adds each output's k products in eight consecutive k-blocks
-# (one per compute warp) and then adds the block sums in order: another order than the
-# oracle's plain row-order chain. Its outputs are therefore held to the oracle's tolerance
-# for other summation orders (oracle.tolerance.gemv_sum_within_tolerance), computed from
-# the plain definition of y = W x and the rank-order sum over ranks.
+# The fused producer computes every output of y_r = W_r x_r as the plain ordered chain over
+# k (one binary32 chain per output column, in row order), so its outputs equal the oracle's
+# bit for bit: the rank-order sum over ranks of oracle.collectives.gemv_payloads.
 
 def fused_sum_ok(got, wts, xs):
     """got: bf16 patterns of the rank-order sum over ranks of the payloads W_r x_r."""
-    return bool(tolerance.gemv_sum_within_tolerance(got, wts, xs).all())
+    want = collectives.allreduce(collectives.gemv_payloads(wts, xs), "bf16")[0]
+    return bits_equal(got, want)
 
 
-def fused_epoch_bounds(wts, xs_by_set):
-    """Device tensors (t, bound) [sets, n] of the acceptance intervals of each input set
-    (finite results only: these cases have no infinities or NaNs)."""
-    ts, bs = [], []
-    for xs in xs_by_set:
-        t, b, ref = tolerance.gemv_sum_interval(wts, xs)
-        assert np.isfinite(oracle_arith.bf16_to_f32(ref)).all()
-        ts.append(t)
-        bs.append(b)
-    return (torch.from_numpy(np.stack(ts)).to("cuda"), torch.from_numpy(np.stack(bs)).to("cuda"))
-
-
-def check_fused_epochs(outs, t_dev, b_dev, n_epochs, pool):
-    """outs[r]: [n_epochs, n] bf16 device tensors; epoch i must lie within input set i %
-    pool's interval. Returns the number of (rank, epoch) rows with an element outside."""
-    idx = torch.arange(n_epochs, device="cuda") % pool
-    t, b = t_dev[idx], b_dev[idx]
-    bad = 0
-    for o in outs:
-        g = ((o.to(torch.int32) & 0xFFFF) << 16).view(torch.float32).double()
-        bad += int(((g - t).abs() > b).any(dim=1).sum())
-    return bad
+def fused_epoch_expect(wts, xs_by_set):
+    """Device tensor [sets, n] of the oracle's output for each input set."""
+    return torch.stack([to_dev(collectives.allreduce(collectives.gemv_payloads(wts, xs),
+                                                     "bf16")[0], "bf16") for xs in xs_by_set])
 
 
 def test_fused_run_replays_inside_a_cuda_graph_and_follows_new_weights():
@@ -963,7 +972,7 @@ def _gemv_case(R, n, k, pool, seed):
                                                      ("spec", "oneshot", 0), ("spec", "twoshot", 0),
                                                      ("spec", "oneshot", 1),
                                                      ("dual", "twoshot_pull", 1)])
-def test_fused_gemv_allreduce_matches_the_oracle(protocol, datapath, chain):
+def test_fused_gemv_allreduce_bit_exact(protocol, datapath, chain):
     R, n, k, pool, E = 8, 4096, 256, 3, 24
     wts, xs = _gemv_case(R, n, k, pool, 97)
     plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol=protocol, datapath=datapath,
@@ -976,10 +985,8 @@ def test_fused_gemv_allreduce_matches_the_oracle(protocol, datapath, chain):
     assert plan.status()["code"] == 0
     for e in range(E):
         xe = [xs[r][e % pool] for r in range(R)]
-        got = [from_dev(outs[r][e], "bf16") for r in range(R)]
-        assert fused_sum_ok(got[0], wts, xe), e
-        for r in range(1, R):  # every rank holds the same sum (same order, same payloads)
-            assert bits_equal(got[r], got[0]), (e, r)
+        for r in range(R):
+            assert fused_sum_ok(from_dev(outs[r][e], "bf16"), wts, xe), (e, r)
     plan.free()
 
 
@@ -989,7 +996,7 @@ def test_fused_gemv_2000_epochs_under_stagger(chain):
     # started apart; every epoch must still equal the oracle
     R, n, k, pool, E = 8, 4096, 256, 3, 2000
     wts, xs = _gemv_case(R, n, k, pool, 97)
-    t_dev, b_dev = fused_epoch_bounds(wts, [[xs[r][e] for r in range(R)] for e in range(pool)])
+    want_dev = fused_epoch_expect(wts, [[xs[r][e] for r in range(R)] for e in range(pool)])
     plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="spec", chain=chain,
                     inject="stagger", inject_seed=7 + chain, inject_prob_ppm=100000,
                     inject_max_ns=20000, inject_start_ns=5000)
@@ -1000,10 +1007,7 @@ def test_fused_gemv_2000_epochs_under_stagger(chain):
                   out_epoch_stride=2 * n)
     st = plan.status()
     assert st["code"] == 0, st
-    assert check_fused_epochs(outs, t_dev, b_dev, E, pool) == 0
-    # timing does not move bits: every epoch equals the first epoch of its input set
-    for o in outs:
-        assert bool((o == o[torch.arange(E, device="cuda") % pool]).all())
+    assert _check_epochs(outs, want_dev, E, pool) == 0
     plan.free()
 
 
@@ -1017,16 +1021,13 @@ def test_fused_gemv_with_a_reduce_scatter_naming_and_bad_arguments():
     outs = [torch.empty(n // R, dtype=torch.int16, device="cuda") for _ in range(R)]
     plan.run_gemv(dw, dx, k, outs)
     assert plan.status()["code"] == 0
-    b = n // R
+    want = collectives.reduce_scatter(collectives.gemv_payloads(wts, x0), "bf16")
     for r in range(R):  # rank r holds block r of the sum
-        ok = tolerance.gemv_sum_within_tolerance(
-            np.concatenate([np.zeros(r * b, np.uint16), from_dev(outs[r], "bf16"),
-                            np.zeros(n - (r + 1) * b, np.uint16)]), wts, x0)
-        assert ok[r * b:(r + 1) * b].all(), r
+        assert bits_equal(from_dev(outs[r], "bf16"), want[r]), r
     with pytest.raises(cdc.CollError):
-        plan.run_gemv(dw, dx, 12, outs)  # k not a multiple of 128
+        plan.run_gemv(dw, dx, 12, outs)  # k not a multiple of 16
     with pytest.raises(cdc.CollError):
-        plan.run_gemv(dw, dx, 64, outs)  # nor is 64
+        plan.run_gemv(dw, dx, 8208, outs)  # x longer than the staging buffer (8192)
     zc = cdc.Plan(namings.allreduce(R, n, "bf16"), zero_copy=1)
     with pytest.raises(cdc.CollError):
         zc.run_gemv(dw, dx, k, [torch.empty(n, dtype=torch.int16, device="cuda") for _ in range(R)])
@@ -1035,19 +1036,23 @@ def test_fused_gemv_with_a_reduce_scatter_naming_and_bad_arguments():
 
 
 
-@pytest.mark.parametrize("k,n,wpr", [(128, 4096, 0), (1024, 4096, 0), (512, 4096, 2),
-                                     (128, 1000, 0), (256, 1000, 0), (8192, 1024, 0),
-                                     (128, 4352, 1), (384, 4096, 0)],
-                         ids=["k128-several-pieces-per-ring-lap", "k1024-ring-wraps-inside-a-piece",
-                              "k512-four-pieces-per-warp", "k128-ragged-last-piece",
-                              "k256-ragged-last-piece-two-fills", "k8192-largest-x",
-                              "k128-seventeen-pieces-per-warp", "k384-three-fills-per-block"])
+@pytest.mark.parametrize("k,n,wpr", [(16, 4096, 0), (80, 4096, 0), (128, 4096, 0),
+                                     (1024, 4096, 0), (512, 4096, 2), (128, 1000, 0),
+                                     (256, 1000, 0), (8192, 1024, 0), (128, 4352, 1),
+                                     (320, 4096, 0), (48, 2048, 0)],
+                         ids=["k16-one-partial-fill", "k80-full-and-partial-fill",
+                              "k128-several-pieces-per-ring-lap",
+                              "k1024-ring-wraps-inside-a-piece", "k512-four-pieces-per-warp",
+                              "k128-ragged-last-piece", "k256-ragged-last-piece",
+                              "k8192-largest-x", "k128-seventeen-pieces-per-warp",
+                              "k320-a-piece-fills-the-ring", "k48-partial-fill"])
 def test_fused_gemv_weight_ring_shapes(k, n, wpr):
-    # Each compute warp streams its rows through a private ring of 3 slots (16 weight rows
-    # per slot, one tensor copy each); these shapes cover a ring lap holding several pieces,
-    # a piece longer than the ring, warps with several stage items (more than the 16 whose
-    # sources are cached), a block as long as the ring, and a last piece shorter than 512
-    # bytes, whose copies read zeros past the matrix.
+    # The weight rows stream through one ring of 5 slots of 64 rows (one tensor copy each)
+    # shared by the compute warps, and x through two buffers: these shapes cover a last fill
+    # only partly inside the matrix (its rows past k read zeros), several pieces per ring
+    # lap, a piece longer than the ring, a piece exactly as long, warps with several stage
+    # items (more than the 16 whose sources are cached), the longest x, and a last piece
+    # shorter than 512 bytes, whose copies read zeros past the matrix's columns.
     R, pool, E = 4, 2, 6
     wts, xs = _gemv_case(R, n, k, pool, 99 + k)
     plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="dual", warps_per_rank=wpr)
@@ -1065,9 +1070,9 @@ def test_fused_gemv_weight_ring_shapes(k, n, wpr):
 
 
 def test_fused_gemv_signed_zeros():
-    # a chain starts from its first product: weights of -0 against x >= +0 give -0 payloads
-    # (in any order: -0 + -0 is -0), and the fixed-order sum of -0 over ranks stays -0; a
-    # rank with +0 payloads turns the sum into +0. Exact bits, whatever the adding order.
+    # a chain starts from its first product: weights of -0 against x >= +0 give -0 payloads,
+    # and the fixed-order sum of -0 over ranks stays -0; a rank with +0 payloads turns the
+    # sum into +0
     R, n, k = 4, 1024, 128
     rng = synth.seeded_rng(93)
     xs = [(synth.normal_bf16(rng, k) & np.uint16(0x7FFF)).astype(np.uint16) for _ in range(R)]
@@ -1107,7 +1112,6 @@ def test_fused_gemv_product_overflow_keeps_the_separate_rounding(unsafe):
         xs[0][1][0], xs[0][1][1] = 0x6000, 0x6080      # epoch 1: 2^65, 2^66
     want = [collectives.allreduce(collectives.gemv_payloads(wts, [xs[r][e] for r in range(R)]),
                                   "bf16")[0] for e in range(E)]
-    # (the infinity is the same in any adding order: +inf absorbs the finite terms)
     if unsafe == "weights":
         assert all(w[0] == 0x7F80 for w in want)
     else:
@@ -1120,12 +1124,8 @@ def test_fused_gemv_product_overflow_keeps_the_separate_rounding(unsafe):
                   out_epoch_stride=2 * n)
     assert plan.status()["code"] == 0
     for e in range(E):
-        xe = [xs[r][e] for r in range(R)]
         for r in range(R):
-            got = from_dev(outs[r][e], "bf16")
-            if want[e][0] == 0x7F80:
-                assert got[0] == 0x7F80, (e, r)
-            assert fused_sum_ok(got, wts, xe), (e, r)
+            assert bits_equal(from_dev(outs[r][e], "bf16"), want[e]), (e, r)
     plan.free()
 
 

@@ -1,131 +1,299 @@
-"""CPU model of a fused-producer compute warp's weight ring (no GPU).
+"""CPU model of the fused producer's shared-memory pipeline (no GPU).
 
-Each compute warp streams its k-block of weight rows through a private ring of 3 shared-
-memory slots, one 16-row tensor copy per slot, completed on the slot's mbarrier. The model
-follows the kernel's steps (the prologue's first 3 fills; per block: a readiness test of
-the fills already issued, a parity wait on the slot, reading it, refilling it with the fill
-3 ahead when that fill belongs to the same block, else holding the refill back until the
-block's results are handed over) under random landing orders of the copies, and checks:
-every read finds its own fill landed; no slot is refilled before its previous fill was read;
-every readiness test targets a fill already issued (a parity test of an unissued fill could
-take the slot's previous phase for it); every fill carries the rows and stage item its
-number stands for; every fill issued is read.
+One fused CTA runs four roles that meet only through mbarriers and one shared counter:
+- the weight streamer fills a ring of S slots (one tensor copy of 64 rows each) with every fill
+  of the run in order, fill f into slot f % S once the compute lanes released the slot's
+  previous fill (empty[s], parity of lap f // S, inverted);
+- the x streamer copies piece q's x into buffer q % 2 once the engine has opened piece q
+  (go > q);
+- four compute warps take the pieces in order: wait for the piece's x (xfull), read the
+  piece's fills in order (full[s], parity of lap), release each slot, write their part of
+  result slot q % 2 and arrive on rfull;
+- the engine takes piece q from its result slot (rfull) and opens piece q + 2 (go =
+  min(taken + 2, pieces its chained epochs allow, total)); with chained epochs, an epoch's
+  pieces are opened only when the engine reaches that epoch.
+The model follows those steps with mbarriers modelled as in the PTX ISA (arrival count,
+transaction bytes, phase; a parity wait passes iff the phase of that parity has completed)
+under random interleavings of the roles and random landing orders of the copies, and checks:
+every read finds the data its number stands for; no slot, x buffer or result slot is
+overwritten before every reader has finished with its previous contents; every role ends
+(no wait on a phase that can no longer complete). The go counter alone also guards the x
+buffers and the result slots: piece q is opened only once piece q - 2 has been taken, so its
+x and its result slot are free by then. Each wait of the protocol is shown necessary by a
+variant without it that the model catches.
 """
 
 import random
 
 import pytest
 
-SLOTS = 3
+WARPS = 4       # compute warps
+LANES = 32      # arrivals per compute warp (every lane arrives)
 
 
-class Ring:
-    def __init__(self, bs, nitems, epochs, seed):
+class MBar:
+    def __init__(self, count):
+        self.count, self.pending, self.tx, self.phase = count, count, 0, 0
+
+    def _check(self):
+        if self.pending == 0 and self.tx == 0:
+            self.phase += 1
+            self.pending = self.count
+
+    def arrive(self, n=1):
+        assert self.pending >= n, "more arrivals than the phase expects"
+        self.pending -= n
+        self._check()
+
+    def expect_tx(self, nbytes):
+        self.tx += nbytes
+        self.arrive()
+
+    def complete_tx(self, nbytes):
+        self.tx -= nbytes
+        assert self.tx >= 0
+        self._check()
+
+    def done(self, parity):
+        return (self.phase & 1) != (parity & 1)
+
+
+class Pipeline:
+    def __init__(self, S, kslots, nitems, epochs, chain, seed, mutant=None):
         self.rnd = random.Random(seed)
-        self.bs, self.nitems = bs, nitems
-        self.total = epochs * nitems * bs
-        self.issued = {}  # fill number -> (slot, row block, item)
-        self.landed = set()
-        self.read = set()
-        self.last_in_slot = {}
-        self.phase = [0] * SLOTS  # completed phases per slot
+        self.mutant = mutant
+        self.S, self.kslots, self.nitems, self.chain = S, kslots, nitems, chain
+        self.total = epochs * nitems
+        self.full = [MBar(1) for _ in range(S)]
+        self.empty = [MBar(WARPS * LANES) for _ in range(S)]
+        self.xfull = [MBar(1) for _ in range(2)]
+        self.rfull = [MBar(WARPS * LANES) for _ in range(2)]
+        self.slot = [None] * S          # fill number held by each slot
+        self.slot_readers = [set(range(WARPS))] * S  # warps that read the current fill
+        self.xbuf = [None, None]
+        self.x_readers = [set(range(WARPS)), set(range(WARPS))]
+        self.res = [[None] * WARPS for _ in range(2)]
+        self.taken_from = [None, None]  # last piece the engine took from each result slot
+        self.copies = []                # in flight: (kind, index, number)
+        self.go = 0 if chain else min(2, self.total)
+        self.taken = 0
+        self.chain_open = 0 if chain else 1 << 62
 
-    def fill(self, slot, rj, item, t):
-        assert t not in self.issued
-        assert slot == t % SLOTS, ("slot", t, slot)
-        assert rj == t % self.bs and item == (t // self.bs) % self.nitems, ("rows", t, rj, item)
-        prev = self.last_in_slot.get(slot)
-        assert prev is None or prev in self.read, ("refill before read", t, prev)
-        self.issued[t] = (slot, rj, item)
-        self.last_in_slot[slot] = t
+    def open_pieces(self):
+        ahead = 3 if self.mutant == "opens three pieces ahead" else 2
+        self.go = min(self.taken + ahead, self.chain_open, self.total)
 
-    def land_some(self):
-        for t in sorted(set(self.issued) - self.landed):
-            # a slot's phases complete in order: its previous fill has landed already
-            if self.rnd.random() < 0.5 and (t < SLOTS or t - SLOTS in self.landed):
-                self.landed.add(t)
-                self.phase[t % SLOTS] += 1
+    # ------------------------------------------------------------ roles (generators)
+    def weight_streamer(self):
+        F = self.total * self.kslots
+        for f in range(F):
+            s, lap = f % self.S, f // self.S
+            while self.mutant != "no empty wait" and not self.empty[s].done((lap & 1) ^ 1):
+                yield
+            assert self.slot_readers[s] == set(range(WARPS)), ("slot refilled before read", f)
+            self.full[s].expect_tx(8192)
+            self.copies.append(("w", s, f))
+            yield
 
-    def parity_done(self, slot, lap):
-        # mbarrier parity test: the phase of parity lap & 1 has completed iff the current
-        # phase's parity differs
-        return (self.phase[slot] & 1) != (lap & 1)
+    def x_streamer(self):
+        for q in range(self.total):
+            while self.mutant != "x streamer ignores go" and self.go <= q:
+                yield
+            p = q % 2
+            assert self.x_readers[p] == set(range(WARPS)), ("x overwritten before read", q)
+            self.xfull[p].expect_tx(1024)
+            self.copies.append(("x", p, q))
+            yield
 
+    def compute(self, w):
+        s = lap = 0
+        for q in range(self.total):
+            p = q % 2
+            while self.mutant != "no xfull wait" and not self.xfull[p].done((q // 2) & 1):
+                yield
+            assert self.xbuf[p] == q, ("wrong x", q, self.xbuf[p])
+            for j in range(self.kslots):
+                while self.mutant != "no full wait" and not self.full[s].done(lap & 1):
+                    yield
+                f = q * self.kslots + j
+                assert self.slot[s] == f, ("wrong rows", f, self.slot[s])
+                self.slot_readers[s] = self.slot_readers[s] | {w}
+                self.empty[s].arrive(LANES)
+                s += 1
+                if s == self.S:
+                    s, lap = 0, lap + 1
+                yield
+            self.x_readers[p] = self.x_readers[p] | {w}
+            assert q < 2 or self.taken_from[p] == q - 2, ("result slot overwritten before taken", q)
+            self.res[p][w] = q
+            self.rfull[p].arrive(LANES)
+            yield
 
-def run(bs, nitems, epochs, seed):
-    m = Ring(bs, nitems, epochs, seed)
-    # prologue: fills 0..2; the refill cursor then points at fill 3
-    j = ri = 0
-    for q in range(SLOTS):
-        if q < m.total:
-            m.fill(q % SLOTS, j, ri, q)
-        j += 1
-        if j == bs:
-            j, ri = 0, (ri + 1) % nitems
-    q, lap, slot, rp_j, r_i = 0, 0, 0, j, ri
-    for _piece in range(epochs * nitems):
-        m.land_some()
-        qe = q + bs
-        pend = None
-        npend = 0
-        for jj in range(bs):
-            if jj % 32 == 0:
-                for lane in range(SLOTS):
-                    if jj + lane < bs:
-                        t = q + lane
-                        assert t in m.issued, ("readiness test of an unissued fill", t)
-                        o = slot + lane
-                        wrap = 1 if o >= SLOTS else 0
-                        s_, l_ = o - wrap * SLOTS, lap + wrap
-                        assert (s_, l_) == (t % SLOTS, t // SLOTS)
-                        if m.parity_done(s_, l_):
-                            assert t in m.landed, ("aliased readiness", t)
-            assert (slot, lap) == (q % SLOTS, q // SLOTS)
-            steps = 0
-            while q not in m.landed:
-                m.land_some()
-                steps += 1
-                assert steps < 10000, "deadlock"
-            m.read.add(q)
-            if q + SLOTS < m.total:
-                if q + SLOTS < qe:
-                    m.fill(slot, rp_j, r_i, q + SLOTS)
-                else:
-                    if npend == 0:
-                        pend = (slot, rp_j, r_i, q + SLOTS)
-                    npend += 1
-            q += 1
-            slot += 1
-            if slot == SLOTS:
-                slot, lap = 0, lap + 1
-            rp_j += 1
-            if rp_j == bs:
-                rp_j, r_i = 0, (r_i + 1) % nitems
-            if m.rnd.random() < 0.3:
-                m.land_some()
-        if npend:  # after the block's results are handed over
-            s_, rj, it, t = pend
-            for d in range(npend):
-                m.fill(s_, rj, it, t + d)
-                s_ = (s_ + 1) % SLOTS
-                rj += 1
-                if rj == bs:
-                    rj, it = 0, (it + 1) % nitems
-    assert len(m.read) == m.total
-    assert set(m.issued) == m.read
+    def engine(self):
+        for q in range(self.total):
+            if self.chain and q % self.nitems == 0:
+                # the chained wait for this epoch (other CTAs' progress): some random delay
+                for _ in range(self.rnd.randrange(4)):
+                    yield
+                self.chain_open = q + self.nitems
+                self.open_pieces()
+            p = q % 2
+            while self.mutant != "no rfull wait" and not self.rfull[p].done((q // 2) & 1):
+                yield
+            assert self.res[p] == [q] * WARPS, ("wrong results", q, self.res[p])
+            self.taken_from[p] = q
+            self.taken = q + 1
+            self.open_pieces()
+            yield
 
-
-@pytest.mark.parametrize("bs", [1, 2, 3, 4, 5, 8, 31, 32, 33, 64])
-@pytest.mark.parametrize("nitems", [1, 2, 3, 17])
-def test_ring_reads_refills_and_readiness(bs, nitems):
-    for epochs in (1, 2, 5):
-        for seed in range(3):
-            run(bs, nitems, epochs, seed)
+    def land_one(self):
+        if not self.copies:
+            return
+        kind, i, n = self.copies.pop(self.rnd.randrange(len(self.copies)))
+        if kind == "w":
+            self.slot[i] = n
+            self.slot_readers[i] = set()
+            self.full[i].complete_tx(8192)
+        else:
+            self.xbuf[i] = n
+            self.x_readers[i] = set()
+            self.xfull[i].complete_tx(1024)
 
 
-def test_model_catches_a_refill_before_the_read():
-    # the check is live: issuing a fill into a slot whose previous fill was not read fails
-    m = Ring(4, 1, 2, 0)
-    m.fill(0, 0, 0, 0)
-    with pytest.raises(AssertionError):
-        m.fill(0, 3, 0, 3)
+def simulate(S, kslots, nitems, epochs, chain, seed, mutant=None):
+    m = Pipeline(S, kslots, nitems, epochs, chain, seed, mutant)
+    roles = [m.weight_streamer(), m.x_streamer(), m.engine()] + [m.compute(w) for w in range(WARPS)]
+    live = list(roles)
+    steps = 0
+    while live:
+        steps += 1
+        assert steps < 200000, "no progress: a wait cannot complete"
+        if m.copies and m.rnd.random() < 0.3:
+            m.land_one()
+            continue
+        g = m.rnd.choice(live)
+        try:
+            next(g)
+        except StopIteration:
+            live.remove(g)
+    assert not m.copies
+    assert m.taken == m.total
+    return m
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_pipeline_orders_every_buffer(seed):
+    rnd = random.Random(1000 + seed)
+    S = rnd.choice([2, 3, 4, 5, 22])
+    kslots = rnd.choice([1, 2, 3, 5, 7, 32])
+    nitems = rnd.choice([1, 1, 2, 3])
+    epochs = rnd.choice([1, 2, 3, 5])
+    chain = rnd.random() < 0.5
+    simulate(S, kslots, nitems, epochs, chain, seed)
+
+
+@pytest.mark.parametrize("mutant", ["no empty wait", "no full wait", "no xfull wait",
+                                    "no rfull wait", "x streamer ignores go",
+                                    "opens three pieces ahead"])
+def test_the_model_catches_a_missing_wait(mutant):
+    # each wait of the protocol is needed: without it, some interleaving overwrites a buffer
+    # that a reader still needs, or reads the wrong data
+    caught = 0
+    for seed in range(60):
+        for cfg in ((2, 3, 1, 4), (4, 1, 2, 4)):
+            try:
+                simulate(*cfg, False, seed, mutant)
+            except AssertionError:
+                caught += 1
+    assert caught > 0, mutant
+
+
+# ------------------------------------------------------------ zero-copy bulk ring
+
+class BulkRing:
+    """The zero-copy bulk ring of one CTA: a producer warp resolves tiles 32 at a time into
+    one half of a two-batch table, then issues each tile into stage k % S once the consumer
+    warps released that stage's previous tile; the consumers take the tiles in order, read
+    the tile's table entry through the stage and release the stage."""
+
+    def __init__(self, S, ntiles, consumers, seed, mutant=None):
+        self.rnd = random.Random(seed)
+        self.S, self.ntiles, self.C, self.mutant = S, ntiles, consumers, mutant
+        self.full = [MBar(1) for _ in range(S)]
+        self.empty = [MBar(consumers) for _ in range(S)]
+        self.table = [[None] * 32 for _ in range(2)]
+        self.stile = [None] * S
+        self.readers = {}       # (half, i) -> consumers still to read that entry's tile
+        self.copies = []
+        self.got = [[] for _ in range(consumers)]
+
+    def producer(self):
+        k = 0
+        for m, t0 in enumerate(range(0, self.ntiles, 32)):
+            half = m % 2 if self.mutant != "one table half" else 0
+            batch = min(32, self.ntiles - t0)
+            for i in range(batch):
+                assert not self.readers.get((half, i)), ("table entry rewritten while read", t0 + i)
+                self.table[half][i] = t0 + i
+            yield
+            for i in range(batch):
+                s, lap = k % self.S, k // self.S
+                while not self.empty[s].done((lap & 1) ^ 1):
+                    yield
+                self.stile[s] = (half, i)
+                self.readers[(half, i)] = set(range(self.C))
+                self.full[s].expect_tx(4096)
+                self.copies.append(s)
+                k += 1
+                yield
+
+    def consumer(self, c):
+        for k in range(self.ntiles):
+            s, lap = k % self.S, k // self.S
+            while not self.full[s].done(lap & 1):
+                yield
+            half, i = self.stile[s]
+            self.got[c].append(self.table[half][i])
+            self.readers[(half, i)].discard(c)
+            self.empty[s].arrive()
+            yield
+
+    def land_one(self):
+        s = self.copies.pop(self.rnd.randrange(len(self.copies)))
+        self.full[s].complete_tx(4096)
+
+
+def simulate_bulk(S, ntiles, consumers, seed, mutant=None):
+    m = BulkRing(S, ntiles, consumers, seed, mutant)
+    live = [m.producer()] + [m.consumer(c) for c in range(consumers)]
+    steps = 0
+    while live:
+        steps += 1
+        assert steps < 200000, "no progress"
+        if m.copies and m.rnd.random() < 0.3:
+            m.land_one()
+            continue
+        g = m.rnd.choice(live)
+        try:
+            next(g)
+        except StopIteration:
+            live.remove(g)
+    for c in range(consumers):
+        assert m.got[c] == list(range(ntiles)), c
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_bulk_ring_table_halves(seed):
+    rnd = random.Random(2000 + seed)
+    simulate_bulk(rnd.choice([2, 3, 6, 8]), rnd.choice([1, 31, 32, 33, 64, 100, 150]),
+                  rnd.choice([1, 8]), seed)
+
+
+def test_the_bulk_model_catches_a_single_table_half():
+    caught = 0
+    for seed in range(40):
+        try:
+            simulate_bulk(6, 100, 8, seed, mutant="one table half")
+        except AssertionError:
+            caught += 1
+    assert caught > 0
