@@ -12,8 +12,8 @@ configuration (eight collectives at 16, 64 and 256 MiB per rank, the prefill all
 one-shot and two-shot, MoE dispatch and combine) as achieved HBM GB/s.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|sweep|prefill|moe|moe_combine|fig15|fused]
-                    [--max-bytes B]
+                    [--workload decode|sweep|prefill|moe|moe_combine|fig15|fused|single]
+                    [--max-bytes B] [--collective C --mib M --datapath D] [--protocols P]
 
 Under torchrun each rank runs an independent replica on its own GPU (the emulated
 collective needs no inter-GPU exchange); rank 0 prints one JSON line.
@@ -785,6 +785,26 @@ def run_workload(args):
     elif args.workload == "prefill":
         res.update(prefill_allreduce(torch, cdc, dev, flush, stream, peak, args.steps,
                                      args.warmup))
+    elif args.workload == "single":
+        # one collective at one size (zero-copy datapath, R=8, bf16 uniform[-1,1]): `steps`
+        # launches, each right after an L2 flush (a short run to profile one kernel)
+        n = (args.mib << 20) // 2
+        nm = getattr(cdc, args.collective)(R, n, "bf16")
+        ins = [synth.device_uniform_bf16(torch, 3000 + r, n, dev) for r in range(R)]
+        outs = [torch.empty(L, dtype=torch.int16, device=dev) for L in nm.out_len]
+        cfg = {"datapath": args.datapath} if args.datapath else {}
+        pl = cdc.Plan(nm, zero_copy=1, **cfg)
+        tt = _time_steps(torch, pl.bind(ins, outs), args.steps, args.warmup, flush, stream)
+        if pl.status()["code"] != 0:
+            raise RuntimeError(f"run failed: {pl.status()}")
+        r = _stats_us(tt)
+        r["gbs"] = round(pl.info.min_bytes / (r["us_median"] * 1e-6) / 1e9, 1)
+        r["frac"] = round(r["gbs"] / peak, 4)
+        res.update({"collective": args.collective, "mib_per_rank": args.mib,
+                    "datapath": args.datapath or "default", "min_bytes": int(pl.info.min_bytes),
+                    "kernel": "bulk_kernel" if pl.info.bulk_tile_bytes else "zc_kernel",
+                    "single": r})
+        pl.free()
     elif args.workload == "fig15":
         # SiFAR Fig. 15 grid: R = 2/4/8 ranks x 8/16/32 KB payloads, every protocol and
         # datapath, 2000 epochs per launch; microseconds per epoch (median of K launches)
@@ -832,7 +852,7 @@ def run_workload(args):
         outs = [torch.empty(E, n, dtype=torch.int16, device=dev) for _ in range(Rr)]
         nm = cdc.allreduce(Rr, n, "bf16")
         rows = []
-        for proto in ("barrier", "dual", "spec"):
+        for proto in args.protocols.split(","):
             for chain in (0, 1):
                 pl = cdc.Plan(nm, protocol=proto, chain=chain)
                 tf = _time_steps(torch, lambda: pl.run_gemv(wts, xs, k, outs, n_epochs=E,
@@ -871,8 +891,14 @@ def main():
                     help="leave out the large-payload collectives of the default run")
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "sweep", "prefill", "moe", "moe_combine", "fig15",
-                             "fused"])
+                             "fused", "single"])
     ap.add_argument("--max-bytes", type=int, default=0, help="sweep: largest bytes per rank")
+    ap.add_argument("--collective", default="allreduce", choices=list(LARGE_KINDS),
+                    help="single: the collective")
+    ap.add_argument("--mib", type=int, default=16, help="single: MiB per rank")
+    ap.add_argument("--datapath", default="", help="single: oneshot or twoshot (sums)")
+    ap.add_argument("--protocols", default="barrier,dual,spec",
+                    help="fused: protocols to run, comma-separated")
     ap.add_argument("--print-sources-sha", action="store_true",
                     help="print the sha256 of the engine kernel's sources and exit")
     args = ap.parse_args()

@@ -374,6 +374,7 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
       a.slot_bytes = c.bulk_slot;
       a.stages = c.bulk_stages;
       a.maxsrc = c.bulk_maxsrc;
+      a.dyn_tail = c.bulk_tail ? 1u : 0u;
       err = coll::launch_bulk(c.op, c.dtype, a, c.cfg.ctas ? c.cfg.ctas : p->num_sms, s);
     } else {
       const int ctas = c.cfg.ctas ? c.cfg.ctas : 3 * p->num_sms;
@@ -440,6 +441,9 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
         c.cfg.protocol != COLL_PROTO_SPEC ? 0u
         : c.cfg.spec_delay_ns >= 0      ? (uint32_t)c.cfg.spec_delay_ns
         : c.cfg.spec_check == COLL_SPEC_TAGGED_RELAXED ? 200u : 0u;
+    // the default window of the fence-free check adapts per warp; a set one stays fixed
+    a.spec_adapt = c.cfg.protocol == COLL_PROTO_SPEC && c.cfg.spec_delay_ns < 0 &&
+                   c.cfg.spec_check == COLL_SPEC_TAGGED_RELAXED;
     a.spin_ns = c.cfg.spin_limit_ns ? c.cfg.spin_limit_ns : 2000000000ull;
     a.inject_flags = c.cfg.inject_flags;
     a.inject_seed = c.cfg.inject_seed;

@@ -25,10 +25,15 @@ namespace {
 constexpr uint32_t kConsumerWarps = 8;
 constexpr unsigned FULLW = 0xFFFFFFFFu;
 constexpr uint32_t kThreads = 32 * (kConsumerWarps + 1);
+constexpr uint32_t kClaim = 2;   // tiles per claim of the dynamic tail
+constexpr uint32_t kTable = 64;  // resolved tiles held (>= 32 + the ring's stages)
 
 // A resolved tile: its sources and destinations as pointers, sizes and counts. The
-// producer warp resolves tiles 32 at a time (one per lane) into one half of a two-batch
-// table in shared memory; a stage records which entry it holds.
+// producer warp resolves a batch of tiles (one per lane) into a table of kTable entries in
+// shared memory, the tile this CTA issues k-th into entry k % kTable; a stage records which
+// entry it holds. Entry k % kTable was last used by tile k - kTable, and issuing tile k - 1
+// waited for tile k - 1 - S to be released (S <= 8 stages): a batch of up to 32 tiles
+// starting at k only overwrites entries of released tiles.
 struct TileRec {
   const char *src[COLL_BULK_MAX_SRC];
   char *dst[COLL_BULK_MAX_DST];
@@ -48,9 +53,10 @@ __device__ void bulk_timeout(coll_dev_status_t *st, uint32_t tile) {
 template <int KIND, bool TREE>
 __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ TileRec table[2][32];
+  __shared__ TileRec table[kTable];
   __shared__ volatile uint32_t s_abort;
   __shared__ uint32_t s_issued;
+  __shared__ volatile uint32_t s_final;  // tiles this CTA issues in all, once known
   const uint32_t S = a.stages;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
   uint64_t *empty = full + S;
@@ -68,76 +74,112 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
     }
     s_abort = 0;
     s_issued = 0;
+    s_final = 0xFFFFFFFFu;
     mbar_init_fence();
   }
   __syncthreads();
 
   uint32_t consumed = 0;
   if (warp == 0) {
-    // Producer warp. Each batch: lane i resolves tile t0 + i * grid from its record (one
-    // memory round trip for 32 tiles) into table[batch & 1][i]. Then, tile by tile: lane 0
-    // waits for the stage to be free, records the tile's entry and the bytes to expect, and
-    // lanes j < nsrc each issue source j's bulk copy. The table half of batch m + 1 is
-    // written only after every tile of batch m was issued, by which time the consumers
-    // have released every tile of batch m - 1 (the ring has fewer than 32 stages).
-    uint32_t k = 0, s = 0, lap = 0, half = 0;
-    bool stop = false;
-    for (uint64_t t0 = blockIdx.x; t0 < total && !stop; t0 += 32ull * gridDim.x, half ^= 1u) {
-      const uint64_t t = t0 + (uint64_t)lane * gridDim.x;
-      const bool have = t < total;
+    // Producer warp. Tiles come in batches: first dealt round-robin (tile b + i * grid of
+    // the first static_tiles), then, for the tail, claimed kClaim at a time from a counter
+    // shared by the CTAs, so that SMs that run faster take more of the last tiles. Lane i
+    // resolves tile i of a batch from its record (one memory round trip per batch) into the
+    // table. Then, tile by tile: lane 0 waits for the stage to be free, records the tile's
+    // entry and the bytes to expect, and lanes j < nsrc each issue source j's bulk copy.
+    uint32_t k = 0, s = 0, lap = 0;
+    bool stop = false, dyn = a.static_tiles == 0;
+    uint64_t t0 = blockIdx.x;
+    uint32_t cnext = 0;      // lane 0: the claim for the batch after this one, taken ahead
+    bool cnext_valid = false;
+    // The tiles of the next batch (lane i: one tile), one batch ahead of their issue, so
+    // that the claim's and the records' memory round trips overlap the current batch.
+    auto next_batch = [&](uint64_t &t, bool &have) {
+      have = false;
+      if (!dyn) {
+        t = t0 + (uint64_t)lane * gridDim.x;
+        have = t < a.static_tiles;
+        t0 += 32ull * gridDim.x;
+        if (!__any_sync(FULLW, have)) dyn = true;
+      }
+      if (dyn) {
+        uint32_t c = 0;
+        if (lane == 0) {
+          c = cnext_valid ? cnext : atomicAdd(&a.st->tail_claim, kClaim);
+          cnext = atomicAdd(&a.st->tail_claim, kClaim);  // (its value is used next time)
+          cnext_valid = true;
+        }
+        c = __shfl_sync(FULLW, c, 0);
+        t = a.static_tiles + c + lane;
+        have = lane < kClaim && t < total;
+      }
+    };
+    auto load_record = [&](uint64_t t, bool have, uint4 w[9]) {
       if (have) {
         const uint32_t e = (uint32_t)(t / a.ntiles);
         const uint4 *rec = reinterpret_cast<const uint4 *>(a.btiles + (t - (uint64_t)e * a.ntiles));
-        uint4 w[9];  // the 144-byte record, loaded at once
 #pragma unroll
         for (uint32_t q = 0; q < 9; ++q) w[q] = ld_nc_v4(rec + q);
-        const uint64_t start = ((uint64_t)w[0].y << 32) | w[0].x;
-        TileRec &tr = table[half][lane];
-        tr.nbytes = w[0].z;
-        tr.nsrc = w[0].w & 0xFFFFu;
-        tr.ndst = w[0].w >> 16;
+      }
+    };
+    uint64_t tA = 0, tB = 0;
+    bool haveA = false, haveB = false;
+    uint4 wA[9], wB[9];  // the 144-byte records
+    next_batch(tA, haveA);
+    load_record(tA, haveA, wA);
+    while (!stop) {
+      const uint32_t batch = __popc(__ballot_sync(FULLW, haveA));
+      if (batch == 0) break;
+      if (haveA) {
+        const uint32_t e = (uint32_t)(tA / a.ntiles);
+        const uint64_t start = ((uint64_t)wA[0].y << 32) | wA[0].x;
+        TileRec &tr = table[(k + lane) % kTable];
+        tr.nbytes = wA[0].z;
+        tr.nsrc = wA[0].w & 0xFFFFu;
+        tr.ndst = wA[0].w >> 16;
         const int64_t ioff = (int64_t)(e % (uint32_t)a.in_pool) * a.in_stride + (int64_t)start;
         const int64_t ooff = (int64_t)e * a.out_stride + (int64_t)start;
         constexpr uint64_t kOffMask = (1ull << 56) - 1u;
+        // references 0..7 are sources, 8..15 destinations; word q + 1 holds 2q and 2q + 1
 #pragma unroll
         for (uint32_t q = 0; q < 8; ++q) {
-          const uint64_t rs = ((uint64_t)w[q + 1].y << 32) | w[q + 1].x;   // ref 2q
-          const uint64_t rd = ((uint64_t)w[q + 1].w << 32) | w[q + 1].z;   // ref 2q + 1
-          // refs 0..7 are sources, 8..15 destinations
-          const uint64_t r0 = rs, r1 = rd;
-          const uint32_t i0 = 2 * q, i1 = 2 * q + 1;
-          if (i0 < COLL_BULK_MAX_SRC) {
-            tr.src[i0] = i0 < tr.nsrc ? a.ptr.in[(uint32_t)(r0 >> 56)] + (r0 & kOffMask) + ioff : nullptr;
-          } else {
-            const uint32_t d = i0 - COLL_BULK_MAX_SRC;
-            tr.dst[d] = d < tr.ndst ? a.ptr.out[(uint32_t)(r0 >> 56)] + (r0 & kOffMask) + ooff : nullptr;
-          }
-          if (i1 < COLL_BULK_MAX_SRC) {
-            tr.src[i1] = i1 < tr.nsrc ? a.ptr.in[(uint32_t)(r1 >> 56)] + (r1 & kOffMask) + ioff : nullptr;
-          } else {
-            const uint32_t d = i1 - COLL_BULK_MAX_SRC;
-            tr.dst[d] = d < tr.ndst ? a.ptr.out[(uint32_t)(r1 >> 56)] + (r1 & kOffMask) + ooff : nullptr;
+          const uint64_t ra = ((uint64_t)wA[q + 1].y << 32) | wA[q + 1].x;
+          const uint64_t rb = ((uint64_t)wA[q + 1].w << 32) | wA[q + 1].z;
+#pragma unroll
+          for (uint32_t h2 = 0; h2 < 2; ++h2) {
+            const uint64_t r = h2 ? rb : ra;
+            const uint32_t i = 2 * q + h2;
+            if (i < COLL_BULK_MAX_SRC) {
+              tr.src[i] = i < tr.nsrc ? a.ptr.in[(uint32_t)(r >> 56)] + (r & kOffMask) + ioff
+                                      : nullptr;
+            } else {
+              const uint32_t d = i - COLL_BULK_MAX_SRC;
+              tr.dst[d] = d < tr.ndst ? a.ptr.out[(uint32_t)(r >> 56)] + (r & kOffMask) + ooff
+                                      : nullptr;
+            }
           }
         }
       }
-      const uint32_t batch = __popc(__ballot_sync(FULLW, have));
-      __syncwarp();  // the table half is written before any lane reads it
+      __syncwarp();  // the batch's table entries are written before any lane reads them
+      next_batch(tB, haveB);
+      load_record(tB, haveB, wB);
       for (uint32_t i = 0; i < batch; ++i, ++k) {
         bool ok = true;
         if (lane == 0) ok = mbar_wait(&empty[s], (lap & 1u) ^ 1u, a.spin_ns, &s_abort);
         ok = __shfl_sync(FULLW, ok, 0);
         if (!ok) {
           if (lane == 0) {
-            bulk_timeout(a.st, (uint32_t)(t0 + (uint64_t)i * gridDim.x));
+            bulk_timeout(a.st, k);
             s_abort = 1;
           }
           stop = true;
           break;
         }
-        const TileRec &tr = table[half][i];
+        const uint32_t ent = k % kTable;
+        const TileRec &tr = table[ent];
         const uint32_t nb = tr.nbytes, ns = tr.nsrc;
         if (lane == 0) {
-          stile[s] = half * 32u + i;
+          stile[s] = ent;
           mbar_expect_tx(&full[s], ns * nb);
           s_issued = k + 1;
         }
@@ -150,20 +192,33 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
           ++lap;
         }
       }
+      tA = tB;
+      haveA = haveB;
+#pragma unroll
+      for (uint32_t q = 0; q < 9; ++q) wA[q] = wB[q];
+    }
+    // The end: tile k does not exist. Once its stage is free, record k and complete the
+    // stage's barrier with a plain arrival (no bytes), so that the consumers waiting for
+    // tile k wake, read the count and stop.
+    if (lane == 0) {
+      bool ok = !stop && !s_abort;
+      if (ok) ok = mbar_wait(&empty[s], (lap & 1u) ^ 1u, a.spin_ns, &s_abort);
+      s_final = k;
+      if (ok) mbar_arrive(&full[s]);
     }
   } else {
     const uint32_t ctid = threadIdx.x - 32;  // consumer thread index
     const uint32_t slot_vec = a.slot_bytes >> 4;
     uint32_t k = 0, s = 0, lap = 0;
-    for (uint64_t t = blockIdx.x; t < total; t += gridDim.x, ++k) {
+    for (;; ++k) {
       const bool ok = __all_sync(FULLW, mbar_wait(&full[s], lap & 1u, a.spin_ns, &s_abort));
+      if (ok && k >= s_final) break;  // the producer's end marker, not a tile
       if (!ok) {
-        if (lane == 0) bulk_timeout(a.st, (uint32_t)t);
+        if (lane == 0) bulk_timeout(a.st, k);
         s_abort = 1;
         break;
       }
-      const uint32_t ent = stile[s];
-      const TileRec &h = table[ent >> 5][ent & 31u];
+      const TileRec &h = table[stile[s]];
       const uint32_t nvec = h.nbytes >> 4, nsrc = h.nsrc, ndst = h.ndst;
       const uint4 *sd = reinterpret_cast<const uint4 *>(data + (size_t)s * stage_bytes);
       for (uint32_t v = ctid; v < nvec; v += 32 * kConsumerWarps) {
@@ -205,6 +260,15 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
     for (uint32_t k = consumed; k < s_issued; ++k)
       mbar_wait(&full[k % S], (k / S) & 1u, 100000000ull, &never);
   }
+  if (threadIdx.x == 0) {
+    // the last CTA to finish zeroes the tail counters for the plan's next run
+    __threadfence();
+    if (atomicAdd(&a.st->tail_done, 1u) == gridDim.x - 1u) {
+      atomicExch(&a.st->tail_claim, 0u);
+      atomicExch(&a.st->tail_done, 0u);
+      __threadfence();
+    }
+  }
 }
 
 }  // namespace
@@ -219,13 +283,18 @@ cudaError_t launch_bulk(int op, int dtype, const ZcArgs &a, int ctas, cudaStream
   if (total == 0) return cudaSuccess;
   const int grid = (int)((uint64_t)ctas < total ? (uint64_t)ctas : total);
   const uint32_t smem = bulk_smem_bytes(a.stages, a.maxsrc, a.slot_bytes);
+  // whole rounds of four fifths of the tiles are dealt round-robin and the rest claimed, or
+  // (many-to-one sums) every tile dealt round-robin
+  ZcArgs la = a;
+  la.static_tiles = a.dyn_tail ? total * 4 / 5 / (uint64_t)grid * (uint64_t)grid : total;
+  if (total - la.static_tiles >= (1ull << 31)) la.static_tiles = total;  // (claim counter)
   const void *fn;
   if (op == COLL_OP_COPY) fn = (const void *)bulk_kernel<0, false>;
   else if (dtype == COLL_BF16) fn = a.tree ? (const void *)bulk_kernel<1, true> : (const void *)bulk_kernel<1, false>;
   else fn = a.tree ? (const void *)bulk_kernel<2, true> : (const void *)bulk_kernel<2, false>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  void *args[] = {(void *)&a};
+  void *args[] = {(void *)&la};
   return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, smem, s);
 }
 

@@ -91,6 +91,8 @@ struct coll_dev_status_t {
   uint32_t pad;
   unsigned long long spec_checks;
   unsigned long long spec_retries;
+  uint32_t tail_claim;  // zero-copy bulk ring: tiles of the dynamic tail claimed so far
+  uint32_t tail_done;   // ... and CTAs finished (the last one resets both to zero)
 };
 
 // Host-side compiled plan (no device pointers); built by coll_compile().
@@ -114,6 +116,7 @@ struct coll_compiled {
   uint32_t bulk_slot = 0;     // bytes of one staged piece (= tile size)
   uint32_t bulk_maxsrc = 0;   // slots per stage
   uint32_t bulk_stages = 0;   // stages in the shared-memory ring
+  bool bulk_tail = false;     // claim the last tiles dynamically (see bulk.cu)
   uint64_t xpar_bytes = 0;  // exchange bytes per parity
   uint64_t rpar_bytes = 0;  // two-shot pull: reduced-piece bytes per parity
   uint32_t n_pflag = 0, n_cflag = 0, n_dflag = 0;

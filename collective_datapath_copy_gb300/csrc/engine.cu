@@ -863,6 +863,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
   const bool chained = !fast && a.chain && a.rank_done;
   const bool stagger = !fast && (a.inject_flags & COLL_INJECT_STAGGER);
   uint32_t n_checks = 0, n_retries = 0;
+  uint32_t win = a.spec_delay_ns;  // the speculation window of this warp (ns)
   bool failed = false;
   uint64_t gpiece = 0;  // fused producer: pieces computed so far
 
@@ -1110,8 +1111,8 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
         const bool side = pipelined && tagged && !nh_ready;
         // The speculation window: loads issued right after this warp's own notify mostly
         // race the peers' stores of the same epoch and fail validation; a short wait first
-        // (the plan's spec_delay_ns) trades a little latency for fewer reloads.
-        if (a.spec_delay_ns) spin_ns(a.spec_delay_ns);
+        // trades a little latency for fewer reloads.
+        if (win) spin_ns(win);
         res = spec_attempt<KIND>(xb, u.nbytes, n, lane, active, tagged, pf, !relaxed,
                                  !pause_consumer, f, myh, side, nx,
                                  pipelined ? (su.nbytes >> 4) : 0u, nh);
@@ -1132,6 +1133,11 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
           ok = tags_match(f, myh, n, E, lane);
         }
         ++n_checks;
+        // adaptive window: 4 ns shorter after a passed first attempt, 40 ns longer after one
+        // that failed and passed at the first reload (a race with the peers' stores, which a
+        // wider window avoids; a producer that is late shows as several reloads instead, and
+        // a window does not help there), so that about one first attempt in eleven fails
+        if (a.spec_adapt && ok) win = win > 4u ? win - 4u : 0u;
         if (ok) {
           have = true;
         } else {
@@ -1148,6 +1154,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
               fe = flag_epoch(f);
               if (tags_match(f, myh, n, E, lane)) {
                 have = true;
+                if (a.spec_adapt && k == 0) win = win < 1960u ? win + 40u : 2000u;
                 break;
               }
               const bool late = (globaltimer() - t0 > a.spin_ns) ||

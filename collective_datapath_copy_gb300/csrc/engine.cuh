@@ -31,6 +31,9 @@ struct ZcArgs {
   uint32_t stages;        // bulk kernel: ring depth
   uint32_t maxsrc;        // bulk kernel: slots per stage
   uint32_t tree;          // 1: pairwise (tree) summation order within groups of 8
+  uint64_t static_tiles;  // bulk kernel: tiles dealt round-robin; the rest are claimed
+  uint32_t dyn_tail;      // bulk kernel: 1 = claim the last fifth of the tiles dynamically
+  uint32_t pad2;
 };
 
 struct EngArgs {
@@ -79,6 +82,7 @@ struct EngArgs {
   int32_t R;
   uint32_t single_items;  // 1: every warp has one stage item and one consume item
   uint32_t spec_delay_ns; // speculative protocol: wait before the first speculative loads
+  uint32_t spec_adapt;    // 1: each warp adapts that wait to its own failed first attempts
 };
 
 // Fused producer: one 2-D tensor map per rank over W_r ([k rows][in_len[r] bf16 columns],

@@ -159,9 +159,13 @@ typedef struct {
   int32_t spec_delay_ns;    /* COLL_PROTO_SPEC: ns a consumer waits after its own notify
                                before its first speculative loads (loads issued at once
                                mostly race the peers' stores of the same epoch and are
-                               retried): -1 = the check's default (200 for
-                               COLL_SPEC_TAGGED_RELAXED, 0 otherwise), 0..100000 = that
-                               many ns                                                   */
+                               retried): -1 = the check's default: for
+                               COLL_SPEC_TAGGED_RELAXED a window per warp that starts at
+                               200 ns, grows by 40 ns after a first attempt that failed
+                               and passed at the first reload (a race) and shrinks by 4 ns
+                               after one that passed (about one in eleven then fails), no
+                               window for the other checks; 0..100000 = that many ns,
+                               fixed                                                     */
   int32_t reduce_order;     /* COLL_ORDER_*; zero-copy plans only                      */
   int32_t reserved3;        /* must be 0                                                */
 } coll_config_t;

@@ -211,51 +211,69 @@ def test_the_model_catches_a_missing_wait(mutant):
 # ------------------------------------------------------------ zero-copy bulk ring
 
 class BulkRing:
-    """The zero-copy bulk ring of one CTA: a producer warp resolves tiles 32 at a time into
-    one half of a two-batch table, then issues each tile into stage k % S once the consumer
-    warps released that stage's previous tile; the consumers take the tiles in order, read
-    the tile's table entry through the stage and release the stage."""
+    """The zero-copy bulk ring of one CTA: the producer warp resolves tiles in batches (first
+    32 dealt round-robin at a time, then the tail claimed two at a time) into a table of
+    `entries` slots, the tile it issues k-th into entry k % entries, then issues each tile
+    into stage k % S once the consumer warps released that stage's previous tile; the
+    consumers take the tiles in order, read the tile's entry through the stage, release the
+    stage, and stop at the producer's end marker (a plain arrival on the next stage)."""
 
-    def __init__(self, S, ntiles, consumers, seed, mutant=None):
+    def __init__(self, S, nstatic, ntail, consumers, seed, entries=64):
         self.rnd = random.Random(seed)
-        self.S, self.ntiles, self.C, self.mutant = S, ntiles, consumers, mutant
+        self.S, self.C, self.entries = S, consumers, entries
+        self.batches = [min(32, nstatic - i) for i in range(0, nstatic, 32)]
+        self.batches += [min(2, ntail - i) for i in range(0, ntail, 2)]
+        self.ntiles = nstatic + ntail
         self.full = [MBar(1) for _ in range(S)]
         self.empty = [MBar(consumers) for _ in range(S)]
-        self.table = [[None] * 32 for _ in range(2)]
+        self.table = [None] * entries
         self.stile = [None] * S
-        self.readers = {}       # (half, i) -> consumers still to read that entry's tile
+        self.readers = {}       # entry -> consumers still to read its tile
+        self.final = None
         self.copies = []
         self.got = [[] for _ in range(consumers)]
 
     def producer(self):
-        k = 0
-        for m, t0 in enumerate(range(0, self.ntiles, 32)):
-            half = m % 2 if self.mutant != "one table half" else 0
-            batch = min(32, self.ntiles - t0)
+        k = s = lap = 0
+        for batch in self.batches:
             for i in range(batch):
-                assert not self.readers.get((half, i)), ("table entry rewritten while read", t0 + i)
-                self.table[half][i] = t0 + i
+                e = (k + i) % self.entries
+                assert not self.readers.get(e), ("table entry rewritten while read", k + i)
+                self.table[e] = k + i
             yield
             for i in range(batch):
-                s, lap = k % self.S, k // self.S
                 while not self.empty[s].done((lap & 1) ^ 1):
                     yield
-                self.stile[s] = (half, i)
-                self.readers[(half, i)] = set(range(self.C))
+                e = k % self.entries
+                self.stile[s] = e
+                self.readers[e] = set(range(self.C))
                 self.full[s].expect_tx(4096)
                 self.copies.append(s)
                 k += 1
+                s += 1
+                if s == self.S:
+                    s, lap = 0, lap + 1
                 yield
+        while not self.empty[s].done((lap & 1) ^ 1):
+            yield
+        self.final = k
+        self.full[s].arrive()   # the end marker
 
     def consumer(self, c):
-        for k in range(self.ntiles):
-            s, lap = k % self.S, k // self.S
+        k = s = lap = 0
+        while True:
             while not self.full[s].done(lap & 1):
                 yield
-            half, i = self.stile[s]
-            self.got[c].append(self.table[half][i])
-            self.readers[(half, i)].discard(c)
+            if self.final is not None and k >= self.final:
+                return
+            e = self.stile[s]
+            self.got[c].append(self.table[e])
+            self.readers[e].discard(c)
             self.empty[s].arrive()
+            k += 1
+            s += 1
+            if s == self.S:
+                s, lap = 0, lap + 1
             yield
 
     def land_one(self):
@@ -263,13 +281,13 @@ class BulkRing:
         self.full[s].complete_tx(4096)
 
 
-def simulate_bulk(S, ntiles, consumers, seed, mutant=None):
-    m = BulkRing(S, ntiles, consumers, seed, mutant)
+def simulate_bulk(S, nstatic, ntail, consumers, seed, entries=64):
+    m = BulkRing(S, nstatic, ntail, consumers, seed, entries)
     live = [m.producer()] + [m.consumer(c) for c in range(consumers)]
     steps = 0
     while live:
         steps += 1
-        assert steps < 200000, "no progress"
+        assert steps < 400000, "no progress"
         if m.copies and m.rnd.random() < 0.3:
             m.land_one()
             continue
@@ -279,21 +297,22 @@ def simulate_bulk(S, ntiles, consumers, seed, mutant=None):
         except StopIteration:
             live.remove(g)
     for c in range(consumers):
-        assert m.got[c] == list(range(ntiles)), c
+        assert m.got[c] == list(range(m.ntiles)), c
 
 
 @pytest.mark.parametrize("seed", range(40))
-def test_bulk_ring_table_halves(seed):
+def test_bulk_ring_table_and_end_marker(seed):
     rnd = random.Random(2000 + seed)
-    simulate_bulk(rnd.choice([2, 3, 6, 8]), rnd.choice([1, 31, 32, 33, 64, 100, 150]),
-                  rnd.choice([1, 8]), seed)
+    simulate_bulk(rnd.choice([2, 3, 6, 8]), rnd.choice([0, 1, 31, 32, 33, 64, 100]),
+                  rnd.choice([0, 1, 2, 7, 40]), rnd.choice([1, 8]), seed)
 
 
-def test_the_bulk_model_catches_a_single_table_half():
+def test_the_bulk_model_catches_a_table_too_small():
+    # a table of 32 entries would be overwritten while the ring still holds its tiles
     caught = 0
     for seed in range(40):
         try:
-            simulate_bulk(6, 100, 8, seed, mutant="one table half")
+            simulate_bulk(8, 100, 10, 8, seed, entries=32)
         except AssertionError:
             caught += 1
     assert caught > 0
