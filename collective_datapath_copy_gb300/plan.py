@@ -158,7 +158,7 @@ class Plan:
                  out_epoch_stride=0, stream=None):
         """Fused producer: each rank's payload is W_r x_r computed inside the engine.
         wts[r]: [k, in_len[r]] bf16 (W_r transposed); xs[r]: x vectors (k bf16 per epoch);
-        k a multiple of 128 (coll_run_gemv has the full contract)."""
+        k a multiple of 16, at most 8192 (coll_run_gemv has the full contract)."""
         R = self.naming.R
         self._check(xs, outs, n_epochs, x_epoch_stride, x_pool, out_epoch_stride,
                     in_bytes=[2 * int(k)] * R)
