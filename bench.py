@@ -534,7 +534,7 @@ def run_ours(args, rank, world, dist):
         "config": {"workload": "TP decode all-reduce: R=8 emulated ranks x 4096 bf16 per rank, "
                                "10000 epochs per step in one persistent launch, speculative "
                                "protocol (dual buffers, fence-free content-tagged validation, "
-                               "200 ns speculation delay), oneshot",
+                               "adaptive speculation window from 200 ns), oneshot",
                    "ranks": R_DECODE, "elems_per_rank": N_DECODE, "epochs_per_step": EPOCHS,
                    "input_pool": POOL, "protocol": "spec", "l2": "flushed before every timed "
                    "step (256 MiB written, then another 256 MiB read)",
