@@ -483,9 +483,8 @@ def run_ours(args, rank, world, dist):
 
     # the smallest configuration: all-reduce of 2 x 1024 fp32, barrier protocol, one epoch per
     # launch; median of 1000 launches, each timed with CUDA events
-    g1 = torch.Generator(device=dev)
-    g1.manual_seed(1)
-    s_in = [(torch.rand(1024, device=dev, generator=g1) * 2 - 1) for _ in range(2)]
+    s_rng = synth.seeded_rng(1)
+    s_in = [torch.from_numpy(synth.uniform_f32(s_rng, 1024)).to(dev) for _ in range(2)]
     s_out = [torch.empty(1024, device=dev) for _ in range(2)]
     s_plan = cdc.Plan(cdc.allreduce(2, 1024, "f32"), protocol="barrier")
     for _ in range(20):
@@ -744,7 +743,6 @@ def run_workload(args):
     flush = make_flush(torch, dev)
     peak, peak_kind = peaks()
     R = 8
-    g = torch.Generator(device=dev)
     res = {"workload": args.workload, "peak_gbs": peak, "peak_kind": peak_kind}
     # context for the single-launch times: a one-element kernel timed the same way (L2
     # flush, then CUDA events around one launch)
@@ -819,9 +817,8 @@ def run_workload(args):
         for Rr in (2, 4, 8):
             for kb in (8, 16, 32):
                 n = kb * 1024 // 2
-                g.manual_seed(15)
-                ins = [torch.randn(7, n, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
-                       for _ in range(Rr)]
+                ins = [synth.device_normal_bf16(torch, 1500 + 10 * Rr + r, (7, n), dev)
+                       for r in range(Rr)]
                 outs = [torch.empty(E, n, dtype=torch.int16, device=dev) for _ in range(Rr)]
                 nm = cdc.allreduce(Rr, n, "bf16")
                 for proto in ("barrier", "dual", "spec", "ll"):
@@ -848,32 +845,36 @@ def run_workload(args):
         # (8 ranks, 4096 outputs, k = 512 per rank) computed in the stage step, then
         # all-reduced; compared with the all-reduce alone on the same payload size
         Rr, n, k, E, pool = 8, 4096, 512, 2000, 7
-        g.manual_seed(9)
-        wts = [torch.randn(k, n, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
-               for _ in range(Rr)]
-        xs = [torch.randn(pool, k, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
-              for _ in range(Rr)]
-        ys = [torch.randn(pool, n, device=dev, generator=g).to(torch.bfloat16).view(torch.int16)
-              for _ in range(Rr)]
+        wts = [synth.device_normal_bf16(torch, 900 + r, (k, n), dev) for r in range(Rr)]
+        xs = [synth.device_normal_bf16(torch, 910 + r, (pool, k), dev) for r in range(Rr)]
+        ys = [synth.device_normal_bf16(torch, 920 + r, (pool, n), dev) for r in range(Rr)]
         outs = [torch.empty(E, n, dtype=torch.int16, device=dev) for _ in range(Rr)]
         nm = cdc.allreduce(Rr, n, "bf16")
+        # units: the default 512 bytes (16 pieces per rank, 128 CTAs), and the smallest that
+        # spreads the pieces over every SM (8 ranks x 19 units of 432 bytes on 152 SMs)
+        nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+        per_rank = max(1, nsm // Rr)
+        fill = -(-(2 * n) // per_rank)
+        fill = max(64, -(-fill // 16) * 16)
+        units = [512] + ([fill] if fill < 512 else [])
         rows = []
-        for proto in args.protocols.split(","):
-            for chain in (0, 1):
-                pl = cdc.Plan(nm, protocol=proto, chain=chain)
-                tf = _time_steps(torch, lambda: pl.run_gemv(wts, xs, k, outs, n_epochs=E,
-                                                            x_epoch_stride=2 * k, x_pool=pool,
-                                                            out_epoch_stride=2 * n),
-                                 args.steps, args.warmup, flush, stream)
-                ta = _time_steps(torch, lambda: pl.run(ys, outs, n_epochs=E, in_epoch_stride=2 * n,
-                                                       in_pool=pool, out_epoch_stride=2 * n),
-                                 args.steps, args.warmup, flush, stream)
-                if pl.status()["code"] != 0:
-                    raise RuntimeError(f"fused {proto}: {pl.status()}")
-                med = lambda t: round(sorted(t)[len(t) // 2] * 1000 / E, 4)
-                rows.append({"protocol": proto, "chain": chain, "fused_us_per_epoch": med(tf),
-                             "allreduce_only_us_per_epoch": med(ta)})
-                pl.free()
+        for proto, unit, chain in [(p_, u_, c_) for p_ in args.protocols.split(",")
+                                   for u_ in units for c_ in (0, 1)]:
+            pl = cdc.Plan(nm, protocol=proto, chain=chain, unit_bytes=unit)
+            tf = _time_steps(torch, lambda: pl.run_gemv(wts, xs, k, outs, n_epochs=E,
+                                                        x_epoch_stride=2 * k, x_pool=pool,
+                                                        out_epoch_stride=2 * n),
+                             args.steps, args.warmup, flush, stream)
+            ta = _time_steps(torch, lambda: pl.run(ys, outs, n_epochs=E, in_epoch_stride=2 * n,
+                                                   in_pool=pool, out_epoch_stride=2 * n),
+                             args.steps, args.warmup, flush, stream)
+            if pl.status()["code"] != 0:
+                raise RuntimeError(f"fused {proto}: {pl.status()}")
+            med = lambda t: round(sorted(t)[len(t) // 2] * 1000 / E, 4)
+            rows.append({"protocol": proto, "chain": chain, "unit_bytes": unit,
+                         "ctas": int(pl.info.n_warps), "fused_us_per_epoch": med(tf),
+                         "allreduce_only_us_per_epoch": med(ta)})
+            pl.free()
         res["rows"] = rows
         res["gemv"] = {"ranks": Rr, "outputs": n, "k_per_rank": k,
                        "weight_bytes_per_epoch": Rr * n * k * 2}

@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <memory>
 #include <new>
 #include <vector>
@@ -127,8 +128,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // Tensor maps of the fused run's weight matrices W_r ([k rows][in_len[r] bf16], rows
-// in_bytes[r] apart), boxes of 256 columns x 64 rows; reused while the run's matrices and
-// k stay the same.
+// in_bytes[r] apart), boxes of one unit's columns (at most 256) x 64 rows; reused while the
+// run's matrices and k stay the same.
+// Bytes per staged weight row of the fused producer: the plan's unit.
+uint32_t gemv_pitch(const coll_compiled &c) {
+  return c.cfg.unit_bytes ? (uint32_t)c.cfg.unit_bytes : 512u;
+}
+
 int gemv_maps(coll_plan_s *p, const void *const *wt, uint32_t k) {
   const coll_compiled &c = p->c;
   std::vector<const void *> key(wt, wt + c.R);
@@ -145,7 +151,7 @@ int gemv_maps(coll_plan_s *p, const void *const *wt, uint32_t k) {
     if (!c.in_used[r]) continue;
     const cuuint64_t dims[2] = {(cuuint64_t)(c.in_bytes[r] / 2), (cuuint64_t)k};
     const cuuint64_t strides[1] = {(cuuint64_t)c.in_bytes[r]};
-    const cuuint32_t box[2] = {256, 64};
+    const cuuint32_t box[2] = {gemv_pitch(c) / 2u, 64};
     const cuuint32_t estr[2] = {1, 1};
     if (dims[0] > 0xFFFFFFFFull || strides[0] >= (1ull << 40)) return COLL_EINVAL;
     if (encode(&p->gmaps->m[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(wt[r]),
@@ -461,6 +467,8 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
         a.wt_stride[r] = (int64_t)c.in_bytes[r];
       }
       a.gemv_k = k;
+      a.gemv_pitch = gemv_pitch(c);
+      a.gemv_slots = coll::gemv_ring_slots(a.gemv_pitch);
     }
     err = coll::launch_engine(c.op, c.dtype, a, wt ? p->gmaps.get() : nullptr, s);
     if (err == cudaSuccess && !restart) p->epochs_issued += (uint64_t)n_epochs;

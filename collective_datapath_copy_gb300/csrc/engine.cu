@@ -336,18 +336,19 @@ __device__ __forceinline__ uint4 gather_pieces(const char *xb, uint32_t nbytes, 
 // in the order it is written. A CTA runs eight warps:
 //   warp 0      the engine warp (the staged protocol, unchanged);
 //   warp 1      the weight streamer: lane 0 fills a ring of shared-memory slots, each one
-//               tensor copy (TMA) of 64 rows x 256 columns of W_r, for the pieces of the
-//               whole run in order (the weights do not depend on the epoch's data, so it
-//               runs ahead by as many slots as the ring holds, across exchanges);
+//               tensor copy (TMA) of 64 rows x the unit's columns (at most 256) of W_r, for
+//               the pieces of the whole run in order (the weights do not depend on the
+//               epoch's data, so it runs ahead by as many slots as the ring holds, across
+//               exchanges);
 //   warp 2      the x streamer: lane 0 copies piece q's x (k bf16, one bulk copy) into one
 //               of two buffers, once the engine has opened piece q (that also frees the
 //               buffer: piece q is opened only after piece q - 2 was taken, whose x was read
 //               before its results were written);
 //   warp 3      idle;
 //   warps 4..7  compute warps: lane l of compute warp w owns columns 64w + 2l and
-//               64w + 2l + 1 of the piece and carries their two chains over all k rows
-//               (packed binary32 pairs), so no order is split; it writes the rounded
-//               results into one of two result slots.
+//               64w + 2l + 1 of the piece (lanes past the unit's columns idle) and carries
+//               their two chains over all k rows (packed binary32 pairs), so no order is
+//               split; it writes the rounded results into one of two result slots.
 // The engine takes piece q's results from its slot and opens piece q + 2 (at most one
 // piece computed ahead; the result slot of piece q + 2 is the one just taken): without chained epochs the next piece is computed while the
 // engine runs the current exchange. With chained epochs an epoch's pieces are opened only
@@ -358,18 +359,18 @@ constexpr uint32_t kGemvComputeWarps = 4;
 constexpr uint32_t kGemvFirst = 4;                        // warp of compute warp 0
 constexpr uint32_t kGemvThreads = 32 * (kGemvFirst + kGemvComputeWarps);  // 256
 constexpr uint32_t kGemvRows = 64;                        // weight rows per slot (one copy)
-constexpr uint32_t kGemvCols = 256;                       // bf16 columns of a piece
-constexpr uint32_t kGemvPitch = 2 * kGemvCols;            // bytes per staged row
-constexpr uint32_t kGemvSlotBytes = kGemvRows * kGemvPitch;  // 32 KiB
-constexpr uint32_t kGemvSlots = 5;                        // 160 KiB of rows in flight
+constexpr uint32_t kGemvMaxPitch = 512;                   // bytes per staged row, at most
+constexpr uint32_t kGemvRingBytes = 168u << 10;           // the ring: 5 slots of 512-byte
+                                                          // rows, 6 of 432, at most 8
+constexpr uint32_t kGemvMaxSlots = 8;
 constexpr uint32_t kGemvMaxK = 8192;                      // rows of W_r (length of x)
 constexpr uint32_t kGemvXBytes = 2 * kGemvMaxK;
 constexpr uint32_t kGemvMaxItems = 16;                    // stage items whose rows are cached
 // dynamic shared memory: ring, two x buffers, two result slots, barriers (+128 for the
 // alignment of the ring, where the tensor copies land)
-constexpr uint32_t kGemvBars = 2 * kGemvSlots + 4;
+constexpr uint32_t kGemvBars = 2 * kGemvMaxSlots + 4;
 constexpr uint32_t kGemvSmemBytes =
-    kGemvSlots * kGemvSlotBytes + 2 * kGemvXBytes + 2 * kGemvPitch + kGemvBars * 8 + 128;
+    kGemvRingBytes + 2 * kGemvXBytes + 2 * kGemvMaxPitch + kGemvBars * 8 + 128;
 
 struct GemvShared {
   uint64_t go;          // pieces the compute may start (written by warp 0, release.cta)
@@ -392,11 +393,11 @@ __device__ __forceinline__ GemvShared &gemv_smem() {
 }
 
 struct GemvBufs {
-  unsigned char *ring;  // [kGemvSlots][kGemvRows][kGemvPitch]
+  unsigned char *ring;  // [gemv_slots][kGemvRows][gemv_pitch]
   unsigned char *x;     // [2][kGemvXBytes]
-  unsigned char *res;   // [2][kGemvPitch]
-  uint64_t *full;       // [kGemvSlots] a fill's rows have landed
-  uint64_t *empty;      // [kGemvSlots] every compute warp has read the slot
+  unsigned char *res;   // [2][kGemvMaxPitch]
+  uint64_t *full;       // [kGemvMaxSlots] a fill's rows have landed
+  uint64_t *empty;      // [kGemvMaxSlots] every compute warp has read the slot
   uint64_t *xfull;      // [2] piece's x has landed
   uint64_t *rfull;      // [2] every compute warp has written its results
 };
@@ -405,11 +406,11 @@ __device__ __forceinline__ GemvBufs gemv_bufs() {
   extern __shared__ __align__(128) unsigned char gemv_dyn[];
   GemvBufs b;
   b.ring = gemv_dyn + ((128u - (smem_u32(gemv_dyn) & 127u)) & 127u);
-  b.x = b.ring + kGemvSlots * kGemvSlotBytes;
+  b.x = b.ring + kGemvRingBytes;
   b.res = b.x + 2 * kGemvXBytes;
-  b.full = reinterpret_cast<uint64_t *>(b.res + 2 * kGemvPitch);
-  b.empty = b.full + kGemvSlots;
-  b.xfull = b.empty + kGemvSlots;
+  b.full = reinterpret_cast<uint64_t *>(b.res + 2 * kGemvMaxPitch);
+  b.empty = b.full + kGemvMaxSlots;
+  b.xfull = b.empty + kGemvMaxSlots;
   b.rfull = b.xfull + 2;
   return b;
 }
@@ -497,6 +498,7 @@ __device__ void gemv_weight_streamer(const EngArgs &a, const coll_warp_t &W) {
   GemvShared &g = gemv_smem();
   const GemvBufs b = gemv_bufs();
   const uint64_t fills = g.total * g.kslots;
+  const uint32_t S = a.gemv_slots, slot_bytes = kGemvRows * a.gemv_pitch;
   uint64_t f = 0;
   uint32_t s = 0, lap = 0, j = 0, item = 0;
   GemvSrc src = gemv_item(a, g, W, 0);
@@ -505,10 +507,9 @@ __device__ void gemv_weight_streamer(const EngArgs &a, const coll_warp_t &W) {
     ok = mbar_wait_until(&b.empty[s], (lap & 1u) ^ 1u, gemv_role_limit(a),
                          [&a]() { return gemv_stop(a); });
     if (!ok) break;
-    mbar_expect_tx(&b.full[s], kGemvSlotBytes);
-    tensor_load_2d(b.ring + (size_t)s * kGemvSlotBytes, src.map, src.col, j * kGemvRows,
-                   &b.full[s]);
-    if (++s == kGemvSlots) {
+    mbar_expect_tx(&b.full[s], slot_bytes);
+    tensor_load_2d(b.ring + (size_t)s * slot_bytes, src.map, src.col, j * kGemvRows, &b.full[s]);
+    if (++s == S) {
       s = 0;
       ++lap;
     }
@@ -522,9 +523,9 @@ __device__ void gemv_weight_streamer(const EngArgs &a, const coll_warp_t &W) {
   // every fill issued has landed before the CTA may exit (bounded): the last fill of each
   // slot is the latest phase of its barrier
   const uint64_t issued = f;
-  for (uint32_t t = 0; t < kGemvSlots && (uint64_t)t < issued; ++t) {
-    const uint64_t last = issued - 1u - ((issued - 1u - t) % kGemvSlots);
-    mbar_wait_until(&b.full[t], (uint32_t)((last / kGemvSlots) & 1u), 100000000ull,
+  for (uint32_t t = 0; t < S && (uint64_t)t < issued; ++t) {
+    const uint64_t last = issued - 1u - ((issued - 1u - t) % S);
+    mbar_wait_until(&b.full[t], (uint32_t)((last / S) & 1u), 100000000ull,
                     []() { return false; });
   }
 }
@@ -587,15 +588,20 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 }
 
 // The products of sixteen rows for this lane's two columns: prod[r] = w[row][c..c+1] * x[row]
-// (each rounded to binary32), independent of the running sums.
+// (each rounded to binary32), independent of the running sums. PITCH: bytes per staged row
+// when known at compile time (the rows' offsets are then immediates of the loads), else 0
+// and `pitch` gives it.
+template <uint32_t PITCH>
 __device__ __forceinline__ void gemv_prods16(uint64_t prod[16], const unsigned char *slot,
-                                             uint32_t colb, const unsigned char *xrow) {
+                                             uint32_t pitch, uint32_t colb,
+                                             const unsigned char *xrow) {
+  if constexpr (PITCH != 0) pitch = PITCH;
   const uint4 xa = *reinterpret_cast<const uint4 *>(xrow);
   const uint4 xb = *reinterpret_cast<const uint4 *>(xrow + 16);
   const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
   for (uint32_t r = 0; r < 16; ++r) {
-    const uint32_t w = *reinterpret_cast<const uint32_t *>(slot + r * kGemvPitch + colb);
+    const uint32_t w = *reinterpret_cast<const uint32_t *>(slot + r * pitch + colb);
     const float xf = __uint_as_float((r & 1u) ? (xw[r >> 1] & 0xFFFF0000u) : (xw[r >> 1] << 16));
     prod[r] = f2_mul(f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)),
                      f2_pack(xf, xf));
@@ -613,30 +619,33 @@ __device__ __forceinline__ void gemv_adds16(uint64_t &acc, const uint64_t prod[1
 // BLOCKS blocks of sixteen rows of a slot, in order: the products of block c + 1 are formed
 // while block c's sums run (they do not depend on them), so the in-order chain of adds has
 // independent work to overlap; the order of the adds is unchanged.
-template <bool FIRST, uint32_t BLOCKS>
+template <bool FIRST, uint32_t BLOCKS, uint32_t PITCH>
 __device__ __forceinline__ void gemv_slot_rows(uint64_t &acc, const unsigned char *slot,
-                                               uint32_t colb, const unsigned char *xs) {
+                                               uint32_t pitch, uint32_t colb,
+                                               const unsigned char *xs) {
+  if constexpr (PITCH != 0) pitch = PITCH;
   uint64_t prod[2][16];
-  gemv_prods16(prod[0], slot, colb, xs);
+  gemv_prods16<PITCH>(prod[0], slot, pitch, colb, xs);
 #pragma unroll
   for (uint32_t c = 0; c < BLOCKS; ++c) {
     if (c + 1 < BLOCKS)
-      gemv_prods16(prod[(c + 1) & 1], slot + (c + 1) * 16 * kGemvPitch, colb, xs + (c + 1) * 32);
+      gemv_prods16<PITCH>(prod[(c + 1) & 1], slot + (c + 1) * 16 * pitch, pitch, colb,
+                          xs + (c + 1) * 32);
     if (FIRST && c == 0) gemv_adds16<true>(acc, prod[c & 1]);
     else gemv_adds16<false>(acc, prod[c & 1]);
   }
 }
 
 // The rows of one fill: 64, or fewer (a multiple of 16) in a last fill past row k.
-template <bool FIRST>
+template <bool FIRST, uint32_t PITCH>
 __device__ __forceinline__ void gemv_fill_rows(uint64_t &acc, const unsigned char *slot,
-                                               uint32_t colb, const unsigned char *xs,
-                                               uint32_t rows) {
+                                               uint32_t pitch, uint32_t colb,
+                                               const unsigned char *xs, uint32_t rows) {
   switch (rows) {
-    case 16: gemv_slot_rows<FIRST, 1>(acc, slot, colb, xs); break;
-    case 32: gemv_slot_rows<FIRST, 2>(acc, slot, colb, xs); break;
-    case 48: gemv_slot_rows<FIRST, 3>(acc, slot, colb, xs); break;
-    default: gemv_slot_rows<FIRST, 4>(acc, slot, colb, xs); break;
+    case 16: gemv_slot_rows<FIRST, 1, PITCH>(acc, slot, pitch, colb, xs); break;
+    case 32: gemv_slot_rows<FIRST, 2, PITCH>(acc, slot, pitch, colb, xs); break;
+    case 48: gemv_slot_rows<FIRST, 3, PITCH>(acc, slot, pitch, colb, xs); break;
+    default: gemv_slot_rows<FIRST, 4, PITCH>(acc, slot, pitch, colb, xs); break;
   }
 }
 
@@ -644,11 +653,15 @@ __device__ __forceinline__ void gemv_fill_rows(uint64_t &acc, const unsigned cha
 // shared; a __syncwarp after each orders lane 0's acquiring wait before every lane's reads,
 // and one before each of lane 0's arrivals orders every lane's reads (of a slot) or writes
 // (of results) before it.
+template <uint32_t PITCH>
 __device__ void gemv_compute(const EngArgs &a, const coll_warp_t &W, uint32_t cw,
                              uint32_t lane) {
   GemvShared &g = gemv_smem();
   const GemvBufs b = gemv_bufs();
   const uint32_t colb = (64u * cw + 2u * lane) * 2u;  // byte offset of this lane's columns
+  const uint32_t pitch = PITCH ? PITCH : a.gemv_pitch, S = a.gemv_slots;
+  const uint32_t slot_bytes = kGemvRows * pitch;
+  const bool live = PITCH == kGemvMaxPitch || colb < pitch;  // columns inside the unit
   uint32_t s = 0, lap = 0;
   bool ok = true;
   for (uint64_t q = 0; q < g.total && ok; ++q) {
@@ -668,15 +681,17 @@ __device__ void gemv_compute(const EngArgs &a, const coll_warp_t &W, uint32_t cw
       ok = __shfl_sync(FULL, ok, 0);
       __syncwarp();
       if (!ok) break;
-      const unsigned char *slot = b.ring + (size_t)s * kGemvSlotBytes;
+      const unsigned char *slot = b.ring + (size_t)s * slot_bytes;
       const unsigned char *xs = xq + (size_t)j * (kGemvRows * 2);
       // rows of this fill: 64, or fewer (a multiple of 16) in a last fill past row k
       const uint32_t rows = g.k - j * kGemvRows < kGemvRows ? g.k - j * kGemvRows : kGemvRows;
-      if (j == 0) gemv_fill_rows<true>(acc, slot, colb, xs, rows);
-      else gemv_fill_rows<false>(acc, slot, colb, xs, rows);
+      if (live) {
+        if (j == 0) gemv_fill_rows<true, PITCH>(acc, slot, pitch, colb, xs, rows);
+        else gemv_fill_rows<false, PITCH>(acc, slot, pitch, colb, xs, rows);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&b.empty[s]);  // the warp's reads of the slot are done
-      if (++s == kGemvSlots) {
+      if (++s == S) {
         s = 0;
         ++lap;
       }
@@ -687,7 +702,8 @@ __device__ void gemv_compute(const EngArgs &a, const coll_warp_t &W, uint32_t cw
     // x barrier order that before these writes)
     float lo, hi;
     asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(acc));
-    *reinterpret_cast<uint32_t *>(b.res + (size_t)p * kGemvPitch + colb) = pack_bf16x2(lo, hi);
+    if (live)
+      *reinterpret_cast<uint32_t *>(b.res + (size_t)p * kGemvMaxPitch + colb) = pack_bf16x2(lo, hi);
     __syncwarp();
     if (lane == 0) mbar_arrive(&b.rfull[p]);
   }
@@ -708,7 +724,7 @@ __device__ __forceinline__ bool gemv_take(const EngArgs &a, uint64_t q, uint32_t
   ok = __shfl_sync(FULL, ok, 0);
   __syncwarp();
   if (!ok) return false;
-  res = lane < active ? *reinterpret_cast<const uint4 *>(b.res + (size_t)p * kGemvPitch + lane * 16)
+  res = lane < active ? *reinterpret_cast<const uint4 *>(b.res + (size_t)p * kGemvMaxPitch + lane * 16)
                       : make_uint4(0, 0, 0, 0);
   __syncwarp();  // every lane's read of the slot precedes lane 0's release of it
   if (lane == 0) {
@@ -814,7 +830,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
     const uint32_t wid = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
       const GemvBufs bb = gemv_bufs();
-      for (uint32_t s = 0; s < kGemvSlots; ++s) {
+      for (uint32_t s = 0; s < kGemvMaxSlots; ++s) {
         mbar_init(&bb.full[s], 1);  // the streamer's arrival, plus the copy's bytes
         mbar_init(&bb.empty[s], kGemvComputeWarps);
       }
@@ -837,7 +853,10 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
       return;
     }
     if (wid >= kGemvFirst) {
-      gemv_compute(a, a.warps[gw], wid - kGemvFirst, lane);
+      // the two unit sizes in use get the rows' offsets compiled in
+      if (a.gemv_pitch == 512) gemv_compute<512>(a, a.warps[gw], wid - kGemvFirst, lane);
+      else if (a.gemv_pitch == 432) gemv_compute<432>(a, a.warps[gw], wid - kGemvFirst, lane);
+      else gemv_compute<0>(a, a.warps[gw], wid - kGemvFirst, lane);
       return;
     }
     if (wid != 0) return;
@@ -1403,6 +1422,11 @@ cudaError_t engine_max_coresident(int op, int dtype, int protocol, int datapath,
   }
   *max_ctas = per_sm * sms;
   return cudaSuccess;
+}
+
+uint32_t gemv_ring_slots(uint32_t pitch) {
+  const uint32_t n = kGemvRingBytes / (kGemvRows * pitch);
+  return n < kGemvMaxSlots ? n : kGemvMaxSlots;
 }
 
 cudaError_t engine_gemv_max_coresident(bool pull, int *max_ctas) {

@@ -41,6 +41,9 @@ struct EngArgs {
   const char *wt[COLL_MAX_RANKS];      // fused producer: W_r transposed, [k][in_len[r]] bf16
   int64_t wt_stride[COLL_MAX_RANKS];   // bytes per row of wt[r]
   uint32_t gemv_k;                     // 0: stage loads its payload; k: stage computes W_r x_r
+  uint32_t gemv_pitch;                 // fused producer: bytes per staged weight row (the
+                                       // unit's bytes: its columns x 2)
+  uint32_t gemv_slots;                 // fused producer: slots of the weight ring
   const coll_unit_t *units;
   const coll_item_t *sitems;
   const coll_item_t *citems;
@@ -113,6 +116,9 @@ cudaError_t launch_probe_rtt(unsigned long long *flags, uint32_t iters, uint32_t
 
 // How many one-warp engine CTAs can be co-resident on the current device.
 cudaError_t engine_max_coresident(int op, int dtype, int protocol, int datapath, int *max_ctas);
+
+// Slots of the fused producer's weight ring for staged rows of `pitch` bytes.
+uint32_t gemv_ring_slots(uint32_t pitch);
 
 // How many fused-producer engine CTAs (twelve warps, a 192 KiB weight ring) can be co-resident.
 cudaError_t engine_gemv_max_coresident(bool pull, int *max_ctas);

@@ -55,7 +55,8 @@ static int check_config(const coll_config_t &c) {
     return COLL_EINVAL;
   if (c.zero_copy < 0 || c.zero_copy > 1) return COLL_EINVAL;
   if (c.spec_check < 0 || c.spec_check > 2) return COLL_EINVAL;
-  if (c.unit_bytes != 0 && c.unit_bytes != 512) return COLL_EINVAL;
+  if (c.unit_bytes != 0 && (c.unit_bytes < 64 || c.unit_bytes > 512 || (c.unit_bytes & 15)))
+    return COLL_EINVAL;
   if (c.warps_per_rank < 0 || c.ctas < 0) return COLL_EINVAL;
   if (c.tile_bytes < 0 || (c.tile_bytes % 16) != 0) return COLL_EINVAL;
   if (c.inject_prob_ppm > 1000000u) return COLL_EINVAL;
@@ -330,7 +331,7 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
   }
 
   // ---------------- staged: units, items, warps
-  const uint32_t U = 512;
+  const uint32_t U = cfg.unit_bytes ? (uint32_t)cfg.unit_bytes : 512u;
   std::vector<std::vector<coll_item_t>> S(R), C(R), P(R);  // per-rank stage / consume / pull
   std::vector<uint32_t> unit_owner;
   for (auto &nm : names) {

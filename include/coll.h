@@ -130,7 +130,8 @@ typedef struct {
                              coll_run, no exchange buffers or flags (the kernel launch
                              is the barrier). 0: staged Stage/Notify/Consume engine.   */
   int32_t spec_check;     /* COLL_SPEC_*                                              */
-  int32_t unit_bytes;     /* staged: bytes per synchronisation unit: 0 or 512         */
+  int32_t unit_bytes;     /* staged: bytes per synchronisation unit (one warp's piece):
+                             0 (= 512) or a multiple of 16 from 64 to 512               */
   int32_t warps_per_rank; /* staged: warps per emulated rank; 0 = one per unit        */
   int32_t ctas;           /* zero-copy: CTAs (8 warps each) in the grid; 0 = 3 x SMs  */
   int32_t tile_bytes;     /* zero-copy: bytes per warp tile, multiple of 16; 0 = auto
@@ -274,7 +275,9 @@ int coll_run(coll_plan_t p, void *const *in, void *const *out, int n_epochs,
  * in row order i = 0..k-1 from the first product (round to nearest even, no fused
  * multiply-add), then rounded once to bf16. Results are bit-exact. Each engine CTA runs
  * eight warps in this mode (four compute, two streaming the weight rows and x into shared
- * memory by tensor and bulk copies), one CTA per SM; without chained epochs the next piece
+ * memory by tensor and bulk copies), one CTA per SM, and computes one unit of the plan
+ * (coll_config_t.unit_bytes: units of 432 bytes spread an 8 KiB payload of 8 ranks over 152
+ * SMs instead of 128); without chained epochs the next piece
  * is computed while the current one is exchanged. k must be a multiple of 16, at most
  * 8192; in_len[r], wt[r], x[r] and the strides must give 16-byte alignment, and in_len[r]
  * must be below 2^32. The tensor maps of W_r are encoded on the host at the first run with

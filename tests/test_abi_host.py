@@ -112,8 +112,15 @@ def test_bad_config_rejected():
     n = namings.allreduce(2, 256)
     with pytest.raises(cdc.CollError):
         cdc.validate(n, protocol=7)
-    with pytest.raises(cdc.CollError):
-        cdc.validate(n, unit_bytes=100)
+    for bad in (100, 48, 520, 1024, -16):
+        with pytest.raises(cdc.CollError):
+            cdc.validate(n, unit_bytes=bad)
+    # units of 64..512 bytes, multiples of 16: the 8 KiB name in ceil(8192 / u) units, each
+    # staged by all 8 ranks (one warp per rank and unit)
+    nm8 = namings.allreduce(8, 4096, "bf16")
+    for u, units in ((0, 16), (512, 16), (432, 19), (256, 32), (64, 128)):
+        info = cdc.validate(nm8, unit_bytes=u)
+        assert (info.n_units, info.n_warps) == (units, 8 * units)
     with pytest.raises(cdc.CollError):
         cdc.validate(n, datapath=3)
     # the two-shot pull needs the staged exchange and flags

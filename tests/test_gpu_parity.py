@@ -1021,15 +1021,16 @@ def _gemv_case(R, n, k, pool, seed):
     return wts, xs
 
 
-@pytest.mark.parametrize("protocol,datapath,chain", [("barrier", "oneshot", 0), ("dual", "oneshot", 0),
-                                                     ("spec", "oneshot", 0), ("spec", "twoshot", 0),
-                                                     ("spec", "oneshot", 1),
-                                                     ("dual", "twoshot_pull", 1)])
-def test_fused_gemv_allreduce_bit_exact(protocol, datapath, chain):
+@pytest.mark.parametrize("protocol,datapath,chain,unit", [
+    ("barrier", "oneshot", 0, 0), ("dual", "oneshot", 0, 0), ("spec", "oneshot", 0, 0),
+    ("spec", "twoshot", 0, 0), ("spec", "oneshot", 1, 0), ("dual", "twoshot_pull", 1, 0),
+    ("dual", "oneshot", 0, 432), ("spec", "oneshot", 1, 432), ("spec", "twoshot", 0, 432)])
+def test_fused_gemv_allreduce_bit_exact(protocol, datapath, chain, unit):
+    # unit 432: 19 pieces of 216 columns per rank (the last 208), 152 fused CTAs
     R, n, k, pool, E = 8, 4096, 256, 3, 24
     wts, xs = _gemv_case(R, n, k, pool, 97)
     plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol=protocol, datapath=datapath,
-                    chain=chain)
+                    chain=chain, unit_bytes=unit)
     dw = [to_dev(w.ravel(), "bf16") for w in wts]
     dx = [torch.stack([to_dev(x, "bf16") for x in xs[r]]).contiguous() for r in range(R)]
     outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
@@ -1089,26 +1090,35 @@ def test_fused_gemv_with_a_reduce_scatter_naming_and_bad_arguments():
 
 
 
-@pytest.mark.parametrize("k,n,wpr", [(16, 4096, 0), (80, 4096, 0), (128, 4096, 0),
-                                     (1024, 4096, 0), (512, 4096, 2), (128, 1000, 0),
-                                     (256, 1000, 0), (8192, 1024, 0), (128, 4352, 1),
-                                     (320, 4096, 0), (48, 2048, 0)],
+@pytest.mark.parametrize("k,n,wpr,unit", [(16, 4096, 0, 0), (80, 4096, 0, 0), (128, 4096, 0, 0),
+                                          (1024, 4096, 0, 0), (512, 4096, 2, 0), (128, 1000, 0, 0),
+                                          (256, 1000, 0, 0), (8192, 1024, 0, 0), (128, 4352, 1, 0),
+                                          (320, 4096, 0, 0), (48, 2048, 0, 0),
+                                          (512, 4096, 0, 432), (1024, 4096, 0, 432),
+                                          (128, 1000, 0, 432), (384, 4096, 0, 256),
+                                          (80, 1024, 0, 64)],
                          ids=["k16-one-partial-fill", "k80-full-and-partial-fill",
                               "k128-several-pieces-per-ring-lap",
                               "k1024-ring-wraps-inside-a-piece", "k512-four-pieces-per-warp",
                               "k128-ragged-last-piece", "k256-ragged-last-piece",
                               "k8192-largest-x", "k128-seventeen-pieces-per-warp",
-                              "k320-a-piece-fills-the-ring", "k48-partial-fill"])
-def test_fused_gemv_weight_ring_shapes(k, n, wpr):
-    # The weight rows stream through one ring of 5 slots of 64 rows (one tensor copy each)
-    # shared by the compute warps, and x through two buffers: these shapes cover a last fill
-    # only partly inside the matrix (its rows past k read zeros), several pieces per ring
-    # lap, a piece longer than the ring, a piece exactly as long, warps with several stage
-    # items (more than the 16 whose sources are cached), the longest x, and a last piece
-    # shorter than 512 bytes, whose copies read zeros past the matrix's columns.
+                              "k320-a-piece-fills-the-ring", "k48-partial-fill",
+                              "u432-k512-six-slot-ring", "u432-k1024-ring-wraps",
+                              "u432-k128-ragged-last-piece", "u256-k384-two-warps-idle",
+                              "u64-k80-sixteen-live-lanes"])
+def test_fused_gemv_weight_ring_shapes(k, n, wpr, unit):
+    # The weight rows stream through one ring of slots of 64 rows (one tensor copy each, 5
+    # slots of 512-byte rows, 6 of 432-byte rows, 8 of smaller ones) shared by the compute
+    # warps, and x through two buffers: these shapes cover a last fill only partly inside
+    # the matrix (its rows past k read zeros), several pieces per ring lap, a piece longer
+    # than the ring, a piece exactly as long, warps with several stage items (more than the
+    # 16 whose sources are cached), the longest x, a last piece shorter than the unit, whose
+    # copies read zeros past the matrix's columns, and units narrower than 512 bytes, whose
+    # compute lanes past the unit's columns idle.
     R, pool, E = 4, 2, 6
-    wts, xs = _gemv_case(R, n, k, pool, 99 + k)
-    plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="dual", warps_per_rank=wpr)
+    wts, xs = _gemv_case(R, n, k, pool, 99 + k + unit)
+    plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="dual", warps_per_rank=wpr,
+                    unit_bytes=unit)
     dw = [to_dev(w.ravel(), "bf16") for w in wts]
     dx = [torch.stack([to_dev(x, "bf16") for x in xs[r]]).contiguous() for r in range(R)]
     outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
