@@ -806,10 +806,10 @@ __device__ __forceinline__ uint4 spec_attempt(const char *xb, uint32_t nbytes, u
 // KIND: 0 copy, 1 sum of bf16, 2 sum of f32. GEMV: fused producer. LL: tagged data.
 // PULL: two-shot pull plans (the publish/pull steps are compiled only into this variant).
 // FP: 0 for the general engine; otherwise a variant for plans whose every warp has one
-// stage item and one consume item, run without fault injection, phase stamps or chained
-// epochs, under one speculative protocol known at compile time (1 with content tags, 2 the
-// same fence-free; 3 and 4 the same two with one %globaltimer stamp per epoch, so that the
-// latency distribution is taken on the specialised code). On the single warp that carries a
+// stage item and one consume item, run without fault injection or phase stamps, under one
+// speculative protocol known at compile time (1 with content tags, 2 the same fence-free;
+// 3 and 4 the same two with one %globaltimer stamp per epoch, so that the latency
+// distribution is taken on the specialised code; 5 and 6 the same two with chained epochs). On the single warp that carries a
 // piece through an epoch, every runtime mode test is a dependent instruction on the critical
 // path; compiled out, the decode epoch drops by about a sixth. (A dual-buffer variant
 // measured slower than the general engine and is not built.)
@@ -822,8 +822,9 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
     engine_kernel(const EngArgs a, const __grid_constant__ typename MapsArg<GEMV>::type maps) {
   static_assert(FP == 0 || (!GEMV && !LL && !PULL), "the specialised variants are plain");
   constexpr bool fast = FP != 0;
-  constexpr bool fp_relaxed = FP == 2 || FP == 4;  // the specialised fence-free check
-  constexpr bool fp_stamps = FP >= 3;              // ... with one stamp per epoch
+  constexpr bool fp_relaxed = FP == 2 || FP == 4 || FP == 6;  // the fence-free check
+  constexpr bool fp_stamps = FP == 3 || FP == 4;  // ... with one stamp per epoch
+  constexpr bool fp_chain = FP >= 5;              // ... with chained epochs
   const uint32_t gw = blockIdx.x;
   const uint32_t lane = threadIdx.x & 31u;
   if constexpr (GEMV) {
@@ -879,7 +880,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
                               (int)W.rank == a.inject_rank;
   const bool delay_producer = !fast && (a.inject_flags & COLL_INJECT_SPEC_PAUSE) &&
                               (int)W.rank == (a.inject_rank + 1) % a.R;
-  const bool chained = !fast && a.chain && a.rank_done;
+  const bool chained = fast ? fp_chain : a.chain && a.rank_done;
   const bool stagger = !fast && (a.inject_flags & COLL_INJECT_STAGGER);
   uint32_t n_checks = 0, n_retries = 0;
   uint32_t win = a.spec_delay_ns;  // the speculation window of this warp (ns)
@@ -1374,15 +1375,19 @@ static const void *engine_fn(int kind, bool gemv, bool ll, bool pull, int fp = 0
     return kind == 1 ? (const void *)engine_kernel<1, false, false, true, 0>
                      : (const void *)engine_kernel<2, false, false, true, 0>;
   if (fp != 0 && kind != 0) {  // (the specialised variants are sums)
-    switch ((kind - 1) * 4 + fp) {
+    switch ((kind - 1) * 6 + fp) {
       case 1: return (const void *)engine_kernel<1, false, false, false, 1>;
       case 2: return (const void *)engine_kernel<1, false, false, false, 2>;
       case 3: return (const void *)engine_kernel<1, false, false, false, 3>;
       case 4: return (const void *)engine_kernel<1, false, false, false, 4>;
-      case 5: return (const void *)engine_kernel<2, false, false, false, 1>;
-      case 6: return (const void *)engine_kernel<2, false, false, false, 2>;
-      case 7: return (const void *)engine_kernel<2, false, false, false, 3>;
-      default: return (const void *)engine_kernel<2, false, false, false, 4>;
+      case 5: return (const void *)engine_kernel<1, false, false, false, 5>;
+      case 6: return (const void *)engine_kernel<1, false, false, false, 6>;
+      case 7: return (const void *)engine_kernel<2, false, false, false, 1>;
+      case 8: return (const void *)engine_kernel<2, false, false, false, 2>;
+      case 9: return (const void *)engine_kernel<2, false, false, false, 3>;
+      case 10: return (const void *)engine_kernel<2, false, false, false, 4>;
+      case 11: return (const void *)engine_kernel<2, false, false, false, 5>;
+      default: return (const void *)engine_kernel<2, false, false, false, 6>;
     }
   }
   switch (kind) {
@@ -1393,13 +1398,17 @@ static const void *engine_fn(int kind, bool gemv, bool ll, bool pull, int fp = 0
 }
 
 // The specialised variant a run of these arguments may use (0: the general engine).
+// FP 1/2: tagged / fence-free check; 3/4: the same with one stamp per epoch; 5/6: the same
+// checks with chained epochs (no stamps).
 static int engine_fp(int kind, const EngArgs &a) {
   if (kind == 0 || a.gemv_k != 0 || a.rpar != 0 || !a.single_items || a.inject_flags != 0 ||
-      (a.stamps != nullptr && a.stamp_phases) || a.dbg != nullptr || (a.chain && a.rank_done))
+      (a.stamps != nullptr && a.stamp_phases) || a.dbg != nullptr)
     return 0;
-  const int st = a.stamps != nullptr ? 2 : 0;
-  if (a.protocol == COLL_PROTO_SPEC && a.spec_check == COLL_SPEC_TAGGED) return 1 + st;
-  if (a.protocol == COLL_PROTO_SPEC && a.spec_check == COLL_SPEC_TAGGED_RELAXED) return 2 + st;
+  const bool chain = a.chain && a.rank_done;
+  if (chain && a.stamps != nullptr) return 0;
+  const int off = chain ? 4 : a.stamps != nullptr ? 2 : 0;
+  if (a.protocol == COLL_PROTO_SPEC && a.spec_check == COLL_SPEC_TAGGED) return 1 + off;
+  if (a.protocol == COLL_PROTO_SPEC && a.spec_check == COLL_SPEC_TAGGED_RELAXED) return 2 + off;
   return 0;
 }
 
@@ -1413,7 +1422,7 @@ cudaError_t engine_max_coresident(int op, int dtype, int protocol, int datapath,
   const bool ll = protocol == COLL_PROTO_LL, pull = datapath == COLL_DP_TWOSHOT_PULL;
   // a run may use a specialised variant: every variant it may use must fit
   int per_sm = 1 << 30;
-  for (int fp = 0; fp <= ((kind != 0 && !ll && !pull) ? 4 : 0); ++fp) {
+  for (int fp = 0; fp <= ((kind != 0 && !ll && !pull) ? 6 : 0); ++fp) {
     int n = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, engine_fn(kind, false, ll, pull, fp),
                                                       32, 0);

@@ -356,6 +356,24 @@ def test_decode_allreduce_epochs_bit_exact(protocol, datapath, chain):
     plan.free()
 
 
+@pytest.mark.parametrize("check", ["tagged", "relaxed"])
+def test_chained_specialised_variants_bit_exact(check):
+    # chained epochs (a rank stages epoch e + 1 only after its whole epoch-e output is done)
+    # on the variants specialised for one item per warp, both speculative checks; two runs,
+    # every epoch against the oracle
+    R, n, pool, E = 8, 4096, 7, 5000
+    ins, expect = _decode_case(R, n, pool, seed=31)
+    plan = cdc.Plan(namings.allreduce(R, n, "bf16"), protocol="spec", spec_check=check, chain=1)
+    outs = [torch.empty(E, n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    for _ in range(2):
+        plan.run(ins, outs, n_epochs=E, in_epoch_stride=n * 2, in_pool=pool,
+                 out_epoch_stride=n * 2)
+        st = plan.status()
+        assert st["code"] == 0, st
+        assert _check_epochs(outs, expect, E, pool) == 0
+    plan.free()
+
+
 @pytest.mark.parametrize("cfg", [dict(protocol="barrier"), dict(protocol="dual"),
                                  dict(protocol="spec"), dict(protocol="spec", spec_check="relaxed"),
                                  dict(protocol="spec", spec_check="literal"),
