@@ -811,8 +811,6 @@ def run_workload(args):
         ins = [synth.device_uniform_bf16(torch, 3000 + r, n, dev) for r in range(R)]
         outs = [torch.empty(L, dtype=torch.int16, device=dev) for L in nm.out_len]
         cfg = {"datapath": args.datapath} if args.datapath else {}
-        if args.bulk_cluster >= 0:
-            cfg["bulk_cluster"] = args.bulk_cluster
         if args.warp_kernel:
             cfg["tma_min_bytes"] = (1 << 64) - 1
         if args.tile_bytes:
@@ -827,7 +825,7 @@ def run_workload(args):
         res.update({"collective": args.collective, "mib_per_rank": args.mib,
                     "datapath": args.datapath or "default", "min_bytes": int(pl.info.min_bytes),
                     "kernel": "bulk_kernel" if pl.info.bulk_tile_bytes else "zc_kernel",
-                    "bulk_cluster": int(pl.info.bulk_cluster), "single": r})
+                    "single": r})
         pl.free()
     elif args.workload == "fig15":
         # SiFAR Fig. 15 grid: R = 2/4/8 ranks x 8/16/32 KB payloads, every protocol and
@@ -928,9 +926,6 @@ def main():
                     help="single: the warp kernel instead of the bulk (TMA) ring")
     ap.add_argument("--tile-bytes", type=int, default=0,
                     help="single: warp kernel bytes per tile (0: the plan's choice)")
-    ap.add_argument("--bulk-cluster", type=int, default=-1,
-                    help="single: CTAs per multicast cluster of a one-shot sum (0: none, "
-                         "the default)")
     ap.add_argument("--protocols", default="barrier,dual,spec",
                     help="fused: protocols to run, comma-separated")
     ap.add_argument("--print-sources-sha", action="store_true",

@@ -62,13 +62,13 @@ class Config(C.Structure):
                 ("inject_max_ns", C.c_uint64), ("inject_start_ns", C.c_uint64),
                 ("inject_pause_ns", C.c_uint64), ("chain", C.c_int32),
                 ("spec_delay_ns", C.c_int32), ("reduce_order", C.c_int32),
-                ("bulk_cluster", C.c_int32)]
+                ("reserved3", C.c_int32)]
 
 
 class PlanInfo(C.Structure):
     _fields_ = [(n, C.c_uint64) for n in ("n_names", "n_jobs", "n_tiles", "n_units", "n_warps",
                                           "min_bytes", "xbuf_bytes", "flag_bytes",
-                                          "bulk_tile_bytes", "bulk_cluster")]
+                                          "bulk_tile_bytes")]
 
 
 class Stats(C.Structure):

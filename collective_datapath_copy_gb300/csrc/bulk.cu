@@ -8,26 +8,11 @@
 // the stage. The ring keeps up to `stages` tiles of loads in flight per SM independently of
 // register pressure, which is what a streaming copy/reduce needs to reach HBM bandwidth.
 //
-// One-shot sums (every consumer reduces all producers' pieces of a chunk itself) can run on
-// clusters of C = 2, 4 or 8 CTAs instead. The plan lists a chunk's consumer tiles next to
-// each other, so C consecutive tiles share their sources; cluster g takes tile groups g,
-// g + G, ... and its CTA q the q-th tile of each. Each source piece is then read once per
-// cluster: CTA q's issuer warp brings in the pieces j with j % C == q with one multicast bulk
-// copy into the same stage of all C CTAs. Before any CTA copies into a stage, every CTA of
-// the cluster must have released it and armed its full barrier with the tile's bytes: each
-// CTA's producer warp, once its own consumers released the stage, arms it and arrives on the
-// stage's `ready` barrier in every CTA of the cluster, and the issuer warps copy only after
-// their own `ready` barrier saw all C arrivals. The consumers are unchanged.
-//
 // Every mbarrier wait is bounded by the plan's spin limit; on expiry the CTA records
-// COLL_ETIMEDOUT in the plan status, waits (bounded) for the bulk copies into its shared
-// memory that it armed, and returns (a cluster's CTAs leave together, after a cluster
-// barrier, so that no CTA exits while a peer may still arrive on its barriers).
+// COLL_ETIMEDOUT in the plan status, waits (bounded) for the bulk copies it issued, and
+// returns.
 #include <cuda_runtime.h>
 #include <stdint.h>
-
-#include <algorithm>
-#include <mutex>
 
 #include "atom.cuh"
 #include "engine.cuh"
@@ -40,8 +25,6 @@ namespace {
 constexpr uint32_t kConsumerWarps = 8;
 constexpr unsigned FULLW = 0xFFFFFFFFu;
 constexpr uint32_t kThreads = 32 * (kConsumerWarps + 1);
-constexpr uint32_t kThreadsMc = kThreads + 32;  // + the multicast issuer warp
-constexpr uint32_t kIssuerWarp = kConsumerWarps + 1;
 constexpr uint32_t kClaim = 2;   // tiles per claim of the dynamic tail
 constexpr uint32_t kTable = 64;  // resolved tiles held (>= 32 + the ring's stages)
 
@@ -66,53 +49,35 @@ __device__ void bulk_timeout(coll_dev_status_t *st, uint32_t tile) {
   }
 }
 
-__host__ __device__ constexpr uint32_t bulk_head(uint32_t stages) {
-  return ((24u * stages + 4u * stages) + 127u) & ~127u;
-}
-
-// KIND: 0 copy, 1 sum of bf16, 2 sum of f32. MC: cluster multicast (one-shot sums).
-template <int KIND, bool TREE, bool MC>
-__global__ void __launch_bounds__(MC ? kThreadsMc : kThreads, 1) bulk_kernel(const ZcArgs a) {
+// KIND: 0 copy, 1 sum of bf16, 2 sum of f32.
+template <int KIND, bool TREE>
+__global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ TileRec table[kTable];
   __shared__ volatile uint32_t s_abort;
-  __shared__ uint32_t s_issued;          // tiles whose full barrier this CTA has armed
+  __shared__ uint32_t s_issued;
   __shared__ volatile uint32_t s_final;  // tiles this CTA issues in all, once known
   const uint32_t S = a.stages;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
   uint64_t *empty = full + S;
-  uint64_t *ready = empty + S;  // MC: every CTA of the cluster has armed the stage
-  uint32_t *stile = reinterpret_cast<uint32_t *>(ready + S);  // table entry of each stage
-  unsigned char *data = smem + bulk_head(S);
+  uint32_t *stile = reinterpret_cast<uint32_t *>(empty + S);  // table entry of each stage
+  const uint32_t head = ((16u * S + 4u * S) + 127u) & ~127u;
+  unsigned char *data = smem + head;
   const uint32_t stage_bytes = a.maxsrc * a.slot_bytes;
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
   const uint64_t total = (uint64_t)a.ntiles * a.n_epochs;
-  // MC: C CTAs per cluster, this CTA's rank qc in it, cluster cid of G; NG groups of C tiles
-  uint32_t C = 1, qc = 0;
-  uint64_t cid = blockIdx.x, G = gridDim.x, NG = total, count = 0;
-  if constexpr (MC) {
-    C = a.cluster;
-    qc = cluster_ctarank();
-    cid = blockIdx.x / C;
-    G = gridDim.x / C;
-    NG = total / C;
-    count = cid < NG ? (NG - 1u - cid) / G + 1u : 0u;
-  }
 
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
-      if constexpr (MC) mbar_init(&ready[s], C);
     }
     s_abort = 0;
     s_issued = 0;
     s_final = 0xFFFFFFFFu;
     mbar_init_fence();
   }
-  // (MC: the peers' barriers are initialised before any CTA arrives on them or copies)
-  if constexpr (MC) cluster_sync_all();
-  else __syncthreads();
+  __syncthreads();
 
   uint32_t consumed = 0;
   if (warp == 0) {
@@ -121,25 +86,16 @@ __global__ void __launch_bounds__(MC ? kThreadsMc : kThreads, 1) bulk_kernel(con
     // shared by the CTAs, so that SMs that run faster take more of the last tiles. Lane i
     // resolves tile i of a batch from its record (one memory round trip per batch) into the
     // table. Then, tile by tile: lane 0 waits for the stage to be free, records the tile's
-    // entry and the bytes to expect, and lanes j < nsrc each issue source j's bulk copy
-    // (MC: the tiles are this CTA's of its cluster's groups, all dealt, and lanes j < C
-    // arrive on the stage's `ready` barrier of cluster CTA j instead; the issuer warp copies).
+    // entry and the bytes to expect, and lanes j < nsrc each issue source j's bulk copy.
     uint32_t k = 0, s = 0, lap = 0;
-    bool stop = false, dyn = !MC && a.static_tiles == 0;
-    uint64_t t0 = cid;
+    bool stop = false, dyn = a.static_tiles == 0;
+    uint64_t t0 = blockIdx.x;
     uint32_t cnext = 0;      // lane 0: the claim for the batch after this one, taken ahead
     bool cnext_valid = false;
     // The tiles of the next batch (lane i: one tile), one batch ahead of their issue, so
     // that the claim's and the records' memory round trips overlap the current batch.
     auto next_batch = [&](uint64_t &t, bool &have) {
       have = false;
-      if constexpr (MC) {  // tile qc of groups cid + i * G (t0 counts groups)
-        const uint64_t g = t0 + (uint64_t)lane * G;
-        t = g * C + qc;
-        have = g < NG;
-        t0 += 32ull * G;
-        return;
-      }
       if (!dyn) {
         t = t0 + (uint64_t)lane * gridDim.x;
         have = t < a.static_tiles;
@@ -228,13 +184,9 @@ __global__ void __launch_bounds__(MC ? kThreadsMc : kThreads, 1) bulk_kernel(con
           s_issued = k + 1;
         }
         __syncwarp();  // the bytes are expected before any copy can complete them
-        if constexpr (MC) {
-          // this CTA's stage s is free and armed: tell every issuer of the cluster
-          if (lane < C) mbar_arrive_cluster(cluster_map(&ready[s], lane));
-        } else if (lane < ns) {
+        if (lane < ns)
           bulk_load(data + (size_t)s * stage_bytes + (size_t)lane * a.slot_bytes, tr.src[lane], nb,
                     &full[s]);
-        }
         if (++s == S) {
           s = 0;
           ++lap;
@@ -253,33 +205,6 @@ __global__ void __launch_bounds__(MC ? kThreadsMc : kThreads, 1) bulk_kernel(con
       if (ok) ok = mbar_wait(&empty[s], (lap & 1u) ^ 1u, a.spin_ns, &s_abort);
       s_final = k;
       if (ok) mbar_arrive(&full[s]);
-    }
-  } else if (MC && warp == kIssuerWarp) {
-    // Issuer warp (MC): once every CTA of the cluster has armed stage s for tile k, copy
-    // this CTA's pieces of the tile into all of them. The table entry was written before the
-    // producer's own arrival on `ready` (acquired here).
-    uint32_t s = 0, lap = 0;
-    const uint16_t mask = (uint16_t)((1u << C) - 1u);
-    for (uint64_t k = 0; k < count; ++k) {
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait_cluster(&ready[s], lap & 1u, a.spin_ns, &s_abort);
-      ok = __shfl_sync(FULLW, ok, 0);
-      if (!ok) {
-        if (lane == 0) {
-          bulk_timeout(a.st, (uint32_t)k);
-          s_abort = 1;
-        }
-        break;
-      }
-      const TileRec &tr = table[k % kTable];
-      const uint32_t nb = tr.nbytes, ns = tr.nsrc;
-      if (lane < ns && lane % C == qc)
-        bulk_load_multicast(data + (size_t)s * stage_bytes + (size_t)lane * a.slot_bytes,
-                            tr.src[lane], nb, &full[s], mask);
-      if (++s == S) {
-        s = 0;
-        ++lap;
-      }
     }
   } else {
     const uint32_t ctid = threadIdx.x - 32;  // consumer thread index
@@ -335,7 +260,6 @@ __global__ void __launch_bounds__(MC ? kThreadsMc : kThreads, 1) bulk_kernel(con
     for (uint32_t k = consumed; k < s_issued; ++k)
       mbar_wait(&full[k % S], (k / S) & 1u, 100000000ull, &never);
   }
-  if constexpr (MC) cluster_sync_all();
   if (threadIdx.x == 0) {
     // the last CTA to finish zeroes the tail counters for the plan's next run
     __threadfence();
@@ -347,101 +271,28 @@ __global__ void __launch_bounds__(MC ? kThreadsMc : kThreads, 1) bulk_kernel(con
   }
 }
 
-// Clusters of C CTAs of the multicast variant that fit on the device at once (cached per
-// device, kernel and shared-memory size; 0 if none fits).
-int max_active_clusters(const void *fn, uint32_t C, uint32_t smem) {
-  struct Entry {
-    int dev;
-    const void *fn;
-    uint32_t C, smem;
-    int n;
-  };
-  static Entry cache[32];
-  static int used = 0;
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  std::lock_guard<std::mutex> g(mu);
-  for (int i = 0; i < used; ++i)
-    if (cache[i].dev == dev && cache[i].fn == fn && cache[i].C == C && cache[i].smem == smem)
-      return cache[i].n;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = C;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(C);
-  cfg.blockDim = dim3(kThreadsMc);
-  cfg.dynamicSmemBytes = smem;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
-    (void)cudaGetLastError();
-    n = 0;
-  }
-  if (used < 32) cache[used++] = Entry{dev, fn, C, smem, n};
-  return n;
-}
-
 }  // namespace
 
 uint32_t bulk_smem_bytes(uint32_t stages, uint32_t maxsrc, uint32_t slot_bytes) {
-  return bulk_head(stages) + stages * maxsrc * slot_bytes;
+  const uint32_t head = ((16u * stages + 4u * stages) + 127u) & ~127u;
+  return head + stages * maxsrc * slot_bytes;
 }
 
 cudaError_t launch_bulk(int op, int dtype, const ZcArgs &a, int ctas, cudaStream_t s) {
   const uint64_t total = (uint64_t)a.ntiles * a.n_epochs;
   if (total == 0) return cudaSuccess;
-  const uint32_t smem = bulk_smem_bytes(a.stages, a.maxsrc, a.slot_bytes);
-  ZcArgs la = a;
-  cudaError_t e;
-  if (a.cluster > 1 && op != COLL_OP_COPY) {
-    // One-shot sum on multicast clusters: as many clusters as fit at once (each takes
-    // every G-th group of C tiles), none if the device cannot hold one.
-    const uint32_t C = a.cluster;
-    const void *fn = dtype == COLL_BF16
-                         ? (a.tree ? (const void *)bulk_kernel<1, true, true>
-                                   : (const void *)bulk_kernel<1, false, true>)
-                         : (a.tree ? (const void *)bulk_kernel<2, true, true>
-                                   : (const void *)bulk_kernel<2, false, true>);
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    uint64_t G = (uint64_t)max_active_clusters(fn, C, smem);
-    G = std::min<uint64_t>(G, (uint64_t)ctas / C);
-    G = std::min<uint64_t>(G, total / C);
-    if (G >= 1 && total % C == 0) {
-      la.static_tiles = total;
-      la.dyn_tail = 0;
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute at[1];
-      at[0].id = cudaLaunchAttributeClusterDimension;
-      at[0].val.clusterDim.x = C;
-      at[0].val.clusterDim.y = 1;
-      at[0].val.clusterDim.z = 1;
-      cfg.gridDim = dim3((unsigned)(G * C));
-      cfg.blockDim = dim3(kThreadsMc);
-      cfg.dynamicSmemBytes = smem;
-      cfg.stream = s;
-      cfg.attrs = at;
-      cfg.numAttrs = 1;
-      void *args[] = {(void *)&la};
-      return cudaLaunchKernelExC(&cfg, fn, args);
-    }
-    la.cluster = 0;  // no cluster fits: the unclustered ring
-  }
-  la.cluster = 0;
   const int grid = (int)((uint64_t)ctas < total ? (uint64_t)ctas : total);
+  const uint32_t smem = bulk_smem_bytes(a.stages, a.maxsrc, a.slot_bytes);
   // whole rounds of four fifths of the tiles are dealt round-robin and the rest claimed, or
   // (many-to-one sums) every tile dealt round-robin
+  ZcArgs la = a;
   la.static_tiles = a.dyn_tail ? total * 4 / 5 / (uint64_t)grid * (uint64_t)grid : total;
   if (total - la.static_tiles >= (1ull << 31)) la.static_tiles = total;  // (claim counter)
   const void *fn;
-  if (op == COLL_OP_COPY) fn = (const void *)bulk_kernel<0, false, false>;
-  else if (dtype == COLL_BF16) fn = a.tree ? (const void *)bulk_kernel<1, true, false> : (const void *)bulk_kernel<1, false, false>;
-  else fn = a.tree ? (const void *)bulk_kernel<2, true, false> : (const void *)bulk_kernel<2, false, false>;
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (op == COLL_OP_COPY) fn = (const void *)bulk_kernel<0, false>;
+  else if (dtype == COLL_BF16) fn = a.tree ? (const void *)bulk_kernel<1, true> : (const void *)bulk_kernel<1, false>;
+  else fn = a.tree ? (const void *)bulk_kernel<2, true> : (const void *)bulk_kernel<2, false>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   void *args[] = {(void *)&la};
   return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, smem, s);

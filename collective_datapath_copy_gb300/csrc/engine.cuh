@@ -33,7 +33,7 @@ struct ZcArgs {
   uint32_t tree;          // 1: pairwise (tree) summation order within groups of 8
   uint64_t static_tiles;  // bulk kernel: tiles dealt round-robin; the rest are claimed
   uint32_t dyn_tail;      // bulk kernel: 1 = claim the last fifth of the tiles dynamically
-  uint32_t cluster;       // bulk kernel: CTAs per multicast cluster (0: none)
+  uint32_t pad2;
 };
 
 struct EngArgs {

@@ -60,9 +60,7 @@ static int check_config(const coll_config_t &c) {
   if (c.warps_per_rank < 0 || c.ctas < 0) return COLL_EINVAL;
   if (c.tile_bytes < 0 || (c.tile_bytes % 16) != 0) return COLL_EINVAL;
   if (c.inject_prob_ppm > 1000000u) return COLL_EINVAL;
-  if (c.chain < 0 || c.chain > 1) return COLL_EINVAL;
-  if (c.bulk_cluster != 0 && c.bulk_cluster != 2 && c.bulk_cluster != 4 && c.bulk_cluster != 8)
-    return COLL_EINVAL;
+  if (c.chain < 0 || c.chain > 1 || c.reserved3 != 0) return COLL_EINVAL;
   if (c.spec_delay_ns < -1 || c.spec_delay_ns > 100000) return COLL_EINVAL;
   if (c.reduce_order < 0 || c.reduce_order > 1) return COLL_EINVAL;
   // the staged engine always sums in rank order
@@ -244,21 +242,6 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
       // claims its last tiles dynamically; many-to-one sums (reduce-scatter, reduce to
       // root, one-shot all-reduce) are faster with every tile dealt round-robin (measured).
       c.bulk_tail = maxdst >= maxsrc;
-      // One-shot sums: the consumers of a chunk are consecutive tiles with the same sources
-      // (see the tile order below), so clusters of C CTAs can share each source piece, if
-      // asked for and C divides every name's consumer count (no group of C tiles then spans
-      // two names).
-      if (sum && !twoshot && cfg.bulk_cluster) {
-        uint32_t C = (uint32_t)cfg.bulk_cluster;
-        for (auto &nm : names) {
-          if (nm.cons.size() % C) {
-            C = 0;
-            break;
-          }
-        }
-        c.bulk_cluster = C;
-        if (c.bulk_cluster) c.bulk_tail = false;
-      }
     } else if (!T) {
       // One warp per tile: the largest power of two (512 B .. 32 KiB) that still gives
       // about four tiles per resident warp (32 per SM).
@@ -468,7 +451,6 @@ void coll_fill_info(const coll_compiled &c, coll_plan_info_t *info) {
   info->n_warps = c.warps.size();
   info->min_bytes = c.min_bytes;
   info->bulk_tile_bytes = c.bulk ? c.bulk_slot : 0;
-  info->bulk_cluster = c.bulk ? c.bulk_cluster : 0;
   const bool dual = c.cfg.protocol != COLL_PROTO_BARRIER;
   info->xbuf_bytes = c.cfg.zero_copy ? 0 : (c.xpar_bytes + c.rpar_bytes) * (dual ? 2 : 1);
   info->flag_bytes = c.cfg.zero_copy ? 0

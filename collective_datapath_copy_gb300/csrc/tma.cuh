@@ -93,76 +93,6 @@ __device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t
       : "memory");
 }
 
-// ---- thread-block clusters
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Every thread of every CTA in the cluster arrives (release) and waits (acquire): shared
-// memory written before it is visible to the cluster's threads after it, and no CTA gets
-// past it while another has not reached it.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
-// The shared::cluster address of the same CTA-relative location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t cluster_map(const void *local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
-  return r;
-}
-
-// Arrive once (release at cluster scope) on an mbarrier given by its shared::cluster address.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
-// try_wait with acquire at cluster scope (the phase was completed by arrivals from other CTAs).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait (as mbar_wait) for a phase completed by arrivals from other CTAs of the
-// cluster; acquires at cluster scope.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint64_t limit,
-                                                  const volatile uint32_t *abort_flag) {
-  uint64_t t0 = 0;
-  for (uint32_t i = 0;; ++i) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((i & 15u) == 15u) {
-      const uint64_t now = globaltimer();
-      if (t0 == 0) t0 = now;
-      else if (now - t0 > limit) return false;
-      if (*abort_flag != 0u) return false;
-    }
-  }
-}
-
-// Bulk copy of `bytes` from global memory into the shared memory of every CTA of the cluster
-// whose bit is set in `cta_mask`, at the same CTA-relative offset as `sdst`; each destination
-// CTA's mbarrier at the offset of `bar` receives the completed bytes. Same size and alignment
-// rules as bulk_load.
-__device__ __forceinline__ void bulk_load_multicast(void *sdst, const void *gsrc, uint32_t bytes,
-                                                    uint64_t *bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(sdst)),
-      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "h"(cta_mask)
-      : "memory");
-}
-
 // Tensor copy of one 2-D box (the map's box size) at element coordinates (x, y) from global
 // memory to this CTA's shared memory (128-byte aligned); completion is counted on `bar`'s
 // transaction count. x times the element size must be a multiple of 16 bytes. A slot that

@@ -168,16 +168,7 @@ typedef struct {
                                window for the other checks; 0..100000 = that many ns,
                                fixed                                                     */
   int32_t reduce_order;     /* COLL_ORDER_*; zero-copy plans only                      */
-  int32_t bulk_cluster;     /* zero-copy one-shot sums on the bulk (TMA) ring: CTAs per
-                               thread-block cluster that share each source piece through
-                               one multicast copy (SiFAR review, Fig. 5: every consumer
-                               pulls the whole payload; here the C consumers of a chunk
-                               pull it together). 0 = no cluster (the default: on GB300
-                               each SM still takes in every piece of its tiles, and the
-                               cluster's lockstep made the ring slower); 2, 4 or 8 = that
-                               size, used where it divides every name's consumer count.
-                               Other plans ignore it. If the device cannot hold one such
-                               cluster at run time, the run uses the unclustered ring.   */
+  int32_t reserved3;        /* must be 0                                                */
 } coll_config_t;
 
 typedef struct {
@@ -192,9 +183,6 @@ typedef struct {
   uint64_t flag_bytes;   /* staged flag words                                         */
   uint64_t bulk_tile_bytes; /* zero-copy: bytes per tile of the bulk (TMA) ring kernel the
                                plan was compiled for; 0 = the warp kernel               */
-  uint64_t bulk_cluster;    /* zero-copy: CTAs per multicast cluster of the bulk ring the
-                               plan was compiled for (see coll_config_t.bulk_cluster);
-                               0 = no cluster                                           */
 } coll_plan_info_t;
 
 typedef struct {

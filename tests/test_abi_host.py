@@ -136,32 +136,6 @@ def test_bad_config_rejected():
             cdc.validate(n, protocol="spec", spec_delay_ns=bad)
 
 
-def test_bulk_cluster_config_and_the_planners_choice():
-    n = namings.allreduce(2, 256)
-    for bad in (-1, 1, 3, 5, 6, 16):
-        with pytest.raises(cdc.CollError):
-            cdc.validate(n, zero_copy=1, bulk_cluster=bad)
-    big = 8 << 20   # 16 MiB of bf16 per rank: the bulk ring
-    ar8 = namings.allreduce(8, big, "bf16")
-    info = cdc.validate(ar8, zero_copy=1)   # one-shot: 8 consumers per chunk, no cluster
-    assert info.bulk_tile_bytes > 0 and info.bulk_cluster == 0
-    for C in (2, 4, 8):
-        assert cdc.validate(ar8, zero_copy=1, bulk_cluster=C).bulk_cluster == C
-    # one consumer per job (two-shot push, reduce-scatter) or copies: no cluster
-    assert cdc.validate(ar8, zero_copy=1, datapath="twoshot", bulk_cluster=8).bulk_cluster == 0
-    assert cdc.validate(namings.reduce_scatter(8, big, "bf16"), zero_copy=1,
-                        bulk_cluster=8).bulk_cluster == 0
-    assert cdc.validate(namings.allgather(8, big // 8, "bf16"), zero_copy=1,
-                        bulk_cluster=8).bulk_cluster == 0
-    # 6 consumers: 2 divides them, 4 does not
-    ar6 = namings.allreduce(6, big, "bf16")
-    assert cdc.validate(ar6, zero_copy=1, bulk_cluster=2).bulk_cluster == 2
-    assert cdc.validate(ar6, zero_copy=1, bulk_cluster=4).bulk_cluster == 0
-    # small plans stay on the warp kernel
-    assert cdc.validate(namings.allreduce(8, 4096, "bf16"), zero_copy=1,
-                        bulk_cluster=8).bulk_cluster == 0
-
-
 def test_default_config_is_the_fence_free_speculative_check():
     c = _lib.make_config()
     assert c.protocol == _lib.D["COLL_PROTO_SPEC"]

@@ -849,59 +849,6 @@ def test_bulk_ring_epochs_over_an_input_pool():
         plan.free()
 
 
-@pytest.mark.parametrize("cluster", [0, 2, 4, 8])
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_oneshot_multicast_clusters_bit_exact(cluster, dtype):
-    # the one-shot bulk ring on clusters of C CTAs that share each source piece (one
-    # multicast copy into the C consumers of a chunk): every epoch of a pooled run against
-    # the oracle, with a ragged last tile; 0 = the unclustered ring
-    R, pool, E = 8, 3, 4
-    k = 8 if dtype == "bf16" else 4
-    n = 5 * 4096 + 3 * k
-    rng = synth.seeded_rng(84)
-    pool_np = [[gen("normal", rng, n, dtype) for _ in range(R)] for _ in range(pool)]
-    ins = [torch.stack([to_dev(pool_np[p][r], dtype) for p in range(pool)]).contiguous()
-           for r in range(R)]
-    nm = namings.allreduce(R, n, dtype)
-    plan = cdc.Plan(nm, zero_copy=1, tma_min_bytes=1, bulk_cluster=cluster)
-    assert plan.info.bulk_tile_bytes > 0
-    assert plan.info.bulk_cluster == cluster
-    es = 2 if dtype == "bf16" else 4
-    outs = [torch.zeros(E, n * es, dtype=torch.uint8, device="cuda") for _ in range(R)]
-    for rep in range(2):   # the plan's second run finds its counters reset
-        plan.run(ins, outs, n_epochs=E, in_epoch_stride=n * es, in_pool=pool,
-                 out_epoch_stride=n * es)
-        assert plan.status()["code"] == 0
-        for e in range(E):
-            want = collectives.allreduce(pool_np[e % pool], dtype)[0]
-            for r in range(R):
-                got = outs[r][e].cpu().numpy().view(want.dtype)
-                assert bits_equal(got, want), (rep, e, r)
-        for o in outs:
-            o.zero_()
-    plan.free()
-
-
-def test_oneshot_multicast_with_uneven_consumer_counts():
-    # two names: one summed to all 8 ranks, one to ranks 0..3 only; clusters of 4 divide
-    # both consumer counts (8 does not), and every output matches the oracle bit for bit
-    R, h = 8, 6 * 1024 + 16
-    i = [(r, 0, h, 0) for r in range(R)] + [(r, h, h, 1) for r in range(R)]
-    o = [(r, 0, h, 0) for r in range(R)] + [(r, h, h, 1) for r in range(4)]
-    il, ol = [2 * h] * R, [2 * h] * R
-    nm = namings.Naming(R, "sum", "bf16", il, namings.segs(i), ol, namings.segs(o))
-    rng = synth.seeded_rng(85)
-    xs = [gen("uniform", rng, n, "bf16") for n in il]
-    assert cdc.Plan(nm, zero_copy=1, tma_min_bytes=1, bulk_cluster=8).info.bulk_cluster == 0
-    plan = cdc.Plan(nm, zero_copy=1, tma_min_bytes=1, bulk_cluster=4)
-    assert plan.info.bulk_cluster == 4
-    plan.free()
-    got, init = run_once(nm, xs, zero_copy=1, tma_min_bytes=1, bulk_cluster=4)
-    want = oracle_outputs(nm, xs, init)
-    for g, w in zip(got, want):
-        assert bits_equal(g, w)
-
-
 def test_bulk_plan_with_misaligned_buffers_falls_back_and_stays_exact():
     R, n = 4, 1 << 20
     rng = synth.seeded_rng(83)

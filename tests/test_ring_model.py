@@ -316,171 +316,3 @@ def test_the_bulk_model_catches_a_table_too_small():
         except AssertionError:
             caught += 1
     assert caught > 0
-
-
-# ------------------------------------------------------------ multicast clusters
-
-class SignedMBar(MBar):
-    """An mbarrier whose transaction count may go below zero within a phase (the PTX ISA
-    allows -(2^20 - 1)..2^20 - 1): a peer's bytes can land before this CTA's own
-    expect-tx of the same phase."""
-
-    def complete_tx(self, nbytes):
-        self.tx -= nbytes
-        self._check()
-
-
-class ClusterRing:
-    """The bulk ring's multicast variant on one cluster of C CTAs. Every CTA runs:
-    - a producer: tile k into stage k % S once its own consumers released the stage's
-      previous tile (empty), then arms full[s] with the tile's bytes and arrives on ready[s]
-      of every CTA of the cluster;
-    - an issuer: once its own ready[s] saw all C arrivals, one multicast copy of each piece
-      j with j % C == its rank, landing in stage s of every CTA (separately, in any order);
-    - consumers: wait full[s], check every piece of the stage is tile k's, release.
-    The tiles of a table entry are resolved in batches of 32 by the producer, as in the
-    unclustered ring; the issuer reads the entry after its ready wait. The producer ends
-    with a plain arrival on the next stage's full barrier (the consumers' end marker)."""
-
-    def __init__(self, C, S, ntiles, nsrc, consumers, seed, mutant=None, entries=64):
-        self.rnd = random.Random(seed)
-        self.C, self.S, self.ntiles, self.nsrc = C, S, ntiles, nsrc
-        self.ncons, self.mutant, self.entries = consumers, mutant, entries
-        ready_count = 1 if mutant == "ready counts only this CTA" else C
-        self.full = [[SignedMBar(1) for _ in range(S)] for _ in range(C)]
-        self.empty = [[MBar(consumers) for _ in range(S)] for _ in range(C)]
-        self.ready = [[MBar(ready_count) for _ in range(S)] for _ in range(C)]
-        self.slot = [[[None] * nsrc for _ in range(S)] for _ in range(C)]   # tile held
-        self.readers = [[set() for _ in range(S)] for _ in range(C)]
-        self.table = [[None] * entries for _ in range(C)]
-        self.tneed = [dict() for _ in range(C)]   # entry -> roles still to read it
-        self.final = [None] * C
-        self.flying = []            # (dest CTA, stage, piece, tile)
-        self.got = [[[] for _ in range(consumers)] for _ in range(C)]
-
-    def producer(self, d):
-        k = s = lap = 0
-        while k < self.ntiles:
-            batch = min(32, self.ntiles - k)
-            for i in range(batch):
-                e = (k + i) % self.entries
-                assert not self.tneed[d].get(e), ("table entry rewritten while needed", d, k + i)
-                self.table[d][e] = k + i
-            yield
-            for _ in range(batch):
-                while self.mutant != "no release wait" and not self.empty[d][s].done((lap & 1) ^ 1):
-                    yield
-                self.tneed[d][k % self.entries] = {"issuer"} | set(range(self.ncons))
-                self.full[d][s].expect_tx(4096 * self.nsrc)
-                targets = [d] if self.mutant == "ready counts only this CTA" else range(self.C)
-                for p in targets:
-                    self.ready[p][s].arrive()
-                    yield
-                k += 1
-                s += 1
-                if s == self.S:
-                    s, lap = 0, lap + 1
-        while not self.empty[d][s].done((lap & 1) ^ 1):
-            yield
-        self.final[d] = k
-        self.full[d][s].arrive()
-
-    def issuer(self, d):
-        s = lap = 0
-        for k in range(self.ntiles):
-            while self.mutant != "issuer ignores ready" and not self.ready[d][s].done(lap & 1):
-                yield
-            e = k % self.entries
-            if self.mutant == "issuer ignores ready":
-                while self.table[d][e] != k:   # (at least wait for the entry)
-                    yield
-            assert self.table[d][e] == k, ("issuer read a stale entry", d, k)
-            self.tneed[d].get(e, set()).discard("issuer")
-            for j in range(d % self.C, self.nsrc, self.C):
-                for p in range(self.C):
-                    self.flying.append((p, s, j, k))
-            s += 1
-            if s == self.S:
-                s, lap = 0, lap + 1
-            yield
-
-    def consumer(self, d, c):
-        k = s = lap = 0
-        while True:
-            while not self.full[d][s].done(lap & 1):
-                yield
-            if self.final[d] is not None and k >= self.final[d]:
-                return
-            assert self.slot[d][s] == [k] * self.nsrc, ("stage read before its pieces", d, k)
-            e = k % self.entries
-            assert self.table[d][e] == k
-            self.tneed[d][e].discard(c)
-            self.got[d][c].append(k)
-            self.readers[d][s].discard((c, k))
-            self.empty[d][s].arrive()
-            k += 1
-            s += 1
-            if s == self.S:
-                s, lap = 0, lap + 1
-            yield
-
-    def land_one(self):
-        p, s, j, k = self.flying.pop(self.rnd.randrange(len(self.flying)))
-        assert not self.readers[p][s], ("stage overwritten while read", p, s, k)
-        self.slot[p][s][j] = k
-        if all(x == k for x in self.slot[p][s]):
-            self.readers[p][s] = {(c, k) for c in range(self.ncons)}
-        self.full[p][s].complete_tx(4096)
-
-
-def simulate_cluster(C, S, ntiles, nsrc, consumers, seed, mutant=None, entries=64):
-    m = ClusterRing(C, S, ntiles, nsrc, consumers, seed, mutant, entries)
-    live = []
-    for d in range(C):
-        live += [m.producer(d), m.issuer(d)] + [m.consumer(d, c) for c in range(consumers)]
-    steps = 0
-    while live:
-        steps += 1
-        assert steps < 600000, "no progress"
-        if m.flying and m.rnd.random() < 0.3:
-            m.land_one()
-            continue
-        g = m.rnd.choice(live)
-        try:
-            next(g)
-        except StopIteration:
-            live.remove(g)
-    assert not m.flying
-    for d in range(C):
-        for c in range(consumers):
-            assert m.got[d][c] == list(range(ntiles)), (d, c)
-
-
-@pytest.mark.parametrize("seed", range(40))
-def test_cluster_ring_orders_every_stage(seed):
-    rnd = random.Random(3000 + seed)
-    C = rnd.choice([2, 4, 8])
-    simulate_cluster(C, rnd.choice([2, 3, 6]), rnd.choice([0, 1, 5, 33, 70]),
-                     rnd.choice([C, 8]), rnd.choice([1, 2]), seed)
-
-
-@pytest.mark.parametrize("mutant", ["no release wait", "issuer ignores ready",
-                                    "ready counts only this CTA"])
-def test_the_cluster_model_catches_a_missing_wait(mutant):
-    caught = 0
-    for seed in range(30):
-        try:
-            simulate_cluster(4, 2, 40, 8, 2, seed, mutant)
-        except AssertionError:
-            caught += 1
-    assert caught > 0, mutant
-
-
-def test_the_cluster_model_catches_a_table_too_small():
-    caught = 0
-    for seed in range(30):
-        try:
-            simulate_cluster(2, 8, 100, 8, 2, seed, entries=8)
-        except AssertionError:
-            caught += 1
-    assert caught > 0
