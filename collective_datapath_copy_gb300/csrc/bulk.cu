@@ -8,6 +8,13 @@
 // the stage. The ring keeps up to `stages` tiles of loads in flight per SM independently of
 // register pressure, which is what a streaming copy/reduce needs to reach HBM bandwidth.
 //
+// The ring is launched as a programmatic dependent of the previous kernel in its stream: a
+// CTA initialises its barriers and resolves its first batch of tile records, which are the
+// plan's and never written by a run, while the previous kernel finishes, and its producer
+// waits for that kernel's completion (griddep_wait) before it touches the plan's counters or
+// any caller buffer. Once a CTA's producer has issued its last tile, the CTA lets the next
+// kernel start (on the SMs this grid releases).
+//
 // Every mbarrier wait is bounded by the plan's spin limit; on expiry the CTA records
 // COLL_ETIMEDOUT in the plan status, waits (bounded) for the bulk copies it issued, and
 // returns.
@@ -125,6 +132,12 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
     uint64_t tA = 0, tB = 0;
     bool haveA = false, haveB = false;
     uint4 wA[9], wB[9];  // the 144-byte records
+    bool waited = false;  // the previous kernel in the stream has completed
+    auto dep_wait = [&]() {
+      if (!waited) griddep_wait();
+      waited = true;
+    };
+    if (dyn) dep_wait();  // (a claimed first batch reads the plan's counter)
     next_batch(tA, haveA);
     load_record(tA, haveA, wA);
     while (!stop) {
@@ -161,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
         }
       }
       __syncwarp();  // the batch's table entries are written before any lane reads them
+      dep_wait();    // before the plan's counters and the caller's buffers are touched
       next_batch(tB, haveB);
       load_record(tB, haveB, wB);
       for (uint32_t i = 0; i < batch; ++i, ++k) {
@@ -200,7 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
     // The end: tile k does not exist. Once its stage is free, record k and complete the
     // stage's barrier with a plain arrival (no bytes), so that the consumers waiting for
     // tile k wake, read the count and stop.
+    dep_wait();  // (a CTA without tiles still updates the plan's counters at the end)
     if (lane == 0) {
+      griddep_launch();  // every copy of this CTA is issued: the next kernel may start
       bool ok = !stop && !s_abort;
       if (ok) ok = mbar_wait(&empty[s], (lap & 1u) ^ 1u, a.spin_ns, &s_abort);
       s_final = k;
@@ -295,7 +311,17 @@ cudaError_t launch_bulk(int op, int dtype, const ZcArgs &a, int ctas, cudaStream
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   void *args[] = {(void *)&la};
-  return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, smem, s);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace coll

@@ -37,7 +37,11 @@ __device__ __forceinline__ uint4 zc_load(const char *p) {
 // One warp per tile. Lane k holds the pointer of producer k and of consumer k for the
 // tile (up to 32 each); the vector loops fetch them with shuffles. Tiles with more than 32
 // producers or consumers, or with an address not 16-byte aligned, take the element-wise
-// path (same arithmetic, same order).
+// path (same arithmetic, same order). The kernel is launched as a programmatic dependent of
+// the previous kernel in its stream: each CTA lets the next kernel start at once (which waits
+// for this one before it touches caller buffers), and each warp reads its first tile's
+// record, the plan's, before it waits for the previous kernel (griddep_wait) and touches
+// the caller's buffers.
 template <int KIND, bool KEEP, bool TREE>
 __global__ void __launch_bounds__(256, TREE ? 2 : 3) zc_kernel(const ZcArgs a) {
   const uint32_t lane = threadIdx.x & 31u;
@@ -45,6 +49,8 @@ __global__ void __launch_bounds__(256, TREE ? 2 : 3) zc_kernel(const ZcArgs a) {
   const uint64_t nw = ((uint64_t)gridDim.x * blockDim.x) >> 5;
   const uint64_t total = (uint64_t)a.ntiles * a.n_epochs;
   constexpr uint64_t kOffMask = (1ull << 56) - 1u;
+  griddep_launch();
+  bool waited = false;  // the previous kernel in the stream has completed
   for (uint64_t t = gw; t < total; t += nw) {
     const uint32_t e = (uint32_t)(t / a.ntiles);
     const uint32_t ti = (uint32_t)(t - (uint64_t)e * a.ntiles);
@@ -69,6 +75,8 @@ __global__ void __launch_bounds__(256, TREE ? 2 : 3) zc_kernel(const ZcArgs a) {
       nsrc = job.nsrc;
       ndst = job.ndst;
     }
+    if (!waited) griddep_wait();
+    waited = true;
     const int64_t ioff = (int64_t)(e % (uint32_t)a.in_pool) * a.in_stride + (int64_t)start;
     const int64_t ooff = (int64_t)e * a.out_stride + (int64_t)start;
     const char *sp = nullptr;
@@ -1340,25 +1348,36 @@ cudaError_t launch_zero_copy(int op, int dtype, int keep, const ZcArgs &a, int c
   if (total == 0) return cudaSuccess;
   const uint64_t need = (total + 7) / 8;  // 8 warps per CTA
   const int grid = (int)((uint64_t)ctas < need ? (uint64_t)ctas : need);
-  const dim3 block(256);
+  const void *fn;
   if (a.tree && kind != 0) {
     switch (kind * 2 + (keep ? 1 : 0)) {
-      case 2: zc_kernel<1, false, true><<<grid, block, 0, s>>>(a); break;
-      case 3: zc_kernel<1, true, true><<<grid, block, 0, s>>>(a); break;
-      case 4: zc_kernel<2, false, true><<<grid, block, 0, s>>>(a); break;
-      default: zc_kernel<2, true, true><<<grid, block, 0, s>>>(a); break;
+      case 2: fn = (const void *)zc_kernel<1, false, true>; break;
+      case 3: fn = (const void *)zc_kernel<1, true, true>; break;
+      case 4: fn = (const void *)zc_kernel<2, false, true>; break;
+      default: fn = (const void *)zc_kernel<2, true, true>; break;
     }
-    return cudaGetLastError();
+  } else {
+    switch (kind * 2 + (keep ? 1 : 0)) {
+      case 0: fn = (const void *)zc_kernel<0, false, false>; break;
+      case 1: fn = (const void *)zc_kernel<0, true, false>; break;
+      case 2: fn = (const void *)zc_kernel<1, false, false>; break;
+      case 3: fn = (const void *)zc_kernel<1, true, false>; break;
+      case 4: fn = (const void *)zc_kernel<2, false, false>; break;
+      default: fn = (const void *)zc_kernel<2, true, false>; break;
+    }
   }
-  switch (kind * 2 + (keep ? 1 : 0)) {
-    case 0: zc_kernel<0, false, false><<<grid, block, 0, s>>>(a); break;
-    case 1: zc_kernel<0, true, false><<<grid, block, 0, s>>>(a); break;
-    case 2: zc_kernel<1, false, false><<<grid, block, 0, s>>>(a); break;
-    case 3: zc_kernel<1, true, false><<<grid, block, 0, s>>>(a); break;
-    case 4: zc_kernel<2, false, false><<<grid, block, 0, s>>>(a); break;
-    default: zc_kernel<2, true, false><<<grid, block, 0, s>>>(a); break;
-  }
-  return cudaGetLastError();
+  ZcArgs la = a;
+  void *args[] = {(void *)&la};
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 static const void *engine_fn(int kind, bool gemv, bool ll, bool pull, int fp = 0) {

@@ -93,6 +93,17 @@ __device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t
       : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may
+// start before the previous kernel in its stream has finished. griddep_wait() returns once
+// that kernel has completed and its memory operations are visible; griddep_launch() lets the
+// next kernel start as soon as every CTA of this grid has called it or exited.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Tensor copy of one 2-D box (the map's box size) at element coordinates (x, y) from global
 // memory to this CTA's shared memory (128-byte aligned); completion is counted on `bar`'s
 // transaction count. x times the element size must be a multiple of 16 bytes. A slot that
