@@ -891,7 +891,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
   const bool chained = fast ? fp_chain : a.chain && a.rank_done;
   const bool stagger = !fast && (a.inject_flags & COLL_INJECT_STAGGER);
   uint32_t n_checks = 0, n_retries = 0;
-  uint32_t win = a.spec_delay_ns;  // the speculation window of this warp (ns)
+  uint32_t win = a.spec_delay_ns << 3;  // the speculation window of this warp (ns / 8)
   bool failed = false;
   uint64_t gpiece = 0;  // fused producer: pieces computed so far
 
@@ -1140,7 +1140,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
         // The speculation window: loads issued right after this warp's own notify mostly
         // race the peers' stores of the same epoch and fail validation; a short wait first
         // trades a little latency for fewer reloads.
-        if (win) spin_ns(win);
+        if (win >= 8u) spin_ns(win >> 3);
         res = spec_attempt<KIND>(xb, u.nbytes, n, lane, active, tagged, pf, !relaxed,
                                  !pause_consumer, f, myh, side, nx,
                                  pipelined ? (su.nbytes >> 4) : 0u, nh);
@@ -1161,11 +1161,13 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
           ok = tags_match(f, myh, n, E, lane);
         }
         ++n_checks;
-        // adaptive window: 4 ns shorter after a passed first attempt, 40 ns longer after one
-        // that failed and passed at the first reload (a race with the peers' stores, which a
-        // wider window avoids; a producer that is late shows as several reloads instead, and
-        // a window does not help there), so that about one first attempt in eleven fails
-        if (a.spec_adapt && ok) win = win > 4u ? win - 4u : 0u;
+        // adaptive window (in eighths of a ns): 1/8 ns shorter after a passed first attempt,
+        // 2 ns longer after one that failed and passed at the first reload (a race with the
+        // peers' stores, which a wider window avoids; a producer that is late shows as
+        // several reloads instead, and a window does not help there), so that about one
+        // first attempt in seventeen fails; small steps keep the window close to where it
+        // balances (steps of 4 and 40 ns measured 4 % slower per epoch)
+        if (a.spec_adapt && ok) win = win > 0u ? win - 1u : 0u;
         if (ok) {
           have = true;
         } else {
@@ -1182,7 +1184,7 @@ __global__ void __launch_bounds__(GEMV ? kGemvThreads : 32, 1)
               fe = flag_epoch(f);
               if (tags_match(f, myh, n, E, lane)) {
                 have = true;
-                if (a.spec_adapt && k == 0) win = win < 1960u ? win + 40u : 2000u;
+                if (a.spec_adapt && k == 0) win = win < (1998u << 3) ? win + 16u : (2000u << 3);
                 break;
               }
               const bool late = (globaltimer() - t0 > a.spin_ns) ||

@@ -162,11 +162,11 @@ typedef struct {
                                mostly race the peers' stores of the same epoch and are
                                retried): -1 = the check's default: for
                                COLL_SPEC_TAGGED_RELAXED a window per warp that starts at
-                               200 ns, grows by 40 ns after a first attempt that failed
-                               and passed at the first reload (a race) and shrinks by 4 ns
-                               after one that passed (about one in eleven then fails), no
-                               window for the other checks; 0..100000 = that many ns,
-                               fixed                                                     */
+                               200 ns, grows by 2 ns after a first attempt that failed
+                               and passed at the first reload (a race) and shrinks by
+                               1/8 ns after one that passed (about one in seventeen then
+                               fails), no window for the other checks; 0..100000 = that
+                               many ns, fixed                                            */
   int32_t reduce_order;     /* COLL_ORDER_*; zero-copy plans only                      */
   int32_t reserved3;        /* must be 0                                                */
 } coll_config_t;
