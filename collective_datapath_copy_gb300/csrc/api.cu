@@ -110,7 +110,7 @@ bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
   return a0 < b1 && b0 < a1;
 }
 
-// The driver's tensor-map encoder, looked up once through the runtime (no link to the
+// The CUDA driver API's tensor-map encoder, looked up once through the runtime (no link to the
 // driver library).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
