@@ -380,7 +380,7 @@ static int run_impl(coll_plan_s *p, void *const *in, void *const *out, int n_epo
       a.slot_bytes = c.bulk_slot;
       a.stages = c.bulk_stages;
       a.maxsrc = c.bulk_maxsrc;
-      a.dyn_tail = c.bulk_tail ? 1u : 0u;
+      a.dyn_tail = c.bulk_tail;
       err = coll::launch_bulk(c.op, c.dtype, a, c.cfg.ctas ? c.cfg.ctas : p->num_sms, s);
     } else {
       const int ctas = c.cfg.ctas ? c.cfg.ctas : 3 * p->num_sms;

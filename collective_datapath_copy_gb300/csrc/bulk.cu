@@ -32,7 +32,7 @@ namespace {
 constexpr uint32_t kConsumerWarps = 8;
 constexpr unsigned FULLW = 0xFFFFFFFFu;
 constexpr uint32_t kThreads = 32 * (kConsumerWarps + 1);
-constexpr uint32_t kClaim = 2;   // tiles per claim of the dynamic tail
+constexpr uint32_t kClaim = 2;   // tiles per claim of the dynamic tail (the least, if guided)
 constexpr uint32_t kTable = 64;  // resolved tiles held (>= 32 + the ring's stages)
 
 // A resolved tile: its sources and destinations as pointers, sizes and counts. The
@@ -89,16 +89,26 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
   uint32_t consumed = 0;
   if (warp == 0) {
     // Producer warp. Tiles come in batches: first dealt round-robin (tile b + i * grid of
-    // the first static_tiles), then, for the tail, claimed kClaim at a time from a counter
-    // shared by the CTAs, so that SMs that run faster take more of the last tiles. Lane i
-    // resolves tile i of a batch from its record (one memory round trip per batch) into the
-    // table. Then, tile by tile: lane 0 waits for the stage to be free, records the tile's
-    // entry and the bytes to expect, and lanes j < nsrc each issue source j's bulk copy.
+    // the first static_tiles), then, for the tail, claimed from a counter shared by the
+    // CTAs, so that SMs that run faster take more of the last tiles. A claim takes kClaim
+    // tiles or, guided, about half of this CTA's fair share of the tail still unclaimed
+    // (kClaim to 32 tiles): fewer claims, each covering the memory round trips of the
+    // next one. Lane i resolves tile i of a batch from its record (one memory round trip
+    // per batch) into the table. Then, tile by tile: lane 0 waits for the stage to be
+    // free, records the tile's entry and the bytes to expect, and lanes j < nsrc each
+    // issue source j's bulk copy.
     uint32_t k = 0, s = 0, lap = 0;
     bool stop = false, dyn = a.static_tiles == 0;
     uint64_t t0 = blockIdx.x;
-    uint32_t cnext = 0;      // lane 0: the claim for the batch after this one, taken ahead
+    uint32_t cnext = 0, nnext = 0;  // lane 0: the claim for the batch after this one, taken ahead
     bool cnext_valid = false;
+    const uint64_t tail_tiles = total - a.static_tiles;
+    auto claim_size = [&](uint64_t claimed) -> uint32_t {
+      if (a.dyn_tail != 2u) return kClaim;
+      const uint64_t left = claimed < tail_tiles ? tail_tiles - claimed : 0u;
+      const uint64_t q = left / (2ull * gridDim.x);
+      return q < kClaim ? kClaim : (q > 32u ? 32u : (uint32_t)q);
+    };
     // The tiles of the next batch (lane i: one tile), one batch ahead of their issue, so
     // that the claim's and the records' memory round trips overlap the current batch.
     auto next_batch = [&](uint64_t &t, bool &have) {
@@ -110,15 +120,23 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
         if (!__any_sync(FULLW, have)) dyn = true;
       }
       if (dyn) {
-        uint32_t c = 0;
+        uint32_t c = 0, n = 0;
         if (lane == 0) {
-          c = cnext_valid ? cnext : atomicAdd(&a.st->tail_claim, kClaim);
-          cnext = atomicAdd(&a.st->tail_claim, kClaim);  // (its value is used next time)
+          if (cnext_valid) {
+            c = cnext;
+            n = nnext;
+          } else {
+            n = claim_size(0);
+            c = atomicAdd(&a.st->tail_claim, n);
+          }
+          nnext = claim_size((uint64_t)c + n);
+          cnext = atomicAdd(&a.st->tail_claim, nnext);  // (its value is used next time)
           cnext_valid = true;
         }
         c = __shfl_sync(FULLW, c, 0);
+        n = __shfl_sync(FULLW, n, 0);
         t = a.static_tiles + c + lane;
-        have = lane < kClaim && t < total;
+        have = lane < n && t < total;
       }
     };
     auto load_record = [&](uint64_t t, bool have, uint4 w[9]) {
@@ -299,10 +317,13 @@ cudaError_t launch_bulk(int op, int dtype, const ZcArgs &a, int ctas, cudaStream
   if (total == 0) return cudaSuccess;
   const int grid = (int)((uint64_t)ctas < total ? (uint64_t)ctas : total);
   const uint32_t smem = bulk_smem_bytes(a.stages, a.maxsrc, a.slot_bytes);
-  // whole rounds of four fifths of the tiles are dealt round-robin and the rest claimed, or
-  // (many-to-one sums) every tile dealt round-robin
+  // Whole rounds of four fifths of the tiles are dealt round-robin and the rest claimed,
+  // two at a time (dyn_tail 1) or in guided sizes (dyn_tail 2), else every tile is dealt
+  // round-robin. A guided tail pays for its claims only in long runs: with fewer than 64
+  // tiles per CTA every tile is dealt.
   ZcArgs la = a;
-  la.static_tiles = a.dyn_tail ? total * 4 / 5 / (uint64_t)grid * (uint64_t)grid : total;
+  const bool tail = a.dyn_tail == 1u || (a.dyn_tail == 2u && total >= 64ull * (uint64_t)grid);
+  la.static_tiles = tail ? total * 4 / 5 / (uint64_t)grid * (uint64_t)grid : total;
   if (total - la.static_tiles >= (1ull << 31)) la.static_tiles = total;  // (claim counter)
   const void *fn;
   if (op == COLL_OP_COPY) fn = (const void *)bulk_kernel<0, false>;

@@ -116,7 +116,8 @@ struct coll_compiled {
   uint32_t bulk_slot = 0;     // bytes of one staged piece (= tile size)
   uint32_t bulk_maxsrc = 0;   // slots per stage
   uint32_t bulk_stages = 0;   // stages in the shared-memory ring
-  bool bulk_tail = false;     // claim the last tiles dynamically (see bulk.cu)
+  uint32_t bulk_tail = 0;     // claim the last tiles dynamically: 1 two at a time, 2 in
+                              // guided sizes (see bulk.cu)
   uint64_t xpar_bytes = 0;  // exchange bytes per parity
   uint64_t rpar_bytes = 0;  // two-shot pull: reduced-piece bytes per parity
   uint32_t n_pflag = 0, n_cflag = 0, n_dflag = 0;

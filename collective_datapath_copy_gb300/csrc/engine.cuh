@@ -32,7 +32,8 @@ struct ZcArgs {
   uint32_t maxsrc;        // bulk kernel: slots per stage
   uint32_t tree;          // 1: pairwise (tree) summation order within groups of 8
   uint64_t static_tiles;  // bulk kernel: tiles dealt round-robin; the rest are claimed
-  uint32_t dyn_tail;      // bulk kernel: 1 = claim the last fifth of the tiles dynamically
+  uint32_t dyn_tail;      // bulk kernel: claim the last fifth of the tiles dynamically,
+                          // 1: two at a time, 2: in guided sizes (long runs only)
   uint32_t pad2;
 };
 

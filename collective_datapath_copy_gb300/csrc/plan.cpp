@@ -239,9 +239,11 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
       const uint64_t stage = (uint64_t)maxsrc * T;
       c.bulk_stages = (uint32_t)std::max<uint64_t>(2, std::min<uint64_t>(8, (192u << 10) / stage));
       // Jobs with at least as many consumers as producers finish faster when the ring
-      // claims its last tiles dynamically; many-to-one sums (reduce-scatter, reduce to
-      // root, one-shot all-reduce) are faster with every tile dealt round-robin (measured).
-      c.bulk_tail = maxdst >= maxsrc;
+      // claims its last tiles two at a time. Many-to-one sums that read each input once
+      // (reduce-scatter, reduce to root) lose with such small claims and gain, in long
+      // runs, with guided ones; the one-shot all-reduce, whose inputs are re-read, deals
+      // every tile round-robin (all measured).
+      c.bulk_tail = maxdst >= maxsrc ? 1u : (c.zc_keep ? 0u : 2u);
     } else if (!T) {
       // One warp per tile: the largest power of two (512 B .. 32 KiB) that still gives
       // about four tiles per resident warp (32 per SM).

@@ -603,6 +603,34 @@ def test_prefill_allreduce_64mib_oneshot_and_twoshot_full():
         plan.free()
 
 
+@pytest.mark.parametrize("kind", ["reduce_scatter", "reduce_to_root"])
+def test_many_to_one_64mib_guided_tail_full(kind):
+    # 64 MiB per rank: long enough (over 64 tiles per CTA) for the ring to claim its last
+    # tiles in guided sizes; every output element against the oracle, twice (the second run
+    # starts from the claim counter the first run's last CTA reset)
+    R, n = 8, (64 << 20) // 2
+    rng = synth.seeded_rng(3)
+    xs = [synth.uniform_bf16(rng, n) for _ in range(R)]
+    if kind == "reduce_scatter":
+        want = collectives.reduce_scatter(xs, "bf16")
+    else:
+        want = [collectives.allreduce(xs, "bf16")[0]]
+    nm = getattr(namings, kind)(R, n, "bf16")
+    plan = cdc.Plan(nm, zero_copy=1)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert plan.info.bulk_tile_bytes > 0 and plan.info.n_tiles >= 64 * sms
+    ins = [to_dev(x, "bf16") for x in xs]
+    outs = [torch.empty(L, dtype=torch.int16, device="cuda") for L in nm.out_len]
+    for rep in range(2):
+        for o in outs:
+            o.fill_(0)
+        plan.run(ins, outs)
+        assert plan.status()["code"] == 0
+        for d, w in enumerate(want):
+            assert torch.equal(outs[d], to_dev(w, "bf16")), (kind, rep, d)
+    plan.free()
+
+
 def test_moe_dispatch_full_size():
     R, T, H, E, k = 8, 4096, 7168, 256, 8
     routing = synth.zipf_topk_routing(5, R, T, E, k, 1.1)

@@ -212,17 +212,21 @@ def test_the_model_catches_a_missing_wait(mutant):
 
 class BulkRing:
     """The zero-copy bulk ring of one CTA: the producer warp resolves tiles in batches (first
-    32 dealt round-robin at a time, then the tail claimed two at a time) into a table of
-    `entries` slots, the tile it issues k-th into entry k % entries, then issues each tile
-    into stage k % S once the consumer warps released that stage's previous tile; the
-    consumers take the tiles in order, read the tile's entry through the stage, release the
-    stage, and stop at the producer's end marker (a plain arrival on the next stage)."""
+    32 dealt round-robin at a time, then the tail claimed two at a time, or in the claims'
+    sizes `tail_batches`, 1 to 32 tiles) into a table of `entries` slots, the tile it issues
+    k-th into entry k % entries, then issues each tile into stage k % S once the consumer
+    warps released that stage's previous tile; the consumers take the tiles in order, read
+    the tile's entry through the stage, release the stage, and stop at the producer's end
+    marker (a plain arrival on the next stage)."""
 
-    def __init__(self, S, nstatic, ntail, consumers, seed, entries=64):
+    def __init__(self, S, nstatic, ntail, consumers, seed, entries=64, tail_batches=None):
         self.rnd = random.Random(seed)
         self.S, self.C, self.entries = S, consumers, entries
         self.batches = [min(32, nstatic - i) for i in range(0, nstatic, 32)]
-        self.batches += [min(2, ntail - i) for i in range(0, ntail, 2)]
+        if tail_batches is None:
+            tail_batches = [min(2, ntail - i) for i in range(0, ntail, 2)]
+        assert sum(tail_batches) == ntail and all(1 <= b <= 32 for b in tail_batches)
+        self.batches += list(tail_batches)
         self.ntiles = nstatic + ntail
         self.full = [MBar(1) for _ in range(S)]
         self.empty = [MBar(consumers) for _ in range(S)]
@@ -281,8 +285,8 @@ class BulkRing:
         self.full[s].complete_tx(4096)
 
 
-def simulate_bulk(S, nstatic, ntail, consumers, seed, entries=64):
-    m = BulkRing(S, nstatic, ntail, consumers, seed, entries)
+def simulate_bulk(S, nstatic, ntail, consumers, seed, entries=64, tail_batches=None):
+    m = BulkRing(S, nstatic, ntail, consumers, seed, entries, tail_batches)
     live = [m.producer()] + [m.consumer(c) for c in range(consumers)]
     steps = 0
     while live:
@@ -316,3 +320,79 @@ def test_the_bulk_model_catches_a_table_too_small():
         except AssertionError:
             caught += 1
     assert caught > 0
+
+
+# ------------------------------------------------------------ claims of the bulk ring's tail
+
+def claim_size(claimed, tail, grid, guided):
+    """Tiles one claim takes: two, or (guided) about half of a CTA's fair share of the tail
+    still unclaimed after `claimed`, from two to 32."""
+    if not guided:
+        return 2
+    q = max(tail - claimed, 0) // (2 * grid)
+    return min(max(q, 2), 32)
+
+
+def claim_tail(tail, grid, guided, seed):
+    """CTAs claiming the tail from one shared counter in a random interleaving. Each takes
+    its next claim one batch ahead (size from the position after its current claim) and
+    stops at the first claim that starts past the tail. Returns each CTA's batches."""
+    rnd = random.Random(seed)
+    counter = 0
+    state = [{"cur": None, "next": None, "done": False, "batches": []} for _ in range(grid)]
+
+    def take(n):
+        nonlocal counter
+        c = counter
+        counter += n
+        return c, n
+
+    while not all(st["done"] for st in state):
+        st = rnd.choice([x for x in state if not x["done"]])
+        if st["next"] is None:
+            st["cur"] = take(claim_size(0, tail, grid, guided))
+        else:
+            st["cur"] = st["next"]
+        c, n = st["cur"]
+        st["next"] = take(claim_size(c + n, tail, grid, guided))
+        got = [c + i for i in range(n) if c + i < tail]
+        if not got:
+            st["done"] = True
+        else:
+            st["batches"].append(got)
+    return [st["batches"] for st in state]
+
+
+@pytest.mark.parametrize("guided", [False, True])
+@pytest.mark.parametrize("seed", range(12))
+def test_tail_claims_cover_every_tile_once(guided, seed):
+    rnd = random.Random(3000 + seed)
+    grid = rnd.choice([1, 2, 7, 152])
+    tail = rnd.choice([0, 1, 2, 3, 63, 64 * grid, 5 * 64 * grid + 17])
+    per_cta = claim_tail(tail, grid, guided, seed)
+    seen = sorted(t for batches in per_cta for b in batches for t in b)
+    assert seen == list(range(tail))
+    for batches in per_cta:
+        for b in batches:
+            assert 1 <= len(b) <= 32 and b == list(range(b[0], b[0] + len(b)))
+            assert guided or len(b) <= 2
+
+
+def test_guided_claims_shrink_toward_the_end():
+    # early claims are large (fewer claims, each covering the next one's round trips), the
+    # last ones small (the tail stays balanced)
+    grid, tail = 152, 64 * 152 // 5
+    assert claim_size(0, tail, grid, True) == max(2, min(32, tail // (2 * grid)))
+    assert claim_size(tail - 10, tail, grid, True) == 2
+    sizes = [claim_size(c, 100000, 4, True) for c in list(range(0, 100000, 997)) + [99990]]
+    assert sizes == sorted(sizes, reverse=True) and sizes[0] == 32 and sizes[-1] == 2
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_bulk_ring_with_guided_tail_batches(seed):
+    # one CTA's share of a guided tail runs through the table and the stages like any batch
+    rnd = random.Random(4000 + seed)
+    per_cta = claim_tail(rnd.choice([40, 300, 2000]), rnd.choice([1, 3]), True, seed)
+    batches = [len(b) for b in per_cta[0]]
+    simulate_bulk(rnd.choice([2, 6, 8]), rnd.choice([0, 33, 64]), sum(batches), 8, seed,
+                  tail_batches=batches)
