@@ -877,6 +877,31 @@ def test_bulk_ring_epochs_over_an_input_pool():
         plan.free()
 
 
+def test_bulk_ring_guided_tail_across_epochs():
+    # a small reduce-scatter over 80 epochs: enough tiles in all (over 64 per CTA) for the
+    # ring to claim its tail in guided sizes, with claims that cross epoch boundaries
+    R, n, pool, E = 8, 1 << 16, 3, 80
+    rng = synth.seeded_rng(84)
+    pool_np = [[synth.uniform_bf16(rng, n) for _ in range(R)] for _ in range(pool)]
+    ins = [torch.stack([to_dev(pool_np[p][r], "bf16") for p in range(pool)]).contiguous()
+           for r in range(R)]
+    nm = namings.reduce_scatter(R, n, "bf16")
+    plan = cdc.Plan(nm, zero_copy=1, tma_min_bytes=1)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert plan.info.bulk_tile_bytes > 0 and plan.info.n_tiles * E >= 64 * sms
+    m = n // R
+    outs = [torch.zeros(E, m, dtype=torch.int16, device="cuda") for _ in range(R)]
+    wants = [collectives.reduce_scatter(pool_np[p], "bf16") for p in range(pool)]
+    for rep in range(2):
+        plan.run(ins, outs, n_epochs=E, in_epoch_stride=2 * n, in_pool=pool,
+                 out_epoch_stride=2 * m)
+        assert plan.status()["code"] == 0
+        for e in range(E):
+            for r in range(R):
+                assert bits_equal(from_dev(outs[r][e], "bf16"), wants[e % pool][r]), (rep, e, r)
+    plan.free()
+
+
 def test_bulk_plan_with_misaligned_buffers_falls_back_and_stays_exact():
     R, n = 4, 1 << 20
     rng = synth.seeded_rng(83)
