@@ -39,7 +39,7 @@ constexpr uint32_t kTable = 64;  // resolved tiles held (>= 32 + the ring's stag
 // producer warp resolves a batch of tiles (one per lane) into a table of kTable entries in
 // shared memory, the tile this CTA issues k-th into entry k % kTable; a stage records which
 // entry it holds. Entry k % kTable was last used by tile k - kTable, and issuing tile k - 1
-// waited for tile k - 1 - S to be released (S <= 8 stages): a batch of up to 32 tiles
+// waited for tile k - 1 - S to be released (S <= 12 stages): a batch of up to 32 tiles
 // starting at k only overwrites entries of released tiles.
 struct TileRec {
   const char *src[COLL_BULK_MAX_SRC];

@@ -307,7 +307,7 @@ def simulate_bulk(S, nstatic, ntail, consumers, seed, entries=64, tail_batches=N
 @pytest.mark.parametrize("seed", range(40))
 def test_bulk_ring_table_and_end_marker(seed):
     rnd = random.Random(2000 + seed)
-    simulate_bulk(rnd.choice([2, 3, 6, 8]), rnd.choice([0, 1, 31, 32, 33, 64, 100]),
+    simulate_bulk(rnd.choice([2, 3, 6, 8, 12]), rnd.choice([0, 1, 31, 32, 33, 64, 100]),
                   rnd.choice([0, 1, 2, 7, 40]), rnd.choice([1, 8]), seed)
 
 
@@ -394,5 +394,5 @@ def test_bulk_ring_with_guided_tail_batches(seed):
     rnd = random.Random(4000 + seed)
     per_cta = claim_tail(rnd.choice([40, 300, 2000]), rnd.choice([1, 3]), True, seed)
     batches = [len(b) for b in per_cta[0]]
-    simulate_bulk(rnd.choice([2, 6, 8]), rnd.choice([0, 33, 64]), sum(batches), 8, seed,
+    simulate_bulk(rnd.choice([2, 6, 8, 12]), rnd.choice([0, 33, 64]), sum(batches), 8, seed,
                   tail_batches=batches)
