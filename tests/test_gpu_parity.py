@@ -631,6 +631,26 @@ def test_many_to_one_64mib_guided_tail_full(kind):
     plan.free()
 
 
+@pytest.mark.parametrize("kind,mib", [("broadcast", 64), ("allgather", 16)])
+def test_multi_destination_copies_16k_tiles_full(kind, mib):
+    # jobs that write each byte to every rank run on 16 KiB tiles with up to 12 stages;
+    # every output byte against the oracle
+    R, n = 8, (mib << 20) // 2
+    rng = synth.seeded_rng(3)
+    xs = [synth.uniform_bf16(rng, n) for _ in range(R)]
+    want = collectives.broadcast(xs, 0) if kind == "broadcast" else collectives.allgather(xs)
+    nm = getattr(namings, kind)(R, n, "bf16")
+    plan = cdc.Plan(nm, zero_copy=1)
+    assert plan.info.bulk_tile_bytes == 16384
+    ins = [to_dev(x, "bf16") for x in xs]
+    outs = [torch.zeros(L, dtype=torch.int16, device="cuda") for L in nm.out_len]
+    plan.run(ins, outs)
+    assert plan.status()["code"] == 0
+    for d in range(R):
+        assert torch.equal(outs[d], to_dev(want[d], "bf16")), (kind, d)
+    plan.free()
+
+
 def test_moe_dispatch_full_size():
     R, T, H, E, k = 8, 4096, 7168, 256, 8
     routing = synth.zipf_topk_routing(5, R, T, E, k, 1.1)
