@@ -30,15 +30,17 @@ namespace coll {
 namespace {
 
 constexpr uint32_t kConsumerWarps = 8;
+constexpr uint32_t kProducerWarps = 2;  // warps issuing copies: tile k by warp k % 2
 constexpr unsigned FULLW = 0xFFFFFFFFu;
-constexpr uint32_t kThreads = 32 * (kConsumerWarps + 1);
+constexpr uint32_t kThreads = 32 * (kConsumerWarps + kProducerWarps);
 constexpr uint32_t kClaim = 2;   // tiles per claim of the dynamic tail (the least, if guided)
 constexpr uint32_t kTable = 64;  // resolved tiles held (>= 32 + the ring's stages)
 
-// A resolved tile: its sources and destinations as pointers, sizes and counts. The
-// producer warp resolves a batch of tiles (one per lane) into a table of kTable entries in
-// shared memory, the tile this CTA issues k-th into entry k % kTable; a stage records which
-// entry it holds. Entry k % kTable was last used by tile k - kTable, and issuing tile k - 1
+// A resolved tile: its sources and destinations as pointers, sizes and counts. Producer
+// warp 0 resolves a batch of tiles (one per lane) into a table of kTable entries in shared
+// memory, the tile this CTA issues k-th into entry k % kTable; a stage records which entry
+// it holds. Entry k % kTable was last used by tile k - kTable. Both producer warps have
+// issued every tile of a batch before the next batch is written, and issuing tile k - 1
 // waited for tile k - 1 - S to be released (S <= 12 stages): a batch of up to 32 tiles
 // starting at k only overwrites entries of released tiles.
 struct TileRec {
@@ -62,8 +64,9 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ TileRec table[kTable];
   __shared__ volatile uint32_t s_abort;
-  __shared__ uint32_t s_issued;
-  __shared__ volatile uint32_t s_final;  // tiles this CTA issues in all, once known
+  __shared__ uint32_t s_issued[kProducerWarps];  // per producer warp: 1 + its last tile issued
+  __shared__ volatile uint32_t s_batch;          // tiles of the batch warp 0 has published
+  __shared__ volatile uint32_t s_final;          // tiles this CTA issues in all, once known
   const uint32_t S = a.stages;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
   uint64_t *empty = full + S;
@@ -80,27 +83,31 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
       mbar_init(&empty[s], kConsumerWarps);
     }
     s_abort = 0;
-    s_issued = 0;
+    for (uint32_t p = 0; p < kProducerWarps; ++p) s_issued[p] = 0;
+    s_batch = 0;
     s_final = 0xFFFFFFFFu;
     mbar_init_fence();
   }
   __syncthreads();
 
   uint32_t consumed = 0;
-  if (warp == 0) {
-    // Producer warp. Tiles come in batches: first dealt round-robin (tile b + i * grid of
+  if (warp < kProducerWarps) {
+    // Producer warps. Tiles come in batches: first dealt round-robin (tile b + i * grid of
     // the first static_tiles), then, for the tail, claimed from a counter shared by the
     // CTAs, so that SMs that run faster take more of the last tiles. A claim takes kClaim
     // tiles or, guided, about half of this CTA's fair share of the tail still unclaimed
     // (kClaim to 32 tiles): fewer claims, each covering the memory round trips of the
-    // next one. Lane i resolves tile i of a batch from its record (one memory round trip
-    // per batch) into the table. Then, tile by tile: lane 0 waits for the stage to be
-    // free, records the tile's entry and the bytes to expect, and lanes j < nsrc each
-    // issue source j's bulk copy.
-    uint32_t k = 0, s = 0, lap = 0;
+    // next one. Warp 0 resolves a batch (lane i: tile i, from its record; one memory round
+    // trip per batch) into the table and publishes its size; then each warp issues the
+    // batch's tiles of its parity (k % 2), tile by tile: lane 0 waits for the stage to be
+    // free, records the tile's entry and the bytes to expect, and lanes j < nsrc each issue
+    // source j's bulk copy. A warp's bulk copies enter the copy engine one stage's worth at
+    // a time, so two issuing warps keep twice the copies moving. The two warps meet at a
+    // named barrier after each publication and after each batch's issue.
+    uint32_t k0 = 0;  // tiles of the CTA issued before the current batch
     bool stop = false, dyn = a.static_tiles == 0;
     uint64_t t0 = blockIdx.x;
-    uint32_t cnext = 0, nnext = 0;  // lane 0: the claim for the batch after this one, taken ahead
+    uint32_t cnext = 0, nnext = 0;  // warp 0, lane 0: the claim for the batch after this one
     bool cnext_valid = false;
     const uint64_t tail_tiles = total - a.static_tiles;
     auto claim_size = [&](uint64_t claimed) -> uint32_t {
@@ -149,53 +156,68 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
     };
     uint64_t tA = 0, tB = 0;
     bool haveA = false, haveB = false;
-    uint4 wA[9], wB[9];  // the 144-byte records
+    uint4 wA[9], wB[9];  // warp 0: the 144-byte records
     bool waited = false;  // the previous kernel in the stream has completed
     auto dep_wait = [&]() {
       if (!waited) griddep_wait();
       waited = true;
     };
-    if (dyn) dep_wait();  // (a claimed first batch reads the plan's counter)
-    next_batch(tA, haveA);
-    load_record(tA, haveA, wA);
-    while (!stop) {
-      const uint32_t batch = __popc(__ballot_sync(FULLW, haveA));
-      if (batch == 0) break;
-      if (haveA) {
-        const uint32_t e = (uint32_t)(tA / a.ntiles);
-        const uint64_t start = ((uint64_t)wA[0].y << 32) | wA[0].x;
-        TileRec &tr = table[(k + lane) % kTable];
-        tr.nbytes = wA[0].z;
-        tr.nsrc = wA[0].w & 0xFFFFu;
-        tr.ndst = wA[0].w >> 16;
-        const int64_t ioff = (int64_t)(e % (uint32_t)a.in_pool) * a.in_stride + (int64_t)start;
-        const int64_t ooff = (int64_t)e * a.out_stride + (int64_t)start;
-        constexpr uint64_t kOffMask = (1ull << 56) - 1u;
-        // references 0..7 are sources, 8..15 destinations; word q + 1 holds 2q and 2q + 1
+    if (warp == 0) {
+      if (dyn) dep_wait();  // (a claimed first batch reads the plan's counter)
+      next_batch(tA, haveA);
+      load_record(tA, haveA, wA);
+    }
+    for (;;) {
+      if (warp == 0) {
+        const uint32_t nhave = __popc(__ballot_sync(FULLW, haveA));
+        // (one lane reads the abort word, so that the warp takes one decision)
+        const bool halt = __shfl_sync(FULLW, (stop || s_abort) ? 1u : 0u, 0) != 0u;
+        const uint32_t batch = halt ? 0u : nhave;
+        if (haveA && batch) {
+          const uint32_t e = (uint32_t)(tA / a.ntiles);
+          const uint64_t start = ((uint64_t)wA[0].y << 32) | wA[0].x;
+          TileRec &tr = table[(k0 + lane) % kTable];
+          tr.nbytes = wA[0].z;
+          tr.nsrc = wA[0].w & 0xFFFFu;
+          tr.ndst = wA[0].w >> 16;
+          const int64_t ioff = (int64_t)(e % (uint32_t)a.in_pool) * a.in_stride + (int64_t)start;
+          const int64_t ooff = (int64_t)e * a.out_stride + (int64_t)start;
+          constexpr uint64_t kOffMask = (1ull << 56) - 1u;
+          // references 0..7 are sources, 8..15 destinations; word q + 1 holds 2q and 2q + 1
 #pragma unroll
-        for (uint32_t q = 0; q < 8; ++q) {
-          const uint64_t ra = ((uint64_t)wA[q + 1].y << 32) | wA[q + 1].x;
-          const uint64_t rb = ((uint64_t)wA[q + 1].w << 32) | wA[q + 1].z;
+          for (uint32_t q = 0; q < 8; ++q) {
+            const uint64_t ra = ((uint64_t)wA[q + 1].y << 32) | wA[q + 1].x;
+            const uint64_t rb = ((uint64_t)wA[q + 1].w << 32) | wA[q + 1].z;
 #pragma unroll
-          for (uint32_t h2 = 0; h2 < 2; ++h2) {
-            const uint64_t r = h2 ? rb : ra;
-            const uint32_t i = 2 * q + h2;
-            if (i < COLL_BULK_MAX_SRC) {
-              tr.src[i] = i < tr.nsrc ? a.ptr.in[(uint32_t)(r >> 56)] + (r & kOffMask) + ioff
-                                      : nullptr;
-            } else {
-              const uint32_t d = i - COLL_BULK_MAX_SRC;
-              tr.dst[d] = d < tr.ndst ? a.ptr.out[(uint32_t)(r >> 56)] + (r & kOffMask) + ooff
-                                      : nullptr;
+            for (uint32_t h2 = 0; h2 < 2; ++h2) {
+              const uint64_t r = h2 ? rb : ra;
+              const uint32_t i = 2 * q + h2;
+              if (i < COLL_BULK_MAX_SRC) {
+                tr.src[i] = i < tr.nsrc ? a.ptr.in[(uint32_t)(r >> 56)] + (r & kOffMask) + ioff
+                                        : nullptr;
+              } else {
+                const uint32_t d = i - COLL_BULK_MAX_SRC;
+                tr.dst[d] = d < tr.ndst ? a.ptr.out[(uint32_t)(r >> 56)] + (r & kOffMask) + ooff
+                                        : nullptr;
+              }
             }
           }
         }
+        __syncwarp();  // the batch's table entries are written before it is published
+        if (batch) dep_wait();  // before the plan's counters and the caller's buffers are touched
+        if (lane == 0) s_batch = batch;
       }
-      __syncwarp();  // the batch's table entries are written before any lane reads them
-      dep_wait();    // before the plan's counters and the caller's buffers are touched
-      next_batch(tB, haveB);
-      load_record(tB, haveB, wB);
-      for (uint32_t i = 0; i < batch; ++i, ++k) {
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kProducerWarps) : "memory");  // published
+      const uint32_t batch = s_batch;
+      if (batch == 0) break;
+      if (warp == 0) {
+        next_batch(tB, haveB);
+        load_record(tB, haveB, wB);
+      } else {
+        dep_wait();  // (already satisfied: warp 0 waited before publishing)
+      }
+      for (uint32_t k = k0 + ((k0 & 1u) != warp ? 1u : 0u); k < k0 + batch && !stop; k += 2) {
+        const uint32_t s = k % S, lap = k / S;
         bool ok = true;
         if (lane == 0) ok = mbar_wait(&empty[s], (lap & 1u) ^ 1u, a.spin_ns, &s_abort);
         ok = __shfl_sync(FULLW, ok, 0);
@@ -213,35 +235,38 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
         if (lane == 0) {
           stile[s] = ent;
           mbar_expect_tx(&full[s], ns * nb);
-          s_issued = k + 1;
+          s_issued[warp] = k + 1;
         }
         __syncwarp();  // the bytes are expected before any copy can complete them
         if (lane < ns)
           bulk_load(data + (size_t)s * stage_bytes + (size_t)lane * a.slot_bytes, tr.src[lane], nb,
                     &full[s]);
-        if (++s == S) {
-          s = 0;
-          ++lap;
-        }
       }
-      tA = tB;
-      haveA = haveB;
+      k0 += batch;
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kProducerWarps) : "memory");  // batch issued
+      if (warp == 0) {
+        tA = tB;
+        haveA = haveB;
 #pragma unroll
-      for (uint32_t q = 0; q < 9; ++q) wA[q] = wB[q];
+        for (uint32_t q = 0; q < 9; ++q) wA[q] = wB[q];
+      }
     }
-    // The end: tile k does not exist. Once its stage is free, record k and complete the
+    // The end: tile k0 does not exist. Once its stage is free, record k0 and complete the
     // stage's barrier with a plain arrival (no bytes), so that the consumers waiting for
-    // tile k wake, read the count and stop.
-    dep_wait();  // (a CTA without tiles still updates the plan's counters at the end)
-    if (lane == 0) {
-      griddep_launch();  // every copy of this CTA is issued: the next kernel may start
-      bool ok = !stop && !s_abort;
-      if (ok) ok = mbar_wait(&empty[s], (lap & 1u) ^ 1u, a.spin_ns, &s_abort);
-      s_final = k;
-      if (ok) mbar_arrive(&full[s]);
+    // tile k0 wake, read the count and stop.
+    if (warp == 0) {
+      dep_wait();  // (a CTA without tiles still updates the plan's counters at the end)
+      if (lane == 0) {
+        griddep_launch();  // every copy of this CTA is issued: the next kernel may start
+        const uint32_t s = k0 % S, lap = k0 / S;
+        bool ok = !stop && !s_abort;
+        if (ok) ok = mbar_wait(&empty[s], (lap & 1u) ^ 1u, a.spin_ns, &s_abort);
+        s_final = k0;
+        if (ok) mbar_arrive(&full[s]);
+      }
     }
   } else {
-    const uint32_t ctid = threadIdx.x - 32;  // consumer thread index
+    const uint32_t ctid = threadIdx.x - 32 * kProducerWarps;  // consumer thread index
     const uint32_t slot_vec = a.slot_bytes >> 4;
     uint32_t k = 0, s = 0, lap = 0;
     for (;; ++k) {
@@ -287,12 +312,14 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const ZcArgs a) {
     }
   }
   __syncthreads();
-  if (s_abort && threadIdx.x == 32) {
+  if (s_abort && threadIdx.x == 32 * kProducerWarps) {
     // bulk copies issued but not consumed may still be landing in this CTA's shared
-    // memory: wait for them (bounded) before the CTA exits
+    // memory: wait for them (bounded) before the CTA exits. Warp p issued the tiles
+    // k = p (mod 2) below s_issued[p].
     const volatile uint32_t never = 0;
-    for (uint32_t k = consumed; k < s_issued; ++k)
-      mbar_wait(&full[k % S], (k / S) & 1u, 100000000ull, &never);
+    const uint32_t hi = s_issued[0] > s_issued[1] ? s_issued[0] : s_issued[1];
+    for (uint32_t k = consumed; k < hi; ++k)
+      if (k < s_issued[k & 1u]) mbar_wait(&full[k % S], (k / S) & 1u, 100000000ull, &never);
   }
   if (threadIdx.x == 0) {
     // the last CTA to finish zeroes the tail counters for the plan's next run

@@ -211,17 +211,20 @@ def test_the_model_catches_a_missing_wait(mutant):
 # ------------------------------------------------------------ zero-copy bulk ring
 
 class BulkRing:
-    """The zero-copy bulk ring of one CTA: the producer warp resolves tiles in batches (first
-    32 dealt round-robin at a time, then the tail claimed two at a time, or in the claims'
-    sizes `tail_batches`, 1 to 32 tiles) into a table of `entries` slots, the tile it issues
-    k-th into entry k % entries, then issues each tile into stage k % S once the consumer
-    warps released that stage's previous tile; the consumers take the tiles in order, read
-    the tile's entry through the stage, release the stage, and stop at the producer's end
-    marker (a plain arrival on the next stage)."""
+    """The zero-copy bulk ring of one CTA. Producer warp 0 resolves tiles in batches (first 32
+    dealt round-robin at a time, then the tail claimed two at a time, or in the claims' sizes
+    `tail_batches`, 1 to 32 tiles) into a table of `entries` slots, the tile the CTA issues
+    k-th into entry k % entries, and publishes the batch; then each of the `issuers` producer
+    warps issues the batch's tiles k with k % issuers == its index, each into stage k % S once
+    the consumer warps released that stage's previous tile; the producer warps meet at a
+    barrier after each publication and after each batch's issue. The consumers take the tiles
+    in order, read the tile's entry through the stage, release the stage, and stop at the end
+    marker (warp 0's plain arrival on the next stage)."""
 
-    def __init__(self, S, nstatic, ntail, consumers, seed, entries=64, tail_batches=None):
+    def __init__(self, S, nstatic, ntail, consumers, seed, entries=64, tail_batches=None,
+                 issuers=2, mutant=None):
         self.rnd = random.Random(seed)
-        self.S, self.C, self.entries = S, consumers, entries
+        self.S, self.C, self.entries, self.P, self.mutant = S, consumers, entries, issuers, mutant
         self.batches = [min(32, nstatic - i) for i in range(0, nstatic, 32)]
         if tail_batches is None:
             tail_batches = [min(2, ntail - i) for i in range(0, ntail, 2)]
@@ -236,32 +239,57 @@ class BulkRing:
         self.final = None
         self.copies = []
         self.got = [[] for _ in range(consumers)]
+        self.published = None   # size of the batch published for the current round
+        self.bar = [0, 0]       # arrivals at the producers' barrier, generation
+        self.issued = 0
 
-    def producer(self):
-        k = s = lap = 0
-        for batch in self.batches:
-            for i in range(batch):
-                e = (k + i) % self.entries
-                assert not self.readers.get(e), ("table entry rewritten while read", k + i)
-                self.table[e] = k + i
+    def barrier(self):
+        gen = self.bar[1]
+        self.bar[0] += 1
+        if self.bar[0] == self.P:
+            self.bar = [0, gen + 1]
+        while self.bar[1] == gen:
             yield
-            for i in range(batch):
+
+    def producer(self, w):
+        k0 = 0
+        for rnd in range(len(self.batches) + 1):
+            if w == 0:
+                batch = self.batches[rnd] if rnd < len(self.batches) else 0
+                for i in range(batch):
+                    e = (k0 + i) % self.entries
+                    assert not self.readers.get(e), ("table entry rewritten while read", k0 + i)
+                    self.table[e] = k0 + i
+                self.published = batch
+                yield
+            if self.mutant != "no publish barrier":
+                yield from self.barrier()
+            batch = self.published
+            if batch == 0:
+                break
+            for k in range(k0, k0 + batch):
+                if k % self.P != w:
+                    continue
+                s, lap = k % self.S, k // self.S
                 while not self.empty[s].done((lap & 1) ^ 1):
                     yield
                 e = k % self.entries
+                assert self.table[e] == k, ("table entry not yet written", k)
                 self.stile[s] = e
                 self.readers[e] = set(range(self.C))
                 self.full[s].expect_tx(4096)
                 self.copies.append(s)
-                k += 1
-                s += 1
-                if s == self.S:
-                    s, lap = 0, lap + 1
+                self.issued += 1
                 yield
-        while not self.empty[s].done((lap & 1) ^ 1):
-            yield
-        self.final = k
-        self.full[s].arrive()   # the end marker
+            k0 += batch
+            if self.mutant != "no issue barrier":
+                yield from self.barrier()
+        if w == 0:
+            s, lap = k0 % self.S, k0 // self.S
+            while not self.empty[s].done((lap & 1) ^ 1):
+                yield
+            self.final = k0
+            self.full[s].arrive()   # the end marker
 
     def consumer(self, c):
         k = s = lap = 0
@@ -285,9 +313,10 @@ class BulkRing:
         self.full[s].complete_tx(4096)
 
 
-def simulate_bulk(S, nstatic, ntail, consumers, seed, entries=64, tail_batches=None):
-    m = BulkRing(S, nstatic, ntail, consumers, seed, entries, tail_batches)
-    live = [m.producer()] + [m.consumer(c) for c in range(consumers)]
+def simulate_bulk(S, nstatic, ntail, consumers, seed, entries=64, tail_batches=None, issuers=2,
+                  mutant=None):
+    m = BulkRing(S, nstatic, ntail, consumers, seed, entries, tail_batches, issuers, mutant)
+    live = [m.producer(w) for w in range(issuers)] + [m.consumer(c) for c in range(consumers)]
     steps = 0
     while live:
         steps += 1
@@ -320,6 +349,27 @@ def test_the_bulk_model_catches_a_table_too_small():
         except AssertionError:
             caught += 1
     assert caught > 0
+
+
+@pytest.mark.parametrize("issuers", [1, 2])
+@pytest.mark.parametrize("seed", range(20))
+def test_bulk_ring_one_or_two_issuing_warps(issuers, seed):
+    rnd = random.Random(5000 + seed)
+    simulate_bulk(rnd.choice([2, 3, 6, 12]), rnd.choice([0, 1, 31, 33, 64, 100]),
+                  rnd.choice([0, 1, 2, 7, 40]), rnd.choice([1, 8]), seed, issuers=issuers)
+
+
+@pytest.mark.parametrize("mutant", ["no publish barrier", "no issue barrier"])
+def test_the_bulk_model_needs_both_producer_barriers(mutant):
+    # without the barrier after publication, warp 1 issues from entries not yet written;
+    # without the one after the issue, warp 0 rewrites entries of tiles still in the ring
+    caught = 0
+    for seed in range(60):
+        try:
+            simulate_bulk(12, 100, 40, 8, seed, issuers=2, mutant=mutant)
+        except (AssertionError, TypeError):
+            caught += 1
+    assert caught > 0, mutant
 
 
 # ------------------------------------------------------------ claims of the bulk ring's tail
