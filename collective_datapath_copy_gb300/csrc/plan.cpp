@@ -219,7 +219,10 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
     // Jobs that write each loaded byte to four or more destinations (broadcast,
     // all-gather, MoE dispatch) take longest per tile; their tiles are capped at 16 KiB,
     // which doubles the tiles per CTA for the same bytes in flight (measured: broadcast
-    // 64 MiB 0.85 -> 0.91, all-gather 16 MiB 0.89 -> 0.93).
+    // 64 MiB 0.85 -> 0.91, all-gather 16 MiB 0.89 -> 0.93). Plans whose inputs are re-read
+    // (one-shot sums) take most of their bytes from L2, where larger copies move faster:
+    // their stages hold 64 KiB (one-shot all-reduce 8 x 32 MiB 0.29 -> 0.34; the plans
+    // that stream from DRAM keep six stages of 32 KiB, which measured better for them).
     // The ring's stages are sized for the largest producer count; jobs with fewer
     // producers leave stage space idle, so the ring is used only when jobs fill at least
     // three quarters of it on average (uniform collectives); uneven ones (MoE combine)
@@ -233,8 +236,9 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
     if (c.bulk) {
       uint32_t p2 = 1;
       while (p2 < maxsrc) p2 *= 2;
-      const uint64_t cap = maxdst >= 4u * maxsrc ? std::min<uint64_t>(16384u, 32768u / p2)
-                                                 : 32768u / p2;
+      const uint64_t stage_cap = c.zc_keep ? 65536u : 32768u;
+      const uint64_t cap = maxdst >= 4u * maxsrc ? std::min<uint64_t>(16384u, stage_cap / p2)
+                                                 : stage_cap / p2;
       const uint64_t want = job_bytes / (4u * sms);
       T = 1024;
       while (T < cap && T * 2 <= want) T *= 2;
