@@ -1,8 +1,8 @@
 // Zero-copy datapath, bulk-copy (TMA) variant for large 16-byte-aligned plans, sm_103a.
 //
-// One persistent CTA per SM. Warp 0 is the producer: for each tile it issues one
-// cp.async.bulk (global -> shared, completion on an mbarrier) per producer segment into a
-// ring of shared-memory stages. Warps 1..8 are consumers: they wait for a stage, reduce the
+// One persistent CTA per SM. Warps 0 and 1 are the producers: for each tile one of them
+// issues one cp.async.bulk (global -> shared, completion on an mbarrier) per producer segment
+// into a ring of shared-memory stages. Warps 2..9 are consumers: they wait for a stage, reduce the
 // staged pieces in the plan's order (binary32, one RNE to bf16) or take the single piece
 // (copy), store the result to every destination with streaming 16-byte stores, and release
 // the stage. The ring keeps up to `stages` tiles of loads in flight per SM independently of
@@ -31,6 +31,7 @@ namespace {
 
 constexpr uint32_t kConsumerWarps = 8;
 constexpr uint32_t kProducerWarps = 2;  // warps issuing copies: tile k by warp k % 2
+static_assert(kProducerWarps == 2, "the issue loop and the abort path split tiles by parity");
 constexpr unsigned FULLW = 0xFFFFFFFFu;
 constexpr uint32_t kThreads = 32 * (kConsumerWarps + kProducerWarps);
 constexpr uint32_t kClaim = 2;   // tiles per claim of the dynamic tail (the least, if guided)
