@@ -574,7 +574,8 @@ def run_ours(args, rank, world, dist):
                 "d2h_bytes_per_step": d2h, "runs_per_step": len(chunks),
                 "overlap": "each run's outputs copied to pinned host memory on a second "
                            "stream while the next run computes",
-                "host_copy_matches_device": bool(e2e_exact)},
+                "host_copy_matches_device": bool(e2e_exact),
+                "step_stats": _stats_us(te, EPOCHS)},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 3),
