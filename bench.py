@@ -494,6 +494,10 @@ def run_ours(args, rank, world, dist):
 
     te = _time_steps(torch, e2e_step, max(3, args.steps // 2), 2, flush, stream)
     e2e_us = sum(te) / len(te) * 1000 / EPOCHS
+    # the host link's rate for these copies alone (one rank's outputs, device to pinned host)
+    copy_ms = _time_steps(torch, lambda: host_pinned_out[0].copy_(outs[0], non_blocking=True),
+                          3, 1, flush, stream)
+    d2h_gbs = outs[0].numel() * 2 / (sorted(copy_ms)[1] * 1e-3) / 1e9
     # the copies landed: check the last step's outputs on the host against the device
     torch.cuda.synchronize()
     e2e_exact = all(torch.equal(host_pinned_out[r], outs[r].cpu()) for r in range(R_DECODE))
@@ -575,7 +579,8 @@ def run_ours(args, rank, world, dist):
                 "overlap": "each run's outputs copied to pinned host memory on a second "
                            "stream while the next run computes",
                 "host_copy_matches_device": bool(e2e_exact),
-                "step_stats": _stats_us(te, EPOCHS)},
+                "step_stats": _stats_us(te, EPOCHS),
+                "d2h_copy_gbs": round(d2h_gbs, 1)},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 3),
