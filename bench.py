@@ -494,13 +494,13 @@ def run_ours(args, rank, world, dist):
 
     te = _time_steps(torch, e2e_step, max(3, args.steps // 2), 2, flush, stream)
     e2e_us = sum(te) / len(te) * 1000 / EPOCHS
+    # the copies landed: check the last step's outputs on the host against the device
+    torch.cuda.synchronize()
+    e2e_exact = all(torch.equal(host_pinned_out[r], outs[r].cpu()) for r in range(R_DECODE))
     # the host link's rate for these copies alone (one rank's outputs, device to pinned host)
     copy_ms = _time_steps(torch, lambda: host_pinned_out[0].copy_(outs[0], non_blocking=True),
                           3, 1, flush, stream)
     d2h_gbs = outs[0].numel() * 2 / (sorted(copy_ms)[1] * 1e-3) / 1e9
-    # the copies landed: check the last step's outputs on the host against the device
-    torch.cuda.synchronize()
-    e2e_exact = all(torch.equal(host_pinned_out[r], outs[r].cpu()) for r in range(R_DECODE))
 
     # the smallest configuration: all-reduce of 2 x 1024 fp32, barrier protocol, one epoch per
     # launch; median of 1000 launches, each timed with CUDA events
