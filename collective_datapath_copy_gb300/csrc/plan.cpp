@@ -260,6 +260,13 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
       T = 512;
       while (T < 32768u && T * 2 <= want) T *= 2;
     }
+    // On the ring, a plan whose jobs write each piece to eight or more destinations and that
+    // would give a CTA fewer than 16 tiles splits each such job into two, each writing to half
+    // of the destinations (the second reads the piece again, from L2). A 16 MiB broadcast
+    // (7 tiles per CTA, each writing 128 KiB) then balances its SMs better: 0.68-0.72 /
+    // 0.78 -> 0.78 / 0.85 single / back to back, measured; with 27 or more tiles per CTA
+    // the split did not pay.
+    const bool dsplit = c.bulk && T && job_bytes / T < 16u * sms;
     for (auto &nm : names) {
       const uint64_t bytes = nm.count * es;
       const uint32_t job0 = (uint32_t)c.jobs.size();
@@ -267,13 +274,18 @@ int coll_compile(int R, int op, int dtype, const coll_seg_t *in_segs, size_t n_i
       const uint32_t nsrc = sum ? (uint32_t)nm.prod.size() : 1u;
       for (uint32_t k = 0; k < nsrc; ++k) c.refs.push_back(ref_of(in_segs[nm.prod[k]]));
       if (!sum || twoshot) {
-        coll_job_t j;
-        j.src0 = src0;
-        j.nsrc = nsrc;
-        j.dst0 = (uint32_t)c.refs.size();
-        j.ndst = (uint32_t)nm.cons.size();
-        for (uint32_t q : nm.cons) c.refs.push_back(ref_of(out_segs[q]));
-        c.jobs.push_back(j);
+        const uint32_t nd = (uint32_t)nm.cons.size();
+        const uint32_t G = dsplit && nd >= 8u && nd >= 8u * nsrc ? 2u : 1u;
+        for (uint32_t g = 0; g < G; ++g) {
+          const uint32_t d0 = nd * g / G, d1 = nd * (g + 1) / G;
+          coll_job_t j;
+          j.src0 = src0;
+          j.nsrc = nsrc;
+          j.dst0 = (uint32_t)c.refs.size();
+          j.ndst = d1 - d0;
+          for (uint32_t q = d0; q < d1; ++q) c.refs.push_back(ref_of(out_segs[nm.cons[q]]));
+          c.jobs.push_back(j);
+        }
       } else {
         for (uint32_t q : nm.cons) {
           coll_job_t j;

@@ -631,9 +631,11 @@ def test_many_to_one_64mib_guided_tail_full(kind):
     plan.free()
 
 
-@pytest.mark.parametrize("kind,mib", [("broadcast", 64), ("allgather", 16)])
+@pytest.mark.parametrize("kind,mib", [("broadcast", 64), ("allgather", 16), ("broadcast", 16),
+                                      ("allgather", 4)])
 def test_multi_destination_copies_16k_tiles_full(kind, mib):
-    # jobs that write each byte to every rank run on 16 KiB tiles with up to 12 stages;
+    # jobs that write each byte to every rank run on 16 KiB tiles with up to 12 stages (the
+    # 16 MiB broadcast and the 4 MiB all-gather also split each job's destinations in two);
     # every output byte against the oracle
     R, n = 8, (mib << 20) // 2
     rng = synth.seeded_rng(3)
