@@ -603,31 +603,35 @@ def test_prefill_allreduce_64mib_oneshot_and_twoshot_full():
         plan.free()
 
 
-@pytest.mark.parametrize("kind", ["reduce_scatter", "reduce_to_root"])
-def test_many_to_one_64mib_guided_tail_full(kind):
+@pytest.mark.parametrize("kind,dtype", [("reduce_scatter", "bf16"), ("reduce_to_root", "bf16"),
+                                        ("reduce_scatter", "f32")])
+def test_many_to_one_64mib_guided_tail_full(kind, dtype):
     # 64 MiB per rank: long enough (over 64 tiles per CTA) for the ring to claim its last
     # tiles in guided sizes; every output element against the oracle, twice (the second run
     # starts from the claim counter the first run's last CTA reset)
-    R, n = 8, (64 << 20) // 2
+    R = 8
+    n = (64 << 20) // (2 if dtype == "bf16" else 4)
     rng = synth.seeded_rng(3)
-    xs = [synth.uniform_bf16(rng, n) for _ in range(R)]
+    gen_u = synth.uniform_bf16 if dtype == "bf16" else synth.uniform_f32
+    xs = [gen_u(rng, n) for _ in range(R)]
     if kind == "reduce_scatter":
-        want = collectives.reduce_scatter(xs, "bf16")
+        want = collectives.reduce_scatter(xs, dtype)
     else:
-        want = [collectives.allreduce(xs, "bf16")[0]]
-    nm = getattr(namings, kind)(R, n, "bf16")
+        want = [collectives.allreduce(xs, dtype)[0]]
+    nm = getattr(namings, kind)(R, n, dtype)
     plan = cdc.Plan(nm, zero_copy=1)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert plan.info.bulk_tile_bytes > 0 and plan.info.n_tiles >= 64 * sms
-    ins = [to_dev(x, "bf16") for x in xs]
-    outs = [torch.empty(L, dtype=torch.int16, device="cuda") for L in nm.out_len]
+    ins = [to_dev(x, dtype) for x in xs]
+    outs = [empty_dev(L, dtype) for L in nm.out_len]
     for rep in range(2):
         for o in outs:
             o.fill_(0)
         plan.run(ins, outs)
         assert plan.status()["code"] == 0
         for d, w in enumerate(want):
-            assert torch.equal(outs[d], to_dev(w, "bf16")), (kind, rep, d)
+            assert torch.equal(outs[d].view(torch.uint8), to_dev(w, dtype).view(torch.uint8)), \
+                (kind, dtype, rep, d)
     plan.free()
 
 
