@@ -347,10 +347,10 @@ cudaError_t launch_bulk(int op, int dtype, const ZcArgs &a, int ctas, cudaStream
   const uint32_t smem = bulk_smem_bytes(a.stages, a.maxsrc, a.slot_bytes);
   // Whole rounds of four fifths of the tiles are dealt round-robin and the rest claimed,
   // two at a time (dyn_tail 1) or in guided sizes (dyn_tail 2), else every tile is dealt
-  // round-robin. A guided tail pays for its claims only in long runs: with fewer than 64
-  // tiles per CTA every tile is dealt.
+  // round-robin. A guided tail pays for its claims only in long enough runs: with fewer than
+  // 16 tiles per CTA every tile is dealt.
   ZcArgs la = a;
-  const bool tail = a.dyn_tail == 1u || (a.dyn_tail == 2u && total >= 64ull * (uint64_t)grid);
+  const bool tail = a.dyn_tail == 1u || (a.dyn_tail == 2u && total >= 16ull * (uint64_t)grid);
   la.static_tiles = tail ? total * 4 / 5 / (uint64_t)grid * (uint64_t)grid : total;
   if (total - la.static_tiles >= (1ull << 31)) la.static_tiles = total;  // (claim counter)
   const void *fn;

@@ -606,7 +606,7 @@ def test_prefill_allreduce_64mib_oneshot_and_twoshot_full():
 @pytest.mark.parametrize("kind,dtype", [("reduce_scatter", "bf16"), ("reduce_to_root", "bf16"),
                                         ("reduce_scatter", "f32")])
 def test_many_to_one_64mib_guided_tail_full(kind, dtype):
-    # 64 MiB per rank: long enough (over 64 tiles per CTA) for the ring to claim its last
+    # 64 MiB per rank: long enough (over 16 tiles per CTA) for the ring to claim its last
     # tiles in guided sizes; every output element against the oracle, twice (the second run
     # starts from the claim counter the first run's last CTA reset)
     R = 8
@@ -904,7 +904,7 @@ def test_bulk_ring_epochs_over_an_input_pool():
 
 
 def test_bulk_ring_guided_tail_across_epochs():
-    # a small reduce-scatter over 80 epochs: enough tiles in all (over 64 per CTA) for the
+    # a small reduce-scatter over 80 epochs: enough tiles in all (over 16 per CTA) for the
     # ring to claim its tail in guided sizes, with claims that cross epoch boundaries
     R, n, pool, E = 8, 1 << 16, 3, 80
     rng = synth.seeded_rng(84)
