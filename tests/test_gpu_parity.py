@@ -657,6 +657,36 @@ def test_multi_destination_copies_16k_tiles_full(kind, mib):
     plan.free()
 
 
+@pytest.mark.parametrize("kind", ["reduce_scatter", "broadcast"])
+def test_bulk_ring_back_to_back_runs_each_exact(kind):
+    # 40 launches back to back (each may start while the previous one finishes), cycling two
+    # input sets into distinct outputs; every output of every launch against the oracle. The
+    # 16 MiB reduce-scatter claims its tail in guided sizes; the 16 MiB broadcast splits its
+    # destinations over two jobs. Both issue from two producer warps.
+    R, n, runs = 8, (16 << 20) // 2, 40
+    rng = synth.seeded_rng(86)
+    sets = [[synth.uniform_bf16(rng, n) for _ in range(R)] for _ in range(2)]
+    if kind == "reduce_scatter":
+        wants = [collectives.reduce_scatter(xs, "bf16") for xs in sets]
+    else:
+        wants = [collectives.broadcast(xs, 0) for xs in sets]
+    nm = getattr(namings, kind)(R, n, "bf16")
+    plan = cdc.Plan(nm, zero_copy=1)
+    assert plan.info.bulk_tile_bytes > 0
+    ins = [[to_dev(x, "bf16") for x in xs] for xs in sets]
+    want_dev = [[to_dev(w, "bf16") for w in ws] for ws in wants]
+    outs = [[torch.zeros(L, dtype=torch.int16, device="cuda") for L in nm.out_len]
+            for _ in range(runs)]
+    for i in range(runs):
+        plan.run(ins[i % 2], outs[i])
+    torch.cuda.synchronize()
+    assert plan.status()["code"] == 0
+    for i in range(runs):
+        for d in range(R):
+            assert torch.equal(outs[i][d], want_dev[i % 2][d]), (kind, i, d)
+    plan.free()
+
+
 def test_moe_dispatch_full_size():
     R, T, H, E, k = 8, 4096, 7168, 256, 8
     routing = synth.zipf_topk_routing(5, R, T, E, k, 1.1)
